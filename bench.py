@@ -1,0 +1,406 @@
+"""Benchmark: paged decode HBM GB/s (and prefill TFLOP/s) on seeded inputs.
+
+One step = the whole hot path over one batch: reshape_and_cache of the new
+K/V rows, then paged attention (decode kernel, split-KV partials folded by
+LSE).  The timed workload is the batched Llama-3-8B-shape decode: 64
+requests, query_len 1, 32/8 heads, D 128, block_size 16, lengths U[512, 4096]
+from a shuffled 20k-block pool, bf16.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line (rank 0).  ``value`` is the algorithmic bytes of a step
+(admissible KV rows, Q, O, block-table rows, seqused/cu_seqlens, and the
+new K/V rows read and written by the cache write) divided by the device time
+per step, summed over ranks.  ``--impl reference`` times the float64 CPU
+oracle on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+# the CPU oracle legs run single-threaded numpy; say so by construction
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_cache_318_gb300 import _build, api, workloads  # noqa: E402
+from paged_kv_cache_318_gb300.batch import DeviceBatch  # noqa: E402
+
+METRIC = ("paged decode HBM GB/s & prefill attn TFLOP/s "
+          "(% of GB300 roofline)")
+UNIT = "GB/s"
+SEED_DECODE = 319
+SEED_PREFILL = 320
+
+
+# --------------------------------------------------------------- accounting
+def decode_bytes(wl) -> dict:
+    """Algorithmic bytes of one decode step (what the method must move)."""
+    e = 2  # bf16
+    Hq, Hkv, D, BS = wl.num_heads, wl.num_kv_heads, wl.head_size, \
+        wl.block_size
+    L = wl.seq_lens.astype(np.int64)
+    T = wl.num_tokens
+    kv = int(L.sum()) * 2 * Hkv * D * e
+    qo = 2 * T * Hq * D * e
+    tables = int((-(-L // BS)).sum()) * 4 + wl.batch * 4 + (wl.batch + 1) * 4
+    cache_write = T * Hkv * D * e * 2 * 2 + T * 8
+    return dict(kv=kv, qo=qo, tables=tables, cache_write=cache_write,
+                attention=kv + qo + tables,
+                step=kv + qo + tables + cache_write)
+
+
+def prefill_flops(wl) -> float:
+    """QK^T + PV flops over admissible (query, key) pairs."""
+    total = 0
+    for b in range(wl.batch):
+        q, L = int(wl.q_lens[b]), int(wl.seq_lens[b])
+        c = L - q
+        total += sum(c + i + 1 for i in range(q))   # causal pairs
+    return 4.0 * wl.head_size * wl.num_heads * total
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), \
+            "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def ncu_traffic(kernel_tag):
+    """Per-launch DRAM bytes from a committed ncu summary, if it was taken on
+    the current kernel source (null otherwise)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "%s_traffic.txt" % kernel_tag)
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    for line in open(path):
+        if ":" in line:
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip()
+    src = os.path.join(ROOT, "paged_kv_cache_318_gb300", "csrc",
+                       fields.get("source", "attn_mma.cu"))
+    if not os.path.exists(src):
+        return None
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if fields.get("source_sha256_16") != h:
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch_full_workload"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.rows = []
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index),
+                 "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        self.t_marks = []
+
+    def mark(self):
+        self.t_marks.append(time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm),
+                "window": "warm-up through timed region"}
+
+
+# ---------------------------------------------------------------- GPU arm
+def time_steps(fn, steps, stream, attn_events=None):
+    """Total device ms of ``steps`` calls of fn on ``stream``."""
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(steps):
+        fn(i)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(stop)
+
+
+def gpu_arm(args, rank, world, dev):
+    hbm_peak, tf_peak, peak_src = measured_peaks()
+    wl = workloads.batched_decode(seed=SEED_DECODE, device=dev)
+    batch = DeviceBatch(wl, dev, poison=False)
+    batch.write_context()
+    stream = torch.cuda.current_stream(dev)
+    acct = decode_bytes(wl)
+
+    # per-step events around the attention call (decode + split combine)
+    n_ev = args.steps
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+    timing = {"on": False}
+
+    def step(i):
+        batch.write_new()
+        if timing["on"]:
+            ev_a[i].record(stream)
+        batch.attend(return_lse=False)
+        if timing["on"]:
+            ev_b[i].record(stream)
+
+    clocks = ClockSampler(dev.index or 0)
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    launches0 = api.launch_count()
+    timing["on"] = True
+    ms = time_steps(step, args.steps, stream)
+    timing["on"] = False
+    launches = api.launch_count() - launches0
+    if world > 1:
+        torch.distributed.barrier()
+    attn_ms = float(np.mean([a.elapsed_time(b) for a, b in zip(ev_a, ev_b)]))
+    api.check_device_errors(dev)
+
+    # e2e: same step through the public API from pinned host buffers
+    host = {k: getattr(batch, k).cpu().pin_memory() for k in
+            ("q", "k_new", "v_new", "slots_new", "block_table", "seqused_k",
+             "cu_seqlens_q")}
+    out_host = torch.empty(batch.out.shape, dtype=batch.out.dtype,
+                           pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step(i):
+        for k, t in host.items():
+            getattr(batch, k).copy_(t, non_blocking=True)
+        batch.step()
+        out_host.copy_(batch.out, non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    e2e_ms = time_steps(e2e_step, args.steps, stream)
+    clk = clocks.stop()
+
+    # secondary: varlen causal prefill with prefix cache (TFLOP/s)
+    pre = workloads.prefill_with_prefix(seed=SEED_PREFILL, device=dev)
+    pb = DeviceBatch(pre, dev, poison=False)
+    pb.write_context()
+    pb.write_new()
+    for _ in range(3):
+        pb.attend(return_lse=False)
+    pre_ms = time_steps(lambda i: pb.attend(return_lse=False), 10, stream) / 10
+    flops = prefill_flops(pre)
+    del pb
+
+    step_ms = ms / args.steps
+    stats = torch.tensor([step_ms, e2e_ms / args.steps, attn_ms, pre_ms],
+                         dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(stats, op=torch.distributed.ReduceOp.MAX)
+    step_ms, e2e_step_ms, attn_ms, pre_ms = stats.tolist()
+    value = world * acct["step"] / (step_ms * 1e-3) / 1e9
+    achieved = acct["attention"] / (attn_ms * 1e-3) / 1e9
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": "batched_paged_decode_llama3_8b",
+            "requests": wl.batch, "query_len": 1, "num_heads": 32,
+            "num_kv_heads": 8, "head_size": 128, "block_size": 16,
+            "context_lens": "U[512,4096] seed %d" % SEED_DECODE,
+            "sum_context": int(wl.seq_lens.sum()),
+            "pool_blocks": wl.num_blocks,
+            "num_splits": "auto",
+            "l2": "inputs larger than L2: %.0f MB of KV per step vs 129 MB"
+                  % (acct["kv"] / 1e6),
+            "parallelism": "replicas" if world > 1 else "single",
+        },
+        "step_bytes": acct,
+        "gpu_launches": int(launches),
+        "launches_per_step": launches / args.steps,
+        "e2e": {"value": round(world * acct["step"] /
+                               (e2e_step_ms * 1e-3) / 1e9, 1),
+                "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h),
+                "ms_per_step": round(e2e_step_ms, 5)},
+        "roofline": {
+            "kernel": "paged decode attention (decode kernel + split "
+                      "combine)",
+            "bound": "hbm", "achieved": round(achieved, 1),
+            "peak": hbm_peak, "unit": "GB/s",
+            "frac": round(achieved / hbm_peak, 4),
+            "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_src,
+            "traffic": ncu_traffic("decode_attention_batched_decode"),
+            "avg_launch_ms": round(attn_ms, 5),
+            "algorithmic_bytes_per_launch": acct["attention"],
+        },
+        "prefill": {
+            "workload": "varlen_causal_prefill_with_prefix",
+            "seqs": pre.batch, "tokens": pre.num_tokens,
+            "flops": flops, "ms": round(pre_ms, 4),
+            "tflops": round(flops / (pre_ms * 1e-3) / 1e12, 1),
+            "peak_tflops": tf_peak,
+            "frac": round(flops / (pre_ms * 1e-3) / 1e12 / tf_peak, 4),
+        },
+        "clocks": clk,
+    }
+    return res
+
+
+# -------------------------------------------------------------- CPU legs
+def oracle_sample(wl, budget_s, max_requests=None, start=0):
+    """Time the oracle on whole requests (from ``start``) until ``budget_s``
+    is spent.  Returns (bytes processed, seconds, requests)."""
+    from oracle.harness import request_reference
+    done, nbytes, t_total = 0, 0, 0.0
+    e = 2
+    per_tok = 2 * wl.num_kv_heads * wl.head_size * e
+    order = [(start + i) % wl.batch for i in range(wl.batch)]
+    for b in order:
+        t0 = time.perf_counter()
+        request_reference(wl, b)
+        t_total += time.perf_counter() - t0
+        L = int(wl.seq_lens[b])
+        nbytes += L * per_tok + 2 * wl.num_heads * wl.head_size * e
+        done += 1
+        if t_total >= budget_s or (max_requests and done >= max_requests):
+            break
+    return nbytes, t_total, done
+
+
+def cpu_baseline(budget_s=12.0):
+    wl = workloads.batched_decode(seed=SEED_DECODE, device="cpu")
+    nbytes, secs, n = oracle_sample(wl, budget_s)
+    return {"value": round(nbytes / secs / 1e9, 4), "unit": UNIT, "cores": 1,
+            "kind": "oracle",
+            "sample": "%d of %d requests of the batched decode workload "
+                      "(float64 numpy oracle, single thread, %.1f s)"
+                      % (n, wl.batch, secs)}
+
+
+def reference_arm(args):
+    wl = workloads.batched_decode(seed=SEED_DECODE, device="cpu")
+    per_step = []
+    for i in range(args.warmup + args.steps):
+        nbytes, secs, n = oracle_sample(wl, 0.0, max_requests=1,
+                                        start=i % wl.batch)
+        if i >= args.warmup:
+            per_step.append((nbytes, secs))
+    tot_b = sum(b for b, _ in per_step)
+    tot_s = sum(s for _, s in per_step)
+    value = tot_b / tot_s / 1e9
+    sample = ("one request of the batched decode workload per step "
+              "(float64 numpy oracle, single thread)")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4),
+        "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(1e3 * tot_s / len(per_step), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "batched_paged_decode_llama3_8b",
+                   "requests": wl.batch},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT,
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="native",
+                    choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(reference_arm(args)), flush=True)
+        return
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    if rank == 0 and not os.path.exists(_build.LIB_PATH):
+        _build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    api.load_library()
+    res = gpu_arm(args, rank, world, dev)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline()
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,230 @@
+/*
+ * pkv.h -- C ABI of the paged KV-cache attention library (libpkv.so).
+ *
+ * Three operations, named and shaped after the calls that the vLLM and
+ * Aphrodite attention backends make (sources cited per function, by page
+ * title and section):
+ *
+ *   pkv_reshape_and_cache        -- "reshape_and_cache_flash"
+ *   pkv_paged_attention_varlen   -- "flash_attn_varlen_func" with block_table
+ *   pkv_merge_attn_states        -- "merge_attn_states"
+ *
+ * Conventions shared by every entry point:
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller.  The
+ *     library allocates no device memory and keeps no per-call state; scratch
+ *     space is the caller's `workspace` buffer.
+ *   - All work is enqueued on the caller's stream and is ordered on it.  No
+ *     entry point synchronises the host, so calls can be issued inside CUDA
+ *     graph capture (except pkv_check_device_errors, which synchronises).
+ *   - Element strides are in ELEMENTS, not bytes.  The innermost (head_size)
+ *     dimension is always contiguous.  16-byte alignment of every row start
+ *     (pointer and strides a multiple of 8 elements for fp16/bf16) is required.
+ *   - On failure an entry point returns a non-zero pkv_status, launches
+ *     nothing, and leaves a message for pkv_last_error().  Nothing aborts the
+ *     process or traps the GPU.
+ *   - Thread safety: entry points may be called from several host threads;
+ *     the error message is per thread.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+/* Same underlying type as cudaStream_t / CUstream (NULL = legacy stream). */
+typedef struct CUstream_st* pkv_stream_t;
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1,          /* shape / pointer / value is wrong       */
+  PKV_ERR_UNSUPPORTED = 2,          /* valid but not built (dtype, D, fp8 ...) */
+  PKV_ERR_WORKSPACE_TOO_SMALL = 3,  /* workspace_bytes below the needed size  */
+  PKV_ERR_CUDA = 4,                 /* a CUDA runtime call failed              */
+  PKV_ERR_BAD_INDEX = 5,            /* a kernel met an out-of-range block id or
+                                       slot and skipped it (see
+                                       pkv_check_device_errors)               */
+  PKV_ERR_TIMEOUT = 6               /* reserved: a bounded device wait gave up */
+} pkv_status;
+
+typedef enum { PKV_F16 = 0, PKV_BF16 = 1, PKV_F32 = 2 } pkv_dtype;
+
+/*
+ * pkv_reshape_and_cache -- scatter new K/V rows into the paged cache.
+ *
+ * Source: "vllm/v1/attention/backends/flash_attn.py", FlashAttentionImpl.
+ * forward (the reshape_and_cache_flash call and its note that the op takes
+ * the token count from slot_mapping, so key/value may carry padded rows);
+ * "vllm.v1.attention.backends.flash_attn" (v0.9.0.1 docs),
+ * FlashAttentionMetadataBuilder.build (unused slots are filled with -1).
+ *
+ * For t in [0, num_tokens) with s = slot_mapping[t] >= 0:
+ *   key_cache[s / block_size, s % block_size, h, :]   = key[t, h, :]
+ *   value_cache[s / block_size, s % block_size, h, :] = value[t, h, :]
+ * for every KV head h.  Entries with s < 0 are skipped.  Rows are copied bit
+ * for bit.  Slots >= num_blocks * block_size are skipped and flagged
+ * (PKV_ERR_BAD_INDEX through pkv_check_device_errors).
+ *
+ * key, value      : [>= num_tokens, num_kv_heads, head_size] with element
+ *                   strides (k_stride_tok, k_stride_head), (v_stride_tok,
+ *                   v_stride_head).
+ * key_cache,
+ * value_cache     : 4-D views [num_blocks, block_size, num_kv_heads,
+ *                   head_size] with element strides cache_strides[0..3]
+ *                   (host array; cache_strides[3] must be 1).  The usual
+ *                   NHD cache [2, NB, BS, Hkv, D] gives strides
+ *                   (BS*Hkv*D, Hkv*D, D, 1); an HND cache [2, NB, Hkv, BS, D]
+ *                   viewed as NHD gives (Hkv*BS*D, D, BS*D, 1).
+ * slot_mapping    : int64 [num_tokens], device.
+ * block_size      : multiple of 16 (else PKV_ERR_INVALID_ARG).
+ * kv_cache_dtype  : "auto" (cache has the dtype of key/value).  "fp8",
+ *                   "fp8_e4m3" and anything else return PKV_ERR_UNSUPPORTED.
+ * k_scale, v_scale: device float scalars for an fp8 cache; ignored for "auto"
+ *                   and may be NULL.
+ * num_tokens == 0 is a no-op.
+ */
+PKV_API pkv_status pkv_reshape_and_cache(
+    const void* key, const void* value,
+    int64_t k_stride_tok, int64_t k_stride_head,
+    int64_t v_stride_tok, int64_t v_stride_head,
+    void* key_cache, void* value_cache, const int64_t cache_strides[4],
+    const int64_t* slot_mapping, int64_t num_tokens,
+    int num_kv_heads, int head_size, int block_size, int64_t num_blocks,
+    pkv_dtype dtype, const char* kv_cache_dtype,
+    const float* k_scale, const float* v_scale,
+    pkv_stream_t stream);
+
+/*
+ * pkv_paged_attention_varlen -- varlen attention over the paged cache.
+ *
+ * Source: "vllm/v1/attention/backends/flash_attn.py", FlashAttentionImpl.
+ * forward (the flash_attn_varlen_func call: cu_seqlens_q, seqused_k,
+ * block_table, window_size, softcap, alibi_slopes, num_splits, out) and
+ * _forward_with_dcp (return_softmax_lse, LSE laid out [num_heads, tokens]);
+ * FlashAttentionMetadata (seq_len = context_len + query_len, the queries are
+ * the last query_len positions); FlashAttentionImpl.__init__ (window tuple,
+ * soft-cap 0 = none, num_heads / num_kv_heads query heads per KV head).
+ *
+ * For request b with q_b = cu_seqlens_q[b+1] - cu_seqlens_q[b] queries and
+ * L_b = seqused_k[b] keys, query i (token t = cu_seqlens_q[b] + i) sits at
+ * position p = L_b - q_b + i.  Query head h reads KV head h / (Hq / Hkv).
+ * Key j (< L_b) lives at key_cache[block_table[b, j / BS], j % BS].
+ *   s_j = softmax_scale * <q[t,h], k_j>
+ *   if softcap > 0:   s_j = softcap * tanh(s_j / softcap)
+ *   if alibi_slopes:  s_j -= alibi_slopes[h] * |p - j|
+ *   admissible iff (!causal || j <= p) && (window_left < 0 || j >= p -
+ *   window_left) && (window_right < 0 || j <= p + window_right)
+ *   out[t,h]  = sum_adm softmax(s)_j * v_j      (rounded to dtype)
+ *   lse[h, t] = ln sum_adm exp(s_j)             (float)
+ * A row with no admissible key gets out = 0 and lse = -inf.
+ *
+ * q            : [T, Hq, D], strides (q_stride_tok, q_stride_head).
+ * key_cache,
+ * value_cache  : 4-D views as in pkv_reshape_and_cache.
+ * out          : [T, Hq, D], strides (o_stride_tok, o_stride_head); only
+ *                rows [0, T) are written, T = cu_seqlens_q[batch] (which must
+ *                not exceed total_q).
+ * cu_seqlens_q : int32 [batch+1] device; seqused_k: int32 [batch] device.
+ * total_q      : rows of q/out/lse the caller allocated (>= T).
+ * max_seqlen_q,
+ * max_seqlen_k : host upper bounds of q_b and L_b (they size the grid).
+ * block_table  : int32 [batch, >= ceil(L_b / BS)] device, row stride
+ *                block_table_stride elements; entries must lie in
+ *                [0, num_blocks) (out-of-range ids are not followed: the key
+ *                is read as zero and the error is flagged).
+ * num_splits   : 0 = choose; 1 = no split; N > 1 = split each request's keys
+ *                into N chunks (split-KV), combined by LSE in a second launch.
+ * softmax_lse  : float [num_heads, total_q] device, natural log, or NULL.
+ * workspace    : device scratch of workspace_bytes >= the value
+ *                pkv_paged_attention_workspace_size returns for the same
+ *                arguments (may be NULL when that value is 0).
+ * dtype        : PKV_F16 or PKV_BF16 (q, cache and out share it).
+ * head_size    : 64, 128 or 256 (others: PKV_ERR_UNSUPPORTED).
+ * Hq % Hkv != 0, block_size % 16 != 0: PKV_ERR_INVALID_ARG.
+ */
+PKV_API pkv_status pkv_paged_attention_varlen(
+    const void* q, int64_t q_stride_tok, int64_t q_stride_head,
+    const void* key_cache, const void* value_cache,
+    const int64_t cache_strides[4],
+    void* out, int64_t o_stride_tok, int64_t o_stride_head,
+    const int32_t* cu_seqlens_q, const int32_t* seqused_k, int batch,
+    int total_q, int max_seqlen_q, int max_seqlen_k,
+    const int32_t* block_table, int64_t block_table_stride,
+    int max_blocks_per_seq,
+    int num_heads, int num_kv_heads, int head_size, int block_size,
+    int64_t num_blocks,
+    float softmax_scale, int causal, int window_left, int window_right,
+    float softcap, const float* alibi_slopes,
+    int num_splits, float* softmax_lse,
+    void* workspace, size_t workspace_bytes,
+    pkv_dtype dtype, pkv_stream_t stream);
+
+/*
+ * Bytes of workspace pkv_paged_attention_varlen needs for these arguments
+ * (on the current device: the split plan depends on its SM count).  Returns
+ * 0 when no scratch is needed, and (size_t)-1 for invalid arguments.
+ */
+PKV_API size_t pkv_paged_attention_workspace_size(
+    int batch, int total_q, int max_seqlen_q, int max_seqlen_k,
+    int num_heads, int num_kv_heads, int head_size, int block_size,
+    int causal, int window_left, int window_right, int num_splits);
+
+/*
+ * pkv_merge_attn_states -- combine two partial attentions by their LSEs.
+ *
+ * Source: "vllm/v1/attention/backends/flash_attn.py", cascade_attention (the
+ * merge of the shared-prefix and suffix results) and _forward_with_dcp (the
+ * merge of context and new-token results); the FlashInfer backend page
+ * converts base-2 LSEs to natural log before the same merge, so LSEs here
+ * are natural-log.
+ *
+ * With M = max(l1, l2), w_i = exp(l_i - M):
+ *   output = (w1 * prefix_output + w2 * suffix_output) / (w1 + w2)
+ *   output_lse = M + ln(w1 + w2)
+ * A side with lse = -inf holds no keys and is ignored; if both are -inf the
+ * row is 0 with lse -inf.
+ *
+ * output, prefix_output, suffix_output: contiguous [num_tokens, num_heads,
+ *   head_size]; output has out_dtype (PKV_F16/PKV_BF16/PKV_F32), the two
+ *   inputs have in_dtype.
+ * prefix_lse, suffix_lse: contiguous float [num_heads, num_tokens].
+ * output_lse: float [num_heads, num_tokens] or NULL.
+ * head_size: multiple of 8, at most 512.
+ */
+PKV_API pkv_status pkv_merge_attn_states(
+    void* output, const void* prefix_output, const float* prefix_lse,
+    const void* suffix_output, const float* suffix_lse, float* output_lse,
+    int num_tokens, int num_heads, int head_size,
+    pkv_dtype out_dtype, pkv_dtype in_dtype, pkv_stream_t stream);
+
+/*
+ * pkv_check_device_errors -- synchronise `stream`, then read and clear the
+ * library's device error word.  Returns PKV_OK, or PKV_ERR_BAD_INDEX when a
+ * kernel since the last check met an out-of-range block id or slot (the
+ * access was skipped, never performed).  Not for use inside graph capture.
+ */
+PKV_API pkv_status pkv_check_device_errors(pkv_stream_t stream);
+
+/*
+ * Number of kernels this library has launched in this process (all devices,
+ * all threads), for accounting of launches per step.
+ */
+PKV_API uint64_t pkv_launch_count(void);
+
+/* Message for the last non-OK status returned on this host thread. */
+PKV_API const char* pkv_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

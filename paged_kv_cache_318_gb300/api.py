@@ -1,0 +1,309 @@
+"""Python binding of libpkv (ctypes): argument marshalling only.
+
+Every function takes torch tensors that already live on the GPU, reads their
+pointers, strides and the current CUDA stream, and calls the C ABI declared in
+``include/pkv.h``.  All computation happens in the library's kernels.  A
+missing library raises ``RuntimeError``; a non-OK status raises
+``ValueError`` (invalid argument), ``NotImplementedError`` (unsupported
+configuration) or ``RuntimeError`` (anything else), as the attention backends
+on the vLLM pages do.
+
+Names and argument orders follow those pages: ``reshape_and_cache_flash``,
+``flash_attn_varlen_func``, ``merge_attn_states`` and ``cascade_attention``
+("vllm/v1/attention/backends/flash_attn.py").
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+from . import _build
+
+_lib = None
+_lib_lock = threading.Lock()
+
+PKV_OK = 0
+PKV_ERR_INVALID_ARG = 1
+PKV_ERR_UNSUPPORTED = 2
+PKV_ERR_WORKSPACE_TOO_SMALL = 3
+PKV_ERR_CUDA = 4
+PKV_ERR_BAD_INDEX = 5
+
+_DT = {torch.float16: 0, torch.bfloat16: 1, torch.float32: 2}
+
+c_i64p = ctypes.POINTER(ctypes.c_int64)
+vp = ctypes.c_void_p
+i32, i64, f32, sz = ctypes.c_int, ctypes.c_int64, ctypes.c_float, \
+    ctypes.c_size_t
+
+
+class PkvError(RuntimeError):
+    """A libpkv call returned a CUDA or device-index error."""
+
+    def __init__(self, status, message):
+        super().__init__("pkv status %d: %s" % (status, message))
+        self.status = status
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library():
+    """Load libpkv.so (built by ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lib_lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(
+                "libpkv.so is not built (%s); run "
+                "`python -c 'import __graft_entry__ as g; g.build()'`" % path)
+        lib = ctypes.CDLL(path)
+        lib.pkv_last_error.restype = ctypes.c_char_p
+        lib.pkv_last_error.argtypes = []
+        lib.pkv_reshape_and_cache.restype = i32
+        lib.pkv_reshape_and_cache.argtypes = [
+            vp, vp, i64, i64, i64, i64, vp, vp, c_i64p, vp, i64, i32, i32,
+            i32, i64, i32, ctypes.c_char_p, vp, vp, vp]
+        lib.pkv_paged_attention_varlen.restype = i32
+        lib.pkv_paged_attention_varlen.argtypes = [
+            vp, i64, i64, vp, vp, c_i64p, vp, i64, i64, vp, vp, i32, i32,
+            i32, i32, vp, i64, i32, i32, i32, i32, i32, i64, f32, i32, i32,
+            i32, f32, vp, i32, vp, vp, sz, i32, vp]
+        lib.pkv_paged_attention_workspace_size.restype = sz
+        lib.pkv_paged_attention_workspace_size.argtypes = [i32] * 12
+        lib.pkv_merge_attn_states.restype = i32
+        lib.pkv_merge_attn_states.argtypes = [
+            vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]
+        lib.pkv_launch_count.restype = ctypes.c_uint64
+        lib.pkv_launch_count.argtypes = []
+        lib.pkv_check_device_errors.restype = i32
+        lib.pkv_check_device_errors.argtypes = [vp]
+        _lib = lib
+    return _lib
+
+
+def _check(status):
+    if status == PKV_OK:
+        return
+    msg = load_library().pkv_last_error().decode(errors="replace")
+    if status == PKV_ERR_INVALID_ARG:
+        raise ValueError(msg)
+    if status == PKV_ERR_UNSUPPORTED:
+        raise NotImplementedError(msg)
+    raise PkvError(status, msg)
+
+
+def _stream(t: torch.Tensor):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _dtype(t: torch.Tensor) -> int:
+    try:
+        return _DT[t.dtype]
+    except KeyError:
+        raise NotImplementedError("dtype %s is not supported" % t.dtype)
+
+
+def _cache_strides(key_cache, value_cache):
+    if key_cache.dim() != 4:
+        raise ValueError("cache views must be 4-D [num_blocks, block_size, "
+                         "num_kv_heads, head_size]")
+    if tuple(key_cache.stride()) != tuple(value_cache.stride()) or \
+            key_cache.shape != value_cache.shape:
+        raise ValueError("key_cache and value_cache must share shape and "
+                         "strides")
+    return (ctypes.c_int64 * 4)(*key_cache.stride())
+
+
+def launch_count() -> int:
+    """Kernels libpkv has launched in this process so far."""
+    return int(load_library().pkv_launch_count())
+
+
+def check_device_errors(device=None):
+    """Synchronise the current stream and raise if a kernel skipped an
+    out-of-range block id or slot since the last check."""
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    s = torch.cuda.current_stream(dev).cuda_stream
+    _check(load_library().pkv_check_device_errors(ctypes.c_void_p(s)))
+
+
+# ------------------------------------------------------------------ cache write
+
+def reshape_and_cache_flash(key, value, key_cache, value_cache, slot_mapping,
+                            kv_cache_dtype: str = "auto", k_scale=None,
+                            v_scale=None):
+    """Scatter key/value [>= T, Hkv, D] into the paged cache at slot_mapping.
+
+    T = len(slot_mapping); padded rows of key/value are ignored and slots < 0
+    are skipped.  key_cache/value_cache are [num_blocks, block_size, Hkv, D]
+    views (e.g. ``kv_cache.unbind(0)``), any strides with D contiguous.
+    """
+    lib = load_library()
+    if slot_mapping.dtype != torch.int64:
+        raise ValueError("slot_mapping must be int64")
+    if key.stride(-1) != 1 or value.stride(-1) != 1:
+        raise ValueError("key/value head_size dim must be contiguous")
+    if key.dtype != key_cache.dtype and kv_cache_dtype == "auto":
+        raise ValueError("cache dtype must match key dtype for 'auto'")
+    NB, BS, H, D = key_cache.shape
+    cs = _cache_strides(key_cache, value_cache)
+    _check(lib.pkv_reshape_and_cache(
+        _ptr(key), _ptr(value), key.stride(0), key.stride(1), value.stride(0),
+        value.stride(1), _ptr(key_cache), _ptr(value_cache), cs,
+        _ptr(slot_mapping), slot_mapping.shape[0], H, D, BS, NB,
+        _dtype(key), kv_cache_dtype.encode(), _ptr(k_scale), _ptr(v_scale),
+        _stream(key)))
+
+
+# --------------------------------------------------------------- attention
+
+def paged_attention_workspace_size(batch, total_q, max_seqlen_q, max_seqlen_k,
+                                   num_heads, num_kv_heads, head_size,
+                                   block_size, causal=True,
+                                   window_size=(-1, -1), num_splits=0) -> int:
+    n = load_library().pkv_paged_attention_workspace_size(
+        batch, total_q, max_seqlen_q, max_seqlen_k, num_heads, num_kv_heads,
+        head_size, block_size, int(bool(causal)), int(window_size[0]),
+        int(window_size[1]), num_splits)
+    if n == ctypes.c_size_t(-1).value:
+        raise ValueError(load_library().pkv_last_error().decode())
+    return n
+
+
+def flash_attn_varlen_func(q, k, v, max_seqlen_q, cu_seqlens_q, max_seqlen_k,
+                           seqused_k=None, softmax_scale=None, causal=False,
+                           window_size=(-1, -1), softcap=0.0,
+                           alibi_slopes=None, block_table=None,
+                           return_softmax_lse=False, out=None, num_splits=0,
+                           cu_seqlens_k=None, workspace=None):
+    """Varlen attention over a paged KV cache.
+
+    q [T, Hq, D]; k, v: cache views [num_blocks, block_size, Hkv, D];
+    cu_seqlens_q int32 [B+1]; seqused_k int32 [B]; block_table int32
+    [B, max_blocks].  Returns out (and lse [Hq, T] float32 when
+    return_softmax_lse).
+    """
+    lib = load_library()
+    if cu_seqlens_k is not None:
+        raise NotImplementedError("non-paged varlen K/V (cu_seqlens_k) is not "
+                                  "supported; pass seqused_k + block_table")
+    if block_table is None or seqused_k is None:
+        raise ValueError("block_table and seqused_k are required")
+    if q.stride(-1) != 1:
+        raise ValueError("q head_size dim must be contiguous")
+    T, Hq, D = q.shape
+    NB, BS, Hkv, Dk = k.shape
+    if Dk != D:
+        raise ValueError("q and cache head_size differ")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise NotImplementedError("q and cache dtypes must match")
+    if cu_seqlens_q.dtype != torch.int32 or seqused_k.dtype != torch.int32 \
+            or block_table.dtype != torch.int32:
+        raise ValueError("cu_seqlens_q, seqused_k and block_table must be "
+                         "int32")
+    if block_table.stride(-1) != 1:
+        raise ValueError("block_table rows must be contiguous")
+    if softmax_scale is None:
+        softmax_scale = D ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    batch = seqused_k.shape[0]
+    lse = None
+    if return_softmax_lse:
+        lse = torch.empty((Hq, T), dtype=torch.float32, device=q.device)
+    ws_need = paged_attention_workspace_size(
+        batch, T, max_seqlen_q, max_seqlen_k, Hq, Hkv, D, BS, causal,
+        window_size, num_splits)
+    if workspace is None and ws_need > 0:
+        workspace = torch.empty(ws_need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * \
+        workspace.element_size()
+    cs = _cache_strides(k, v)
+    if alibi_slopes is not None and alibi_slopes.dtype != torch.float32:
+        raise ValueError("alibi_slopes must be float32")
+    _check(lib.pkv_paged_attention_varlen(
+        _ptr(q), q.stride(0), q.stride(1), _ptr(k), _ptr(v), cs, _ptr(out),
+        out.stride(0), out.stride(1), _ptr(cu_seqlens_q), _ptr(seqused_k),
+        batch, T, int(max_seqlen_q), int(max_seqlen_k), _ptr(block_table),
+        block_table.stride(0), block_table.shape[1], Hq, Hkv, D, BS, NB,
+        float(softmax_scale), int(bool(causal)), int(window_size[0]),
+        int(window_size[1]), float(softcap or 0.0), _ptr(alibi_slopes),
+        int(num_splits), _ptr(lse), _ptr(workspace), ws_bytes, _dtype(q),
+        _stream(q)))
+    if return_softmax_lse:
+        return out, lse
+    return out
+
+
+def merge_attn_states(output, prefix_output, prefix_lse, suffix_output,
+                      suffix_lse, output_lse=None):
+    """output = LSE-weighted combination of two partial attentions.
+
+    outputs [T, H, D] contiguous; LSEs float32 [H, T] contiguous.
+    """
+    lib = load_library()
+    for t in (output, prefix_output, suffix_output, prefix_lse, suffix_lse):
+        if not t.is_contiguous():
+            raise ValueError("merge_attn_states needs contiguous tensors")
+    if prefix_output.dtype != suffix_output.dtype:
+        raise ValueError("prefix and suffix outputs must share a dtype")
+    T, H, D = output.shape
+    if prefix_lse.shape != (H, T) or suffix_lse.shape != (H, T):
+        raise ValueError("LSE shape must be [num_heads, num_tokens]")
+    _check(lib.pkv_merge_attn_states(
+        _ptr(output), _ptr(prefix_output), _ptr(prefix_lse),
+        _ptr(suffix_output), _ptr(suffix_lse), _ptr(output_lse), T, H, D,
+        _dtype(output), _dtype(prefix_output), _stream(output)))
+    return output
+
+
+def cascade_attention(output, query, key_cache, value_cache, cu_query_lens,
+                      max_query_len, cu_prefix_query_lens, prefix_kv_lens,
+                      suffix_kv_lens, max_kv_len, softmax_scale,
+                      alibi_slopes, sliding_window, logits_soft_cap,
+                      block_table, common_prefix_len, max_num_splits=0,
+                      workspace=None):
+    """Shared-prefix attention: prefix (non-causal, block_table[:1]) +
+    suffix (causal, block_table[:, P/BS:]) merged by LSE, as in vLLM v1's
+    ``cascade_attention``."""
+    if alibi_slopes is not None:
+        raise ValueError("Cascade attention does not support ALiBi.")
+    if tuple(sliding_window) != (-1, -1):
+        raise ValueError("Cascade attention does not support sliding window.")
+    num_tokens = query.shape[0]
+    block_size = key_cache.shape[-3]
+    if common_prefix_len % block_size != 0:
+        raise ValueError("common_prefix_len must be a multiple of block_size")
+    n_common = common_prefix_len // block_size
+    if n_common <= 0:
+        raise ValueError("common_prefix_len must be > 0")
+    prefix_out, prefix_lse = flash_attn_varlen_func(
+        query, key_cache, value_cache, num_tokens, cu_prefix_query_lens,
+        common_prefix_len, seqused_k=prefix_kv_lens,
+        softmax_scale=softmax_scale, causal=False,
+        window_size=sliding_window, softcap=logits_soft_cap,
+        block_table=block_table[:1], return_softmax_lse=True,
+        num_splits=max_num_splits)
+    suffix_out, suffix_lse = flash_attn_varlen_func(
+        query, key_cache, value_cache, max_query_len, cu_query_lens,
+        max_kv_len - common_prefix_len, seqused_k=suffix_kv_lens,
+        softmax_scale=softmax_scale, causal=True, window_size=sliding_window,
+        softcap=logits_soft_cap, block_table=block_table[:, n_common:],
+        return_softmax_lse=True, num_splits=max_num_splits,
+        workspace=workspace)
+    merge_attn_states(output, prefix_out, prefix_lse, suffix_out, suffix_lse)
+    return output

@@ -1,0 +1,441 @@
+// C ABI of libpkv: argument validation, the split plan, and kernel launches.
+//
+// Every entry point validates its arguments on the host before it enqueues
+// anything; invalid calls return a pkv_status and a per-thread message and
+// launch nothing.  Kernels never trap: out-of-range indices are skipped and
+// recorded in a device error word (pkv_check_device_errors reads it).
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+#include <string>
+
+#include "pkv_common.cuh"
+
+namespace pkv {
+
+__device__ unsigned g_device_error = 0;
+
+static std::atomic<uint64_t> g_launches{0};
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+namespace {
+
+thread_local std::string g_last_error;
+
+pkv_status fail(pkv_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+pkv_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(PKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mu;
+unsigned* g_err_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+
+// Per-device facts, looked up once with that device current.
+pkv_status device_info(unsigned** err, int* sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices)
+    return fail(PKV_ERR_UNSUPPORTED, "device ordinal %d too large", dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (!g_err_ptr[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_device_error);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    g_err_ptr[dev] = static_cast<unsigned*>(ptr);
+    g_sm_count[dev] = n;
+  }
+  if (err) *err = g_err_ptr[dev];
+  if (sms) *sms = g_sm_count[dev];
+  return PKV_OK;
+}
+
+bool aligned16(const void* p) {
+  return reinterpret_cast<uintptr_t>(p) % 16 == 0;
+}
+bool stride16(int64_t s, int elem) { return (s * elem) % 16 == 0; }
+
+// ----------------------------------------------------------- split plan
+
+struct Plan {
+  bool decode = false;    // launch the decode (<= 16 packed rows) kernel
+  bool prefill = false;   // launch the prefill kernel
+  int splits = 1;         // decode grid.x
+  int chunk = 0;          // keys per split; 0 = write outputs directly
+  int prefill_tiles = 0;  // prefill grid.y
+  size_t part_o_bytes = 0, part_lse_bytes = 0;
+  size_t workspace = 0;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+Plan make_plan(int batch, int total_q, int max_q, int max_k, int Hq, int Hkv,
+               int D, int causal, int wl, int wr, int num_splits, int sms) {
+  Plan pl;
+  const int G = Hq / Hkv;
+  if (batch == 0 || max_q == 0) return pl;
+  pl.decode = true;
+  pl.prefill = static_cast<int64_t>(max_q) * G > kDecodeRows;
+  if (pl.prefill)
+    pl.prefill_tiles = static_cast<int>(
+        (static_cast<int64_t>(max_q) * G + 63) / 64);
+  // Widest key range a decode-class CTA can see.
+  int64_t range = max_k;
+  const int q_dec = kDecodeRows / G > 0 ? kDecodeRows / G : 1;
+  if (wl >= 0) {
+    const int64_t span = static_cast<int64_t>(wl) + q_dec +
+                         (wr >= 0 ? wr : (causal ? 0 : max_k));
+    if (span < range) range = span;
+  }
+  int splits = 1;
+  if (num_splits > 1) {
+    splits = num_splits;
+  } else if (num_splits == 0 && range > 0) {
+    // Aim for ~8 waves of 2 resident CTAs per SM; keep >= 256 keys per split.
+    const int64_t units = static_cast<int64_t>(batch) * Hkv;
+    const int64_t target = static_cast<int64_t>(sms) * 2 * 8;
+    int64_t s = (target + units - 1) / units;
+    const int64_t cap = (range + 255) / 256;
+    if (s > cap) s = cap;
+    if (s > 64) s = 64;
+    if (s < 1) s = 1;
+    splits = static_cast<int>(s);
+  }
+  if (splits > 1 && range > 0) {
+    int64_t chunk = (range + splits - 1) / splits;
+    chunk = (chunk + kDecodeKT - 1) / kDecodeKT * kDecodeKT;
+    pl.chunk = static_cast<int>(chunk);
+    pl.splits = static_cast<int>((range + chunk - 1) / chunk);
+    if (pl.splits <= 1) {
+      pl.splits = 1;
+      pl.chunk = 0;
+    }
+  }
+  if (pl.chunk > 0) {
+    pl.part_o_bytes = align256(static_cast<size_t>(pl.splits) * total_q * Hq *
+                               D * sizeof(float));
+    pl.part_lse_bytes = align256(static_cast<size_t>(pl.splits) * Hq *
+                                 total_q * sizeof(float));
+    pl.workspace = pl.part_o_bytes + pl.part_lse_bytes;
+  }
+  return pl;
+}
+
+pkv_status check_attn_shape(int batch, int total_q, int max_q, int max_k,
+                            int Hq, int Hkv, int D, int BS, int num_splits) {
+  if (batch < 0 || total_q < 0 || max_q < 0 || max_k < 0)
+    return fail(PKV_ERR_INVALID_ARG, "negative size argument");
+  if (Hq <= 0 || Hkv <= 0)
+    return fail(PKV_ERR_INVALID_ARG, "num_heads and num_kv_heads must be > 0");
+  if (Hq % Hkv != 0)
+    return fail(PKV_ERR_INVALID_ARG,
+                "num_heads (%d) must be a multiple of num_kv_heads (%d)", Hq,
+                Hkv);
+  if (BS <= 0 || BS % 16 != 0)
+    return fail(PKV_ERR_INVALID_ARG, "block_size must be a multiple of 16");
+  if (D % 8 != 0 || D <= 0 || D > 256)
+    return fail(PKV_ERR_UNSUPPORTED,
+                "head_size %d: must be a multiple of 8 and at most 256", D);
+  if (D != 64 && D != 128 && D != 256)
+    return fail(PKV_ERR_UNSUPPORTED, "head_size %d not built (64, 128, 256)",
+                D);
+  if (num_splits < 0)
+    return fail(PKV_ERR_INVALID_ARG, "num_splits must be >= 0");
+  return PKV_OK;
+}
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+const char* pkv_last_error(void) { return g_last_error.c_str(); }
+
+uint64_t pkv_launch_count(void) {
+  return g_launches.load(std::memory_order_relaxed);
+}
+
+pkv_status pkv_check_device_errors(pkv_stream_t stream) {
+  unsigned* err = nullptr;
+  pkv_status st = device_info(&err, nullptr);
+  if (st != PKV_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned host = 0;
+  e = cudaMemcpy(&host, err, sizeof(unsigned), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+  const unsigned zero = 0;
+  e = cudaMemcpy(err, &zero, sizeof(unsigned), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
+  if (host) {
+    return fail(PKV_ERR_BAD_INDEX,
+                "kernels skipped out-of-range accesses:%s%s%s",
+                (host & kErrBadBlock) ? " block id outside the cache;" : "",
+                (host & kErrBadSlot) ? " slot outside the cache;" : "",
+                (host & kErrBadTable) ? " seqused_k beyond the table row;"
+                                      : "");
+  }
+  return PKV_OK;
+}
+
+pkv_status pkv_reshape_and_cache(
+    const void* key, const void* value, int64_t k_stride_tok,
+    int64_t k_stride_head, int64_t v_stride_tok, int64_t v_stride_head,
+    void* key_cache, void* value_cache, const int64_t cache_strides[4],
+    const int64_t* slot_mapping, int64_t num_tokens, int num_kv_heads,
+    int head_size, int block_size, int64_t num_blocks, pkv_dtype dtype,
+    const char* kv_cache_dtype, const float* k_scale, const float* v_scale,
+    pkv_stream_t stream) {
+  (void)k_scale;
+  (void)v_scale;
+  if (kv_cache_dtype && strcmp(kv_cache_dtype, "auto") != 0)
+    return fail(PKV_ERR_UNSUPPORTED, "kv_cache_dtype '%s' is not supported",
+                kv_cache_dtype);
+  if (dtype != PKV_F16 && dtype != PKV_BF16)
+    return fail(PKV_ERR_UNSUPPORTED, "dtype must be fp16 or bf16");
+  if (num_tokens < 0 || num_blocks < 0)
+    return fail(PKV_ERR_INVALID_ARG, "negative size argument");
+  if (num_kv_heads <= 0 || head_size <= 0)
+    return fail(PKV_ERR_INVALID_ARG, "num_kv_heads / head_size must be > 0");
+  if (block_size <= 0 || block_size % 16 != 0)
+    return fail(PKV_ERR_INVALID_ARG, "block_size must be a multiple of 16");
+  if (head_size % 8 != 0)
+    return fail(PKV_ERR_UNSUPPORTED, "head_size must be a multiple of 8");
+  if (!cache_strides)
+    return fail(PKV_ERR_INVALID_ARG, "cache_strides is NULL");
+  if (cache_strides[3] != 1)
+    return fail(PKV_ERR_INVALID_ARG, "the head_size dim must be contiguous");
+  if (num_tokens == 0) return PKV_OK;
+  if (!key || !value || !key_cache || !value_cache || !slot_mapping)
+    return fail(PKV_ERR_INVALID_ARG, "NULL tensor pointer");
+  unsigned* err = nullptr;
+  pkv_status st = device_info(&err, nullptr);
+  if (st != PKV_OK) return st;
+  cudaError_t e = launch_cache_write(
+      key, value, k_stride_tok, k_stride_head, v_stride_tok, v_stride_head,
+      key_cache, value_cache, cache_strides, slot_mapping, num_tokens,
+      num_kv_heads, head_size, block_size, num_blocks, 2, err,
+      reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "reshape_and_cache launch");
+  return PKV_OK;
+}
+
+size_t pkv_paged_attention_workspace_size(int batch, int total_q,
+                                          int max_seqlen_q, int max_seqlen_k,
+                                          int num_heads, int num_kv_heads,
+                                          int head_size, int block_size,
+                                          int causal, int window_left,
+                                          int window_right, int num_splits) {
+  if (check_attn_shape(batch, total_q, max_seqlen_q, max_seqlen_k, num_heads,
+                       num_kv_heads, head_size, block_size,
+                       num_splits) != PKV_OK)
+    return static_cast<size_t>(-1);
+  int sms = 0;
+  if (device_info(nullptr, &sms) != PKV_OK) return static_cast<size_t>(-1);
+  return make_plan(batch, total_q, max_seqlen_q, max_seqlen_k, num_heads,
+                   num_kv_heads, head_size, causal, window_left, window_right,
+                   num_splits, sms)
+      .workspace;
+}
+
+pkv_status pkv_paged_attention_varlen(
+    const void* q, int64_t q_stride_tok, int64_t q_stride_head,
+    const void* key_cache, const void* value_cache,
+    const int64_t cache_strides[4], void* out, int64_t o_stride_tok,
+    int64_t o_stride_head, const int32_t* cu_seqlens_q,
+    const int32_t* seqused_k, int batch, int total_q, int max_seqlen_q,
+    int max_seqlen_k, const int32_t* block_table, int64_t block_table_stride,
+    int max_blocks_per_seq, int num_heads, int num_kv_heads, int head_size,
+    int block_size, int64_t num_blocks, float softmax_scale, int causal,
+    int window_left, int window_right, float softcap,
+    const float* alibi_slopes, int num_splits, float* softmax_lse,
+    void* workspace, size_t workspace_bytes, pkv_dtype dtype,
+    pkv_stream_t stream) {
+  pkv_status st =
+      check_attn_shape(batch, total_q, max_seqlen_q, max_seqlen_k, num_heads,
+                       num_kv_heads, head_size, block_size, num_splits);
+  if (st != PKV_OK) return st;
+  if (dtype != PKV_F16 && dtype != PKV_BF16)
+    return fail(PKV_ERR_UNSUPPORTED, "dtype must be fp16 or bf16");
+  if (!(softmax_scale == softmax_scale) || isinf(softmax_scale))
+    return fail(PKV_ERR_INVALID_ARG, "softmax_scale must be finite");
+  if (softcap < 0.f || !(softcap == softcap))
+    return fail(PKV_ERR_INVALID_ARG, "softcap must be >= 0 (0 = none)");
+  if (batch == 0 || total_q == 0 || max_seqlen_q == 0) return PKV_OK;
+  if (!q || !key_cache || !value_cache || !out || !cu_seqlens_q ||
+      !seqused_k || !block_table || !cache_strides)
+    return fail(PKV_ERR_INVALID_ARG, "NULL tensor pointer");
+  if (max_blocks_per_seq <= 0 || block_table_stride < max_blocks_per_seq)
+    return fail(PKV_ERR_INVALID_ARG,
+                "block_table: need max_blocks_per_seq >= 1 and stride >= it");
+  if (cache_strides[3] != 1)
+    return fail(PKV_ERR_INVALID_ARG, "the head_size dim must be contiguous");
+  const int eb = 2;
+  if (!aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache) ||
+      !aligned16(out) || !stride16(q_stride_tok, eb) ||
+      !stride16(q_stride_head, eb) || !stride16(o_stride_tok, eb) ||
+      !stride16(o_stride_head, eb) || !stride16(cache_strides[0], eb) ||
+      !stride16(cache_strides[1], eb) || !stride16(cache_strides[2], eb))
+    return fail(PKV_ERR_UNSUPPORTED,
+                "q/out/cache rows must start on 16-byte boundaries");
+  const int wl = window_left < 0 ? -1 : window_left;
+  const int wr = window_right < 0 ? -1 : window_right;
+
+  unsigned* err = nullptr;
+  int sms = 0;
+  st = device_info(&err, &sms);
+  if (st != PKV_OK) return st;
+  const Plan pl = make_plan(batch, total_q, max_seqlen_q, max_seqlen_k,
+                            num_heads, num_kv_heads, head_size, causal, wl, wr,
+                            num_splits, sms);
+  if (pl.workspace > 0) {
+    if (workspace_bytes < pl.workspace || !workspace)
+      return fail(PKV_ERR_WORKSPACE_TOO_SMALL,
+                  "workspace of %zu bytes needed, %zu given", pl.workspace,
+                  workspace_bytes);
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+      return fail(PKV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  }
+
+  AttnParams p{};
+  p.q = q;
+  p.q_st = q_stride_tok;
+  p.q_sh = q_stride_head;
+  p.kc = key_cache;
+  p.vc = value_cache;
+  p.c_sb = cache_strides[0];
+  p.c_sr = cache_strides[1];
+  p.c_sh = cache_strides[2];
+  p.out = out;
+  p.o_st = o_stride_tok;
+  p.o_sh = o_stride_head;
+  p.lse = softmax_lse;
+  p.total_q = total_q;
+  p.cu_q = cu_seqlens_q;
+  p.seqused_k = seqused_k;
+  p.batch = batch;
+  p.block_table = block_table;
+  p.bt_stride = block_table_stride;
+  p.max_blocks = max_blocks_per_seq;
+  p.num_blocks = num_blocks;
+  p.Hq = num_heads;
+  p.Hkv = num_kv_heads;
+  p.G = num_heads / num_kv_heads;
+  p.BS = block_size;
+  p.scale = softmax_scale;
+  p.softcap = softcap;
+  p.alibi = alibi_slopes;
+  p.causal = causal ? 1 : 0;
+  p.wl = wl;
+  p.wr = wr;
+  p.err = err;
+  const bool bf16 = dtype == PKV_BF16;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  if (pl.decode) {
+    AttnParams d = p;
+    d.min_rows = 1;
+    d.max_rows = kDecodeRows;
+    d.chunk = pl.chunk;
+    if (pl.chunk > 0) {
+      d.part_o = static_cast<float*>(workspace);
+      d.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                            pl.part_o_bytes);
+    }
+    cudaError_t e = launch_decode_attn(d, head_size, bf16, pl.splits, 1, s);
+    if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
+    if (pl.chunk > 0) {
+      CombineParams c{};
+      c.part_o = d.part_o;
+      c.part_lse = d.part_lse;
+      c.out = out;
+      c.o_st = o_stride_tok;
+      c.o_sh = o_stride_head;
+      c.lse = softmax_lse;
+      c.total_q = total_q;
+      c.cu_q = cu_seqlens_q;
+      c.seqused_k = seqused_k;
+      c.batch = batch;
+      c.Hq = num_heads;
+      c.G = p.G;
+      c.D = head_size;
+      c.causal = p.causal;
+      c.wl = wl;
+      c.wr = wr;
+      c.chunk = pl.chunk;
+      c.splits = pl.splits;
+      c.min_rows = 1;
+      c.max_rows = kDecodeRows;
+      e = launch_split_combine(c, bf16, s);
+      if (e != cudaSuccess) return cuda_fail(e, "split combine launch");
+    }
+  }
+  if (pl.prefill) {
+    AttnParams f = p;
+    f.min_rows = kDecodeRows + 1;
+    f.max_rows = 0x7fffffff;
+    f.chunk = 0;
+    cudaError_t e =
+        launch_prefill_attn_mma(f, head_size, bf16, pl.prefill_tiles, s);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill attention launch");
+  }
+  return PKV_OK;
+}
+
+pkv_status pkv_merge_attn_states(void* output, const void* prefix_output,
+                                 const float* prefix_lse,
+                                 const void* suffix_output,
+                                 const float* suffix_lse, float* output_lse,
+                                 int num_tokens, int num_heads, int head_size,
+                                 pkv_dtype out_dtype, pkv_dtype in_dtype,
+                                 pkv_stream_t stream) {
+  if (num_tokens < 0 || num_heads <= 0 || head_size <= 0)
+    return fail(PKV_ERR_INVALID_ARG, "bad sizes");
+  if (head_size % 8 != 0 || head_size > 512)
+    return fail(PKV_ERR_UNSUPPORTED,
+                "head_size must be a multiple of 8 and at most 512");
+  auto ok_dt = [](pkv_dtype d) {
+    return d == PKV_F16 || d == PKV_BF16 || d == PKV_F32;
+  };
+  if (!ok_dt(out_dtype) || !ok_dt(in_dtype))
+    return fail(PKV_ERR_UNSUPPORTED, "dtype must be fp16, bf16 or fp32");
+  if ((out_dtype == PKV_F16 && in_dtype == PKV_BF16) ||
+      (out_dtype == PKV_BF16 && in_dtype == PKV_F16))
+    return fail(PKV_ERR_UNSUPPORTED, "fp16 and bf16 cannot be mixed");
+  if (num_tokens == 0) return PKV_OK;
+  if (!output || !prefix_output || !prefix_lse || !suffix_output ||
+      !suffix_lse)
+    return fail(PKV_ERR_INVALID_ARG, "NULL tensor pointer");
+  if (!aligned16(output) || !aligned16(prefix_output) ||
+      !aligned16(suffix_output))
+    return fail(PKV_ERR_UNSUPPORTED, "outputs must be 16-byte aligned");
+  cudaError_t e = launch_merge(output, prefix_output, prefix_lse,
+                               suffix_output, suffix_lse, output_lse,
+                               num_tokens, num_heads, head_size, out_dtype,
+                               in_dtype, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  return PKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,228 @@
+// Shared device helpers and the internal launch interface of libpkv.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pkv.h"
+
+namespace pkv {
+
+// Error bits OR-ed into the device error word by kernels that skip an access.
+constexpr unsigned kErrBadBlock = 1u;   // block id outside [0, num_blocks)
+constexpr unsigned kErrBadSlot = 2u;    // slot outside the cache
+constexpr unsigned kErrBadTable = 4u;   // key beyond the block-table row
+
+// ---------------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// 16-byte global->shared async copy; src_bytes == 0 writes zeros.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src,
+                                            int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst),
+               "l"(src), "r"(src_bytes));
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;\n" ::);
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0,
+                                            uint32_t& r1, uint32_t& r2,
+                                            uint32_t& r3) {
+  asm volatile(
+      "ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+      : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+      : "r"(addr));
+}
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t& r0,
+                                                  uint32_t& r1, uint32_t& r2,
+                                                  uint32_t& r3) {
+  asm volatile(
+      "ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+      : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+      : "r"(addr));
+}
+
+// D = A(16x16, row) * B(16x8, col) + D, fp32 accumulate.
+template <typename T>
+__device__ __forceinline__ void mma_16816(float* d, const uint32_t* a,
+                                          uint32_t b0, uint32_t b1);
+template <>
+__device__ __forceinline__ void mma_16816<__nv_bfloat16>(float* d,
+                                                         const uint32_t* a,
+                                                         uint32_t b0,
+                                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+template <>
+__device__ __forceinline__ void mma_16816<__half>(float* d, const uint32_t* a,
+                                                  uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Hardware base-2 exponential and logarithm (MUFU).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi);
+template <>
+__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+template <>
+__device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T x);
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
+  return __bfloat162float(x);
+}
+template <>
+__device__ __forceinline__ float to_f32<__half>(__half x) {
+  return __half2float(x);
+}
+template <>
+__device__ __forceinline__ float to_f32<float>(float x) {
+  return x;
+}
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+template <>
+__device__ __forceinline__ __half from_f32<__half>(float x) {
+  return __float2half_rn(x);
+}
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) {
+  return x;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Key range [kmin, kmax) that any query row of tokens [i_first, i_last] of a
+// request (q_len queries, L keys) may see.  Query i sits at p = L - q_len + i.
+__device__ __forceinline__ void key_range(int L, int q_len, int i_first,
+                                          int i_last, int causal, int wl,
+                                          int wr, int& kmin, int& kmax) {
+  const int ctx = L - q_len;
+  const int p_lo = ctx + i_first, p_hi = ctx + i_last;
+  kmax = L;
+  if (causal) kmax = min(kmax, p_hi + 1);
+  if (wr >= 0) kmax = min(kmax, p_hi + wr + 1);
+  kmin = 0;
+  if (wl >= 0) kmin = max(0, p_lo - wl);
+  if (kmax < kmin) kmax = kmin;
+}
+
+// ------------------------------------------------------- internal interface
+
+// Parameters of the block-table attention kernels.
+struct AttnParams {
+  const void* q;
+  int64_t q_st, q_sh;
+  const void* kc;
+  const void* vc;
+  int64_t c_sb, c_sr, c_sh;   // cache strides: block, row-in-block, kv-head
+  void* out;
+  int64_t o_st, o_sh;
+  float* lse;                 // [Hq, total_q] natural log, or null
+  int total_q;
+  const int32_t* cu_q;
+  const int32_t* seqused_k;
+  int batch;
+  const int32_t* block_table;
+  int64_t bt_stride;
+  int max_blocks;
+  int64_t num_blocks;
+  int Hq, Hkv, G, BS;
+  float scale;                // softmax scale (natural units)
+  float softcap;              // 0 = none
+  const float* alibi;         // [Hq] or null
+  int causal, wl, wr;
+  // which requests this launch owns: rows = q_b * G in [min_rows, max_rows]
+  int min_rows, max_rows;
+  // split-KV: keys per split (0 = no split: write out/lse directly)
+  int chunk;
+  float* part_o;              // [S, total_q, Hq, D] fp32
+  float* part_lse;            // [S, Hq, total_q] fp32 natural log
+  unsigned* err;
+};
+
+struct CombineParams {
+  const float* part_o;
+  const float* part_lse;
+  void* out;
+  int64_t o_st, o_sh;
+  float* lse;
+  int total_q;
+  const int32_t* cu_q;
+  const int32_t* seqused_k;
+  int batch, Hq, G, D;
+  int causal, wl, wr;
+  int chunk, splits;
+  int min_rows, max_rows;
+};
+
+// Count one kernel launch (reported by pkv_launch_count).
+void note_launch();
+
+// Decode kernel geometry (rows = q_len * G <= kDecodeRows go to it).
+constexpr int kDecodeRows = 16;
+constexpr int kDecodeKT = 64;     // keys per pipeline tile
+
+cudaError_t launch_cache_write(const void* key, const void* value,
+                               int64_t k_st, int64_t k_sh, int64_t v_st,
+                               int64_t v_sh, void* kc, void* vc,
+                               const int64_t* cs, const int64_t* slots,
+                               int64_t num_tokens, int Hkv, int D, int BS,
+                               int64_t num_blocks, int elem_bytes,
+                               unsigned* err, cudaStream_t stream);
+
+cudaError_t launch_decode_attn(const AttnParams& p, int D, bool bf16,
+                               int grid_x, int grid_y, cudaStream_t stream);
+cudaError_t launch_prefill_attn_mma(const AttnParams& p, int D, bool bf16,
+                                    int grid_y, cudaStream_t stream);
+cudaError_t launch_split_combine(const CombineParams& p, bool bf16,
+                                 cudaStream_t stream);
+cudaError_t launch_merge(void* out, const void* o1, const float* l1,
+                         const void* o2, const float* l2, float* lse_out,
+                         int T, int H, int D, pkv_dtype out_dt,
+                         pkv_dtype in_dt, cudaStream_t stream);
+
+}  // namespace pkv

@@ -1,0 +1,302 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle.
+
+Tolerances (stated in the task's correctness bar): attention outputs within
+max-abs 2e-2 (bf16) / 4e-3 (fp16) of the oracle, LSE within 1e-3, the cache
+write bit-exact.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import merge_attn_states_ref, paged_attention_ref
+from oracle.harness import (full_cache_bits, full_reference,
+                            request_reference)
+from paged_kv_cache_318_gb300 import api, workloads
+from paged_kv_cache_318_gb300.batch import DeviceBatch
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"bf16": 2e-2, "f16": 4e-3}
+LSE_TOL = 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built(cuda_device):
+    from paged_kv_cache_318_gb300 import _build
+    _build.build()
+    api.load_library()
+
+
+def nan_bits(dtype):
+    """The 16-bit pattern torch uses for NaN in ``dtype`` (the cache's
+    initial fill)."""
+    t = torch.tensor(float("nan"), dtype=dtype)
+    return int(t.view(torch.int16).item()) & 0xFFFF
+
+
+def run_batch(wl, dev, cascade=False):
+    b = DeviceBatch(wl, dev, cascade=cascade)
+    b.write_context()
+    res = b.step(return_lse=not cascade)
+    torch.cuda.synchronize(dev)
+    api.check_device_errors(dev)
+    out, lse = res if isinstance(res, tuple) else (res, None)
+    return b, out.float().cpu().numpy(), \
+        None if lse is None else lse.cpu().numpy()
+
+
+def assert_close(wl, out, lse, ref_out, ref_lse, what=""):
+    assert np.isfinite(out).all(), what + ": non-finite output"
+    err = np.abs(out - ref_out).max() if out.size else 0.0
+    assert err <= TOL[wl.dtype], "%s out err %g" % (what, err)
+    if lse is not None:
+        fin = np.isfinite(ref_lse)
+        assert np.array_equal(np.isfinite(lse), fin), what + ": lse -inf set"
+        lerr = np.abs(lse[fin] - ref_lse[fin]).max() if fin.any() else 0.0
+        assert lerr <= LSE_TOL, "%s lse err %g" % (what, lerr)
+
+
+# ----------------------------------------------------------- small, full
+def small_cases():
+    return {
+        "tiny_decode": lambda dt: workloads.tiny_decode(dtype=dt),
+        "batched_decode_s": lambda dt: workloads.batched_decode(
+            dtype=dt, batch=9, lo=20, hi=700, pool_blocks=600),
+        "prefill_s": lambda dt: workloads.prefill_with_prefix(
+            dtype=dt, batch=3, q_lo=17, q_hi=200, c_lo=0, c_hi=150),
+        "mixed_s": lambda dt: workloads.mixed_gemma(
+            dtype=dt, n_prefill=2, chunk=40, c_hi=300, n_decode=6, d_lo=50,
+            d_hi=600),
+        "long_decode_s": lambda dt: workloads.long_decode(
+            dtype=dt, batch=2, ctx=3000, num_splits=16),
+    }
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("name", list(small_cases()))
+def test_small_workloads_full_outputs(cuda_device, name, dtype):
+    wl = small_cases()[name](dtype)
+    batch, out, lse = run_batch(wl, cuda_device)
+    ref_out, ref_lse = full_reference(wl)
+    assert_close(wl, out, lse, ref_out, ref_lse, name)
+    bits = batch.kv_cache.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(bits, full_cache_bits(wl, nan_bits(wl.torch_dtype))), \
+        name + ": cache bits"
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_cascade_small(cuda_device, dtype):
+    wl = workloads.cascade_decode(dtype=dtype, batch=9, prefix=128,
+                                  unique=70)
+    _, out, _ = run_batch(wl, cuda_device, cascade=True)
+    ref_out, _ = full_reference(wl)
+    assert_close(wl, out, None, ref_out, None, "cascade")
+
+
+# ------------------------------------------------------ feature matrix
+FEATURES = [
+    # q_lens, seq_lens, Hq, Hkv, D, BS, kwargs
+    ([1, 1, 1], [1, 17, 300], 8, 8, 64, 16, dict()),
+    ([1, 1], [100, 513], 8, 1, 128, 32, dict(num_splits=4)),
+    ([1, 2, 3], [60, 61, 62], 16, 2, 128, 16, dict(num_splits=1)),
+    ([5, 1, 70], [90, 33, 70], 4, 2, 64, 16, dict(causal=False)),
+    ([33, 1], [200, 129], 8, 4, 128, 64, dict(window_size=(31, 0))),
+    ([20, 3], [70, 100], 4, 4, 64, 16, dict(window_size=(10, 5),
+                                            causal=False)),
+    ([1, 40], [500, 90], 4, 2, 256, 32, dict(softcap=5.0)),
+    ([3, 1, 19], [50, 77, 19], 8, 2, 128, 16,
+     dict(alibi_slopes=[0.5, 0.25, 0.125, 0.0625, 0.03, 0.01, 0.3, 0.2])),
+    ([0, 4, 0], [10, 9, 0], 4, 2, 64, 16, dict()),      # empty requests
+    ([1] * 5, [4100] * 5, 16, 2, 256, 32, dict(window_size=(1000, 0),
+                                                 softcap=50.0)),
+]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("idx", range(len(FEATURES)))
+def test_feature_matrix(cuda_device, idx, dtype):
+    q_lens, seq_lens, Hq, Hkv, D, BS, kw = FEATURES[idx]
+    wl = workloads.build_workload("feat%d" % idx, 500 + idx, q_lens,
+                                  seq_lens, Hq, Hkv, D, BS, dtype=dtype, **kw)
+    _, out, lse = run_batch(wl, cuda_device)
+    ref_out, ref_lse = full_reference(wl)
+    assert_close(wl, out, lse, ref_out, ref_lse, "feature %d" % idx)
+
+
+def test_rows_without_keys(cuda_device):
+    """seqused_k below the query count: early rows see no key (out 0,
+    lse -inf); a request with no keys at all likewise."""
+    import dataclasses
+    dev = cuda_device
+    wl = workloads.build_workload("empty", 9, [3, 1, 2], [10, 5, 40], 4, 2,
+                                  64, 16)
+    b = DeviceBatch(wl, dev)
+    b.write_context()
+    b.write_new()
+    short = np.array([2, 0, 40], dtype=np.int32)
+    b.seqused_k.copy_(torch.from_numpy(short))
+    out, lse = b.attend()
+    torch.cuda.synchronize(dev)
+    ref_out, ref_lse = full_reference(dataclasses.replace(wl,
+                                                          seq_lens=short))
+    assert_close(wl, out.float().cpu().numpy(), lse.cpu().numpy(), ref_out,
+                 ref_lse, "rows without keys")
+    assert np.isneginf(ref_lse[:, 0]).all()
+
+
+def test_split_counts_agree(cuda_device):
+    """Every explicit split count gives the same answer within tolerance."""
+    wl = workloads.build_workload("splits", 77, [1] * 4, [3000, 64, 1, 2047],
+                                  32, 8, 128, 16)
+    ref_out, ref_lse = full_reference(wl)
+    for s in (0, 1, 2, 3, 7, 16, 64):
+        wl.num_splits = s
+        _, out, lse = run_batch(wl, cuda_device)
+        assert_close(wl, out, lse, ref_out, ref_lse, "splits=%d" % s)
+
+
+# --------------------------------------------------------- cache write
+def test_cache_write_hnd_view_and_padding(cuda_device):
+    """HND physical cache seen through an NHD view; padded key rows past
+    len(slot_mapping); -1 slots skipped; bit-exact."""
+    dev = cuda_device
+    NB, BS, H, D = 12, 16, 4, 128
+    rng = np.random.default_rng(1)
+    T = 40
+    slots = rng.permutation(NB * BS)[:T].astype(np.int64)
+    slots[[3, 17]] = -1
+    key = torch.randn(T + 5, H, D, dtype=torch.bfloat16, device=dev)
+    val = torch.randn(T + 5, H, D, dtype=torch.bfloat16, device=dev)
+    hnd = torch.full((2, NB, H, BS, D), math.nan, dtype=torch.bfloat16,
+                     device=dev)
+    kc, vc = hnd.permute(0, 1, 3, 2, 4).unbind(0)
+    api.reshape_and_cache_flash(key, val, kc, vc,
+                                torch.from_numpy(slots).to(dev))
+    torch.cuda.synchronize(dev)
+    from oracle import reshape_and_cache_ref
+    kb = key.cpu().view(torch.int16).numpy().view(np.uint16)
+    vb = val.cpu().view(torch.int16).numpy().view(np.uint16)
+    ek = np.full((NB, BS, H, D), nan_bits(torch.bfloat16), np.uint16)
+    ev = ek.copy()
+    reshape_and_cache_ref(kb, vb, ek, ev, slots)
+    got = hnd.permute(0, 1, 3, 2, 4).cpu().contiguous().view(torch.int16) \
+        .numpy().view(np.uint16)
+    assert np.array_equal(got[0], ek) and np.array_equal(got[1], ev)
+
+
+def test_cache_write_strided_key_rows(cuda_device):
+    """key/value as slices of a fused qkv tensor (token stride > Hkv*D)."""
+    dev = cuda_device
+    NB, BS, H, D = 6, 16, 2, 64
+    qkv = torch.randn(30, 4 * H * D, dtype=torch.float16, device=dev)
+    key = qkv[:, H * D:2 * H * D].view(30, H, D)
+    val = qkv[:, 2 * H * D:3 * H * D].view(30, H, D)
+    cache = torch.zeros(2, NB, BS, H, D, dtype=torch.float16, device=dev)
+    slots = torch.arange(30, dtype=torch.int64, device=dev) * 3
+    api.reshape_and_cache_flash(key, val, cache[0], cache[1], slots)
+    torch.cuda.synchronize(dev)
+    flat = cache.view(2, NB * BS, H, D)
+    assert torch.equal(flat[0, slots], key) and torch.equal(flat[1, slots],
+                                                            val)
+
+
+def test_out_of_range_indices_are_skipped_and_flagged(cuda_device):
+    """A block id >= num_blocks and a slot past the cache: the kernels skip
+    them (no access), the error word reports PKV_ERR_BAD_INDEX."""
+    dev = cuda_device
+    wl = workloads.build_workload("bad", 3, [1, 1], [20, 40], 4, 2, 64, 16)
+    b = DeviceBatch(wl, dev)
+    b.write_context()
+    api.check_device_errors(dev)
+    b.block_table[1, 1] = wl.num_blocks + 5
+    b.step()
+    with pytest.raises(api.PkvError) as ei:
+        api.check_device_errors(dev)
+    assert ei.value.status == api.PKV_ERR_BAD_INDEX
+    assert torch.isfinite(b.out).all()
+    bad = torch.tensor([wl.num_blocks * wl.block_size + 7], dtype=torch.int64,
+                       device=dev)
+    api.reshape_and_cache_flash(b.k_new[:1], b.v_new[:1], b.key_cache,
+                                b.value_cache, bad)
+    with pytest.raises(api.PkvError):
+        api.check_device_errors(dev)
+    api.check_device_errors(dev)   # cleared
+
+
+# ---------------------------------------------------------------- merge
+@pytest.mark.parametrize("dts", [("bf16", "bf16"), ("f16", "f16"),
+                                 ("f32", "f32"), ("bf16", "f32")])
+def test_merge_attn_states(cuda_device, dts):
+    dev = cuda_device
+    tmap = {"bf16": torch.bfloat16, "f16": torch.float16,
+            "f32": torch.float32}
+    out_dt, in_dt = tmap[dts[0]], tmap[dts[1]]
+    T, H, D = 37, 6, 128
+    g = torch.Generator(device="cpu").manual_seed(5)
+    o1 = torch.randn(T, H, D, generator=g).to(in_dt)
+    o2 = torch.randn(T, H, D, generator=g).to(in_dt)
+    l1 = torch.randn(H, T, generator=g) * 3
+    l2 = torch.randn(H, T, generator=g) * 3
+    l1[0, :5] = -math.inf
+    l2[1, 3:9] = -math.inf
+    l1[2, 7] = l2[2, 7] = -math.inf
+    out = torch.empty(T, H, D, dtype=out_dt, device=dev)
+    lse = torch.empty(H, T, dtype=torch.float32, device=dev)
+    api.merge_attn_states(out, o1.to(dev), l1.to(dev), o2.to(dev), l2.to(dev),
+                          output_lse=lse)
+    torch.cuda.synchronize(dev)
+    ro, rl = merge_attn_states_ref(o1.double().numpy(), l1.double().numpy(),
+                                   o2.double().numpy(), l2.double().numpy())
+    tol = {torch.bfloat16: 2e-2, torch.float16: 4e-3, torch.float32: 1e-5}
+    assert np.abs(out.float().cpu().numpy() - ro).max() <= tol[out_dt]
+    got_l = lse.cpu().numpy()
+    assert np.array_equal(np.isfinite(got_l), np.isfinite(rl))
+    fin = np.isfinite(rl)
+    assert np.abs(got_l[fin] - rl[fin]).max() <= LSE_TOL
+
+
+# -------------------------------------------- full sizes, sampled outputs
+def _sampled(wl, dev, reqs, last_rows=None, cascade=False):
+    b, out, lse = run_batch(wl, dev, cascade=cascade)
+    for r in reqs:
+        t0, t1 = int(wl.cu_seqlens_q[r]), int(wl.cu_seqlens_q[r + 1])
+        k = t1 - t0 if last_rows is None else min(last_rows, t1 - t0)
+        ref_o, ref_l = request_reference(wl, r, last_rows=k)
+        got_l = None if lse is None else lse[:, t1 - k:t1]
+        assert_close(wl, out[t1 - k:t1], got_l, ref_o, ref_l,
+                     "%s req %d" % (wl.name, r))
+    # the cache rows of sampled slots are bit-exact copies of the inputs
+    slots = wl.slot_mapping_new
+    kbits = b.key_cache.view(torch.int16).reshape(
+        -1, wl.num_kv_heads, wl.head_size)
+    idx = torch.from_numpy(slots[:: max(1, len(slots) // 64)]).to(dev)
+    src = torch.arange(0, len(slots), max(1, len(slots) // 64), device=dev)
+    assert torch.equal(kbits[idx], b.k_new.view(torch.int16)[src])
+    return b
+
+
+def test_full_batched_decode_sampled(cuda_device):
+    wl = workloads.batched_decode(device=cuda_device)
+    _sampled(wl, cuda_device, [0, 17, 63])
+
+
+def test_full_prefill_sampled(cuda_device):
+    wl = workloads.prefill_with_prefix(device=cuda_device)
+    _sampled(wl, cuda_device, [0, 5], last_rows=96)
+
+
+def test_full_mixed_sampled(cuda_device):
+    wl = workloads.mixed_gemma(device=cuda_device)
+    _sampled(wl, cuda_device, [0, 61, 123, 124, 127], last_rows=64)
+
+
+def test_full_long_decode_sampled(cuda_device):
+    wl = workloads.long_decode(device=cuda_device)
+    _sampled(wl, cuda_device, [0, 7])
+
+
+def test_full_cascade_sampled(cuda_device):
+    wl = workloads.cascade_decode(device=cuda_device)
+    _sampled(wl, cuda_device, [0, 100, 255], cascade=True)
