@@ -179,6 +179,52 @@ PKV_API size_t pkv_paged_attention_workspace_size(
     int causal, int window_left, int window_right, int num_splits);
 
 /*
+ * pkv_paged_attention_varlen_static_scratch -- pkv_paged_attention_varlen
+ * for callers that cannot allocate device memory.
+ *
+ * The source pages have no counterpart of this entry point.
+ *
+ * Some callers cannot provide the `workspace` the split-KV path needs:
+ * plugin hosts and serving runtimes that plan all device memory up front and
+ * give an individual call no scratch, and latency-critical loops that must
+ * not call cudaMalloc/cudaFree (they can block the host and synchronise the
+ * whole device).  This variant takes the same arguments minus
+ * workspace/workspace_bytes and computes the same result.  Its scratch is a
+ * fixed array of PKV_STATIC_SCRATCH_BYTES inside the library's own device
+ * memory, which every GPU that loads the library holds until the process
+ * exits.  It calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * - Set-up: the first call on each device looks up the array's device
+ *   address (cudaGetSymbolAddress, with that device current) and caches it.
+ *   Make that first call before any stream capture.
+ * - Limit: a call whose split plan needs more than PKV_STATIC_SCRATCH_BYTES
+ *   (see pkv_paged_attention_workspace_size) is rejected with
+ *   PKV_ERR_WORKSPACE_TOO_SMALL and a message; nothing is launched.
+ * - Sharing: all calls on a device share the one array and it keeps the
+ *   last call's contents.  Nothing in it needs clearing: every scratch value
+ *   a call reads was written earlier in the same call.  Calls that overlap on
+ *   the GPU (different streams, or several host threads) race on the array
+ *   and corrupt each other's results; order them on one stream.
+ */
+#define PKV_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+
+PKV_API pkv_status pkv_paged_attention_varlen_static_scratch(
+    const void* q, int64_t q_stride_tok, int64_t q_stride_head,
+    const void* key_cache, const void* value_cache,
+    const int64_t cache_strides[4],
+    void* out, int64_t o_stride_tok, int64_t o_stride_head,
+    const int32_t* cu_seqlens_q, const int32_t* seqused_k, int batch,
+    int total_q, int max_seqlen_q, int max_seqlen_k,
+    const int32_t* block_table, int64_t block_table_stride,
+    int max_blocks_per_seq,
+    int num_heads, int num_kv_heads, int head_size, int block_size,
+    int64_t num_blocks,
+    float softmax_scale, int causal, int window_left, int window_right,
+    float softcap, const float* alibi_slopes,
+    int num_splits, float* softmax_lse,
+    pkv_dtype dtype, pkv_stream_t stream);
+
+/*
  * pkv_merge_attn_states -- combine two partial attentions by their LSEs.
  *
  * Source: "vllm/v1/attention/backends/flash_attn.py", cascade_attention (the

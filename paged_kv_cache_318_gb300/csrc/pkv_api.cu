@@ -163,6 +163,9 @@ pkv_status check_attn_shape(int batch, int total_q, int max_q, int max_k,
 }
 
 }  // namespace
+
+void set_last_error(const char* msg) { g_last_error = msg; }
+
 }  // namespace pkv
 
 using namespace pkv;

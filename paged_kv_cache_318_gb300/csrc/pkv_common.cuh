@@ -202,6 +202,9 @@ struct CombineParams {
 // Count one kernel launch (reported by pkv_launch_count).
 void note_launch();
 
+// Set this thread's pkv_last_error message.
+void set_last_error(const char* msg);
+
 // Decode kernel geometry (rows = q_len * G <= kDecodeRows go to it).
 constexpr int kDecodeRows = 16;
 constexpr int kDecodeKT = 64;     // keys per pipeline tile
