@@ -164,6 +164,21 @@ class ClockSampler:
                 "window": "warm-up through timed region"}
 
 
+# ------------------------------------------------------------ multi-rank
+def max_over_ranks(values, device, world):
+    """Element-wise max of per-rank timings (the slowest rank sets the pace
+    of a weak-scaling step)."""
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
+
+
+def aggregate_value(bytes_per_rank_step, step_ms, world):
+    """Whole-job GB/s: every rank moves its own batch per step."""
+    return world * bytes_per_rank_step / (step_ms * 1e-3) / 1e9
+
+
 # ---------------------------------------------------------------- GPU arm
 def time_steps(fn, steps, stream, attn_events=None):
     """Total device ms of ``steps`` calls of fn on ``stream``."""
@@ -247,13 +262,9 @@ def gpu_arm(args, rank, world, dev):
     flops = prefill_flops(pre)
     del pb
 
-    step_ms = ms / args.steps
-    stats = torch.tensor([step_ms, e2e_ms / args.steps, attn_ms, pre_ms],
-                         dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(stats, op=torch.distributed.ReduceOp.MAX)
-    step_ms, e2e_step_ms, attn_ms, pre_ms = stats.tolist()
-    value = world * acct["step"] / (step_ms * 1e-3) / 1e9
+    step_ms, e2e_step_ms, attn_ms, pre_ms = max_over_ranks(
+        [ms / args.steps, e2e_ms / args.steps, attn_ms, pre_ms], dev, world)
+    value = aggregate_value(acct["step"], step_ms, world)
     achieved = acct["attention"] / (attn_ms * 1e-3) / 1e9
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT,
@@ -276,8 +287,8 @@ def gpu_arm(args, rank, world, dev):
         "step_bytes": acct,
         "gpu_launches": int(launches),
         "launches_per_step": launches / args.steps,
-        "e2e": {"value": round(world * acct["step"] /
-                               (e2e_step_ms * 1e-3) / 1e9, 1),
+        "e2e": {"value": round(aggregate_value(acct["step"], e2e_step_ms,
+                                               world), 1),
                 "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h),
                 "ms_per_step": round(e2e_step_ms, 5)},

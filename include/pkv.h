@@ -261,6 +261,16 @@ PKV_API pkv_status pkv_merge_attn_states(
 PKV_API pkv_status pkv_check_device_errors(pkv_stream_t stream);
 
 /*
+ * Which kernel serves prefill-class requests (more than 16 packed query rows
+ * per KV head): the tcgen05/TMEM kernel or the warp-level mma.sync kernel.
+ * A process-wide diagnostic switch for A/B comparison; both give the same
+ * result within rounding.  Returns PKV_ERR_INVALID_ARG for other values.
+ */
+#define PKV_PREFILL_TCGEN05 0
+#define PKV_PREFILL_MMA_SYNC 1
+PKV_API pkv_status pkv_set_prefill_kernel(int which);
+
+/*
  * Number of kernels this library has launched in this process (all devices,
  * all threads), for accounting of launches per step.
  */

@@ -83,6 +83,8 @@ def load_library():
         lib.pkv_merge_attn_states.restype = i32
         lib.pkv_merge_attn_states.argtypes = [
             vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]
+        lib.pkv_set_prefill_kernel.restype = i32
+        lib.pkv_set_prefill_kernel.argtypes = [i32]
         lib.pkv_launch_count.restype = ctypes.c_uint64
         lib.pkv_launch_count.argtypes = []
         lib.pkv_check_device_errors.restype = i32
@@ -126,6 +128,15 @@ def _cache_strides(key_cache, value_cache):
         raise ValueError("key_cache and value_cache must share shape and "
                          "strides")
     return (ctypes.c_int64 * 4)(*key_cache.stride())
+
+
+PREFILL_TCGEN05 = 0
+PREFILL_MMA_SYNC = 1
+
+
+def set_prefill_kernel(which: int):
+    """Choose the prefill kernel (PREFILL_TCGEN05 or PREFILL_MMA_SYNC)."""
+    _check(load_library().pkv_set_prefill_kernel(int(which)))
 
 
 def launch_count() -> int:

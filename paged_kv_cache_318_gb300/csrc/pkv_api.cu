@@ -20,6 +20,8 @@ namespace pkv {
 __device__ unsigned g_device_error = 0;
 
 static std::atomic<uint64_t> g_launches{0};
+// prefill kernel: PKV_PREFILL_TCGEN05 or PKV_PREFILL_MMA_SYNC
+static std::atomic<int> g_prefill_kernel{PKV_PREFILL_TCGEN05};
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 namespace {
@@ -173,6 +175,13 @@ using namespace pkv;
 extern "C" {
 
 const char* pkv_last_error(void) { return g_last_error.c_str(); }
+
+pkv_status pkv_set_prefill_kernel(int which) {
+  if (which != PKV_PREFILL_TCGEN05 && which != PKV_PREFILL_MMA_SYNC)
+    return fail(PKV_ERR_INVALID_ARG, "unknown prefill kernel %d", which);
+  g_prefill_kernel.store(which);
+  return PKV_OK;
+}
 
 uint64_t pkv_launch_count(void) {
   return g_launches.load(std::memory_order_relaxed);
@@ -399,8 +408,14 @@ pkv_status pkv_paged_attention_varlen(
     f.min_rows = kDecodeRows + 1;
     f.max_rows = 0x7fffffff;
     f.chunk = 0;
-    cudaError_t e =
-        launch_prefill_attn_mma(f, head_size, bf16, pl.prefill_tiles, s);
+    const int64_t prow = static_cast<int64_t>(max_seqlen_q) * p.G;
+    cudaError_t e;
+    if (g_prefill_kernel.load() == PKV_PREFILL_TCGEN05)
+      e = launch_prefill_attn_tc(f, head_size, bf16,
+                                 static_cast<int>((prow + 127) / 128), s);
+    else
+      e = launch_prefill_attn_mma(f, head_size, bf16,
+                                  static_cast<int>((prow + 63) / 64), s);
     if (e != cudaSuccess) return cuda_fail(e, "prefill attention launch");
   }
   return PKV_OK;

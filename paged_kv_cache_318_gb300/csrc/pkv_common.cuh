@@ -14,6 +14,7 @@ namespace pkv {
 constexpr unsigned kErrBadBlock = 1u;   // block id outside [0, num_blocks)
 constexpr unsigned kErrBadSlot = 2u;    // slot outside the cache
 constexpr unsigned kErrBadTable = 4u;   // key beyond the block-table row
+constexpr unsigned kErrTimeout = 8u;    // a bounded wait gave up
 
 // ---------------------------------------------------------------- PTX helpers
 
@@ -221,6 +222,9 @@ cudaError_t launch_decode_attn(const AttnParams& p, int D, bool bf16,
                                int grid_x, int grid_y, cudaStream_t stream);
 cudaError_t launch_prefill_attn_mma(const AttnParams& p, int D, bool bf16,
                                     int grid_y, cudaStream_t stream);
+cudaError_t launch_prefill_attn_tc(const AttnParams& p, int D, bool bf16,
+                                   int grid_y, cudaStream_t stream);
+int prefill_tc_block_keys(int D);
 cudaError_t launch_split_combine(const CombineParams& p, bool bf16,
                                  cudaStream_t stream);
 cudaError_t launch_merge(void* out, const void* o1, const float* l1,

@@ -1,0 +1,794 @@
+// Prefill attention on 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// Source: "vllm/v1/attention/backends/flash_attn.py", FlashAttentionImpl.
+// forward (flash_attn_varlen_func over the paged cache for requests with more
+// than one query: cu_seqlens_q, seqused_k, block_table, causal, window_size,
+// softcap, alibi_slopes, LSE) and cascade_attention (the shared prefix is one
+// non-causal "sequence" of all the batch's queries).
+//
+// One CTA owns 128 packed query rows of one (request, KV head): packed row R
+// is token R / G, query head g * G + R % G, so the G query heads of a KV head
+// share every K/V tile.  The key range is walked in tiles of BN keys:
+//
+//   S_j  = Q K_j^T           tcgen05.mma kind::f16, M=128, N=BN, K=D, fp32 in
+//                            TMEM (two S buffers, so S_{j+1} runs while the
+//                            softmax warps work on S_j)
+//   P_j  = exp2(S_j - m)     4 softmax warps, one thread per row (TMEM lane),
+//                            written to shared memory as bf16/fp16
+//   O   += P_j V_j           tcgen05.mma, M=128, N=D, K=BN, fp32 in TMEM
+//
+// Warp roles (192 threads): warps 0-3 softmax + epilogue, warp 4 issues the
+// MMAs (one elected lane) and owns the TMEM allocation, warp 5 issues TMA
+// loads of K/V pages through the block table (one 2-D box of RB rows x 64
+// elements per page and 64-column block, 128-byte swizzle) into a 2-stage
+// ring.  Stages and S/P/O hand-offs are tracked with mbarriers; tcgen05.commit
+// arrives on them when the MMAs finish.
+//
+// The running max is only moved when it grows by more than 2^8 (log2 units),
+// so the O rescale (a TMEM load/multiply/store) is rare; softmax values then
+// stay below 256, well inside bf16/fp32 range, and the final 1/l uses the
+// same reference max, so the result is unchanged.
+//
+// Every mbarrier wait is bounded.  A wait that runs out sets the device error
+// word (kErrTimeout), raises a CTA-wide abort flag, and every role drains its
+// in-flight copies and MMAs before the TMEM is freed and the CTA exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include <mutex>
+#include <type_traits>
+
+#include "pkv_common.cuh"
+
+namespace pkv {
+namespace tc {
+
+constexpr int BM = 128;
+constexpr int NUM_THREADS = 192;
+constexpr int MMA_WARP = 4;
+constexpr int LOAD_WARP = 5;
+constexpr uint32_t kSpinLimit = 1u << 28;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+constexpr float kRescaleThreshold = 8.f;   // log2 units
+
+template <int D>
+struct Cfg {
+  static constexpr int BN = (D <= 128) ? 128 : 64;   // keys per tile
+  static constexpr int NCB = D / 64;                 // 64-column blocks of D
+  static constexpr int PCB = BN / 64;                // 64-column blocks of P
+  static constexpr int Q_BYTES = BM * D * 2;
+  static constexpr int KV_BYTES = BN * D * 2;        // one K or V tile
+  static constexpr int P_BYTES = BM * BN * 2;
+  static constexpr int STAGES = 2;
+  static constexpr int S_COL = 0;                    // S buffers at 0, BN
+  static constexpr int O_COL = 2 * BN;
+  static constexpr int TMEM_COLS = 512;
+  static_assert(2 * BN + D <= TMEM_COLS, "TMEM budget");
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + Q_BYTES;
+  static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
+  static constexpr int OFF_P = OFF_V + STAGES * KV_BYTES;
+  static constexpr int OFF_BAR = OFF_P + P_BYTES;
+  static constexpr int BAR_BYTES = 256;
+  // keep one CTA per SM (the CTA takes all 512 TMEM columns)
+  static constexpr int SMEM_USED = OFF_BAR + BAR_BYTES + 1024;
+  static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
+};
+
+struct TcParams {
+  const void* q;
+  int64_t q_st, q_sh;
+  void* out;
+  int64_t o_st, o_sh;
+  float* lse;
+  int total_q;
+  const int32_t* cu_q;
+  const int32_t* seqused_k;
+  const int32_t* block_table;
+  int64_t bt_stride;
+  int max_blocks;
+  int64_t num_blocks;
+  int Hq, Hkv, G, BS, RB;
+  float scale, softcap;
+  const float* alibi;
+  int causal, wl, wr;
+  int min_rows;
+  int kv_order_hnd;   // tensor-map dim order: 1 = (D, BS, Hkv, NB)
+  unsigned* err;
+};
+
+// ------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar),
+               "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile(
+      "mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+      "r"(bytes)
+      : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n.reg .pred p;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait: false when the CTA is aborting, or after kWaitLimitNs (then
+// the error word gets kErrTimeout and the CTA-wide abort flag is raised).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          volatile int* abort_flag,
+                                          unsigned* err) {
+  if (mbar_try(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try(bar, parity)) return true;
+    if ((it & 255u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs || it > kSpinLimit) {
+        *abort_flag = 1;
+        atomicOr(err, kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+// Wait used while draining in-flight work: no abort check, still bounded.
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0; it < kSpinLimit; ++it) {
+    if (mbar_try(bar, parity)) return;
+    if ((it & 255u) == 255u && globaltimer_ns() - t0 > kWaitLimitNs) return;
+  }
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap,
+                                            int c0, int c1, int c2, int c3,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::"
+      "complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2),
+      "r"(c3), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (sm_100 encoding).
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo,
+                                          uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;     // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;     // SWIZZLE_128B
+  return d;
+}
+
+// Instruction descriptor of kind::f16 with fp32 accumulate.
+__host__ __device__ constexpr uint32_t idesc(int M, int N, bool bf16,
+                                             bool b_mn_major) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
+         ((b_mn_major ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a,
+                                        uint64_t b, uint32_t id,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+          d_tmem),
+      "l"(a), "l"(b), "r"(id), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 "
+      "[%0];" ::"r"(bar)
+      : "memory");
+}
+
+// 32 lanes x 32 columns of fp32 from TMEM.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, "
+      "[%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]),
+        "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]),
+        "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+        "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
+          taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])),
+      "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+      "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])),
+      "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])),
+      "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15])),
+      "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])),
+      "r"(__float_as_uint(v[20])), "r"(__float_as_uint(v[21])),
+      "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])),
+      "r"(__float_as_uint(v[26])), "r"(__float_as_uint(v[27])),
+      "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Byte offset of 16-byte chunk c (0..7) of row r inside a 128-byte-swizzled
+// column block whose rows are 128 bytes apart.
+__device__ __forceinline__ uint32_t sw128(int r, int c) {
+  return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <typename T, int D>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v) {
+  using C = Cfg<D>;
+  constexpr int BN = C::BN;
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw_u = smem_u32(smem_raw);
+  const uint32_t base_u = (raw_u + 1023u) & ~1023u;
+  unsigned char* base = smem_raw + (base_u - raw_u);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = blockIdx.x / p.Hkv;
+  const int g = blockIdx.x - b * p.Hkv;
+  const int G = p.G;
+  const int q0 = p.cu_q[b];
+  const int q_len = min(p.cu_q[b + 1] - q0, p.total_q - q0);
+  if (q0 < 0 || q_len <= 0) return;
+  const int rows = q_len * G;
+  if (rows < p.min_rows) return;
+  const int row0 = (gridDim.y - 1 - blockIdx.y) * BM;
+  if (row0 >= rows) return;
+  const int row_end = min(rows, row0 + BM);
+  const int L = p.seqused_k[b];
+  const int L_tab = min(L, p.max_blocks * p.BS);
+  int kmin, kmax;
+  key_range(L, q_len, row0 / G, (row_end - 1) / G, p.causal, p.wl, p.wr, kmin,
+            kmax);
+  kmax = min(kmax, L_tab);
+  const int RB = p.RB;
+  const int kstart = (kmin / RB) * RB;
+  const int n_tiles = kmax > kmin ? (kmax - kstart + BN - 1) / BN : 0;
+  const int ctx = L - q_len;
+  T* __restrict__ OUT = static_cast<T*>(p.out);
+
+  if (n_tiles == 0) {
+    // no admissible key for any row of the tile: out = 0, lse = -inf
+    for (int i = tid; i < (row_end - row0) * (D / 8); i += NUM_THREADS) {
+      const int r = row0 + i / (D / 8), c = i % (D / 8);
+      const int tok = q0 + r / G, h = g * G + r % G;
+      *reinterpret_cast<uint4*>(OUT + static_cast<int64_t>(tok) * p.o_st +
+                                static_cast<int64_t>(h) * p.o_sh + c * 8) =
+          make_uint4(0, 0, 0, 0);
+      if (p.lse && c == 0)
+        p.lse[static_cast<int64_t>(h) * p.total_q + tok] = -INFINITY;
+    }
+    return;
+  }
+
+  const uint32_t sQ = base_u + C::OFF_Q;
+  const uint32_t sK = base_u + C::OFF_K;
+  const uint32_t sV = base_u + C::OFF_V;
+  const uint32_t sP = base_u + C::OFF_P;
+  const uint32_t bar0 = base_u + C::OFF_BAR;
+  // barrier addresses
+  auto k_full = [&](int s) { return bar0 + 8 * (0 + s); };
+  auto v_full = [&](int s) { return bar0 + 8 * (2 + s); };
+  auto k_empty = [&](int s) { return bar0 + 8 * (4 + s); };
+  auto v_empty = [&](int s) { return bar0 + 8 * (6 + s); };
+  auto s_full = [&](int s) { return bar0 + 8 * (8 + s); };
+  auto s_free = [&](int s) { return bar0 + 8 * (10 + s); };
+  const uint32_t p_full = bar0 + 8 * 12;
+  const uint32_t pv_done = bar0 + 8 * 13;
+  const uint32_t final_bar = bar0 + 8 * 14;
+  uint32_t* tmem_slot =
+      reinterpret_cast<uint32_t*>(base + C::OFF_BAR + 8 * 16);
+  volatile int* abort_flag =
+      reinterpret_cast<volatile int*>(base + C::OFF_BAR + 8 * 16 + 4);
+
+  if (tid == 0) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(k_full(s), 1);
+      mbar_init(v_full(s), 1);
+      mbar_init(k_empty(s), 1);
+      mbar_init(v_empty(s), 1);
+      mbar_init(s_full(s), 1);
+      mbar_init(s_free(s), 128);
+    }
+    mbar_init(p_full, 128);
+    mbar_init(pv_done, 1);
+    mbar_init(final_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == MMA_WARP) {
+    asm volatile(
+        "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::
+            "r"(smem_u32(tmem_slot)),
+        "r"(C::TMEM_COLS)
+        : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;"
+                 ::: "memory");
+  }
+
+  // Q tile: packed rows, zero past row_end, 128-byte swizzled column blocks
+  {
+    const T* Q = static_cast<const T*>(p.q);
+    for (int i = tid; i < BM * (D / 8); i += NUM_THREADS) {
+      const int r = i / (D / 8), ch = i % (D / 8);
+      const int R = row0 + r;
+      const bool ok = R < row_end;
+      const T* src = Q;
+      if (ok)
+        src = Q + static_cast<int64_t>(q0 + R / G) * p.q_st +
+              static_cast<int64_t>(g * G + R % G) * p.q_sh + ch * 8;
+      cp_async_16(sQ + (ch >> 3) * (BM * 128) + sw128(r, ch & 7), src,
+                  ok ? 16 : 0);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    fence_proxy_async();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == LOAD_WARP) {
+    // ---------------------------------------------------------- producer
+    int k_iss = 0, v_iss = 0;
+    if (lane == 0) {
+      const int32_t* bt = p.block_table + b * p.bt_stride;
+      for (int j = 0; j < n_tiles; ++j) {
+        const int s = j & 1;
+        const uint32_t ph = (j >> 1) & 1;
+        const int kt = kstart + j * BN;
+        int nbox = (kmax - kt + RB - 1) / RB;
+        if (nbox > BN / RB) nbox = BN / RB;
+        const uint32_t bytes = nbox * C::NCB * RB * 128;
+        bool stop = false;
+        for (int mat = 0; mat < 2; ++mat) {
+          const uint32_t empty = mat ? v_empty(s) : k_empty(s);
+          const uint32_t full = mat ? v_full(s) : k_full(s);
+          if (j >= 2 && !mbar_wait(empty, ph ^ 1, abort_flag, p.err)) {
+            stop = true;
+            break;
+          }
+          mbar_expect_tx(full, bytes);
+          const void* tm = mat ? static_cast<const void*>(&tm_v)
+                               : static_cast<const void*>(&tm_k);
+          const uint32_t dst0 = (mat ? sV : sK) + s * C::KV_BYTES;
+          for (int i = 0; i < nbox; ++i) {
+            const int k0 = kt + i * RB;
+            const int jb = k0 / p.BS;
+            int blk = __ldg(bt + jb);
+            if (blk < 0 || blk >= p.num_blocks) {
+              atomicOr(p.err, kErrBadBlock);
+              blk = 0;
+            }
+            const int row = k0 - jb * p.BS;
+            for (int cb = 0; cb < C::NCB; ++cb) {
+              const uint32_t dst = dst0 + cb * (BN * 128) + i * RB * 128;
+              if (p.kv_order_hnd)
+                tma_load_4d(dst, tm, cb * 64, row, g, blk, full);
+              else
+                tma_load_4d(dst, tm, cb * 64, g, row, blk, full);
+            }
+          }
+          if (mat) v_iss = j + 1; else k_iss = j + 1;
+        }
+        if (stop || *abort_flag) break;
+      }
+      // drain: the last copies of each stage must land before the CTA exits
+      for (int t = max(0, k_iss - 2); t < k_iss; ++t)
+        mbar_drain(k_full(t & 1), (t >> 1) & 1);
+      for (int t = max(0, v_iss - 2); t < v_iss; ++t)
+        mbar_drain(v_full(t & 1), (t >> 1) & 1);
+    }
+  } else if (warp == MMA_WARP) {
+    // ---------------------------------------------------------- MMA issuer
+    constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value;
+    constexpr uint32_t ID_S = idesc(128, BN, kBF16, false);
+    constexpr uint32_t ID_PV = idesc(128, D, kBF16, true);
+    bool ok = true;
+    auto do_pv = [&](int i) -> bool {
+      const int s = i & 1;
+      if (!mbar_wait(p_full, i & 1, abort_flag, p.err)) return false;
+      if (!mbar_wait(v_full(s), (i >> 1) & 1, abort_flag, p.err)) return false;
+      // zero V rows that hold no key of this request (beyond seqused_k, or
+      // pages that were not loaded), so 0 * garbage never reaches O
+      const int kt = kstart + i * BN;
+      int nbox = (kmax - kt + RB - 1) / RB;
+      if (nbox > BN / RB) nbox = BN / RB;
+      int r0 = min(nbox * RB, max(L - kt, 0));
+      if (r0 < BN) {
+        const uint32_t v0 = sV + s * C::KV_BYTES;
+        for (int idx = lane; idx < (BN - r0) * 8 * C::NCB; idx += 32) {
+          const int cb = idx / ((BN - r0) * 8);
+          const int rem = idx - cb * ((BN - r0) * 8);
+          const int r = r0 + rem / 8, c = rem % 8;
+          asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(
+                           v0 + cb * (BN * 128) + r * 128 + (c << 4)),
+                       "r"(0)
+                       : "memory");
+        }
+        fence_proxy_async();
+        __syncwarp();
+      }
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t v0 = sV + s * C::KV_BYTES;
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k) {
+          const uint64_t a = sdesc(sP + (k >> 2) * (BM * 128) + (k & 3) * 32,
+                                   16, 1024);
+          const uint64_t bdesc = sdesc(v0 + k * 16 * 128, BN * 128, 1024);
+          mma_f16(tmem + C::O_COL, a, bdesc, ID_PV, (i > 0 || k > 0) ? 1 : 0);
+        }
+        mma_commit(pv_done);
+        mma_commit(v_empty(s));
+      }
+      __syncwarp();
+      return true;
+    };
+    for (int j = 0; j < n_tiles && ok; ++j) {
+      const int s = j & 1;
+      if (!mbar_wait(k_full(s), (j >> 1) & 1, abort_flag, p.err)) {
+        ok = false;
+        break;
+      }
+      if (j >= 2 &&
+          !mbar_wait(s_free(s), ((j - 2) >> 1) & 1, abort_flag, p.err)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t k0 = sK + s * C::KV_BYTES;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint64_t a =
+              sdesc(sQ + (k >> 2) * (BM * 128) + (k & 3) * 32, 16, 1024);
+          const uint64_t bdesc =
+              sdesc(k0 + (k >> 2) * (BN * 128) + (k & 3) * 32, 16, 1024);
+          mma_f16(tmem + C::S_COL + s * BN, a, bdesc, ID_S, k > 0 ? 1 : 0);
+        }
+        mma_commit(s_full(s));
+        mma_commit(k_empty(s));
+      }
+      __syncwarp();
+      if (j >= 1 && !do_pv(j - 1)) ok = false;
+    }
+    if (ok) do_pv(n_tiles - 1);
+    // all issued MMAs must finish before TMEM is released
+    if (lane == 0) mma_commit(final_bar);
+    __syncwarp();
+    mbar_drain(final_bar, 0);
+  } else {
+    // ---------------------------------------------------- softmax warps
+    const int r = tid;                         // row in tile == TMEM lane
+    const int R = row0 + r;
+    const bool valid = R < row_end;
+    const int pos = ctx + (valid ? R / G : 0);
+    const int h = g * G + (valid ? R % G : 0);
+    const float slope = (p.alibi && valid) ? p.alibi[h] : 0.f;
+    const bool plain = p.softcap <= 0.f && p.alibi == nullptr;
+    const float scale_log2 = p.scale * kLog2e;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int sb = j & 1;
+      if (!mbar_wait(s_full(sb), (j >> 1) & 1, abort_flag, p.err)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float sv[BN];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c)
+        tmem_ld32(tmem + lane_base + C::S_COL + sb * BN + c * 32, sv + c * 32);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(s_free(sb));
+
+      const int kt = kstart + j * BN;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < BN; ++k) {
+        const int key = kt + k;
+        float x = sv[k];
+        if (plain) {
+          x *= scale_log2;
+        } else {
+          x *= p.scale;
+          if (p.softcap > 0.f) x = p.softcap * tanhf(x / p.softcap);
+          if (p.alibi) x -= slope * fabsf(float(pos - key));
+          x *= kLog2e;
+        }
+        bool adm = valid && key >= kmin && key < kmax;
+        if (p.causal) adm = adm && key <= pos;
+        if (p.wl >= 0) adm = adm && key >= pos - p.wl;
+        if (p.wr >= 0) adm = adm && key <= pos + p.wr;
+        x = adm ? x : -INFINITY;
+        sv[k] = x;
+        mx = fmaxf(mx, x);
+      }
+      const bool grow = mx > m_ref + kRescaleThreshold;
+      float alpha = 1.f;
+      if (grow) {
+        alpha = ex2(m_ref - mx);      // m_ref = -inf -> 0
+        m_ref = mx;
+        l *= alpha;
+      }
+      const float base_m = (m_ref == -INFINITY) ? 0.f : m_ref;
+      float sum = 0.f;
+#pragma unroll
+      for (int k = 0; k < BN; ++k) {
+        sv[k] = ex2(sv[k] - base_m);
+        sum += sv[k];
+      }
+      l += sum;
+      // PV_{j-1} must be done before O is rescaled or P is overwritten
+      if (j >= 1 && !mbar_wait(pv_done, (j - 1) & 1, abort_flag, p.err)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (j >= 1 && __any_sync(0xffffffffu, grow)) {
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          float ov[32];
+          const uint32_t ta = tmem + lane_base + C::O_COL + c * 32;
+          tmem_ld32(ta, ov);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ov[e] *= alpha;
+          tmem_st32(ta, ov);
+        }
+        tmem_wait_st();
+      }
+      // P row -> shared memory (K-major, 128-byte swizzle)
+#pragma unroll
+      for (int cb = 0; cb < C::PCB; ++cb) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const float* e = sv + cb * 64 + c * 8;
+          const uint32_t a0 = pack2<T>(e[0], e[1]), a1 = pack2<T>(e[2], e[3]);
+          const uint32_t a2 = pack2<T>(e[4], e[5]), a3 = pack2<T>(e[6], e[7]);
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                           sP + cb * (BM * 128) + sw128(r, c)),
+                       "r"(a0), "r"(a1), "r"(a2), "r"(a3)
+                       : "memory");
+        }
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      mbar_arrive(p_full);
+    }
+    if (ok && mbar_wait(pv_done, (n_tiles - 1) & 1, abort_flag, p.err)) {
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const int tok = q0 + (valid ? R / G : 0);
+      T* dst = OUT + static_cast<int64_t>(tok) * p.o_st +
+               static_cast<int64_t>(h) * p.o_sh;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        float ov[32];
+        tmem_ld32(tmem + lane_base + C::O_COL + c * 32, ov);
+        tmem_wait_ld();
+        if (valid) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            uint4 pk;
+            pk.x = pack2<T>(ov[e] * inv, ov[e + 1] * inv);
+            pk.y = pack2<T>(ov[e + 2] * inv, ov[e + 3] * inv);
+            pk.z = pack2<T>(ov[e + 4] * inv, ov[e + 5] * inv);
+            pk.w = pack2<T>(ov[e + 6] * inv, ov[e + 7] * inv);
+            *reinterpret_cast<uint4*>(dst + c * 32 + e) = pk;
+          }
+        }
+      }
+      if (valid && p.lse)
+        p.lse[static_cast<int64_t>(h) * p.total_q + tok] =
+            l > 0.f ? (m_ref + lg2(l)) * kLn2 : -INFINITY;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    tc_fence_after();
+    asm volatile(
+        "tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+        "r"(C::TMEM_COLS)
+        : "memory");
+  }
+}
+
+// ------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 4-D map over one cache view: (D, Hkv, BS, NB) for NHD strides, (D, BS, Hkv,
+// NB) when the head stride is the larger (HND); box = 64 x 1 x RB x 1.
+bool make_kv_map(CUtensorMap* map, const void* ptr, bool bf16, int D, int BS,
+                 int Hkv, int64_t NB, int64_t s_blk, int64_t s_row,
+                 int64_t s_head, int RB, bool hnd) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4], strides[3];
+  cuuint32_t box[4], estr[4] = {1, 1, 1, 1};
+  dims[0] = D;
+  dims[3] = static_cast<cuuint64_t>(NB);
+  strides[2] = static_cast<cuuint64_t>(s_blk) * 2;
+  box[0] = 64;
+  box[3] = 1;
+  if (hnd) {
+    dims[1] = BS;  strides[0] = static_cast<cuuint64_t>(s_row) * 2;  box[1] = RB;
+    dims[2] = Hkv; strides[1] = static_cast<cuuint64_t>(s_head) * 2; box[2] = 1;
+  } else {
+    dims[1] = Hkv; strides[0] = static_cast<cuuint64_t>(s_head) * 2; box[1] = 1;
+    dims[2] = BS;  strides[1] = static_cast<cuuint64_t>(s_row) * 2;  box[2] = RB;
+  }
+  CUresult r = fn(map,
+                  bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                       : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                  4, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace tc
+
+int prefill_tc_block_keys(int D) { return D <= 128 ? 128 : 64; }
+
+cudaError_t launch_prefill_attn_tc(const AttnParams& a, int D, bool bf16,
+                                   int grid_y, cudaStream_t stream) {
+  using namespace tc;
+  TcParams p{};
+  p.q = a.q;
+  p.q_st = a.q_st;
+  p.q_sh = a.q_sh;
+  p.out = a.out;
+  p.o_st = a.o_st;
+  p.o_sh = a.o_sh;
+  p.lse = a.lse;
+  p.total_q = a.total_q;
+  p.cu_q = a.cu_q;
+  p.seqused_k = a.seqused_k;
+  p.block_table = a.block_table;
+  p.bt_stride = a.bt_stride;
+  p.max_blocks = a.max_blocks;
+  p.num_blocks = a.num_blocks;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.G = a.G;
+  p.BS = a.BS;
+  p.scale = a.scale;
+  p.softcap = a.softcap;
+  p.alibi = a.alibi;
+  p.causal = a.causal;
+  p.wl = a.wl;
+  p.wr = a.wr;
+  p.min_rows = a.min_rows;
+  p.err = a.err;
+  const int BN = prefill_tc_block_keys(D);
+  int RB = 16;
+  while (RB * 2 <= BN && a.BS % (RB * 2) == 0) RB *= 2;
+  p.RB = RB;
+  p.kv_order_hnd = a.c_sh > a.c_sr ? 1 : 0;
+  CUtensorMap mk, mv;
+  if (!make_kv_map(&mk, a.kc, bf16, D, a.BS, a.Hkv, a.num_blocks, a.c_sb,
+                   a.c_sr, a.c_sh, RB, p.kv_order_hnd) ||
+      !make_kv_map(&mv, a.vc, bf16, D, a.BS, a.Hkv, a.num_blocks, a.c_sb,
+                   a.c_sr, a.c_sh, RB, p.kv_order_hnd))
+    return cudaErrorInvalidValue;
+  dim3 grid(a.batch * a.Hkv, grid_y);
+  static bool attr_set[2][3] = {};   // [bf16][D index]; idempotent if racing
+  const int di = D == 64 ? 0 : (D == 128 ? 1 : 2);
+  auto go = [&](void (*kern)(TcParams, CUtensorMap, CUtensorMap),
+                int smem) -> cudaError_t {
+    if (!attr_set[bf16][di]) {
+      cudaError_t e = cudaFuncSetAttribute(
+          kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+      attr_set[bf16][di] = true;
+    }
+    note_launch();
+    kern<<<grid, NUM_THREADS, smem, stream>>>(p, mk, mv);
+    return cudaGetLastError();
+  };
+  if (bf16) {
+    switch (D) {
+      case 64:  return go(prefill_tc_kernel<__nv_bfloat16, 64>, Cfg<64>::SMEM);
+      case 128: return go(prefill_tc_kernel<__nv_bfloat16, 128>, Cfg<128>::SMEM);
+      case 256: return go(prefill_tc_kernel<__nv_bfloat16, 256>, Cfg<256>::SMEM);
+    }
+  } else {
+    switch (D) {
+      case 64:  return go(prefill_tc_kernel<__half, 64>, Cfg<64>::SMEM);
+      case 128: return go(prefill_tc_kernel<__half, 128>, Cfg<128>::SMEM);
+      case 256: return go(prefill_tc_kernel<__half, 256>, Cfg<256>::SMEM);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pkv

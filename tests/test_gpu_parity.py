@@ -125,6 +125,38 @@ def test_feature_matrix(cuda_device, idx, dtype):
     assert_close(wl, out, lse, ref_out, ref_lse, "feature %d" % idx)
 
 
+PREFILL_CASES = [
+    # q_lens, seq_lens, Hq, Hkv, D, BS, kwargs  (all prefill-class)
+    ([40], [200], 4, 2, 128, 16, dict()),
+    ([70, 33], [300, 40], 8, 2, 64, 16, dict()),
+    ([50, 130], [333, 130], 4, 2, 256, 32, dict()),
+    ([60, 20], [90, 200], 4, 4, 128, 16, dict(causal=False)),
+    ([90, 300], [700, 900], 8, 2, 128, 64, dict(window_size=(100, 0),
+                                                softcap=20.0)),
+    ([33], [100], 4, 2, 128, 16, dict(alibi_slopes=[0.1, 0.2, 0.05, 0.3])),
+    ([64, 129], [64, 400], 8, 1, 128, 16, dict(dtype="f16")),
+    ([257, 17], [1000, 517], 16, 8, 128, 16, dict()),
+    ([20, 31], [2000, 31], 32, 8, 128, 16, dict(window_size=(7, 3))),
+]
+
+
+@pytest.mark.parametrize("kernel", ["tcgen05", "mma_sync"])
+@pytest.mark.parametrize("idx", range(len(PREFILL_CASES)))
+def test_prefill_kernels(cuda_device, idx, kernel):
+    q_lens, seq_lens, Hq, Hkv, D, BS, kw = PREFILL_CASES[idx]
+    wl = workloads.build_workload("pre%d" % idx, 900 + idx, q_lens, seq_lens,
+                                  Hq, Hkv, D, BS, **kw)
+    which = api.PREFILL_TCGEN05 if kernel == "tcgen05" else \
+        api.PREFILL_MMA_SYNC
+    api.set_prefill_kernel(which)
+    try:
+        _, out, lse = run_batch(wl, cuda_device)
+    finally:
+        api.set_prefill_kernel(api.PREFILL_TCGEN05)
+    ref_out, ref_lse = full_reference(wl)
+    assert_close(wl, out, lse, ref_out, ref_lse, "%s %d" % (kernel, idx))
+
+
 def test_rows_without_keys(cuda_device):
     """seqused_k below the query count: early rows see no key (out 0,
     lse -inf); a request with no keys at all likewise."""
