@@ -27,6 +27,22 @@
 
 #include "pkv_common.cuh"
 
+// Decode geometry per head size.  D = 128: 2 stages of 64 keys, so three
+// 100-KB-free CTAs (12 warps) share an SM; measured faster than 3 stages
+// with two CTAs on the batched and long decode workloads.
+#ifndef PKV_DECODE_STAGES_D128
+#define PKV_DECODE_STAGES_D128 2
+#endif
+#ifndef PKV_DECODE_D256_KWARPS
+#define PKV_DECODE_D256_KWARPS 2
+#endif
+#ifndef PKV_DECODE_D256_KT
+#define PKV_DECODE_D256_KT 32
+#endif
+#ifndef PKV_DECODE_D256_STAGES
+#define PKV_DECODE_D256_STAGES 2
+#endif
+
 namespace pkv {
 
 template <int D, int ROW_WARPS, int KEY_WARPS, int KT, int STAGES>
@@ -122,33 +138,56 @@ attn_mma_kernel(const AttnParams p) {
   }
 
   const int n_tiles = (hi - lo + KT - 1) / KT;
+  // Page ids travel through a small shared ring: the ids of tile t are
+  // fetched from the block table (global) one iteration before the tile's
+  // copies are issued, so table latency never sits in front of a copy.
+  constexpr int PPT = KT / 16 + 1;              // pages a tile can touch
+  constexpr int RING = STAGES + 1;
+  __shared__ int s_pg[RING][PPT];
+  const int bs_shift = p.bs_shift;
+  auto page_index = [&](int j) { return bs_shift >= 0 ? (j >> bs_shift)
+                                                       : j / p.BS; };
+  auto fetch_id = [&](int t) -> int {           // id of page `tid` of tile t
+    if (t >= n_tiles || tid >= PPT) return -1;
+    const int kt = lo + t * KT;
+    const int jb = page_index(kt) + tid;
+    if (jb * p.BS >= min(L_tab, kt + KT)) return -1;
+    const int blk = __ldg(bt + jb);
+    if (blk < 0 || blk >= p.num_blocks) {
+      atomicOr(p.err, kErrBadBlock);
+      return -1;
+    }
+    return blk;
+  };
   auto load_tile = [&](int it, int stage) {
     const int kt = lo + it * KT;
+    const int jb0 = page_index(kt);
+    const int* pg = s_pg[it % RING];
     const uint32_t sK = sKV_u + stage * C::STAGE_BYTES;
     const uint32_t sV = sK + C::TILE_BYTES;
+#pragma unroll 4
     for (int i = tid; i < KT * C::CPR; i += C::NT) {
       const int r = i / C::CPR, ch = i - (i / C::CPR) * C::CPR;
       const int j = kt + r;
-      bool ok = j < L_tab;
+      const int jb = page_index(j);
+      const int blk = j < L_tab ? pg[jb - jb0] : -1;
+      const bool ok = blk >= 0;
       int64_t off = 0;
-      if (ok) {
-        const int jb = j / p.BS;
-        const int blk = __ldg(bt + jb);
-        if (blk < 0 || blk >= p.num_blocks) {
-          ok = false;
-          atomicOr(p.err, kErrBadBlock);
-        } else {
-          off = static_cast<int64_t>(blk) * p.c_sb +
-                static_cast<int64_t>(j - jb * p.BS) * p.c_sr +
-                static_cast<int64_t>(g) * p.c_sh + ch * 8;
-        }
-      }
+      if (ok)
+        off = static_cast<int64_t>(blk) * p.c_sb +
+              static_cast<int64_t>(j - jb * p.BS) * p.c_sr +
+              static_cast<int64_t>(g) * p.c_sh + ch * 8;
       const uint32_t d = swz<C::ROW_BYTES>(r, ch);
       cp_async_16(sK + d, KC + off, ok ? 16 : 0);
       cp_async_16(sV + d, VC + off, ok ? 16 : 0);
     }
   };
 
+  for (int t = 0; t < STAGES; ++t) {
+    const int id = fetch_id(t);
+    if (tid < PPT) s_pg[t % RING][tid] = id;
+  }
+  __syncthreads();
 #pragma unroll
   for (int st = 0; st < STAGES - 1; ++st) {
     if (st < n_tiles) load_tile(st, st);
@@ -180,6 +219,7 @@ attn_mma_kernel(const AttnParams p) {
   const int lm_mi = lane >> 3, lm_r = lane & 7;
 
   for (int it = 0; it < n_tiles; ++it) {
+    const int next_id = fetch_id(it + STAGES);    // lands in the ring below
     cp_async_wait<STAGES - 2>();
     __syncthreads();
     {
@@ -290,6 +330,7 @@ attn_mma_kernel(const AttnParams p) {
         mma_16816<T>(o[2 * dp + 1], a, b2, b3);
       }
     }
+    if (tid < PPT) s_pg[(it + STAGES) % RING][tid] = next_id;
   }
   cp_async_wait<0>();
 
@@ -489,8 +530,10 @@ static cudaError_t decode_dispatch(const AttnParams& p, int D, dim3 grid,
                                    cudaStream_t s) {
   switch (D) {
     case 64:  return launch_cfg<T, 64, 1, 4, kDecodeKT, 4>(p, grid, s);
-    case 128: return launch_cfg<T, 128, 1, 4, kDecodeKT, 3>(p, grid, s);
-    case 256: return launch_cfg<T, 256, 1, 2, 32, 3>(p, grid, s);
+    case 128: return launch_cfg<T, 128, 1, 4, kDecodeKT, PKV_DECODE_STAGES_D128>(p, grid, s);
+    case 256: return launch_cfg<T, 256, 1, PKV_DECODE_D256_KWARPS,
+                                PKV_DECODE_D256_KT, PKV_DECODE_D256_STAGES>(
+        p, grid, s);
     default:  return cudaErrorInvalidValue;
   }
 }

@@ -355,6 +355,10 @@ pkv_status pkv_paged_attention_varlen(
   p.Hkv = num_kv_heads;
   p.G = num_heads / num_kv_heads;
   p.BS = block_size;
+  p.bs_shift = -1;
+  if ((block_size & (block_size - 1)) == 0)
+    for (int sh = 0; sh < 31; ++sh)
+      if ((1 << sh) == block_size) p.bs_shift = sh;
   p.scale = softmax_scale;
   p.softcap = softcap;
   p.alibi = alibi_slopes;

@@ -172,6 +172,7 @@ struct AttnParams {
   int max_blocks;
   int64_t num_blocks;
   int Hq, Hkv, G, BS;
+  int bs_shift;               // log2(BS) when BS is a power of two, else -1
   float scale;                // softmax scale (natural units)
   float softcap;              // 0 = none
   const float* alibi;         // [Hq] or null

@@ -69,7 +69,7 @@ struct Cfg {
   static constexpr int OFF_K = OFF_Q + Q_BYTES;
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
   static constexpr int OFF_P = OFF_V + STAGES * KV_BYTES;
-  static constexpr int OFF_BAR = OFF_P + P_BYTES;
+  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;   // P double buffer
   static constexpr int BAR_BYTES = 256;
   // keep one CTA per SM (the CTA takes all 512 TMEM columns)
   static constexpr int SMEM_USED = OFF_BAR + BAR_BYTES + 1024;
@@ -94,6 +94,7 @@ struct TcParams {
   const float* alibi;
   int causal, wl, wr;
   int min_rows;
+  int batch;
   int kv_order_hnd;   // tensor-map dim order: 1 = (D, BS, Hkv, NB)
   unsigned* err;
 };
@@ -278,6 +279,30 @@ __device__ __forceinline__ uint32_t sw128(int r, int c) {
 
 // ------------------------------------------------------------------ kernel
 
+// Final logit (log2 units) of one score, with soft-cap, ALiBi and the
+// admissibility mask of query position `pos` (general, per-element path).
+// Hardware tanh (MUFU.TANH); its relative error (about 2^-11) keeps soft-
+// capped logits well inside the output tolerance.
+__device__ __forceinline__ float tanh_fast(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float masked_logit(float s, int key, int pos,
+                                              bool valid, int kmin, int kmax,
+                                              const TcParams& p, float slope) {
+  float x = s * p.scale;
+  if (p.softcap > 0.f) x = p.softcap * tanh_fast(x / p.softcap);
+  if (p.alibi) x -= slope * fabsf(float(pos - key));
+  x *= kLog2e;
+  bool adm = valid && key >= kmin && key < kmax;
+  if (p.causal) adm = adm && key <= pos;
+  if (p.wl >= 0) adm = adm && key >= pos - p.wl;
+  if (p.wr >= 0) adm = adm && key <= pos + p.wr;
+  return adm ? x : -INFINITY;
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
@@ -290,16 +315,48 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
   unsigned char* base = smem_raw + (base_u - raw_u);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = blockIdx.x / p.Hkv;
-  const int g = blockIdx.x - b * p.Hkv;
   const int G = p.G;
-  const int q0 = p.cu_q[b];
-  const int q_len = min(p.cu_q[b + 1] - q0, p.total_q - q0);
-  if (q0 < 0 || q_len <= 0) return;
+  // Compact grid: blockIdx.x = tile_index * Hkv + g, tiles of all
+  // prefill-class requests in batch order, each request's last (longest)
+  // row tile first.  Each warp scans 32 requests per step (one round trip
+  // to the cu_seqlens_q cache lines per 32 requests).
+  const int g = blockIdx.x % p.Hkv;
+  const int t_lin = blockIdx.x / p.Hkv;
+  int b = -1, tile = 0, q0 = 0, q_len = 0;
+  {
+    int acc = 0;
+    for (int base_b = 0; base_b < p.batch && b < 0; base_b += 32) {
+      const int bb = base_b + lane;
+      int s0 = 0, ql = 0, nt = 0;
+      if (bb < p.batch) {
+        s0 = p.cu_q[bb];
+        ql = min(p.cu_q[bb + 1] - s0, p.total_q - s0);
+        const int rb = (s0 >= 0 && ql > 0) ? ql * G : 0;
+        nt = rb >= p.min_rows ? (rb + BM - 1) / BM : 0;
+      }
+      int incl = nt;                         // inclusive prefix over lanes
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const bool hit = t_lin >= acc + incl - nt && t_lin < acc + incl;
+      const unsigned m = __ballot_sync(0xffffffffu, hit);
+      if (m) {
+        const int src = __ffs(m) - 1;
+        b = base_b + src;
+        const int excl = __shfl_sync(0xffffffffu, incl - nt, src);
+        const int ntb = __shfl_sync(0xffffffffu, nt, src);
+        q0 = __shfl_sync(0xffffffffu, s0, src);
+        q_len = __shfl_sync(0xffffffffu, ql, src);
+        tile = ntb - 1 - (t_lin - acc - excl);
+      }
+      acc += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
+  if (b < 0) return;
   const int rows = q_len * G;
-  if (rows < p.min_rows) return;
-  const int row0 = (gridDim.y - 1 - blockIdx.y) * BM;
-  if (row0 >= rows) return;
+  const int row0 = tile * BM;
   const int row_end = min(rows, row0 + BM);
   const int L = p.seqused_k[b];
   const int L_tab = min(L, p.max_blocks * p.BS);
@@ -311,6 +368,14 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
   const int kstart = (kmin / RB) * RB;
   const int n_tiles = kmax > kmin ? (kmax - kstart + BN - 1) / BN : 0;
   const int ctx = L - q_len;
+  // Keys every valid row of this CTA admits: tiles inside [full_lo,
+  // full_hi) need no per-element mask.
+  const int p_lo = ctx + row0 / G, p_hi = ctx + (row_end - 1) / G;
+  int full_lo = kmin, full_hi = kmax;
+  if (p.wl >= 0) full_lo = max(full_lo, p_hi - p.wl);
+  if (p.causal) full_hi = min(full_hi, p_lo + 1);
+  if (p.wr >= 0) full_hi = min(full_hi, p_lo + p.wr + 1);
+  const bool plain = p.softcap <= 0.f && p.alibi == nullptr;
   T* __restrict__ OUT = static_cast<T*>(p.out);
 
   if (n_tiles == 0) {
@@ -332,20 +397,19 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
   const uint32_t sV = base_u + C::OFF_V;
   const uint32_t sP = base_u + C::OFF_P;
   const uint32_t bar0 = base_u + C::OFF_BAR;
-  // barrier addresses
   auto k_full = [&](int s) { return bar0 + 8 * (0 + s); };
   auto v_full = [&](int s) { return bar0 + 8 * (2 + s); };
   auto k_empty = [&](int s) { return bar0 + 8 * (4 + s); };
   auto v_empty = [&](int s) { return bar0 + 8 * (6 + s); };
   auto s_full = [&](int s) { return bar0 + 8 * (8 + s); };
   auto s_free = [&](int s) { return bar0 + 8 * (10 + s); };
-  const uint32_t p_full = bar0 + 8 * 12;
-  const uint32_t pv_done = bar0 + 8 * 13;
-  const uint32_t final_bar = bar0 + 8 * 14;
+  auto p_full = [&](int s) { return bar0 + 8 * (12 + s); };
+  auto pv_done = [&](int s) { return bar0 + 8 * (14 + s); };
+  const uint32_t final_bar = bar0 + 8 * 16;
   uint32_t* tmem_slot =
-      reinterpret_cast<uint32_t*>(base + C::OFF_BAR + 8 * 16);
+      reinterpret_cast<uint32_t*>(base + C::OFF_BAR + 8 * 18);
   volatile int* abort_flag =
-      reinterpret_cast<volatile int*>(base + C::OFF_BAR + 8 * 16 + 4);
+      reinterpret_cast<volatile int*>(base + C::OFF_BAR + 8 * 18 + 4);
 
   if (tid == 0) {
     for (int s = 0; s < 2; ++s) {
@@ -355,9 +419,9 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
       mbar_init(v_empty(s), 1);
       mbar_init(s_full(s), 1);
       mbar_init(s_free(s), 128);
+      mbar_init(p_full(s), 128);
+      mbar_init(pv_done(s), 1);
     }
-    mbar_init(p_full, 128);
-    mbar_init(pv_done, 1);
     mbar_init(final_bar, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -397,50 +461,70 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
 
   if (warp == LOAD_WARP) {
     // ---------------------------------------------------------- producer
+    // Lane i fetches the page id of box i of the next tile while lane 0
+    // issues the TMA boxes of the current one, so block-table latency is
+    // off the critical path.
+    constexpr int MAXBOX = BN / 16;
+    const int32_t* bt = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
+    auto fetch = [&](int j) -> int {
+      const int k0 = kstart + j * BN + lane * RB;
+      if (j >= n_tiles || lane >= BN / RB || k0 >= kmax) return 0;
+      const int blk = __ldg(bt + k0 / p.BS);
+      if (blk < 0 || blk >= p.num_blocks) {
+        atomicOr(p.err, kErrBadBlock);
+        return 0;
+      }
+      return blk;
+    };
     int k_iss = 0, v_iss = 0;
-    if (lane == 0) {
-      const int32_t* bt = p.block_table + b * p.bt_stride;
-      for (int j = 0; j < n_tiles; ++j) {
+    int cur = fetch(0);
+    for (int j = 0; j < n_tiles; ++j) {
+      const int nxt = fetch(j + 1);
+      int ids[MAXBOX];
+#pragma unroll
+      for (int i = 0; i < MAXBOX; ++i) ids[i] = __shfl_sync(0xffffffffu, cur, i);
+      int stop = 0;
+      if (lane == 0) {
         const int s = j & 1;
         const uint32_t ph = (j >> 1) & 1;
         const int kt = kstart + j * BN;
         int nbox = (kmax - kt + RB - 1) / RB;
         if (nbox > BN / RB) nbox = BN / RB;
         const uint32_t bytes = nbox * C::NCB * RB * 128;
-        bool stop = false;
         for (int mat = 0; mat < 2; ++mat) {
           const uint32_t empty = mat ? v_empty(s) : k_empty(s);
           const uint32_t full = mat ? v_full(s) : k_full(s);
           if (j >= 2 && !mbar_wait(empty, ph ^ 1, abort_flag, p.err)) {
-            stop = true;
+            stop = 1;
             break;
           }
           mbar_expect_tx(full, bytes);
           const void* tm = mat ? static_cast<const void*>(&tm_v)
                                : static_cast<const void*>(&tm_k);
           const uint32_t dst0 = (mat ? sV : sK) + s * C::KV_BYTES;
-          for (int i = 0; i < nbox; ++i) {
+#pragma unroll
+          for (int i = 0; i < MAXBOX; ++i) {
+            if (i >= nbox) break;
             const int k0 = kt + i * RB;
-            const int jb = k0 / p.BS;
-            int blk = __ldg(bt + jb);
-            if (blk < 0 || blk >= p.num_blocks) {
-              atomicOr(p.err, kErrBadBlock);
-              blk = 0;
-            }
-            const int row = k0 - jb * p.BS;
+            const int row = k0 % p.BS;
             for (int cb = 0; cb < C::NCB; ++cb) {
               const uint32_t dst = dst0 + cb * (BN * 128) + i * RB * 128;
               if (p.kv_order_hnd)
-                tma_load_4d(dst, tm, cb * 64, row, g, blk, full);
+                tma_load_4d(dst, tm, cb * 64, row, g, ids[i], full);
               else
-                tma_load_4d(dst, tm, cb * 64, g, row, blk, full);
+                tma_load_4d(dst, tm, cb * 64, g, row, ids[i], full);
             }
           }
           if (mat) v_iss = j + 1; else k_iss = j + 1;
         }
-        if (stop || *abort_flag) break;
+        if (*abort_flag) stop = 1;
       }
-      // drain: the last copies of each stage must land before the CTA exits
+      stop = __shfl_sync(0xffffffffu, stop, 0);
+      if (stop) break;
+      cur = nxt;
+    }
+    // drain: the last copies of each stage must land before the CTA exits
+    if (lane == 0) {
       for (int t = max(0, k_iss - 2); t < k_iss; ++t)
         mbar_drain(k_full(t & 1), (t >> 1) & 1);
       for (int t = max(0, v_iss - 2); t < v_iss; ++t)
@@ -454,14 +538,14 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
     bool ok = true;
     auto do_pv = [&](int i) -> bool {
       const int s = i & 1;
-      if (!mbar_wait(p_full, i & 1, abort_flag, p.err)) return false;
+      if (!mbar_wait(p_full(s), (i >> 1) & 1, abort_flag, p.err)) return false;
       if (!mbar_wait(v_full(s), (i >> 1) & 1, abort_flag, p.err)) return false;
       // zero V rows that hold no key of this request (beyond seqused_k, or
       // pages that were not loaded), so 0 * garbage never reaches O
       const int kt = kstart + i * BN;
       int nbox = (kmax - kt + RB - 1) / RB;
       if (nbox > BN / RB) nbox = BN / RB;
-      int r0 = min(nbox * RB, max(L - kt, 0));
+      const int r0 = min(nbox * RB, max(L - kt, 0));
       if (r0 < BN) {
         const uint32_t v0 = sV + s * C::KV_BYTES;
         for (int idx = lane; idx < (BN - r0) * 8 * C::NCB; idx += 32) {
@@ -479,14 +563,15 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
       tc_fence_after();
       if (lane == 0) {
         const uint32_t v0 = sV + s * C::KV_BYTES;
+        const uint32_t p0 = sP + s * C::P_BYTES;
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k) {
-          const uint64_t a = sdesc(sP + (k >> 2) * (BM * 128) + (k & 3) * 32,
+          const uint64_t a = sdesc(p0 + (k >> 2) * (BM * 128) + (k & 3) * 32,
                                    16, 1024);
           const uint64_t bdesc = sdesc(v0 + k * 16 * 128, BN * 128, 1024);
           mma_f16(tmem + C::O_COL, a, bdesc, ID_PV, (i > 0 || k > 0) ? 1 : 0);
         }
-        mma_commit(pv_done);
+        mma_commit(pv_done(s));
         mma_commit(v_empty(s));
       }
       __syncwarp();
@@ -533,8 +618,9 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
     const int pos = ctx + (valid ? R / G : 0);
     const int h = g * G + (valid ? R % G : 0);
     const float slope = (p.alibi && valid) ? p.alibi[h] : 0.f;
-    const bool plain = p.softcap <= 0.f && p.alibi == nullptr;
     const float scale_log2 = p.scale * kLog2e;
+    const float scale_over_cap = p.softcap > 0.f ? p.scale / p.softcap : 0.f;
+    const float cap_log2e = p.softcap * kLog2e;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
@@ -545,36 +631,41 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
         break;
       }
       tc_fence_after();
-      float sv[BN];
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c)
-        tmem_ld32(tmem + lane_base + C::S_COL + sb * BN + c * 32, sv + c * 32);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(s_free(sb));
-
       const int kt = kstart + j * BN;
-      float mx = -INFINITY;
+      const bool unmasked = kt >= full_lo && kt + BN <= full_hi;
+      const bool fast = plain && unmasked;
+      // soft-cap without ALiBi on an unmasked tile: no per-key mask
+      const bool fast_cap = !plain && p.alibi == nullptr && unmasked;
+      const uint32_t s_addr = tmem + lane_base + C::S_COL + sb * BN;
+      // pass 1: row max (log2 units); 8 independent partial maxima keep
+      // the dependent chain short
+      float mx8[8];
 #pragma unroll
-      for (int k = 0; k < BN; ++k) {
-        const int key = kt + k;
-        float x = sv[k];
-        if (plain) {
-          x *= scale_log2;
+      for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        float v[32];
+        tmem_ld32(s_addr + c * 32, v);
+        tmem_wait_ld();
+        if (fast) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            mx8[e & 7] = fmaxf(mx8[e & 7], v[e] * scale_log2);
+        } else if (fast_cap) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            mx8[e & 7] = fmaxf(mx8[e & 7],
+                               cap_log2e * tanh_fast(v[e] * scale_over_cap));
         } else {
-          x *= p.scale;
-          if (p.softcap > 0.f) x = p.softcap * tanhf(x / p.softcap);
-          if (p.alibi) x -= slope * fabsf(float(pos - key));
-          x *= kLog2e;
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            mx8[e & 7] = fmaxf(mx8[e & 7],
+                               masked_logit(v[e], kt + c * 32 + e, pos, valid,
+                                            kmin, kmax, p, slope));
         }
-        bool adm = valid && key >= kmin && key < kmax;
-        if (p.causal) adm = adm && key <= pos;
-        if (p.wl >= 0) adm = adm && key >= pos - p.wl;
-        if (p.wr >= 0) adm = adm && key <= pos + p.wr;
-        x = adm ? x : -INFINITY;
-        sv[k] = x;
-        mx = fmaxf(mx, x);
       }
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const bool grow = mx > m_ref + kRescaleThreshold;
       float alpha = 1.f;
       if (grow) {
@@ -583,20 +674,14 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
         l *= alpha;
       }
       const float base_m = (m_ref == -INFINITY) ? 0.f : m_ref;
-      float sum = 0.f;
-#pragma unroll
-      for (int k = 0; k < BN; ++k) {
-        sv[k] = ex2(sv[k] - base_m);
-        sum += sv[k];
-      }
-      l += sum;
-      // PV_{j-1} must be done before O is rescaled or P is overwritten
-      if (j >= 1 && !mbar_wait(pv_done, (j - 1) & 1, abort_flag, p.err)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
+      // O holds PV_0..PV_{j-1}: rescale it once PV_{j-1} is done
       if (j >= 1 && __any_sync(0xffffffffu, grow)) {
+        const int pb = (j - 1) & 1;
+        if (!mbar_wait(pv_done(pb), ((j - 1) >> 1) & 1, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           float ov[32];
@@ -609,25 +694,60 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
         }
         tmem_wait_st();
       }
-      // P row -> shared memory (K-major, 128-byte swizzle)
+      // P buffer j&1 was last read by PV_{j-2}
+      if (j >= 2 &&
+          !mbar_wait(pv_done(sb), ((j - 2) >> 1) & 1, abort_flag, p.err)) {
+        ok = false;
+        break;
+      }
+      // pass 2: P = exp2(logit - m) -> shared memory (K-major, swizzled)
+      const uint32_t p_row = sP + sb * C::P_BYTES;
+      float sum8[8];
 #pragma unroll
-      for (int cb = 0; cb < C::PCB; ++cb) {
+      for (int e = 0; e < 8; ++e) sum8[e] = 0.f;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        float v[32];
+        tmem_ld32(s_addr + c * 32, v);
+        tmem_wait_ld();
+        if (fast) {
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const float* e = sv + cb * 64 + c * 8;
-          const uint32_t a0 = pack2<T>(e[0], e[1]), a1 = pack2<T>(e[2], e[3]);
-          const uint32_t a2 = pack2<T>(e[4], e[5]), a3 = pack2<T>(e[6], e[7]);
+          for (int e = 0; e < 32; ++e)
+            v[e] = ex2(fmaf(v[e], scale_log2, -base_m));
+        } else if (fast_cap) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            v[e] = ex2(fmaf(cap_log2e, tanh_fast(v[e] * scale_over_cap),
+                            -base_m));
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            v[e] = ex2(masked_logit(v[e], kt + c * 32 + e, pos, valid, kmin,
+                                    kmax, p, slope) - base_m);
+        }
+#pragma unroll
+        for (int e = 0; e < 32; ++e) sum8[e & 7] += v[e];
+        const int cb = (c * 32) >> 6, ch0 = ((c * 32) & 63) >> 3;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float* e = v + q * 8;
           asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
-                           sP + cb * (BM * 128) + sw128(r, c)),
-                       "r"(a0), "r"(a1), "r"(a2), "r"(a3)
+                           p_row + cb * (BM * 128) + sw128(r, ch0 + q)),
+                       "r"(pack2<T>(e[0], e[1])), "r"(pack2<T>(e[2], e[3])),
+                       "r"(pack2<T>(e[4], e[5])), "r"(pack2<T>(e[6], e[7]))
                        : "memory");
         }
       }
-      fence_proxy_async();
+      l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
+           ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(s_free(sb));
+      fence_proxy_async();
+      mbar_arrive(p_full(sb));
     }
-    if (ok && mbar_wait(pv_done, (n_tiles - 1) & 1, abort_flag, p.err)) {
+    const int lb = (n_tiles - 1) & 1;
+    if (ok &&
+        mbar_wait(pv_done(lb), ((n_tiles - 1) >> 1) & 1, abort_flag, p.err)) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const int tok = q0 + (valid ? R / G : 0);
@@ -748,6 +868,7 @@ cudaError_t launch_prefill_attn_tc(const AttnParams& a, int D, bool bf16,
   p.wl = a.wl;
   p.wr = a.wr;
   p.min_rows = a.min_rows;
+  p.batch = a.batch;
   p.err = a.err;
   const int BN = prefill_tc_block_keys(D);
   int RB = 16;
@@ -760,7 +881,14 @@ cudaError_t launch_prefill_attn_tc(const AttnParams& a, int D, bool bf16,
       !make_kv_map(&mv, a.vc, bf16, D, a.BS, a.Hkv, a.num_blocks, a.c_sb,
                    a.c_sr, a.c_sh, RB, p.kv_order_hnd))
     return cudaErrorInvalidValue;
-  dim3 grid(a.batch * a.Hkv, grid_y);
+  // compact 1-D grid: an upper bound on the row tiles of all requests,
+  // sum_b ceil(q_b * G / 128) <= ceil(total_q * G / 128) + batch
+  (void)grid_y;
+  const int64_t tiles =
+      (static_cast<int64_t>(a.total_q) * a.G + BM - 1) / BM + a.batch;
+  const int64_t gx = tiles * a.Hkv;
+  if (gx <= 0 || gx > 0x7fffffff) return cudaErrorInvalidValue;
+  dim3 grid(static_cast<unsigned>(gx));
   static bool attr_set[2][3] = {};   // [bf16][D index]; idempotent if racing
   const int di = D == 64 ? 0 : (D == 128 ? 1 : 2);
   auto go = [&](void (*kern)(TcParams, CUtensorMap, CUtensorMap),
