@@ -52,28 +52,40 @@ constexpr uint32_t kSpinLimit = 1u << 28;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
 constexpr float kRescaleThreshold = 8.f;   // log2 units
 
+// Tile geometry per head size.  D <= 128: 64-key tiles, one P buffer and
+// 256 TMEM columns, so two CTAs share an SM (their prologues, epilogues and
+// softmax phases overlap).  D = 256: 64-key tiles, two P buffers, all 512
+// TMEM columns, one CTA per SM.
 template <int D>
 struct Cfg {
-  static constexpr int BN = (D <= 128) ? 128 : 64;   // keys per tile
+  static constexpr int BN = 64;                      // keys per tile
   static constexpr int NCB = D / 64;                 // 64-column blocks of D
   static constexpr int PCB = BN / 64;                // 64-column blocks of P
   static constexpr int Q_BYTES = BM * D * 2;
   static constexpr int KV_BYTES = BN * D * 2;        // one K or V tile
   static constexpr int P_BYTES = BM * BN * 2;
   static constexpr int STAGES = 2;
+  static constexpr int PBUF = D <= 128 ? 1 : 2;      // P buffers
   static constexpr int S_COL = 0;                    // S buffers at 0, BN
   static constexpr int O_COL = 2 * BN;
-  static constexpr int TMEM_COLS = 512;
-  static_assert(2 * BN + D <= TMEM_COLS, "TMEM budget");
+  static constexpr int TMEM_NEED = 2 * BN + D;
+  static constexpr int TMEM_COLS = TMEM_NEED <= 128 ? 128
+                                   : (TMEM_NEED <= 256 ? 256 : 512);
+  static_assert(TMEM_NEED <= TMEM_COLS, "TMEM budget");
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + Q_BYTES;
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
   static constexpr int OFF_P = OFF_V + STAGES * KV_BYTES;
-  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;   // P double buffer
-  static constexpr int BAR_BYTES = 256;
-  // keep one CTA per SM (the CTA takes all 512 TMEM columns)
-  static constexpr int SMEM_USED = OFF_BAR + BAR_BYTES + 1024;
-  static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
+  static constexpr int OFF_BAR = OFF_P + PBUF * P_BYTES;
+  static constexpr int BAR_BYTES = 192;
+  // The dynamic shared window starts 1024-byte aligned (checked at run
+  // time); a CTA that takes all 512 TMEM columns also takes enough shared
+  // memory that no second CTA fits beside it.
+  static constexpr int SMEM_USED = OFF_BAR + BAR_BYTES;
+  // no more CTAs per SM than TMEM can hold (512 columns per SM)
+  static constexpr int SMEM_FLOOR = TMEM_COLS == 512 ? 120 * 1024
+                                    : (TMEM_COLS == 256 ? 80 * 1024 : 0);
+  static constexpr int SMEM = SMEM_USED < SMEM_FLOOR ? SMEM_FLOOR : SMEM_USED;
 };
 
 struct TcParams {
@@ -304,15 +316,18 @@ __device__ __forceinline__ float masked_logit(float s, int key, int pos,
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(NUM_THREADS, 2)
 prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v) {
   using C = Cfg<D>;
   constexpr int BN = C::BN;
-  extern __shared__ unsigned char smem_raw[];
-  const uint32_t raw_u = smem_u32(smem_raw);
-  const uint32_t base_u = (raw_u + 1023u) & ~1023u;
-  unsigned char* base = smem_raw + (base_u - raw_u);
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t base_u = smem_u32(smem_raw);
+  unsigned char* base = smem_raw;
+  if (base_u & 1023u) {            // 128-byte swizzle atoms need 1 KB
+    if (threadIdx.x == 0) atomicOr(p.err, kErrTimeout);
+    return;
+  }
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = p.G;
@@ -538,7 +553,9 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
     bool ok = true;
     auto do_pv = [&](int i) -> bool {
       const int s = i & 1;
-      if (!mbar_wait(p_full(s), (i >> 1) & 1, abort_flag, p.err)) return false;
+      const int pb = i % C::PBUF;
+      if (!mbar_wait(p_full(pb), (i / C::PBUF) & 1, abort_flag, p.err))
+        return false;
       if (!mbar_wait(v_full(s), (i >> 1) & 1, abort_flag, p.err)) return false;
       // zero V rows that hold no key of this request (beyond seqused_k, or
       // pages that were not loaded), so 0 * garbage never reaches O
@@ -563,7 +580,7 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
       tc_fence_after();
       if (lane == 0) {
         const uint32_t v0 = sV + s * C::KV_BYTES;
-        const uint32_t p0 = sP + s * C::P_BYTES;
+        const uint32_t p0 = sP + pb * C::P_BYTES;
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k) {
           const uint64_t a = sdesc(p0 + (k >> 2) * (BM * 128) + (k & 3) * 32,
@@ -571,7 +588,7 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
           const uint64_t bdesc = sdesc(v0 + k * 16 * 128, BN * 128, 1024);
           mma_f16(tmem + C::O_COL, a, bdesc, ID_PV, (i > 0 || k > 0) ? 1 : 0);
         }
-        mma_commit(pv_done(s));
+        mma_commit(pv_done(pb));
         mma_commit(v_empty(s));
       }
       __syncwarp();
@@ -676,8 +693,9 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
       const float base_m = (m_ref == -INFINITY) ? 0.f : m_ref;
       // O holds PV_0..PV_{j-1}: rescale it once PV_{j-1} is done
       if (j >= 1 && __any_sync(0xffffffffu, grow)) {
-        const int pb = (j - 1) & 1;
-        if (!mbar_wait(pv_done(pb), ((j - 1) >> 1) & 1, abort_flag, p.err)) {
+        const int pb = (j - 1) % C::PBUF;
+        if (!mbar_wait(pv_done(pb), ((j - 1) / C::PBUF) & 1, abort_flag,
+                       p.err)) {
           ok = false;
           break;
         }
@@ -694,14 +712,16 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
         }
         tmem_wait_st();
       }
-      // P buffer j&1 was last read by PV_{j-2}
-      if (j >= 2 &&
-          !mbar_wait(pv_done(sb), ((j - 2) >> 1) & 1, abort_flag, p.err)) {
+      // P buffer j % PBUF was last read by PV_{j-PBUF}
+      const int pbj = j % C::PBUF;
+      if (j >= C::PBUF &&
+          !mbar_wait(pv_done(pbj), ((j - C::PBUF) / C::PBUF) & 1, abort_flag,
+                     p.err)) {
         ok = false;
         break;
       }
       // pass 2: P = exp2(logit - m) -> shared memory (K-major, swizzled)
-      const uint32_t p_row = sP + sb * C::P_BYTES;
+      const uint32_t p_row = sP + pbj * C::P_BYTES;
       float sum8[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) sum8[e] = 0.f;
@@ -743,11 +763,11 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
       tc_fence_before();
       mbar_arrive(s_free(sb));
       fence_proxy_async();
-      mbar_arrive(p_full(sb));
+      mbar_arrive(p_full(pbj));
     }
-    const int lb = (n_tiles - 1) & 1;
-    if (ok &&
-        mbar_wait(pv_done(lb), ((n_tiles - 1) >> 1) & 1, abort_flag, p.err)) {
+    const int lb = (n_tiles - 1) % C::PBUF;
+    if (ok && mbar_wait(pv_done(lb), ((n_tiles - 1) / C::PBUF) & 1,
+                        abort_flag, p.err)) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const int tok = q0 + (valid ? R / G : 0);
@@ -837,7 +857,7 @@ bool make_kv_map(CUtensorMap* map, const void* ptr, bool bf16, int D, int BS,
 
 }  // namespace tc
 
-int prefill_tc_block_keys(int D) { return D <= 128 ? 128 : 64; }
+int prefill_tc_block_keys(int) { return 64; }
 
 cudaError_t launch_prefill_attn_tc(const AttnParams& a, int D, bool bf16,
                                    int grid_y, cudaStream_t stream) {
