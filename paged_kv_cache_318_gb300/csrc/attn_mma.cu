@@ -209,6 +209,15 @@ attn_mma_kernel(const AttnParams p) {
   }
   const bool plain = (p.softcap <= 0.f) && (p.alibi == nullptr);
   const float scale_log2 = p.scale * kLog2e;
+  // keys every valid row of this CTA admits: tiles inside [full_lo,
+  // full_hi) skip the per-key mask (rows past row_end are never stored)
+  int full_lo = lo, full_hi = hi;
+  {
+    const int p_lo = ctx + row0 / G, p_hi = ctx + (row_end - 1) / G;
+    if (p.wl >= 0) full_lo = max(full_lo, p_hi - p.wl);
+    if (p.causal) full_hi = min(full_hi, p_lo + 1);
+    if (p.wr >= 0) full_hi = min(full_hi, p_lo + p.wr + 1);
+  }
 
   float o[D / 8][4];
 #pragma unroll
@@ -258,6 +267,17 @@ attn_mma_kernel(const AttnParams p) {
 
     // logits (base 2) with masks
     float mxA = -INFINITY, mxB = -INFINITY;
+    if (plain && kt >= full_lo && kt + KT <= full_hi) {
+#pragma unroll
+      for (int nt = 0; nt < C::NKT; ++nt) {
+        s[nt][0] *= scale_log2;
+        s[nt][1] *= scale_log2;
+        s[nt][2] *= scale_log2;
+        s[nt][3] *= scale_log2;
+        mxA = fmaxf(mxA, fmaxf(s[nt][0], s[nt][1]));
+        mxB = fmaxf(mxB, fmaxf(s[nt][2], s[nt][3]));
+      }
+    } else {
 #pragma unroll
     for (int nt = 0; nt < C::NKT; ++nt) {
 #pragma unroll
@@ -283,6 +303,7 @@ attn_mma_kernel(const AttnParams p) {
         if (rowB) mxB = fmaxf(mxB, x); else mxA = fmaxf(mxA, x);
       }
     }
+    }
     mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 1));
     mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 2));
     mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 1));
@@ -305,12 +326,15 @@ attn_mma_kernel(const AttnParams p) {
     }
     lA = lA * alA + sumA;
     lB = lB * alB + sumB;
+    // once the running maxima settle, alpha is exactly 1: skip the rescale
+    if (__any_sync(0xffffffffu, alA != 1.f || alB != 1.f)) {
 #pragma unroll
-    for (int i = 0; i < D / 8; ++i) {
-      o[i][0] *= alA;
-      o[i][1] *= alA;
-      o[i][2] *= alB;
-      o[i][3] *= alB;
+      for (int i = 0; i < D / 8; ++i) {
+        o[i][0] *= alA;
+        o[i][1] *= alA;
+        o[i][2] *= alB;
+        o[i][3] *= alB;
+      }
     }
     // O += P V
 #pragma unroll

@@ -58,7 +58,7 @@ constexpr float kRescaleThreshold = 8.f;   // log2 units
 // TMEM columns, one CTA per SM.
 template <int D>
 struct Cfg {
-  static constexpr int BN = 64;                      // keys per tile
+  static constexpr int BN = 64;   // keys per tile (one S row = 64 registers)
   static constexpr int NCB = D / 64;                 // 64-column blocks of D
   static constexpr int PCB = BN / 64;                // 64-column blocks of P
   static constexpr int Q_BYTES = BM * D * 2;
@@ -654,31 +654,32 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
       // soft-cap without ALiBi on an unmasked tile: no per-key mask
       const bool fast_cap = !plain && p.alibi == nullptr && unmasked;
       const uint32_t s_addr = tmem + lane_base + C::S_COL + sb * BN;
-      // pass 1: row max (log2 units); 8 independent partial maxima keep
-      // the dependent chain short
+      // the whole S row (BN = 64 fp32) in one load; S is free right after
+      float v[BN];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_addr + c * 32, v + c * 32);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(s_free(sb));
+      // logits in log2 units (the plain path folds the scale into exp2)
       float mx8[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        float v[32];
-        tmem_ld32(s_addr + c * 32, v);
-        tmem_wait_ld();
-        if (fast) {
+      if (fast) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            mx8[e & 7] = fmaxf(mx8[e & 7], v[e] * scale_log2);
-        } else if (fast_cap) {
+        for (int e = 0; e < BN; ++e)
+          mx8[e & 7] = fmaxf(mx8[e & 7], v[e] * scale_log2);
+      } else if (fast_cap) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            mx8[e & 7] = fmaxf(mx8[e & 7],
-                               cap_log2e * tanh_fast(v[e] * scale_over_cap));
-        } else {
+        for (int e = 0; e < BN; ++e) {
+          v[e] = cap_log2e * tanh_fast(v[e] * scale_over_cap);
+          mx8[e & 7] = fmaxf(mx8[e & 7], v[e]);
+        }
+      } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            mx8[e & 7] = fmaxf(mx8[e & 7],
-                               masked_logit(v[e], kt + c * 32 + e, pos, valid,
-                                            kmin, kmax, p, slope));
+        for (int e = 0; e < BN; ++e) {
+          v[e] = masked_logit(v[e], kt + e, pos, valid, kmin, kmax, p, slope);
+          mx8[e & 7] = fmaxf(mx8[e & 7], v[e]);
         }
       }
       const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
@@ -712,6 +713,23 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
         }
         tmem_wait_st();
       }
+      // P = exp2(logit - m)
+      float sum8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sum8[e] = 0.f;
+      if (fast) {
+#pragma unroll
+        for (int e = 0; e < BN; ++e) {
+          v[e] = ex2(fmaf(v[e], scale_log2, -base_m));
+          sum8[e & 7] += v[e];
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < BN; ++e) {
+          v[e] = ex2(v[e] - base_m);
+          sum8[e & 7] += v[e];
+        }
+      }
       // P buffer j % PBUF was last read by PV_{j-PBUF}
       const int pbj = j % C::PBUF;
       if (j >= C::PBUF &&
@@ -720,48 +738,20 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
         ok = false;
         break;
       }
-      // pass 2: P = exp2(logit - m) -> shared memory (K-major, swizzled)
+      // P row -> shared memory (K-major, 128-byte swizzle)
       const uint32_t p_row = sP + pbj * C::P_BYTES;
-      float sum8[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) sum8[e] = 0.f;
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        float v[32];
-        tmem_ld32(s_addr + c * 32, v);
-        tmem_wait_ld();
-        if (fast) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            v[e] = ex2(fmaf(v[e], scale_log2, -base_m));
-        } else if (fast_cap) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            v[e] = ex2(fmaf(cap_log2e, tanh_fast(v[e] * scale_over_cap),
-                            -base_m));
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            v[e] = ex2(masked_logit(v[e], kt + c * 32 + e, pos, valid, kmin,
-                                    kmax, p, slope) - base_m);
-        }
-#pragma unroll
-        for (int e = 0; e < 32; ++e) sum8[e & 7] += v[e];
-        const int cb = (c * 32) >> 6, ch0 = ((c * 32) & 63) >> 3;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float* e = v + q * 8;
-          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
-                           p_row + cb * (BM * 128) + sw128(r, ch0 + q)),
-                       "r"(pack2<T>(e[0], e[1])), "r"(pack2<T>(e[2], e[3])),
-                       "r"(pack2<T>(e[4], e[5])), "r"(pack2<T>(e[6], e[7]))
-                       : "memory");
-        }
+      for (int q = 0; q < BN / 8; ++q) {
+        const float* e = v + q * 8;
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                         p_row + (q >> 3) * (BM * 128) + sw128(r, q & 7)),
+                     "r"(pack2<T>(e[0], e[1])), "r"(pack2<T>(e[2], e[3])),
+                     "r"(pack2<T>(e[4], e[5])), "r"(pack2<T>(e[6], e[7]))
+                     : "memory");
       }
       l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
            ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
       tc_fence_before();
-      mbar_arrive(s_free(sb));
       fence_proxy_async();
       mbar_arrive(p_full(pbj));
     }
