@@ -233,6 +233,28 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
       : "memory");
 }
 
+// Warp-collective forms: every lane of the warp executes them with the same
+// (warp-uniform) operands and one lane, chosen by elect.sync, issues.  This
+// keeps the descriptors in uniform registers.
+__device__ __forceinline__ void mma_f16_warp(uint32_t d_tmem, uint64_t a,
+                                             uint64_t b, uint32_t id,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p, e;\nsetp.ne.b32 p, %4, 0;\n"
+      "elect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+          d_tmem),
+      "l"(a), "l"(b), "r"(id), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_warp(uint32_t bar) {
+  asm volatile(
+      "{\n.reg .pred e;\nelect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster."
+      "b64 [%0];\n}\n" ::"r"(bar)
+      : "memory");
+}
+
 // 32 lanes x 32 columns of fp32 from TMEM.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   uint32_t r[32];
@@ -797,6 +819,549 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
   }
 }
 
+// ------------------------------------------------ two-tile (ping-pong) kernel
+//
+// For D <= 128 one CTA owns 256 packed rows as two 128-row Q tiles, A and B,
+// that share every K/V tile.  Each Q tile has its own softmax warpgroup
+// (warps 0-3 for A, 4-7 for B), two S buffers in TMEM, two P buffers in
+// shared memory and its own O accumulator in TMEM, so a warpgroup never
+// waits on the MMA of the tile it just finished, and the tensor core always
+// has the other tile's work queued.  Warp 8 issues the MMAs; warps 9 and 10
+// issue the TMA loads of K and V tiles (one lane per page box).
+
+constexpr int PP_THREADS = 352;
+constexpr int PP_MMA_WARP = 8;
+constexpr int PP_LOAD_WARP = 9;    // warps 9 (K) and 10 (V)
+constexpr int PP_ROWS = 2 * BM;
+
+template <int D>
+struct PPCfg {
+  static constexpr int BN = 64;
+  static constexpr int NCB = D / 64;
+  static constexpr int Q_BYTES = BM * D * 2;          // one Q tile
+  static constexpr int KV_BYTES = BN * D * 2;
+  static constexpr int P_BYTES = BM * BN * 2;
+  static constexpr int STAGES = 2;
+  static constexpr int O_COL = 4 * BN;                // S[x][buf] below
+  static constexpr int TMEM_COLS = 512;
+  static_assert(4 * BN + 2 * D <= TMEM_COLS, "TMEM budget");
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
+  static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
+  static constexpr int OFF_P = OFF_V + STAGES * KV_BYTES;   // P[x][buf]
+  static constexpr int OFF_BAR = OFF_P + 4 * P_BYTES;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int SMEM = OFF_BAR + BAR_BYTES;
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(PP_THREADS, 1)
+prefill_pp_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v) {
+  using C = PPCfg<D>;
+  constexpr int BN = C::BN;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t base_u = smem_u32(smem_raw);
+  unsigned char* base = smem_raw;
+  if (base_u & 1023u) {
+    if (threadIdx.x == 0) atomicOr(p.err, kErrTimeout);
+    return;
+  }
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = p.G;
+
+  // ---- work item: (request, 256-row pair tile, KV head)
+  const int g = blockIdx.x % p.Hkv;
+  const int t_lin = blockIdx.x / p.Hkv;
+  int b = -1, tile = 0, q0 = 0, q_len = 0;
+  {
+    int acc = 0;
+    for (int base_b = 0; base_b < p.batch && b < 0; base_b += 32) {
+      const int bb = base_b + lane;
+      int s0 = 0, ql = 0, nt = 0;
+      if (bb < p.batch) {
+        s0 = p.cu_q[bb];
+        ql = min(p.cu_q[bb + 1] - s0, p.total_q - s0);
+        const int rb = (s0 >= 0 && ql > 0) ? ql * G : 0;
+        nt = rb >= p.min_rows ? (rb + PP_ROWS - 1) / PP_ROWS : 0;
+      }
+      int incl = nt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const bool hit = t_lin >= acc + incl - nt && t_lin < acc + incl;
+      const unsigned m = __ballot_sync(0xffffffffu, hit);
+      if (m) {
+        const int src = __ffs(m) - 1;
+        b = base_b + src;
+        const int excl = __shfl_sync(0xffffffffu, incl - nt, src);
+        const int ntb = __shfl_sync(0xffffffffu, nt, src);
+        q0 = __shfl_sync(0xffffffffu, s0, src);
+        q_len = __shfl_sync(0xffffffffu, ql, src);
+        tile = ntb - 1 - (t_lin - acc - excl);
+      }
+      acc += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
+  if (b < 0) return;
+  const int rows = q_len * G;
+  const int L = p.seqused_k[b];
+  const int L_tab = min(L, p.max_blocks * p.BS);
+  const int ctx = L - q_len;
+  const int RB = p.RB;
+  // per Q tile x: rows [rx0, rx_end), keys [kmn[x], kmx[x])
+  int rx0[2], rx_end[2], kmn[2], kmx[2];
+  bool has[2];
+  int kmin_u = 0x7fffffff, kmax_u = 0;
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    rx0[x] = tile * PP_ROWS + x * BM;
+    rx_end[x] = min(rows, rx0[x] + BM);
+    has[x] = rx_end[x] > rx0[x];
+    kmn[x] = 0;
+    kmx[x] = 0;
+    if (has[x]) {
+      key_range(L, q_len, rx0[x] / G, (rx_end[x] - 1) / G, p.causal, p.wl,
+                p.wr, kmn[x], kmx[x]);
+      kmx[x] = min(kmx[x], L_tab);
+      if (kmx[x] > kmn[x]) {
+        kmin_u = min(kmin_u, kmn[x]);
+        kmax_u = max(kmax_u, kmx[x]);
+      }
+    }
+  }
+  const int kstart = kmax_u > 0 ? (kmin_u / RB) * RB : 0;
+  const int n_tiles = kmax_u > 0 ? (kmax_u - kstart + BN - 1) / BN : 0;
+  // tile ranges [tlo[x], tlo[x] + nx[x]) of each Q tile in the union
+  int tlo[2], nx[2];
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    if (has[x] && kmx[x] > kmn[x]) {
+      tlo[x] = (kmn[x] - kstart) / BN;
+      nx[x] = (kmx[x] - kstart + BN - 1) / BN - tlo[x];
+    } else {
+      tlo[x] = 0;
+      nx[x] = 0;
+    }
+  }
+  T* __restrict__ OUT = static_cast<T*>(p.out);
+  const bool plain = p.softcap <= 0.f && p.alibi == nullptr;
+
+  const uint32_t sQ = base_u + C::OFF_Q;
+  const uint32_t sK = base_u + C::OFF_K;
+  const uint32_t sV = base_u + C::OFF_V;
+  const uint32_t sP = base_u + C::OFF_P;
+  const uint32_t bar0 = base_u + C::OFF_BAR;
+  auto k_full = [&](int s) { return bar0 + 8 * (0 + s); };
+  auto v_full = [&](int s) { return bar0 + 8 * (2 + s); };
+  auto k_empty = [&](int s) { return bar0 + 8 * (4 + s); };
+  auto v_empty = [&](int s) { return bar0 + 8 * (6 + s); };
+  auto s_full = [&](int x, int s) { return bar0 + 8 * (8 + 2 * x + s); };
+  auto s_free = [&](int x, int s) { return bar0 + 8 * (12 + 2 * x + s); };
+  auto p_full = [&](int x, int s) { return bar0 + 8 * (16 + 2 * x + s); };
+  auto pv_done = [&](int x, int s) { return bar0 + 8 * (20 + 2 * x + s); };
+  const uint32_t final_bar = bar0 + 8 * 24;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + C::OFF_BAR + 8 * 26);
+  volatile int* abort_flag =
+      reinterpret_cast<volatile int*>(base + C::OFF_BAR + 8 * 26 + 4);
+
+  if (n_tiles > 0) {
+    if (tid == 0) {
+      for (int s = 0; s < 2; ++s) {
+        mbar_init(k_full(s), 1);
+        mbar_init(v_full(s), 1);
+        mbar_init(k_empty(s), 1);
+        mbar_init(v_empty(s), 1);
+        for (int x = 0; x < 2; ++x) {
+          mbar_init(s_full(x, s), 1);
+          mbar_init(s_free(x, s), 128);
+          mbar_init(p_full(x, s), 128);
+          mbar_init(pv_done(x, s), 1);
+        }
+      }
+      mbar_init(final_bar, 1);
+      *abort_flag = 0;
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == PP_MMA_WARP) {
+      asm volatile(
+          "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], "
+          "%1;" ::"r"(smem_u32(tmem_slot)),
+          "r"(C::TMEM_COLS)
+          : "memory");
+      asm volatile(
+          "tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::
+              : "memory");
+    }
+    // Q tiles A and B: packed rows, zero past each tile's end
+    const T* Q = static_cast<const T*>(p.q);
+    for (int i = tid; i < PP_ROWS * (D / 8); i += PP_THREADS) {
+      const int rr = i / (D / 8), ch = i % (D / 8);
+      const int x = rr / BM, r = rr % BM;
+      const int R = rx0[x] + r;
+      const bool ok = R < rx_end[x];
+      const T* src = Q;
+      if (ok)
+        src = Q + static_cast<int64_t>(q0 + R / G) * p.q_st +
+              static_cast<int64_t>(g * G + R % G) * p.q_sh + ch * 8;
+      cp_async_16(sQ + x * C::Q_BYTES + (ch >> 3) * (BM * 128) +
+                      sw128(r, ch & 7),
+                  src, ok ? 16 : 0);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    fence_proxy_async();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = n_tiles > 0 ? *tmem_slot : 0;
+
+  if (warp == PP_LOAD_WARP || warp == PP_LOAD_WARP + 1) {
+    if (n_tiles > 0) {
+      // ------------------------------------------------------ producers
+      // warp 9 loads K tiles, warp 10 V tiles, so a K tile never waits for
+      // the release of a V stage; lane i issues box i of each tile and
+      // prefetches its page id one tile ahead
+      const int mat = warp - PP_LOAD_WARP;       // 0: K, 1: V
+      const int32_t* bt =
+          p.block_table + static_cast<int64_t>(b) * p.bt_stride;
+      auto fetch = [&](int j) -> int {
+        const int k0 = kstart + j * BN + lane * RB;
+        if (j >= n_tiles || lane >= BN / RB || k0 >= kmax_u) return 0;
+        const int blk = __ldg(bt + k0 / p.BS);
+        if (blk < 0 || blk >= p.num_blocks) {
+          atomicOr(p.err, kErrBadBlock);
+          return 0;
+        }
+        return blk;
+      };
+      const void* tm = mat ? static_cast<const void*>(&tm_v)
+                           : static_cast<const void*>(&tm_k);
+      int issued = 0;
+      int cur = fetch(0);
+      for (int j = 0; j < n_tiles; ++j) {
+        const int nxt = fetch(j + 1);
+        const int s = j & 1;
+        const int kt = kstart + j * BN;
+        int nbox = (kmax_u - kt + RB - 1) / RB;
+        if (nbox > BN / RB) nbox = BN / RB;
+        const uint32_t full = mat ? v_full(s) : k_full(s);
+        int stop = 0;
+        if (lane == 0) {
+          const uint32_t empty = mat ? v_empty(s) : k_empty(s);
+          if (j >= 2 && !mbar_wait(empty, ((j >> 1) & 1) ^ 1, abort_flag,
+                                   p.err))
+            stop = 1;
+          else
+            mbar_expect_tx(full, nbox * C::NCB * RB * 128);
+        }
+        stop = __shfl_sync(0xffffffffu, stop, 0);
+        if (stop) break;
+        if (lane < nbox) {
+          const uint32_t dst0 = (mat ? sV : sK) + s * C::KV_BYTES;
+          const int k0 = kt + lane * RB;
+          const int row = k0 % p.BS;
+          for (int cb = 0; cb < C::NCB; ++cb) {
+            const uint32_t dst = dst0 + cb * (BN * 128) + lane * RB * 128;
+            if (p.kv_order_hnd)
+              tma_load_4d(dst, tm, cb * 64, row, g, cur, full);
+            else
+              tma_load_4d(dst, tm, cb * 64, g, row, cur, full);
+          }
+        }
+        issued = j + 1;
+        cur = nxt;
+      }
+      if (lane == 0) {
+        for (int t = max(0, issued - 2); t < issued; ++t)
+          mbar_drain(mat ? v_full(t & 1) : k_full(t & 1), (t >> 1) & 1);
+      }
+    }
+  } else if (warp == PP_MMA_WARP) {
+    if (n_tiles > 0) {
+      // ---------------------------------------------------- MMA issuer
+      constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value;
+      constexpr uint32_t ID_S = idesc(128, BN, kBF16, false);
+      constexpr uint32_t ID_PV = idesc(128, D, kBF16, true);
+      bool ok = true;
+      auto in_range = [&](int x, int j) {
+        return j >= tlo[x] && j < tlo[x] + nx[x];
+      };
+      auto do_pv = [&](int i) -> bool {
+        const int s = i & 1;
+        if (!mbar_wait(v_full(s), (i >> 1) & 1, abort_flag, p.err))
+          return false;
+        const int kt = kstart + i * BN;
+        int nbox = (kmax_u - kt + RB - 1) / RB;
+        if (nbox > BN / RB) nbox = BN / RB;
+        const int r0 = min(nbox * RB, max(L - kt, 0));
+        if (r0 < BN) {
+          const uint32_t v0 = sV + s * C::KV_BYTES;
+          for (int idx = lane; idx < (BN - r0) * 8 * C::NCB; idx += 32) {
+            const int cb = idx / ((BN - r0) * 8);
+            const int rem = idx - cb * ((BN - r0) * 8);
+            const int r = r0 + rem / 8, c = rem % 8;
+            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(
+                             v0 + cb * (BN * 128) + r * 128 + (c << 4)),
+                         "r"(0)
+                         : "memory");
+          }
+          fence_proxy_async();
+          __syncwarp();
+        }
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          if (!in_range(x, i)) continue;
+          const int ix = i - tlo[x];
+          const int pb = ix & 1;
+          if (!mbar_wait(p_full(x, pb), (ix >> 1) & 1, abort_flag, p.err))
+            return false;
+          tc_fence_after();
+          {
+            // descriptors advance by (bytes >> 4) in the start-address field
+            const uint64_t a0 =
+                sdesc(sP + (2 * x + pb) * C::P_BYTES, 16, 1024);
+            const uint64_t b0 = sdesc(sV + s * C::KV_BYTES, BN * 128, 1024);
+#pragma unroll
+            for (int k = 0; k < BN / 16; ++k)
+              mma_f16_warp(tmem + C::O_COL + x * D,
+                           a0 + (((k >> 2) * (BM * 128) + (k & 3) * 32) >> 4),
+                           b0 + ((k * 16 * 128) >> 4), ID_PV,
+                           (ix > 0 || k > 0) ? 1 : 0);
+            mma_commit_warp(pv_done(x, pb));
+          }
+        }
+        mma_commit_warp(v_empty(s));
+        return true;
+      };
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        const int s = j & 1;
+        if (!mbar_wait(k_full(s), (j >> 1) & 1, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          if (!ok || !in_range(x, j)) continue;
+          const int jx = j - tlo[x];
+          const int sb = jx & 1;
+          if (jx >= 2 && !mbar_wait(s_free(x, sb), ((jx - 2) >> 1) & 1,
+                                    abort_flag, p.err)) {
+            ok = false;
+            continue;
+          }
+          tc_fence_after();
+          {
+            const uint64_t a0 = sdesc(sQ + x * C::Q_BYTES, 16, 1024);
+            const uint64_t b0 = sdesc(sK + s * C::KV_BYTES, 16, 1024);
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k)
+              mma_f16_warp(tmem + (2 * x + sb) * BN,
+                           a0 + (((k >> 2) * (BM * 128) + (k & 3) * 32) >> 4),
+                           b0 + (((k >> 2) * (BN * 128) + (k & 3) * 32) >> 4),
+                           ID_S, k > 0 ? 1 : 0);
+            mma_commit_warp(s_full(x, sb));
+          }
+        }
+        if (!ok) break;
+        mma_commit_warp(k_empty(s));
+        if (j >= 1 && !do_pv(j - 1)) ok = false;
+      }
+      if (ok) do_pv(n_tiles - 1);
+      mma_commit_warp(final_bar);
+      mbar_drain(final_bar, 0);
+    }
+  } else {
+    // ---------------------------------------------- softmax warpgroups
+    const int x = warp >> 2;                  // 0: tile A, 1: tile B
+    const int r = tid & 127;                  // row in tile == TMEM lane
+    // per-tile values by select (no runtime-indexed local arrays)
+    const int my_rx0 = x ? rx0[1] : rx0[0];
+    const int my_rx_end = x ? rx_end[1] : rx_end[0];
+    const bool my_has = x ? has[1] : has[0];
+    const int my_tlo = x ? tlo[1] : tlo[0];
+    const int my_nx = x ? nx[1] : nx[0];
+    const int R = my_rx0 + r;
+    const bool valid = R < my_rx_end;
+    const int pos = ctx + (valid ? R / G : 0);
+    const int h = g * G + (valid ? R % G : 0);
+    const int tok = q0 + (valid ? R / G : 0);
+    const float slope = (p.alibi && valid) ? p.alibi[h] : 0.f;
+    const float scale_log2 = p.scale * kLog2e;
+    const float scale_over_cap = p.softcap > 0.f ? p.scale / p.softcap : 0.f;
+    const float cap_log2e = p.softcap * kLog2e;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int kmin = x ? kmn[1] : kmn[0], kmax = x ? kmx[1] : kmx[0];
+    int full_lo = kmin, full_hi = kmax;
+    if (my_has) {
+      const int p_lo = ctx + my_rx0 / G, p_hi = ctx + (my_rx_end - 1) / G;
+      if (p.wl >= 0) full_lo = max(full_lo, p_hi - p.wl);
+      if (p.causal) full_hi = min(full_hi, p_lo + 1);
+      if (p.wr >= 0) full_hi = min(full_hi, p_lo + p.wr + 1);
+    }
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int jx = 0; jx < my_nx; ++jx) {
+      const int sb = jx & 1;
+      if (!mbar_wait(s_full(x, sb), (jx >> 1) & 1, abort_flag, p.err)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int kt = kstart + (my_tlo + jx) * BN;
+      const bool unmasked = kt >= full_lo && kt + BN <= full_hi;
+      const bool fast = plain && unmasked;
+      const bool fast_cap = !plain && p.alibi == nullptr && unmasked;
+      float v[BN];
+      const uint32_t s_addr = tmem + lane_base + (2 * x + sb) * BN;
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_addr + c * 32, v + c * 32);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(s_free(x, sb));
+      float mx8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
+      if (fast) {
+#pragma unroll
+        for (int e = 0; e < BN; ++e)
+          mx8[e & 7] = fmaxf(mx8[e & 7], v[e] * scale_log2);
+      } else if (fast_cap) {
+#pragma unroll
+        for (int e = 0; e < BN; ++e) {
+          v[e] = cap_log2e * tanh_fast(v[e] * scale_over_cap);
+          mx8[e & 7] = fmaxf(mx8[e & 7], v[e]);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < BN; ++e) {
+          v[e] = masked_logit(v[e], kt + e, pos, valid, kmin, kmax, p, slope);
+          mx8[e & 7] = fmaxf(mx8[e & 7], v[e]);
+        }
+      }
+      const float mx =
+          fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      const bool grow = mx > m_ref + kRescaleThreshold;
+      float alpha = 1.f;
+      if (grow) {
+        alpha = ex2(m_ref - mx);
+        m_ref = mx;
+        l *= alpha;
+      }
+      const float base_m = (m_ref == -INFINITY) ? 0.f : m_ref;
+      if (jx >= 1 && __any_sync(0xffffffffu, grow)) {
+        const int pb = (jx - 1) & 1;
+        if (!mbar_wait(pv_done(x, pb), ((jx - 1) >> 1) & 1, abort_flag,
+                       p.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          float ov[32];
+          const uint32_t ta = tmem + lane_base + C::O_COL + x * D + c * 32;
+          tmem_ld32(ta, ov);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ov[e] *= alpha;
+          tmem_st32(ta, ov);
+        }
+        tmem_wait_st();
+      }
+      float sum8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sum8[e] = 0.f;
+      if (fast) {
+#pragma unroll
+        for (int e = 0; e < BN; ++e) {
+          v[e] = ex2(fmaf(v[e], scale_log2, -base_m));
+          sum8[e & 7] += v[e];
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < BN; ++e) {
+          v[e] = ex2(v[e] - base_m);
+          sum8[e & 7] += v[e];
+        }
+      }
+      // P buffer sb was last read by PV_x(jx - 2)
+      if (jx >= 2 && !mbar_wait(pv_done(x, sb), ((jx - 2) >> 1) & 1,
+                                abort_flag, p.err)) {
+        ok = false;
+        break;
+      }
+      const uint32_t p_row = sP + (2 * x + sb) * C::P_BYTES;
+#pragma unroll
+      for (int q = 0; q < BN / 8; ++q) {
+        const float* e = v + q * 8;
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                         p_row + (q >> 3) * (BM * 128) + sw128(r, q & 7)),
+                     "r"(pack2<T>(e[0], e[1])), "r"(pack2<T>(e[2], e[3])),
+                     "r"(pack2<T>(e[4], e[5])), "r"(pack2<T>(e[6], e[7]))
+                     : "memory");
+      }
+      l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
+           ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+      tc_fence_before();
+      fence_proxy_async();
+      mbar_arrive(p_full(x, sb));
+    }
+    T* dst = OUT + static_cast<int64_t>(tok) * p.o_st +
+             static_cast<int64_t>(h) * p.o_sh;
+    if (my_nx == 0) {
+      // no admissible key for this tile's rows: out = 0, lse = -inf
+      if (valid) {
+#pragma unroll
+        for (int c = 0; c < D; c += 8)
+          *reinterpret_cast<uint4*>(dst + c) = make_uint4(0, 0, 0, 0);
+        if (p.lse) p.lse[static_cast<int64_t>(h) * p.total_q + tok] = -INFINITY;
+      }
+    } else if (ok) {
+      const int lb = (my_nx - 1) & 1;
+      if (mbar_wait(pv_done(x, lb), ((my_nx - 1) >> 1) & 1, abort_flag,
+                    p.err)) {
+        tc_fence_after();
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          float ov[32];
+          tmem_ld32(tmem + lane_base + C::O_COL + x * D + c * 32, ov);
+          tmem_wait_ld();
+          if (valid) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 8) {
+              uint4 pk;
+              pk.x = pack2<T>(ov[e] * inv, ov[e + 1] * inv);
+              pk.y = pack2<T>(ov[e + 2] * inv, ov[e + 3] * inv);
+              pk.z = pack2<T>(ov[e + 4] * inv, ov[e + 5] * inv);
+              pk.w = pack2<T>(ov[e + 6] * inv, ov[e + 7] * inv);
+              *reinterpret_cast<uint4*>(dst + c * 32 + e) = pk;
+            }
+          }
+        }
+        if (valid && p.lse)
+          p.lse[static_cast<int64_t>(h) * p.total_q + tok] =
+              l > 0.f ? (m_ref + lg2(l)) * kLn2 : -INFINITY;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == PP_MMA_WARP && n_tiles > 0) {
+    tc_fence_after();
+    asm volatile(
+        "tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+        "r"(C::TMEM_COLS)
+        : "memory");
+  }
+}
+
 // ------------------------------------------------------------ host side
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -892,17 +1457,21 @@ cudaError_t launch_prefill_attn_tc(const AttnParams& a, int D, bool bf16,
                    a.c_sr, a.c_sh, RB, p.kv_order_hnd))
     return cudaErrorInvalidValue;
   // compact 1-D grid: an upper bound on the row tiles of all requests,
-  // sum_b ceil(q_b * G / 128) <= ceil(total_q * G / 128) + batch
+  // sum_b ceil(q_b * G / rows) <= ceil(total_q * G / rows) + batch, with
+  // 256-row pair tiles for D <= 128 and 128-row tiles for D = 256
   (void)grid_y;
+  const bool pp = D <= 128;
+  const int cta_rows = pp ? PP_ROWS : BM;
   const int64_t tiles =
-      (static_cast<int64_t>(a.total_q) * a.G + BM - 1) / BM + a.batch;
+      (static_cast<int64_t>(a.total_q) * a.G + cta_rows - 1) / cta_rows +
+      a.batch;
   const int64_t gx = tiles * a.Hkv;
   if (gx <= 0 || gx > 0x7fffffff) return cudaErrorInvalidValue;
   dim3 grid(static_cast<unsigned>(gx));
   static bool attr_set[2][3] = {};   // [bf16][D index]; idempotent if racing
   const int di = D == 64 ? 0 : (D == 128 ? 1 : 2);
-  auto go = [&](void (*kern)(TcParams, CUtensorMap, CUtensorMap),
-                int smem) -> cudaError_t {
+  auto go = [&](void (*kern)(TcParams, CUtensorMap, CUtensorMap), int smem,
+                int threads) -> cudaError_t {
     if (!attr_set[bf16][di]) {
       cudaError_t e = cudaFuncSetAttribute(
           kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -910,20 +1479,30 @@ cudaError_t launch_prefill_attn_tc(const AttnParams& a, int D, bool bf16,
       attr_set[bf16][di] = true;
     }
     note_launch();
-    kern<<<grid, NUM_THREADS, smem, stream>>>(p, mk, mv);
+    kern<<<grid, threads, smem, stream>>>(p, mk, mv);
     return cudaGetLastError();
   };
   if (bf16) {
     switch (D) {
-      case 64:  return go(prefill_tc_kernel<__nv_bfloat16, 64>, Cfg<64>::SMEM);
-      case 128: return go(prefill_tc_kernel<__nv_bfloat16, 128>, Cfg<128>::SMEM);
-      case 256: return go(prefill_tc_kernel<__nv_bfloat16, 256>, Cfg<256>::SMEM);
+      case 64:
+        return go(prefill_pp_kernel<__nv_bfloat16, 64>, PPCfg<64>::SMEM,
+                  PP_THREADS);
+      case 128:
+        return go(prefill_pp_kernel<__nv_bfloat16, 128>, PPCfg<128>::SMEM,
+                  PP_THREADS);
+      case 256:
+        return go(prefill_tc_kernel<__nv_bfloat16, 256>, Cfg<256>::SMEM,
+                  NUM_THREADS);
     }
   } else {
     switch (D) {
-      case 64:  return go(prefill_tc_kernel<__half, 64>, Cfg<64>::SMEM);
-      case 128: return go(prefill_tc_kernel<__half, 128>, Cfg<128>::SMEM);
-      case 256: return go(prefill_tc_kernel<__half, 256>, Cfg<256>::SMEM);
+      case 64:
+        return go(prefill_pp_kernel<__half, 64>, PPCfg<64>::SMEM, PP_THREADS);
+      case 128:
+        return go(prefill_pp_kernel<__half, 128>, PPCfg<128>::SMEM,
+                  PP_THREADS);
+      case 256:
+        return go(prefill_tc_kernel<__half, 256>, Cfg<256>::SMEM, NUM_THREADS);
     }
   }
   return cudaErrorInvalidValue;

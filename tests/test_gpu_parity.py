@@ -137,6 +137,11 @@ PREFILL_CASES = [
     ([64, 129], [64, 400], 8, 1, 128, 16, dict(dtype="f16")),
     ([257, 17], [1000, 517], 16, 8, 128, 16, dict()),
     ([20, 31], [2000, 31], 32, 8, 128, 16, dict(window_size=(7, 3))),
+    # two-tile CTAs: B tile partly filled, windowed key ranges of A and B
+    # that differ, non-causal, and an fp16 D = 64 case
+    ([100, 70], [3000, 900], 32, 8, 128, 16, dict(window_size=(200, 0))),
+    ([65, 300], [65, 700], 8, 2, 128, 32, dict(causal=False)),
+    ([129, 200], [500, 1200], 16, 4, 64, 16, dict(dtype="f16")),
 ]
 
 
