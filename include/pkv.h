@@ -169,6 +169,43 @@ PKV_API pkv_status pkv_paged_attention_varlen(
     pkv_dtype dtype, pkv_stream_t stream);
 
 /*
+ * Optional features of the attention call; zero-initialise and set what is
+ * used.  A NULL options pointer means all off.
+ *
+ * sinks: [num_heads] float32 device array of per-head attention-sink
+ *   logits, or NULL.  Source: "vllm/v1/attention/backends/flash_attn.py",
+ *   FlashAttentionImpl.__init__ (sinks, one per query head) and forward
+ *   (s_aux=self.sinks); cascade_attention passes s_aux to the prefix call
+ *   only ("incorporated into prefix_lse ... during the final attention
+ *   merge").  The sink is one more logit of the row's softmax with no value:
+ *   out = sum_j e^{s_j} v_j / (e^{sink_h} + sum_j e^{s_j}) and
+ *   lse = ln(e^{sink_h} + sum_j e^{s_j}) (a row without keys gets out = 0,
+ *   lse = sink_h).  The sink is neither scaled nor soft-capped.
+ */
+typedef struct {
+  const float* sinks;
+} pkv_attention_options;
+
+/* pkv_paged_attention_varlen with options (see pkv_attention_options). */
+PKV_API pkv_status pkv_paged_attention_varlen_opts(
+    const void* q, int64_t q_stride_tok, int64_t q_stride_head,
+    const void* key_cache, const void* value_cache,
+    const int64_t cache_strides[4],
+    void* out, int64_t o_stride_tok, int64_t o_stride_head,
+    const int32_t* cu_seqlens_q, const int32_t* seqused_k, int batch,
+    int total_q, int max_seqlen_q, int max_seqlen_k,
+    const int32_t* block_table, int64_t block_table_stride,
+    int max_blocks_per_seq,
+    int num_heads, int num_kv_heads, int head_size, int block_size,
+    int64_t num_blocks,
+    float softmax_scale, int causal, int window_left, int window_right,
+    float softcap, const float* alibi_slopes,
+    int num_splits, float* softmax_lse,
+    void* workspace, size_t workspace_bytes,
+    pkv_dtype dtype, pkv_stream_t stream,
+    const pkv_attention_options* opts);
+
+/*
  * Bytes of workspace pkv_paged_attention_varlen needs for these arguments
  * (on the current device: the split plan depends on its SM count).  Returns
  * 0 when no scratch is needed, and (size_t)-1 for invalid arguments.
@@ -251,6 +288,35 @@ PKV_API pkv_status pkv_merge_attn_states(
     const void* suffix_output, const float* suffix_lse, float* output_lse,
     int num_tokens, int num_heads, int head_size,
     pkv_dtype out_dtype, pkv_dtype in_dtype, pkv_stream_t stream);
+
+/*
+ * pkv_make_local_attention_virtual_batches -- chunked local attention as
+ * virtual requests (HOST arrays in and out; no GPU work).
+ *
+ * Source: "vllm.v1.attention.backends.flash_attn" (vLLM v0.9.0.1 docs),
+ * make_local_attention_virtual_batches and FlashAttentionMetadataBuilder.
+ * build.  With chunk size C (a multiple of block_size), request b with
+ * q_b = query_start_loc[b+1] - query_start_loc[b] > 0 queries and
+ * L_b = seq_lens[b] >= q_b keys is split into one virtual request per C-wide
+ * key chunk c that holds one of its queries: seqlens_q_local = the queries in
+ * chunk c, seqlens_k_local = min(L_b, (c+1)C) - cC, block_table_local row =
+ * columns cC/BS .. cC/BS + C/BS - 1 of block-table row b (clipped to the last
+ * column).  Running pkv_paged_attention_varlen (causal) on the virtual
+ * requests gives chunked local attention: the query at position p sees keys
+ * j <= p with j / C == p / C.
+ *
+ * Pass all four output pointers NULL to get only *num_virtual.  Otherwise
+ * capacity must be >= *num_virtual; cu_seqlens_q_local has capacity + 1
+ * entries and block_table_local is [capacity, C / block_size].
+ * Errors: C not a positive multiple of block_size, q_b <= 0, L_b < q_b, NULL
+ * arrays, too little capacity -> PKV_ERR_INVALID_ARG.
+ */
+PKV_API pkv_status pkv_make_local_attention_virtual_batches(
+    int attn_chunk_size, const int32_t* query_start_loc,
+    const int32_t* seq_lens, int batch, const int32_t* block_table,
+    int64_t block_table_stride, int max_blocks_per_seq, int block_size,
+    int* num_virtual, int32_t* seqlens_q_local, int32_t* cu_seqlens_q_local,
+    int32_t* seqlens_k_local, int32_t* block_table_local, int capacity);
 
 /*
  * pkv_check_device_errors -- synchronise `stream`, then read and clear the

@@ -4,6 +4,7 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
 legs use this package.  The library never imports it.
 """
 from .paged_attention import (  # noqa: F401
+    add_sink_ref,
     admissible_mask,
     attention_logits,
     cascade_ref,

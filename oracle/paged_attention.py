@@ -34,6 +34,8 @@ Readings taken where the pages are silent (each is listed in the design doc):
   ``-slope_h * |p - j|`` is added, then the mask;
 * query head h reads KV head ``h // (Hq // Hkv)``;
 * LSE is natural-log, float, laid out ``[Hq, T]``;
+* an attention sink (``s_aux``) is one more logit per head in the softmax
+  denominator, with no value; the LSE includes it;
 * a row with no admissible key gives out = 0 and lse = -inf.
 
 Parity status: every function is pinned by ``tests/test_oracle_*.py`` against
@@ -133,9 +135,26 @@ def attention_logits(q_rows, k_rows, q_len, k_len, softmax_scale, softcap,
     return s
 
 
+def add_sink_ref(out, lse, sinks):
+    """Fold per-head sink logits into finished attention results.
+
+    vLLM v1 ``FlashAttentionImpl`` passes ``sinks`` [num_heads] float32 as
+    ``s_aux``; ``cascade_attention`` notes that the kernel incorporates it
+    into the prefix LSE so that it takes effect in the merge.  Reading: the
+    sink is one more logit in each row's softmax denominator with no value,
+    so lse' = ln(e^lse + e^sink) and out' = out * e^(lse - lse').
+    out [T, H, D], lse [H, T], sinks [H].
+    """
+    sinks = np.asarray(sinks, dtype=np.float64)[:, None]        # [H, 1]
+    new_lse = np.logaddexp(lse, sinks)
+    w = np.where(np.isfinite(lse), np.exp(lse - new_lse), 0.0)  # [H, T]
+    return out * w.T[..., None], new_lse
+
+
 def paged_attention_ref(q, key_cache, value_cache, cu_seqlens_q, seqused_k,
                         block_table, softmax_scale, causal=True,
-                        window_size=(-1, -1), softcap=0.0, alibi_slopes=None):
+                        window_size=(-1, -1), softcap=0.0, alibi_slopes=None,
+                        sinks=None):
     """Varlen attention of q over the paged cache; returns (out, lse).
 
     vLLM v1 ``FlashAttentionImpl.forward`` call to ``flash_attn_varlen_func``
@@ -180,6 +199,8 @@ def paged_attention_ref(q, key_cache, value_cache, cu_seqlens_q, seqused_k,
             o = (w @ v_b[:, g, :]) / np.where(has, l, 1.0)[:, None]
             out[t0:t1, h, :] = np.where(has[:, None], o, 0.0)
             lse[h, t0:t1] = row_lse
+    if sinks is not None:
+        out, lse = add_sink_ref(out, lse, sinks)
     return out, lse
 
 
@@ -236,7 +257,8 @@ def merge_many_ref(outputs, lses):
 # ---------------------------------------------------------------------------
 
 def cascade_ref(q, key_cache, value_cache, cu_seqlens_q, seqused_k,
-                block_table, common_prefix_len, softmax_scale, softcap=0.0):
+                block_table, common_prefix_len, softmax_scale, softcap=0.0,
+                sinks=None):
     """Shared-prefix attention as vLLM v1 ``cascade_attention`` defines it.
 
     Prefix: all T queries as one non-causal "sequence" over
@@ -253,7 +275,7 @@ def cascade_ref(q, key_cache, value_cache, cu_seqlens_q, seqused_k,
     o_p, l_p = paged_attention_ref(q, key_cache, value_cache, cu_prefix,
                                    prefix_lens, block_table[:1],
                                    softmax_scale, causal=False,
-                                   softcap=softcap)
+                                   softcap=softcap, sinks=sinks)
     suffix_lens = np.asarray(seqused_k) - common_prefix_len
     o_s, l_s = paged_attention_ref(q, key_cache, value_cache, cu_seqlens_q,
                                    suffix_lens, block_table[:, n_common:],

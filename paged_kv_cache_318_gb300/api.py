@@ -41,6 +41,11 @@ i32, i64, f32, sz = ctypes.c_int, ctypes.c_int64, ctypes.c_float, \
     ctypes.c_size_t
 
 
+class _Options(ctypes.Structure):
+    """pkv_attention_options (include/pkv.h)."""
+    _fields_ = [("sinks", ctypes.c_void_p)]
+
+
 class PkvError(RuntimeError):
     """A libpkv call returned a CUDA or device-index error."""
 
@@ -78,11 +83,18 @@ def load_library():
             vp, i64, i64, vp, vp, c_i64p, vp, i64, i64, vp, vp, i32, i32,
             i32, i32, vp, i64, i32, i32, i32, i32, i32, i64, f32, i32, i32,
             i32, f32, vp, i32, vp, vp, sz, i32, vp]
+        lib.pkv_paged_attention_varlen_opts.restype = i32
+        lib.pkv_paged_attention_varlen_opts.argtypes = \
+            lib.pkv_paged_attention_varlen.argtypes + [vp]
         lib.pkv_paged_attention_workspace_size.restype = sz
         lib.pkv_paged_attention_workspace_size.argtypes = [i32] * 12
         lib.pkv_merge_attn_states.restype = i32
         lib.pkv_merge_attn_states.argtypes = [
             vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]
+        lib.pkv_make_local_attention_virtual_batches.restype = i32
+        lib.pkv_make_local_attention_virtual_batches.argtypes = [
+            i32, vp, vp, i32, vp, i64, i32, i32, ctypes.POINTER(ctypes.c_int),
+            vp, vp, vp, vp, i32]
         lib.pkv_set_prefill_kernel.restype = i32
         lib.pkv_set_prefill_kernel.argtypes = [i32]
         lib.pkv_launch_count.restype = ctypes.c_uint64
@@ -200,7 +212,7 @@ def flash_attn_varlen_func(q, k, v, max_seqlen_q, cu_seqlens_q, max_seqlen_k,
                            window_size=(-1, -1), softcap=0.0,
                            alibi_slopes=None, block_table=None,
                            return_softmax_lse=False, out=None, num_splits=0,
-                           cu_seqlens_k=None, workspace=None):
+                           cu_seqlens_k=None, workspace=None, s_aux=None):
     """Varlen attention over a paged KV cache.
 
     q [T, Hq, D]; k, v: cache views [num_blocks, block_size, Hkv, D];
@@ -246,7 +258,12 @@ def flash_attn_varlen_func(q, k, v, max_seqlen_q, cu_seqlens_q, max_seqlen_k,
     cs = _cache_strides(k, v)
     if alibi_slopes is not None and alibi_slopes.dtype != torch.float32:
         raise ValueError("alibi_slopes must be float32")
-    _check(lib.pkv_paged_attention_varlen(
+    opts = None
+    if s_aux is not None:
+        if s_aux.dtype != torch.float32 or s_aux.shape != (Hq,):
+            raise ValueError("s_aux (sinks) must be float32 [num_heads]")
+        opts = _Options(sinks=s_aux.data_ptr())
+    _check(lib.pkv_paged_attention_varlen_opts(
         _ptr(q), q.stride(0), q.stride(1), _ptr(k), _ptr(v), cs, _ptr(out),
         out.stride(0), out.stride(1), _ptr(cu_seqlens_q), _ptr(seqused_k),
         batch, T, int(max_seqlen_q), int(max_seqlen_k), _ptr(block_table),
@@ -254,10 +271,43 @@ def flash_attn_varlen_func(q, k, v, max_seqlen_q, cu_seqlens_q, max_seqlen_k,
         float(softmax_scale), int(bool(causal)), int(window_size[0]),
         int(window_size[1]), float(softcap or 0.0), _ptr(alibi_slopes),
         int(num_splits), _ptr(lse), _ptr(workspace), ws_bytes, _dtype(q),
-        _stream(q)))
+        _stream(q), None if opts is None else ctypes.byref(opts)))
     if return_softmax_lse:
         return out, lse
     return out
+
+
+def make_local_attention_virtual_batches(attn_chunk_size, query_start_loc,
+                                         seq_lens, block_table, block_size):
+    """Chunked local attention as virtual requests (host numpy in/out).
+
+    Returns (seqlens_q_local, cu_seqlens_q_local, seqlens_k_local,
+    block_table_local) as int32 numpy arrays, as the vLLM v0.9.0.1 backend's
+    ``make_local_attention_virtual_batches`` does.
+    """
+    import numpy as np
+    lib = load_library()
+    qsl = np.ascontiguousarray(query_start_loc, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    batch = len(sl)
+    n = ctypes.c_int(0)
+    P = ctypes.c_void_p
+    _check(lib.pkv_make_local_attention_virtual_batches(
+        attn_chunk_size, qsl.ctypes.data_as(P), sl.ctypes.data_as(P), batch,
+        bt.ctypes.data_as(P), bt.shape[1], bt.shape[1], block_size,
+        ctypes.byref(n), None, None, None, None, 0))
+    V, pages = n.value, attn_chunk_size // block_size
+    sq = np.empty(V, np.int32)
+    cu = np.empty(V + 1, np.int32)
+    sk = np.empty(V, np.int32)
+    btl = np.empty((V, pages), np.int32)
+    _check(lib.pkv_make_local_attention_virtual_batches(
+        attn_chunk_size, qsl.ctypes.data_as(P), sl.ctypes.data_as(P), batch,
+        bt.ctypes.data_as(P), bt.shape[1], bt.shape[1], block_size,
+        ctypes.byref(n), sq.ctypes.data_as(P), cu.ctypes.data_as(P),
+        sk.ctypes.data_as(P), btl.ctypes.data_as(P), V))
+    return sq, cu, sk, btl
 
 
 def merge_attn_states(output, prefix_output, prefix_lse, suffix_output,
@@ -287,7 +337,7 @@ def cascade_attention(output, query, key_cache, value_cache, cu_query_lens,
                       suffix_kv_lens, max_kv_len, softmax_scale,
                       alibi_slopes, sliding_window, logits_soft_cap,
                       block_table, common_prefix_len, max_num_splits=0,
-                      workspace=None):
+                      workspace=None, s_aux=None):
     """Shared-prefix attention: prefix (non-causal, block_table[:1]) +
     suffix (causal, block_table[:, P/BS:]) merged by LSE, as in vLLM v1's
     ``cascade_attention``."""
@@ -308,7 +358,7 @@ def cascade_attention(output, query, key_cache, value_cache, cu_query_lens,
         softmax_scale=softmax_scale, causal=False,
         window_size=sliding_window, softcap=logits_soft_cap,
         block_table=block_table[:1], return_softmax_lse=True,
-        num_splits=max_num_splits)
+        num_splits=max_num_splits, s_aux=s_aux)
     suffix_out, suffix_lse = flash_attn_varlen_func(
         query, key_cache, value_cache, max_query_len, cu_query_lens,
         max_kv_len - common_prefix_len, seqused_k=suffix_kv_lens,

@@ -373,9 +373,9 @@ attn_mma_kernel(const AttnParams p) {
       const int r = half ? rB : rA;
       if (r >= row_end) continue;
       const float l = half ? lB : lA, m = half ? mB : mA;
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      const float lse = l > 0.f ? (m + lg2(l)) * kLn2 : -INFINITY;
       const int tok = q0 + r / G, h = g * G + r % G;
+      float inv, lse;   // a sink enters once: here, or in the split combine
+      finish_row(m, l, split ? nullptr : p.sinks, h, &inv, &lse);
       if (!split) {
         T* dst = OUT + static_cast<int64_t>(tok) * p.o_st +
                  static_cast<int64_t>(h) * p.o_sh;
@@ -438,9 +438,9 @@ attn_mma_kernel(const AttnParams p) {
         acc.z += f * v.z;
         acc.w += f * v.w;
       }
-      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-      const float lse = lsum > 0.f ? (M + lg2(lsum)) * kLn2 : -INFINITY;
       const int tok = q0 + R / G, h = g * G + R % G;
+      float inv, lse;   // a sink enters once: here, or in the split combine
+      finish_row(M, lsum, split ? nullptr : p.sinks, h, &inv, &lse);
       if (!split) {
         T* dst = OUT + static_cast<int64_t>(tok) * p.o_st +
                  static_cast<int64_t>(h) * p.o_sh + c;
@@ -493,11 +493,15 @@ split_combine_kernel(const CombineParams p) {
 #pragma unroll
     for (int o = 16; o; o >>= 1)
       M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    // a sink logit is one more softmax term without a value
+    const float sink = p.sinks ? p.sinks[h] : -INFINITY;
+    M = fmaxf(M, sink);
     const float base = (M == -INFINITY) ? 0.f : M;
-    float lsum = 0.f;
+    const float w_sink = p.sinks ? __expf(sink - base) : 0.f;
+    float lsum = w_sink;
     for (int c = lane * 4; c < D; c += 128) {
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      float ls = 0.f;
+      float ls = w_sink;
       for (int s = 0; s < nsplit; ++s) {
         const float l = p.part_lse[(static_cast<int64_t>(s) * p.Hq + h) *
                                        p.total_q + tok];

@@ -284,6 +284,29 @@ pkv_status pkv_paged_attention_varlen(
     const float* alibi_slopes, int num_splits, float* softmax_lse,
     void* workspace, size_t workspace_bytes, pkv_dtype dtype,
     pkv_stream_t stream) {
+  return pkv_paged_attention_varlen_opts(
+      q, q_stride_tok, q_stride_head, key_cache, value_cache, cache_strides,
+      out, o_stride_tok, o_stride_head, cu_seqlens_q, seqused_k, batch,
+      total_q, max_seqlen_q, max_seqlen_k, block_table, block_table_stride,
+      max_blocks_per_seq, num_heads, num_kv_heads, head_size, block_size,
+      num_blocks, softmax_scale, causal, window_left, window_right, softcap,
+      alibi_slopes, num_splits, softmax_lse, workspace, workspace_bytes,
+      dtype, stream, nullptr);
+}
+
+pkv_status pkv_paged_attention_varlen_opts(
+    const void* q, int64_t q_stride_tok, int64_t q_stride_head,
+    const void* key_cache, const void* value_cache,
+    const int64_t cache_strides[4], void* out, int64_t o_stride_tok,
+    int64_t o_stride_head, const int32_t* cu_seqlens_q,
+    const int32_t* seqused_k, int batch, int total_q, int max_seqlen_q,
+    int max_seqlen_k, const int32_t* block_table, int64_t block_table_stride,
+    int max_blocks_per_seq, int num_heads, int num_kv_heads, int head_size,
+    int block_size, int64_t num_blocks, float softmax_scale, int causal,
+    int window_left, int window_right, float softcap,
+    const float* alibi_slopes, int num_splits, float* softmax_lse,
+    void* workspace, size_t workspace_bytes, pkv_dtype dtype,
+    pkv_stream_t stream, const pkv_attention_options* opts) {
   pkv_status st =
       check_attn_shape(batch, total_q, max_seqlen_q, max_seqlen_k, num_heads,
                        num_kv_heads, head_size, block_size, num_splits);
@@ -362,6 +385,7 @@ pkv_status pkv_paged_attention_varlen(
   p.scale = softmax_scale;
   p.softcap = softcap;
   p.alibi = alibi_slopes;
+  p.sinks = opts ? opts->sinks : nullptr;
   p.causal = causal ? 1 : 0;
   p.wl = wl;
   p.wr = wr;
@@ -401,6 +425,7 @@ pkv_status pkv_paged_attention_varlen(
       c.wr = wr;
       c.chunk = pl.chunk;
       c.splits = pl.splits;
+      c.sinks = p.sinks;
       c.min_rows = 1;
       c.max_rows = kDecodeRows;
       e = launch_split_combine(c, bf16, s);

@@ -176,6 +176,7 @@ struct AttnParams {
   float scale;                // softmax scale (natural units)
   float softcap;              // 0 = none
   const float* alibi;         // [Hq] or null
+  const float* sinks;         // [Hq] sink logits (natural log) or null
   int causal, wl, wr;
   // which requests this launch owns: rows = q_b * G in [min_rows, max_rows]
   int min_rows, max_rows;
@@ -199,7 +200,27 @@ struct CombineParams {
   int causal, wl, wr;
   int chunk, splits;
   int min_rows, max_rows;
+  const float* sinks;         // [Hq] sink logits or null (added once here)
 };
+
+// Final normalisation of one row: acc is relative to the running max m
+// (log2 units), l the running sum.  With a sink logit (natural units), it is
+// one more term of the denominator.  Returns 1/denominator relative to m in
+// *inv and the natural-log LSE.
+__device__ __forceinline__ void finish_row(float m, float l, const float* sinks,
+                                          int h, float* inv, float* lse) {
+  if (!sinks) {
+    *inv = l > 0.f ? 1.f / l : 0.f;
+    *lse = l > 0.f ? (m + lg2(l)) * kLn2 : -INFINITY;
+    return;
+  }
+  const float z = sinks[h] * kLog2e;
+  const float M = fmaxf(m, z);
+  const float em = ex2(m - M);             // m = -inf -> 0
+  const float den = l * em + ex2(z - M);
+  *inv = em / den;
+  *lse = (M + lg2(den)) * kLn2;
+}
 
 // Count one kernel launch (reported by pkv_launch_count).
 void note_launch();

@@ -104,6 +104,7 @@ struct TcParams {
   int Hq, Hkv, G, BS, RB;
   float scale, softcap;
   const float* alibi;
+  const float* sinks;
   int causal, wl, wr;
   int min_rows;
   int batch;
@@ -424,7 +425,8 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
                                 static_cast<int64_t>(h) * p.o_sh + c * 8) =
           make_uint4(0, 0, 0, 0);
       if (p.lse && c == 0)
-        p.lse[static_cast<int64_t>(h) * p.total_q + tok] = -INFINITY;
+        p.lse[static_cast<int64_t>(h) * p.total_q + tok] =
+            p.sinks ? p.sinks[h] : -INFINITY;
     }
     return;
   }
@@ -781,7 +783,8 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
     if (ok && mbar_wait(pv_done(lb), ((n_tiles - 1) / C::PBUF) & 1,
                         abort_flag, p.err)) {
       tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      float inv, lse_v;
+      finish_row(m_ref, l, p.sinks, h, &inv, &lse_v);
       const int tok = q0 + (valid ? R / G : 0);
       T* dst = OUT + static_cast<int64_t>(tok) * p.o_st +
                static_cast<int64_t>(h) * p.o_sh;
@@ -804,7 +807,7 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
       }
       if (valid && p.lse)
         p.lse[static_cast<int64_t>(h) * p.total_q + tok] =
-            l > 0.f ? (m_ref + lg2(l)) * kLn2 : -INFINITY;
+            lse_v;
     }
   }
 
@@ -1319,14 +1322,17 @@ prefill_pp_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
 #pragma unroll
         for (int c = 0; c < D; c += 8)
           *reinterpret_cast<uint4*>(dst + c) = make_uint4(0, 0, 0, 0);
-        if (p.lse) p.lse[static_cast<int64_t>(h) * p.total_q + tok] = -INFINITY;
+        if (p.lse)
+          p.lse[static_cast<int64_t>(h) * p.total_q + tok] =
+              p.sinks ? p.sinks[h] : -INFINITY;
       }
     } else if (ok) {
       const int lb = (my_nx - 1) & 1;
       if (mbar_wait(pv_done(x, lb), ((my_nx - 1) >> 1) & 1, abort_flag,
                     p.err)) {
         tc_fence_after();
-        const float inv = l > 0.f ? 1.f / l : 0.f;
+        float inv, lse_v;
+        finish_row(m_ref, l, p.sinks, h, &inv, &lse_v);
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           float ov[32];
@@ -1346,7 +1352,7 @@ prefill_pp_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
         }
         if (valid && p.lse)
           p.lse[static_cast<int64_t>(h) * p.total_q + tok] =
-              l > 0.f ? (m_ref + lg2(l)) * kLn2 : -INFINITY;
+              lse_v;
       }
     }
   }
@@ -1439,6 +1445,7 @@ cudaError_t launch_prefill_attn_tc(const AttnParams& a, int D, bool bf16,
   p.scale = a.scale;
   p.softcap = a.softcap;
   p.alibi = a.alibi;
+  p.sinks = a.sinks;
   p.causal = a.causal;
   p.wl = a.wl;
   p.wr = a.wr;

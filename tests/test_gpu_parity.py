@@ -337,3 +337,87 @@ def test_full_long_decode_sampled(cuda_device):
 def test_full_cascade_sampled(cuda_device):
     wl = workloads.cascade_decode(device=cuda_device)
     _sampled(wl, cuda_device, [0, 100, 255], cascade=True)
+
+
+# -------------------------------------------------------- attention sinks
+SINK_CASES = [
+    # q_lens, seq_lens, Hq, Hkv, D, BS, num_splits, prefill kernel
+    ([1, 1, 1], [500, 3000, 7], 16, 4, 128, 16, 0, "tcgen05"),
+    ([1, 1], [5000, 64], 8, 2, 128, 64, 4, "tcgen05"),
+    ([1, 2], [900, 33], 8, 4, 64, 16, 1, "tcgen05"),
+    ([150, 60], [700, 60], 16, 4, 128, 16, 0, "tcgen05"),
+    ([150, 60], [700, 60], 16, 4, 128, 16, 0, "mma_sync"),
+    ([90, 1], [400, 2000], 8, 4, 256, 32, 0, "tcgen05"),
+    ([2, 3], [1, 2], 4, 2, 64, 16, 0, "tcgen05"),     # rows without keys
+]
+
+
+@pytest.mark.parametrize("idx", range(len(SINK_CASES)))
+def test_sinks(cuda_device, idx):
+    import dataclasses
+    from oracle.harness import _f64
+    from oracle import reshape_and_cache_ref
+    q_lens, seq_lens, Hq, Hkv, D, BS, splits, kern = SINK_CASES[idx]
+    ok_lens = [max(L, q) for q, L in zip(q_lens, seq_lens)]
+    wl = workloads.build_workload("sink%d" % idx, 700 + idx, q_lens, ok_lens,
+                                  Hq, Hkv, D, BS, num_splits=splits)
+    dev = cuda_device
+    b = DeviceBatch(wl, dev)
+    b.write_context()
+    b.write_new()
+    lens = np.array(seq_lens, np.int32)          # may be below q_len
+    b.seqused_k.copy_(torch.from_numpy(lens))
+    sinks = torch.linspace(-1.0, 2.0, Hq, dtype=torch.float32)
+    api.set_prefill_kernel(api.PREFILL_TCGEN05 if kern == "tcgen05"
+                           else api.PREFILL_MMA_SYNC)
+    try:
+        out, lse = api.flash_attn_varlen_func(
+            b.q, b.key_cache, b.value_cache, wl.max_seqlen_q, b.cu_seqlens_q,
+            wl.max_seqlen_k, seqused_k=b.seqused_k,
+            softmax_scale=wl.softmax_scale, causal=True,
+            block_table=b.block_table, return_softmax_lse=True,
+            num_splits=splits, s_aux=sinks.to(dev))
+        torch.cuda.synchronize()
+    finally:
+        api.set_prefill_kernel(api.PREFILL_TCGEN05)
+    wl2 = dataclasses.replace(wl, seq_lens=lens)
+    kc = np.full(wl.cache_shape()[1:], np.nan)
+    vc = np.full(wl.cache_shape()[1:], np.nan)
+    reshape_and_cache_ref(_f64(wl.k_ctx), _f64(wl.v_ctx), kc, vc,
+                          wl.slot_mapping_ctx)
+    reshape_and_cache_ref(_f64(wl.k_new), _f64(wl.v_new), kc, vc,
+                          wl.slot_mapping_new)
+    ro, rl = paged_attention_ref(_f64(wl.q), kc, vc, wl2.cu_seqlens_q,
+                                 lens, wl.block_table, wl.softmax_scale,
+                                 sinks=sinks.double().numpy())
+    assert_close(wl, out.float().cpu().numpy(), lse.cpu().numpy(), ro, rl,
+                 "sinks %d" % idx)
+
+
+def test_cascade_with_sinks(cuda_device):
+    from oracle import cascade_ref
+    wl = workloads.cascade_decode(batch=9, prefix=128, unique=70)
+    dev = cuda_device
+    b = DeviceBatch(wl, dev, cascade=True)
+    b.write_context()
+    b.write_new()
+    sinks = torch.linspace(0.5, -0.5, wl.num_heads, dtype=torch.float32)
+    api.cascade_attention(
+        b.out, b.q, b.key_cache, b.value_cache, b.cu_seqlens_q,
+        wl.max_seqlen_q, b.cu_prefix, b.prefix_lens, b.suffix_lens,
+        wl.max_seqlen_k, wl.softmax_scale, None, (-1, -1), 0.0,
+        b.block_table, wl.common_prefix_len, 0, s_aux=sinks.to(dev))
+    torch.cuda.synchronize()
+    from oracle.harness import _f64
+    from oracle import reshape_and_cache_ref
+    kc = np.full(wl.cache_shape()[1:], np.nan)
+    vc = np.full(wl.cache_shape()[1:], np.nan)
+    reshape_and_cache_ref(_f64(wl.k_ctx), _f64(wl.v_ctx), kc, vc,
+                          wl.slot_mapping_ctx)
+    reshape_and_cache_ref(_f64(wl.k_new), _f64(wl.v_new), kc, vc,
+                          wl.slot_mapping_new)
+    ro, _ = cascade_ref(_f64(wl.q), kc, vc, wl.cu_seqlens_q, wl.seq_lens,
+                        wl.block_table, wl.common_prefix_len,
+                        wl.softmax_scale, sinks=sinks.double().numpy())
+    assert_close(wl, b.out.float().cpu().numpy(), None, ro, None,
+                 "cascade sinks")

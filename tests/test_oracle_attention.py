@@ -290,3 +290,42 @@ def test_poison_never_reaches_output():
     assert np.isnan(kc).any()
     out, lse = paged_attention_ref(q, kc, vc, cu, su, table, 0.5)
     assert np.isfinite(out).all() and np.isfinite(lse).all()
+
+
+# ------------------------------------------------------------ attention sinks
+
+def test_sink_closed_form_identical_keys():
+    """n identical keys with logit s and a sink z: out = n e^s v / (n e^s +
+    e^z), lse = ln(n e^s + e^z)."""
+    q, k_row, kc, vc, table, cu, su = _identical_keys_case(1, 6)
+    out0, lse0 = paged_attention_ref(q, kc, vc, cu, su, table, 0.5)
+    z = 0.7
+    out, lse = paged_attention_ref(q, kc, vc, cu, su, table, 0.5,
+                                   sinks=np.array([z]))
+    s = 0.5 * float(q[0, 0] @ k_row[0, 0])
+    n = 6
+    assert lse[0, 0] == pytest.approx(math.log(n * math.exp(s) + math.exp(z)),
+                                      abs=1e-12)
+    frac = n * math.exp(s) / (n * math.exp(s) + math.exp(z))
+    np.testing.assert_allclose(out[0, 0], frac * out0[0, 0], atol=1e-13)
+
+
+def test_sink_limits_and_empty_rows():
+    rng = np.random.default_rng(21)
+    q, ks, vs, kc, vc, table, cu, su = random_case(rng, [2, 3], [0, 9], 4, 2,
+                                                   8)
+    base = paged_attention_ref(q, kc, vc, cu, su, table, 0.4)
+    off = paged_attention_ref(q, kc, vc, cu, su, table, 0.4,
+                              sinks=np.full(4, -1e300))
+    np.testing.assert_allclose(off[0], base[0], atol=1e-14)
+    np.testing.assert_allclose(off[1][:, 2:], base[1][:, 2:], atol=1e-14)
+    sinks = np.array([0.5, -1.0, 2.0, 0.0])
+    out, lse = paged_attention_ref(q, kc, vc, cu, su, table, 0.4,
+                                   sinks=sinks)
+    # request 0 has no keys: out 0, lse = the sink
+    assert np.all(out[:2] == 0)
+    np.testing.assert_allclose(lse[:, :2], np.repeat(sinks[:, None], 2, 1))
+    # a huge sink swallows the whole row
+    big = paged_attention_ref(q, kc, vc, cu, su, table, 0.4,
+                              sinks=np.full(4, 1e3))
+    assert np.abs(big[0]).max() < 1e-300

@@ -133,3 +133,28 @@ def test_log2_lse_conversion():
     x = np.random.default_rng(3).standard_normal(17) * 4
     lse2 = np.log2(np.sum(np.exp2(x * math.log2(math.e))))
     assert lse_log2_to_ln(lse2) == pytest.approx(logsumexp(x), abs=1e-12)
+
+
+def test_cascade_with_sinks_on_prefix_equals_flat_with_sinks():
+    """vLLM v1 cascade_attention passes s_aux to the prefix call only; its
+    effect reaches the output through the merged LSE."""
+    n = 9
+    wl = workloads.build_workload("cs", 11, [1] * n, [12 + i for i in
+                                                     range(n)], 4, 2, 8, 4,
+                                  shared_prefix_len=8)
+    from oracle import reshape_and_cache_ref
+    kc = np.full(wl.cache_shape()[1:], np.nan)
+    vc = np.full(wl.cache_shape()[1:], np.nan)
+    f64 = lambda t: t.double().numpy()      # noqa: E731
+    reshape_and_cache_ref(f64(wl.k_ctx), f64(wl.v_ctx), kc, vc,
+                          wl.slot_mapping_ctx)
+    reshape_and_cache_ref(f64(wl.k_new), f64(wl.v_new), kc, vc,
+                          wl.slot_mapping_new)
+    sinks = np.array([0.3, -0.2, 1.5, 0.0])
+    q = f64(wl.q)
+    flat = paged_attention_ref(q, kc, vc, wl.cu_seqlens_q, wl.seq_lens,
+                               wl.block_table, 0.4, sinks=sinks)
+    casc = cascade_ref(q, kc, vc, wl.cu_seqlens_q, wl.seq_lens,
+                       wl.block_table, 8, 0.4, sinks=sinks)
+    np.testing.assert_allclose(casc[0], flat[0], atol=1e-13)
+    np.testing.assert_allclose(casc[1], flat[1], atol=1e-13)
