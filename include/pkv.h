@@ -184,7 +184,29 @@ PKV_API pkv_status pkv_paged_attention_varlen(
  */
 typedef struct {
   const float* sinks;
+  /* kv_cache_fp8 != 0: key_cache/value_cache hold E4M3 ("fn") codes, one
+   * byte per element (cache_strides in bytes), and a cached value reads back
+   * as code * (*k_scale) or code * (*v_scale) (device float scalars, the
+   * same ones given to pkv_reshape_and_cache).  Source: "vllm/v1/attention/
+   * backends/flash_attn.py", FlashAttentionImpl.forward (kv_cache_dtype
+   * "fp8", k_descale / v_descale = layer._k_scale / _v_scale); the FlashInfer
+   * page's _trtllm_prefill_attn_kvfp8_dequant (value = fp8 * scale).
+   * Decode-class requests read the fp8 pages directly; prefill-class
+   * requests read them through a 16-bit copy in the workspace.  head_size
+   * must be a multiple of 16 and cache rows 16-byte aligned. */
+  int kv_cache_fp8;
+  const float* k_scale;
+  const float* v_scale;
 } pkv_attention_options;
+
+/* Workspace bytes for pkv_paged_attention_varlen_opts with these options
+ * (an fp8 cache with prefill-class requests needs room for 16-bit copies of
+ * up to batch * max_blocks_per_seq pages).  (size_t)-1 on bad arguments. */
+PKV_API size_t pkv_paged_attention_workspace_size_opts(
+    int batch, int total_q, int max_seqlen_q, int max_seqlen_k,
+    int num_heads, int num_kv_heads, int head_size, int block_size,
+    int causal, int window_left, int window_right, int num_splits,
+    int max_blocks_per_seq, const pkv_attention_options* opts);
 
 /* pkv_paged_attention_varlen with options (see pkv_attention_options). */
 PKV_API pkv_status pkv_paged_attention_varlen_opts(

@@ -43,7 +43,11 @@ i32, i64, f32, sz = ctypes.c_int, ctypes.c_int64, ctypes.c_float, \
 
 class _Options(ctypes.Structure):
     """pkv_attention_options (include/pkv.h)."""
-    _fields_ = [("sinks", ctypes.c_void_p)]
+    _fields_ = [("sinks", ctypes.c_void_p), ("kv_cache_fp8", ctypes.c_int),
+                ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p)]
+
+
+_FP8_CACHE = (torch.float8_e4m3fn, torch.uint8)
 
 
 class PkvError(RuntimeError):
@@ -86,6 +90,9 @@ def load_library():
         lib.pkv_paged_attention_varlen_opts.restype = i32
         lib.pkv_paged_attention_varlen_opts.argtypes = \
             lib.pkv_paged_attention_varlen.argtypes + [vp]
+        lib.pkv_paged_attention_workspace_size_opts.restype = sz
+        lib.pkv_paged_attention_workspace_size_opts.argtypes = [i32] * 13 + [
+            vp]
         lib.pkv_paged_attention_workspace_size.restype = sz
         lib.pkv_paged_attention_workspace_size.argtypes = [i32] * 12
         lib.pkv_merge_attn_states.restype = i32
@@ -182,6 +189,13 @@ def reshape_and_cache_flash(key, value, key_cache, value_cache, slot_mapping,
         raise ValueError("key/value head_size dim must be contiguous")
     if key.dtype != key_cache.dtype and kv_cache_dtype == "auto":
         raise ValueError("cache dtype must match key dtype for 'auto'")
+    if kv_cache_dtype.startswith("fp8"):
+        if key_cache.dtype not in _FP8_CACHE:
+            raise ValueError("an fp8 cache must be float8_e4m3fn or uint8")
+        if k_scale is None or v_scale is None or \
+                k_scale.dtype != torch.float32 or \
+                v_scale.dtype != torch.float32:
+            raise ValueError("fp8 cache needs float32 k_scale and v_scale")
     NB, BS, H, D = key_cache.shape
     cs = _cache_strides(key_cache, value_cache)
     _check(lib.pkv_reshape_and_cache(
@@ -212,7 +226,8 @@ def flash_attn_varlen_func(q, k, v, max_seqlen_q, cu_seqlens_q, max_seqlen_k,
                            window_size=(-1, -1), softcap=0.0,
                            alibi_slopes=None, block_table=None,
                            return_softmax_lse=False, out=None, num_splits=0,
-                           cu_seqlens_k=None, workspace=None, s_aux=None):
+                           cu_seqlens_k=None, workspace=None, s_aux=None,
+                           k_descale=None, v_descale=None):
     """Varlen attention over a paged KV cache.
 
     q [T, Hq, D]; k, v: cache views [num_blocks, block_size, Hkv, D];
@@ -232,7 +247,12 @@ def flash_attn_varlen_func(q, k, v, max_seqlen_q, cu_seqlens_q, max_seqlen_k,
     NB, BS, Hkv, Dk = k.shape
     if Dk != D:
         raise ValueError("q and cache head_size differ")
-    if k.dtype != q.dtype or v.dtype != q.dtype:
+    kv8 = k.dtype in _FP8_CACHE
+    if kv8:
+        if v.dtype not in _FP8_CACHE or k_descale is None or \
+                v_descale is None:
+            raise ValueError("an fp8 cache needs k_descale and v_descale")
+    elif k.dtype != q.dtype or v.dtype != q.dtype:
         raise NotImplementedError("q and cache dtypes must match")
     if cu_seqlens_q.dtype != torch.int32 or seqused_k.dtype != torch.int32 \
             or block_table.dtype != torch.int32:
@@ -248,9 +268,24 @@ def flash_attn_varlen_func(q, k, v, max_seqlen_q, cu_seqlens_q, max_seqlen_k,
     lse = None
     if return_softmax_lse:
         lse = torch.empty((Hq, T), dtype=torch.float32, device=q.device)
-    ws_need = paged_attention_workspace_size(
-        batch, T, max_seqlen_q, max_seqlen_k, Hq, Hkv, D, BS, causal,
-        window_size, num_splits)
+    opts = _Options()
+    if s_aux is not None:
+        if s_aux.dtype != torch.float32 or s_aux.shape != (Hq,):
+            raise ValueError("s_aux (sinks) must be float32 [num_heads]")
+        opts.sinks = s_aux.data_ptr()
+    if kv8:
+        for t in (k_descale, v_descale):
+            if t.dtype != torch.float32 or t.numel() < 1:
+                raise ValueError("k_descale/v_descale must be float32")
+        opts.kv_cache_fp8 = 1
+        opts.k_scale = k_descale.data_ptr()
+        opts.v_scale = v_descale.data_ptr()
+    ws_need = load_library().pkv_paged_attention_workspace_size_opts(
+        batch, T, max_seqlen_q, max_seqlen_k, Hq, Hkv, D, BS,
+        int(bool(causal)), int(window_size[0]), int(window_size[1]),
+        num_splits, block_table.shape[1], ctypes.byref(opts))
+    if ws_need == ctypes.c_size_t(-1).value:
+        raise ValueError(load_library().pkv_last_error().decode())
     if workspace is None and ws_need > 0:
         workspace = torch.empty(ws_need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * \
@@ -258,11 +293,6 @@ def flash_attn_varlen_func(q, k, v, max_seqlen_q, cu_seqlens_q, max_seqlen_k,
     cs = _cache_strides(k, v)
     if alibi_slopes is not None and alibi_slopes.dtype != torch.float32:
         raise ValueError("alibi_slopes must be float32")
-    opts = None
-    if s_aux is not None:
-        if s_aux.dtype != torch.float32 or s_aux.shape != (Hq,):
-            raise ValueError("s_aux (sinks) must be float32 [num_heads]")
-        opts = _Options(sinks=s_aux.data_ptr())
     _check(lib.pkv_paged_attention_varlen_opts(
         _ptr(q), q.stride(0), q.stride(1), _ptr(k), _ptr(v), cs, _ptr(out),
         out.stride(0), out.stride(1), _ptr(cu_seqlens_q), _ptr(seqused_k),
@@ -271,7 +301,7 @@ def flash_attn_varlen_func(q, k, v, max_seqlen_q, cu_seqlens_q, max_seqlen_k,
         float(softmax_scale), int(bool(causal)), int(window_size[0]),
         int(window_size[1]), float(softcap or 0.0), _ptr(alibi_slopes),
         int(num_splits), _ptr(lse), _ptr(workspace), ws_bytes, _dtype(q),
-        _stream(q), None if opts is None else ctypes.byref(opts)))
+        _stream(q), ctypes.byref(opts)))
     if return_softmax_lse:
         return out, lse
     return out

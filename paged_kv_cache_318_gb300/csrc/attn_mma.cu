@@ -45,7 +45,8 @@
 
 namespace pkv {
 
-template <int D, int ROW_WARPS, int KEY_WARPS, int KT, int STAGES>
+template <int D, int ROW_WARPS, int KEY_WARPS, int KT, int STAGES,
+          bool KV8 = false>
 struct MmaCfg {
   static constexpr int NW = ROW_WARPS * KEY_WARPS;
   static constexpr int NT = NW * 32;
@@ -59,11 +60,17 @@ struct MmaCfg {
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
   static constexpr int COMBINE_BYTES =
       KEY_WARPS > 1 ? KEY_WARPS * 16 * (D + 2) * 4 : 0;
-  static constexpr int SMEM = Q_BYTES + STAGES * STAGE_BYTES;
+  // fp8 cache: stages hold E4M3 tiles (1 byte per element); each tile is
+  // converted into one 16-bit K/V work tile before the MMAs read it
+  static constexpr int CPR8 = D / 16;         // 16-byte fp8 chunks per row
+  static constexpr int STAGE8_BYTES = 2 * KT * D;
+  static constexpr int RING_BYTES = KV8 ? STAGES * STAGE8_BYTES + STAGE_BYTES
+                                        : STAGES * STAGE_BYTES;
+  static constexpr int SMEM = Q_BYTES + RING_BYTES;
   static_assert(KW % 16 == 0, "each warp needs whole k16 steps of keys");
   static_assert(D % 64 == 0 || D == 64, "swizzle needs >= 8 chunks per row");
   static_assert(KEY_WARPS == 1 || ROW_WARPS == 1, "one split axis per CTA");
-  static_assert(COMBINE_BYTES <= STAGES * STAGE_BYTES, "combine buffer");
+  static_assert(COMBINE_BYTES <= RING_BYTES, "combine buffer");
 };
 
 // Byte offset of 16-byte chunk `ch` of row `r` in a swizzled tile.
@@ -72,10 +79,27 @@ __device__ __forceinline__ uint32_t swz(int r, int ch) {
   return static_cast<uint32_t>(r * ROW_BYTES + ((ch ^ (r & 7)) << 4));
 }
 
-template <typename T, int D, int ROW_WARPS, int KEY_WARPS, int KT, int STAGES>
+// Two E4M3 codes (low byte first) -> two 16-bit values of type T (exact).
+template <typename T>
+__device__ __forceinline__ uint32_t e4m3x2_to(uint16_t v);
+template <>
+__device__ __forceinline__ uint32_t e4m3x2_to<__half>(uint16_t v) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(v));
+  return h;
+}
+template <>
+__device__ __forceinline__ uint32_t e4m3x2_to<__nv_bfloat16>(uint16_t v) {
+  const uint32_t h = e4m3x2_to<__half>(v);
+  const __half2 hh = *reinterpret_cast<const __half2*>(&h);
+  return pack2<__nv_bfloat16>(__low2float(hh), __high2float(hh));
+}
+
+template <typename T, int D, int ROW_WARPS, int KEY_WARPS, int KT, int STAGES,
+          bool KV8 = false>
 __global__ void __launch_bounds__(32 * ROW_WARPS * KEY_WARPS)
 attn_mma_kernel(const AttnParams p) {
-  using C = MmaCfg<D, ROW_WARPS, KEY_WARPS, KT, STAGES>;
+  using C = MmaCfg<D, ROW_WARPS, KEY_WARPS, KT, STAGES, KV8>;
   extern __shared__ __align__(128) unsigned char smem[];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -163,6 +187,29 @@ attn_mma_kernel(const AttnParams p) {
     const int kt = lo + it * KT;
     const int jb0 = page_index(kt);
     const int* pg = s_pg[it % RING];
+    if constexpr (KV8) {
+      // E4M3 rows, D bytes each, unswizzled (read once by the converter)
+      const uint32_t sK8 = sKV_u + stage * C::STAGE8_BYTES;
+      const uint32_t sV8 = sK8 + KT * D;
+      const unsigned char* K8 = static_cast<const unsigned char*>(p.kc);
+      const unsigned char* V8 = static_cast<const unsigned char*>(p.vc);
+#pragma unroll 4
+      for (int i = tid; i < KT * C::CPR8; i += C::NT) {
+        const int r = i / C::CPR8, ch = i - (i / C::CPR8) * C::CPR8;
+        const int j = kt + r;
+        const int jb = page_index(j);
+        const int blk = j < L_tab ? pg[jb - jb0] : -1;
+        const bool ok = blk >= 0;
+        int64_t off = 0;
+        if (ok)
+          off = static_cast<int64_t>(blk) * p.c_sb +
+                static_cast<int64_t>(j - jb * p.BS) * p.c_sr +
+                static_cast<int64_t>(g) * p.c_sh + ch * 16;
+        cp_async_16(sK8 + r * D + ch * 16, K8 + off, ok ? 16 : 0);
+        cp_async_16(sV8 + r * D + ch * 16, V8 + off, ok ? 16 : 0);
+      }
+      return;
+    }
     const uint32_t sK = sKV_u + stage * C::STAGE_BYTES;
     const uint32_t sV = sK + C::TILE_BYTES;
 #pragma unroll 4
@@ -208,7 +255,12 @@ attn_mma_kernel(const AttnParams p) {
     if (okB) slopeB = p.alibi[g * G + rB % G];
   }
   const bool plain = (p.softcap <= 0.f) && (p.alibi == nullptr);
-  const float scale_log2 = p.scale * kLog2e;
+  // fp8 cache: value = code * scale, so k_scale joins the logit scale and
+  // v_scale multiplies the output
+  const float kscale = p.k_scale ? *p.k_scale : 1.f;
+  const float vscale = p.v_scale ? *p.v_scale : 1.f;
+  const float qk_scale = p.scale * kscale;
+  const float scale_log2 = qk_scale * kLog2e;
   // keys every valid row of this CTA admits: tiles inside [full_lo,
   // full_hi) skip the per-key mask (rows past row_end are never stored)
   int full_lo = lo, full_hi = hi;
@@ -237,8 +289,40 @@ attn_mma_kernel(const AttnParams p) {
       cp_async_commit();
     }
     const int stage = it % STAGES;
-    const uint32_t sK = sKV_u + stage * C::STAGE_BYTES;
-    const uint32_t sV = sK + C::TILE_BYTES;
+    uint32_t sK = sKV_u + stage * C::STAGE_BYTES;
+    uint32_t sV = sK + C::TILE_BYTES;
+    if constexpr (KV8) {
+      // E4M3 stage -> 16-bit work tile (exact; the scales are applied to
+      // the logits and to the output instead)
+      const uint32_t sK8 = sKV_u + stage * C::STAGE8_BYTES;
+      const uint32_t sW = sKV_u + STAGES * C::STAGE8_BYTES;
+      for (int i = tid; i < 2 * KT * C::CPR8; i += C::NT) {
+        const int mat = i / (KT * C::CPR8);
+        const int rem = i - mat * (KT * C::CPR8);
+        const int r = rem / C::CPR8, ch = rem - (rem / C::CPR8) * C::CPR8;
+        uint4 raw;
+        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(raw.x), "=r"(raw.y), "=r"(raw.z), "=r"(raw.w)
+                     : "r"(sK8 + mat * KT * D + r * D + ch * 16));
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          o[2 * q] = e4m3x2_to<T>(static_cast<uint16_t>(w[q] & 0xFFFF));
+          o[2 * q + 1] = e4m3x2_to<T>(static_cast<uint16_t>(w[q] >> 16));
+        }
+        const uint32_t dst = sW + mat * C::TILE_BYTES;
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
+                         dst + swz<C::ROW_BYTES>(r, 2 * ch)),
+                     "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3]));
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
+                         dst + swz<C::ROW_BYTES>(r, 2 * ch + 1)),
+                     "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7]));
+      }
+      __syncthreads();
+      sK = sW;
+      sV = sW + C::TILE_BYTES;
+    }
     const int kw0 = wkey * C::KW;          // first key of this warp in tile
     const int kt = lo + it * KT;
 
@@ -289,7 +373,7 @@ attn_mma_kernel(const AttnParams p) {
         if (plain) {
           x *= scale_log2;
         } else {
-          x *= p.scale;
+          x *= qk_scale;
           if (p.softcap > 0.f) x = p.softcap * tanhf(x / p.softcap);
           if (p.alibi) x -= (rowB ? slopeB : slopeA) * fabsf(float(pos - key));
           x *= kLog2e;
@@ -376,6 +460,7 @@ attn_mma_kernel(const AttnParams p) {
       const int tok = q0 + r / G, h = g * G + r % G;
       float inv, lse;   // a sink enters once: here, or in the split combine
       finish_row(m, l, split ? nullptr : p.sinks, h, &inv, &lse);
+      inv *= vscale;
       if (!split) {
         T* dst = OUT + static_cast<int64_t>(tok) * p.o_st +
                  static_cast<int64_t>(h) * p.o_sh;
@@ -441,6 +526,7 @@ attn_mma_kernel(const AttnParams p) {
       const int tok = q0 + R / G, h = g * G + R % G;
       float inv, lse;   // a sink enters once: here, or in the split combine
       finish_row(M, lsum, split ? nullptr : p.sinks, h, &inv, &lse);
+      inv *= vscale;
       if (!split) {
         T* dst = OUT + static_cast<int64_t>(tok) * p.o_st +
                  static_cast<int64_t>(h) * p.o_sh + c;
@@ -536,11 +622,12 @@ split_combine_kernel(const CombineParams p) {
 
 // ------------------------------------------------------------------ launch
 
-template <typename T, int D, int RW, int KWp, int KT, int ST>
+template <typename T, int D, int RW, int KWp, int KT, int ST,
+          bool KV8 = false>
 static cudaError_t launch_cfg(const AttnParams& p, dim3 grid,
                               cudaStream_t stream) {
-  using C = MmaCfg<D, RW, KWp, KT, ST>;
-  auto kern = attn_mma_kernel<T, D, RW, KWp, KT, ST>;
+  using C = MmaCfg<D, RW, KWp, KT, ST, KV8>;
+  auto kern = attn_mma_kernel<T, D, RW, KWp, KT, ST, KV8>;
   static bool attr_set = false;   // per instantiation; idempotent if racing
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(
@@ -556,6 +643,14 @@ static cudaError_t launch_cfg(const AttnParams& p, dim3 grid,
 template <typename T>
 static cudaError_t decode_dispatch(const AttnParams& p, int D, dim3 grid,
                                    cudaStream_t s) {
+  if (p.kv_fp8) {
+    switch (D) {
+      case 64:  return launch_cfg<T, 64, 1, 4, kDecodeKT, 4, true>(p, grid, s);
+      case 128: return launch_cfg<T, 128, 1, 4, kDecodeKT, 2, true>(p, grid, s);
+      case 256: return launch_cfg<T, 256, 1, 2, 32, 2, true>(p, grid, s);
+      default:  return cudaErrorInvalidValue;
+    }
+  }
   switch (D) {
     case 64:  return launch_cfg<T, 64, 1, 4, kDecodeKT, 4>(p, grid, s);
     case 128: return launch_cfg<T, 128, 1, 4, kDecodeKT, PKV_DECODE_STAGES_D128>(p, grid, s);

@@ -141,6 +141,13 @@ Plan make_plan(int batch, int total_q, int max_q, int max_k, int Hq, int Hkv,
   return pl;
 }
 
+// fp8 cache with prefill-class requests: 16-bit copies of up to
+// batch * max_blocks pages (K and V) plus their block table.
+size_t fp8_mock_bytes(int batch, int max_blocks, int BS, int Hkv, int D) {
+  const size_t pages = static_cast<size_t>(batch) * max_blocks;
+  return 2 * align256(pages * BS * Hkv * D * 2) + align256(pages * 4);
+}
+
 pkv_status check_attn_shape(int batch, int total_q, int max_q, int max_k,
                             int Hq, int Hkv, int D, int BS, int num_splits) {
   if (batch < 0 || total_q < 0 || max_q < 0 || max_k < 0)
@@ -219,11 +226,17 @@ pkv_status pkv_reshape_and_cache(
     int head_size, int block_size, int64_t num_blocks, pkv_dtype dtype,
     const char* kv_cache_dtype, const float* k_scale, const float* v_scale,
     pkv_stream_t stream) {
-  (void)k_scale;
-  (void)v_scale;
-  if (kv_cache_dtype && strcmp(kv_cache_dtype, "auto") != 0)
-    return fail(PKV_ERR_UNSUPPORTED, "kv_cache_dtype '%s' is not supported",
-                kv_cache_dtype);
+  bool fp8 = false;
+  if (kv_cache_dtype && strcmp(kv_cache_dtype, "auto") != 0) {
+    if (strcmp(kv_cache_dtype, "fp8") == 0 ||
+        strcmp(kv_cache_dtype, "fp8_e4m3") == 0)
+      fp8 = true;
+    else
+      return fail(PKV_ERR_UNSUPPORTED, "kv_cache_dtype '%s' is not supported",
+                  kv_cache_dtype);
+  }
+  if (fp8 && (!k_scale || !v_scale))
+    return fail(PKV_ERR_INVALID_ARG, "fp8 cache needs k_scale and v_scale");
   if (dtype != PKV_F16 && dtype != PKV_BF16)
     return fail(PKV_ERR_UNSUPPORTED, "dtype must be fp16 or bf16");
   if (num_tokens < 0 || num_blocks < 0)
@@ -244,13 +257,53 @@ pkv_status pkv_reshape_and_cache(
   unsigned* err = nullptr;
   pkv_status st = device_info(&err, nullptr);
   if (st != PKV_OK) return st;
-  cudaError_t e = launch_cache_write(
-      key, value, k_stride_tok, k_stride_head, v_stride_tok, v_stride_head,
-      key_cache, value_cache, cache_strides, slot_mapping, num_tokens,
-      num_kv_heads, head_size, block_size, num_blocks, 2, err,
-      reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e;
+  if (fp8) {
+    auto a16 = [](const void* ptr, int64_t st, int64_t sh, int eb) {
+      return reinterpret_cast<uintptr_t>(ptr) % 16 == 0 &&
+             (st * eb) % 16 == 0 && (sh * eb) % 16 == 0;
+    };
+    if (!a16(key, k_stride_tok, k_stride_head, 2) ||
+        !a16(value, v_stride_tok, v_stride_head, 2) ||
+        reinterpret_cast<uintptr_t>(key_cache) % 8 != 0 ||
+        reinterpret_cast<uintptr_t>(value_cache) % 8 != 0 ||
+        cache_strides[0] % 8 || cache_strides[1] % 8 || cache_strides[2] % 8)
+      return fail(PKV_ERR_UNSUPPORTED,
+                  "fp8 cache write needs 16-byte aligned key/value rows and "
+                  "8-byte aligned cache rows");
+    e = launch_cache_write_fp8(
+        key, value, k_stride_tok, k_stride_head, v_stride_tok, v_stride_head,
+        key_cache, value_cache, cache_strides, slot_mapping, num_tokens,
+        num_kv_heads, head_size, block_size, num_blocks, dtype == PKV_BF16,
+        k_scale, v_scale, err, reinterpret_cast<cudaStream_t>(stream));
+  } else {
+    e = launch_cache_write(
+        key, value, k_stride_tok, k_stride_head, v_stride_tok, v_stride_head,
+        key_cache, value_cache, cache_strides, slot_mapping, num_tokens,
+        num_kv_heads, head_size, block_size, num_blocks, 2, err,
+        reinterpret_cast<cudaStream_t>(stream));
+  }
   if (e != cudaSuccess) return cuda_fail(e, "reshape_and_cache launch");
   return PKV_OK;
+}
+
+size_t pkv_paged_attention_workspace_size_opts(
+    int batch, int total_q, int max_seqlen_q, int max_seqlen_k, int num_heads,
+    int num_kv_heads, int head_size, int block_size, int causal,
+    int window_left, int window_right, int num_splits,
+    int max_blocks_per_seq, const pkv_attention_options* opts) {
+  const size_t base = pkv_paged_attention_workspace_size(
+      batch, total_q, max_seqlen_q, max_seqlen_k, num_heads, num_kv_heads,
+      head_size, block_size, causal, window_left, window_right, num_splits);
+  if (base == static_cast<size_t>(-1)) return base;
+  const bool fp8 = opts && opts->kv_cache_fp8;
+  const bool prefill =
+      static_cast<int64_t>(max_seqlen_q) * (num_heads / num_kv_heads) >
+      kDecodeRows;
+  if (!fp8 || !prefill || batch == 0) return base;
+  if (max_blocks_per_seq <= 0) return static_cast<size_t>(-1);
+  return align256(base) + fp8_mock_bytes(batch, max_blocks_per_seq,
+                                         block_size, num_kv_heads, head_size);
 }
 
 size_t pkv_paged_attention_workspace_size(int batch, int total_q,
@@ -326,12 +379,17 @@ pkv_status pkv_paged_attention_varlen_opts(
                 "block_table: need max_blocks_per_seq >= 1 and stride >= it");
   if (cache_strides[3] != 1)
     return fail(PKV_ERR_INVALID_ARG, "the head_size dim must be contiguous");
-  const int eb = 2;
+  const bool kv8 = opts && opts->kv_cache_fp8;
+  if (kv8 && (!opts->k_scale || !opts->v_scale))
+    return fail(PKV_ERR_INVALID_ARG, "fp8 cache needs k_scale and v_scale");
+  if (kv8 && head_size % 16 != 0)
+    return fail(PKV_ERR_UNSUPPORTED, "fp8 cache needs head_size % 16 == 0");
+  const int eb = 2, cb = kv8 ? 1 : 2;
   if (!aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache) ||
       !aligned16(out) || !stride16(q_stride_tok, eb) ||
       !stride16(q_stride_head, eb) || !stride16(o_stride_tok, eb) ||
-      !stride16(o_stride_head, eb) || !stride16(cache_strides[0], eb) ||
-      !stride16(cache_strides[1], eb) || !stride16(cache_strides[2], eb))
+      !stride16(o_stride_head, eb) || !stride16(cache_strides[0], cb) ||
+      !stride16(cache_strides[1], cb) || !stride16(cache_strides[2], cb))
     return fail(PKV_ERR_UNSUPPORTED,
                 "q/out/cache rows must start on 16-byte boundaries");
   const int wl = window_left < 0 ? -1 : window_left;
@@ -344,10 +402,17 @@ pkv_status pkv_paged_attention_varlen_opts(
   const Plan pl = make_plan(batch, total_q, max_seqlen_q, max_seqlen_k,
                             num_heads, num_kv_heads, head_size, causal, wl, wr,
                             num_splits, sms);
-  if (pl.workspace > 0) {
-    if (workspace_bytes < pl.workspace || !workspace)
+  size_t need = pl.workspace;
+  size_t mock_off = 0;
+  if (kv8 && pl.prefill) {
+    mock_off = align256(pl.workspace);
+    need = mock_off + fp8_mock_bytes(batch, max_blocks_per_seq, block_size,
+                                     num_kv_heads, head_size);
+  }
+  if (need > 0) {
+    if (workspace_bytes < need || !workspace)
       return fail(PKV_ERR_WORKSPACE_TOO_SMALL,
-                  "workspace of %zu bytes needed, %zu given", pl.workspace,
+                  "workspace of %zu bytes needed, %zu given", need,
                   workspace_bytes);
     if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
       return fail(PKV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
@@ -386,6 +451,9 @@ pkv_status pkv_paged_attention_varlen_opts(
   p.softcap = softcap;
   p.alibi = alibi_slopes;
   p.sinks = opts ? opts->sinks : nullptr;
+  p.kv_fp8 = kv8 ? 1 : 0;
+  p.k_scale = kv8 ? opts->k_scale : nullptr;
+  p.v_scale = kv8 ? opts->v_scale : nullptr;
   p.causal = causal ? 1 : 0;
   p.wl = wl;
   p.wr = wr;
@@ -439,6 +507,28 @@ pkv_status pkv_paged_attention_varlen_opts(
     f.chunk = 0;
     const int64_t prow = static_cast<int64_t>(max_seqlen_q) * p.G;
     cudaError_t e;
+    if (kv8) {
+      // 16-bit copies of the pages prefill-class requests read
+      const size_t pages = static_cast<size_t>(batch) * max_blocks_per_seq;
+      const size_t page_bytes =
+          static_cast<size_t>(block_size) * num_kv_heads * head_size * 2;
+      char* base_ptr = static_cast<char*>(workspace) + mock_off;
+      void* mk = base_ptr;
+      void* mv = base_ptr + align256(pages * page_bytes);
+      int32_t* mt = reinterpret_cast<int32_t*>(
+          base_ptr + 2 * align256(pages * page_bytes));
+      e = launch_fp8_dequant_pages(f, head_size, bf16, mk, mv, mt, s);
+      if (e != cudaSuccess) return cuda_fail(e, "fp8 page dequant launch");
+      f.kc = mk;
+      f.vc = mv;
+      f.c_sb = static_cast<int64_t>(block_size) * num_kv_heads * head_size;
+      f.c_sr = static_cast<int64_t>(num_kv_heads) * head_size;
+      f.c_sh = head_size;
+      f.block_table = mt;
+      f.bt_stride = max_blocks_per_seq;
+      f.num_blocks = static_cast<int64_t>(pages);
+      f.kv_fp8 = 0;          // 16-bit copies; k_scale / v_scale still apply
+    }
     if (g_prefill_kernel.load() == PKV_PREFILL_TCGEN05)
       e = launch_prefill_attn_tc(f, head_size, bf16,
                                  static_cast<int>((prow + 127) / 128), s);

@@ -177,6 +177,9 @@ struct AttnParams {
   float softcap;              // 0 = none
   const float* alibi;         // [Hq] or null
   const float* sinks;         // [Hq] sink logits (natural log) or null
+  int kv_fp8;                 // cache holds E4M3 codes (1 byte / element)
+  const float* k_scale;       // fp8: device scalar, value = code * scale
+  const float* v_scale;
   int causal, wl, wr;
   // which requests this launch owns: rows = q_b * G in [min_rows, max_rows]
   int min_rows, max_rows;
@@ -239,6 +242,18 @@ cudaError_t launch_cache_write(const void* key, const void* value,
                                int64_t num_tokens, int Hkv, int D, int BS,
                                int64_t num_blocks, int elem_bytes,
                                unsigned* err, cudaStream_t stream);
+
+cudaError_t launch_cache_write_fp8(const void* key, const void* value,
+                                   int64_t k_st, int64_t k_sh, int64_t v_st,
+                                   int64_t v_sh, void* kc, void* vc,
+                                   const int64_t* cs, const int64_t* slots,
+                                   int64_t num_tokens, int Hkv, int D, int BS,
+                                   int64_t num_blocks, bool bf16,
+                                   const float* k_scale, const float* v_scale,
+                                   unsigned* err, cudaStream_t stream);
+cudaError_t launch_fp8_dequant_pages(const AttnParams& p, int D, bool bf16,
+                                     void* mock_k, void* mock_v,
+                                     int32_t* mock_table, cudaStream_t stream);
 
 cudaError_t launch_decode_attn(const AttnParams& p, int D, bool bf16,
                                int grid_x, int grid_y, cudaStream_t stream);

@@ -105,6 +105,8 @@ struct TcParams {
   float scale, softcap;
   const float* alibi;
   const float* sinks;
+  const float* k_scale;   // fp8-sourced caches: value = code * scale
+  const float* v_scale;
   int causal, wl, wr;
   int min_rows;
   int batch;
@@ -326,8 +328,9 @@ __device__ __forceinline__ float tanh_fast(float x) {
 
 __device__ __forceinline__ float masked_logit(float s, int key, int pos,
                                               bool valid, int kmin, int kmax,
-                                              const TcParams& p, float slope) {
-  float x = s * p.scale;
+                                              const TcParams& p, float slope,
+                                              float qk_scale) {
+  float x = s * qk_scale;
   if (p.softcap > 0.f) x = p.softcap * tanh_fast(x / p.softcap);
   if (p.alibi) x -= slope * fabsf(float(pos - key));
   x *= kLog2e;
@@ -659,8 +662,12 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
     const int pos = ctx + (valid ? R / G : 0);
     const int h = g * G + (valid ? R % G : 0);
     const float slope = (p.alibi && valid) ? p.alibi[h] : 0.f;
-    const float scale_log2 = p.scale * kLog2e;
-    const float scale_over_cap = p.softcap > 0.f ? p.scale / p.softcap : 0.f;
+    // caches converted from fp8: k_scale joins the logit scale, v_scale
+    // multiplies the output
+    const float qk_scale = p.scale * (p.k_scale ? *p.k_scale : 1.f);
+    const float vscale = p.v_scale ? *p.v_scale : 1.f;
+    const float scale_log2 = qk_scale * kLog2e;
+    const float scale_over_cap = p.softcap > 0.f ? qk_scale / p.softcap : 0.f;
     const float cap_log2e = p.softcap * kLog2e;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     float m_ref = -INFINITY, l = 0.f;
@@ -702,7 +709,8 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
       } else {
 #pragma unroll
         for (int e = 0; e < BN; ++e) {
-          v[e] = masked_logit(v[e], kt + e, pos, valid, kmin, kmax, p, slope);
+          v[e] = masked_logit(v[e], kt + e, pos, valid, kmin, kmax, p, slope,
+                               qk_scale);
           mx8[e & 7] = fmaxf(mx8[e & 7], v[e]);
         }
       }
@@ -785,6 +793,7 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
       tc_fence_after();
       float inv, lse_v;
       finish_row(m_ref, l, p.sinks, h, &inv, &lse_v);
+      inv *= vscale;
       const int tok = q0 + (valid ? R / G : 0);
       T* dst = OUT + static_cast<int64_t>(tok) * p.o_st +
                static_cast<int64_t>(h) * p.o_sh;
@@ -1193,8 +1202,12 @@ prefill_pp_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
     const int h = g * G + (valid ? R % G : 0);
     const int tok = q0 + (valid ? R / G : 0);
     const float slope = (p.alibi && valid) ? p.alibi[h] : 0.f;
-    const float scale_log2 = p.scale * kLog2e;
-    const float scale_over_cap = p.softcap > 0.f ? p.scale / p.softcap : 0.f;
+    // caches converted from fp8: k_scale joins the logit scale, v_scale
+    // multiplies the output
+    const float qk_scale = p.scale * (p.k_scale ? *p.k_scale : 1.f);
+    const float vscale = p.v_scale ? *p.v_scale : 1.f;
+    const float scale_log2 = qk_scale * kLog2e;
+    const float scale_over_cap = p.softcap > 0.f ? qk_scale / p.softcap : 0.f;
     const float cap_log2e = p.softcap * kLog2e;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int kmin = x ? kmn[1] : kmn[0], kmax = x ? kmx[1] : kmx[0];
@@ -1241,7 +1254,8 @@ prefill_pp_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
       } else {
 #pragma unroll
         for (int e = 0; e < BN; ++e) {
-          v[e] = masked_logit(v[e], kt + e, pos, valid, kmin, kmax, p, slope);
+          v[e] = masked_logit(v[e], kt + e, pos, valid, kmin, kmax, p, slope,
+                               qk_scale);
           mx8[e & 7] = fmaxf(mx8[e & 7], v[e]);
         }
       }
@@ -1333,6 +1347,7 @@ prefill_pp_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
         tc_fence_after();
         float inv, lse_v;
         finish_row(m_ref, l, p.sinks, h, &inv, &lse_v);
+      inv *= vscale;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           float ov[32];
@@ -1446,6 +1461,8 @@ cudaError_t launch_prefill_attn_tc(const AttnParams& a, int D, bool bf16,
   p.softcap = a.softcap;
   p.alibi = a.alibi;
   p.sinks = a.sinks;
+  p.k_scale = a.k_scale;
+  p.v_scale = a.v_scale;
   p.causal = a.causal;
   p.wl = a.wl;
   p.wr = a.wr;

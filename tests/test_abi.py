@@ -66,12 +66,16 @@ def test_attention_empty_batch_is_noop(lib):
     assert _attn_call(lib, batch=0) == 0
 
 
-def test_cache_write_rejects_fp8_and_bad_block_size(lib):
+def test_cache_write_rejects_bad_kv_dtype_and_block_size(lib):
     cs = (ctypes.c_int64 * 4)(2048, 128, 16, 1)
     common = [None, None, 0, 0, 0, 0, None, None, cs, None, 4, 2, 64]
+    st = lib.pkv_reshape_and_cache(*common, 16, 8, 1, b"fp8_e5m2", None,
+                                   None, None)
+    assert st == 2 and b"fp8_e5m2" in lib.pkv_last_error()
+    # fp8 (E4M3) is supported but needs its scales
     st = lib.pkv_reshape_and_cache(*common, 16, 8, 1, b"fp8", None, None,
                                    None)
-    assert st == 2 and b"fp8" in lib.pkv_last_error()
+    assert st == 1 and b"scale" in lib.pkv_last_error()
     st = lib.pkv_reshape_and_cache(*common, 20, 8, 1, b"auto", None, None,
                                    None)
     assert st == 1
