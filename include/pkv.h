@@ -341,6 +341,23 @@ PKV_API pkv_status pkv_make_local_attention_virtual_batches(
     int32_t* seqlens_k_local, int32_t* block_table_local, int capacity);
 
 /*
+ * pkv_use_cascade_attention -- host policy: 1 if a batch whose requests share
+ * a common_prefix_len-token prefix should run cascade attention, else 0.
+ *
+ * Source: "vllm/v1/attention/backends/flash_attn.py", use_cascade_attention:
+ * off for a prefix < 256 tokens, < 8 requests, ALiBi, sliding window, local
+ * attention or DCP (dcp_world_size > 1); on when the plain call would not
+ * use split-KV decoding (GQA ratio 1 or any query_lens[i] != 1); otherwise
+ * on iff ceil(Hq * ceil(B/128) / SMs) * ceil(P/128) <
+ * ceil(B * Hkv * ceil(G/128) * ceil(P/128) / SMs).  query_lens: host int32
+ * [num_reqs].  Pure host arithmetic; no GPU work.
+ */
+PKV_API int pkv_use_cascade_attention(
+    int common_prefix_len, const int32_t* query_lens, int num_reqs,
+    int num_heads, int num_kv_heads, int use_alibi, int use_sliding_window,
+    int use_local_attention, int num_sms, int dcp_world_size);
+
+/*
  * pkv_check_device_errors -- synchronise `stream`, then read and clear the
  * library's device error word.  Returns PKV_OK, or PKV_ERR_BAD_INDEX when a
  * kernel since the last check met an out-of-range block id or slot (the

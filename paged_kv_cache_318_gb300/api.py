@@ -102,6 +102,8 @@ def load_library():
         lib.pkv_make_local_attention_virtual_batches.argtypes = [
             i32, vp, vp, i32, vp, i64, i32, i32, ctypes.POINTER(ctypes.c_int),
             vp, vp, vp, vp, i32]
+        lib.pkv_use_cascade_attention.restype = i32
+        lib.pkv_use_cascade_attention.argtypes = [i32, vp] + [i32] * 8
         lib.pkv_set_prefill_kernel.restype = i32
         lib.pkv_set_prefill_kernel.argtypes = [i32]
         lib.pkv_launch_count.restype = ctypes.c_uint64
@@ -338,6 +340,19 @@ def make_local_attention_virtual_batches(attn_chunk_size, query_start_loc,
         ctypes.byref(n), sq.ctypes.data_as(P), cu.ctypes.data_as(P),
         sk.ctypes.data_as(P), btl.ctypes.data_as(P), V))
     return sq, cu, sk, btl
+
+
+def use_cascade_attention(common_prefix_len, query_lens, num_query_heads,
+                          num_kv_heads, use_alibi, use_sliding_window,
+                          use_local_attention, num_sms, dcp_world_size=1):
+    """vLLM v1 ``use_cascade_attention`` policy (host, native)."""
+    import numpy as np
+    ql = np.ascontiguousarray(query_lens, dtype=np.int32)
+    return bool(load_library().pkv_use_cascade_attention(
+        int(common_prefix_len), ql.ctypes.data_as(ctypes.c_void_p), len(ql),
+        num_query_heads, num_kv_heads, int(bool(use_alibi)),
+        int(bool(use_sliding_window)), int(bool(use_local_attention)),
+        int(num_sms), int(dcp_world_size)))
 
 
 def merge_attn_states(output, prefix_output, prefix_lse, suffix_output,

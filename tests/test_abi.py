@@ -89,3 +89,25 @@ def test_merge_rejects_mixed_half_types(lib):
     st = lib.pkv_merge_attn_states(None, None, None, None, None, None, 4, 2,
                                    64, 0, 1, None)
     assert st == 2
+
+
+def test_native_cascade_policy_matches_oracle(lib):
+    import numpy as np
+    from oracle import use_cascade_attention_ref
+    from paged_kv_cache_318_gb300 import api
+    rng = np.random.default_rng(0)
+    for trial in range(400):
+        n = int(rng.integers(1, 300))
+        ql = np.ones(n, np.int32) if rng.random() < 0.7 else \
+            rng.integers(1, 4, size=n).astype(np.int32)
+        P = int(rng.choice([0, 100, 255, 256, 1024, 8192, 65536]))
+        hkv = int(rng.choice([1, 2, 8]))
+        hq = hkv * int(rng.choice([1, 2, 4, 8, 16]))
+        flags = [bool(rng.random() < 0.15) for _ in range(3)]
+        sms = int(rng.choice([132, 148, 152]))
+        want = use_cascade_attention_ref(P, ql, hq, hkv, *flags, sms)
+        got = api.use_cascade_attention(P, ql, hq, hkv, *flags, sms)
+        assert got == want, (trial, P, n, hq, hkv, flags, sms)
+    # DCP disables cascade
+    assert not api.use_cascade_attention(8192, np.ones(256), 64, 8, False,
+                                         False, False, 152, dcp_world_size=2)
