@@ -197,6 +197,36 @@ typedef struct {
   int kv_cache_fp8;
   const float* k_scale;
   const float* v_scale;
+  /* cu_seqlens_k != NULL selects non-paged (encoder) attention: the keys of
+   * request b are rows cu_seqlens_k[b] .. cu_seqlens_k[b+1]-1 of one K/V
+   * tensor of total_k rows, passed as key_cache / value_cache.  Its layout
+   * is [total_k, num_kv_heads, head_size] under cache_strides = {ignored,
+   * row stride, head stride, 1} (elements; 16-byte multiples), so a
+   * head-major [num_kv_heads, total_k, head_size] view works too.  The key
+   * count of request b is cu_seqlens_k[b+1] - cu_seqlens_k[b]; seqused_k,
+   * block_table, max_blocks_per_seq, block_size and num_blocks are ignored
+   * (may be NULL / 0).  Causal alignment, windows, softcap, ALiBi and sinks
+   * apply as in the paged call; an fp8 cache is rejected
+   * (PKV_ERR_UNSUPPORTED).  Rows outside [0, total_k) are never read: a
+   * request whose range leaves the tensor is clipped and the device error
+   * word records PKV_ERR_BAD_INDEX.  Source: "vllm/v1/attention/backends/
+   * flash_attn.py", FlashAttentionImpl._forward_encoder_attention (query,
+   * key and value of shape [num_encoder_tokens, heads, head_size];
+   * cu_seqlens_k = query_start_loc; bidirectional; no cache; fp8 rejected);
+   * the aphrodite-engine flash_attn.py page, prefill without a cache
+   * (cu_seqlens_k = seq_start_loc). */
+  const int32_t* cu_seqlens_k;
+  int total_k;
+  /* fixed_split_size > 0: batch-invariant split-KV.  Every decode-class
+   * request is cut into key ranges of fixed_split_size keys (rounded up to
+   * a multiple of 64) counted from the start of its own key range, whatever
+   * the rest of the batch is, and always goes through the split-combine
+   * path, so a request's output bits do not depend on the batch it shares
+   * a call with.  num_splits must then be 0.  Source: the FlashInfer
+   * backend page, FlashInferMetadataBuilder (decode_fixed_split_size 2048
+   * and prefill_fixed_split_size 4096 under batch invariance) and the
+   * flash_attn.py page (num_splits = 1 under vllm_is_batch_invariant). */
+  int fixed_split_size;
 } pkv_attention_options;
 
 /* Workspace bytes for pkv_paged_attention_varlen_opts with these options

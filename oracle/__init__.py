@@ -15,4 +15,5 @@ from .paged_attention import (  # noqa: F401
     paged_attention_ref,
     reshape_and_cache_ref,
     use_cascade_attention_ref,
+    varlen_attention_ref,
 )

@@ -13,14 +13,16 @@ cache scatter).  Sources, cited by page title and section:
   ``FlashAttentionMetadata`` (context/query/seq length note),
   ``FlashAttentionImpl.__init__`` (window tuple, soft-cap 0 = none, GQA ratio),
   ``FlashAttentionImpl.forward`` (cache write, varlen call, LSE return),
-  ``cascade_attention``, ``use_cascade_attention``.
+  ``FlashAttentionImpl._forward_encoder_attention`` (attention without a
+  cache), ``cascade_attention``, ``use_cascade_attention``.
 * "vllm.v1.attention.backends.flash_attn" (vLLM v0.9.0.1 API docs):
   ``FlashAttentionMetadataBuilder.build`` (slot_mapping tail filled with -1),
   ``make_local_attention_virtual_batches`` (worked example).
 * "flashinfer.py . tduncan/Nvidia-Optimization-Stack-VLLM": end-aligned causal
   mask note, base-2 LSE converted to natural log before merging.
 * "aphrodite-engine/aphrodite/attention/backends/flash_attn.py":
-  ``FlashAttentionMetadata`` block-table and seq_start_loc examples.
+  ``FlashAttentionMetadata`` block-table and seq_start_loc examples; the
+  cache-free prefill call (``cu_seqlens_k = seq_start_loc``).
 
 Readings taken where the pages are silent (each is listed in the design doc):
 
@@ -182,23 +184,67 @@ def paged_attention_ref(q, key_cache, value_cache, cu_seqlens_q, seqused_k,
             continue
         k_b = gather_ref(key_cache, block_table[b], k_len).astype(np.float64)
         v_b = gather_ref(value_cache, block_table[b], k_len).astype(np.float64)
-        ok = admissible_mask(q_len, k_len, causal, window_size)
-        for h in range(Hq):
-            g = h // group
-            slope = None if alibi_slopes is None else float(alibi_slopes[h])
-            s = attention_logits(q[t0:t1, h, :], k_b[:, g, :], q_len, k_len,
-                                 softmax_scale, softcap, slope)
-            s = np.where(ok, s, -np.inf)
-            m = s.max(axis=1, initial=-np.inf)
-            has = np.isfinite(m)
-            m_safe = np.where(has, m, 0.0)
-            w = np.exp(s - m_safe[:, None])          # masked entries -> 0
-            l = w.sum(axis=1)
-            row_lse = np.where(has, m_safe + np.log(np.where(has, l, 1.0)),
-                               -np.inf)
-            o = (w @ v_b[:, g, :]) / np.where(has, l, 1.0)[:, None]
-            out[t0:t1, h, :] = np.where(has[:, None], o, 0.0)
-            lse[h, t0:t1] = row_lse
+        _attend_request(q, t0, t1, k_b, v_b, group, softmax_scale, causal,
+                        window_size, softcap, alibi_slopes, out, lse)
+    if sinks is not None:
+        out, lse = add_sink_ref(out, lse, sinks)
+    return out, lse
+
+
+def _attend_request(q, t0, t1, k_b, v_b, group, softmax_scale, causal,
+                    window_size, softcap, alibi_slopes, out, lse):
+    """Softmax attention of queries t0..t1-1 over one request's key rows
+    k_b, v_b [k_len, Hkv, D]; writes out[t0:t1] and lse[:, t0:t1]."""
+    q_len, k_len = t1 - t0, k_b.shape[0]
+    ok = admissible_mask(q_len, k_len, causal, window_size)
+    for h in range(q.shape[1]):
+        g = h // group
+        slope = None if alibi_slopes is None else float(alibi_slopes[h])
+        s = attention_logits(q[t0:t1, h, :], k_b[:, g, :], q_len, k_len,
+                             softmax_scale, softcap, slope)
+        s = np.where(ok, s, -np.inf)
+        m = s.max(axis=1, initial=-np.inf)
+        has = np.isfinite(m)
+        m_safe = np.where(has, m, 0.0)
+        w = np.exp(s - m_safe[:, None])          # masked entries -> 0
+        l = w.sum(axis=1)
+        row_lse = np.where(has, m_safe + np.log(np.where(has, l, 1.0)),
+                           -np.inf)
+        o = (w @ v_b[:, g, :]) / np.where(has, l, 1.0)[:, None]
+        out[t0:t1, h, :] = np.where(has[:, None], o, 0.0)
+        lse[h, t0:t1] = row_lse
+
+
+def varlen_attention_ref(q, k, v, cu_seqlens_q, cu_seqlens_k, softmax_scale,
+                         causal=False, window_size=(-1, -1), softcap=0.0,
+                         alibi_slopes=None, sinks=None):
+    """Varlen attention over plain (non-paged) K/V rows; returns (out, lse).
+
+    vLLM v1 ``FlashAttentionImpl._forward_encoder_attention``: query, key and
+    value are [num_tokens, heads, head_size] with no cache, request b's keys
+    are rows ``cu_seqlens_k[b] .. cu_seqlens_k[b+1]-1`` (the encoder passes
+    ``cu_seqlens_k = query_start_loc`` and ``causal=False``); the aphrodite
+    page's cache-free prefill passes ``cu_seqlens_k = seq_start_loc`` with
+    ``causal=True``.  Every other rule is that of ``paged_attention_ref``.
+
+    q [T, Hq, D]; k, v [Tk, Hkv, D]; cu_seqlens_q, cu_seqlens_k [B+1].
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    T, Hq, D = q.shape
+    Hkv = k.shape[1]
+    assert Hq % Hkv == 0
+    out = np.zeros((T, Hq, D), dtype=np.float64)
+    lse = np.full((Hq, T), -np.inf, dtype=np.float64)
+    for b in range(len(cu_seqlens_q) - 1):
+        t0, t1 = int(cu_seqlens_q[b]), int(cu_seqlens_q[b + 1])
+        k0, k1 = int(cu_seqlens_k[b]), int(cu_seqlens_k[b + 1])
+        if t1 == t0:
+            continue
+        _attend_request(q, t0, t1, k[k0:k1], v[k0:k1], Hq // Hkv,
+                        softmax_scale, causal, window_size, softcap,
+                        alibi_slopes, out, lse)
     if sinks is not None:
         out, lse = add_sink_ref(out, lse, sinks)
     return out, lse

@@ -44,7 +44,9 @@ i32, i64, f32, sz = ctypes.c_int, ctypes.c_int64, ctypes.c_float, \
 class _Options(ctypes.Structure):
     """pkv_attention_options (include/pkv.h)."""
     _fields_ = [("sinks", ctypes.c_void_p), ("kv_cache_fp8", ctypes.c_int),
-                ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p)]
+                ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+                ("cu_seqlens_k", ctypes.c_void_p), ("total_k", ctypes.c_int),
+                ("fixed_split_size", ctypes.c_int)]
 
 
 _FP8_CACHE = (torch.float8_e4m3fn, torch.uint8)
@@ -229,44 +231,65 @@ def flash_attn_varlen_func(q, k, v, max_seqlen_q, cu_seqlens_q, max_seqlen_k,
                            alibi_slopes=None, block_table=None,
                            return_softmax_lse=False, out=None, num_splits=0,
                            cu_seqlens_k=None, workspace=None, s_aux=None,
-                           k_descale=None, v_descale=None):
-    """Varlen attention over a paged KV cache.
+                           k_descale=None, v_descale=None,
+                           fixed_split_size=0):
+    """Varlen attention over a paged KV cache, or over plain K/V rows.
 
-    q [T, Hq, D]; k, v: cache views [num_blocks, block_size, Hkv, D];
-    cu_seqlens_q int32 [B+1]; seqused_k int32 [B]; block_table int32
-    [B, max_blocks].  Returns out (and lse [Hq, T] float32 when
-    return_softmax_lse).
+    q [T, Hq, D].  Paged: k, v are cache views [num_blocks, block_size, Hkv,
+    D] with seqused_k int32 [B] and block_table int32 [B, max_blocks].
+    Non-paged (encoder / cache-free prefill): k, v are [Tk, Hkv, D] and
+    cu_seqlens_k int32 [B+1] gives each request's rows.  cu_seqlens_q int32
+    [B+1].  fixed_split_size > 0 makes decode split-KV batch-invariant.
+    Returns out (and lse [Hq, T] float32 when return_softmax_lse).
     """
     lib = load_library()
-    if cu_seqlens_k is not None:
-        raise NotImplementedError("non-paged varlen K/V (cu_seqlens_k) is not "
-                                  "supported; pass seqused_k + block_table")
-    if block_table is None or seqused_k is None:
-        raise ValueError("block_table and seqused_k are required")
+    nonpaged = cu_seqlens_k is not None
     if q.stride(-1) != 1:
         raise ValueError("q head_size dim must be contiguous")
     T, Hq, D = q.shape
-    NB, BS, Hkv, Dk = k.shape
+    if nonpaged:
+        if k.dim() != 3 or v.shape != k.shape:
+            raise ValueError("non-paged k and v must both be [Tk, Hkv, D]")
+        Tk, Hkv, Dk = k.shape
+        NB, BS = 1, 16
+        if cu_seqlens_k.dtype != torch.int32:
+            raise ValueError("cu_seqlens_k must be int32")
+        batch = cu_seqlens_k.shape[0] - 1
+        if cu_seqlens_q.shape[0] != batch + 1:
+            raise ValueError("cu_seqlens_q and cu_seqlens_k lengths differ")
+        if k.stride(1) != v.stride(1) or k.stride(0) != v.stride(0) or \
+                k.stride(2) != 1 or v.stride(2) != 1:
+            raise ValueError("k and v need the same strides, D contiguous")
+        cs = (ctypes.c_int64 * 4)(0, k.stride(0), k.stride(1), 1)
+        max_blocks, bt_stride = 0, 0
+    else:
+        if block_table is None or seqused_k is None:
+            raise ValueError("block_table and seqused_k are required")
+        NB, BS, Hkv, Dk = k.shape
+        if seqused_k.dtype != torch.int32 or block_table.dtype != torch.int32:
+            raise ValueError("seqused_k and block_table must be int32")
+        if block_table.stride(-1) != 1:
+            raise ValueError("block_table rows must be contiguous")
+        batch = seqused_k.shape[0]
+        cs = _cache_strides(k, v)
+        max_blocks, bt_stride = block_table.shape[1], block_table.stride(0)
     if Dk != D:
-        raise ValueError("q and cache head_size differ")
+        raise ValueError("q and k head_size differ")
     kv8 = k.dtype in _FP8_CACHE
     if kv8:
+        if nonpaged:
+            raise NotImplementedError("fp8 K/V needs the paged cache")
         if v.dtype not in _FP8_CACHE or k_descale is None or \
                 v_descale is None:
             raise ValueError("an fp8 cache needs k_descale and v_descale")
     elif k.dtype != q.dtype or v.dtype != q.dtype:
         raise NotImplementedError("q and cache dtypes must match")
-    if cu_seqlens_q.dtype != torch.int32 or seqused_k.dtype != torch.int32 \
-            or block_table.dtype != torch.int32:
-        raise ValueError("cu_seqlens_q, seqused_k and block_table must be "
-                         "int32")
-    if block_table.stride(-1) != 1:
-        raise ValueError("block_table rows must be contiguous")
+    if cu_seqlens_q.dtype != torch.int32:
+        raise ValueError("cu_seqlens_q must be int32")
     if softmax_scale is None:
         softmax_scale = D ** -0.5
     if out is None:
         out = torch.empty_like(q)
-    batch = seqused_k.shape[0]
     lse = None
     if return_softmax_lse:
         lse = torch.empty((Hq, T), dtype=torch.float32, device=q.device)
@@ -282,24 +305,27 @@ def flash_attn_varlen_func(q, k, v, max_seqlen_q, cu_seqlens_q, max_seqlen_k,
         opts.kv_cache_fp8 = 1
         opts.k_scale = k_descale.data_ptr()
         opts.v_scale = v_descale.data_ptr()
-    ws_need = load_library().pkv_paged_attention_workspace_size_opts(
+    if nonpaged:
+        opts.cu_seqlens_k = cu_seqlens_k.data_ptr()
+        opts.total_k = k.shape[0]
+    opts.fixed_split_size = int(fixed_split_size)
+    ws_need = lib.pkv_paged_attention_workspace_size_opts(
         batch, T, max_seqlen_q, max_seqlen_k, Hq, Hkv, D, BS,
         int(bool(causal)), int(window_size[0]), int(window_size[1]),
-        num_splits, block_table.shape[1], ctypes.byref(opts))
+        num_splits, max_blocks, ctypes.byref(opts))
     if ws_need == ctypes.c_size_t(-1).value:
-        raise ValueError(load_library().pkv_last_error().decode())
+        raise ValueError(lib.pkv_last_error().decode())
     if workspace is None and ws_need > 0:
         workspace = torch.empty(ws_need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * \
         workspace.element_size()
-    cs = _cache_strides(k, v)
     if alibi_slopes is not None and alibi_slopes.dtype != torch.float32:
         raise ValueError("alibi_slopes must be float32")
     _check(lib.pkv_paged_attention_varlen_opts(
         _ptr(q), q.stride(0), q.stride(1), _ptr(k), _ptr(v), cs, _ptr(out),
         out.stride(0), out.stride(1), _ptr(cu_seqlens_q), _ptr(seqused_k),
         batch, T, int(max_seqlen_q), int(max_seqlen_k), _ptr(block_table),
-        block_table.stride(0), block_table.shape[1], Hq, Hkv, D, BS, NB,
+        bt_stride, max_blocks, Hq, Hkv, D, BS, NB,
         float(softmax_scale), int(bool(causal)), int(window_size[0]),
         int(window_size[1]), float(softcap or 0.0), _ptr(alibi_slopes),
         int(num_splits), _ptr(lse), _ptr(workspace), ws_bytes, _dtype(q),

@@ -109,7 +109,8 @@ attn_mma_kernel(const AttnParams p) {
   // rows past total_q (a cu_seqlens_q beyond the caller's buffers) are
   // never read or written
   const int q_len = min(p.cu_q[b + 1] - q0, p.total_q - q0);
-  const int L = p.seqused_k[b];
+  const int koff = p.cu_k ? p.cu_k[b] : 0;      // non-paged: first key row
+  const int L = p.cu_k ? p.cu_k[b + 1] - koff : p.seqused_k[b];
   if (q0 < 0 || q_len <= 0) return;
   const int rows = q_len * G;
   if (rows < p.min_rows || rows > p.max_rows) return;
@@ -133,7 +134,9 @@ attn_mma_kernel(const AttnParams p) {
     if (hi < lo) hi = lo;
   }
   // Keys are only followed through the table while it has entries.
-  const int L_tab = min(L, p.max_blocks * p.BS);
+  // rows past the table (or, non-paged, past the K/V tensor) are not read
+  const int L_tab = p.cu_k ? (koff < 0 ? 0 : max(0, min(L, p.total_k - koff)))
+                           : min(L, p.max_blocks * p.BS);
   if (L_tab < L && tid == 0 && blockIdx.x == 0 && blockIdx.y == 0)
     atomicOr(p.err, kErrBadTable);
 
@@ -172,7 +175,7 @@ attn_mma_kernel(const AttnParams p) {
   auto page_index = [&](int j) { return bs_shift >= 0 ? (j >> bs_shift)
                                                        : j / p.BS; };
   auto fetch_id = [&](int t) -> int {           // id of page `tid` of tile t
-    if (t >= n_tiles || tid >= PPT) return -1;
+    if (t >= n_tiles || tid >= PPT || p.cu_k) return -1;
     const int kt = lo + t * KT;
     const int jb = page_index(kt) + tid;
     if (jb * p.BS >= min(L_tab, kt + KT)) return -1;
@@ -197,13 +200,13 @@ attn_mma_kernel(const AttnParams p) {
       for (int i = tid; i < KT * C::CPR8; i += C::NT) {
         const int r = i / C::CPR8, ch = i - (i / C::CPR8) * C::CPR8;
         const int j = kt + r;
-        const int jb = page_index(j);
-        const int blk = j < L_tab ? pg[jb - jb0] : -1;
+        const int jb = p.cu_k ? 0 : page_index(j);
+        const int blk = j < L_tab ? (p.cu_k ? 0 : pg[jb - jb0]) : -1;
         const bool ok = blk >= 0;
         int64_t off = 0;
         if (ok)
           off = static_cast<int64_t>(blk) * p.c_sb +
-                static_cast<int64_t>(j - jb * p.BS) * p.c_sr +
+                static_cast<int64_t>(p.cu_k ? koff + j : j - jb * p.BS) * p.c_sr +
                 static_cast<int64_t>(g) * p.c_sh + ch * 16;
         cp_async_16(sK8 + r * D + ch * 16, K8 + off, ok ? 16 : 0);
         cp_async_16(sV8 + r * D + ch * 16, V8 + off, ok ? 16 : 0);
@@ -216,13 +219,13 @@ attn_mma_kernel(const AttnParams p) {
     for (int i = tid; i < KT * C::CPR; i += C::NT) {
       const int r = i / C::CPR, ch = i - (i / C::CPR) * C::CPR;
       const int j = kt + r;
-      const int jb = page_index(j);
-      const int blk = j < L_tab ? pg[jb - jb0] : -1;
+      const int jb = p.cu_k ? 0 : page_index(j);
+      const int blk = j < L_tab ? (p.cu_k ? 0 : pg[jb - jb0]) : -1;
       const bool ok = blk >= 0;
       int64_t off = 0;
       if (ok)
         off = static_cast<int64_t>(blk) * p.c_sb +
-              static_cast<int64_t>(j - jb * p.BS) * p.c_sr +
+              static_cast<int64_t>(p.cu_k ? koff + j : j - jb * p.BS) * p.c_sr +
               static_cast<int64_t>(g) * p.c_sh + ch * 8;
       const uint32_t d = swz<C::ROW_BYTES>(r, ch);
       cp_async_16(sK + d, KC + off, ok ? 16 : 0);
@@ -563,7 +566,7 @@ split_combine_kernel(const CombineParams p) {
   if (q0 < 0 || q_len <= 0) return;
   const int rows = q_len * p.G;
   if (rows < p.min_rows || rows > p.max_rows) return;
-  const int L = p.seqused_k[b];
+  const int L = p.cu_k ? p.cu_k[b + 1] - p.cu_k[b] : p.seqused_k[b];
   int kmin, kmax;
   key_range(L, q_len, 0, q_len - 1, p.causal, p.wl, p.wr, kmin, kmax);
   const int nsplit =

@@ -90,7 +90,8 @@ struct Plan {
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 Plan make_plan(int batch, int total_q, int max_q, int max_k, int Hq, int Hkv,
-               int D, int causal, int wl, int wr, int num_splits, int sms) {
+               int D, int causal, int wl, int wr, int num_splits, int sms,
+               int fixed_split = 0) {
   Plan pl;
   const int G = Hq / Hkv;
   if (batch == 0 || max_q == 0) return pl;
@@ -107,8 +108,19 @@ Plan make_plan(int batch, int total_q, int max_q, int max_k, int Hq, int Hkv,
                          (wr >= 0 ? wr : (causal ? 0 : max_k));
     if (span < range) range = span;
   }
+  if (fixed_split > 0) {
+    // batch-invariant: fixed key ranges, always through the combine
+    int64_t chunk = (static_cast<int64_t>(fixed_split) + kDecodeKT - 1) /
+                    kDecodeKT * kDecodeKT;
+    if (chunk > (1 << 30)) chunk = 1 << 30;
+    pl.chunk = static_cast<int>(chunk);
+    const int64_t n = range > 0 ? (range + chunk - 1) / chunk : 1;
+    pl.splits = static_cast<int>(n > 65535 ? 65535 : n);
+  }
   int splits = 1;
-  if (num_splits > 1) {
+  if (fixed_split > 0) {
+    // plan made above
+  } else if (num_splits > 1) {
     splits = num_splits;
   } else if (num_splits == 0 && range > 0) {
     // Aim for ~8 waves of 2 resident CTAs per SM; keep >= 256 keys per split.
@@ -121,7 +133,7 @@ Plan make_plan(int batch, int total_q, int max_q, int max_k, int Hq, int Hkv,
     if (s < 1) s = 1;
     splits = static_cast<int>(s);
   }
-  if (splits > 1 && range > 0) {
+  if (fixed_split <= 0 && splits > 1 && range > 0) {
     int64_t chunk = (range + splits - 1) / splits;
     chunk = (chunk + kDecodeKT - 1) / kDecodeKT * kDecodeKT;
     pl.chunk = static_cast<int>(chunk);
@@ -146,6 +158,13 @@ Plan make_plan(int batch, int total_q, int max_q, int max_k, int Hq, int Hkv,
 size_t fp8_mock_bytes(int batch, int max_blocks, int BS, int Hkv, int D) {
   const size_t pages = static_cast<size_t>(batch) * max_blocks;
   return 2 * align256(pages * BS * Hkv * D * 2) + align256(pages * 4);
+}
+
+bool non_paged(const pkv_attention_options* o) {
+  return o && o->cu_seqlens_k;
+}
+int fixed_split_of(const pkv_attention_options* o) {
+  return o ? o->fixed_split_size : 0;
 }
 
 pkv_status check_attn_shape(int batch, int total_q, int max_q, int max_k,
@@ -212,7 +231,7 @@ pkv_status pkv_check_device_errors(pkv_stream_t stream) {
                 "kernels skipped out-of-range accesses:%s%s%s",
                 (host & kErrBadBlock) ? " block id outside the cache;" : "",
                 (host & kErrBadSlot) ? " slot outside the cache;" : "",
-                (host & kErrBadTable) ? " seqused_k beyond the table row;"
+                (host & kErrBadTable) ? " key range beyond the table row or the K/V rows;"
                                       : "");
   }
   return PKV_OK;
@@ -292,10 +311,21 @@ size_t pkv_paged_attention_workspace_size_opts(
     int num_kv_heads, int head_size, int block_size, int causal,
     int window_left, int window_right, int num_splits,
     int max_blocks_per_seq, const pkv_attention_options* opts) {
-  const size_t base = pkv_paged_attention_workspace_size(
-      batch, total_q, max_seqlen_q, max_seqlen_k, num_heads, num_kv_heads,
-      head_size, block_size, causal, window_left, window_right, num_splits);
-  if (base == static_cast<size_t>(-1)) return base;
+  const int bs = non_paged(opts) ? 16 : block_size;
+  if (check_attn_shape(batch, total_q, max_seqlen_q, max_seqlen_k, num_heads,
+                       num_kv_heads, head_size, bs, num_splits) != PKV_OK)
+    return static_cast<size_t>(-1);
+  if (fixed_split_of(opts) < 0 || (fixed_split_of(opts) > 0 && num_splits))
+    return static_cast<size_t>(-1);
+  int sms = 0;
+  if (device_info(nullptr, &sms) != PKV_OK) return static_cast<size_t>(-1);
+  const size_t base =
+      make_plan(batch, total_q, max_seqlen_q, max_seqlen_k, num_heads,
+                num_kv_heads, head_size, causal,
+                window_left < 0 ? -1 : window_left,
+                window_right < 0 ? -1 : window_right, num_splits, sms,
+                fixed_split_of(opts))
+          .workspace;
   const bool fp8 = opts && opts->kv_cache_fp8;
   const bool prefill =
       static_cast<int64_t>(max_seqlen_q) * (num_heads / num_kv_heads) >
@@ -360,10 +390,17 @@ pkv_status pkv_paged_attention_varlen_opts(
     const float* alibi_slopes, int num_splits, float* softmax_lse,
     void* workspace, size_t workspace_bytes, pkv_dtype dtype,
     pkv_stream_t stream, const pkv_attention_options* opts) {
-  pkv_status st =
-      check_attn_shape(batch, total_q, max_seqlen_q, max_seqlen_k, num_heads,
-                       num_kv_heads, head_size, block_size, num_splits);
+  const bool nonpaged = non_paged(opts);
+  pkv_status st = check_attn_shape(batch, total_q, max_seqlen_q, max_seqlen_k,
+                                   num_heads, num_kv_heads, head_size,
+                                   nonpaged ? 16 : block_size, num_splits);
   if (st != PKV_OK) return st;
+  const int fixed_split = fixed_split_of(opts);
+  if (fixed_split < 0)
+    return fail(PKV_ERR_INVALID_ARG, "fixed_split_size must be >= 0");
+  if (fixed_split > 0 && num_splits != 0)
+    return fail(PKV_ERR_INVALID_ARG,
+                "fixed_split_size and num_splits are exclusive");
   if (dtype != PKV_F16 && dtype != PKV_BF16)
     return fail(PKV_ERR_UNSUPPORTED, "dtype must be fp16 or bf16");
   if (!(softmax_scale == softmax_scale) || isinf(softmax_scale))
@@ -372,14 +409,24 @@ pkv_status pkv_paged_attention_varlen_opts(
     return fail(PKV_ERR_INVALID_ARG, "softcap must be >= 0 (0 = none)");
   if (batch == 0 || total_q == 0 || max_seqlen_q == 0) return PKV_OK;
   if (!q || !key_cache || !value_cache || !out || !cu_seqlens_q ||
-      !seqused_k || !block_table || !cache_strides)
+      !cache_strides)
     return fail(PKV_ERR_INVALID_ARG, "NULL tensor pointer");
-  if (max_blocks_per_seq <= 0 || block_table_stride < max_blocks_per_seq)
+  if (!nonpaged && (!seqused_k || !block_table))
+    return fail(PKV_ERR_INVALID_ARG, "NULL seqused_k or block_table");
+  if (!nonpaged &&
+      (max_blocks_per_seq <= 0 || block_table_stride < max_blocks_per_seq))
     return fail(PKV_ERR_INVALID_ARG,
                 "block_table: need max_blocks_per_seq >= 1 and stride >= it");
   if (cache_strides[3] != 1)
     return fail(PKV_ERR_INVALID_ARG, "the head_size dim must be contiguous");
   const bool kv8 = opts && opts->kv_cache_fp8;
+  if (nonpaged && kv8)
+    return fail(PKV_ERR_UNSUPPORTED,
+                "an fp8 cache is not supported for non-paged attention");
+  if (nonpaged && opts->total_k < 0)
+    return fail(PKV_ERR_INVALID_ARG, "total_k must be >= 0");
+  if (nonpaged && (cache_strides[1] <= 0 || cache_strides[2] <= 0))
+    return fail(PKV_ERR_INVALID_ARG, "non-paged K/V strides must be > 0");
   if (kv8 && (!opts->k_scale || !opts->v_scale))
     return fail(PKV_ERR_INVALID_ARG, "fp8 cache needs k_scale and v_scale");
   if (kv8 && head_size % 16 != 0)
@@ -388,7 +435,8 @@ pkv_status pkv_paged_attention_varlen_opts(
   if (!aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache) ||
       !aligned16(out) || !stride16(q_stride_tok, eb) ||
       !stride16(q_stride_head, eb) || !stride16(o_stride_tok, eb) ||
-      !stride16(o_stride_head, eb) || !stride16(cache_strides[0], cb) ||
+      !stride16(o_stride_head, eb) ||
+      !stride16(nonpaged ? 0 : cache_strides[0], cb) ||
       !stride16(cache_strides[1], cb) || !stride16(cache_strides[2], cb))
     return fail(PKV_ERR_UNSUPPORTED,
                 "q/out/cache rows must start on 16-byte boundaries");
@@ -401,7 +449,7 @@ pkv_status pkv_paged_attention_varlen_opts(
   if (st != PKV_OK) return st;
   const Plan pl = make_plan(batch, total_q, max_seqlen_q, max_seqlen_k,
                             num_heads, num_kv_heads, head_size, causal, wl, wr,
-                            num_splits, sms);
+                            num_splits, sms, fixed_split);
   size_t need = pl.workspace;
   size_t mock_off = 0;
   if (kv8 && pl.prefill) {
@@ -454,6 +502,21 @@ pkv_status pkv_paged_attention_varlen_opts(
   p.kv_fp8 = kv8 ? 1 : 0;
   p.k_scale = kv8 ? opts->k_scale : nullptr;
   p.v_scale = kv8 ? opts->v_scale : nullptr;
+  if (nonpaged) {
+    // one "block" holding all total_k rows; kernels index rows by cu_k
+    const int rows = opts->total_k > 0 ? opts->total_k : 1;
+    p.cu_k = opts->cu_seqlens_k;
+    p.total_k = opts->total_k;
+    p.block_table = nullptr;
+    p.bt_stride = 0;
+    p.max_blocks = 1;
+    p.num_blocks = 1;
+    p.BS = rows;
+    p.bs_shift = -1;
+    const int64_t ext_r = static_cast<int64_t>(rows) * p.c_sr;
+    const int64_t ext_h = static_cast<int64_t>(num_kv_heads) * p.c_sh;
+    p.c_sb = ext_r > ext_h ? ext_r : ext_h;
+  }
   p.causal = causal ? 1 : 0;
   p.wl = wl;
   p.wr = wr;
@@ -484,6 +547,7 @@ pkv_status pkv_paged_attention_varlen_opts(
       c.total_q = total_q;
       c.cu_q = cu_seqlens_q;
       c.seqused_k = seqused_k;
+      c.cu_k = p.cu_k;
       c.batch = batch;
       c.Hq = num_heads;
       c.G = p.G;

@@ -166,6 +166,11 @@ struct AttnParams {
   int total_q;
   const int32_t* cu_q;
   const int32_t* seqused_k;
+  // non-paged mode: keys of request b are rows cu_k[b] .. cu_k[b+1]-1 of one
+  // K/V tensor of total_k rows (c_sr: row stride, c_sh: head stride); null
+  // = paged
+  const int32_t* cu_k;
+  int total_k;
   int batch;
   const int32_t* block_table;
   int64_t bt_stride;
@@ -199,6 +204,7 @@ struct CombineParams {
   int total_q;
   const int32_t* cu_q;
   const int32_t* seqused_k;
+  const int32_t* cu_k;        // non-paged mode (see AttnParams)
   int batch, Hq, G, D;
   int causal, wl, wr;
   int chunk, splits;

@@ -97,6 +97,8 @@ struct TcParams {
   int total_q;
   const int32_t* cu_q;
   const int32_t* seqused_k;
+  const int32_t* cu_k;    // non-paged mode: rows cu_k[b] .. of one K/V tensor
+  int total_k;
   const int32_t* block_table;
   int64_t bt_stride;
   int max_blocks;
@@ -399,8 +401,12 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
   const int rows = q_len * G;
   const int row0 = tile * BM;
   const int row_end = min(rows, row0 + BM);
-  const int L = p.seqused_k[b];
-  const int L_tab = min(L, p.max_blocks * p.BS);
+  const int koff = p.cu_k ? p.cu_k[b] : 0;     // non-paged: first key row
+  const int L = p.cu_k ? p.cu_k[b + 1] - koff : p.seqused_k[b];
+  // rows past the table (or, non-paged, past the K/V tensor) are not read
+  const int L_tab = p.cu_k ? (koff < 0 ? 0 : max(0, min(L, p.total_k - koff)))
+                           : min(L, p.max_blocks * p.BS);
+  if (L_tab < L && threadIdx.x == 0) atomicOr(p.err, kErrBadTable);
   int kmin, kmax;
   key_range(L, q_len, row0 / G, (row_end - 1) / G, p.causal, p.wl, p.wr, kmin,
             kmax);
@@ -511,6 +517,7 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
     auto fetch = [&](int j) -> int {
       const int k0 = kstart + j * BN + lane * RB;
       if (j >= n_tiles || lane >= BN / RB || k0 >= kmax) return 0;
+      if (p.cu_k) return 0;
       const int blk = __ldg(bt + k0 / p.BS);
       if (blk < 0 || blk >= p.num_blocks) {
         atomicOr(p.err, kErrBadBlock);
@@ -548,7 +555,7 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
           for (int i = 0; i < MAXBOX; ++i) {
             if (i >= nbox) break;
             const int k0 = kt + i * RB;
-            const int row = k0 % p.BS;
+            const int row = p.cu_k ? koff + k0 : k0 % p.BS;
             for (int cb = 0; cb < C::NCB; ++cb) {
               const uint32_t dst = dst0 + cb * (BN * 128) + i * RB * 128;
               if (p.kv_order_hnd)
@@ -919,8 +926,12 @@ prefill_pp_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
   }
   if (b < 0) return;
   const int rows = q_len * G;
-  const int L = p.seqused_k[b];
-  const int L_tab = min(L, p.max_blocks * p.BS);
+  const int koff = p.cu_k ? p.cu_k[b] : 0;     // non-paged: first key row
+  const int L = p.cu_k ? p.cu_k[b + 1] - koff : p.seqused_k[b];
+  // rows past the table (or, non-paged, past the K/V tensor) are not read
+  const int L_tab = p.cu_k ? (koff < 0 ? 0 : max(0, min(L, p.total_k - koff)))
+                           : min(L, p.max_blocks * p.BS);
+  if (L_tab < L && threadIdx.x == 0) atomicOr(p.err, kErrBadTable);
   const int ctx = L - q_len;
   const int RB = p.RB;
   // per Q tile x: rows [rx0, rx_end), keys [kmn[x], kmx[x])
@@ -1043,7 +1054,8 @@ prefill_pp_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
       auto fetch = [&](int j) -> int {
         const int k0 = kstart + j * BN + lane * RB;
         if (j >= n_tiles || lane >= BN / RB || k0 >= kmax_u) return 0;
-        const int blk = __ldg(bt + k0 / p.BS);
+        if (p.cu_k) return 0;
+      const int blk = __ldg(bt + k0 / p.BS);
         if (blk < 0 || blk >= p.num_blocks) {
           atomicOr(p.err, kErrBadBlock);
           return 0;
@@ -1075,7 +1087,7 @@ prefill_pp_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
         if (lane < nbox) {
           const uint32_t dst0 = (mat ? sV : sK) + s * C::KV_BYTES;
           const int k0 = kt + lane * RB;
-          const int row = k0 % p.BS;
+          const int row = p.cu_k ? koff + k0 : k0 % p.BS;
           for (int cb = 0; cb < C::NCB; ++cb) {
             const uint32_t dst = dst0 + cb * (BN * 128) + lane * RB * 128;
             if (p.kv_order_hnd)
@@ -1449,6 +1461,8 @@ cudaError_t launch_prefill_attn_tc(const AttnParams& a, int D, bool bf16,
   p.total_q = a.total_q;
   p.cu_q = a.cu_q;
   p.seqused_k = a.seqused_k;
+  p.cu_k = a.cu_k;
+  p.total_k = a.total_k;
   p.block_table = a.block_table;
   p.bt_stride = a.bt_stride;
   p.max_blocks = a.max_blocks;
@@ -1472,6 +1486,7 @@ cudaError_t launch_prefill_attn_tc(const AttnParams& a, int D, bool bf16,
   const int BN = prefill_tc_block_keys(D);
   int RB = 16;
   while (RB * 2 <= BN && a.BS % (RB * 2) == 0) RB *= 2;
+  if (a.cu_k) RB = BN;    // non-paged: boxes may start on any row
   p.RB = RB;
   p.kv_order_hnd = a.c_sh > a.c_sr ? 1 : 0;
   CUtensorMap mk, mv;

@@ -287,3 +287,35 @@ WORKLOADS = {
     "long_decode": long_decode,
     "cascade_decode": cascade_decode,
 }
+
+
+# ---------------------------------------------------------------------------
+# Attention without a cache (encoder / cache-free prefill inputs)
+# ---------------------------------------------------------------------------
+
+@dataclasses.dataclass
+class NonPagedInputs:
+    """Q [T, Hq, D] and K/V rows [Tk, Hkv, D] with their cu_seqlens."""
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    cu_seqlens_q: np.ndarray
+    cu_seqlens_k: np.ndarray
+    dtype: str
+
+
+def nonpaged_inputs(seed, q_lens, k_lens, num_heads, num_kv_heads, head_size,
+                    dtype="bf16"):
+    """N(0,1) values rounded to ``dtype`` (CPU tensors), drawn in a fixed
+    order from one seeded generator."""
+    tdt = {"bf16": torch.bfloat16, "f16": torch.float16}[dtype]
+    rng = np.random.default_rng([seed, 2])
+    T, Tk = int(sum(q_lens)), int(sum(k_lens))
+    draw = lambda shp: torch.from_numpy(                     # noqa: E731
+        rng.standard_normal(size=shp, dtype=np.float32)).to(tdt)
+    return NonPagedInputs(
+        q=draw((T, num_heads, head_size)),
+        k=draw((Tk, num_kv_heads, head_size)),
+        v=draw((Tk, num_kv_heads, head_size)),
+        cu_seqlens_q=cu_seqlens(q_lens), cu_seqlens_k=cu_seqlens(k_lens),
+        dtype=dtype)

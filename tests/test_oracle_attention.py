@@ -329,3 +329,67 @@ def test_sink_limits_and_empty_rows():
     big = paged_attention_ref(q, kc, vc, cu, su, table, 0.4,
                               sinks=np.full(4, 1e3))
     assert np.abs(big[0]).max() < 1e-300
+
+
+# --------------------------------------------------------------- non-paged
+
+NONPAGED_CASES = [
+    # q_lens, k_lens, Hq, Hkv, D, causal, window
+    ([4, 9, 1], [4, 9, 1], 4, 2, 8, False, (-1, -1)),   # encoder: cu_k = cu_q
+    ([4, 9, 3], [4, 9, 3], 4, 4, 8, True, (-1, -1)),    # cache-free prefill
+    ([2, 5], [11, 7], 6, 2, 16, True, (3, 1)),          # more keys than queries
+    ([6, 1], [3, 0], 2, 1, 8, False, (-1, -1)),         # fewer / no keys
+]
+
+
+@pytest.mark.parametrize("case", NONPAGED_CASES)
+def test_nonpaged_matches_torch_sdpa(case):
+    from oracle import varlen_attention_ref
+    q_lens, k_lens, Hq, Hkv, D, causal, window = case
+    rng = np.random.default_rng(len(str(case)) + sum(k_lens))
+    q = rng.standard_normal((sum(q_lens), Hq, D))
+    ks = [rng.standard_normal((L, Hkv, D)) for L in k_lens]
+    vs = [rng.standard_normal((L, Hkv, D)) for L in k_lens]
+    cu_q = np.concatenate([[0], np.cumsum(q_lens)])
+    cu_k = np.concatenate([[0], np.cumsum(k_lens)])
+    k = np.concatenate(ks) if sum(k_lens) else np.zeros((0, Hkv, D))
+    v = np.concatenate(vs) if sum(k_lens) else np.zeros((0, Hkv, D))
+    out, lse = varlen_attention_ref(q, k, v, cu_q, cu_k, 0.41, causal=causal,
+                                    window_size=window)
+    keep = [b for b in range(len(k_lens)) if k_lens[b] > 0]
+    ro, rl = sdpa_reference(q[np.concatenate([np.arange(cu_q[b], cu_q[b + 1])
+                                              for b in keep])],
+                            [ks[b] for b in keep], [vs[b] for b in keep],
+                            np.concatenate([[0], np.cumsum([q_lens[b]
+                                                            for b in keep])]),
+                            0.41, causal, window, G=Hq // Hkv)
+    rows = np.concatenate([np.arange(cu_q[b], cu_q[b + 1]) for b in keep])
+    np.testing.assert_allclose(out[rows], ro, atol=1e-12, rtol=0)
+    np.testing.assert_allclose(lse[:, rows], rl, atol=1e-12, rtol=0)
+    for b in range(len(k_lens)):               # requests without keys
+        if k_lens[b] == 0:
+            sl = slice(cu_q[b], cu_q[b + 1])
+            assert (out[sl] == 0).all() and np.isneginf(lse[:, sl]).all()
+
+
+def test_nonpaged_reads_only_its_own_rows_and_is_order_free():
+    """Changing another request's rows changes nothing; without a causal
+    mask or window, permuting a request's (key, value) rows changes
+    nothing either (the softmax is a sum over keys)."""
+    from oracle import varlen_attention_ref
+    rng = np.random.default_rng(5)
+    q = rng.standard_normal((7, 4, 8))
+    k = rng.standard_normal((12, 2, 8))
+    v = rng.standard_normal((12, 2, 8))
+    cu_q, cu_k = np.array([0, 3, 7]), np.array([0, 5, 12])
+    base = varlen_attention_ref(q, k, v, cu_q, cu_k, 0.3)
+    k2, v2 = k.copy(), v.copy()
+    k2[5:] = rng.standard_normal((7, 2, 8))
+    v2[5:] = rng.standard_normal((7, 2, 8))
+    other = varlen_attention_ref(q, k2, v2, cu_q, cu_k, 0.3)
+    np.testing.assert_array_equal(other[0][:3], base[0][:3])
+    np.testing.assert_array_equal(other[1][:, :3], base[1][:, :3])
+    perm = np.concatenate([rng.permutation(5), 5 + rng.permutation(7)])
+    shuffled = varlen_attention_ref(q, k[perm], v[perm], cu_q, cu_k, 0.3)
+    np.testing.assert_allclose(shuffled[0], base[0], atol=1e-13)
+    np.testing.assert_allclose(shuffled[1], base[1], atol=1e-13)
