@@ -41,6 +41,7 @@ METRIC = ("paged decode HBM GB/s & prefill attn TFLOP/s "
 UNIT = "GB/s"
 SEED_DECODE = 319
 SEED_PREFILL = 320
+CLOCK_SOAK_S = 0.5      # seconds of extra load for the clock samples
 
 
 # --------------------------------------------------------------- accounting
@@ -92,11 +93,14 @@ def ncu_traffic(kernel_tag):
         if ":" in line:
             k, v = line.split(":", 1)
             fields[k.strip()] = v.strip()
-    src = os.path.join(ROOT, "paged_kv_cache_318_gb300", "csrc",
-                       fields.get("source", "attn_mma.cu"))
-    if not os.path.exists(src):
-        return None
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for name in fields.get("source", "").split(","):
+        src = os.path.join(ROOT, "paged_kv_cache_318_gb300", "csrc",
+                           name.strip())
+        if not name.strip() or not os.path.exists(src):
+            return None
+        h.update(open(src, "rb").read())
+    h = h.hexdigest()[:16]
     if fields.get("source_sha256_16") != h:
         return None
     try:
@@ -107,7 +111,10 @@ def ncu_traffic(kernel_tag):
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling in the background."""
+    """nvidia-smi clock / throttle sampling in the background.
+
+    A reader thread timestamps every sample, so the summary can be limited
+    to the window between ``begin()`` and ``end()``."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,"
               "clocks_event_reasons.active,"
@@ -117,35 +124,51 @@ class ClockSampler:
               "clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index):
+        import threading
         self.proc = None
-        self.rows = []
-        self.gpu = gpu_index
+        self.lines = []                     # (time, line)
+        self.window = [None, None]
+        self.first = threading.Event()
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(gpu_index),
                  "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE,
+                 "-lms", "50"], stdout=subprocess.PIPE,
                 stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
-        self.t_marks = []
+            return
+        self.reader = threading.Thread(target=self._read, daemon=True)
+        self.reader.start()
+        self.first.wait(timeout=10.0)       # sampling has started
 
-    def mark(self):
-        self.t_marks.append(time.time())
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line))
+            self.first.set()
 
-    def stop(self):
+    def begin(self):
+        self.window[0] = time.time()
+
+    def end(self):
+        self.window[1] = time.time()
+
+    def stop(self, label):
         if self.proc is None:
             return None
         self.proc.terminate()
         try:
-            out, _ = self.proc.communicate(timeout=5)
+            self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-            out, _ = self.proc.communicate()
+        self.reader.join(timeout=5)
+        t0, t1 = self.window
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
                  "sw_power_cap"]
-        for line in out.strip().splitlines():
+        for t, line in self.lines:
+            if t0 is not None and (t < t0 or (t1 is not None and t > t1)):
+                continue
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -161,7 +184,7 @@ class ClockSampler:
             return None
         return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx),
                 "reasons": sorted(reasons), "samples": len(sm),
-                "window": "warm-up through timed region"}
+                "window": label}
 
 
 # ------------------------------------------------------------ multi-rank
@@ -216,6 +239,7 @@ def gpu_arm(args, rank, world, dev):
             ev_b[i].record(stream)
 
     clocks = ClockSampler(dev.index or 0)
+    clocks.begin()
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
@@ -229,6 +253,16 @@ def gpu_arm(args, rank, world, dev):
     if world > 1:
         torch.distributed.barrier()
     attn_ms = float(np.mean([a.elapsed_time(b) for a, b in zip(ev_a, ev_b)]))
+    # the timed region is shorter than the sampling interval: keep the same
+    # step running for CLOCK_SOAK_S more so the samples see this load
+    t_soak = time.time()
+    while time.time() - t_soak < CLOCK_SOAK_S:
+        for i in range(20):
+            step(0)
+        torch.cuda.synchronize()
+    clocks.end()
+    clk = clocks.stop("warm-up, timed region and %.1f s of the same steps "
+                      "right after it" % CLOCK_SOAK_S)
     api.check_device_errors(dev)
 
     # e2e: same step through the public API from pinned host buffers
@@ -249,7 +283,6 @@ def gpu_arm(args, rank, world, dev):
     for i in range(args.warmup):
         e2e_step(i)
     e2e_ms = time_steps(e2e_step, args.steps, stream)
-    clk = clocks.stop()
 
     # secondary: varlen causal prefill with prefix cache (TFLOP/s)
     pre = workloads.prefill_with_prefix(seed=SEED_PREFILL, device=dev)
@@ -293,8 +326,8 @@ def gpu_arm(args, rank, world, dev):
                 "d2h_bytes_per_step": int(d2h),
                 "ms_per_step": round(e2e_step_ms, 5)},
         "roofline": {
-            "kernel": "paged decode attention (decode kernel + split "
-                      "combine)",
+            "kernel": "paged decode attention call (TMA decode kernel, "
+                      "plus the split combine when the plan splits)",
             "bound": "hbm", "achieved": round(achieved, 1),
             "peak": hbm_peak, "unit": "GB/s",
             "frac": round(achieved / hbm_peak, 4),

@@ -406,6 +406,18 @@ PKV_API pkv_status pkv_check_device_errors(pkv_stream_t stream);
 PKV_API pkv_status pkv_set_prefill_kernel(int which);
 
 /*
+ * Which kernel serves decode-class requests (at most 16 packed query rows
+ * per KV head) over a 16-bit cache: the kernel whose producer warp moves
+ * K/V pages with TMA (the default) or the one whose threads gather them with
+ * 16-byte cp.async.  fp8 caches always use the cp.async kernel.  A
+ * process-wide diagnostic switch for A/B comparison; both give the same
+ * result within rounding.  Returns PKV_ERR_INVALID_ARG for other values.
+ */
+#define PKV_DECODE_TMA 0
+#define PKV_DECODE_CP_ASYNC 1
+PKV_API pkv_status pkv_set_decode_kernel(int which);
+
+/*
  * Number of kernels this library has launched in this process (all devices,
  * all threads), for accounting of launches per step.
  */

@@ -108,6 +108,8 @@ def load_library():
         lib.pkv_use_cascade_attention.argtypes = [i32, vp] + [i32] * 8
         lib.pkv_set_prefill_kernel.restype = i32
         lib.pkv_set_prefill_kernel.argtypes = [i32]
+        lib.pkv_set_decode_kernel.restype = i32
+        lib.pkv_set_decode_kernel.argtypes = [i32]
         lib.pkv_launch_count.restype = ctypes.c_uint64
         lib.pkv_launch_count.argtypes = []
         lib.pkv_check_device_errors.restype = i32
@@ -160,6 +162,15 @@ PREFILL_MMA_SYNC = 1
 def set_prefill_kernel(which: int):
     """Choose the prefill kernel (PREFILL_TCGEN05 or PREFILL_MMA_SYNC)."""
     _check(load_library().pkv_set_prefill_kernel(int(which)))
+
+
+DECODE_TMA = 0
+DECODE_CP_ASYNC = 1
+
+
+def set_decode_kernel(which: int):
+    """Choose the 16-bit decode kernel (DECODE_TMA or DECODE_CP_ASYNC)."""
+    _check(load_library().pkv_set_decode_kernel(int(which)))
 
 
 def launch_count() -> int:

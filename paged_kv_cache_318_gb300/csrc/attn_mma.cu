@@ -73,12 +73,6 @@ struct MmaCfg {
   static_assert(COMBINE_BYTES <= RING_BYTES, "combine buffer");
 };
 
-// Byte offset of 16-byte chunk `ch` of row `r` in a swizzled tile.
-template <int ROW_BYTES>
-__device__ __forceinline__ uint32_t swz(int r, int ch) {
-  return static_cast<uint32_t>(r * ROW_BYTES + ((ch ^ (r & 7)) << 4));
-}
-
 // Two E4M3 codes (low byte first) -> two 16-bit values of type T (exact).
 template <typename T>
 __device__ __forceinline__ uint32_t e4m3x2_to(uint16_t v);
@@ -125,13 +119,9 @@ attn_mma_kernel(const AttnParams p) {
   if (p.chunk > 0) {
     // The grid has gridDim.x splits; if the caller's max_seqlen_k was too
     // small for this request, the last split takes the rest of the range.
-    const int nsplit = min(max((kmax - kmin + p.chunk - 1) / p.chunk, 1),
-                           static_cast<int>(gridDim.x));
+    const int nsplit = split_count(kmin, kmax, p.chunk, gridDim.x);
     if (static_cast<int>(blockIdx.x) >= nsplit) return;
-    lo = kmin + blockIdx.x * p.chunk;
-    hi = (static_cast<int>(blockIdx.x) == nsplit - 1) ? kmax
-                                                      : min(kmax, lo + p.chunk);
-    if (hi < lo) hi = lo;
+    split_bounds(kmin, kmax, p.chunk, nsplit, blockIdx.x, lo, hi);
   }
   // Keys are only followed through the table while it has entries.
   // rows past the table (or, non-paged, past the K/V tensor) are not read
@@ -258,6 +248,9 @@ attn_mma_kernel(const AttnParams p) {
     if (okB) slopeB = p.alibi[g * G + rB % G];
   }
   const bool plain = (p.softcap <= 0.f) && (p.alibi == nullptr);
+  // soft-cap without ALiBi: interior tiles need only the capped logit
+  const bool capped = (p.softcap > 0.f) && (p.alibi == nullptr);
+  const float inv_cap = p.softcap > 0.f ? 1.f / p.softcap : 0.f;
   // fp8 cache: value = code * scale, so k_scale joins the logit scale and
   // v_scale multiplies the output
   const float kscale = p.k_scale ? *p.k_scale : 1.f;
@@ -354,13 +347,23 @@ attn_mma_kernel(const AttnParams p) {
 
     // logits (base 2) with masks
     float mxA = -INFINITY, mxB = -INFINITY;
-    if (plain && kt >= full_lo && kt + KT <= full_hi) {
+    const bool interior = kt >= full_lo && kt + KT <= full_hi;
+    if (plain && interior) {
 #pragma unroll
       for (int nt = 0; nt < C::NKT; ++nt) {
         s[nt][0] *= scale_log2;
         s[nt][1] *= scale_log2;
         s[nt][2] *= scale_log2;
         s[nt][3] *= scale_log2;
+        mxA = fmaxf(mxA, fmaxf(s[nt][0], s[nt][1]));
+        mxB = fmaxf(mxB, fmaxf(s[nt][2], s[nt][3]));
+      }
+    } else if (capped && interior) {
+      const float pre = qk_scale * inv_cap, post = p.softcap * kLog2e;
+#pragma unroll
+      for (int nt = 0; nt < C::NKT; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[nt][e] = post * tanh_fast(s[nt][e] * pre);
         mxA = fmaxf(mxA, fmaxf(s[nt][0], s[nt][1]));
         mxB = fmaxf(mxB, fmaxf(s[nt][2], s[nt][3]));
       }
@@ -377,7 +380,7 @@ attn_mma_kernel(const AttnParams p) {
           x *= scale_log2;
         } else {
           x *= qk_scale;
-          if (p.softcap > 0.f) x = p.softcap * tanhf(x / p.softcap);
+          if (p.softcap > 0.f) x = p.softcap * tanh_fast(x * inv_cap);
           if (p.alibi) x -= (rowB ? slopeB : slopeA) * fabsf(float(pos - key));
           x *= kLog2e;
         }
@@ -569,8 +572,7 @@ split_combine_kernel(const CombineParams p) {
   const int L = p.cu_k ? p.cu_k[b + 1] - p.cu_k[b] : p.seqused_k[b];
   int kmin, kmax;
   key_range(L, q_len, 0, q_len - 1, p.causal, p.wl, p.wr, kmin, kmax);
-  const int nsplit =
-      min(max((kmax - kmin + p.chunk - 1) / p.chunk, 1), p.splits);
+  const int nsplit = split_count(kmin, kmax, p.chunk, p.splits);
   const int D = p.D;
   T* __restrict__ OUT = static_cast<T*>(p.out);
   for (int i = 0; i < q_len; ++i) {

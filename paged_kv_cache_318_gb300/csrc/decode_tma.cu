@@ -1,0 +1,566 @@
+// Decode attention with TMA page loads and a producer warp.
+//
+// Source: "vllm/v1/attention/backends/flash_attn.py", FlashAttentionImpl.
+// forward (flash_attn_varlen_func over the paged cache: cu_seqlens_q,
+// seqused_k, block_table, causal, window_size, softcap, alibi_slopes, LSE)
+// and FlashAttentionMetadataBuilder (split-KV decoding of requests with one
+// query per KV-head group, intermediates of [num_splits, ...] combined by
+// LSE).  Same math as the cp.async decode kernel in attn_mma.cu; this one
+// moves K/V with the tensor-memory accelerator.
+//
+// One CTA owns (request b, KV head g, split s).  Its rows are the request's
+// q_len * G <= 16 packed (token, head-in-group) query rows, the M dimension
+// of mma.sync m16n8k16 (a 16 x KT x D contraction is far too small for a
+// 128-row tcgen05 tile; the kernel is bound by HBM, not by the MMAs).
+//
+//   warp NCW (producer)  lane i fetches the page id of box i of the next
+//                        tile from the block table, then issues the tile's
+//                        K and V boxes (cp.async.bulk.tensor.4d, RB rows x
+//                        64 columns, 128-byte swizzle) into a STAGES-deep
+//                        ring; K and V complete on separate mbarriers
+//   warps 0..NCW-1       each owns KW = KT / NCW keys of every tile:
+//                        S = Q K^T, online softmax (base 2), O += P V, then
+//                        releases the stage; at the end the warps' partial
+//                        states are merged through shared memory
+//
+// Tiles start on KT-key boundaries, so every box starts on a page boundary
+// multiple of RB (RB divides both block_size and KT).  Keys outside the
+// split's [lo, hi) are masked; V rows at or past the end of the loaded range
+// are zeroed before P V (they may hold another request's NaN padding).
+// Every mbarrier wait is bounded (kWaitLimitNs); a CTA whose wait runs out
+// records kErrTimeout, drains the copies it issued and exits without
+// writing.
+#include <cuda.h>
+#include <math.h>
+
+#include "pkv_common.cuh"
+#include "tma_util.cuh"
+
+namespace pkv {
+namespace dtma {
+
+template <int D, int NCW, int KT, int STAGES>
+struct Cfg {
+  static constexpr int NT = (NCW + 1) * 32;     // consumers + producer warp
+  static constexpr int CT = NCW * 32;           // consumer threads
+  static constexpr int KW = KT / NCW;           // keys per warp per tile
+  static constexpr int NKT = KW / 8;            // n8 tiles of S per warp
+  static constexpr int NCB = D / 64;            // 64-column (128 B) blocks
+  static constexpr int CPR = D / 8;             // 16-byte chunks per row
+  static constexpr int ROW_BYTES = D * 2;
+  static constexpr int CB_BYTES = KT * 128;     // one column block of a tile
+  static constexpr int TILE_BYTES = NCB * CB_BYTES;
+  static constexpr int RING_BYTES = STAGES * 2 * TILE_BYTES;
+  static constexpr int Q_BYTES = 16 * ROW_BYTES;
+  static constexpr int OFF_Q = RING_BYTES;
+  static constexpr int OFF_BAR = OFF_Q + Q_BYTES;
+  static constexpr int BAR_BYTES = 3 * STAGES * 8 + 8 + 4 * STAGES;
+  static constexpr int SMEM = OFF_BAR + BAR_BYTES + 1024;   // + alignment
+  static constexpr int COMBINE_BYTES = NCW * 16 * (D + 2) * 4;
+  static_assert(KW % 16 == 0, "each warp needs whole k16 steps of keys");
+  static_assert(D % 64 == 0, "64-column TMA boxes");
+  static_assert(CB_BYTES % 1024 == 0, "128-byte swizzle atoms");
+  static_assert(COMBINE_BYTES <= RING_BYTES, "combine buffer");
+};
+
+// Byte offset of 16-byte chunk `ch` (0 .. D/8-1) of row r in a K/V tile
+// written by 64-column TMA boxes with the 128-byte swizzle.
+template <int KT>
+__device__ __forceinline__ uint32_t kv_off(int r, int ch) {
+  return static_cast<uint32_t>((ch >> 3) * (KT * 128)) + sw128(r, ch & 7);
+}
+
+template <typename T, int D, int NCW, int KT, int STAGES>
+__global__ void __launch_bounds__((NCW + 1) * 32)
+decode_tma_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v) {
+  using C = Cfg<D, NCW, KT, STAGES>;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t raw_u = smem_u32(smem_raw);
+  const uint32_t base_u = (raw_u + 1023u) & ~1023u;
+  unsigned char* base = smem_raw + (base_u - raw_u);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = blockIdx.z / p.Hkv, g = blockIdx.z - (blockIdx.z / p.Hkv) * p.Hkv;
+  const int G = p.G;
+  const int q0 = p.cu_q[b];
+  const int q_len = min(p.cu_q[b + 1] - q0, p.total_q - q0);
+  if (q0 < 0 || q_len <= 0) return;
+  const int rows = q_len * G;
+  if (rows < p.min_rows || rows > p.max_rows || rows > 16) return;
+  const int koff = p.cu_k ? p.cu_k[b] : 0;      // non-paged: first key row
+  const int L = p.cu_k ? p.cu_k[b + 1] - koff : p.seqused_k[b];
+  // rows past the table (or, non-paged, past the K/V tensor) are not read
+  const int L_tab = p.cu_k ? (koff < 0 ? 0 : max(0, min(L, p.total_k - koff)))
+                           : min(L, p.max_blocks * p.BS);
+  if (L_tab < L && tid == 0 && blockIdx.x == 0)
+    atomicOr(p.err, kErrBadTable);
+
+  int kmin, kmax;
+  key_range(L, q_len, 0, q_len - 1, p.causal, p.wl, p.wr, kmin, kmax);
+  int lo = kmin, hi = kmax;
+  if (p.chunk > 0) {
+    const int nsplit = split_count(kmin, kmax, p.chunk, gridDim.x);
+    if (static_cast<int>(blockIdx.x) >= nsplit) return;
+    split_bounds(kmin, kmax, p.chunk, nsplit, blockIdx.x, lo, hi);
+  }
+  hi = min(hi, L_tab);
+  const int kt0 = (lo / KT) * KT;
+  const int n_tiles = hi > lo ? (hi - kt0 + KT - 1) / KT : 0;
+  const int RB = p.rb;                          // rows per box
+
+  const uint32_t ring = base_u;
+  const uint32_t sQ = base_u + C::OFF_Q;
+  const uint32_t bar0 = base_u + C::OFF_BAR;
+  auto full_k = [&](int s) { return bar0 + 8 * s; };
+  auto full_v = [&](int s) { return bar0 + 8 * (STAGES + s); };
+  auto empty = [&](int s) { return bar0 + 8 * (2 * STAGES + s); };
+  volatile int* abort_flag =
+      reinterpret_cast<volatile int*>(base + C::OFF_BAR + 3 * STAGES * 8);
+  // per stage: boxes of the tile whose page id was out of range (not
+  // loaded; their K and V rows are zeroed by the consumers instead)
+  volatile unsigned* bad_boxes = reinterpret_cast<volatile unsigned*>(
+      base + C::OFF_BAR + 3 * STAGES * 8 + 8);
+  auto tile_k = [&](int s) { return ring + s * 2 * C::TILE_BYTES; };
+  auto tile_v = [&](int s) { return ring + s * 2 * C::TILE_BYTES + C::TILE_BYTES; };
+
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_k(s), 1);
+      mbar_init(full_v(s), 1);
+      mbar_init(empty(s), NCW);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp < NCW) {
+    // ---- Q tile: packed rows 0 .. 16 (zero past rows)
+    const T* Q = static_cast<const T*>(p.q);
+    for (int i = tid; i < 16 * C::CPR; i += C::CT) {
+      const int r = i / C::CPR, ch = i - (i / C::CPR) * C::CPR;
+      const bool ok = r < rows;
+      const T* src = Q;
+      if (ok)
+        src = Q + static_cast<int64_t>(q0 + r / G) * p.q_st +
+              static_cast<int64_t>(g * G + r % G) * p.q_sh + ch * 8;
+      cp_async_16(sQ + swz<C::ROW_BYTES>(r, ch), src, ok ? 16 : 0);
+    }
+    cp_async_commit();
+  }
+  __syncthreads();
+
+  if (warp == NCW) {
+    // ------------------------------------------------------------ producer
+    if (n_tiles == 0) return;
+    const int nb_max = KT / RB;
+    const int32_t* bt = p.cu_k ? nullptr
+                               : p.block_table + static_cast<int64_t>(b) * p.bt_stride;
+    auto fetch = [&](int t) -> int {            // page id of box `lane`
+      const int k0 = kt0 + t * KT + lane * RB;
+      if (t >= n_tiles || lane >= nb_max || k0 >= hi || !bt) return 0;
+      const int blk = __ldg(bt + k0 / p.BS);
+      if (blk < 0 || blk >= p.num_blocks) {
+        atomicOr(p.err, kErrBadBlock);
+        return -1;
+      }
+      return blk;
+    };
+    int issued = 0;
+    int cur = fetch(0);
+    for (int t = 0; t < n_tiles; ++t) {
+      const int nxt = fetch(t + 1);
+      const int s = t % STAGES;
+      const int kt = kt0 + t * KT;
+      int nbox = (hi - kt + RB - 1) / RB;
+      if (nbox > nb_max) nbox = nb_max;
+      const unsigned bad = __ballot_sync(0xffffffffu, lane < nbox && cur < 0);
+      int stop = 0;
+      if (lane == 0) {
+        if (t >= STAGES &&
+            !mbar_wait(empty(s), ((t / STAGES) - 1) & 1, abort_flag, p.err)) {
+          stop = 1;
+        } else {
+          bad_boxes[s] = bad;
+          const uint32_t bytes = (nbox - __popc(bad)) * C::NCB * RB * 128;
+          mbar_expect_tx(full_k(s), bytes);
+          mbar_expect_tx(full_v(s), bytes);
+        }
+      }
+      stop = __shfl_sync(0xffffffffu, stop, 0);
+      if (stop) break;
+      if (lane < nbox && cur >= 0) {
+        const int k0 = kt + lane * RB;
+        const int row = p.cu_k ? koff + k0 : k0 % p.BS;
+#pragma unroll
+        for (int cb = 0; cb < C::NCB; ++cb) {
+          const uint32_t dst = tile_k(s) + cb * C::CB_BYTES + lane * RB * 128;
+          if (p.kv_order_hnd)
+            tma_load_4d(dst, &tm_k, cb * 64, row, g, cur, full_k(s));
+          else
+            tma_load_4d(dst, &tm_k, cb * 64, g, row, cur, full_k(s));
+        }
+#pragma unroll
+        for (int cb = 0; cb < C::NCB; ++cb) {
+          const uint32_t dst = tile_v(s) + cb * C::CB_BYTES + lane * RB * 128;
+          if (p.kv_order_hnd)
+            tma_load_4d(dst, &tm_v, cb * 64, row, g, cur, full_v(s));
+          else
+            tma_load_4d(dst, &tm_v, cb * 64, g, row, cur, full_v(s));
+        }
+      }
+      issued = t + 1;
+      cur = nxt;
+    }
+    if (lane == 0) {
+      // no copy of this CTA may still be in flight when it exits (the
+      // consumers wait for every tile, unless a wait ran out)
+      for (int t = max(0, issued - STAGES); t < issued; ++t) {
+        mbar_drain(full_k(t % STAGES), (t / STAGES) & 1);
+        mbar_drain(full_v(t % STAGES), (t / STAGES) & 1);
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  cp_async_wait<0>();
+  asm volatile("bar.sync 1, %0;" ::"n"(C::CT) : "memory");
+
+  const int g8 = lane >> 2, c4 = lane & 3;
+  const int rA = g8, rB = g8 + 8;
+  const int ctx = L - q_len;
+  const int pA = ctx + rA / G, pB = ctx + rB / G;
+  const bool okA = rA < rows, okB = rB < rows;
+  float slopeA = 0.f, slopeB = 0.f;
+  if (p.alibi) {
+    if (okA) slopeA = p.alibi[g * G + rA % G];
+    if (okB) slopeB = p.alibi[g * G + rB % G];
+  }
+  const bool plain = (p.softcap <= 0.f) && (p.alibi == nullptr);
+  // soft-cap without ALiBi: interior tiles need only the capped logit
+  const bool capped = (p.softcap > 0.f) && (p.alibi == nullptr);
+  const float inv_cap = p.softcap > 0.f ? 1.f / p.softcap : 0.f;
+  const float qk_scale = p.scale * (p.k_scale ? *p.k_scale : 1.f);
+  const float vscale = p.v_scale ? *p.v_scale : 1.f;
+  const float scale_log2 = qk_scale * kLog2e;
+  // keys every row admits: tiles inside [full_lo, full_hi) skip the mask
+  int full_lo = lo, full_hi = hi;
+  {
+    const int p_lo = ctx, p_hi = ctx + (rows - 1) / G;
+    if (p.wl >= 0) full_lo = max(full_lo, p_hi - p.wl);
+    if (p.causal) full_hi = min(full_hi, p_lo + 1);
+    if (p.wr >= 0) full_hi = min(full_hi, p_lo + p.wr + 1);
+  }
+
+  float o[D / 8][4];
+#pragma unroll
+  for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
+  const int lm_mi = lane >> 3, lm_r = lane & 7;
+  const int kw0 = warp * C::KW;                 // this warp's keys in a tile
+
+  for (int it = 0; it < n_tiles; ++it) {
+    const int s = it % STAGES;
+    const uint32_t par = (it / STAGES) & 1;
+    const int kt = kt0 + it * KT;
+    if (!mbar_wait(full_k(s), par, abort_flag, p.err)) break;
+    const uint32_t sK = tile_k(s), sV = tile_v(s);
+    if (const unsigned bad = bad_boxes[s]) {
+      // pages the table pointed outside the cache: zero keys and values
+      for (int idx = lane; idx < C::KW * C::CPR; idx += 32) {
+        const int r = kw0 + idx / C::CPR, ch = idx % C::CPR;
+        if (!((bad >> (r / RB)) & 1u)) continue;
+        asm volatile("st.shared.v4.u32 [%0], {%2, %2, %2, %2};\n"
+                     "st.shared.v4.u32 [%1], {%2, %2, %2, %2};" ::"r"(
+                         sK + kv_off<KT>(r, ch)),
+                     "r"(sV + kv_off<KT>(r, ch)), "r"(0)
+                     : "memory");
+      }
+      fence_proxy_async();
+      __syncwarp();
+    }
+
+    // S = Q K^T for 16 rows x KW keys
+    float sc[C::NKT][4];
+#pragma unroll
+    for (int i = 0; i < C::NKT; ++i)
+      sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      uint32_t a[4];
+      {
+        const int r = lm_r + (lm_mi & 1) * 8;
+        const int ch = kk * 2 + (lm_mi >> 1);
+        ldmatrix_x4(sQ + swz<C::ROW_BYTES>(r, ch), a[0], a[1], a[2], a[3]);
+      }
+#pragma unroll
+      for (int np = 0; np < C::NKT / 2; ++np) {
+        uint32_t b0, b1, b2, b3;
+        const int r = kw0 + np * 16 + lm_r + (lm_mi >> 1) * 8;
+        const int ch = kk * 2 + (lm_mi & 1);
+        ldmatrix_x4(sK + kv_off<KT>(r, ch), b0, b1, b2, b3);
+        mma_16816<T>(sc[2 * np], a, b0, b1);
+        mma_16816<T>(sc[2 * np + 1], a, b2, b3);
+      }
+    }
+
+    // logits (base 2) with masks
+    float mxA = -INFINITY, mxB = -INFINITY;
+    const bool interior = kt >= full_lo && kt + KT <= full_hi;
+    if (plain && interior) {
+#pragma unroll
+      for (int nt = 0; nt < C::NKT; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[nt][e] *= scale_log2;
+        mxA = fmaxf(mxA, fmaxf(sc[nt][0], sc[nt][1]));
+        mxB = fmaxf(mxB, fmaxf(sc[nt][2], sc[nt][3]));
+      }
+    } else if (capped && interior) {
+      const float pre = qk_scale * inv_cap, post = p.softcap * kLog2e;
+#pragma unroll
+      for (int nt = 0; nt < C::NKT; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[nt][e] = post * tanh_fast(sc[nt][e] * pre);
+        mxA = fmaxf(mxA, fmaxf(sc[nt][0], sc[nt][1]));
+        mxB = fmaxf(mxB, fmaxf(sc[nt][2], sc[nt][3]));
+      }
+    } else {
+#pragma unroll
+      for (int nt = 0; nt < C::NKT; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int key = kt + kw0 + nt * 8 + 2 * c4 + (e & 1);
+          const bool rowB = e >= 2;
+          const int pos = rowB ? pB : pA;
+          float x = sc[nt][e];
+          if (plain) {
+            x *= scale_log2;
+          } else {
+            x *= qk_scale;
+            if (p.softcap > 0.f) x = p.softcap * tanh_fast(x * inv_cap);
+            if (p.alibi)
+              x -= (rowB ? slopeB : slopeA) * fabsf(float(pos - key));
+            x *= kLog2e;
+          }
+          bool ok = (rowB ? okB : okA) && key >= lo && key < hi;
+          if (p.causal) ok = ok && key <= pos;
+          if (p.wl >= 0) ok = ok && key >= pos - p.wl;
+          if (p.wr >= 0) ok = ok && key <= pos + p.wr;
+          x = ok ? x : -INFINITY;
+          sc[nt][e] = x;
+          if (rowB) mxB = fmaxf(mxB, x); else mxA = fmaxf(mxA, x);
+        }
+      }
+    }
+    mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 1));
+    mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 2));
+    mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 1));
+    mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 2));
+    const float mnA = fmaxf(mA, mxA), mnB = fmaxf(mB, mxB);
+    const float baseA = (mnA == -INFINITY) ? 0.f : mnA;
+    const float baseB = (mnB == -INFINITY) ? 0.f : mnB;
+    const float alA = ex2(mA - baseA), alB = ex2(mB - baseB);
+    mA = mnA;
+    mB = mnB;
+    float sumA = 0.f, sumB = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < C::NKT; ++nt) {
+      sc[nt][0] = ex2(sc[nt][0] - baseA);
+      sc[nt][1] = ex2(sc[nt][1] - baseA);
+      sc[nt][2] = ex2(sc[nt][2] - baseB);
+      sc[nt][3] = ex2(sc[nt][3] - baseB);
+      sumA += sc[nt][0] + sc[nt][1];
+      sumB += sc[nt][2] + sc[nt][3];
+    }
+    lA = lA * alA + sumA;
+    lB = lB * alB + sumB;
+    // once the running maxima settle, alpha is exactly 1: skip the rescale
+    if (__any_sync(0xffffffffu, alA != 1.f || alB != 1.f)) {
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i) {
+        o[i][0] *= alA;
+        o[i][1] *= alA;
+        o[i][2] *= alB;
+        o[i][3] *= alB;
+      }
+    }
+
+    if (!mbar_wait(full_v(s), par, abort_flag, p.err)) break;
+    if (kt + kw0 + C::KW > hi) {
+      // rows of this warp at or past the loaded range: zero them, so that
+      // P = 0 never meets NaN padding or a stale row
+      const int r0 = max(hi - kt, kw0);
+      for (int idx = lane; idx < (kw0 + C::KW - r0) * C::CPR; idx += 32) {
+        const int r = r0 + idx / C::CPR, ch = idx % C::CPR;
+        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(
+                         sV + kv_off<KT>(r, ch)),
+                     "r"(0)
+                     : "memory");
+      }
+      fence_proxy_async();
+      __syncwarp();
+    }
+    // O += P V
+#pragma unroll
+    for (int ks = 0; ks < C::KW / 16; ++ks) {
+      uint32_t a[4];
+      a[0] = pack2<T>(sc[2 * ks][0], sc[2 * ks][1]);
+      a[1] = pack2<T>(sc[2 * ks][2], sc[2 * ks][3]);
+      a[2] = pack2<T>(sc[2 * ks + 1][0], sc[2 * ks + 1][1]);
+      a[3] = pack2<T>(sc[2 * ks + 1][2], sc[2 * ks + 1][3]);
+#pragma unroll
+      for (int dp = 0; dp < D / 16; ++dp) {
+        uint32_t b0, b1, b2, b3;
+        const int r = kw0 + ks * 16 + lm_r + (lm_mi & 1) * 8;
+        const int ch = dp * 2 + (lm_mi >> 1);
+        ldmatrix_x4_trans(sV + kv_off<KT>(r, ch), b0, b1, b2, b3);
+        mma_16816<T>(o[2 * dp], a, b0, b1);
+        mma_16816<T>(o[2 * dp + 1], a, b2, b3);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty(s));
+  }
+
+  lA += __shfl_xor_sync(0xffffffffu, lA, 1);
+  lA += __shfl_xor_sync(0xffffffffu, lA, 2);
+  lB += __shfl_xor_sync(0xffffffffu, lB, 1);
+  lB += __shfl_xor_sync(0xffffffffu, lB, 2);
+
+  // every consumer has finished with the ring: it becomes the combine buffer
+  asm volatile("bar.sync 1, %0;" ::"n"(C::CT) : "memory");
+  if (*abort_flag) return;
+  float* sm_ml = reinterpret_cast<float*>(base);            // [NCW][16][2]
+  float* sm_o = sm_ml + NCW * 16 * 2;                       // [NCW][16][D]
+  if (c4 == 0) {
+    sm_ml[(warp * 16 + g8) * 2 + 0] = mA;
+    sm_ml[(warp * 16 + g8) * 2 + 1] = lA;
+    sm_ml[(warp * 16 + g8 + 8) * 2 + 0] = mB;
+    sm_ml[(warp * 16 + g8 + 8) * 2 + 1] = lB;
+  }
+#pragma unroll
+  for (int dn = 0; dn < D / 8; ++dn) {
+    *reinterpret_cast<float2*>(sm_o + (warp * 16 + g8) * D + dn * 8 + 2 * c4) =
+        make_float2(o[dn][0], o[dn][1]);
+    *reinterpret_cast<float2*>(sm_o + (warp * 16 + g8 + 8) * D + dn * 8 +
+                               2 * c4) = make_float2(o[dn][2], o[dn][3]);
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(C::CT) : "memory");
+
+  const bool split = p.chunk > 0;
+  T* __restrict__ OUT = static_cast<T*>(p.out);
+  for (int i = tid; i < rows * (D / 4); i += C::CT) {
+    const int rr = i / (D / 4), c = (i - rr * (D / 4)) * 4;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NCW; ++w) M = fmaxf(M, sm_ml[(w * 16 + rr) * 2]);
+    const float mb = (M == -INFINITY) ? 0.f : M;
+    float lsum = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < NCW; ++w) {
+      const float f = ex2(sm_ml[(w * 16 + rr) * 2] - mb);
+      lsum += f * sm_ml[(w * 16 + rr) * 2 + 1];
+      const float4 v =
+          *reinterpret_cast<const float4*>(sm_o + (w * 16 + rr) * D + c);
+      acc.x += f * v.x;
+      acc.y += f * v.y;
+      acc.z += f * v.z;
+      acc.w += f * v.w;
+    }
+    const int tok = q0 + rr / G, h = g * G + rr % G;
+    float inv, lse;   // a sink enters once: here, or in the split combine
+    finish_row(M, lsum, split ? nullptr : p.sinks, h, &inv, &lse);
+    inv *= vscale;
+    if (!split) {
+      T* dst = OUT + static_cast<int64_t>(tok) * p.o_st +
+               static_cast<int64_t>(h) * p.o_sh + c;
+      uint2 pk;
+      pk.x = pack2<T>(acc.x * inv, acc.y * inv);
+      pk.y = pack2<T>(acc.z * inv, acc.w * inv);
+      *reinterpret_cast<uint2*>(dst) = pk;
+      if (p.lse && c == 0)
+        p.lse[static_cast<int64_t>(h) * p.total_q + tok] = lse;
+    } else {
+      float* dst = p.part_o +
+                   ((static_cast<int64_t>(blockIdx.x) * p.total_q + tok) *
+                        p.Hq + h) * D + c;
+      *reinterpret_cast<float4*>(dst) =
+          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+      if (c == 0)
+        p.part_lse[(static_cast<int64_t>(blockIdx.x) * p.Hq + h) *
+                       p.total_q + tok] = lse;
+    }
+  }
+}
+
+#ifndef PKV_DTMA_D128_STAGES
+#define PKV_DTMA_D128_STAGES 2
+#endif
+#ifndef PKV_DTMA_D256_STAGES
+#define PKV_DTMA_D256_STAGES 2
+#endif
+#ifndef PKV_DTMA_D64_STAGES
+#define PKV_DTMA_D64_STAGES 4
+#endif
+
+template <typename T, int D, int NCW, int KT, int STAGES>
+cudaError_t launch_cfg(const AttnParams& p, const CUtensorMap& mk,
+                       const CUtensorMap& mv, dim3 grid,
+                       cudaStream_t stream) {
+  using C = Cfg<D, NCW, KT, STAGES>;
+  auto kern = decode_tma_kernel<T, D, NCW, KT, STAGES>;
+  static bool attr_set = false;   // per instantiation; idempotent if racing
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(
+        kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  note_launch();
+  kern<<<grid, C::NT, C::SMEM, stream>>>(p, mk, mv);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t dispatch(const AttnParams& p, int D, const CUtensorMap& mk,
+                     const CUtensorMap& mv, dim3 grid, cudaStream_t s) {
+  switch (D) {
+    case 64:
+      return launch_cfg<T, 64, 4, 64, PKV_DTMA_D64_STAGES>(p, mk, mv, grid, s);
+    case 128:
+      return launch_cfg<T, 128, 4, 64, PKV_DTMA_D128_STAGES>(p, mk, mv, grid,
+                                                             s);
+    case 256:
+      return launch_cfg<T, 256, 2, 32, PKV_DTMA_D256_STAGES>(p, mk, mv, grid,
+                                                             s);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace dtma
+
+int decode_tma_tile_keys(int D) { return D == 256 ? 32 : 64; }
+
+cudaError_t launch_decode_attn_tma(const AttnParams& a, int D, bool bf16,
+                                   int grid_x, cudaStream_t stream) {
+  AttnParams p = a;
+  const int KT = decode_tma_tile_keys(D);
+  int RB = 16;
+  while (RB * 2 <= KT && p.BS % (RB * 2) == 0) RB *= 2;
+  if (p.cu_k) RB = KT;    // non-paged: a box may start on any row
+  p.rb = RB;
+  p.kv_order_hnd = p.c_sh > p.c_sr ? 1 : 0;
+  CUtensorMap mk, mv;
+  if (!make_kv_map(&mk, p.kc, bf16, D, p.BS, p.Hkv, p.num_blocks, p.c_sb,
+                   p.c_sr, p.c_sh, RB, p.kv_order_hnd) ||
+      !make_kv_map(&mv, p.vc, bf16, D, p.BS, p.Hkv, p.num_blocks, p.c_sb,
+                   p.c_sr, p.c_sh, RB, p.kv_order_hnd))
+    return cudaErrorInvalidValue;
+  dim3 grid(grid_x, 1, p.batch * p.Hkv);
+  return bf16 ? dtma::dispatch<__nv_bfloat16>(p, D, mk, mv, grid, stream)
+              : dtma::dispatch<__half>(p, D, mk, mv, grid, stream);
+}
+
+}  // namespace pkv

@@ -22,6 +22,8 @@ __device__ unsigned g_device_error = 0;
 static std::atomic<uint64_t> g_launches{0};
 // prefill kernel: PKV_PREFILL_TCGEN05 or PKV_PREFILL_MMA_SYNC
 static std::atomic<int> g_prefill_kernel{PKV_PREFILL_TCGEN05};
+// decode kernel for 16-bit caches: PKV_DECODE_TMA or PKV_DECODE_CP_ASYNC
+static std::atomic<int> g_decode_kernel{PKV_DECODE_TMA};
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 namespace {
@@ -108,13 +110,16 @@ Plan make_plan(int batch, int total_q, int max_q, int max_k, int Hq, int Hkv,
                          (wr >= 0 ? wr : (causal ? 0 : max_k));
     if (span < range) range = span;
   }
+  // splits start on 64-key boundaries counted from the first admissible
+  // key rounded down; with a left window that adds up to 63 keys of range
+  const int64_t pad = wl >= 0 ? 63 : 0;
   if (fixed_split > 0) {
     // batch-invariant: fixed key ranges, always through the combine
     int64_t chunk = (static_cast<int64_t>(fixed_split) + kDecodeKT - 1) /
                     kDecodeKT * kDecodeKT;
     if (chunk > (1 << 30)) chunk = 1 << 30;
     pl.chunk = static_cast<int>(chunk);
-    const int64_t n = range > 0 ? (range + chunk - 1) / chunk : 1;
+    const int64_t n = range > 0 ? (range + pad + chunk - 1) / chunk : 1;
     pl.splits = static_cast<int>(n > 65535 ? 65535 : n);
   }
   int splits = 1;
@@ -123,10 +128,14 @@ Plan make_plan(int batch, int total_q, int max_q, int max_k, int Hq, int Hkv,
   } else if (num_splits > 1) {
     splits = num_splits;
   } else if (num_splits == 0 && range > 0) {
-    // Aim for ~8 waves of 2 resident CTAs per SM; keep >= 256 keys per split.
+    // Split only to fill the GPU: with at least one (request, KV head) per
+    // resident CTA slot the requests' own length spread balances the SMs,
+    // and a split would only add partials and a combine.  Below that, cut
+    // each range into as many pieces as keep every CTA resident in one
+    // wave.  Keep >= 256 keys per split.
     const int64_t units = static_cast<int64_t>(batch) * Hkv;
-    const int64_t target = static_cast<int64_t>(sms) * 2 * 8;
-    int64_t s = (target + units - 1) / units;
+    const int64_t slots = static_cast<int64_t>(sms) * kDecodeCtasPerSm;
+    int64_t s = units >= slots ? 1 : slots / units;
     const int64_t cap = (range + 255) / 256;
     if (s > cap) s = cap;
     if (s > 64) s = 64;
@@ -137,7 +146,7 @@ Plan make_plan(int batch, int total_q, int max_q, int max_k, int Hq, int Hkv,
     int64_t chunk = (range + splits - 1) / splits;
     chunk = (chunk + kDecodeKT - 1) / kDecodeKT * kDecodeKT;
     pl.chunk = static_cast<int>(chunk);
-    pl.splits = static_cast<int>((range + chunk - 1) / chunk);
+    pl.splits = static_cast<int>((range + pad + chunk - 1) / chunk);
     if (pl.splits <= 1) {
       pl.splits = 1;
       pl.chunk = 0;
@@ -206,6 +215,13 @@ pkv_status pkv_set_prefill_kernel(int which) {
   if (which != PKV_PREFILL_TCGEN05 && which != PKV_PREFILL_MMA_SYNC)
     return fail(PKV_ERR_INVALID_ARG, "unknown prefill kernel %d", which);
   g_prefill_kernel.store(which);
+  return PKV_OK;
+}
+
+pkv_status pkv_set_decode_kernel(int which) {
+  if (which != PKV_DECODE_TMA && which != PKV_DECODE_CP_ASYNC)
+    return fail(PKV_ERR_INVALID_ARG, "unknown decode kernel %d", which);
+  g_decode_kernel.store(which);
   return PKV_OK;
 }
 
@@ -534,7 +550,10 @@ pkv_status pkv_paged_attention_varlen_opts(
       d.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                             pl.part_o_bytes);
     }
-    cudaError_t e = launch_decode_attn(d, head_size, bf16, pl.splits, 1, s);
+    cudaError_t e =
+        (!kv8 && g_decode_kernel.load() == PKV_DECODE_TMA)
+            ? launch_decode_attn_tma(d, head_size, bf16, pl.splits, s)
+            : launch_decode_attn(d, head_size, bf16, pl.splits, 1, s);
     if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
     if (pl.chunk > 0) {
       CombineParams c{};

@@ -151,6 +151,39 @@ __device__ __forceinline__ void key_range(int L, int q_len, int i_first,
   if (kmax < kmin) kmax = kmin;
 }
 
+// Hardware tanh (tanh.approx.f32); its relative error (about 2^-11) keeps
+// soft-capped logits well inside the output tolerance.
+__device__ __forceinline__ float tanh_fast(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Split-KV: split s of a request's key range [kmin, kmax) covers `chunk`
+// keys (a multiple of 64) counted from kmin rounded down to 64, so every
+// split after the first starts on a 64-key boundary.  The last of the
+// request's splits (at most max_splits) takes the rest of the range.
+__device__ __forceinline__ int split_count(int kmin, int kmax, int chunk,
+                                           int max_splits) {
+  const int base = kmin & ~63;
+  return min(max((kmax - base + chunk - 1) / chunk, 1), max_splits);
+}
+__device__ __forceinline__ void split_bounds(int kmin, int kmax, int chunk,
+                                             int nsplit, int s, int& lo,
+                                             int& hi) {
+  const int base = kmin & ~63;
+  lo = max(kmin, base + s * chunk);
+  hi = (s == nsplit - 1) ? kmax : min(kmax, base + (s + 1) * chunk);
+  if (hi < lo) hi = lo;
+}
+
+// Byte offset of 16-byte chunk `ch` of row `r` in a tile whose rows are
+// ROW_BYTES apart, XOR-swizzled over 8-chunk groups (conflict-free ldmatrix).
+template <int ROW_BYTES>
+__device__ __forceinline__ uint32_t swz(int r, int ch) {
+  return static_cast<uint32_t>(r * ROW_BYTES + ((ch ^ (r & 7)) << 4));
+}
+
 // ------------------------------------------------------- internal interface
 
 // Parameters of the block-table attention kernels.
@@ -160,6 +193,8 @@ struct AttnParams {
   const void* kc;
   const void* vc;
   int64_t c_sb, c_sr, c_sh;   // cache strides: block, row-in-block, kv-head
+  int rb;                     // TMA kernels: rows per K/V box
+  int kv_order_hnd;           // TMA kernels: 1 = head stride > row stride
   void* out;
   int64_t o_st, o_sh;
   float* lse;                 // [Hq, total_q] natural log, or null
@@ -240,6 +275,9 @@ void set_last_error(const char* msg);
 // Decode kernel geometry (rows = q_len * G <= kDecodeRows go to it).
 constexpr int kDecodeRows = 16;
 constexpr int kDecodeKT = 64;     // keys per pipeline tile
+// Resident decode CTAs per SM: every decode configuration (both kernels,
+// every head size) takes 66-73 KB of shared memory and <= 21K registers.
+constexpr int kDecodeCtasPerSm = 3;
 
 cudaError_t launch_cache_write(const void* key, const void* value,
                                int64_t k_st, int64_t k_sh, int64_t v_st,
@@ -268,6 +306,10 @@ cudaError_t launch_prefill_attn_mma(const AttnParams& p, int D, bool bf16,
 cudaError_t launch_prefill_attn_tc(const AttnParams& p, int D, bool bf16,
                                    int grid_y, cudaStream_t stream);
 int prefill_tc_block_keys(int D);
+// Decode attention with TMA page loads (decode_tma.cu); 16-bit caches.
+cudaError_t launch_decode_attn_tma(const AttnParams& p, int D, bool bf16,
+                                   int grid_x, cudaStream_t stream);
+
 cudaError_t launch_split_combine(const CombineParams& p, bool bf16,
                                  cudaStream_t stream);
 cudaError_t launch_merge(void* out, const void* o1, const float* l1,

@@ -40,6 +40,7 @@
 #include <type_traits>
 
 #include "pkv_common.cuh"
+#include "tma_util.cuh"
 
 namespace pkv {
 namespace tc {
@@ -48,8 +49,6 @@ constexpr int BM = 128;
 constexpr int NUM_THREADS = 192;
 constexpr int MMA_WARP = 4;
 constexpr int LOAD_WARP = 5;
-constexpr uint32_t kSpinLimit = 1u << 28;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
 constexpr float kRescaleThreshold = 8.f;   // log2 units
 
 // Tile geometry per head size.  D <= 128: 64-key tiles, one P buffer and
@@ -118,81 +117,6 @@ struct TcParams {
 
 // ------------------------------------------------------------ PTX wrappers
 
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar),
-               "r"(count));
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile(
-      "mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
-      "r"(bytes)
-      : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n.reg .pred p;\n"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      "selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(done)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-
-__device__ __forceinline__ uint64_t globaltimer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-  return t;
-}
-
-// Bounded wait: false when the CTA is aborting, or after kWaitLimitNs (then
-// the error word gets kErrTimeout and the CTA-wide abort flag is raised).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          volatile int* abort_flag,
-                                          unsigned* err) {
-  if (mbar_try(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try(bar, parity)) return true;
-    if ((it & 255u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs || it > kSpinLimit) {
-        *abort_flag = 1;
-        atomicOr(err, kErrTimeout);
-        return false;
-      }
-    }
-  }
-}
-
-// Wait used while draining in-flight work: no abort check, still bounded.
-__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 0; it < kSpinLimit; ++it) {
-    if (mbar_try(bar, parity)) return;
-    if ((it & 255u) == 255u && globaltimer_ns() - t0 > kWaitLimitNs) return;
-  }
-}
-
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap,
-                                            int c0, int c1, int c2, int c3,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::"
-      "complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2),
-      "r"(c3), "r"(bar)
-      : "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -310,23 +234,11 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// Byte offset of 16-byte chunk c (0..7) of row r inside a 128-byte-swizzled
-// column block whose rows are 128 bytes apart.
-__device__ __forceinline__ uint32_t sw128(int r, int c) {
-  return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
-}
 
 // ------------------------------------------------------------------ kernel
 
 // Final logit (log2 units) of one score, with soft-cap, ALiBi and the
 // admissibility mask of query position `pos` (general, per-element path).
-// Hardware tanh (MUFU.TANH); its relative error (about 2^-11) keeps soft-
-// capped logits well inside the output tolerance.
-__device__ __forceinline__ float tanh_fast(float x) {
-  float y;
-  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 
 __device__ __forceinline__ float masked_logit(float s, int key, int pos,
                                               bool valid, int kmin, int kmax,
@@ -1397,6 +1309,8 @@ prefill_pp_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
 
 // ------------------------------------------------------------ host side
 
+}  // namespace tc
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -1443,7 +1357,6 @@ bool make_kv_map(CUtensorMap* map, const void* ptr, bool bf16, int D, int BS,
   return r == CUDA_SUCCESS;
 }
 
-}  // namespace tc
 
 int prefill_tc_block_keys(int) { return 64; }
 

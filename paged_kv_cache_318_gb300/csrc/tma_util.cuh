@@ -1,0 +1,108 @@
+// mbarrier and TMA helpers shared by the kernels that move K/V pages with
+// the tensor-memory accelerator (cp.async.bulk.tensor), and the host-side
+// tensor-map builder for a paged cache view.
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+#include "pkv_common.cuh"
+
+namespace pkv {
+
+constexpr uint32_t kSpinLimit = 1u << 28;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+
+// Byte offset of 16-byte chunk c (0..7) of row r inside a 128-byte-swizzled
+// column block whose rows are 128 bytes apart (the layout a TMA box with
+// CU_TENSOR_MAP_SWIZZLE_128B and a 128-byte inner extent writes).
+__device__ __forceinline__ uint32_t sw128(int r, int c) {
+  return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar),
+               "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile(
+      "mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+      "r"(bytes)
+      : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n.reg .pred p;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait: false when the CTA is aborting, or after kWaitLimitNs (then
+// the error word gets kErrTimeout and the CTA-wide abort flag is raised).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          volatile int* abort_flag,
+                                          unsigned* err) {
+  if (mbar_try(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try(bar, parity)) return true;
+    if ((it & 255u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs || it > kSpinLimit) {
+        *abort_flag = 1;
+        atomicOr(err, kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+// Wait used while draining in-flight work: no abort check, still bounded.
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0; it < kSpinLimit; ++it) {
+    if (mbar_try(bar, parity)) return;
+    if ((it & 255u) == 255u && globaltimer_ns() - t0 > kWaitLimitNs) return;
+  }
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap,
+                                            int c0, int c1, int c2, int c3,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::"
+      "complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2),
+      "r"(c3), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 4-D map over one cache view [NB, BS, Hkv, D] (element strides s_blk,
+// s_row, s_head; unit stride along D): dims (D, Hkv, BS, NB) for NHD
+// strides, (D, BS, Hkv, NB) when the head stride is the larger (HND).  The
+// box is 64 x 1 x RB x 1 (NHD) or 64 x RB x 1 x 1 (HND) elements, 128-byte
+// swizzled.  False if the driver entry point is missing or rejects the map.
+bool make_kv_map(CUtensorMap* map, const void* ptr, bool bf16, int D, int BS,
+                 int Hkv, int64_t NB, int64_t s_blk, int64_t s_row,
+                 int64_t s_head, int RB, bool hnd);
+
+}  // namespace pkv

@@ -162,6 +162,42 @@ def test_prefill_kernels(cuda_device, idx, kernel):
     assert_close(wl, out, lse, ref_out, ref_lse, "%s %d" % (kernel, idx))
 
 
+DECODE_CASES = [
+    # q_lens, seq_lens, Hq, Hkv, D, BS, kwargs  (all decode-class)
+    ([1, 1, 1, 1], [1, 15, 16, 17], 8, 2, 128, 16, dict()),
+    ([1, 2, 1], [700, 1500, 90], 8, 4, 128, 16, dict(num_splits=5)),
+    ([1] * 6, [64, 65, 127, 128, 129, 4000], 32, 8, 128, 64, dict()),
+    ([1, 1], [3000, 2999], 16, 8, 256, 32, dict(window_size=(1000, 0),
+                                               softcap=30.0)),
+    ([1, 1, 4], [333, 1030, 77], 8, 2, 64, 16, dict(window_size=(100, 0),
+                                                    num_splits=3)),
+    ([2, 1], [500, 2049], 8, 8, 128, 48, dict()),        # block_size 48
+    ([3, 1], [30, 260], 4, 1, 64, 128, dict(causal=False)),
+    ([1, 1], [900, 901], 16, 2, 128, 16, dict(
+        alibi_slopes=[0.01 * (i + 1) for i in range(16)], dtype="f16")),
+    ([1], [131], 4, 4, 256, 16, dict(window_size=(20, 0))),
+]
+
+
+@pytest.mark.parametrize("kernel", ["tma", "cp_async"])
+@pytest.mark.parametrize("idx", range(len(DECODE_CASES)))
+def test_decode_kernels(cuda_device, idx, kernel):
+    """Both decode kernels over page sizes 16-128 (and a non-power-of-two
+    48), window starts off the tile grid, split counts, poisoned page tails
+    and every head size."""
+    q_lens, seq_lens, Hq, Hkv, D, BS, kw = DECODE_CASES[idx]
+    wl = workloads.build_workload("dec%d" % idx, 950 + idx, q_lens, seq_lens,
+                                  Hq, Hkv, D, BS, **kw)
+    which = api.DECODE_TMA if kernel == "tma" else api.DECODE_CP_ASYNC
+    api.set_decode_kernel(which)
+    try:
+        _, out, lse = run_batch(wl, cuda_device)
+    finally:
+        api.set_decode_kernel(api.DECODE_TMA)
+    ref_out, ref_lse = full_reference(wl)
+    assert_close(wl, out, lse, ref_out, ref_lse, "%s %d" % (kernel, idx))
+
+
 def test_rows_without_keys(cuda_device):
     """seqused_k below the query count: early rows see no key (out 0,
     lse -inf); a request with no keys at all likewise."""
