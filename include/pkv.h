@@ -397,12 +397,15 @@ PKV_API pkv_status pkv_check_device_errors(pkv_stream_t stream);
 
 /*
  * Which kernel serves prefill-class requests (more than 16 packed query rows
- * per KV head): the tcgen05/TMEM kernel or the warp-level mma.sync kernel.
- * A process-wide diagnostic switch for A/B comparison; both give the same
- * result within rounding.  Returns PKV_ERR_INVALID_ARG for other values.
+ * per KV head): the tcgen05/TMEM kernel (for head sizes up to 128 it keeps
+ * the softmax output P in tensor memory), the tcgen05 kernel that stages P
+ * through shared memory, or the warp-level mma.sync kernel.  A process-wide
+ * diagnostic switch for A/B comparison; all give the same result within
+ * rounding.  Returns PKV_ERR_INVALID_ARG for other values.
  */
 #define PKV_PREFILL_TCGEN05 0
 #define PKV_PREFILL_MMA_SYNC 1
+#define PKV_PREFILL_TCGEN05_SMEM_P 2
 PKV_API pkv_status pkv_set_prefill_kernel(int which);
 
 /*

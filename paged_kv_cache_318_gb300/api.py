@@ -157,10 +157,12 @@ def _cache_strides(key_cache, value_cache):
 
 PREFILL_TCGEN05 = 0
 PREFILL_MMA_SYNC = 1
+PREFILL_TCGEN05_SMEM_P = 2
 
 
 def set_prefill_kernel(which: int):
-    """Choose the prefill kernel (PREFILL_TCGEN05 or PREFILL_MMA_SYNC)."""
+    """Choose the prefill kernel (PREFILL_TCGEN05, PREFILL_TCGEN05_SMEM_P
+    or PREFILL_MMA_SYNC)."""
     _check(load_library().pkv_set_prefill_kernel(int(which)))
 
 

@@ -212,7 +212,8 @@ extern "C" {
 const char* pkv_last_error(void) { return g_last_error.c_str(); }
 
 pkv_status pkv_set_prefill_kernel(int which) {
-  if (which != PKV_PREFILL_TCGEN05 && which != PKV_PREFILL_MMA_SYNC)
+  if (which != PKV_PREFILL_TCGEN05 && which != PKV_PREFILL_MMA_SYNC &&
+      which != PKV_PREFILL_TCGEN05_SMEM_P)
     return fail(PKV_ERR_INVALID_ARG, "unknown prefill kernel %d", which);
   g_prefill_kernel.store(which);
   return PKV_OK;
@@ -612,9 +613,11 @@ pkv_status pkv_paged_attention_varlen_opts(
       f.num_blocks = static_cast<int64_t>(pages);
       f.kv_fp8 = 0;          // 16-bit copies; k_scale / v_scale still apply
     }
-    if (g_prefill_kernel.load() == PKV_PREFILL_TCGEN05)
+    const int which = g_prefill_kernel.load();
+    if (which == PKV_PREFILL_TCGEN05 || which == PKV_PREFILL_TCGEN05_SMEM_P)
       e = launch_prefill_attn_tc(f, head_size, bf16,
-                                 static_cast<int>((prow + 127) / 128), s);
+                                 static_cast<int>((prow + 127) / 128),
+                                 which == PKV_PREFILL_TCGEN05, s);
     else
       e = launch_prefill_attn_mma(f, head_size, bf16,
                                   static_cast<int>((prow + 63) / 64), s);

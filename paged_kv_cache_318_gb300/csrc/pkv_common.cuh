@@ -304,7 +304,8 @@ cudaError_t launch_decode_attn(const AttnParams& p, int D, bool bf16,
 cudaError_t launch_prefill_attn_mma(const AttnParams& p, int D, bool bf16,
                                     int grid_y, cudaStream_t stream);
 cudaError_t launch_prefill_attn_tc(const AttnParams& p, int D, bool bf16,
-                                   int grid_y, cudaStream_t stream);
+                                   int grid_y, bool p_in_tmem,
+                                   cudaStream_t stream);
 int prefill_tc_block_keys(int D);
 // Decode attention with TMA page loads (decode_tma.cu); 16-bit caches.
 cudaError_t launch_decode_attn_tma(const AttnParams& p, int D, bool bf16,

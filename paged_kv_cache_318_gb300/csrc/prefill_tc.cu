@@ -1307,6 +1307,581 @@ prefill_pp_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
   }
 }
 
+// ------------------------------- two-tile kernel with P in tensor memory
+//
+// Same work split as prefill_pp_kernel (one CTA = two 128-row Q tiles of a
+// (request, KV head), 8 softmax warps, one MMA warp, K and V loader warps),
+// with 128-key tiles.  Tensor memory holds, per Q tile x, S_x (128 fp32
+// columns) and O_x (D columns).  The softmax reads S_x into registers and
+// writes P_x back as packed 16-bit pairs over the first 64 columns of S_x;
+// the P V MMA then reads its A operand straight from tensor memory, so P
+// never touches shared memory.  Because P_x overwrites S_x, the MMA warp
+// issues P_x(j) V_j before S_x(j+1) = Q_x K_{j+1}^T (tcgen05 MMAs of one
+// thread run in issue order); the overlap comes from the other Q tile,
+// whose MMAs run while this tile's softmax works.
+//
+// Per key tile j of the union of both tiles' ranges the MMA warp issues
+//   P_A(j-1) V_{j-1}, S_A(j), P_B(j-1) V_{j-1}, S_B(j)
+// and each commit to s_full[x] also covers P_x(j-1) V_{j-1}, so when the
+// softmax of tile x sees S_x(j) its O_x is complete (the rare rescale of
+// O_x needs no extra wait).
+constexpr int PT_THREADS = 384;
+constexpr int PT_MMA_WARP = 8;
+constexpr int PT_LOAD_WARP = 9;    // warps 9 (K) and 10 (V); warp 11 idles
+// Register split (setmaxnreg): the launch gives 168 per thread (384 x 168 =
+// 64512); the softmax warpgroups take 224, warpgroup 2 keeps 56:
+// 256 x 224 + 128 x 56 = 64512.  The launcher checks the 168.
+constexpr int PT_LAUNCH_REGS = 168;
+constexpr int PT_SOFTMAX_REGS = 224;
+constexpr int PT_OTHER_REGS = 56;
+static_assert(256 * PT_SOFTMAX_REGS + 128 * PT_OTHER_REGS <=
+                  PT_THREADS * PT_LAUNCH_REGS,
+              "register split exceeds the launch allocation");
+
+template <int D>
+struct PTCfg {
+  static constexpr int BN = 128;
+  static constexpr int NCB = D / 64;
+  static constexpr int Q_BYTES = BM * D * 2;          // one Q tile
+  static constexpr int KV_BYTES = BN * D * 2;
+  static constexpr int STAGES = 2;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int X_COLS = BN + D;               // S_x then O_x
+  static_assert(2 * X_COLS <= TMEM_COLS, "TMEM budget");
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
+  static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
+  static constexpr int OFF_BAR = OFF_V + STAGES * KV_BYTES;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int SMEM = OFF_BAR + BAR_BYTES;
+};
+
+// D += A * B with A (M = 128 rows x K = 16, 16-bit) in tensor memory.
+__device__ __forceinline__ void mma_f16_tmem_a_warp(uint32_t d_tmem,
+                                                    uint32_t a_tmem,
+                                                    uint64_t b, uint32_t id,
+                                                    uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p, e;\nsetp.ne.b32 p, %4, 0;\n"
+      "elect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::
+          "r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(id), "r"(accumulate)
+      : "memory");
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(PT_THREADS, 1)
+prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v) {
+  using C = PTCfg<D>;
+  constexpr int BN = C::BN;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t base_u = smem_u32(smem_raw);
+  unsigned char* base = smem_raw;
+  if (base_u & 1023u) {
+    if (threadIdx.x == 0) atomicOr(p.err, kErrTimeout);
+    return;
+  }
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = p.G;
+
+  // ---- work item: (request, 256-row pair tile, KV head)
+  const int g = blockIdx.x % p.Hkv;
+  const int t_lin = blockIdx.x / p.Hkv;
+  int b = -1, tile = 0, q0 = 0, q_len = 0;
+  {
+    int acc = 0;
+    for (int base_b = 0; base_b < p.batch && b < 0; base_b += 32) {
+      const int bb = base_b + lane;
+      int s0 = 0, ql = 0, nt = 0;
+      if (bb < p.batch) {
+        s0 = p.cu_q[bb];
+        ql = min(p.cu_q[bb + 1] - s0, p.total_q - s0);
+        const int rb = (s0 >= 0 && ql > 0) ? ql * G : 0;
+        nt = rb >= p.min_rows ? (rb + PP_ROWS - 1) / PP_ROWS : 0;
+      }
+      int incl = nt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const bool hit = t_lin >= acc + incl - nt && t_lin < acc + incl;
+      const unsigned m = __ballot_sync(0xffffffffu, hit);
+      if (m) {
+        const int src = __ffs(m) - 1;
+        b = base_b + src;
+        const int excl = __shfl_sync(0xffffffffu, incl - nt, src);
+        const int ntb = __shfl_sync(0xffffffffu, nt, src);
+        q0 = __shfl_sync(0xffffffffu, s0, src);
+        q_len = __shfl_sync(0xffffffffu, ql, src);
+        tile = ntb - 1 - (t_lin - acc - excl);
+      }
+      acc += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
+  if (b < 0) return;
+  const int rows = q_len * G;
+  const int koff = p.cu_k ? p.cu_k[b] : 0;     // non-paged: first key row
+  const int L = p.cu_k ? p.cu_k[b + 1] - koff : p.seqused_k[b];
+  // rows past the table (or, non-paged, past the K/V tensor) are not read
+  const int L_tab = p.cu_k ? (koff < 0 ? 0 : max(0, min(L, p.total_k - koff)))
+                           : min(L, p.max_blocks * p.BS);
+  if (L_tab < L && threadIdx.x == 0) atomicOr(p.err, kErrBadTable);
+  const int ctx = L - q_len;
+  const int RB = p.RB;
+  // per Q tile x: rows [rx0, rx_end), keys [kmn[x], kmx[x])
+  int rx0[2], rx_end[2], kmn[2], kmx[2];
+  bool has[2];
+  int kmin_u = 0x7fffffff, kmax_u = 0;
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    rx0[x] = tile * PP_ROWS + x * BM;
+    rx_end[x] = min(rows, rx0[x] + BM);
+    has[x] = rx_end[x] > rx0[x];
+    kmn[x] = 0;
+    kmx[x] = 0;
+    if (has[x]) {
+      key_range(L, q_len, rx0[x] / G, (rx_end[x] - 1) / G, p.causal, p.wl,
+                p.wr, kmn[x], kmx[x]);
+      kmx[x] = min(kmx[x], L_tab);
+      if (kmx[x] > kmn[x]) {
+        kmin_u = min(kmin_u, kmn[x]);
+        kmax_u = max(kmax_u, kmx[x]);
+      }
+    }
+  }
+  const int kstart = kmax_u > 0 ? (kmin_u / RB) * RB : 0;
+  const int n_tiles = kmax_u > 0 ? (kmax_u - kstart + BN - 1) / BN : 0;
+  // tile ranges [tlo[x], tlo[x] + nx[x]) of each Q tile in the union
+  int tlo[2], nx[2];
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    if (has[x] && kmx[x] > kmn[x]) {
+      tlo[x] = (kmn[x] - kstart) / BN;
+      nx[x] = (kmx[x] - kstart + BN - 1) / BN - tlo[x];
+    } else {
+      tlo[x] = 0;
+      nx[x] = 0;
+    }
+  }
+  T* __restrict__ OUT = static_cast<T*>(p.out);
+  const bool plain = p.softcap <= 0.f && p.alibi == nullptr;
+
+  const uint32_t sQ = base_u + C::OFF_Q;
+  const uint32_t sK = base_u + C::OFF_K;
+  const uint32_t sV = base_u + C::OFF_V;
+  const uint32_t bar0 = base_u + C::OFF_BAR;
+  auto k_full = [&](int s) { return bar0 + 8 * (0 + s); };
+  auto v_full = [&](int s) { return bar0 + 8 * (2 + s); };
+  auto k_empty = [&](int s) { return bar0 + 8 * (4 + s); };
+  auto v_empty = [&](int s) { return bar0 + 8 * (6 + s); };
+  auto s_full = [&](int x) { return bar0 + 8 * (8 + x); };
+  auto p_full = [&](int x) { return bar0 + 8 * (10 + x); };
+  const uint32_t final_bar = bar0 + 8 * 12;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + C::OFF_BAR + 8 * 14);
+  volatile int* abort_flag =
+      reinterpret_cast<volatile int*>(base + C::OFF_BAR + 8 * 14 + 4);
+
+  if (n_tiles > 0) {
+    if (tid == 0) {
+      for (int s = 0; s < 2; ++s) {
+        mbar_init(k_full(s), 1);
+        mbar_init(v_full(s), 1);
+        mbar_init(k_empty(s), 1);
+        mbar_init(v_empty(s), 1);
+        mbar_init(s_full(s), 1);
+        mbar_init(p_full(s), 128);
+      }
+      mbar_init(final_bar, 1);
+      *abort_flag = 0;
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == PT_MMA_WARP) {
+      asm volatile(
+          "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], "
+          "%1;" ::"r"(smem_u32(tmem_slot)),
+          "r"(C::TMEM_COLS)
+          : "memory");
+      asm volatile(
+          "tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::
+              : "memory");
+    }
+    // Q tiles A and B: packed rows, zero past each tile's end
+    const T* Q = static_cast<const T*>(p.q);
+    for (int i = tid; i < PP_ROWS * (D / 8); i += PT_THREADS) {
+      const int rr = i / (D / 8), ch = i % (D / 8);
+      const int x = rr / BM, r = rr % BM;
+      const int R = rx0[x] + r;
+      const bool ok = R < rx_end[x];
+      const T* src = Q;
+      if (ok)
+        src = Q + static_cast<int64_t>(q0 + R / G) * p.q_st +
+              static_cast<int64_t>(g * G + R % G) * p.q_sh + ch * 8;
+      cp_async_16(sQ + x * C::Q_BYTES + (ch >> 3) * (BM * 128) +
+                      sw128(r, ch & 7),
+                  src, ok ? 16 : 0);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    fence_proxy_async();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = n_tiles > 0 ? *tmem_slot : 0;
+
+  if (warp >= 8) {
+  // warpgroup 2 (MMA, loaders, one idle warp) gives registers back to the
+  // softmax warpgroups, all four warps on this one instruction
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(PT_OTHER_REGS));
+  if (warp == PT_LOAD_WARP || warp == PT_LOAD_WARP + 1) {
+    if (n_tiles > 0) {
+      // ------------------------------------------------------ producers
+      // warp 9 loads K tiles, warp 10 V tiles; lane i issues box i of each
+      // tile and prefetches its page id one tile ahead
+      const int mat = warp - PT_LOAD_WARP;       // 0: K, 1: V
+      const int32_t* bt =
+          p.cu_k ? nullptr
+                 : p.block_table + static_cast<int64_t>(b) * p.bt_stride;
+      auto fetch = [&](int j) -> int {
+        const int k0 = kstart + j * BN + lane * RB;
+        if (j >= n_tiles || lane >= BN / RB || k0 >= kmax_u || !bt) return 0;
+        const int blk = __ldg(bt + k0 / p.BS);
+        if (blk < 0 || blk >= p.num_blocks) {
+          atomicOr(p.err, kErrBadBlock);
+          return 0;
+        }
+        return blk;
+      };
+      const void* tm = mat ? static_cast<const void*>(&tm_v)
+                           : static_cast<const void*>(&tm_k);
+      int issued = 0;
+      int cur = fetch(0);
+      for (int j = 0; j < n_tiles; ++j) {
+        const int nxt = fetch(j + 1);
+        const int s = j & 1;
+        const int kt = kstart + j * BN;
+        int nbox = (kmax_u - kt + RB - 1) / RB;
+        if (nbox > BN / RB) nbox = BN / RB;
+        const uint32_t full = mat ? v_full(s) : k_full(s);
+        int stop = 0;
+        if (lane == 0) {
+          const uint32_t empty = mat ? v_empty(s) : k_empty(s);
+          if (j >= 2 && !mbar_wait(empty, ((j >> 1) & 1) ^ 1, abort_flag,
+                                   p.err))
+            stop = 1;
+          else
+            mbar_expect_tx(full, nbox * C::NCB * RB * 128);
+        }
+        stop = __shfl_sync(0xffffffffu, stop, 0);
+        if (stop) break;
+        if (lane < nbox) {
+          const uint32_t dst0 = (mat ? sV : sK) + s * C::KV_BYTES;
+          const int k0 = kt + lane * RB;
+          const int row = p.cu_k ? koff + k0 : k0 % p.BS;
+          for (int cb = 0; cb < C::NCB; ++cb) {
+            const uint32_t dst = dst0 + cb * (BN * 128) + lane * RB * 128;
+            if (p.kv_order_hnd)
+              tma_load_4d(dst, tm, cb * 64, row, g, cur, full);
+            else
+              tma_load_4d(dst, tm, cb * 64, g, row, cur, full);
+          }
+        }
+        issued = j + 1;
+        cur = nxt;
+      }
+      if (lane == 0) {
+        for (int t = max(0, issued - 2); t < issued; ++t)
+          mbar_drain(mat ? v_full(t & 1) : k_full(t & 1), (t >> 1) & 1);
+      }
+    }
+  } else if (warp == PT_MMA_WARP) {
+    if (n_tiles > 0) {
+      // ---------------------------------------------------- MMA issuer
+      constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value;
+      constexpr uint32_t ID_S = idesc(128, BN, kBF16, false);
+      constexpr uint32_t ID_PV = idesc(128, D, kBF16, true);
+      bool ok = true;
+      auto in_range = [&](int x, int j) {
+        return j >= tlo[x] && j < tlo[x] + nx[x];
+      };
+      // V_i resident (rows past the keys zeroed); false on abort
+      auto v_ready = [&](int i) -> bool {
+        const int s = i & 1;
+        if (!mbar_wait(v_full(s), (i >> 1) & 1, abort_flag, p.err))
+          return false;
+        const int kt = kstart + i * BN;
+        int nbox = (kmax_u - kt + RB - 1) / RB;
+        if (nbox > BN / RB) nbox = BN / RB;
+        const int r0 = min(nbox * RB, max(L - kt, 0));
+        if (r0 < BN) {
+          // rows past the last key may hold another request's NaN padding
+          const uint32_t v0 = sV + s * C::KV_BYTES;
+          for (int idx = lane; idx < (BN - r0) * 8 * C::NCB; idx += 32) {
+            const int cb = idx / ((BN - r0) * 8);
+            const int rem = idx - cb * ((BN - r0) * 8);
+            const int r = r0 + rem / 8, c = rem % 8;
+            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(
+                             v0 + cb * (BN * 128) + r * 128 + (c << 4)),
+                         "r"(0)
+                         : "memory");
+          }
+          fence_proxy_async();
+          __syncwarp();
+        }
+        return true;
+      };
+      auto issue_pv = [&](int x, int i) -> bool {
+        const int ix = i - tlo[x];
+        if (!mbar_wait(p_full(x), ix & 1, abort_flag, p.err)) return false;
+        tc_fence_after();
+        const uint64_t b0 = sdesc(sV + (i & 1) * C::KV_BYTES, BN * 128, 1024);
+        const uint32_t s_col = tmem + x * C::X_COLS;
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k)
+          mma_f16_tmem_a_warp(s_col + BN, s_col + 8 * k,
+                              b0 + ((k * 16 * 128) >> 4), ID_PV,
+                              (ix > 0 || k > 0) ? 1 : 0);
+        return true;
+      };
+      auto issue_s = [&](int x, int j) {
+        const uint64_t a0 = sdesc(sQ + x * C::Q_BYTES, 16, 1024);
+        const uint64_t b0 = sdesc(sK + (j & 1) * C::KV_BYTES, 16, 1024);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          mma_f16_warp(tmem + x * C::X_COLS,
+                       a0 + (((k >> 2) * (BM * 128) + (k & 3) * 32) >> 4),
+                       b0 + (((k >> 2) * (BN * 128) + (k & 3) * 32) >> 4),
+                       ID_S, k > 0 ? 1 : 0);
+        mma_commit_warp(s_full(x));
+      };
+      for (int j = 0; j <= n_tiles && ok; ++j) {
+        const int s = j & 1;
+        const bool pv = j >= 1;              // P(j-1) V_{j-1} this round
+        const bool sj = j < n_tiles;         // S(j) this round
+        bool k_here = false;                 // K_j waited for
+        if (pv && !v_ready(j - 1)) {
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          if (pv && in_range(x, j - 1) && !issue_pv(x, j - 1)) {
+            ok = false;
+            break;
+          }
+          if (sj && in_range(x, j)) {
+            if (!k_here) {
+              if (!mbar_wait(k_full(s), (j >> 1) & 1, abort_flag, p.err)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              k_here = true;
+            }
+            issue_s(x, j);
+          }
+        }
+        if (!ok) break;
+        if (sj) mma_commit_warp(k_empty(s));
+        if (pv) mma_commit_warp(v_empty((j - 1) & 1));
+      }
+      mma_commit_warp(final_bar);
+      mbar_drain(final_bar, 0);
+    }
+  }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(PT_SOFTMAX_REGS));
+    // ---------------------------------------------- softmax warpgroups
+    const int x = warp >> 2;                  // 0: tile A, 1: tile B
+    const int r = tid & 127;                  // row in tile == TMEM lane
+    const int my_rx0 = x ? rx0[1] : rx0[0];
+    const int my_rx_end = x ? rx_end[1] : rx_end[0];
+    const bool my_has = x ? has[1] : has[0];
+    const int my_tlo = x ? tlo[1] : tlo[0];
+    const int my_nx = x ? nx[1] : nx[0];
+    const int R = my_rx0 + r;
+    const bool valid = R < my_rx_end;
+    const int pos = ctx + (valid ? R / G : 0);
+    const int h = g * G + (valid ? R % G : 0);
+    const int tok = q0 + (valid ? R / G : 0);
+    const float slope = (p.alibi && valid) ? p.alibi[h] : 0.f;
+    const float qk_scale = p.scale * (p.k_scale ? *p.k_scale : 1.f);
+    const float vscale = p.v_scale ? *p.v_scale : 1.f;
+    const float scale_log2 = qk_scale * kLog2e;
+    const float inv_cap = p.softcap > 0.f ? 1.f / p.softcap : 0.f;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t s_addr = tmem + lane_base + x * C::X_COLS;
+    const uint32_t o_addr = s_addr + BN;
+    const int kmin = x ? kmn[1] : kmn[0], kmax = x ? kmx[1] : kmx[0];
+    int full_lo = kmin, full_hi = kmax;
+    if (my_has) {
+      const int p_lo = ctx + my_rx0 / G, p_hi = ctx + (my_rx_end - 1) / G;
+      if (p.wl >= 0) full_lo = max(full_lo, p_hi - p.wl);
+      if (p.causal) full_hi = min(full_hi, p_lo + 1);
+      if (p.wr >= 0) full_hi = min(full_hi, p_lo + p.wr + 1);
+    }
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int jx = 0; jx < my_nx; ++jx) {
+      if (!mbar_wait(s_full(x), jx & 1, abort_flag, p.err)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int kt = kstart + (my_tlo + jx) * BN;
+      const bool unmasked = kt >= full_lo && kt + BN <= full_hi;
+      float v[BN];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_addr + c * 32, v + c * 32);
+      tmem_wait_ld();
+      // logits in log2 units; keys outside this row's admissible interval
+      // [a_lo, a_hi) (causal, window, split range) become -inf.  The
+      // interval test keeps the masked code short: a fully unrolled
+      // per-key predicate chain over 128 keys overflows the instruction
+      // cache.
+      int lo_rel = 0, n_rel = BN;               // admissible e in [lo, lo+n)
+      if (!unmasked) {
+        int a_lo = kmin, a_hi = kmax;
+        if (p.causal) a_hi = min(a_hi, pos + 1);
+        if (p.wl >= 0) a_lo = max(a_lo, pos - p.wl);
+        if (p.wr >= 0) a_hi = min(a_hi, pos + p.wr + 1);
+        if (!valid) a_hi = a_lo;
+        lo_rel = a_lo - kt;
+        n_rel = max(a_hi - a_lo, 0);
+      }
+      float mx8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
+      if (plain && unmasked) {
+#pragma unroll
+        for (int e = 0; e < BN; ++e) {
+          v[e] *= scale_log2;
+          mx8[e & 7] = fmaxf(mx8[e & 7], v[e]);
+        }
+      } else if (plain) {
+#pragma unroll
+        for (int e = 0; e < BN; ++e) {
+          const bool in = static_cast<unsigned>(e - lo_rel) <
+                          static_cast<unsigned>(n_rel);
+          v[e] = in ? v[e] * scale_log2 : -INFINITY;
+          mx8[e & 7] = fmaxf(mx8[e & 7], v[e]);
+        }
+      } else {
+        // soft-cap and / or ALiBi (their own slower path)
+#pragma unroll
+        for (int e = 0; e < BN; ++e) {
+          float x = v[e] * qk_scale;
+          if (p.softcap > 0.f) x = p.softcap * tanh_fast(x * inv_cap);
+          if (p.alibi) x -= slope * fabsf(float(pos - (kt + e)));
+          const bool in = static_cast<unsigned>(e - lo_rel) <
+                          static_cast<unsigned>(n_rel);
+          v[e] = in ? x * kLog2e : -INFINITY;
+          mx8[e & 7] = fmaxf(mx8[e & 7], v[e]);
+        }
+      }
+      const float mx =
+          fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      const bool grow = mx > m_ref + kRescaleThreshold;
+      float alpha = 1.f;
+      if (grow) {
+        alpha = ex2(m_ref - mx);
+        m_ref = mx;
+        l *= alpha;
+      }
+      const float base_m = (m_ref == -INFINITY) ? 0.f : m_ref;
+      if (jx >= 1 && __any_sync(0xffffffffu, grow)) {
+        // O_x is complete: the commit behind s_full covered P(j-1) V
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          float ov[32];
+          tmem_ld32(o_addr + c * 32, ov);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ov[e] *= alpha;
+          tmem_st32(o_addr + c * 32, ov);
+        }
+      }
+      float sum8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sum8[e] = 0.f;
+#pragma unroll
+      for (int e = 0; e < BN; ++e) {
+        v[e] = ex2(v[e] - base_m);
+        sum8[e & 7] += v[e];
+      }
+      // P_x over the first BN / 2 columns of S_x: column c holds the keys
+      // 2c (low half) and 2c + 1 (high half)
+#pragma unroll
+      for (int c = 0; c < BN / 64; ++c) {
+        float pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          pk[e] = __uint_as_float(pack2<T>(v[c * 64 + 2 * e],
+                                           v[c * 64 + 2 * e + 1]));
+        tmem_st32(s_addr + c * 32, pk);
+      }
+      l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
+           ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_full(x));
+    }
+    T* dst = OUT + static_cast<int64_t>(tok) * p.o_st +
+             static_cast<int64_t>(h) * p.o_sh;
+    if (my_nx == 0) {
+      // no admissible key for this tile's rows: out = 0, lse = -inf
+      if (valid) {
+#pragma unroll
+        for (int c = 0; c < D; c += 8)
+          *reinterpret_cast<uint4*>(dst + c) = make_uint4(0, 0, 0, 0);
+        if (p.lse)
+          p.lse[static_cast<int64_t>(h) * p.total_q + tok] =
+              p.sinks ? p.sinks[h] : -INFINITY;
+      }
+    } else if (ok) {
+      if (mbar_wait(final_bar, 0, abort_flag, p.err)) {
+        tc_fence_after();
+        float inv, lse_v;
+        finish_row(m_ref, l, p.sinks, h, &inv, &lse_v);
+        inv *= vscale;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          float ov[32];
+          tmem_ld32(o_addr + c * 32, ov);
+          tmem_wait_ld();
+          if (valid) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 8) {
+              uint4 pk;
+              pk.x = pack2<T>(ov[e] * inv, ov[e + 1] * inv);
+              pk.y = pack2<T>(ov[e + 2] * inv, ov[e + 3] * inv);
+              pk.z = pack2<T>(ov[e + 4] * inv, ov[e + 5] * inv);
+              pk.w = pack2<T>(ov[e + 6] * inv, ov[e + 7] * inv);
+              *reinterpret_cast<uint4*>(dst + c * 32 + e) = pk;
+            }
+          }
+        }
+        if (valid && p.lse)
+          p.lse[static_cast<int64_t>(h) * p.total_q + tok] = lse_v;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == PT_MMA_WARP && n_tiles > 0) {
+    tc_fence_after();
+    asm volatile(
+        "tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+        "r"(C::TMEM_COLS)
+        : "memory");
+  }
+}
+
 // ------------------------------------------------------------ host side
 
 }  // namespace tc
@@ -1361,7 +1936,8 @@ bool make_kv_map(CUtensorMap* map, const void* ptr, bool bf16, int D, int BS,
 int prefill_tc_block_keys(int) { return 64; }
 
 cudaError_t launch_prefill_attn_tc(const AttnParams& a, int D, bool bf16,
-                                   int grid_y, cudaStream_t stream) {
+                                   int grid_y, bool p_in_tmem,
+                                   cudaStream_t stream) {
   using namespace tc;
   TcParams p{};
   p.q = a.q;
@@ -1420,20 +1996,66 @@ cudaError_t launch_prefill_attn_tc(const AttnParams& a, int D, bool bf16,
   const int64_t gx = tiles * a.Hkv;
   if (gx <= 0 || gx > 0x7fffffff) return cudaErrorInvalidValue;
   dim3 grid(static_cast<unsigned>(gx));
-  static bool attr_set[2][3] = {};   // [bf16][D index]; idempotent if racing
-  const int di = D == 64 ? 0 : (D == 128 ? 1 : 2);
   auto go = [&](void (*kern)(TcParams, CUtensorMap, CUtensorMap), int smem,
                 int threads) -> cudaError_t {
-    if (!attr_set[bf16][di]) {
+    // shared-memory opt-in once per kernel (a short list: 10 kernels)
+    static std::mutex mu;
+    static const void* done[16] = {};
+    std::lock_guard<std::mutex> lk(mu);
+    int i = 0;
+    while (i < 16 && done[i] && done[i] != reinterpret_cast<const void*>(kern))
+      ++i;
+    if (i == 16 || !done[i]) {
       cudaError_t e = cudaFuncSetAttribute(
           kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (e != cudaSuccess) return e;
-      attr_set[bf16][di] = true;
+      if (i < 16) done[i] = reinterpret_cast<const void*>(kern);
     }
     note_launch();
     kern<<<grid, threads, smem, stream>>>(p, mk, mv);
     return cudaGetLastError();
   };
+  if (p_in_tmem) {
+    // the register split inside the kernel assumes exactly PT_LAUNCH_REGS
+    // per thread at launch; anything else falls back to the kernel that
+    // stages P through shared memory
+    static int regs[2][2] = {};
+    const int bi = bf16 ? 1 : 0, di = D == 64 ? 0 : 1;
+    if (D <= 128 && regs[bi][di] == 0) {
+      cudaFuncAttributes fa;
+      cudaError_t e = cudaFuncGetAttributes(
+          &fa, bf16 ? (D == 64 ? (const void*)prefill_ptmem_kernel<__nv_bfloat16, 64>
+                               : (const void*)prefill_ptmem_kernel<__nv_bfloat16, 128>)
+                    : (D == 64 ? (const void*)prefill_ptmem_kernel<__half, 64>
+                               : (const void*)prefill_ptmem_kernel<__half, 128>));
+      if (e != cudaSuccess) return e;
+      regs[bi][di] = fa.numRegs;
+    }
+    if (D <= 128 && regs[bi][di] != PT_LAUNCH_REGS) p_in_tmem = false;
+  }
+  if (p_in_tmem && bf16) {
+    switch (D) {
+      case 64:
+        return go(prefill_ptmem_kernel<__nv_bfloat16, 64>, PTCfg<64>::SMEM,
+                  PT_THREADS);
+      case 128:
+        return go(prefill_ptmem_kernel<__nv_bfloat16, 128>,
+                  PTCfg<128>::SMEM, PT_THREADS);
+      default:
+        break;
+    }
+  } else if (p_in_tmem) {
+    switch (D) {
+      case 64:
+        return go(prefill_ptmem_kernel<__half, 64>, PTCfg<64>::SMEM,
+                  PT_THREADS);
+      case 128:
+        return go(prefill_ptmem_kernel<__half, 128>, PTCfg<128>::SMEM,
+                  PT_THREADS);
+      default:
+        break;
+    }
+  }
   if (bf16) {
     switch (D) {
       case 64:

@@ -145,14 +145,16 @@ PREFILL_CASES = [
 ]
 
 
-@pytest.mark.parametrize("kernel", ["tcgen05", "mma_sync"])
+@pytest.mark.parametrize("kernel", ["tcgen05", "tcgen05_smem_p",
+                                    "mma_sync"])
 @pytest.mark.parametrize("idx", range(len(PREFILL_CASES)))
 def test_prefill_kernels(cuda_device, idx, kernel):
     q_lens, seq_lens, Hq, Hkv, D, BS, kw = PREFILL_CASES[idx]
     wl = workloads.build_workload("pre%d" % idx, 900 + idx, q_lens, seq_lens,
                                   Hq, Hkv, D, BS, **kw)
-    which = api.PREFILL_TCGEN05 if kernel == "tcgen05" else \
-        api.PREFILL_MMA_SYNC
+    which = {"tcgen05": api.PREFILL_TCGEN05,
+             "tcgen05_smem_p": api.PREFILL_TCGEN05_SMEM_P,
+             "mma_sync": api.PREFILL_MMA_SYNC}[kernel]
     api.set_prefill_kernel(which)
     try:
         _, out, lse = run_batch(wl, cuda_device)
