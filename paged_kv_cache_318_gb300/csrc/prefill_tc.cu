@@ -1356,6 +1356,25 @@ struct PTCfg {
   static constexpr int SMEM = OFF_BAR + BAR_BYTES;
 };
 
+// Packed pair arithmetic on the FMA pipe (one instruction for two fp32
+// values): (a0, a1) = (a0, a1) * s + c and (s0, s1) += (a0, a1).
+__device__ __forceinline__ void fma2(float& a0, float& a1, float s, float c) {
+  uint64_t a, sv, cv;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(sv) : "f"(s));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(cv) : "f"(c));
+  asm("fma.rn.f32x2 %0, %0, %1, %2;" : "+l"(a) : "l"(sv), "l"(cv));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(a));
+}
+__device__ __forceinline__ void add2(float& s0, float& s1, float a0,
+                                     float a1) {
+  uint64_t sv, av;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(sv) : "f"(s0), "f"(s1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(av) : "f"(a0), "f"(a1));
+  asm("add.rn.f32x2 %0, %0, %1;" : "+l"(sv) : "l"(av));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(s0), "=f"(s1) : "l"(sv));
+}
+
 // D += A * B with A (M = 128 rows x K = 16, 16-bit) in tensor memory.
 __device__ __forceinline__ void mma_f16_tmem_a_warp(uint32_t d_tmem,
                                                     uint32_t a_tmem,
@@ -1755,12 +1774,12 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
       float mx8[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
-      if (plain && unmasked) {
+      // interior tiles keep the raw scores: max(scale * s) = scale * max(s)
+      // for scale > 0, and the scale joins the exponent's FMA below
+      const bool raw = plain && unmasked && scale_log2 > 0.f;
+      if (raw) {
 #pragma unroll
-        for (int e = 0; e < BN; ++e) {
-          v[e] *= scale_log2;
-          mx8[e & 7] = fmaxf(mx8[e & 7], v[e]);
-        }
+        for (int e = 0; e < BN; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], v[e]);
       } else if (plain) {
 #pragma unroll
         for (int e = 0; e < BN; ++e) {
@@ -1782,9 +1801,10 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
           mx8[e & 7] = fmaxf(mx8[e & 7], v[e]);
         }
       }
-      const float mx =
+      float mx =
           fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                 fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      if (raw) mx *= scale_log2;
       const bool grow = mx > m_ref + kRescaleThreshold;
       float alpha = 1.f;
       if (grow) {
@@ -1808,10 +1828,16 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
       float sum8[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) sum8[e] = 0.f;
+      const float sc = raw ? scale_log2 : 1.f;
 #pragma unroll
-      for (int e = 0; e < BN; ++e) {
-        v[e] = ex2(v[e] - base_m);
-        sum8[e & 7] += v[e];
+      for (int e = 0; e < BN; e += 2) {
+        float x0 = v[e], x1 = v[e + 1];
+        fma2(x0, x1, sc, -base_m);
+        x0 = ex2(x0);
+        x1 = ex2(x1);
+        v[e] = x0;
+        v[e + 1] = x1;
+        add2(sum8[2 * ((e >> 1) & 3)], sum8[2 * ((e >> 1) & 3) + 1], x0, x1);
       }
       // P_x over the first BN / 2 columns of S_x: column c holds the keys
       // 2c (low half) and 2c + 1 (high half)
