@@ -111,6 +111,8 @@ struct TcParams {
   int causal, wl, wr;
   int min_rows;
   int batch;
+  int n_items;            // persistent kernel: work items (an upper bound)
+  int out_v8;             // output rows 32-byte aligned: 256-bit stores
   int kv_order_hnd;   // tensor-map dim order: 1 = (D, BS, Hkv, NB)
   unsigned* err;
 };
@@ -1329,11 +1331,11 @@ constexpr int PT_THREADS = 384;
 constexpr int PT_MMA_WARP = 8;
 constexpr int PT_LOAD_WARP = 9;    // warps 9 (K) and 10 (V); warp 11 idles
 // Register split (setmaxnreg): the launch gives 168 per thread (384 x 168 =
-// 64512); the softmax warpgroups take 224, warpgroup 2 keeps 56:
-// 256 x 224 + 128 x 56 = 64512.  The launcher checks the 168.
+// 64512); the softmax warpgroups take 200, warpgroup 2 keeps 96:
+// 256 x 200 + 128 x 96 = 63488.  The launcher checks the 168.
 constexpr int PT_LAUNCH_REGS = 168;
-constexpr int PT_SOFTMAX_REGS = 224;
-constexpr int PT_OTHER_REGS = 56;
+constexpr int PT_SOFTMAX_REGS = 200;
+constexpr int PT_OTHER_REGS = 96;
 static_assert(256 * PT_SOFTMAX_REGS + 128 * PT_OTHER_REGS <=
                   PT_THREADS * PT_LAUNCH_REGS,
               "register split exceeds the launch allocation");
@@ -1353,8 +1355,22 @@ struct PTCfg {
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
   static constexpr int OFF_BAR = OFF_V + STAGES * KV_BYTES;
   static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM = OFF_BAR + BAR_BYTES;
+  // per-request metadata (cu_seqlens_q, key count, key offset) cached in
+  // shared memory for batches up to META_MAX requests
+  static constexpr int META_MAX = 2048;
+  static constexpr int OFF_META = OFF_BAR + BAR_BYTES;
+  static constexpr int META_BYTES = (3 * META_MAX + 4) * 4;
+  static constexpr int SMEM = OFF_META + META_BYTES;
 };
+
+// 32 bytes to global memory in one store (address 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t* w) {
+  asm volatile(
+      "st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr),
+      "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]),
+      "r"(w[6]), "r"(w[7])
+      : "memory");
+}
 
 // Packed pair arithmetic on the FMA pipe (one instruction for two fp32
 // values): (a0, a1) = (a0, a1) * s + c and (s0, s1) += (a0, a1).
@@ -1389,6 +1405,117 @@ __device__ __forceinline__ void mma_f16_tmem_a_warp(uint32_t d_tmem,
       : "memory");
 }
 
+// Geometry of one work item (request b, 256-row pair tile, KV head g),
+// computed by every warp that needs it (a warp-wide scan over cu_seqlens_q;
+// all lanes must call it).  False for an index past the real items.
+struct PtItem {
+  int b, g, q0, q_len, rows, L, ctx, koff, L_tab;
+  int rx0[2], rx_end[2], kmn[2], kmx[2], tlo[2], nx[2];
+  bool has[2];
+  int kstart, kmax_u, n_tiles;
+};
+
+struct PtMeta {
+  const int* cu_q;     // [batch + 1]
+  const int* len;      // [batch]: key count
+  const int* koff;     // [batch]: first key row (non-paged), else 0
+  bool cached;         // false: read the caller's arrays in global memory
+};
+
+__device__ __forceinline__ bool pt_item(const TcParams& p, int item, int lane,
+                                        int BN, const PtMeta& md,
+                                        PtItem& it) {
+  const int G = p.G;
+  it.g = item % p.Hkv;
+  const int t_lin = item / p.Hkv;
+  int b = -1, tile = 0, q0 = 0, q_len = 0;
+  int acc = 0;
+  for (int base_b = 0; base_b < p.batch && b < 0; base_b += 32) {
+    const int bb = base_b + lane;
+    int s0 = 0, ql = 0, nt = 0;
+    if (bb < p.batch) {
+      s0 = md.cached ? md.cu_q[bb] : p.cu_q[bb];
+      const int s1 = md.cached ? md.cu_q[bb + 1] : p.cu_q[bb + 1];
+      ql = min(s1 - s0, p.total_q - s0);
+      const int rb = (s0 >= 0 && ql > 0) ? ql * G : 0;
+      nt = rb >= p.min_rows ? (rb + PP_ROWS - 1) / PP_ROWS : 0;
+    }
+    int incl = nt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const bool hit = t_lin >= acc + incl - nt && t_lin < acc + incl;
+    const unsigned m = __ballot_sync(0xffffffffu, hit);
+    if (m) {
+      const int src = __ffs(m) - 1;
+      b = base_b + src;
+      const int excl = __shfl_sync(0xffffffffu, incl - nt, src);
+      const int ntb = __shfl_sync(0xffffffffu, nt, src);
+      q0 = __shfl_sync(0xffffffffu, s0, src);
+      q_len = __shfl_sync(0xffffffffu, ql, src);
+      tile = ntb - 1 - (t_lin - acc - excl);
+    }
+    acc += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (b < 0) return false;
+  it.b = b;
+  it.q0 = q0;
+  it.q_len = q_len;
+  it.rows = q_len * G;
+  if (md.cached) {
+    it.koff = md.koff[b];
+    it.L = md.len[b];
+  } else {
+    it.koff = p.cu_k ? p.cu_k[b] : 0;        // non-paged: first key row
+    it.L = p.cu_k ? p.cu_k[b + 1] - it.koff : p.seqused_k[b];
+  }
+  // rows past the table (or, non-paged, past the K/V tensor) are not read
+  it.L_tab = p.cu_k ? (it.koff < 0 ? 0 : max(0, min(it.L, p.total_k - it.koff)))
+                    : min(it.L, p.max_blocks * p.BS);
+  it.ctx = it.L - q_len;
+  int kmin_u = 0x7fffffff, kmax_u = 0;
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    it.rx0[x] = tile * PP_ROWS + x * BM;
+    it.rx_end[x] = min(it.rows, it.rx0[x] + BM);
+    it.has[x] = it.rx_end[x] > it.rx0[x];
+    it.kmn[x] = 0;
+    it.kmx[x] = 0;
+    if (it.has[x]) {
+      key_range(it.L, q_len, it.rx0[x] / G, (it.rx_end[x] - 1) / G, p.causal,
+                p.wl, p.wr, it.kmn[x], it.kmx[x]);
+      it.kmx[x] = min(it.kmx[x], it.L_tab);
+      if (it.kmx[x] > it.kmn[x]) {
+        kmin_u = min(kmin_u, it.kmn[x]);
+        kmax_u = max(kmax_u, it.kmx[x]);
+      }
+    }
+  }
+  it.kmax_u = kmax_u;
+  it.kstart = kmax_u > 0 ? (kmin_u / p.RB) * p.RB : 0;
+  it.n_tiles = kmax_u > 0 ? (kmax_u - it.kstart + BN - 1) / BN : 0;
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    if (it.has[x] && it.kmx[x] > it.kmn[x]) {
+      it.tlo[x] = (it.kmn[x] - it.kstart) / BN;
+      it.nx[x] = (it.kmx[x] - it.kstart + BN - 1) / BN - it.tlo[x];
+    } else {
+      it.tlo[x] = 0;
+      it.nx[x] = 0;
+    }
+  }
+  return true;
+}
+
+// Persistent: each CTA walks the work items blockIdx.x, blockIdx.x +
+// gridDim.x, ...; every role keeps running counters across items, so the
+// loaders fetch the next item's K / V and warp 11 its Q while the softmax
+// warps finish the previous item's output.  Per item: q_full (Q in place),
+// q_empty (the item's S MMAs are done with Q), o_ready (its MMAs are
+// complete) and o_free[x] (the softmax of tile x has read O_x); the MMA
+// warp waits o_free[x] of the previous item before it writes O_x again.
 template <typename T, int D>
 __global__ void __launch_bounds__(PT_THREADS, 1)
 prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
@@ -1404,89 +1531,7 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
   }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = p.G;
-
-  // ---- work item: (request, 256-row pair tile, KV head)
-  const int g = blockIdx.x % p.Hkv;
-  const int t_lin = blockIdx.x / p.Hkv;
-  int b = -1, tile = 0, q0 = 0, q_len = 0;
-  {
-    int acc = 0;
-    for (int base_b = 0; base_b < p.batch && b < 0; base_b += 32) {
-      const int bb = base_b + lane;
-      int s0 = 0, ql = 0, nt = 0;
-      if (bb < p.batch) {
-        s0 = p.cu_q[bb];
-        ql = min(p.cu_q[bb + 1] - s0, p.total_q - s0);
-        const int rb = (s0 >= 0 && ql > 0) ? ql * G : 0;
-        nt = rb >= p.min_rows ? (rb + PP_ROWS - 1) / PP_ROWS : 0;
-      }
-      int incl = nt;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const bool hit = t_lin >= acc + incl - nt && t_lin < acc + incl;
-      const unsigned m = __ballot_sync(0xffffffffu, hit);
-      if (m) {
-        const int src = __ffs(m) - 1;
-        b = base_b + src;
-        const int excl = __shfl_sync(0xffffffffu, incl - nt, src);
-        const int ntb = __shfl_sync(0xffffffffu, nt, src);
-        q0 = __shfl_sync(0xffffffffu, s0, src);
-        q_len = __shfl_sync(0xffffffffu, ql, src);
-        tile = ntb - 1 - (t_lin - acc - excl);
-      }
-      acc += __shfl_sync(0xffffffffu, incl, 31);
-    }
-  }
-  if (b < 0) return;
-  const int rows = q_len * G;
-  const int koff = p.cu_k ? p.cu_k[b] : 0;     // non-paged: first key row
-  const int L = p.cu_k ? p.cu_k[b + 1] - koff : p.seqused_k[b];
-  // rows past the table (or, non-paged, past the K/V tensor) are not read
-  const int L_tab = p.cu_k ? (koff < 0 ? 0 : max(0, min(L, p.total_k - koff)))
-                           : min(L, p.max_blocks * p.BS);
-  if (L_tab < L && threadIdx.x == 0) atomicOr(p.err, kErrBadTable);
-  const int ctx = L - q_len;
   const int RB = p.RB;
-  // per Q tile x: rows [rx0, rx_end), keys [kmn[x], kmx[x])
-  int rx0[2], rx_end[2], kmn[2], kmx[2];
-  bool has[2];
-  int kmin_u = 0x7fffffff, kmax_u = 0;
-#pragma unroll
-  for (int x = 0; x < 2; ++x) {
-    rx0[x] = tile * PP_ROWS + x * BM;
-    rx_end[x] = min(rows, rx0[x] + BM);
-    has[x] = rx_end[x] > rx0[x];
-    kmn[x] = 0;
-    kmx[x] = 0;
-    if (has[x]) {
-      key_range(L, q_len, rx0[x] / G, (rx_end[x] - 1) / G, p.causal, p.wl,
-                p.wr, kmn[x], kmx[x]);
-      kmx[x] = min(kmx[x], L_tab);
-      if (kmx[x] > kmn[x]) {
-        kmin_u = min(kmin_u, kmn[x]);
-        kmax_u = max(kmax_u, kmx[x]);
-      }
-    }
-  }
-  const int kstart = kmax_u > 0 ? (kmin_u / RB) * RB : 0;
-  const int n_tiles = kmax_u > 0 ? (kmax_u - kstart + BN - 1) / BN : 0;
-  // tile ranges [tlo[x], tlo[x] + nx[x]) of each Q tile in the union
-  int tlo[2], nx[2];
-#pragma unroll
-  for (int x = 0; x < 2; ++x) {
-    if (has[x] && kmx[x] > kmn[x]) {
-      tlo[x] = (kmn[x] - kstart) / BN;
-      nx[x] = (kmx[x] - kstart + BN - 1) / BN - tlo[x];
-    } else {
-      tlo[x] = 0;
-      nx[x] = 0;
-    }
-  }
-  T* __restrict__ OUT = static_cast<T*>(p.out);
-  const bool plain = p.softcap <= 0.f && p.alibi == nullptr;
 
   const uint32_t sQ = base_u + C::OFF_Q;
   const uint32_t sK = base_u + C::OFF_K;
@@ -1498,75 +1543,94 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
   auto v_empty = [&](int s) { return bar0 + 8 * (6 + s); };
   auto s_full = [&](int x) { return bar0 + 8 * (8 + x); };
   auto p_full = [&](int x) { return bar0 + 8 * (10 + x); };
-  const uint32_t final_bar = bar0 + 8 * 12;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + C::OFF_BAR + 8 * 14);
+  auto o_free = [&](int x) { return bar0 + 8 * (12 + x); };
+  const uint32_t o_ready = bar0 + 8 * 14;
+  const uint32_t q_full = bar0 + 8 * 15;
+  const uint32_t q_empty = bar0 + 8 * 16;
+  const uint32_t drain_bar = bar0 + 8 * 17;    // the MMA warp's final drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + C::OFF_BAR + 8 * 18);
   volatile int* abort_flag =
-      reinterpret_cast<volatile int*>(base + C::OFF_BAR + 8 * 14 + 4);
+      reinterpret_cast<volatile int*>(base + C::OFF_BAR + 8 * 18 + 4);
 
-  if (n_tiles > 0) {
-    if (tid == 0) {
-      for (int s = 0; s < 2; ++s) {
-        mbar_init(k_full(s), 1);
-        mbar_init(v_full(s), 1);
-        mbar_init(k_empty(s), 1);
-        mbar_init(v_empty(s), 1);
-        mbar_init(s_full(s), 1);
-        mbar_init(p_full(s), 128);
+  if (tid == 0) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(k_full(s), 1);
+      mbar_init(v_full(s), 1);
+      mbar_init(k_empty(s), 1);
+      mbar_init(v_empty(s), 1);
+      mbar_init(s_full(s), 1);
+      mbar_init(p_full(s), 128);
+      mbar_init(o_free(s), 128);
+    }
+    mbar_init(o_ready, 1);
+    mbar_init(q_full, 32);
+    mbar_init(q_empty, 1);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == PT_MMA_WARP) {
+    asm volatile(
+        "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], "
+        "%1;" ::"r"(smem_u32(tmem_slot)),
+        "r"(C::TMEM_COLS)
+        : "memory");
+    asm volatile(
+        "tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::
+            : "memory");
+  }
+  // request metadata, read once per CTA instead of once per item and warp
+  PtMeta md;
+  {
+    int* m_q = reinterpret_cast<int*>(base + C::OFF_META);
+    int* m_len = m_q + C::META_MAX + 1;
+    int* m_koff = m_len + C::META_MAX;
+    md.cu_q = m_q;
+    md.len = m_len;
+    md.koff = m_koff;
+    md.cached = p.batch <= C::META_MAX;
+    if (md.cached) {
+      for (int i = tid; i <= p.batch; i += PT_THREADS) {
+        m_q[i] = p.cu_q[i];
+        if (i < p.batch) {
+          const int ko = p.cu_k ? p.cu_k[i] : 0;
+          m_koff[i] = ko;
+          m_len[i] = p.cu_k ? p.cu_k[i + 1] - ko : p.seqused_k[i];
+        }
       }
-      mbar_init(final_bar, 1);
-      *abort_flag = 0;
-      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == PT_MMA_WARP) {
-      asm volatile(
-          "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], "
-          "%1;" ::"r"(smem_u32(tmem_slot)),
-          "r"(C::TMEM_COLS)
-          : "memory");
-      asm volatile(
-          "tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::
-              : "memory");
-    }
-    // Q tiles A and B: packed rows, zero past each tile's end
-    const T* Q = static_cast<const T*>(p.q);
-    for (int i = tid; i < PP_ROWS * (D / 8); i += PT_THREADS) {
-      const int rr = i / (D / 8), ch = i % (D / 8);
-      const int x = rr / BM, r = rr % BM;
-      const int R = rx0[x] + r;
-      const bool ok = R < rx_end[x];
-      const T* src = Q;
-      if (ok)
-        src = Q + static_cast<int64_t>(q0 + R / G) * p.q_st +
-              static_cast<int64_t>(g * G + R % G) * p.q_sh + ch * 8;
-      cp_async_16(sQ + x * C::Q_BYTES + (ch >> 3) * (BM * 128) +
-                      sw128(r, ch & 7),
-                  src, ok ? 16 : 0);
-    }
-    cp_async_commit();
-    cp_async_wait<0>();
-    fence_proxy_async();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = n_tiles > 0 ? *tmem_slot : 0;
+  const uint32_t tmem = *tmem_slot;
+  const int n_items = p.n_items;
 
   if (warp >= 8) {
-  // warpgroup 2 (MMA, loaders, one idle warp) gives registers back to the
+  // warpgroup 2 (MMA, K / V loaders, Q loader) gives registers back to the
   // softmax warpgroups, all four warps on this one instruction
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(PT_OTHER_REGS));
   if (warp == PT_LOAD_WARP || warp == PT_LOAD_WARP + 1) {
-    if (n_tiles > 0) {
-      // ------------------------------------------------------ producers
-      // warp 9 loads K tiles, warp 10 V tiles; lane i issues box i of each
-      // tile and prefetches its page id one tile ahead
-      const int mat = warp - PT_LOAD_WARP;       // 0: K, 1: V
+    // -------------------------------------------------------- K / V loaders
+    // warp 9 loads K tiles, warp 10 V tiles; lane i issues box i of each
+    // tile and prefetches its page id one tile ahead
+    const int mat = warp - PT_LOAD_WARP;       // 0: K, 1: V
+    const void* tm = mat ? static_cast<const void*>(&tm_v)
+                         : static_cast<const void*>(&tm_k);
+    int gj = 0;                                // tiles issued so far
+    bool ok = true;
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+      PtItem it;
+      if (!pt_item(p, item, lane, BN, md, it)) continue;
+      if (it.L_tab < it.L && lane == 0 && warp == PT_LOAD_WARP)
+        atomicOr(p.err, kErrBadTable);
       const int32_t* bt =
           p.cu_k ? nullptr
-                 : p.block_table + static_cast<int64_t>(b) * p.bt_stride;
+                 : p.block_table + static_cast<int64_t>(it.b) * p.bt_stride;
       auto fetch = [&](int j) -> int {
-        const int k0 = kstart + j * BN + lane * RB;
-        if (j >= n_tiles || lane >= BN / RB || k0 >= kmax_u || !bt) return 0;
+        const int k0 = it.kstart + j * BN + lane * RB;
+        if (j >= it.n_tiles || lane >= BN / RB || k0 >= it.kmax_u || !bt)
+          return 0;
         const int blk = __ldg(bt + k0 / p.BS);
         if (blk < 0 || blk >= p.num_blocks) {
           atomicOr(p.err, kErrBadBlock);
@@ -1574,67 +1638,86 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
         }
         return blk;
       };
-      const void* tm = mat ? static_cast<const void*>(&tm_v)
-                           : static_cast<const void*>(&tm_k);
-      int issued = 0;
       int cur = fetch(0);
-      for (int j = 0; j < n_tiles; ++j) {
+      for (int j = 0; j < it.n_tiles; ++j, ++gj) {
         const int nxt = fetch(j + 1);
-        const int s = j & 1;
-        const int kt = kstart + j * BN;
-        int nbox = (kmax_u - kt + RB - 1) / RB;
+        const int s = gj & 1;
+        const int kt = it.kstart + j * BN;
+        int nbox = (it.kmax_u - kt + RB - 1) / RB;
         if (nbox > BN / RB) nbox = BN / RB;
         const uint32_t full = mat ? v_full(s) : k_full(s);
         int stop = 0;
         if (lane == 0) {
           const uint32_t empty = mat ? v_empty(s) : k_empty(s);
-          if (j >= 2 && !mbar_wait(empty, ((j >> 1) & 1) ^ 1, abort_flag,
-                                   p.err))
+          if (gj >= 2 && !mbar_wait(empty, ((gj >> 1) & 1) ^ 1, abort_flag,
+                                    p.err))
             stop = 1;
           else
             mbar_expect_tx(full, nbox * C::NCB * RB * 128);
         }
         stop = __shfl_sync(0xffffffffu, stop, 0);
-        if (stop) break;
+        if (stop) {
+          ok = false;
+          break;
+        }
         if (lane < nbox) {
           const uint32_t dst0 = (mat ? sV : sK) + s * C::KV_BYTES;
           const int k0 = kt + lane * RB;
-          const int row = p.cu_k ? koff + k0 : k0 % p.BS;
+          const int row = p.cu_k ? it.koff + k0 : k0 % p.BS;
           for (int cb = 0; cb < C::NCB; ++cb) {
             const uint32_t dst = dst0 + cb * (BN * 128) + lane * RB * 128;
             if (p.kv_order_hnd)
-              tma_load_4d(dst, tm, cb * 64, row, g, cur, full);
+              tma_load_4d(dst, tm, cb * 64, row, it.g, cur, full);
             else
-              tma_load_4d(dst, tm, cb * 64, g, row, cur, full);
+              tma_load_4d(dst, tm, cb * 64, it.g, row, cur, full);
           }
         }
-        issued = j + 1;
         cur = nxt;
       }
-      if (lane == 0) {
-        for (int t = max(0, issued - 2); t < issued; ++t)
-          mbar_drain(mat ? v_full(t & 1) : k_full(t & 1), (t >> 1) & 1);
-      }
+    }
+    if (lane == 0) {
+      // no copy may be in flight when the CTA exits
+      for (int t = max(0, gj - 2); t < gj; ++t)
+        mbar_drain(mat ? v_full(t & 1) : k_full(t & 1), (t >> 1) & 1);
     }
   } else if (warp == PT_MMA_WARP) {
-    if (n_tiles > 0) {
-      // ---------------------------------------------------- MMA issuer
-      constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value;
-      constexpr uint32_t ID_S = idesc(128, BN, kBF16, false);
-      constexpr uint32_t ID_PV = idesc(128, D, kBF16, true);
-      bool ok = true;
+    // ------------------------------------------------------------ MMA issuer
+    constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value;
+    constexpr uint32_t ID_S = idesc(128, BN, kBF16, false);
+    constexpr uint32_t ID_PV = idesc(128, D, kBF16, true);
+    bool ok = true;
+    int gj = 0;                       // K / V tiles consumed so far
+    int pv_cnt[2] = {0, 0};           // P_x V MMAs issued so far
+    int n_done = 0;                   // items finished
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+      PtItem it;
+      if (!pt_item(p, item, lane, BN, md, it)) continue;
+      if (!mbar_wait(q_full, n_done & 1, abort_flag, p.err)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      bool o_mine[2] = {n_done == 0, n_done == 0};   // O_x free to write
+      auto claim_o = [&](int x) -> bool {
+        if (o_mine[x]) return true;
+        if (!mbar_wait(o_free(x), (n_done - 1) & 1, abort_flag, p.err))
+          return false;
+        tc_fence_after();
+        o_mine[x] = true;
+        return true;
+      };
       auto in_range = [&](int x, int j) {
-        return j >= tlo[x] && j < tlo[x] + nx[x];
+        return j >= it.tlo[x] && j < it.tlo[x] + it.nx[x];
       };
       // V_i resident (rows past the keys zeroed); false on abort
       auto v_ready = [&](int i) -> bool {
-        const int s = i & 1;
-        if (!mbar_wait(v_full(s), (i >> 1) & 1, abort_flag, p.err))
+        const int gi = gj + i, s = gi & 1;
+        if (!mbar_wait(v_full(s), (gi >> 1) & 1, abort_flag, p.err))
           return false;
-        const int kt = kstart + i * BN;
-        int nbox = (kmax_u - kt + RB - 1) / RB;
+        const int kt = it.kstart + i * BN;
+        int nbox = (it.kmax_u - kt + RB - 1) / RB;
         if (nbox > BN / RB) nbox = BN / RB;
-        const int r0 = min(nbox * RB, max(L - kt, 0));
+        const int r0 = min(nbox * RB, max(it.L - kt, 0));
         if (r0 < BN) {
           // rows past the last key may hold another request's NaN padding
           const uint32_t v0 = sV + s * C::KV_BYTES;
@@ -1653,10 +1736,14 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
         return true;
       };
       auto issue_pv = [&](int x, int i) -> bool {
-        const int ix = i - tlo[x];
-        if (!mbar_wait(p_full(x), ix & 1, abort_flag, p.err)) return false;
+        const int ix = i - it.tlo[x];
+        if (ix == 0 && !claim_o(x)) return false;
+        if (!mbar_wait(p_full(x), pv_cnt[x] & 1, abort_flag, p.err))
+          return false;
+        ++pv_cnt[x];
         tc_fence_after();
-        const uint64_t b0 = sdesc(sV + (i & 1) * C::KV_BYTES, BN * 128, 1024);
+        const uint64_t b0 =
+            sdesc(sV + ((gj + i) & 1) * C::KV_BYTES, BN * 128, 1024);
         const uint32_t s_col = tmem + x * C::X_COLS;
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k)
@@ -1667,7 +1754,8 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
       };
       auto issue_s = [&](int x, int j) {
         const uint64_t a0 = sdesc(sQ + x * C::Q_BYTES, 16, 1024);
-        const uint64_t b0 = sdesc(sK + (j & 1) * C::KV_BYTES, 16, 1024);
+        const uint64_t b0 =
+            sdesc(sK + ((gj + j) & 1) * C::KV_BYTES, 16, 1024);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
           mma_f16_warp(tmem + x * C::X_COLS,
@@ -1676,10 +1764,10 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
                        ID_S, k > 0 ? 1 : 0);
         mma_commit_warp(s_full(x));
       };
-      for (int j = 0; j <= n_tiles && ok; ++j) {
-        const int s = j & 1;
+      for (int j = 0; j <= it.n_tiles && ok; ++j) {
         const bool pv = j >= 1;              // P(j-1) V_{j-1} this round
-        const bool sj = j < n_tiles;         // S(j) this round
+        const bool sj = j < it.n_tiles;      // S(j) this round
+        const int gk = gj + j;
         bool k_here = false;                 // K_j waited for
         if (pv && !v_ready(j - 1)) {
           ok = false;
@@ -1693,7 +1781,8 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
           }
           if (sj && in_range(x, j)) {
             if (!k_here) {
-              if (!mbar_wait(k_full(s), (j >> 1) & 1, abort_flag, p.err)) {
+              if (!mbar_wait(k_full(gk & 1), (gk >> 1) & 1, abort_flag,
+                             p.err)) {
                 ok = false;
                 break;
               }
@@ -1704,11 +1793,56 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
           }
         }
         if (!ok) break;
-        if (sj) mma_commit_warp(k_empty(s));
-        if (pv) mma_commit_warp(v_empty((j - 1) & 1));
+        if (sj) mma_commit_warp(k_empty(gk & 1));
+        if (pv) mma_commit_warp(v_empty((gk - 1) & 1));
+        if (j == it.n_tiles - 1 || it.n_tiles == 0) mma_commit_warp(q_empty);
       }
-      mma_commit_warp(final_bar);
-      mbar_drain(final_bar, 0);
+      if (!ok) break;
+      // the previous item's O_x must be read before o_ready can move on
+      if (!claim_o(0) || !claim_o(1)) {
+        ok = false;
+        break;
+      }
+      mma_commit_warp(o_ready);
+      gj += it.n_tiles;
+      ++n_done;
+    }
+    // wait for every MMA of this CTA on a barrier no other role waits on (an
+    // extra o_ready phase could complete before a softmax warp has waited
+    // for the previous one, and the parity wait would then never return)
+    mma_commit_warp(drain_bar);
+    mbar_drain(drain_bar, 0);
+  } else if (warp == PT_LOAD_WARP + 2) {
+    // ---------------------------------------------------- Q loader (warp 11)
+    int n_done = 0;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+      PtItem it;
+      if (!pt_item(p, item, lane, BN, md, it)) continue;
+      if (n_done >= 1 &&
+          !mbar_wait(q_empty, (n_done - 1) & 1, abort_flag, p.err))
+        break;
+      // both Q tiles: packed rows, zero past each tile's end; lane i
+      // copies rows i, i + 32, ... (one address computation per row)
+      const T* Q = static_cast<const T*>(p.q);
+      for (int rr = lane; rr < PP_ROWS; rr += 32) {
+        const int xq = rr / BM, rq = rr % BM;
+        const int Rq = it.rx0[xq] + rq;
+        const bool okq = Rq < it.rx_end[xq];
+        const T* src = Q;
+        if (okq)
+          src = Q + static_cast<int64_t>(it.q0 + Rq / G) * p.q_st +
+                static_cast<int64_t>(it.g * G + Rq % G) * p.q_sh;
+        const uint32_t dst = sQ + xq * C::Q_BYTES;
+#pragma unroll
+        for (int ch = 0; ch < D / 8; ++ch)
+          cp_async_16(dst + (ch >> 3) * (BM * 128) + sw128(rq, ch & 7),
+                      okq ? src + ch * 8 : src, okq ? 16 : 0);
+      }
+      cp_async_commit();
+      cp_async_wait<0>();
+      fence_proxy_async();
+      mbar_arrive(q_full);
+      ++n_done;
     }
   }
   } else {
@@ -1716,17 +1850,8 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
     // ---------------------------------------------- softmax warpgroups
     const int x = warp >> 2;                  // 0: tile A, 1: tile B
     const int r = tid & 127;                  // row in tile == TMEM lane
-    const int my_rx0 = x ? rx0[1] : rx0[0];
-    const int my_rx_end = x ? rx_end[1] : rx_end[0];
-    const bool my_has = x ? has[1] : has[0];
-    const int my_tlo = x ? tlo[1] : tlo[0];
-    const int my_nx = x ? nx[1] : nx[0];
-    const int R = my_rx0 + r;
-    const bool valid = R < my_rx_end;
-    const int pos = ctx + (valid ? R / G : 0);
-    const int h = g * G + (valid ? R % G : 0);
-    const int tok = q0 + (valid ? R / G : 0);
-    const float slope = (p.alibi && valid) ? p.alibi[h] : 0.f;
+    T* __restrict__ OUT = static_cast<T*>(p.out);
+    const bool plain = p.softcap <= 0.f && p.alibi == nullptr;
     const float qk_scale = p.scale * (p.k_scale ? *p.k_scale : 1.f);
     const float vscale = p.v_scale ? *p.v_scale : 1.f;
     const float scale_log2 = qk_scale * kLog2e;
@@ -1734,172 +1859,209 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t s_addr = tmem + lane_base + x * C::X_COLS;
     const uint32_t o_addr = s_addr + BN;
-    const int kmin = x ? kmn[1] : kmn[0], kmax = x ? kmx[1] : kmx[0];
-    int full_lo = kmin, full_hi = kmax;
-    if (my_has) {
-      const int p_lo = ctx + my_rx0 / G, p_hi = ctx + (my_rx_end - 1) / G;
-      if (p.wl >= 0) full_lo = max(full_lo, p_hi - p.wl);
-      if (p.causal) full_hi = min(full_hi, p_lo + 1);
-      if (p.wr >= 0) full_hi = min(full_hi, p_lo + p.wr + 1);
-    }
-    float m_ref = -INFINITY, l = 0.f;
+    int s_cnt = 0;                            // S_x tiles seen so far
+    int n_done = 0;
     bool ok = true;
-    for (int jx = 0; jx < my_nx; ++jx) {
-      if (!mbar_wait(s_full(x), jx & 1, abort_flag, p.err)) {
-        ok = false;
-        break;
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+      PtItem it;
+      if (!pt_item(p, item, lane, BN, md, it)) continue;
+      const int my_rx0 = x ? it.rx0[1] : it.rx0[0];
+      const int my_rx_end = x ? it.rx_end[1] : it.rx_end[0];
+      const bool my_has = x ? it.has[1] : it.has[0];
+      const int my_tlo = x ? it.tlo[1] : it.tlo[0];
+      const int my_nx = x ? it.nx[1] : it.nx[0];
+      const int R = my_rx0 + r;
+      const bool valid = R < my_rx_end;
+      const int pos = it.ctx + (valid ? R / G : 0);
+      const int h = it.g * G + (valid ? R % G : 0);
+      const int tok = it.q0 + (valid ? R / G : 0);
+      const float slope = (p.alibi && valid) ? p.alibi[h] : 0.f;
+      const int kmin = x ? it.kmn[1] : it.kmn[0];
+      const int kmax = x ? it.kmx[1] : it.kmx[0];
+      int full_lo = kmin, full_hi = kmax;
+      if (my_has) {
+        const int p_lo = it.ctx + my_rx0 / G;
+        const int p_hi = it.ctx + (my_rx_end - 1) / G;
+        if (p.wl >= 0) full_lo = max(full_lo, p_hi - p.wl);
+        if (p.causal) full_hi = min(full_hi, p_lo + 1);
+        if (p.wr >= 0) full_hi = min(full_hi, p_lo + p.wr + 1);
       }
+      float m_ref = -INFINITY, l = 0.f;
+      for (int jx = 0; jx < my_nx; ++jx, ++s_cnt) {
+        if (!mbar_wait(s_full(x), s_cnt & 1, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int kt = it.kstart + (my_tlo + jx) * BN;
+        const bool unmasked = kt >= full_lo && kt + BN <= full_hi;
+        float v[BN];
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c)
+          tmem_ld32(s_addr + c * 32, v + c * 32);
+        tmem_wait_ld();
+        // logits in log2 units; keys outside this row's admissible
+        // interval [a_lo, a_hi) (causal, window, item range) become -inf.
+        // The interval test keeps the masked code short: a fully unrolled
+        // per-key predicate chain over 128 keys overflows the instruction
+        // cache.
+        int lo_rel = 0, n_rel = BN;             // admissible e in [lo, lo+n)
+        if (!unmasked) {
+          int a_lo = kmin, a_hi = kmax;
+          if (p.causal) a_hi = min(a_hi, pos + 1);
+          if (p.wl >= 0) a_lo = max(a_lo, pos - p.wl);
+          if (p.wr >= 0) a_hi = min(a_hi, pos + p.wr + 1);
+          if (!valid) a_hi = a_lo;
+          lo_rel = a_lo - kt;
+          n_rel = max(a_hi - a_lo, 0);
+        }
+        float mx8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
+        // interior tiles keep the raw scores: max(scale * s) = scale *
+        // max(s) for scale > 0, and the scale joins the exponent's FMA
+        const bool raw = plain && unmasked && scale_log2 > 0.f;
+        if (raw) {
+#pragma unroll
+          for (int e = 0; e < BN; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], v[e]);
+        } else if (plain) {
+#pragma unroll
+          for (int e = 0; e < BN; ++e) {
+            const bool in = static_cast<unsigned>(e - lo_rel) <
+                            static_cast<unsigned>(n_rel);
+            v[e] = in ? v[e] * scale_log2 : -INFINITY;
+            mx8[e & 7] = fmaxf(mx8[e & 7], v[e]);
+          }
+        } else {
+          // soft-cap and / or ALiBi (their own slower path)
+#pragma unroll
+          for (int e = 0; e < BN; ++e) {
+            float xs = v[e] * qk_scale;
+            if (p.softcap > 0.f) xs = p.softcap * tanh_fast(xs * inv_cap);
+            if (p.alibi) xs -= slope * fabsf(float(pos - (kt + e)));
+            const bool in = static_cast<unsigned>(e - lo_rel) <
+                            static_cast<unsigned>(n_rel);
+            v[e] = in ? xs * kLog2e : -INFINITY;
+            mx8[e & 7] = fmaxf(mx8[e & 7], v[e]);
+          }
+        }
+        float mx =
+            fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                  fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        if (raw) mx *= scale_log2;
+        const bool grow = mx > m_ref + kRescaleThreshold;
+        float alpha = 1.f;
+        if (grow) {
+          alpha = ex2(m_ref - mx);
+          m_ref = mx;
+          l *= alpha;
+        }
+        const float base_m = (m_ref == -INFINITY) ? 0.f : m_ref;
+        if (jx >= 1 && __any_sync(0xffffffffu, grow)) {
+          // O_x is complete: the commit behind s_full covered P(j-1) V
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            float ov[32];
+            tmem_ld32(o_addr + c * 32, ov);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] *= alpha;
+            tmem_st32(o_addr + c * 32, ov);
+          }
+        }
+        float sum8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sum8[e] = 0.f;
+        const float sc = raw ? scale_log2 : 1.f;
+#pragma unroll
+        for (int e = 0; e < BN; e += 2) {
+          float x0 = v[e], x1 = v[e + 1];
+          fma2(x0, x1, sc, -base_m);
+          x0 = ex2(x0);
+          x1 = ex2(x1);
+          v[e] = x0;
+          v[e + 1] = x1;
+          add2(sum8[2 * ((e >> 1) & 3)], sum8[2 * ((e >> 1) & 3) + 1], x0,
+               x1);
+        }
+        // P_x over the first BN / 2 columns of S_x: column c holds the keys
+        // 2c (low half) and 2c + 1 (high half)
+#pragma unroll
+        for (int c = 0; c < BN / 64; ++c) {
+          float pk[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            pk[e] = __uint_as_float(pack2<T>(v[c * 64 + 2 * e],
+                                             v[c * 64 + 2 * e + 1]));
+          tmem_st32(s_addr + c * 32, pk);
+        }
+        l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
+             ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(p_full(x));
+      }
+      if (!ok) break;
+      // ---- epilogue: every MMA of the item is complete
+      if (!mbar_wait(o_ready, n_done & 1, abort_flag, p.err)) break;
       tc_fence_after();
-      const int kt = kstart + (my_tlo + jx) * BN;
-      const bool unmasked = kt >= full_lo && kt + BN <= full_hi;
-      float v[BN];
+      T* dst = OUT + static_cast<int64_t>(tok) * p.o_st +
+               static_cast<int64_t>(h) * p.o_sh;
+      if (my_nx == 0) {
+        // no admissible key for this tile's rows: out = 0, lse = -inf
+        tc_fence_before();
+        mbar_arrive(o_free(x));
+        if (valid) {
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_addr + c * 32, v + c * 32);
-      tmem_wait_ld();
-      // logits in log2 units; keys outside this row's admissible interval
-      // [a_lo, a_hi) (causal, window, split range) become -inf.  The
-      // interval test keeps the masked code short: a fully unrolled
-      // per-key predicate chain over 128 keys overflows the instruction
-      // cache.
-      int lo_rel = 0, n_rel = BN;               // admissible e in [lo, lo+n)
-      if (!unmasked) {
-        int a_lo = kmin, a_hi = kmax;
-        if (p.causal) a_hi = min(a_hi, pos + 1);
-        if (p.wl >= 0) a_lo = max(a_lo, pos - p.wl);
-        if (p.wr >= 0) a_hi = min(a_hi, pos + p.wr + 1);
-        if (!valid) a_hi = a_lo;
-        lo_rel = a_lo - kt;
-        n_rel = max(a_hi - a_lo, 0);
-      }
-      float mx8[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
-      // interior tiles keep the raw scores: max(scale * s) = scale * max(s)
-      // for scale > 0, and the scale joins the exponent's FMA below
-      const bool raw = plain && unmasked && scale_log2 > 0.f;
-      if (raw) {
-#pragma unroll
-        for (int e = 0; e < BN; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], v[e]);
-      } else if (plain) {
-#pragma unroll
-        for (int e = 0; e < BN; ++e) {
-          const bool in = static_cast<unsigned>(e - lo_rel) <
-                          static_cast<unsigned>(n_rel);
-          v[e] = in ? v[e] * scale_log2 : -INFINITY;
-          mx8[e & 7] = fmaxf(mx8[e & 7], v[e]);
+          for (int c = 0; c < D; c += 8)
+            *reinterpret_cast<uint4*>(dst + c) = make_uint4(0, 0, 0, 0);
+          if (p.lse)
+            p.lse[static_cast<int64_t>(h) * p.total_q + tok] =
+                p.sinks ? p.sinks[h] : -INFINITY;
         }
       } else {
-        // soft-cap and / or ALiBi (their own slower path)
-#pragma unroll
-        for (int e = 0; e < BN; ++e) {
-          float x = v[e] * qk_scale;
-          if (p.softcap > 0.f) x = p.softcap * tanh_fast(x * inv_cap);
-          if (p.alibi) x -= slope * fabsf(float(pos - (kt + e)));
-          const bool in = static_cast<unsigned>(e - lo_rel) <
-                          static_cast<unsigned>(n_rel);
-          v[e] = in ? x * kLog2e : -INFINITY;
-          mx8[e & 7] = fmaxf(mx8[e & 7], v[e]);
-        }
-      }
-      float mx =
-          fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      if (raw) mx *= scale_log2;
-      const bool grow = mx > m_ref + kRescaleThreshold;
-      float alpha = 1.f;
-      if (grow) {
-        alpha = ex2(m_ref - mx);
-        m_ref = mx;
-        l *= alpha;
-      }
-      const float base_m = (m_ref == -INFINITY) ? 0.f : m_ref;
-      if (jx >= 1 && __any_sync(0xffffffffu, grow)) {
-        // O_x is complete: the commit behind s_full covered P(j-1) V
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          float ov[32];
-          tmem_ld32(o_addr + c * 32, ov);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) ov[e] *= alpha;
-          tmem_st32(o_addr + c * 32, ov);
-        }
-      }
-      float sum8[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) sum8[e] = 0.f;
-      const float sc = raw ? scale_log2 : 1.f;
-#pragma unroll
-      for (int e = 0; e < BN; e += 2) {
-        float x0 = v[e], x1 = v[e + 1];
-        fma2(x0, x1, sc, -base_m);
-        x0 = ex2(x0);
-        x1 = ex2(x1);
-        v[e] = x0;
-        v[e + 1] = x1;
-        add2(sum8[2 * ((e >> 1) & 3)], sum8[2 * ((e >> 1) & 3) + 1], x0, x1);
-      }
-      // P_x over the first BN / 2 columns of S_x: column c holds the keys
-      // 2c (low half) and 2c + 1 (high half)
-#pragma unroll
-      for (int c = 0; c < BN / 64; ++c) {
-        float pk[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e)
-          pk[e] = __uint_as_float(pack2<T>(v[c * 64 + 2 * e],
-                                           v[c * 64 + 2 * e + 1]));
-        tmem_st32(s_addr + c * 32, pk);
-      }
-      l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
-           ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(p_full(x));
-    }
-    T* dst = OUT + static_cast<int64_t>(tok) * p.o_st +
-             static_cast<int64_t>(h) * p.o_sh;
-    if (my_nx == 0) {
-      // no admissible key for this tile's rows: out = 0, lse = -inf
-      if (valid) {
-#pragma unroll
-        for (int c = 0; c < D; c += 8)
-          *reinterpret_cast<uint4*>(dst + c) = make_uint4(0, 0, 0, 0);
-        if (p.lse)
-          p.lse[static_cast<int64_t>(h) * p.total_q + tok] =
-              p.sinks ? p.sinks[h] : -INFINITY;
-      }
-    } else if (ok) {
-      if (mbar_wait(final_bar, 0, abort_flag, p.err)) {
-        tc_fence_after();
         float inv, lse_v;
         finish_row(m_ref, l, p.sinks, h, &inv, &lse_v);
         inv *= vscale;
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          float ov[32];
-          tmem_ld32(o_addr + c * 32, ov);
-          tmem_wait_ld();
-          if (valid) {
+        float ov[D];
 #pragma unroll
-            for (int e = 0; e < 32; e += 8) {
+        for (int c = 0; c < D / 32; ++c)
+          tmem_ld32(o_addr + c * 32, ov + c * 32);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(o_free(x));              // O_x may be overwritten now
+        if (valid) {
+          if (p.out_v8) {
+            // whole 32-byte sectors: half the store transactions of 16 B
+#pragma unroll
+            for (int e = 0; e < D; e += 16) {
+              uint32_t w[8];
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                w[q] = pack2<T>(ov[e + 2 * q] * inv, ov[e + 2 * q + 1] * inv);
+              st_global_v8(dst + e, w);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < D; e += 8) {
               uint4 pk;
               pk.x = pack2<T>(ov[e] * inv, ov[e + 1] * inv);
               pk.y = pack2<T>(ov[e + 2] * inv, ov[e + 3] * inv);
               pk.z = pack2<T>(ov[e + 4] * inv, ov[e + 5] * inv);
               pk.w = pack2<T>(ov[e + 6] * inv, ov[e + 7] * inv);
-              *reinterpret_cast<uint4*>(dst + c * 32 + e) = pk;
+              *reinterpret_cast<uint4*>(dst + e) = pk;
             }
           }
+          if (p.lse) p.lse[static_cast<int64_t>(h) * p.total_q + tok] = lse_v;
         }
-        if (valid && p.lse)
-          p.lse[static_cast<int64_t>(h) * p.total_q + tok] = lse_v;
       }
+      ++n_done;
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == PT_MMA_WARP && n_tiles > 0) {
+  if (warp == PT_MMA_WARP) {
     tc_fence_after();
     asm volatile(
         "tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
@@ -2004,6 +2166,10 @@ cudaError_t launch_prefill_attn_tc(const AttnParams& a, int D, bool bf16,
   if (a.cu_k) RB = BN;    // non-paged: boxes may start on any row
   p.RB = RB;
   p.kv_order_hnd = a.c_sh > a.c_sr ? 1 : 0;
+  p.out_v8 = (reinterpret_cast<uintptr_t>(a.out) % 32 == 0 &&
+              (a.o_st * 2) % 32 == 0 && (a.o_sh * 2) % 32 == 0)
+                 ? 1
+                 : 0;
   CUtensorMap mk, mv;
   if (!make_kv_map(&mk, a.kc, bf16, D, a.BS, a.Hkv, a.num_blocks, a.c_sb,
                    a.c_sr, a.c_sh, RB, p.kv_order_hnd) ||
@@ -2022,6 +2188,7 @@ cudaError_t launch_prefill_attn_tc(const AttnParams& a, int D, bool bf16,
   const int64_t gx = tiles * a.Hkv;
   if (gx <= 0 || gx > 0x7fffffff) return cudaErrorInvalidValue;
   dim3 grid(static_cast<unsigned>(gx));
+  p.n_items = static_cast<int>(gx);
   auto go = [&](void (*kern)(TcParams, CUtensorMap, CUtensorMap), int smem,
                 int threads) -> cudaError_t {
     // shared-memory opt-in once per kernel (a short list: 10 kernels)
@@ -2058,6 +2225,16 @@ cudaError_t launch_prefill_attn_tc(const AttnParams& a, int D, bool bf16,
       regs[bi][di] = fa.numRegs;
     }
     if (D <= 128 && regs[bi][di] != PT_LAUNCH_REGS) p_in_tmem = false;
+  }
+  if (p_in_tmem && D <= 128) {
+    // persistent: one CTA per SM walks the items (an item needs two 128-row
+    // Q tiles of packed rows, so the item count is that of the pair grid)
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+            cudaSuccess || sms <= 0)
+      sms = 1;
+    if (static_cast<int64_t>(sms) < gx) grid = dim3(static_cast<unsigned>(sms));
   }
   if (p_in_tmem && bf16) {
     switch (D) {
