@@ -72,6 +72,8 @@ CASES = [
     ([200, 90], [900, 90], 32, 8, 128, 16, 0, "bf16", "mma_sync"),
     ([70, 1], [600, 1200], 16, 8, 256, 32, 0, "bf16", "tcgen05"),
     ([130, 1], [400, 800], 16, 4, 64, 16, 0, "f16", "tcgen05"),
+    ([1, 3, 1], [33, 2049, 4100], 16, 8, 256, 32, 3, "f16", "tcgen05"),
+    ([1, 1], [1, 129], 8, 4, 128, 128, 0, "bf16", "tcgen05"),
 ]
 
 
