@@ -349,6 +349,102 @@ def gpu_arm(args, rank, world, dev):
     return res
 
 
+# ------------------------------------------------- other workloads (rank 0)
+def _time_ms(fn, iters=10, warm=3):
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(iters):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / iters
+
+
+def _kv_bytes(wl, elem=2):
+    """Admissible K/V bytes of decode-class requests (window aware)."""
+    L = wl.seq_lens.astype(np.int64)
+    if wl.window_size[0] >= 0:
+        L = np.minimum(L, wl.window_size[0] + 1)
+    return int(L.sum()) * 2 * wl.num_kv_heads * wl.head_size * elem
+
+
+def other_workloads(dev, hbm_peak, tf_peak):
+    """Attention-call rates on the other configurations (CUDA events; each
+    decode working set exceeds the L2)."""
+    out = {}
+
+    def rec(name, desc, ms, amount, unit, peak):
+        rate = amount / (ms * 1e-3) / (1e9 if unit == "GB/s" else 1e12)
+        out[name] = {"workload": desc, "ms": round(ms, 4),
+                     "value": round(rate, 1), "unit": unit,
+                     "frac": round(rate / peak, 4)}
+
+    wl = workloads.long_decode(device=dev)
+    b = DeviceBatch(wl, dev, poison=False)
+    b.write_context()
+    b.write_new()
+    rec("long_decode", "8 x 131072-key decodes, 64/8 heads, D 128, BS 64, "
+        "16 splits", _time_ms(lambda: b.attend(return_lse=False)),
+        _kv_bytes(wl), "GB/s", hbm_peak)
+    del b
+    wl = workloads.mixed_gemma(device=dev, n_prefill=0)
+    b = DeviceBatch(wl, dev, poison=False)
+    b.write_context()
+    b.write_new()
+    rec("mixed_decode", "124 decodes, L ~ U[1024, 16384], 16/8 heads, D 256, "
+        "window (4095, 0), soft-cap 50", _time_ms(
+            lambda: b.attend(return_lse=False)), _kv_bytes(wl), "GB/s",
+        hbm_peak)
+    del b
+    wl = workloads.cascade_decode(device=dev)
+    b = DeviceBatch(wl, dev, poison=False, cascade=True)
+    b.write_context()
+    b.write_new()
+    P = wl.common_prefix_len
+    uniq = (P + int((wl.seq_lens - P).sum())) * 2 * wl.num_kv_heads * \
+        wl.head_size * 2
+    rec("cascade_decode", "256 decodes sharing an 8192-token prefix + 512 own "
+        "keys each, 64/8 heads, D 128 (unique K/V bytes)", _time_ms(
+            lambda: b.attend(return_lse=False)), uniq, "GB/s", hbm_peak)
+    del b
+    # fp8 (E4M3) cache: the batched decode workload's cache quantized
+    wl = workloads.batched_decode(seed=SEED_DECODE, device=dev)
+    b = DeviceBatch(wl, dev, poison=False)
+    b.write_context()
+    b.write_new()
+    c8 = torch.zeros(wl.cache_shape(), dtype=torch.uint8, device=dev)
+    k8, v8 = c8.unbind(0)
+    ks = torch.tensor([0.02], device=dev)
+    vs = torch.tensor([0.02], device=dev)
+    for rk, rv, sl in ((b.k_ctx, b.v_ctx, b.slots_ctx),
+                       (b.k_new, b.v_new, b.slots_new)):
+        api.reshape_and_cache_flash(rk, rv, k8, v8, sl, "fp8", ks, vs)
+    rec("fp8_decode", "batched decode workload over an E4M3 cache (fp8 "
+        "bytes)", _time_ms(lambda: api.flash_attn_varlen_func(
+            b.q, k8, v8, 1, b.cu_seqlens_q, wl.max_seqlen_k,
+            seqused_k=b.seqused_k, softmax_scale=wl.softmax_scale,
+            causal=True, block_table=b.block_table, out=b.out,
+            k_descale=ks, v_descale=vs)), _kv_bytes(wl, 1), "GB/s",
+        hbm_peak)
+    del b, c8
+    wl = workloads.build_workload("long_prefill", 324, [2048], [8192], 32, 8,
+                                  128, 64, device=dev)
+    b = DeviceBatch(wl, dev, poison=False)
+    b.write_context()
+    b.write_new()
+    rec("long_prefill", "one request, 2048 queries over 8192 keys (causal), "
+        "32/8 heads, D 128 (K/V fit in L2)", _time_ms(
+            lambda: b.attend(return_lse=False)), prefill_flops(wl),
+        "TFLOP/s", tf_peak)
+    del b
+    torch.cuda.empty_cache()
+    return out
+
+
 # -------------------------------------------------------------- CPU legs
 def oracle_sample(wl, budget_s, max_requests=None, start=0):
     """Time the oracle on whole requests (from ``start``) until ``budget_s``
@@ -417,6 +513,8 @@ def main():
     ap.add_argument("--impl", default="native",
                     choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the other-workload rates")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -438,6 +536,9 @@ def main():
         torch.distributed.barrier()
     api.load_library()
     res = gpu_arm(args, rank, world, dev)
+    if rank == 0 and world == 1 and not args.no_extras:
+        hbm_peak, tf_peak, _ = measured_peaks()
+        res["other_workloads"] = other_workloads(dev, hbm_peak, tf_peak)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline()
     if rank == 0:
