@@ -265,18 +265,35 @@ def gpu_arm(args, rank, world, dev):
                       "right after it" % CLOCK_SOAK_S)
     api.check_device_errors(dev)
 
-    # e2e: same step through the public API from pinned host buffers
-    host = {k: getattr(batch, k).cpu().pin_memory() for k in
-            ("q", "k_new", "v_new", "slots_new", "block_table", "seqused_k",
-             "cu_seqlens_q")}
+    # e2e: same step through the public API from pinned host memory.  The
+    # step's inputs live in one pinned host buffer and one device buffer
+    # (256-byte aligned segments; the batch's tensors become views of the
+    # device one), so each step is one host->device copy, the step, and one
+    # device->host copy of the output.
+    names = ("q", "k_new", "v_new", "slots_new", "block_table", "seqused_k",
+             "cu_seqlens_q")
+    segs, total = [], 0
+    for k in names:
+        t = getattr(batch, k)
+        nb = t.numel() * t.element_size()
+        segs.append((k, total, nb))
+        total = (total + nb + 255) // 256 * 256
+    dev_in = torch.empty(total, dtype=torch.uint8, device=dev)
+    host_in = torch.empty(total, dtype=torch.uint8, pin_memory=True)
+    for k, off, nb in segs:
+        t = getattr(batch, k)
+        view = dev_in[off:off + nb].view(t.dtype).view(t.shape)
+        view.copy_(t)
+        host_in[off:off + nb].copy_(t.contiguous().view(-1).view(torch.uint8)
+                                    .cpu())
+        setattr(batch, k, view)
     out_host = torch.empty(batch.out.shape, dtype=batch.out.dtype,
                            pin_memory=True)
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d = sum(nb for _, _, nb in segs)
     d2h = out_host.numel() * out_host.element_size()
 
     def e2e_step(i):
-        for k, t in host.items():
-            getattr(batch, k).copy_(t, non_blocking=True)
+        dev_in.copy_(host_in, non_blocking=True)
         batch.step()
         out_host.copy_(batch.out, non_blocking=True)
 
