@@ -459,3 +459,18 @@ def test_cascade_with_sinks(cuda_device):
                         wl.softmax_scale, sinks=sinks.double().numpy())
     assert_close(wl, b.out.float().cpu().numpy(), None, ro, None,
                  "cascade sinks")
+
+
+def test_many_requests_prefill_and_decode(cuda_device):
+    """2100 requests, a mix of decode-class and prefill-class ones: more than
+    the prefill kernel caches per CTA (its request metadata is then read from
+    global memory), many work items per CTA, and a decode grid over
+    thousands of (request, KV head) pairs."""
+    rng = np.random.default_rng(77)
+    n = 2100
+    q_lens = np.where(rng.random(n) < 0.5, 1, rng.integers(5, 40, n))
+    seq_lens = q_lens + rng.integers(0, 300, n)
+    wl = workloads.build_workload("many", 78, q_lens.tolist(),
+                                  seq_lens.tolist(), 8, 2, 128, 16,
+                                  device=cuda_device)
+    _sampled(wl, cuda_device, [0, 1, 777, 1500, 2098, 2099])
