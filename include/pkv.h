@@ -146,7 +146,13 @@ PKV_API pkv_status pkv_reshape_and_cache(
  * softmax_lse  : float [num_heads, total_q] device, natural log, or NULL.
  * workspace    : device scratch of workspace_bytes >= the value
  *                pkv_paged_attention_workspace_size returns for the same
- *                arguments (may be NULL when that value is 0).
+ *                arguments (may be NULL when that value is 0), 256-byte
+ *                aligned.  For calls with prefill-class requests its last
+ *                256 bytes hold the prefill kernel's work-item counter,
+ *                which the call zeroes itself; a workspace short of those
+ *                256 bytes (or NULL, when the rest needs none) is accepted
+ *                and the kernel then deals its items in a fixed order, which
+ *                balances the SMs less well.
  * dtype        : PKV_F16 or PKV_BF16 (q, cache and out share it).
  * head_size    : 64, 128 or 256 (others: PKV_ERR_UNSUPPORTED).
  * Hq % Hkv != 0, block_size % 16 != 0: PKV_ERR_INVALID_ARG.
@@ -259,8 +265,10 @@ PKV_API pkv_status pkv_paged_attention_varlen_opts(
 
 /*
  * Bytes of workspace pkv_paged_attention_varlen needs for these arguments
- * (on the current device: the split plan depends on its SM count).  Returns
- * 0 when no scratch is needed, and (size_t)-1 for invalid arguments.
+ * (on the current device: the split plan depends on its SM count), counting
+ * the optional 256-byte item counter of calls with prefill-class requests
+ * (max_seqlen_q * num_heads / num_kv_heads > 16).  Returns 0 when no
+ * scratch is needed, and (size_t)-1 for invalid arguments.
  */
 PKV_API size_t pkv_paged_attention_workspace_size(
     int batch, int total_q, int max_seqlen_q, int max_seqlen_k,

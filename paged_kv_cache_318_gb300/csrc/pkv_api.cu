@@ -162,6 +162,14 @@ Plan make_plan(int batch, int total_q, int max_q, int max_k, int Hq, int Hkv,
   return pl;
 }
 
+// Past the required workspace, calls with prefill-class requests take 256
+// bytes more for the persistent prefill kernel's item counter.  They are
+// optional: a workspace without them still runs, with a fixed item order.
+constexpr size_t kSchedBytes = 256;
+size_t with_sched(size_t need, bool prefill) {
+  return prefill ? align256(need) + kSchedBytes : need;
+}
+
 // fp8 cache with prefill-class requests: 16-bit copies of up to
 // batch * max_blocks pages (K and V) plus their block table.
 size_t fp8_mock_bytes(int batch, int max_blocks, int BS, int Hkv, int D) {
@@ -336,21 +344,19 @@ size_t pkv_paged_attention_workspace_size_opts(
     return static_cast<size_t>(-1);
   int sms = 0;
   if (device_info(nullptr, &sms) != PKV_OK) return static_cast<size_t>(-1);
-  const size_t base =
+  const Plan pl =
       make_plan(batch, total_q, max_seqlen_q, max_seqlen_k, num_heads,
                 num_kv_heads, head_size, causal,
                 window_left < 0 ? -1 : window_left,
                 window_right < 0 ? -1 : window_right, num_splits, sms,
-                fixed_split_of(opts))
-          .workspace;
+                fixed_split_of(opts));
   const bool fp8 = opts && opts->kv_cache_fp8;
-  const bool prefill =
-      static_cast<int64_t>(max_seqlen_q) * (num_heads / num_kv_heads) >
-      kDecodeRows;
-  if (!fp8 || !prefill || batch == 0) return base;
+  if (!fp8 || !pl.prefill) return with_sched(pl.workspace, pl.prefill);
   if (max_blocks_per_seq <= 0) return static_cast<size_t>(-1);
-  return align256(base) + fp8_mock_bytes(batch, max_blocks_per_seq,
-                                         block_size, num_kv_heads, head_size);
+  return with_sched(align256(pl.workspace) +
+                        fp8_mock_bytes(batch, max_blocks_per_seq, block_size,
+                                       num_kv_heads, head_size),
+                    true);
 }
 
 size_t pkv_paged_attention_workspace_size(int batch, int total_q,
@@ -365,10 +371,10 @@ size_t pkv_paged_attention_workspace_size(int batch, int total_q,
     return static_cast<size_t>(-1);
   int sms = 0;
   if (device_info(nullptr, &sms) != PKV_OK) return static_cast<size_t>(-1);
-  return make_plan(batch, total_q, max_seqlen_q, max_seqlen_k, num_heads,
-                   num_kv_heads, head_size, causal, window_left, window_right,
-                   num_splits, sms)
-      .workspace;
+  const Plan pl = make_plan(batch, total_q, max_seqlen_q, max_seqlen_k,
+                            num_heads, num_kv_heads, head_size, causal,
+                            window_left, window_right, num_splits, sms);
+  return with_sched(pl.workspace, pl.prefill);
 }
 
 pkv_status pkv_paged_attention_varlen(
@@ -482,6 +488,12 @@ pkv_status pkv_paged_attention_varlen_opts(
     if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
       return fail(PKV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   }
+  int* sched = nullptr;
+  if (pl.prefill && workspace &&
+      reinterpret_cast<uintptr_t>(workspace) % 256 == 0 &&
+      workspace_bytes >= with_sched(need, true))
+    sched = reinterpret_cast<int*>(static_cast<char*>(workspace) +
+                                   align256(need));
 
   AttnParams p{};
   p.q = q;
@@ -589,6 +601,7 @@ pkv_status pkv_paged_attention_varlen_opts(
     f.min_rows = kDecodeRows + 1;
     f.max_rows = 0x7fffffff;
     f.chunk = 0;
+    f.sched = sched;
     const int64_t prow = static_cast<int64_t>(max_seqlen_q) * p.G;
     cudaError_t e;
     if (kv8) {

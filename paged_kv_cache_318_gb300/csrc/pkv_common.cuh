@@ -227,6 +227,9 @@ struct AttnParams {
   int chunk;
   float* part_o;              // [S, total_q, Hq, D] fp32
   float* part_lse;            // [S, Hq, total_q] fp32 natural log
+  // persistent prefill: one int of workspace the kernel hands work items
+  // out through (the launcher zeroes it first); null = fixed item order
+  int* sched;
   unsigned* err;
 };
 

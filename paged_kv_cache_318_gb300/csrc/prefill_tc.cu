@@ -35,6 +35,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
+#include <string.h>
 
 #include <mutex>
 #include <type_traits>
@@ -114,6 +115,8 @@ struct TcParams {
   int n_items;            // persistent kernel: work items (an upper bound)
   int out_v8;             // output rows 32-byte aligned: 256-bit stores
   int kv_order_hnd;   // tensor-map dim order: 1 = (D, BS, Hkv, NB)
+  int* sched;             // persistent kernel: zeroed item counter, or null
+  int q_tma;              // persistent kernel: Q tiles arrive as TMA boxes
   unsigned* err;
 };
 
@@ -1329,7 +1332,12 @@ prefill_pp_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
 // O_x needs no extra wait).
 constexpr int PT_THREADS = 384;
 constexpr int PT_MMA_WARP = 8;
-constexpr int PT_LOAD_WARP = 9;    // warps 9 (K) and 10 (V); warp 11 idles
+constexpr int PT_LOAD_WARP = 9;    // warps 9 (K) and 10 (V); warp 11: Q
+// Work items (their geometry) travel through a ring of PT_ITEM_SLOTS
+// shared-memory slots; every warp but warp 11 (which fills it) reads each
+// slot once: 8 softmax warps, the MMA warp and the K and V loaders.
+constexpr int PT_ITEM_SLOTS = 4;
+constexpr int PT_ITEM_READERS = 11;
 // Register split (setmaxnreg): the launch gives 168 per thread (384 x 168 =
 // 64512); the softmax warpgroups take 200, warpgroup 2 keeps 96:
 // 256 x 200 + 128 x 96 = 63488.  The launcher checks the 168.
@@ -1355,10 +1363,13 @@ struct PTCfg {
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
   static constexpr int OFF_BAR = OFF_V + STAGES * KV_BYTES;
   static constexpr int BAR_BYTES = 256;
+  // ring of work items (PtItem, 112 bytes each) dealt by warp 11
+  static constexpr int OFF_RING = OFF_BAR + BAR_BYTES;
+  static constexpr int RING_BYTES = PT_ITEM_SLOTS * 112;
   // per-request metadata (cu_seqlens_q, key count, key offset) cached in
   // shared memory for batches up to META_MAX requests
   static constexpr int META_MAX = 2048;
-  static constexpr int OFF_META = OFF_BAR + BAR_BYTES;
+  static constexpr int OFF_META = OFF_RING + RING_BYTES;
   static constexpr int META_BYTES = (3 * META_MAX + 4) * 4;
   static constexpr int SMEM = OFF_META + META_BYTES;
 };
@@ -1391,6 +1402,31 @@ __device__ __forceinline__ void add2(float& s0, float& s1, float a0,
   asm("mov.b64 {%0, %1}, %2;" : "=f"(s0), "=f"(s1) : "l"(sv));
 }
 
+// max(a, b, c) in one instruction (three-input max, sm_100 and later).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// min(max(a + b, 0), 1): the saturating add of the FMA pipe.
+__device__ __forceinline__ float add_sat(float a, float b) {
+  float d;
+  asm("add.rn.sat.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+
+// (s0, s1) <- (s0, s1) * m + c, one packed FMA.
+__device__ __forceinline__ void fma2_pair(float& s0, float& s1, float m,
+                                          float c) {
+  uint64_t sv, mv, cv;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(sv) : "f"(s0), "f"(s1));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(mv) : "f"(m));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(cv) : "f"(c));
+  asm("fma.rn.f32x2 %0, %0, %1, %2;" : "+l"(sv) : "l"(mv), "l"(cv));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(s0), "=f"(s1) : "l"(sv));
+}
+
 // D += A * B with A (M = 128 rows x K = 16, 16-bit) in tensor memory.
 __device__ __forceinline__ void mma_f16_tmem_a_warp(uint32_t d_tmem,
                                                     uint32_t a_tmem,
@@ -1405,15 +1441,20 @@ __device__ __forceinline__ void mma_f16_tmem_a_warp(uint32_t d_tmem,
       : "memory");
 }
 
-// Geometry of one work item (request b, 256-row pair tile, KV head g),
-// computed by every warp that needs it (a warp-wide scan over cu_seqlens_q;
-// all lanes must call it).  False for an index past the real items.
+// Geometry of one work item (request b, 256-row pair tile, KV head g).
+// pt_item computes it (a warp-wide scan over cu_seqlens_q; all lanes must
+// call it; false for an index past the real items); the persistent kernel
+// does that in one warp and hands the struct to the others through shared
+// memory, so it is plain ints, 16-byte multiple in size.
 struct PtItem {
+  int item;                      // work-item index; -1 marks the end
   int b, g, q0, q_len, rows, L, ctx, koff, L_tab;
   int rx0[2], rx_end[2], kmn[2], kmx[2], tlo[2], nx[2];
-  bool has[2];
+  int has[2];
   int kstart, kmax_u, n_tiles;
+  int unused;                    // pads the struct to 7 x 16 bytes
 };
+static_assert(sizeof(PtItem) == 112, "PtItem is copied as 7 x 16 bytes");
 
 struct PtMeta {
   const int* cu_q;     // [batch + 1]
@@ -1509,17 +1550,23 @@ __device__ __forceinline__ bool pt_item(const TcParams& p, int item, int lane,
   return true;
 }
 
-// Persistent: each CTA walks the work items blockIdx.x, blockIdx.x +
-// gridDim.x, ...; every role keeps running counters across items, so the
-// loaders fetch the next item's K / V and warp 11 its Q while the softmax
-// warps finish the previous item's output.  Per item: q_full (Q in place),
+// Persistent: each CTA walks a sequence of work items; every role keeps
+// running counters across items, so the loaders fetch the next item's K / V
+// and warp 11 its Q while the softmax warps finish the previous item's
+// output.  With p.sched (a zeroed counter) the items are dealt out at run
+// time: a CTA starts with item blockIdx.x, and warp 11 claims the next one
+// (gridDim.x + an atomic ticket) as the current one starts, so an SM that
+// drew short items takes more of them and the SMs finish within about two
+// items of each other.  Without a counter the items are blockIdx.x,
+// blockIdx.x + gridDim.x, ...  Per item: q_full (Q in place),
 // q_empty (the item's S MMAs are done with Q), o_ready (its MMAs are
 // complete) and o_free[x] (the softmax of tile x has read O_x); the MMA
 // warp waits o_free[x] of the previous item before it writes O_x again.
 template <typename T, int D>
 __global__ void __launch_bounds__(PT_THREADS, 1)
 prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v) {
+                     const __grid_constant__ CUtensorMap tm_v,
+                     const __grid_constant__ CUtensorMap tm_q) {
   using C = PTCfg<D>;
   constexpr int BN = C::BN;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -1551,6 +1598,12 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + C::OFF_BAR + 8 * 18);
   volatile int* abort_flag =
       reinterpret_cast<volatile int*>(base + C::OFF_BAR + 8 * 18 + 4);
+  // item ring: it_full[s] (warp 11 wrote slot s), it_empty[s] (all readers
+  // are done with it)
+  auto it_full = [&](int s) { return bar0 + 8 * (19 + s); };
+  auto it_empty = [&](int s) { return bar0 + 8 * (19 + PT_ITEM_SLOTS + s); };
+  static_assert(8 * (19 + 2 * PT_ITEM_SLOTS) <= C::BAR_BYTES, "barrier area");
+  const bool dyn = p.sched != nullptr;
 
   if (tid == 0) {
     for (int s = 0; s < 2; ++s) {
@@ -1563,9 +1616,13 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
       mbar_init(o_free(s), 128);
     }
     mbar_init(o_ready, 1);
-    mbar_init(q_full, 32);
+    mbar_init(q_full, p.q_tma ? 1 : 32);
     mbar_init(q_empty, 1);
     mbar_init(drain_bar, 1);
+    for (int s = 0; s < PT_ITEM_SLOTS; ++s) {
+      mbar_init(it_full(s), 1);
+      mbar_init(it_empty(s), PT_ITEM_READERS);
+    }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -1605,6 +1662,22 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int n_items = p.n_items;
+  // The CTA's n-th item from the ring (all lanes of a reader warp call it,
+  // in order n = 0, 1, ...): 1 = an item, 0 = no more items, -1 = abort.
+  auto take_item = [&](int n, PtItem& it) -> int {
+    const int s = n % PT_ITEM_SLOTS;
+    if (!mbar_wait(it_full(s), (n / PT_ITEM_SLOTS) & 1, abort_flag, p.err))
+      return -1;
+    const int4* src =
+        reinterpret_cast<const int4*>(base + C::OFF_RING + s * 112);
+    int4 w[7];
+#pragma unroll
+    for (int k = 0; k < 7; ++k) w[k] = src[k];
+    memcpy(&it, w, sizeof(PtItem));
+    __syncwarp();
+    if (lane == 0) mbar_arrive(it_empty(s));
+    return it.item >= 0 ? 1 : 0;
+  };
 
   if (warp >= 8) {
   // warpgroup 2 (MMA, K / V loaders, Q loader) gives registers back to the
@@ -1619,9 +1692,13 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
                          : static_cast<const void*>(&tm_k);
     int gj = 0;                                // tiles issued so far
     bool ok = true;
-    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+    for (int n = 0; ok; ++n) {
       PtItem it;
-      if (!pt_item(p, item, lane, BN, md, it)) continue;
+      const int got = take_item(n, it);
+      if (got <= 0) {
+        ok = got == 0;
+        break;
+      }
       if (it.L_tab < it.L && lane == 0 && warp == PT_LOAD_WARP)
         atomicOr(p.err, kErrBadTable);
       const int32_t* bt =
@@ -1689,9 +1766,10 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
     int gj = 0;                       // K / V tiles consumed so far
     int pv_cnt[2] = {0, 0};           // P_x V MMAs issued so far
     int n_done = 0;                   // items finished
-    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-      PtItem it;
-      if (!pt_item(p, item, lane, BN, md, it)) continue;
+    PtItem it;
+    int got = take_item(0, it);
+    ok = got >= 0;
+    while (got > 0 && ok) {
       if (!mbar_wait(q_full, n_done & 1, abort_flag, p.err)) {
         ok = false;
         break;
@@ -1798,6 +1876,11 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
         if (j == it.n_tiles - 1 || it.n_tiles == 0) mma_commit_warp(q_empty);
       }
       if (!ok) break;
+      // the next item, taken from the ring before o_ready lets the output
+      // stores start (they hold up shared-memory access while they drain)
+      PtItem it_next;
+      const int got_next = take_item(n_done + 1, it_next);
+      if (got_next < 0) break;
       // the previous item's O_x must be read before o_ready can move on
       if (!claim_o(0) || !claim_o(1)) {
         ok = false;
@@ -1806,6 +1889,8 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
       mma_commit_warp(o_ready);
       gj += it.n_tiles;
       ++n_done;
+      it = it_next;
+      got = got_next;
     }
     // wait for every MMA of this CTA on a barrier no other role waits on (an
     // extra o_ready phase could complete before a softmax warp has waited
@@ -1813,37 +1898,93 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
     mma_commit_warp(drain_bar);
     mbar_drain(drain_bar, 0);
   } else if (warp == PT_LOAD_WARP + 2) {
-    // ---------------------------------------------------- Q loader (warp 11)
-    int n_done = 0;
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-      PtItem it;
-      if (!pt_item(p, item, lane, BN, md, it)) continue;
-      if (n_done >= 1 &&
-          !mbar_wait(q_empty, (n_done - 1) & 1, abort_flag, p.err))
-        break;
-      // both Q tiles: packed rows, zero past each tile's end; lane i
-      // copies rows i, i + 32, ... (one address computation per row)
-      const T* Q = static_cast<const T*>(p.q);
-      for (int rr = lane; rr < PP_ROWS; rr += 32) {
-        const int xq = rr / BM, rq = rr % BM;
-        const int Rq = it.rx0[xq] + rq;
-        const bool okq = Rq < it.rx_end[xq];
-        const T* src = Q;
-        if (okq)
-          src = Q + static_cast<int64_t>(it.q0 + Rq / G) * p.q_st +
-                static_cast<int64_t>(it.g * G + Rq % G) * p.q_sh;
-        const uint32_t dst = sQ + xq * C::Q_BYTES;
+    // ------------------------------------ Q loader and item dealer (warp 11)
+    // Slot n of the ring gets the CTA's n-th item (its PtItem; item = -1
+    // ends every reader's loop).  Item n + 1 is chosen and published as
+    // item n starts, so the loaders can fetch its first K / V tiles and the
+    // MMA and softmax warps read its geometry while item n still runs.
+    auto publish = [&](int n, const PtItem& it) -> bool {
+      const int s = n % PT_ITEM_SLOTS;
+      if (n >= PT_ITEM_SLOTS &&
+          !mbar_wait(it_empty(s), ((n / PT_ITEM_SLOTS) - 1) & 1, abort_flag,
+                     p.err))
+        return false;
+      if (lane == 0) {
+        int4 w[7];
+        memcpy(w, &it, sizeof(PtItem));
+        int4* dst = reinterpret_cast<int4*>(base + C::OFF_RING + s * 112);
 #pragma unroll
-        for (int ch = 0; ch < D / 8; ++ch)
-          cp_async_16(dst + (ch >> 3) * (BM * 128) + sw128(rq, ch & 7),
-                      okq ? src + ch * 8 : src, okq ? 16 : 0);
+        for (int k = 0; k < 7; ++k) dst[k] = w[k];
+        mbar_arrive(it_full(s));
       }
-      cp_async_commit();
-      cp_async_wait<0>();
-      fence_proxy_async();
-      mbar_arrive(q_full);
-      ++n_done;
+      return true;
+    };
+    int item = static_cast<int>(blockIdx.x);     // gridDim.x <= n_items
+    int q_issued = 0;                            // Q loads as TMA boxes
+    for (int n = 0;; ++n) {
+      PtItem it;
+      const bool real = item >= 0 && pt_item(p, item, lane, BN, md, it);
+      it.item = real ? item : -1;
+      if (!publish(n, it) || !real) break;
+      // the previous item's S MMAs are done with Q
+      if (n >= 1 && !mbar_wait(q_empty, (n - 1) & 1, abort_flag, p.err))
+        break;
+      if (p.q_tma) {
+        // one box per (tile, 64 columns): 128 / G tokens x the G heads of
+        // KV head g, which is the tile's 128 packed rows in order.  Rows
+        // past the request are the next tokens' (or, past the tensor,
+        // zeros): they only feed S rows no output is taken from.
+        if (lane == 0) {
+          mbar_expect_tx(q_full, (it.has[1] ? 2 : 1) * C::Q_BYTES);
+#pragma unroll
+          for (int xq = 0; xq < 2; ++xq) {
+            if (!it.has[xq]) continue;
+#pragma unroll
+            for (int cb = 0; cb < C::NCB; ++cb)
+              tma_load_3d(sQ + xq * C::Q_BYTES + cb * (BM * 128), &tm_q,
+                          cb * 64, it.g * G, it.q0 + it.rx0[xq] / G, q_full);
+          }
+        }
+        ++q_issued;
+      } else {
+        // both Q tiles: packed rows, zero past each tile's end; lane i
+        // copies rows i, i + 32, ... (one address computation per row)
+        const T* Q = static_cast<const T*>(p.q);
+        for (int rr = lane; rr < PP_ROWS; rr += 32) {
+          const int xq = rr / BM, rq = rr % BM;
+          const int Rq = it.rx0[xq] + rq;
+          const bool okq = Rq < it.rx_end[xq];
+          const T* src = Q;
+          if (okq)
+            src = Q + static_cast<int64_t>(it.q0 + Rq / G) * p.q_st +
+                  static_cast<int64_t>(it.g * G + Rq % G) * p.q_sh;
+          const uint32_t dst = sQ + xq * C::Q_BYTES;
+#pragma unroll
+          for (int ch = 0; ch < D / 8; ++ch)
+            cp_async_16(dst + (ch >> 3) * (BM * 128) + sw128(rq, ch & 7),
+                        okq ? src + ch * 8 : src, okq ? 16 : 0);
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+        fence_proxy_async();
+        mbar_arrive(q_full);
+      }
+      // the next item: dealt at run time (an atomic ticket) or the fixed
+      // stride; an index past the real items becomes the end marker
+      if (dyn) {
+        int v = 0;
+        if (lane == 0)
+          v = static_cast<int>(gridDim.x) + atomicAdd(p.sched, 1);
+        item = __shfl_sync(0xffffffffu, v, 0);
+      } else {
+        const int64_t i = blockIdx.x + static_cast<int64_t>(n + 1) * gridDim.x;
+        item = i < n_items ? static_cast<int>(i) : -1;
+      }
+      if (item >= n_items) item = -1;
     }
+    // no Q box may be in flight when the CTA exits (the MMA warp waits for
+    // every one it uses, but not after an abort)
+    if (lane == 0 && q_issued > 0) mbar_drain(q_full, (q_issued - 1) & 1);
   }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(PT_SOFTMAX_REGS));
@@ -1862,9 +2003,10 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
     int s_cnt = 0;                            // S_x tiles seen so far
     int n_done = 0;
     bool ok = true;
-    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-      PtItem it;
-      if (!pt_item(p, item, lane, BN, md, it)) continue;
+    PtItem it;
+    int got = take_item(0, it);
+    ok = got >= 0;
+    while (got > 0 && ok) {
       const int my_rx0 = x ? it.rx0[1] : it.rx0[0];
       const int my_rx_end = x ? it.rx_end[1] : it.rx_end[0];
       const bool my_has = x ? it.has[1] : it.has[0];
@@ -1918,12 +2060,51 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
         float mx8[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
-        // interior tiles keep the raw scores: max(scale * s) = scale *
-        // max(s) for scale > 0, and the scale joins the exponent's FMA
-        const bool raw = plain && unmasked && scale_log2 > 0.f;
-        if (raw) {
+        // plain scores stay raw: max(scale * s) = scale * max(s) for scale
+        // > 0, and the scale joins the exponent's FMA
+        const bool raw = plain && scale_log2 > 0.f;
+        if (raw && unmasked) {
 #pragma unroll
-          for (int e = 0; e < BN; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], v[e]);
+          for (int e = 0; e < BN; e += 2)
+            mx8[(e >> 1) & 7] = max3f(mx8[(e >> 1) & 7], v[e], v[e + 1]);
+        } else if (raw) {
+          // a key outside [lo_rel, lo_rel + n_rel) becomes min(s, -2^126):
+          // its flag f (1 out, 0 in) comes from saturating adds on the FMA
+          // pipe and the bound 2^126 - f * 2^127 from one packed FMA, in
+          // place of integer compares and a select per key on the ALU pipe.
+          // The min also replaces a NaN score (a key row past the
+          // request's end may hold one).
+          constexpr float kBig = 8.50705917e37f;       // 2^126
+          const int hi_rel = lo_rel + n_rel;
+          if (p.wl < 0) {
+            // no left window: lo_rel <= 0, only keys >= hi_rel are out;
+            // f = sat(e + 1 - hi_rel)
+            const float one_m_hi = static_cast<float>(1 - hi_rel);
+#pragma unroll
+            for (int e = 0; e < BN; e += 2) {
+              float b0 = add_sat(static_cast<float>(e), one_m_hi);
+              float b1 = add_sat(static_cast<float>(e + 1), one_m_hi);
+              fma2_pair(b0, b1, -2.f * kBig, kBig);
+              v[e] = fminf(v[e], b0);
+              v[e + 1] = fminf(v[e + 1], b1);
+              mx8[(e >> 1) & 7] = max3f(mx8[(e >> 1) & 7], v[e], v[e + 1]);
+            }
+          } else {
+            // out iff |2e - (lo + hi - 1)| > hi - 1 - lo, i.e. f =
+            // sat(|2e - c2| - r2) (the left side moves in steps of 2)
+            const float c2 = static_cast<float>(lo_rel + hi_rel - 1);
+            const float r2 = static_cast<float>(hi_rel - 1 - lo_rel);
+#pragma unroll
+            for (int e = 0; e < BN; e += 2) {
+              float b0 = add_sat(fabsf(static_cast<float>(2 * e) - c2), -r2);
+              float b1 =
+                  add_sat(fabsf(static_cast<float>(2 * e + 2) - c2), -r2);
+              fma2_pair(b0, b1, -2.f * kBig, kBig);
+              v[e] = fminf(v[e], b0);
+              v[e + 1] = fminf(v[e + 1], b1);
+              mx8[(e >> 1) & 7] = max3f(mx8[(e >> 1) & 7], v[e], v[e + 1]);
+            }
+          }
         } else if (plain) {
 #pragma unroll
           for (int e = 0; e < BN; ++e) {
@@ -1945,10 +2126,11 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
             mx8[e & 7] = fmaxf(mx8[e & 7], v[e]);
           }
         }
-        float mx =
-            fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                  fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-        if (raw) mx *= scale_log2;
+        float mx = max3f(max3f(mx8[0], mx8[1], mx8[2]),
+                         max3f(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+        // a row with every key of the tile out keeps -inf (its scores sit
+        // at -2^126)
+        if (raw) mx = mx < -0.5f * 8.50705917e37f ? -INFINITY : mx * scale_log2;
         const bool grow = mx > m_ref + kRescaleThreshold;
         float alpha = 1.f;
         if (grow) {
@@ -2002,6 +2184,11 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
         mbar_arrive(p_full(x));
       }
       if (!ok) break;
+      // the next item's geometry, read before this item's output stores
+      // (they hold up shared-memory access while they drain)
+      PtItem it_next;
+      const int got_next = take_item(n_done + 1, it_next);
+      if (got_next < 0) break;
       // ---- epilogue: every MMA of the item is complete
       if (!mbar_wait(o_ready, n_done & 1, abort_flag, p.err)) break;
       tc_fence_after();
@@ -2056,6 +2243,8 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
         }
       }
       ++n_done;
+      it = it_next;
+      got = got_next;
     }
   }
 
@@ -2121,7 +2310,51 @@ bool make_kv_map(CUtensorMap* map, const void* ptr, bool bf16, int D, int BS,
 }
 
 
+// 3-D map over the query rows [T, Hq, D] (element strides s_tok, s_head;
+// unit stride along D): dims (D, Hq, T), box 64 x G x (128 / G), 128-byte
+// swizzled.  One box holds 64 columns of the 128 packed rows (token, head of
+// one KV group) of a Q tile, in the order and layout the S MMA reads.
+// False when G does not divide 128 or the driver rejects the map.
+static bool make_rows_map(CUtensorMap* map, const void* ptr, bool bf16, int D,
+                          int Hq, int T, int64_t s_tok, int64_t s_head,
+                          int G) {
+  auto fn = encode_fn();
+  if (!fn || G <= 0 || 128 % G != 0 || T <= 0) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D),
+                        static_cast<cuuint64_t>(Hq),
+                        static_cast<cuuint64_t>(T)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(s_head) * 2,
+                           static_cast<cuuint64_t>(s_tok) * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G),
+                       static_cast<cuuint32_t>(128 / G)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map,
+                  bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                       : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                  3, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int prefill_tc_block_keys(int) { return 64; }
+
+// Shared-memory opt-in once per kernel (a short list: 10 kernels).
+static cudaError_t smem_opt_in(const void* kern, int smem) {
+  static std::mutex mu;
+  static const void* done[16] = {};
+  std::lock_guard<std::mutex> lk(mu);
+  int i = 0;
+  while (i < 16 && done[i] && done[i] != kern) ++i;
+  if (i == 16 || !done[i]) {
+    cudaError_t e = cudaFuncSetAttribute(
+        kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    if (i < 16) done[i] = kern;
+  }
+  return cudaSuccess;
+}
 
 cudaError_t launch_prefill_attn_tc(const AttnParams& a, int D, bool bf16,
                                    int grid_y, bool p_in_tmem,
@@ -2191,19 +2424,8 @@ cudaError_t launch_prefill_attn_tc(const AttnParams& a, int D, bool bf16,
   p.n_items = static_cast<int>(gx);
   auto go = [&](void (*kern)(TcParams, CUtensorMap, CUtensorMap), int smem,
                 int threads) -> cudaError_t {
-    // shared-memory opt-in once per kernel (a short list: 10 kernels)
-    static std::mutex mu;
-    static const void* done[16] = {};
-    std::lock_guard<std::mutex> lk(mu);
-    int i = 0;
-    while (i < 16 && done[i] && done[i] != reinterpret_cast<const void*>(kern))
-      ++i;
-    if (i == 16 || !done[i]) {
-      cudaError_t e = cudaFuncSetAttribute(
-          kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      if (e != cudaSuccess) return e;
-      if (i < 16) done[i] = reinterpret_cast<const void*>(kern);
-    }
+    cudaError_t e = smem_opt_in(reinterpret_cast<const void*>(kern), smem);
+    if (e != cudaSuccess) return e;
     note_launch();
     kern<<<grid, threads, smem, stream>>>(p, mk, mv);
     return cudaGetLastError();
@@ -2234,30 +2456,41 @@ cudaError_t launch_prefill_attn_tc(const AttnParams& a, int D, bool bf16,
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
             cudaSuccess || sms <= 0)
       sms = 1;
-    if (static_cast<int64_t>(sms) < gx) grid = dim3(static_cast<unsigned>(sms));
+    if (static_cast<int64_t>(sms) < gx) {
+      grid = dim3(static_cast<unsigned>(sms));
+      // items dealt at run time when the caller's workspace holds a counter
+      if (a.sched) {
+        cudaError_t e = cudaMemsetAsync(a.sched, 0, sizeof(int), stream);
+        if (e != cudaSuccess) return e;
+        p.sched = a.sched;
+      }
+    }
   }
-  if (p_in_tmem && bf16) {
-    switch (D) {
-      case 64:
-        return go(prefill_ptmem_kernel<__nv_bfloat16, 64>, PTCfg<64>::SMEM,
-                  PT_THREADS);
-      case 128:
-        return go(prefill_ptmem_kernel<__nv_bfloat16, 128>,
-                  PTCfg<128>::SMEM, PT_THREADS);
-      default:
-        break;
-    }
-  } else if (p_in_tmem) {
-    switch (D) {
-      case 64:
-        return go(prefill_ptmem_kernel<__half, 64>, PTCfg<64>::SMEM,
-                  PT_THREADS);
-      case 128:
-        return go(prefill_ptmem_kernel<__half, 128>, PTCfg<128>::SMEM,
-                  PT_THREADS);
-      default:
-        break;
-    }
+  if (p_in_tmem && D <= 128) {
+    // Q tiles as TMA boxes when the KV group size divides the 128-row tile
+    // (the rows of a tile are then whole tokens); else cp.async rows
+    CUtensorMap mq;
+    memset(&mq, 0, sizeof(mq));
+    p.q_tma = make_rows_map(&mq, a.q, bf16, D, a.Hq, a.total_q, a.q_st,
+                            a.q_sh, a.G)
+                  ? 1
+                  : 0;
+    auto go3 = [&](void (*kern)(TcParams, CUtensorMap, CUtensorMap,
+                                CUtensorMap),
+                   int smem) -> cudaError_t {
+      cudaError_t e = smem_opt_in(reinterpret_cast<const void*>(kern), smem);
+      if (e != cudaSuccess) return e;
+      note_launch();
+      kern<<<grid, PT_THREADS, smem, stream>>>(p, mk, mv, mq);
+      return cudaGetLastError();
+    };
+    if (bf16)
+      return D == 64 ? go3(prefill_ptmem_kernel<__nv_bfloat16, 64>,
+                           PTCfg<64>::SMEM)
+                     : go3(prefill_ptmem_kernel<__nv_bfloat16, 128>,
+                           PTCfg<128>::SMEM);
+    return D == 64 ? go3(prefill_ptmem_kernel<__half, 64>, PTCfg<64>::SMEM)
+                   : go3(prefill_ptmem_kernel<__half, 128>, PTCfg<128>::SMEM);
   }
   if (bf16) {
     switch (D) {

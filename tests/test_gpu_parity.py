@@ -474,3 +474,43 @@ def test_many_requests_prefill_and_decode(cuda_device):
                                   seq_lens.tolist(), 8, 2, 128, 16,
                                   device=cuda_device)
     _sampled(wl, cuda_device, [0, 1, 777, 1500, 2098, 2099])
+
+
+@pytest.mark.parametrize("name", ["prefill_with_prefix", "many"])
+def test_prefill_item_order_leaves_bits_unchanged(cuda_device, name):
+    """The persistent prefill kernel deals its work items at run time when
+    the workspace holds its counter, and in a fixed order when it does not.
+    Which SM computes an item must not change a bit of the output or LSE."""
+    if name == "many":
+        rng = np.random.default_rng(79)
+        n = 700
+        q_lens = np.where(rng.random(n) < 0.3, 1, rng.integers(5, 200, n))
+        seq_lens = q_lens + rng.integers(0, 900, n)
+        wl = workloads.build_workload("many_order", 80, q_lens.tolist(),
+                                      seq_lens.tolist(), 16, 4, 128, 16,
+                                      device=cuda_device)
+    else:
+        wl = workloads.prefill_with_prefix(device=cuda_device)
+    b = DeviceBatch(wl, cuda_device)
+    b.write_context()
+    b.write_new()
+    full = b.workspace
+    assert full is not None and full.numel() >= 256
+    out_dyn, lse_dyn = [t.clone() for t in b.attend()]
+    # the same call with the counter's 256 bytes left out of the workspace
+    b.workspace = full[:full.numel() - 256]
+    out_fix, lse_fix = [t.clone() for t in b.attend()]
+    b.workspace = full
+    torch.cuda.synchronize()
+    api.check_device_errors(cuda_device)
+    assert torch.equal(out_dyn.view(torch.int16), out_fix.view(torch.int16))
+    assert torch.equal(lse_dyn.view(torch.int32), lse_fix.view(torch.int32))
+    # and both are right: the last rows of a few requests against the oracle
+    o = out_dyn.float().cpu().numpy()
+    lse = lse_dyn.cpu().numpy()
+    for r in (0, wl.batch // 2, wl.batch - 1):
+        t1 = int(wl.cu_seqlens_q[r + 1])
+        k = min(8, t1 - int(wl.cu_seqlens_q[r]))
+        ref_o, ref_l = request_reference(wl, r, last_rows=k)
+        assert_close(wl, o[t1 - k:t1], lse[:, t1 - k:t1], ref_o, ref_l,
+                     "%s req %d" % (name, r))
