@@ -147,12 +147,13 @@ PKV_API pkv_status pkv_reshape_and_cache(
  * workspace    : device scratch of workspace_bytes >= the value
  *                pkv_paged_attention_workspace_size returns for the same
  *                arguments (may be NULL when that value is 0), 256-byte
- *                aligned.  For calls with prefill-class requests its last
- *                256 bytes hold the prefill kernel's work-item counter,
- *                which the call zeroes itself; a workspace short of those
- *                256 bytes (or NULL, when the rest needs none) is accepted
- *                and the kernel then deals its items in a fixed order, which
- *                balances the SMs less well.
+ *                aligned.  For calls with prefill-class requests it ends
+ *                with an optional tail: 256 bytes for the prefill kernel's
+ *                work-item counter (the call zeroes it), then, when the
+ *                call has fewer prefill work items than SMs, fp32 split-KV
+ *                partials of the prefill kernel.  A workspace short of the
+ *                tail (or NULL, when the rest needs none) is accepted: the
+ *                items are then dealt in a fixed order, or not split.
  * dtype        : PKV_F16 or PKV_BF16 (q, cache and out share it).
  * head_size    : 64, 128 or 256 (others: PKV_ERR_UNSUPPORTED).
  * Hq % Hkv != 0, block_size % 16 != 0: PKV_ERR_INVALID_ARG.
@@ -265,10 +266,11 @@ PKV_API pkv_status pkv_paged_attention_varlen_opts(
 
 /*
  * Bytes of workspace pkv_paged_attention_varlen needs for these arguments
- * (on the current device: the split plan depends on its SM count), counting
- * the optional 256-byte item counter of calls with prefill-class requests
- * (max_seqlen_q * num_heads / num_kv_heads > 16).  Returns 0 when no
- * scratch is needed, and (size_t)-1 for invalid arguments.
+ * (on the current device: the split plans depend on its SM count),
+ * counting the optional tail of calls with prefill-class requests
+ * (max_seqlen_q * num_heads / num_kv_heads > 16): the 256-byte item
+ * counter and the prefill split-KV partials.  Returns 0 when no scratch is
+ * needed, and (size_t)-1 for invalid arguments.
  */
 PKV_API size_t pkv_paged_attention_workspace_size(
     int batch, int total_q, int max_seqlen_q, int max_seqlen_k,
@@ -294,9 +296,11 @@ PKV_API size_t pkv_paged_attention_workspace_size(
  * - Set-up: the first call on each device looks up the array's device
  *   address (cudaGetSymbolAddress, with that device current) and caches it.
  *   Make that first call before any stream capture.
- * - Limit: a call whose split plan needs more than PKV_STATIC_SCRATCH_BYTES
- *   (see pkv_paged_attention_workspace_size) is rejected with
- *   PKV_ERR_WORKSPACE_TOO_SMALL and a message; nothing is launched.
+ * - Limit: a call whose decode split plan (or fp8 page copies) needs more
+ *   than PKV_STATIC_SCRATCH_BYTES is rejected with
+ *   PKV_ERR_WORKSPACE_TOO_SMALL and a message; nothing is launched.  The
+ *   optional prefill tail (see pkv_paged_attention_workspace_size) is used
+ *   when it fits in the rest of the array.
  * - Sharing: all calls on a device share the one array and it keeps the
  *   last call's contents.  Nothing in it needs clearing: every scratch value
  *   a call reads was written earlier in the same call.  Calls that overlap on

@@ -163,11 +163,36 @@ Plan make_plan(int batch, int total_q, int max_q, int max_k, int Hq, int Hkv,
 }
 
 // Past the required workspace, calls with prefill-class requests take 256
-// bytes more for the persistent prefill kernel's item counter.  They are
-// optional: a workspace without them still runs, with a fixed item order.
+// bytes more for the persistent prefill kernel's item counter, then, when
+// the call has fewer prefill work items than SMs, room for that kernel's
+// split-KV partials.  Both are optional: a workspace without them still
+// runs, with a fixed item order and no split.
 constexpr size_t kSchedBytes = 256;
-size_t with_sched(size_t need, bool prefill) {
-  return prefill ? align256(need) + kSchedBytes : need;
+
+// Key splits for the persistent prefill kernel (head size <= 128): only
+// when even an upper bound of its work items, (ceil(total_q * G / 256) +
+// batch) * Hkv, leaves half the SMs idle; as many as keep one wave, with
+// at least 4 key tiles of 128 per split, at most 16.
+int prefill_splits(int batch, int total_q, int G, int Hkv, int max_k, int D,
+                   int sms) {
+  if (D > 128) return 1;
+  const int64_t items =
+      ((static_cast<int64_t>(total_q) * G + 255) / 256 + batch) * Hkv;
+  if (items <= 0 || items * 2 > sms) return 1;
+  int64_t s = sms / items;
+  if (s > max_k / 512) s = max_k / 512;
+  if (s > 16) s = 16;
+  return s >= 2 ? static_cast<int>(s) : 1;
+}
+size_t prefill_split_bytes(int splits, int total_q, int Hq, int D) {
+  if (splits <= 1) return 0;
+  return align256(static_cast<size_t>(splits) * total_q * Hq * D * 4) +
+         align256(static_cast<size_t>(splits) * Hq * total_q * 4);
+}
+// The whole workspace: the required part, then (prefill-class calls) the
+// counter and the split partials.
+size_t with_tail(size_t need, bool prefill, size_t split_bytes) {
+  return prefill ? align256(need) + kSchedBytes + split_bytes : need;
 }
 
 // fp8 cache with prefill-class requests: 16-bit copies of up to
@@ -208,6 +233,25 @@ pkv_status check_attn_shape(int batch, int total_q, int max_q, int max_k,
 }
 
 }  // namespace
+
+// The workspace a call cannot do without (no prefill counter or split
+// partials); the allocation-free entry point checks its scratch against it.
+size_t required_workspace_bytes(int batch, int total_q, int max_seqlen_q,
+                                int max_seqlen_k, int num_heads,
+                                int num_kv_heads, int head_size,
+                                int block_size, int causal, int window_left,
+                                int window_right, int num_splits) {
+  if (check_attn_shape(batch, total_q, max_seqlen_q, max_seqlen_k, num_heads,
+                       num_kv_heads, head_size, block_size,
+                       num_splits) != PKV_OK)
+    return static_cast<size_t>(-1);
+  int sms = 0;
+  if (device_info(nullptr, &sms) != PKV_OK) return static_cast<size_t>(-1);
+  return make_plan(batch, total_q, max_seqlen_q, max_seqlen_k, num_heads,
+                   num_kv_heads, head_size, causal, window_left, window_right,
+                   num_splits, sms)
+      .workspace;
+}
 
 void set_last_error(const char* msg) { g_last_error = msg; }
 
@@ -351,12 +395,18 @@ size_t pkv_paged_attention_workspace_size_opts(
                 window_right < 0 ? -1 : window_right, num_splits, sms,
                 fixed_split_of(opts));
   const bool fp8 = opts && opts->kv_cache_fp8;
-  if (!fp8 || !pl.prefill) return with_sched(pl.workspace, pl.prefill);
+  const size_t split_bytes = prefill_split_bytes(
+      pl.prefill ? prefill_splits(batch, total_q, num_heads / num_kv_heads,
+                                  num_kv_heads, max_seqlen_k, head_size, sms)
+                 : 1,
+      total_q, num_heads, head_size);
+  if (!fp8 || !pl.prefill)
+    return with_tail(pl.workspace, pl.prefill, split_bytes);
   if (max_blocks_per_seq <= 0) return static_cast<size_t>(-1);
-  return with_sched(align256(pl.workspace) +
-                        fp8_mock_bytes(batch, max_blocks_per_seq, block_size,
-                                       num_kv_heads, head_size),
-                    true);
+  return with_tail(align256(pl.workspace) +
+                       fp8_mock_bytes(batch, max_blocks_per_seq, block_size,
+                                      num_kv_heads, head_size),
+                   true, split_bytes);
 }
 
 size_t pkv_paged_attention_workspace_size(int batch, int total_q,
@@ -374,7 +424,12 @@ size_t pkv_paged_attention_workspace_size(int batch, int total_q,
   const Plan pl = make_plan(batch, total_q, max_seqlen_q, max_seqlen_k,
                             num_heads, num_kv_heads, head_size, causal,
                             window_left, window_right, num_splits, sms);
-  return with_sched(pl.workspace, pl.prefill);
+  const size_t split_bytes = prefill_split_bytes(
+      pl.prefill ? prefill_splits(batch, total_q, num_heads / num_kv_heads,
+                                  num_kv_heads, max_seqlen_k, head_size, sms)
+                 : 1,
+      total_q, num_heads, head_size);
+  return with_tail(pl.workspace, pl.prefill, split_bytes);
 }
 
 pkv_status pkv_paged_attention_varlen(
@@ -488,12 +543,28 @@ pkv_status pkv_paged_attention_varlen_opts(
     if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
       return fail(PKV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   }
+  // optional tail: the prefill item counter, then its split partials
   int* sched = nullptr;
+  int pre_splits = 1;
+  float* pre_o = nullptr;
+  float* pre_lse = nullptr;
   if (pl.prefill && workspace &&
-      reinterpret_cast<uintptr_t>(workspace) % 256 == 0 &&
-      workspace_bytes >= with_sched(need, true))
-    sched = reinterpret_cast<int*>(static_cast<char*>(workspace) +
-                                   align256(need));
+      reinterpret_cast<uintptr_t>(workspace) % 256 == 0) {
+    char* tail = static_cast<char*>(workspace) + align256(need);
+    if (workspace_bytes >= with_tail(need, true, 0))
+      sched = reinterpret_cast<int*>(tail);
+    const int sp = prefill_splits(batch, total_q, num_heads / num_kv_heads,
+                                  num_kv_heads, max_seqlen_k, head_size, sms);
+    const size_t sb = prefill_split_bytes(sp, total_q, num_heads, head_size);
+    if (sp > 1 && workspace_bytes >= with_tail(need, true, sb)) {
+      pre_splits = sp;
+      pre_o = reinterpret_cast<float*>(tail + kSchedBytes);
+      pre_lse = reinterpret_cast<float*>(
+          tail + kSchedBytes +
+          align256(static_cast<size_t>(sp) * total_q * num_heads *
+                   head_size * 4));
+    }
+  }
 
   AttnParams p{};
   p.q = q;
@@ -602,6 +673,9 @@ pkv_status pkv_paged_attention_varlen_opts(
     f.max_rows = 0x7fffffff;
     f.chunk = 0;
     f.sched = sched;
+    f.pre_splits = pre_splits;
+    f.pre_o = pre_o;
+    f.pre_lse = pre_lse;
     const int64_t prow = static_cast<int64_t>(max_seqlen_q) * p.G;
     cudaError_t e;
     if (kv8) {
@@ -627,14 +701,36 @@ pkv_status pkv_paged_attention_varlen_opts(
       f.kv_fp8 = 0;          // 16-bit copies; k_scale / v_scale still apply
     }
     const int which = g_prefill_kernel.load();
+    int used = 1;
     if (which == PKV_PREFILL_TCGEN05 || which == PKV_PREFILL_TCGEN05_SMEM_P)
       e = launch_prefill_attn_tc(f, head_size, bf16,
                                  static_cast<int>((prow + 127) / 128),
-                                 which == PKV_PREFILL_TCGEN05, s);
+                                 which == PKV_PREFILL_TCGEN05, &used, s);
     else
       e = launch_prefill_attn_mma(f, head_size, bf16,
                                   static_cast<int>((prow + 63) / 64), s);
     if (e != cudaSuccess) return cuda_fail(e, "prefill attention launch");
+    if (used > 1) {
+      CombineParams c{};
+      c.part_o = pre_o;
+      c.part_lse = pre_lse;
+      c.out = out;
+      c.o_st = o_stride_tok;
+      c.o_sh = o_stride_head;
+      c.lse = softmax_lse;
+      c.total_q = total_q;
+      c.cu_q = cu_seqlens_q;
+      c.batch = batch;
+      c.Hq = num_heads;
+      c.G = p.G;
+      c.D = head_size;
+      c.splits = used;
+      c.sinks = p.sinks;
+      c.min_rows = kDecodeRows + 1;
+      c.max_rows = 0x7fffffff;
+      e = launch_prefill_split_combine(c, max_seqlen_q, bf16, s);
+      if (e != cudaSuccess) return cuda_fail(e, "prefill split combine");
+    }
   }
   return PKV_OK;
 }

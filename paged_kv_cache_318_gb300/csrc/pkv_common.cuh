@@ -230,6 +230,12 @@ struct AttnParams {
   // persistent prefill: one int of workspace the kernel hands work items
   // out through (the launcher zeroes it first); null = fixed item order
   int* sched;
+  // persistent prefill split-KV: key splits per work item (1 = none); with
+  // more, partials go to pre_o [S, total_q, Hq, D] / pre_lse [S, Hq,
+  // total_q] and launch_prefill_split_combine folds them
+  int pre_splits;
+  float* pre_o;
+  float* pre_lse;
   unsigned* err;
 };
 
@@ -306,9 +312,16 @@ cudaError_t launch_decode_attn(const AttnParams& p, int D, bool bf16,
                                int grid_x, int grid_y, cudaStream_t stream);
 cudaError_t launch_prefill_attn_mma(const AttnParams& p, int D, bool bf16,
                                     int grid_y, cudaStream_t stream);
+// *splits_used: the key splits the launch wrote partials for (1 = the
+// outputs themselves were written).
 cudaError_t launch_prefill_attn_tc(const AttnParams& p, int D, bool bf16,
                                    int grid_y, bool p_in_tmem,
-                                   cudaStream_t stream);
+                                   int* splits_used, cudaStream_t stream);
+// Fold the prefill kernel's split-KV partials (p.splits of them, every one
+// written for each row) of the requests with rows >= p.min_rows.
+cudaError_t launch_prefill_split_combine(const CombineParams& p,
+                                         int max_seqlen_q, bool bf16,
+                                         cudaStream_t stream);
 int prefill_tc_block_keys(int D);
 // Decode attention with TMA page loads (decode_tma.cu); 16-bit caches.
 cudaError_t launch_decode_attn_tma(const AttnParams& p, int D, bool bf16,
@@ -316,6 +329,13 @@ cudaError_t launch_decode_attn_tma(const AttnParams& p, int D, bool bf16,
 
 cudaError_t launch_split_combine(const CombineParams& p, bool bf16,
                                  cudaStream_t stream);
+// Required workspace bytes of an attention call (pkv_api.cu): the split-KV
+// partials and fp8 copies it needs, not the optional prefill tail.
+size_t required_workspace_bytes(int batch, int total_q, int max_seqlen_q,
+                                int max_seqlen_k, int num_heads,
+                                int num_kv_heads, int head_size,
+                                int block_size, int causal, int window_left,
+                                int window_right, int num_splits);
 cudaError_t launch_merge(void* out, const void* o1, const float* l1,
                          const void* o2, const float* l2, float* lse_out,
                          int T, int H, int D, pkv_dtype out_dt,

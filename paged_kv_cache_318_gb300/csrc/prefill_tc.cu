@@ -117,6 +117,11 @@ struct TcParams {
   int kv_order_hnd;   // tensor-map dim order: 1 = (D, BS, Hkv, NB)
   int* sched;             // persistent kernel: zeroed item counter, or null
   int q_tma;              // persistent kernel: Q tiles arrive as TMA boxes
+  // persistent kernel split-KV: every pair tile's key tiles cut into
+  // n_split ranges, one work item each; partials to pre_o / pre_lse
+  int n_split;
+  float* pre_o;           // [n_split, total_q, Hq, D] fp32, rows O / l
+  float* pre_lse;         // [n_split, Hq, total_q] fp32, natural log
   unsigned* err;
 };
 
@@ -1452,7 +1457,7 @@ struct PtItem {
   int rx0[2], rx_end[2], kmn[2], kmx[2], tlo[2], nx[2];
   int has[2];
   int kstart, kmax_u, n_tiles;
-  int unused;                    // pads the struct to 7 x 16 bytes
+  int split;                     // key split of a split-KV launch, else 0
 };
 static_assert(sizeof(PtItem) == 112, "PtItem is copied as 7 x 16 bytes");
 
@@ -1923,8 +1928,37 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
     int q_issued = 0;                            // Q loads as TMA boxes
     for (int n = 0;; ++n) {
       PtItem it;
-      const bool real = item >= 0 && pt_item(p, item, lane, BN, md, it);
+      const int pair = p.n_split > 1 ? item / p.n_split : item;
+      const bool real = item >= 0 && pt_item(p, pair, lane, BN, md, it);
       it.item = real ? item : -1;
+      it.split = 0;
+      if (real && p.n_split > 1) {
+        // split s: key tiles [j0, j1) of the pair's union range; each Q
+        // tile keeps its own range clipped to them
+        const int s = item - pair * p.n_split;
+        const int per = (it.n_tiles + p.n_split - 1) / p.n_split;
+        const int j0 = min(s * per, it.n_tiles);
+        const int j1 = min(j0 + per, it.n_tiles);
+        const int k0 = it.kstart + j0 * BN, k1 = it.kstart + j1 * BN;
+#pragma unroll
+        for (int xs = 0; xs < 2; ++xs) {
+          const int lo = max(it.tlo[xs], j0);
+          const int hi = min(it.tlo[xs] + it.nx[xs], j1);
+          if (hi > lo) {
+            it.tlo[xs] = lo - j0;
+            it.nx[xs] = hi - lo;
+            it.kmn[xs] = max(it.kmn[xs], k0);
+            it.kmx[xs] = min(it.kmx[xs], k1);
+          } else {
+            it.tlo[xs] = 0;
+            it.nx[xs] = 0;
+          }
+        }
+        it.kstart = k0;
+        it.kmax_u = min(it.kmax_u, k1);
+        it.n_tiles = j1 - j0;
+        it.split = s;
+      }
       if (!publish(n, it) || !real) break;
       // the previous item's S MMAs are done with Q
       if (n >= 1 && !mbar_wait(q_empty, (n - 1) & 1, abort_flag, p.err))
@@ -2194,7 +2228,47 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
       tc_fence_after();
       T* dst = OUT + static_cast<int64_t>(tok) * p.o_st +
                static_cast<int64_t>(h) * p.o_sh;
-      if (my_nx == 0) {
+      if (p.n_split > 1) {
+        // split-KV partial of this row: O / l in fp32 and its LSE (the sink
+        // joins once, in the combine); no key in the split: 0 and -inf
+        float* po = p.pre_o + ((static_cast<int64_t>(it.split) * p.total_q +
+                                tok) * p.Hq + h) * D;
+        float* pl = p.pre_lse +
+                    (static_cast<int64_t>(it.split) * p.Hq + h) * p.total_q +
+                    tok;
+        if (my_nx == 0) {
+          tc_fence_before();
+          mbar_arrive(o_free(x));
+          if (valid) {
+            const uint32_t z[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int e = 0; e < D; e += 8) st_global_v8(po + e, z);
+            *pl = -INFINITY;
+          }
+        } else {
+          float inv, lse_v;
+          finish_row(m_ref, l, nullptr, h, &inv, &lse_v);
+          inv *= vscale;
+          float ov[D];
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c)
+            tmem_ld32(o_addr + c * 32, ov + c * 32);
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(o_free(x));
+          if (valid) {
+#pragma unroll
+            for (int e = 0; e < D; e += 8) {
+              uint32_t w[8];
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                w[q] = __float_as_uint(ov[e + q] * inv);
+              st_global_v8(po + e, w);
+            }
+            *pl = lse_v;
+          }
+        }
+      } else if (my_nx == 0) {
         // no admissible key for this tile's rows: out = 0, lse = -inf
         tc_fence_before();
         mbar_arrive(o_free(x));
@@ -2257,6 +2331,70 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
         "r"(C::TMEM_COLS)
         : "memory");
   }
+}
+
+// Fold the split-KV partials of prefill-class requests.  One warp per
+// (token, query head) row, its lanes across D: M = the largest partial LSE
+// (and the sink logit), w_s = e^(lse_s - M), out = sum w_s o_s / sum w_s,
+// lse = M + ln sum w_s.  Grid: (rows / 8, 1, request).
+template <typename T>
+__global__ void __launch_bounds__(256)
+prefill_split_combine_kernel(const CombineParams p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.z;
+  const int q0 = p.cu_q[b];
+  const int q_len = min(p.cu_q[b + 1] - q0, p.total_q - q0);
+  if (q0 < 0 || q_len <= 0 || q_len * p.G < p.min_rows) return;
+  const int row = blockIdx.x * 8 + warp;
+  if (row >= q_len * p.Hq) return;
+  const int tok = q0 + row / p.Hq, h = row - (row / p.Hq) * p.Hq;
+  const int S = p.splits, D = p.D;
+  float M = -INFINITY;
+  for (int s = 0; s < S; ++s)
+    M = fmaxf(M, p.part_lse[(static_cast<int64_t>(s) * p.Hq + h) *
+                                p.total_q + tok]);
+  const float sink = p.sinks ? p.sinks[h] : -INFINITY;
+  M = fmaxf(M, sink);
+  const float base = (M == -INFINITY) ? 0.f : M;
+  float lsum = p.sinks ? __expf(sink - base) : 0.f;
+  float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f),
+                   make_float4(0.f, 0.f, 0.f, 0.f)};
+  for (int s = 0; s < S; ++s) {
+    const float l = p.part_lse[(static_cast<int64_t>(s) * p.Hq + h) *
+                                   p.total_q + tok];
+    const float w = (l == -INFINITY) ? 0.f : __expf(l - base);
+    lsum += w;
+    if (w == 0.f) continue;
+    const float* src =
+        p.part_o + ((static_cast<int64_t>(s) * p.total_q + tok) * p.Hq + h) * D;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int c = lane * 4 + k * 128;
+      if (c < D) {
+        const float4 v = *reinterpret_cast<const float4*>(src + c);
+        acc[k].x += w * v.x;
+        acc[k].y += w * v.y;
+        acc[k].z += w * v.z;
+        acc[k].w += w * v.w;
+      }
+    }
+  }
+  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+  T* dst = static_cast<T*>(p.out) + static_cast<int64_t>(tok) * p.o_st +
+           static_cast<int64_t>(h) * p.o_sh;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int c = lane * 4 + k * 128;
+    if (c < D) {
+      uint2 pk;
+      pk.x = pack2<T>(acc[k].x * inv, acc[k].y * inv);
+      pk.y = pack2<T>(acc[k].z * inv, acc[k].w * inv);
+      *reinterpret_cast<uint2*>(dst + c) = pk;
+    }
+  }
+  if (p.lse && lane == 0)
+    p.lse[static_cast<int64_t>(h) * p.total_q + tok] =
+        lsum > 0.f ? base + __logf(lsum) : -INFINITY;
 }
 
 // ------------------------------------------------------------ host side
@@ -2356,10 +2494,29 @@ static cudaError_t smem_opt_in(const void* kern, int smem) {
   return cudaSuccess;
 }
 
+cudaError_t launch_prefill_split_combine(const CombineParams& p,
+                                         int max_seqlen_q, bool bf16,
+                                         cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(max_seqlen_q) * p.Hq;
+  if (p.batch <= 0 || rows <= 0) return cudaSuccess;
+  if ((rows + 7) / 8 > 0x7fffffff || p.batch > 65535 || p.D > 256)
+    return cudaErrorInvalidValue;
+  dim3 grid(static_cast<unsigned>((rows + 7) / 8), 1,
+            static_cast<unsigned>(p.batch));
+  note_launch();
+  if (bf16)
+    tc::prefill_split_combine_kernel<__nv_bfloat16>
+        <<<grid, 256, 0, stream>>>(p);
+  else
+    tc::prefill_split_combine_kernel<__half><<<grid, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_prefill_attn_tc(const AttnParams& a, int D, bool bf16,
                                    int grid_y, bool p_in_tmem,
-                                   cudaStream_t stream) {
+                                   int* splits_used, cudaStream_t stream) {
   using namespace tc;
+  if (splits_used) *splits_used = 1;
   TcParams p{};
   p.q = a.q;
   p.q_st = a.q_st;
@@ -2422,6 +2579,7 @@ cudaError_t launch_prefill_attn_tc(const AttnParams& a, int D, bool bf16,
   if (gx <= 0 || gx > 0x7fffffff) return cudaErrorInvalidValue;
   dim3 grid(static_cast<unsigned>(gx));
   p.n_items = static_cast<int>(gx);
+  p.n_split = 1;
   auto go = [&](void (*kern)(TcParams, CUtensorMap, CUtensorMap), int smem,
                 int threads) -> cudaError_t {
     cudaError_t e = smem_opt_in(reinterpret_cast<const void*>(kern), smem);
@@ -2456,7 +2614,20 @@ cudaError_t launch_prefill_attn_tc(const AttnParams& a, int D, bool bf16,
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
             cudaSuccess || sms <= 0)
       sms = 1;
-    if (static_cast<int64_t>(sms) < gx) {
+    // split-KV: each pair tile's keys in a.pre_splits ranges, one item
+    // each, when the caller planned it (few items for the SMs)
+    int64_t items = gx;
+    if (a.pre_splits > 1 && a.pre_o && a.pre_lse &&
+        gx * a.pre_splits <= 0x7fffffff) {
+      p.n_split = a.pre_splits;
+      p.pre_o = a.pre_o;
+      p.pre_lse = a.pre_lse;
+      items = gx * a.pre_splits;
+      p.n_items = static_cast<int>(items);
+      if (splits_used) *splits_used = a.pre_splits;
+    }
+    grid = dim3(static_cast<unsigned>(items));
+    if (static_cast<int64_t>(sms) < items) {
       grid = dim3(static_cast<unsigned>(sms));
       // items dealt at run time when the caller's workspace holds a counter
       if (a.sched) {

@@ -67,12 +67,14 @@ pkv_status pkv_paged_attention_varlen_static_scratch(
     int window_left, int window_right, float softcap,
     const float* alibi_slopes, int num_splits, float* softmax_lse,
     pkv_dtype dtype, pkv_stream_t stream) {
-  const size_t need = pkv_paged_attention_workspace_size(
+  // the scratch must hold what the call requires; the optional prefill
+  // tail (item counter, split partials) is used when it fits as well
+  const size_t need = pkv::required_workspace_bytes(
       batch, total_q, max_seqlen_q, max_seqlen_k, num_heads, num_kv_heads,
       head_size, block_size, causal, window_left, window_right, num_splits);
   void* scratch = nullptr;
   size_t scratch_bytes = 0;
-  if (need != static_cast<size_t>(-1) && need > 0) {
+  if (need != static_cast<size_t>(-1)) {
     if (need > pkv::kStaticScratchBytes) {
       char msg[256];
       snprintf(msg, sizeof(msg),

@@ -10,7 +10,7 @@ import numpy as np
 import pytest
 import torch
 
-from oracle import merge_attn_states_ref, paged_attention_ref
+from oracle import add_sink_ref, merge_attn_states_ref, paged_attention_ref
 from oracle.harness import (full_cache_bits, full_reference,
                             request_reference)
 from paged_kv_cache_318_gb300 import api, workloads
@@ -514,3 +514,89 @@ def test_prefill_item_order_leaves_bits_unchanged(cuda_device, name):
         ref_o, ref_l = request_reference(wl, r, last_rows=k)
         assert_close(wl, o[t1 - k:t1], lse[:, t1 - k:t1], ref_o, ref_l,
                      "%s req %d" % (name, r))
+
+
+def _a256(x):
+    return (x + 255) // 256 * 256
+
+
+def _prefill_splits(wl, sms):
+    """The key splits the library plans for the persistent prefill kernel
+    (restated from its rule: an upper bound of the work items must leave half
+    the SMs idle; one wave; >= 4 key tiles of 128 per split; <= 16)."""
+    G = wl.num_heads // wl.num_kv_heads
+    items = (-(-wl.num_tokens * G // 256) + wl.batch) * wl.num_kv_heads
+    if wl.head_size > 128 or items * 2 > sms:
+        return 1
+    s = min(sms // items, int(wl.max_seqlen_k) // 512, 16)
+    return s if s >= 2 else 1
+
+
+SPLIT_CASES = [
+    # q_lens, seq_lens, Hq, Hkv, D, BS, kwargs
+    ([300], [6000], 32, 8, 128, 16, dict()),                    # causal
+    ([200, 40], [3000, 2500], 16, 4, 128, 32, dict(causal=False)),
+    ([130, 17, 64], [4100, 1000, 64], 8, 2, 64, 16,
+     dict(window_size=(700, 0))),                               # empty splits
+    ([256], [8192], 64, 8, 128, 64, dict(causal=False)),        # cascade prefix
+    ([100, 70], [3000, 900], 32, 8, 128, 16, dict(softcap=30.0, dtype="f16")),
+]
+
+
+@pytest.mark.parametrize("idx", range(len(SPLIT_CASES)))
+def test_prefill_split_kv(cuda_device, idx):
+    """Calls with few prefill work items split each item's keys across
+    more SMs and fold the partials by LSE.  Split and unsplit runs (the
+    workspace without the split partials) both match the oracle."""
+    q_lens, seq_lens, Hq, Hkv, D, BS, kw = SPLIT_CASES[idx]
+    wl = workloads.build_workload("split%d" % idx, 950 + idx, q_lens,
+                                  seq_lens, Hq, Hkv, D, BS, **kw)
+    sms = torch.cuda.get_device_properties(cuda_device).multi_processor_count
+    S = _prefill_splits(wl, sms)
+    assert S >= 2, "case %d does not exercise the split path" % idx
+    ref_out, ref_lse = full_reference(wl)
+    b = DeviceBatch(wl, cuda_device)
+    b.write_context()
+    b.write_new()
+    full = b.workspace
+    T = wl.num_tokens
+    split_bytes = _a256(S * T * Hq * D * 4) + _a256(S * Hq * T * 4)
+    assert full.numel() >= split_bytes + 256
+    for ws in (full, full[:full.numel() - split_bytes]):
+        b.workspace = ws
+        out, lse = b.attend()
+        torch.cuda.synchronize()
+        api.check_device_errors(cuda_device)
+        assert_close(wl, out.float().cpu().numpy(), lse.cpu().numpy(),
+                     ref_out, ref_lse,
+                     "split case %d ws %d" % (idx, ws.numel()))
+    b.workspace = full
+
+
+def test_prefill_split_kv_with_sinks(cuda_device):
+    wl = workloads.build_workload("split_sink", 960, [120, 3], [5000, 900],
+                                  16, 4, 128, 16)
+    sms = torch.cuda.get_device_properties(cuda_device).multi_processor_count
+    assert _prefill_splits(wl, sms) >= 2
+    rng = np.random.default_rng(961)
+    sinks = torch.from_numpy(rng.uniform(-1, 3, 16).astype(np.float32))
+    b = DeviceBatch(wl, cuda_device)
+    b.write_context()
+    b.write_new()
+    out, lse = api.flash_attn_varlen_func(
+        b.q, b.key_cache, b.value_cache, wl.max_seqlen_q, b.cu_seqlens_q,
+        wl.max_seqlen_k, seqused_k=b.seqused_k,
+        softmax_scale=wl.softmax_scale, causal=True,
+        block_table=b.block_table, return_softmax_lse=True,
+        s_aux=sinks.to(cuda_device))
+    torch.cuda.synchronize()
+    api.check_device_errors(cuda_device)
+    for r in range(wl.batch):
+        t1 = int(wl.cu_seqlens_q[r + 1])
+        k = min(16, t1 - int(wl.cu_seqlens_q[r]))
+        ro, rl = request_reference(wl, r, last_rows=k)
+        # the sink is one more logit of the softmax denominator
+        ro, rl = add_sink_ref(ro, rl, sinks.double().numpy())
+        assert_close(wl, out[t1 - k:t1].float().cpu().numpy(),
+                     lse[:, t1 - k:t1].cpu().numpy(), ro, rl,
+                     "sinks req %d" % r)
