@@ -266,40 +266,86 @@ def gpu_arm(args, rank, world, dev):
     api.check_device_errors(dev)
 
     # e2e: same step through the public API from pinned host memory.  The
-    # step's inputs live in one pinned host buffer and one device buffer
-    # (256-byte aligned segments; the batch's tensors become views of the
-    # device one), so each step is one host->device copy, the step, and one
-    # device->host copy of the output.
+    # step's inputs live in one pinned host buffer; each step copies them
+    # into one of two device buffers (256-byte aligned segments; the
+    # batch's tensors become views of it), runs the step, and copies the
+    # output back into one of two pinned host buffers.  The copies run on a
+    # second stream, one step ahead (inputs) and one step behind (output),
+    # as a serving loop overlaps them; every copy of every timed step is
+    # inside the timed region.
     names = ("q", "k_new", "v_new", "slots_new", "block_table", "seqused_k",
              "cu_seqlens_q")
+    ref_out = batch.out.clone()        # the step's output, device-resident
     segs, total = [], 0
     for k in names:
         t = getattr(batch, k)
         nb = t.numel() * t.element_size()
         segs.append((k, total, nb))
         total = (total + nb + 255) // 256 * 256
-    dev_in = torch.empty(total, dtype=torch.uint8, device=dev)
     host_in = torch.empty(total, dtype=torch.uint8, pin_memory=True)
     for k, off, nb in segs:
         t = getattr(batch, k)
-        view = dev_in[off:off + nb].view(t.dtype).view(t.shape)
-        view.copy_(t)
         host_in[off:off + nb].copy_(t.contiguous().view(-1).view(torch.uint8)
                                     .cpu())
-        setattr(batch, k, view)
-    out_host = torch.empty(batch.out.shape, dtype=batch.out.dtype,
-                           pin_memory=True)
+    slots = []
+    for _ in range(2):
+        dev_in = torch.empty(total, dtype=torch.uint8, device=dev)
+        views = {k: dev_in[off:off + nb].view(getattr(batch, k).dtype)
+                 .view(getattr(batch, k).shape) for k, off, nb in segs}
+        out_host = torch.empty(batch.out.shape, dtype=batch.out.dtype,
+                               pin_memory=True)
+        slots.append({"dev_in": dev_in, "views": views,
+                      "out": torch.empty_like(batch.out), "out_host": out_host,
+                      "h2d": torch.cuda.Event(), "done": torch.cuda.Event(),
+                      "d2h": torch.cuda.Event()})
+    copy_stream = torch.cuda.Stream(dev)
     h2d = sum(nb for _, _, nb in segs)
-    d2h = out_host.numel() * out_host.element_size()
+    d2h = slots[0]["out_host"].numel() * slots[0]["out_host"].element_size()
 
-    def e2e_step(i):
-        dev_in.copy_(host_in, non_blocking=True)
-        batch.step()
-        out_host.copy_(batch.out, non_blocking=True)
+    def h2d_copy(sl):
+        # the buffer's previous step must be done with it
+        copy_stream.wait_event(sl["done"])
+        with torch.cuda.stream(copy_stream):
+            sl["dev_in"].copy_(host_in, non_blocking=True)
+        sl["h2d"].record(copy_stream)
 
-    for i in range(args.warmup):
-        e2e_step(i)
-    e2e_ms = time_steps(e2e_step, args.steps, stream)
+    def e2e_run(steps):
+        """steps e2e steps; returns device ms from the first copy to the
+        last output copy."""
+        if steps <= 0:
+            return 0.0
+        start = torch.cuda.Event(enable_timing=True)
+        stop = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        start.record(stream)
+        copy_stream.wait_event(start)
+        h2d_copy(slots[0])
+        for i in range(steps):
+            sl = slots[i % 2]
+            if i + 1 < steps:
+                h2d_copy(slots[(i + 1) % 2])        # next step's inputs
+            stream.wait_event(sl["h2d"])
+            for k, v in sl["views"].items():
+                setattr(batch, k, v)
+            batch.out = sl["out"]
+            batch.step()
+            sl["done"].record(stream)
+            copy_stream.wait_event(sl["done"])
+            with torch.cuda.stream(copy_stream):
+                sl["out_host"].copy_(sl["out"], non_blocking=True)
+            sl["d2h"].record(copy_stream)
+        for sl in slots:
+            stream.wait_event(sl["d2h"])        # the last output copies
+        stop.record(stream)
+        torch.cuda.synchronize()
+        return start.elapsed_time(stop)
+
+    e2e_run(args.warmup)
+    e2e_ms = e2e_run(args.steps)
+    # the same inputs every step: the copied-back output must equal it
+    if not torch.equal(slots[(args.steps - 1) % 2]["out_host"],
+                       ref_out.cpu()):
+        raise RuntimeError("e2e output differs from the device step's")
 
     # secondary: varlen causal prefill with prefix cache (TFLOP/s)
     pre = workloads.prefill_with_prefix(seed=SEED_PREFILL, device=dev)
