@@ -246,12 +246,15 @@ def gpu_arm(args, rank, world, dev):
     if world > 1:
         torch.distributed.barrier()
     launches0 = api.launch_count()
-    timing["on"] = True
     ms = time_steps(step, args.steps, stream)
-    timing["on"] = False
     launches = api.launch_count() - launches0
     if world > 1:
         torch.distributed.barrier()
+    # the attention call's own time: the same steps again, with events
+    # around each call (kept out of the step timing above)
+    timing["on"] = True
+    time_steps(step, args.steps, stream)
+    timing["on"] = False
     attn_ms = float(np.mean([a.elapsed_time(b) for a, b in zip(ev_a, ev_b)]))
     # the timed region is shorter than the sampling interval: keep the same
     # step running for CLOCK_SOAK_S more so the samples see this load

@@ -477,7 +477,8 @@ attn_mma_kernel(const AttnParams p) {
         if (p.lse && c4 == 0) p.lse[static_cast<int64_t>(h) * p.total_q + tok] = lse;
       } else {
         float* dst = p.part_o +
-                     ((static_cast<int64_t>(blockIdx.x) * p.total_q + tok) *
+                     ((static_cast<int64_t>(blockIdx.x) * p.part_rows +
+                       part_row(p.part_tpr, b, q0, tok)) *
                           p.Hq + h) * D;
 #pragma unroll
         for (int dn = 0; dn < D / 8; ++dn)
@@ -485,7 +486,8 @@ attn_mma_kernel(const AttnParams p) {
               make_float2(o[dn][2 * half] * inv, o[dn][2 * half + 1] * inv);
         if (c4 == 0)
           p.part_lse[(static_cast<int64_t>(blockIdx.x) * p.Hq + h) *
-                         p.total_q + tok] = lse;
+                         p.part_rows +
+                     part_row(p.part_tpr, b, q0, tok)] = lse;
       }
     }
   } else {
@@ -543,13 +545,15 @@ attn_mma_kernel(const AttnParams p) {
         if (p.lse && c == 0) p.lse[static_cast<int64_t>(h) * p.total_q + tok] = lse;
       } else {
         float* dst = p.part_o +
-                     ((static_cast<int64_t>(blockIdx.x) * p.total_q + tok) *
+                     ((static_cast<int64_t>(blockIdx.x) * p.part_rows +
+                       part_row(p.part_tpr, b, q0, tok)) *
                           p.Hq + h) * D + c;
         *reinterpret_cast<float4*>(dst) =
             make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
         if (c == 0)
           p.part_lse[(static_cast<int64_t>(blockIdx.x) * p.Hq + h) *
-                         p.total_q + tok] = lse;
+                         p.part_rows +
+                     part_row(p.part_tpr, b, q0, tok)] = lse;
       }
     }
   }
@@ -577,10 +581,11 @@ split_combine_kernel(const CombineParams p) {
   T* __restrict__ OUT = static_cast<T*>(p.out);
   for (int i = 0; i < q_len; ++i) {
     const int tok = q0 + i;
+    const int64_t prow = part_row(p.part_tpr, b, q0, tok);
     float M = -INFINITY;
     for (int s = lane; s < nsplit; s += 32)
       M = fmaxf(M, p.part_lse[(static_cast<int64_t>(s) * p.Hq + h) *
-                                  p.total_q + tok]);
+                                  p.part_rows + prow]);
 #pragma unroll
     for (int o = 16; o; o >>= 1)
       M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
@@ -595,13 +600,14 @@ split_combine_kernel(const CombineParams p) {
       float ls = w_sink;
       for (int s = 0; s < nsplit; ++s) {
         const float l = p.part_lse[(static_cast<int64_t>(s) * p.Hq + h) *
-                                       p.total_q + tok];
+                                       p.part_rows + prow];
         const float w = (l == -INFINITY) ? 0.f : __expf(l - base);
         ls += w;
         if (w != 0.f) {
           const float4 v = *reinterpret_cast<const float4*>(
-              p.part_o + ((static_cast<int64_t>(s) * p.total_q + tok) * p.Hq +
-                          h) * D + c);
+              p.part_o +
+              ((static_cast<int64_t>(s) * p.part_rows + prow) * p.Hq + h) * D +
+              c);
           acc.x += w * v.x;
           acc.y += w * v.y;
           acc.z += w * v.z;

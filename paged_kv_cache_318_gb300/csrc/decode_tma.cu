@@ -483,13 +483,15 @@ decode_tma_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
         p.lse[static_cast<int64_t>(h) * p.total_q + tok] = lse;
     } else {
       float* dst = p.part_o +
-                   ((static_cast<int64_t>(blockIdx.x) * p.total_q + tok) *
+                   ((static_cast<int64_t>(blockIdx.x) * p.part_rows +
+                       part_row(p.part_tpr, b, q0, tok)) *
                         p.Hq + h) * D + c;
       *reinterpret_cast<float4*>(dst) =
           make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
       if (c == 0)
         p.part_lse[(static_cast<int64_t>(blockIdx.x) * p.Hq + h) *
-                       p.total_q + tok] = lse;
+                       p.part_rows +
+                   part_row(p.part_tpr, b, q0, tok)] = lse;
     }
   }
 }

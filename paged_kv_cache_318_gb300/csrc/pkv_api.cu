@@ -85,6 +85,8 @@ struct Plan {
   int splits = 1;         // decode grid.x
   int chunk = 0;          // keys per split; 0 = write outputs directly
   int prefill_tiles = 0;  // prefill grid.y
+  // decode partial rows: per token (tpr 0) or tpr rows per request
+  int part_tpr = 0, part_rows = 0;
   size_t part_o_bytes = 0, part_lse_bytes = 0;
   size_t workspace = 0;
 };
@@ -153,10 +155,16 @@ Plan make_plan(int batch, int total_q, int max_q, int max_k, int Hq, int Hkv,
     }
   }
   if (pl.chunk > 0) {
-    pl.part_o_bytes = align256(static_cast<size_t>(pl.splits) * total_q * Hq *
-                               D * sizeof(float));
+    // only decode-class requests (at most kDecodeRows / G tokens each)
+    // write partials: rows per request when that is fewer than total_q
+    const int tpr = kDecodeRows / G > 0 ? kDecodeRows / G : 1;
+    const int64_t compact = static_cast<int64_t>(batch) * tpr;
+    pl.part_tpr = compact < total_q ? tpr : 0;
+    pl.part_rows = compact < total_q ? static_cast<int>(compact) : total_q;
+    pl.part_o_bytes = align256(static_cast<size_t>(pl.splits) * pl.part_rows *
+                               Hq * D * sizeof(float));
     pl.part_lse_bytes = align256(static_cast<size_t>(pl.splits) * Hq *
-                                 total_q * sizeof(float));
+                                 pl.part_rows * sizeof(float));
     pl.workspace = pl.part_o_bytes + pl.part_lse_bytes;
   }
   return pl;
@@ -629,6 +637,8 @@ pkv_status pkv_paged_attention_varlen_opts(
     d.min_rows = 1;
     d.max_rows = kDecodeRows;
     d.chunk = pl.chunk;
+    d.part_tpr = pl.part_tpr;
+    d.part_rows = pl.part_rows;
     if (pl.chunk > 0) {
       d.part_o = static_cast<float*>(workspace);
       d.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
@@ -643,6 +653,8 @@ pkv_status pkv_paged_attention_varlen_opts(
       CombineParams c{};
       c.part_o = d.part_o;
       c.part_lse = d.part_lse;
+      c.part_tpr = pl.part_tpr;
+      c.part_rows = pl.part_rows;
       c.out = out;
       c.o_st = o_stride_tok;
       c.o_sh = o_stride_head;
@@ -714,6 +726,8 @@ pkv_status pkv_paged_attention_varlen_opts(
       CombineParams c{};
       c.part_o = pre_o;
       c.part_lse = pre_lse;
+      c.part_tpr = 0;              // prefill partials: one row per token
+      c.part_rows = total_q;
       c.out = out;
       c.o_st = o_stride_tok;
       c.o_sh = o_stride_head;

@@ -225,8 +225,11 @@ struct AttnParams {
   int min_rows, max_rows;
   // split-KV: keys per split (0 = no split: write out/lse directly)
   int chunk;
-  float* part_o;              // [S, total_q, Hq, D] fp32
-  float* part_lse;            // [S, Hq, total_q] fp32 natural log
+  float* part_o;              // [S, part_rows, Hq, D] fp32
+  float* part_lse;            // [S, Hq, part_rows] fp32 natural log
+  // partial rows: a token's own index (part_tpr = 0, part_rows = total_q)
+  // or, compact, part_tpr rows per request (see part_row)
+  int part_tpr, part_rows;
   // persistent prefill: one int of workspace the kernel hands work items
   // out through (the launcher zeroes it first); null = fixed item order
   int* sched;
@@ -242,6 +245,7 @@ struct AttnParams {
 struct CombineParams {
   const float* part_o;
   const float* part_lse;
+  int part_tpr, part_rows;    // partial row layout (see AttnParams)
   void* out;
   int64_t o_st, o_sh;
   float* lse;
@@ -255,6 +259,17 @@ struct CombineParams {
   int min_rows, max_rows;
   const float* sinks;         // [Hq] sink logits or null (added once here)
 };
+
+// Row of token tok (request b, first token q0) in the split-KV partial
+// buffers: the token itself, or with part_tpr > 0 row (tok - q0) of request
+// b's block of part_tpr rows.  Only decode-class requests (at most 16 / G
+// tokens) write partials, so the compact form needs batch * 16 / G rows
+// instead of total_q.
+__device__ __forceinline__ int64_t part_row(int part_tpr, int b, int q0,
+                                            int tok) {
+  return part_tpr > 0 ? static_cast<int64_t>(b) * part_tpr + (tok - q0)
+                      : static_cast<int64_t>(tok);
+}
 
 // Final normalisation of one row: acc is relative to the running max m
 // (log2 units), l the running sum.  With a sink logit (natural units), it is

@@ -114,3 +114,37 @@ def test_static_scratch_rejects_oversized_plans(cuda_device, lib):
     st = _call_static(fn, b, out, None, 64, max_seqlen_k=1 << 21)
     assert st == api.PKV_ERR_WORKSPACE_TOO_SMALL
     assert b"built-in scratch" in lib.pkv_last_error()
+
+
+def test_static_scratch_prefill_uses_the_optional_tail(cuda_device, lib):
+    """Prefill-class calls: the required scratch is zero, and the optional
+    tail (the prefill item counter and, with few work items, its split-KV
+    partials) comes from the built-in array when it fits.  The results equal
+    the workspace entry point's bit for bit, with and without a split."""
+    fn = _entry(lib)
+    cases = [
+        # few items: the prefill kernel splits its keys
+        workloads.build_workload("ss_split", 970, [200], [6000], 32, 8, 128,
+                                 16, device=cuda_device),
+        # many items: no split, items dealt at run time
+        workloads.prefill_with_prefix(device=cuda_device),
+    ]
+    for wl in cases:
+        b = DeviceBatch(wl, cuda_device)
+        b.write_context()
+        b.write_new()
+        need = api.paged_attention_workspace_size(
+            wl.batch, wl.num_tokens, wl.max_seqlen_q, wl.max_seqlen_k,
+            wl.num_heads, wl.num_kv_heads, wl.head_size, wl.block_size,
+            wl.causal, wl.window_size, 0)
+        assert 256 <= need <= STATIC_SCRATCH_BYTES   # the tail fits
+        ref_out, ref_lse = b.attend()
+        ref_out, ref_lse = ref_out.clone(), ref_lse.clone()
+        out = torch.full_like(b.q, float("nan"))
+        lse = torch.full_like(ref_lse, float("nan"))
+        st = _call_static(fn, b, out, lse, 0)
+        assert st == 0, lib.pkv_last_error()
+        torch.cuda.synchronize()
+        api.check_device_errors(cuda_device)
+        assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+        assert torch.equal(lse.view(torch.int32), ref_lse.view(torch.int32))
