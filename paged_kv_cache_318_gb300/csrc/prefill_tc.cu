@@ -2334,9 +2334,12 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
 }
 
 // Fold the split-KV partials of prefill-class requests.  One warp per
-// (token, query head) row, its lanes across D: M = the largest partial LSE
-// (and the sink logit), w_s = e^(lse_s - M), out = sum w_s o_s / sum w_s,
-// lse = M + ln sum w_s.  Grid: (rows / 8, 1, request).
+// (token, query head) row, its lanes across D (D <= 128, S <= 16): M = the
+// largest partial LSE (and the sink logit), w_s = e^(lse_s - M), out =
+// sum w_s o_s / sum w_s, lse = M + ln sum w_s.  Every partial of the row is
+// loaded before any is used, so the row costs one memory round trip.
+// Grid: (rows / 8, 1, request).
+constexpr int kPreMaxSplits = 16;
 template <typename T>
 __global__ void __launch_bounds__(256)
 prefill_split_combine_kernel(const CombineParams p) {
@@ -2349,48 +2352,47 @@ prefill_split_combine_kernel(const CombineParams p) {
   if (row >= q_len * p.Hq) return;
   const int tok = q0 + row / p.Hq, h = row - (row / p.Hq) * p.Hq;
   const int S = p.splits, D = p.D;
+  const int c = lane * 4;
+  float l[kPreMaxSplits];
+  float4 v[kPreMaxSplits];
+#pragma unroll
+  for (int s = 0; s < kPreMaxSplits; ++s) {
+    l[s] = -INFINITY;
+    v[s] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (s < S) {
+      l[s] = p.part_lse[(static_cast<int64_t>(s) * p.Hq + h) * p.total_q +
+                        tok];
+      if (c < D)
+        v[s] = *reinterpret_cast<const float4*>(
+            p.part_o +
+            ((static_cast<int64_t>(s) * p.total_q + tok) * p.Hq + h) * D + c);
+    }
+  }
   float M = -INFINITY;
-  for (int s = 0; s < S; ++s)
-    M = fmaxf(M, p.part_lse[(static_cast<int64_t>(s) * p.Hq + h) *
-                                p.total_q + tok]);
+#pragma unroll
+  for (int s = 0; s < kPreMaxSplits; ++s) M = fmaxf(M, l[s]);
   const float sink = p.sinks ? p.sinks[h] : -INFINITY;
   M = fmaxf(M, sink);
   const float base = (M == -INFINITY) ? 0.f : M;
   float lsum = p.sinks ? __expf(sink - base) : 0.f;
-  float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f),
-                   make_float4(0.f, 0.f, 0.f, 0.f)};
-  for (int s = 0; s < S; ++s) {
-    const float l = p.part_lse[(static_cast<int64_t>(s) * p.Hq + h) *
-                                   p.total_q + tok];
-    const float w = (l == -INFINITY) ? 0.f : __expf(l - base);
-    lsum += w;
-    if (w == 0.f) continue;
-    const float* src =
-        p.part_o + ((static_cast<int64_t>(s) * p.total_q + tok) * p.Hq + h) * D;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int c = lane * 4 + k * 128;
-      if (c < D) {
-        const float4 v = *reinterpret_cast<const float4*>(src + c);
-        acc[k].x += w * v.x;
-        acc[k].y += w * v.y;
-        acc[k].z += w * v.z;
-        acc[k].w += w * v.w;
-      }
-    }
+  for (int s = 0; s < kPreMaxSplits; ++s) {
+    const float w = (l[s] == -INFINITY) ? 0.f : __expf(l[s] - base);
+    lsum += w;
+    acc.x += w * v[s].x;
+    acc.y += w * v[s].y;
+    acc.z += w * v[s].z;
+    acc.w += w * v[s].w;
   }
   const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-  T* dst = static_cast<T*>(p.out) + static_cast<int64_t>(tok) * p.o_st +
-           static_cast<int64_t>(h) * p.o_sh;
-#pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const int c = lane * 4 + k * 128;
-    if (c < D) {
-      uint2 pk;
-      pk.x = pack2<T>(acc[k].x * inv, acc[k].y * inv);
-      pk.y = pack2<T>(acc[k].z * inv, acc[k].w * inv);
-      *reinterpret_cast<uint2*>(dst + c) = pk;
-    }
+  if (c < D) {
+    T* dst = static_cast<T*>(p.out) + static_cast<int64_t>(tok) * p.o_st +
+             static_cast<int64_t>(h) * p.o_sh + c;
+    uint2 pk;
+    pk.x = pack2<T>(acc.x * inv, acc.y * inv);
+    pk.y = pack2<T>(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2*>(dst) = pk;
   }
   if (p.lse && lane == 0)
     p.lse[static_cast<int64_t>(h) * p.total_q + tok] =
@@ -2499,7 +2501,8 @@ cudaError_t launch_prefill_split_combine(const CombineParams& p,
                                          cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(max_seqlen_q) * p.Hq;
   if (p.batch <= 0 || rows <= 0) return cudaSuccess;
-  if ((rows + 7) / 8 > 0x7fffffff || p.batch > 65535 || p.D > 256)
+  if ((rows + 7) / 8 > 0x7fffffff || p.batch > 65535 || p.D > 128 ||
+      p.splits > tc::kPreMaxSplits)
     return cudaErrorInvalidValue;
   dim3 grid(static_cast<unsigned>((rows + 7) / 8), 1,
             static_cast<unsigned>(p.batch));
