@@ -180,10 +180,13 @@ constexpr size_t kSchedBytes = 256;
 // Key splits for the persistent prefill kernel (head size <= 128): only
 // when even an upper bound of its work items, (ceil(total_q * G / 256) +
 // batch) * Hkv, leaves half the SMs idle; as many as keep one wave, with
-// at least 4 key tiles of 128 per split, at most 16.
+// at least 4 key tiles of 128 per split, at most 16.  Never with
+// num_splits = 1 (no split asked for) or a fixed split size: the split
+// depends on the rest of the batch, and those modes promise each request
+// the same bits in any batch.
 int prefill_splits(int batch, int total_q, int G, int Hkv, int max_k, int D,
-                   int sms) {
-  if (D > 128) return 1;
+                   int sms, int num_splits, int fixed_split) {
+  if (D > 128 || num_splits == 1 || fixed_split > 0) return 1;
   const int64_t items =
       ((static_cast<int64_t>(total_q) * G + 255) / 256 + batch) * Hkv;
   if (items <= 0 || items * 2 > sms) return 1;
@@ -405,7 +408,8 @@ size_t pkv_paged_attention_workspace_size_opts(
   const bool fp8 = opts && opts->kv_cache_fp8;
   const size_t split_bytes = prefill_split_bytes(
       pl.prefill ? prefill_splits(batch, total_q, num_heads / num_kv_heads,
-                                  num_kv_heads, max_seqlen_k, head_size, sms)
+                                  num_kv_heads, max_seqlen_k, head_size, sms,
+                                  num_splits, fixed_split_of(opts))
                  : 1,
       total_q, num_heads, head_size);
   if (!fp8 || !pl.prefill)
@@ -434,7 +438,8 @@ size_t pkv_paged_attention_workspace_size(int batch, int total_q,
                             window_left, window_right, num_splits, sms);
   const size_t split_bytes = prefill_split_bytes(
       pl.prefill ? prefill_splits(batch, total_q, num_heads / num_kv_heads,
-                                  num_kv_heads, max_seqlen_k, head_size, sms)
+                                  num_kv_heads, max_seqlen_k, head_size, sms,
+                                  num_splits, 0)
                  : 1,
       total_q, num_heads, head_size);
   return with_tail(pl.workspace, pl.prefill, split_bytes);
@@ -562,7 +567,8 @@ pkv_status pkv_paged_attention_varlen_opts(
     if (workspace_bytes >= with_tail(need, true, 0))
       sched = reinterpret_cast<int*>(tail);
     const int sp = prefill_splits(batch, total_q, num_heads / num_kv_heads,
-                                  num_kv_heads, max_seqlen_k, head_size, sms);
+                                  num_kv_heads, max_seqlen_k, head_size, sms,
+                                  num_splits, fixed_split);
     const size_t sb = prefill_split_bytes(sp, total_q, num_heads, head_size);
     if (sp > 1 && workspace_bytes >= with_tail(need, true, sb)) {
       pre_splits = sp;

@@ -172,13 +172,31 @@ def _sub_batch_call(b, idx, **kw):
     return rows, out, lse
 
 
+def _mixed_d128(dtype):
+    """40 decodes (L ~ U[100, 9000]) then 3 chunks of 90 tokens (context
+    ~ U[0, 2000]), 32/8 heads, D 128: sub-batches that hold a chunk have few
+    prefill work items, where a free plan would split the chunk's keys."""
+    rng = np.random.default_rng([326, 2])
+    dec = rng.integers(100, 9001, 40)
+    ctx = rng.integers(0, 2001, 3)
+    q = [1] * 40 + [90] * 3
+    L = list(dec) + list(ctx + 90)
+    return workloads.build_workload("mixed_d128", 326, q, L, 32, 8, 128, 16,
+                                    dtype=dtype)
+
+
+@pytest.mark.parametrize("kind", ["gemma_d256", "llama_d128"])
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 @pytest.mark.parametrize("mode", [dict(fixed_split_size=2048),
                                   dict(fixed_split_size=100),
                                   dict(num_splits=1)])
-def test_fixed_splits_are_batch_invariant(cuda_device, mode, dtype):
-    wl = workloads.mixed_gemma(dtype=dtype, n_prefill=3, chunk=90, c_hi=2000,
-                               n_decode=40, d_lo=100, d_hi=9000)
+def test_fixed_splits_are_batch_invariant(cuda_device, mode, dtype, kind):
+    if kind == "gemma_d256":
+        wl = workloads.mixed_gemma(dtype=dtype, n_prefill=3, chunk=90,
+                                   c_hi=2000, n_decode=40, d_lo=100,
+                                   d_hi=9000)
+    else:
+        wl = _mixed_d128(dtype)
     wl.num_splits = 0
     b = DeviceBatch(wl, cuda_device)
     b.write_context()
