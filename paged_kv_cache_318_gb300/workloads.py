@@ -222,29 +222,31 @@ def tiny_decode(seed=318, dtype="bf16", device="cpu"):
 
 
 def batched_decode(seed=319, dtype="bf16", device="cpu", batch=64,
-                   lo=512, hi=4096, pool_blocks=20000):
+                   lo=512, hi=4096, pool_blocks=20000, values=True):
     """Llama-3-8B attention shape: 64 requests, query_len 1, 32/8 heads,
     D 128, BS 16, lengths U[512, 4096], 20k-block shuffled pool."""
     rng = np.random.default_rng([seed, 2])
     L = _draw_lengths(rng, lo, hi, batch)
     return build_workload("batched_decode", seed, np.ones(batch, np.int32), L,
                           32, 8, 128, 16, dtype=dtype,
-                          pool_blocks=pool_blocks, device=device)
+                          pool_blocks=pool_blocks, device=device,
+                          values=values)
 
 
 def prefill_with_prefix(seed=320, dtype="bf16", device="cpu", batch=8,
-                        q_lo=256, q_hi=2048, c_lo=0, c_hi=1024):
+                        q_lo=256, q_hi=2048, c_lo=0, c_hi=1024, values=True):
     """Varlen causal prefill: 8 sequences, new tokens U[256, 2048], cached
     prefix U[0, 1024], 32/8 heads, D 128, BS 16."""
     rng = np.random.default_rng([seed, 2])
     q = _draw_lengths(rng, q_lo, q_hi, batch)
     c = _draw_lengths(rng, c_lo, c_hi, batch)
     return build_workload("prefill_with_prefix", seed, q, q + c, 32, 8, 128,
-                          16, dtype=dtype, device=device)
+                          16, dtype=dtype, device=device, values=values)
 
 
 def mixed_gemma(seed=321, dtype="bf16", device="cpu", n_prefill=4,
-                chunk=512, c_hi=8192, n_decode=124, d_lo=1024, d_hi=16384):
+                chunk=512, c_hi=8192, n_decode=124, d_lo=1024, d_hi=16384,
+                values=True):
     """Chunked prefill + decode, Gemma-like: 4 chunks of 512 (context
     U[0, 8192]) after 124 decodes (context U[1024, 16384]); 16/8 heads,
     D 256, BS 32, window (4095, 0), soft-cap 50; decodes first."""
@@ -256,27 +258,29 @@ def mixed_gemma(seed=321, dtype="bf16", device="cpu", n_prefill=4,
     L = np.concatenate([dec_L, pre_c + chunk]).astype(np.int32)
     return build_workload("mixed_gemma", seed, q, L, 16, 8, 256, 32,
                           dtype=dtype, window_size=(4095, 0), softcap=50.0,
-                          device=device)
+                          device=device, values=values)
 
 
 def long_decode(seed=322, dtype="bf16", device="cpu", batch=8,
-                ctx=131072, num_splits=16):
+                ctx=131072, num_splits=16, values=True):
     """Long-context split-KV decode: 8 requests x 131072 keys, 64/8 heads,
     D 128, BS 64, 16 splits per request."""
     return build_workload("long_decode", seed, np.ones(batch, np.int32),
                           np.full(batch, ctx, np.int32), 64, 8, 128, 64,
-                          dtype=dtype, num_splits=num_splits, device=device)
+                          dtype=dtype, num_splits=num_splits, device=device,
+                          values=values)
 
 
 def cascade_decode(seed=323, dtype="bf16", device="cpu", batch=256,
-                   prefix=8192, unique=512):
+                   prefix=8192, unique=512, values=True):
     """Shared-prefix decode: 256 requests over one 8192-token prefix held in
     the same physical blocks, plus 512 own tokens each; 64/8 heads, D 128,
     BS 64."""
     L = np.full(batch, prefix + unique, np.int32)
     return build_workload("cascade_decode", seed, np.ones(batch, np.int32), L,
                           64, 8, 128, 64, dtype=dtype,
-                          shared_prefix_len=prefix, device=device)
+                          shared_prefix_len=prefix, device=device,
+                          values=values)
 
 
 WORKLOADS = {
