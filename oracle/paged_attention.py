@@ -24,7 +24,7 @@ cache scatter).  Sources, cited by page title and section:
   ``FlashAttentionMetadata`` block-table and seq_start_loc examples; the
   cache-free prefill call (``cu_seqlens_k = seq_start_loc``).
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
 
 * slot s addresses block ``s // block_size``, row ``s % block_size``; s < 0 is
   a padding slot and is skipped;
