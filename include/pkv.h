@@ -86,10 +86,15 @@ typedef enum { PKV_F16 = 0, PKV_BF16 = 1, PKV_F32 = 2 } pkv_dtype;
  *                   viewed as NHD gives (Hkv*BS*D, D, BS*D, 1).
  * slot_mapping    : int64 [num_tokens], device.
  * block_size      : multiple of 16 (else PKV_ERR_INVALID_ARG).
- * kv_cache_dtype  : "auto" (cache has the dtype of key/value).  "fp8",
- *                   "fp8_e4m3" and anything else return PKV_ERR_UNSUPPORTED.
- * k_scale, v_scale: device float scalars for an fp8 cache; ignored for "auto"
- *                   and may be NULL.
+ * kv_cache_dtype  : "auto" (the cache has the dtype of key/value), or "fp8"
+ *                   / "fp8_e4m3": the cache holds one-byte E4M3 ("fn")
+ *                   codes, code = e4m3(x / scale) rounded to nearest (ties
+ *                   to even) and saturated at +-448, with cache_strides in
+ *                   bytes (key/value rows 16-byte aligned, cache rows 8-byte
+ *                   aligned, else PKV_ERR_UNSUPPORTED).  Anything else
+ *                   returns PKV_ERR_UNSUPPORTED.
+ * k_scale, v_scale: device float scalars for an fp8 cache (required there);
+ *                   ignored for "auto" and may be NULL.
  * num_tokens == 0 is a no-op.
  */
 PKV_API pkv_status pkv_reshape_and_cache(
@@ -266,11 +271,12 @@ PKV_API pkv_status pkv_paged_attention_varlen_opts(
 
 /*
  * Bytes of workspace pkv_paged_attention_varlen needs for these arguments
- * (on the current device: the split plans depend on its SM count),
- * counting the optional tail of calls with prefill-class requests
- * (max_seqlen_q * num_heads / num_kv_heads > 16): the 256-byte item
- * counter and the prefill split-KV partials.  Returns 0 when no scratch is
- * needed, and (size_t)-1 for invalid arguments.
+ * (on the current device: the split plans and the persistent decode grid
+ * depend on its SM count), counting the optional tail: the persistent
+ * decode kernel's scratch (num_splits = 0), and for calls with
+ * prefill-class requests (max_seqlen_q * num_heads / num_kv_heads > 16)
+ * the 256-byte item counter and the prefill split-KV partials.  Returns 0
+ * when no scratch is needed, and (size_t)-1 for invalid arguments.
  */
 PKV_API size_t pkv_paged_attention_workspace_size(
     int batch, int total_q, int max_seqlen_q, int max_seqlen_k,
@@ -422,14 +428,26 @@ PKV_API pkv_status pkv_set_prefill_kernel(int which);
 
 /*
  * Which kernel serves decode-class requests (at most 16 packed query rows
- * per KV head) over a 16-bit cache: the kernel whose producer warp moves
- * K/V pages with TMA (the default) or the one whose threads gather them with
- * 16-byte cp.async.  fp8 caches always use the cp.async kernel.  A
- * process-wide diagnostic switch for A/B comparison; both give the same
+ * per KV head):
+ *   PKV_DECODE_PERSISTENT (default)  one wave of CTAs, each streaming an
+ *       equal share of the batch's key tiles (a request's keys may be cut
+ *       between CTAs; the pieces are merged by LSE).  Used for calls that
+ *       leave the split to the library (num_splits = 0, no fixed split
+ *       size) when the workspace holds its scratch (see
+ *       pkv_paged_attention_workspace_size); 16-bit caches with head_size
+ *       64/128/256 and fp8 caches with head_size 128/256.  Other calls fall
+ *       back to the kernels below.
+ *   PKV_DECODE_TMA  one CTA per (request, KV head, split), K/V pages moved
+ *       by a TMA producer warp (16-bit caches).
+ *   PKV_DECODE_CP_ASYNC  one CTA per (request, KV head, split), pages
+ *       gathered with 16-byte cp.async (always used for fp8 caches the
+ *       persistent kernel does not take).
+ * A process-wide diagnostic switch for A/B comparison; all give the same
  * result within rounding.  Returns PKV_ERR_INVALID_ARG for other values.
  */
 #define PKV_DECODE_TMA 0
 #define PKV_DECODE_CP_ASYNC 1
+#define PKV_DECODE_PERSISTENT 2
 PKV_API pkv_status pkv_set_decode_kernel(int which);
 
 /*

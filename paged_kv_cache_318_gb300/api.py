@@ -168,10 +168,12 @@ def set_prefill_kernel(which: int):
 
 DECODE_TMA = 0
 DECODE_CP_ASYNC = 1
+DECODE_PERSISTENT = 2
 
 
 def set_decode_kernel(which: int):
-    """Choose the 16-bit decode kernel (DECODE_TMA or DECODE_CP_ASYNC)."""
+    """Choose the decode kernel: DECODE_PERSISTENT (default), DECODE_TMA or
+    DECODE_CP_ASYNC."""
     _check(load_library().pkv_set_decode_kernel(int(which)))
 
 

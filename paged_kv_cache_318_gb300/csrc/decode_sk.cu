@@ -1,0 +1,1188 @@
+// Persistent decode attention: every CTA streams an equal share of the
+// batch's key tiles, for 16-bit and E4M3 (fp8) caches.
+//
+// Source: "vllm/v1/attention/backends/flash_attn.py", FlashAttentionImpl.
+// forward (flash_attn_varlen_func over the paged cache: cu_seqlens_q,
+// seqused_k, block_table, causal, window_size, softcap, alibi_slopes, LSE;
+// kv_cache_dtype "fp8" with k_descale / v_descale) and
+// FlashAttentionMetadataBuilder (split-KV decoding of requests with one
+// query per KV-head group; partial results combined by their LSEs).
+//
+// Work order.  The decode-class requests (q_len * G <= 16 packed query rows
+// per KV head) form a sequence of units u = b * Hkv + g (request b, KV head
+// g), each a run of KT-key tiles over the unit's admissible key range.  The
+// launch is one wave of C CTAs.  CTA c takes tiles [c N / C, (c+1) N / C)
+// of the concatenated sequence (N tiles in all), so every CTA moves the
+// same number of K/V bytes whatever the spread of the request lengths
+// (with one CTA per unit, the longest units of the last wave set the
+// kernel's time).  A unit inside one CTA's range is finished there.  A unit
+// that a range boundary cuts leaves one partial state (O normalised, LSE)
+// per piece in the workspace, and fold_kernel merges the pieces by LSE.
+//
+// CTA roles (NCW consumer warps + one producer warp):
+//   producer   walks the CTA's units in order.  For each it publishes a
+//              descriptor and cp.async-loads the unit's 16 packed query
+//              rows into one of two Q slots (unit_full barrier), then
+//              issues the unit's K and V page boxes with TMA into a
+//              STAGES-deep ring, as the decode_tma kernel does.  It runs
+//              ahead across unit boundaries, so the ring never drains
+//              between units.
+//   consumers  each own KT / NCW keys of every tile: S = Q K^T, online
+//              softmax (base 2), O += P V on mma.sync m16n8k16.  At the end
+//              of a unit warps 1.. NCW-1 hand their states to warp 0
+//              through shared memory and warp 0 writes the output (or the
+//              piece's partial state).
+//
+// E4M3 caches.  The ring holds the codes (one byte per element, 128-column
+// boxes).  The consumers convert them to f16 in registers with
+// cvt.rn.f16x2.e4m3x2 (exact): K straight from an ldmatrix of the code
+// bytes, V from 32-bit loads of four keys' code quads transposed with prmt.
+// The query rows are converted to f16 once per unit (a bf16 query is first
+// scaled by a power of two that puts its largest magnitude in [2^14, 2^15),
+// which keeps every value exact in f16; the factor joins the logit scale).
+// The MMAs then run in f16, with the same key order in S and P V and a
+// fixed permutation of the head dimension in S (the same for Q and K, so
+// the dot products are unchanged).  k_scale joins the logit scale and
+// v_scale multiplies the output.
+//
+// Every mbarrier wait is bounded (kWaitLimitNs).  A wait that runs out
+// records kErrTimeout and raises the CTA's abort flag; the consumers agree
+// on leaving at a barrier that reduces their flags (bar.red.or), and the
+// producer drains the copies it issued before it exits.
+#include <cuda.h>
+#include <math.h>
+
+#include <atomic>
+#include <type_traits>
+
+#include "pkv_common.cuh"
+#include "tma_util.cuh"
+
+namespace pkv {
+namespace dsk {
+
+constexpr int kMaxDevices = 64;
+
+template <int D, int NCW, int KT, int STAGES, bool KV8>
+struct Cfg {
+  static constexpr int NT = (NCW + 1) * 32;     // consumers + producer warp
+  static constexpr int CT = NCW * 32;           // consumer threads
+  static constexpr int KW = KT / NCW;           // keys per warp per tile
+  static constexpr int NKT = KW / 8;            // n8 tiles of S per warp
+  static constexpr int BOXC = KV8 ? 128 : 64;   // columns per TMA box
+  static constexpr int NCB = D / BOXC;          // 128-byte column blocks
+  static constexpr int CPR = D / 8;             // 16-byte chunks per Q row
+  static constexpr int ROW_BYTES = D * 2;       // one 16-bit Q row
+  static constexpr int CB_BYTES = KT * 128;     // one column block of a tile
+  static constexpr int TILE_BYTES = NCB * CB_BYTES;
+  static constexpr int RING_BYTES = STAGES * 2 * TILE_BYTES;
+  static constexpr int QRAW_BYTES = 16 * ROW_BYTES;
+  static constexpr int QFRAG_BYTES = KV8 ? (D / 16) * 32 * 16 : 0;
+  // combine rows: float4 stores (fp8) want a 16-byte row shift, float2
+  // stores (16-bit) a 32-byte one, for conflict-free shared stores
+  static constexpr int CST = D + (KV8 ? 4 : 8);
+  static constexpr int COMB_BYTES = (NCW - 1) * 16 * CST * 4;
+  static constexpr int ML_BYTES = (NCW - 1) * 16 * 2 * 4;
+  static constexpr int OFF_QRAW = RING_BYTES;
+  static constexpr int OFF_QFRAG = OFF_QRAW + 2 * QRAW_BYTES;
+  static constexpr int OFF_COMB = OFF_QFRAG + QFRAG_BYTES;
+  static constexpr int OFF_ML = OFF_COMB + COMB_BYTES;
+  static constexpr int OFF_DESC = OFF_ML + ML_BYTES;        // 2 x 64 bytes
+  static constexpr int OFF_MISC = OFF_DESC + 128;           // 256 bytes
+  static constexpr int OFF_BAR = OFF_MISC + 256;
+  static constexpr int BAR_BYTES = (3 * STAGES + 4) * 8;
+  static constexpr int SMEM = OFF_BAR + BAR_BYTES + 1024;   // + alignment
+  static_assert(KW % 16 == 0, "each warp needs whole k16 steps of keys");
+  static_assert(NKT == 2 || NKT == 4, "ldmatrix grouping of K");
+  static_assert(D % BOXC == 0, "whole TMA boxes per row");
+  static_assert(CB_BYTES % 1024 == 0, "128-byte swizzle atoms");
+  static_assert(NCW >= 2, "warp 0 merges the others' states");
+};
+
+// One unit piece as the producer hands it to the consumers (64 bytes).
+struct UnitDesc {
+  int b, g, q0, q_len;
+  int rows, L, lo, hi;
+  int kt0, t_beg, n_tiles, slot;   // slot: partial slot, or -1 (output)
+  int end, pad0, pad1, pad2;       // end: no more units
+};
+
+// What a request contributes: its tile count per unit (0: not a
+// decode-class request here) and its key geometry.
+struct ReqInfo {
+  int q0, q_len, rows, L, lo, hi, kt0, koff;
+  int n_real;   // tiles over [kt0, hi)
+  int n;        // tiles in the work sequence: max(n_real, 1), or 0
+};
+
+template <int KT>
+__device__ __forceinline__ ReqInfo req_info(const AttnParams& p, int b,
+                                            bool flag_table) {
+  ReqInfo r{};
+  r.q0 = p.cu_q[b];
+  r.q_len = min(p.cu_q[b + 1] - r.q0, p.total_q - r.q0);
+  if (r.q0 < 0 || r.q_len <= 0) return r;
+  r.rows = r.q_len * p.G;
+  if (r.rows < p.min_rows || r.rows > p.max_rows || r.rows > 16) return r;
+  r.koff = p.cu_k ? p.cu_k[b] : 0;
+  r.L = p.cu_k ? p.cu_k[b + 1] - r.koff : p.seqused_k[b];
+  // rows past the table (or, non-paged, past the K/V tensor) are not read
+  const int L_tab = p.cu_k ? (r.koff < 0 ? 0 : max(0, min(r.L, p.total_k - r.koff)))
+                           : min(r.L, p.max_blocks * p.BS);
+  if (flag_table && L_tab < r.L) atomicOr(p.err, kErrBadTable);
+  int kmin, kmax;
+  key_range(r.L, r.q_len, 0, r.q_len - 1, p.causal, p.wl, p.wr, kmin, kmax);
+  r.lo = kmin;
+  r.hi = max(kmin, min(kmax, L_tab));
+  r.kt0 = (r.lo / KT) * KT;
+  r.n_real = r.hi > r.lo ? (r.hi - r.kt0 + KT - 1) / KT : 0;
+  r.n = max(r.n_real, 1);
+  return r;
+}
+
+// Byte offset of 16-byte chunk `ch` (0 .. D*EB/16-1) of row r in a tile
+// written by 128-byte-wide TMA boxes with the 128-byte swizzle.
+template <int KT>
+__device__ __forceinline__ uint32_t kv_off(int r, int ch) {
+  return static_cast<uint32_t>((ch >> 3) * (KT * 128)) + sw128(r, ch & 7);
+}
+
+// All consumer threads reach named barrier 1; returns the OR of `pred`.
+__device__ __forceinline__ bool bar_or(int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n.reg .pred p, q;\n"
+      "setp.ne.u32 p, %1, 0;\n"
+      "bar.red.or.pred q, 1, %2, p;\n"
+      "selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+
+// Four E4M3 codes (low byte first) -> two f16x2 (exact).
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t& lo,
+                                              uint32_t& hi) {
+  asm("{\n.reg .b16 a, b;\n"
+      "mov.b32 {a, b}, %2;\n"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n"
+      "cvt.rn.f16x2.e4m3x2 %1, b;\n}\n"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b,
+                                         uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+
+template <typename T>
+__device__ __forceinline__ float elem_f32(uint32_t w, int hi);
+template <>
+__device__ __forceinline__ float elem_f32<__nv_bfloat16>(uint32_t w,
+                                                         int hi) {
+  return __uint_as_float(hi ? (w & 0xffff0000u) : (w << 16));
+}
+template <>
+__device__ __forceinline__ float elem_f32<__half>(uint32_t w, int hi) {
+  return __half2float(__ushort_as_half(
+      static_cast<unsigned short>(hi ? (w >> 16) : (w & 0xffffu))));
+}
+
+template <typename T, int D, int NCW, int KT, int STAGES, bool KV8>
+__global__ void __launch_bounds__((NCW + 1) * 32, 2)
+decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v) {
+  using C = Cfg<D, NCW, KT, STAGES, KV8>;
+  // MMA input type: the cache's type, or f16 for E4M3 codes
+  using MT = typename std::conditional<KV8, __half, T>::type;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t raw_u = smem_u32(smem_raw);
+  const uint32_t base_u = (raw_u + 1023u) & ~1023u;
+  unsigned char* base = smem_raw + (base_u - raw_u);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int c = blockIdx.x;
+  const int Hkv = p.Hkv, G = p.G;
+
+  const uint32_t ring = base_u;
+  const uint32_t bar0 = base_u + C::OFF_BAR;
+  auto full_k = [&](int s) { return bar0 + 8 * s; };
+  auto full_v = [&](int s) { return bar0 + 8 * (STAGES + s); };
+  auto empty = [&](int s) { return bar0 + 8 * (2 * STAGES + s); };
+  auto ufull = [&](int s) { return bar0 + 8 * (3 * STAGES + s); };
+  auto uempty = [&](int s) { return bar0 + 8 * (3 * STAGES + 2 + s); };
+  auto tile_k = [&](int s) { return ring + s * 2 * C::TILE_BYTES; };
+  auto tile_v = [&](int s) {
+    return ring + s * 2 * C::TILE_BYTES + C::TILE_BYTES;
+  };
+  auto qraw = [&](int s) { return base_u + C::OFF_QRAW + s * C::QRAW_BYTES; };
+  const uint32_t qfrag = base_u + C::OFF_QFRAG;
+  float* comb = reinterpret_cast<float*>(base + C::OFF_COMB);
+  float* ml = reinterpret_cast<float*>(base + C::OFF_ML);
+  volatile UnitDesc* desc =
+      reinterpret_cast<volatile UnitDesc*>(base + C::OFF_DESC);
+  int* misc = reinterpret_cast<int*>(base + C::OFF_MISC);
+  volatile int* abort_flag = misc;                 // [0]
+  volatile unsigned* bad_boxes =
+      reinterpret_cast<volatile unsigned*>(misc + 1);   // [1 .. STAGES]
+  int* start = misc + 8;                           // [8 .. 15]
+  long long* scan = reinterpret_cast<long long*>(misc + 16);   // [16 .. 31]
+  float* qmax = reinterpret_cast<float*>(misc + 32);            // [32 .. 39]
+
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_k(s), 1);
+      mbar_init(full_v(s), 1);
+      mbar_init(empty(s), NCW);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(ufull(s), 1 + 32);   // descriptor + the producer's cp.asyncs
+      mbar_init(uempty(s), NCW);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+
+  // ---- this CTA's share of the tile sequence (every CTA derives the same
+  // prefix over the requests; thread t scans a contiguous run of them)
+  const int B = p.batch;
+  const int per = (B + C::NT - 1) / C::NT;
+  const int b_lo = min(B, tid * per), b_hi = min(B, b_lo + per);
+  long long mine = 0;
+  for (int b = b_lo; b < b_hi; ++b)
+    mine += static_cast<long long>(req_info<KT>(p, b, c == 0).n) * Hkv;
+  long long incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) scan[warp] = incl;
+  __syncthreads();
+  long long excl = incl - mine, N = 0;
+  for (int w = 0; w < NCW + 1; ++w) {
+    if (w < warp) excl += scan[w];
+    N += scan[w];
+  }
+  const int C_all = gridDim.x;
+  const long long C_eff = max(1LL, min(static_cast<long long>(C_all), N / 2));
+  long long T0 = 0, T1 = 0;
+  if (c < C_eff) {
+    T0 = c * N / C_eff;
+    T1 = (c + 1) * N / C_eff;
+  }
+  // the units holding tiles T0 and T1 - 1
+  if (T0 < T1 && mine > 0) {
+    long long acc = excl;
+    for (int b = b_lo; b < b_hi; ++b) {
+      const int n = req_info<KT>(p, b, false).n;
+      const long long t = static_cast<long long>(n) * Hkv;
+      if (n > 0) {
+        if (T0 >= acc && T0 < acc + t) {
+          const long long rel = T0 - acc;
+          start[0] = b;
+          start[1] = static_cast<int>(rel / n);
+          start[2] = static_cast<int>(rel % n);
+        }
+        if (T1 - 1 >= acc && T1 - 1 < acc + t) {
+          const long long rel = T1 - 1 - acc;
+          start[3] = b;
+          start[4] = static_cast<int>(rel / n);
+          start[5] = static_cast<int>(rel % n);
+          start[6] = n;
+        }
+      }
+      acc += t;
+    }
+  }
+  __syncthreads();
+  // pieces this CTA leaves for the fold: the unit it starts inside (head,
+  // slot 2c) and the unit it starts that runs past its range (tail, slot
+  // 2c + 1)
+  int head_u = -1, tail_u = -1;
+  if (T0 < T1) {
+    const int u0 = start[0] * Hkv + start[1];
+    const int u1 = start[3] * Hkv + start[4];
+    if (start[2] > 0) head_u = u0;
+    if (start[5] + 1 < start[6] && !(u1 == u0 && start[2] > 0)) tail_u = u1;
+  }
+  if (tid == 0) p.sk_marks[c] = make_int2(head_u, tail_u);
+
+  if (warp == NCW) {
+    // ------------------------------------------------------------ producer
+    constexpr int CPR = C::CPR;
+    const int RB = p.rb;
+    const int nb_max = KT / RB;
+    const T* Q = static_cast<const T*>(p.q);
+    int b = start[0], g = start[1], t = start[2];
+    long long pos = T0;
+    int k = 0, it = 0;
+    bool stop = false;
+    ReqInfo ri{};
+    if (pos < T1) ri = req_info<KT>(p, b, false);
+    for (;;) {
+      const int slot = k & 1;
+      if (k >= 2) {
+        int ok = 1;
+        if (lane == 0)
+          ok = mbar_wait(uempty(slot), ((k >> 1) - 1) & 1, abort_flag, p.err);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {
+          stop = true;
+          break;
+        }
+      }
+      if (pos >= T1) {
+        if (lane == 0) {
+          desc[slot].end = 1;
+          mbar_arrive(ufull(slot));
+        }
+        cp_async_mbar_arrive(ufull(slot));
+        break;
+      }
+      const long long len =
+          min(static_cast<long long>(ri.n - t), T1 - pos);
+      int pslot = -1;
+      if (pos == T0 && head_u >= 0)
+        pslot = 2 * c;
+      else if (pos + len == T1 && tail_u >= 0)
+        pslot = 2 * c + 1;
+      const int j_beg = t;
+      const int j_end = min(t + static_cast<int>(len), ri.n_real);
+      if (lane == 0) {
+        volatile UnitDesc& d = desc[slot];
+        d.b = b;
+        d.g = g;
+        d.q0 = ri.q0;
+        d.q_len = ri.q_len;
+        d.rows = ri.rows;
+        d.L = ri.L;
+        d.lo = ri.lo;
+        d.hi = ri.hi;
+        d.kt0 = ri.kt0;
+        d.t_beg = j_beg;
+        d.n_tiles = max(0, j_end - j_beg);
+        d.slot = pslot;
+        d.end = 0;
+      }
+      // the unit's 16 packed query rows (zeros past `rows`)
+      for (int i = lane; i < 16 * CPR; i += 32) {
+        const int r = i / CPR, ch = i - (i / CPR) * CPR;
+        const bool ok = r < ri.rows;
+        const T* src = Q;
+        if (ok)
+          src = Q + static_cast<int64_t>(ri.q0 + r / G) * p.q_st +
+                static_cast<int64_t>(g * G + r % G) * p.q_sh + ch * 8;
+        cp_async_16(qraw(slot) + swz<C::ROW_BYTES>(r, ch), src, ok ? 16 : 0);
+      }
+      if (lane == 0) mbar_arrive(ufull(slot));
+      cp_async_mbar_arrive(ufull(slot));
+
+      // the piece's K and V tiles
+      const int32_t* bt =
+          p.cu_k ? nullptr
+                 : p.block_table + static_cast<int64_t>(b) * p.bt_stride;
+      auto fetch = [&](int j) -> int {            // page id of box `lane`
+        const int k0 = ri.kt0 + j * KT + lane * RB;
+        if (j >= j_end || lane >= nb_max || k0 >= ri.hi || !bt) return 0;
+        const int blk = __ldg(bt + k0 / p.BS);
+        if (blk < 0 || blk >= p.num_blocks) {
+          atomicOr(p.err, kErrBadBlock);
+          return -1;
+        }
+        return blk;
+      };
+      int cur = fetch(j_beg);
+      for (int j = j_beg; j < j_end; ++j) {
+        const int nxt = fetch(j + 1);
+        const int s = it % STAGES;
+        const int kt = ri.kt0 + j * KT;
+        int nbox = (ri.hi - kt + RB - 1) / RB;
+        if (nbox > nb_max) nbox = nb_max;
+        const unsigned bad =
+            __ballot_sync(0xffffffffu, lane < nbox && cur < 0);
+        int halt = 0;
+        if (lane == 0) {
+          if (it >= STAGES &&
+              !mbar_wait(empty(s), ((it / STAGES) - 1) & 1, abort_flag,
+                         p.err)) {
+            halt = 1;
+          } else {
+            bad_boxes[s] = bad;
+            const uint32_t bytes = (nbox - __popc(bad)) * C::NCB * RB * 128;
+            mbar_expect_tx(full_k(s), bytes);
+            mbar_expect_tx(full_v(s), bytes);
+          }
+        }
+        if (__shfl_sync(0xffffffffu, halt, 0)) {
+          stop = true;
+          break;
+        }
+        if (lane < nbox && cur >= 0) {
+          const int k0 = kt + lane * RB;
+          const int row = p.cu_k ? ri.koff + k0 : k0 % p.BS;
+#pragma unroll
+          for (int cb = 0; cb < C::NCB; ++cb) {
+            const uint32_t dk = tile_k(s) + cb * C::CB_BYTES + lane * RB * 128;
+            const uint32_t dv = tile_v(s) + cb * C::CB_BYTES + lane * RB * 128;
+            if (p.kv_order_hnd) {
+              tma_load_4d(dk, &tm_k, cb * C::BOXC, row, g, cur, full_k(s));
+              tma_load_4d(dv, &tm_v, cb * C::BOXC, row, g, cur, full_v(s));
+            } else {
+              tma_load_4d(dk, &tm_k, cb * C::BOXC, g, row, cur, full_k(s));
+              tma_load_4d(dv, &tm_v, cb * C::BOXC, g, row, cur, full_v(s));
+            }
+          }
+        }
+        ++it;
+        cur = nxt;
+      }
+      if (stop) break;
+      pos += len;
+      ++k;
+      if (pos < T1) {
+        t = 0;
+        if (++g == Hkv) {
+          g = 0;
+          do {
+            ++b;
+            ri = req_info<KT>(p, b, false);
+          } while (ri.n == 0 && b + 1 < B);
+          if (ri.n == 0) pos = T1;    // (unreachable: the scan saw tiles)
+        }
+      }
+    }
+    if (lane == 0) {
+      // no copy of this CTA may still be in flight when it exits
+      for (int j = max(0, it - STAGES); j < it; ++j) {
+        mbar_drain(full_k(j % STAGES), (j / STAGES) & 1);
+        mbar_drain(full_v(j % STAGES), (j / STAGES) & 1);
+      }
+    }
+    cp_async_wait<0>();
+    (void)stop;
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int g8 = lane >> 2, c4 = lane & 3;
+  const int rA = g8, rB = g8 + 8;
+  const int lm_mi = lane >> 3, lm_r = lane & 7;
+  const int kw0 = warp * C::KW;
+  const bool plain = (p.softcap <= 0.f) && (p.alibi == nullptr);
+  const bool capped = (p.softcap > 0.f) && (p.alibi == nullptr);
+  const float inv_cap = p.softcap > 0.f ? 1.f / p.softcap : 0.f;
+  const float vscale = p.v_scale ? *p.v_scale : 1.f;
+  const float kscale = p.k_scale ? *p.k_scale : 1.f;
+  T* __restrict__ OUT = static_cast<T*>(p.out);
+  int it = 0;
+
+  for (int k = 0;; ++k) {
+    const int slot = k & 1;
+    const bool got = mbar_wait(ufull(slot), (k >> 1) & 1, abort_flag, p.err);
+    float qshift_f = 1.f;    // 2^shift: the query scaling of an fp8 unit
+    if constexpr (KV8) {
+      // largest |q| of the unit's rows (bf16 queries only)
+      float mx = 0.f;
+      if (got && std::is_same<T, __nv_bfloat16>::value) {
+        for (int i = tid; i < 16 * C::CPR; i += C::CT) {
+          const int r = i / C::CPR, ch = i - (i / C::CPR) * C::CPR;
+          uint32_t w[4];
+          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                       : "r"(qraw(slot) + swz<C::ROW_BYTES>(r, ch)));
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            mx = fmaxf(mx, fabsf(elem_f32<T>(w[e], 0)));
+            mx = fmaxf(mx, fabsf(elem_f32<T>(w[e], 1)));
+          }
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1)
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (lane == 0) qmax[warp] = mx;
+      }
+      if (bar_or(C::CT, !got)) return;
+      int shift = 0;
+      if (std::is_same<T, __nv_bfloat16>::value) {
+        float m = 0.f;
+        for (int w = 0; w < NCW; ++w) m = fmaxf(m, qmax[w]);
+        if (m > 0.f) {
+          const int e = static_cast<int>((__float_as_uint(m) >> 23) & 0xff) - 127;
+          shift = max(-100, min(100, e - 14));
+        }
+      }
+      qshift_f = exp2f(static_cast<float>(shift));
+      const float qmul = exp2f(static_cast<float>(-shift));
+      // f16 A fragments of Q for every k16 step, in the head-dimension
+      // order the K fragments arrive in (d = 16 ks + 4 c4 + {0,1} in
+      // registers 0/1, + {2,3} in registers 2/3)
+      for (int i = tid; i < (D / 16) * 32; i += C::CT) {
+        const int ks = i >> 5, ln = i & 31;
+        const int gg = ln >> 2, cc = ln & 3;
+        const int d = 16 * ks + 4 * cc;
+        const uint32_t off = (d & 7) * 2;
+        uint32_t a[4];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t w0, w1;
+          asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];"
+                       : "=r"(w0), "=r"(w1)
+                       : "r"(qraw(slot) + swz<C::ROW_BYTES>(gg + 8 * h, d >> 3) +
+                             off));
+          if (std::is_same<T, __half>::value) {
+            a[h] = w0;
+            a[2 + h] = w1;
+          } else {
+            a[h] = pack2<__half>(elem_f32<T>(w0, 0) * qmul,
+                                 elem_f32<T>(w0, 1) * qmul);
+            a[2 + h] = pack2<__half>(elem_f32<T>(w1, 0) * qmul,
+                                     elem_f32<T>(w1, 1) * qmul);
+          }
+        }
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
+                         qfrag + (ks * 32 + ln) * 16),
+                     "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3])
+                     : "memory");
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(C::CT) : "memory");
+    } else {
+      if (bar_or(C::CT, !got)) return;
+    }
+    const int d_end = desc[slot].end;
+    if (d_end) return;
+    const int b = desc[slot].b, g = desc[slot].g, q0 = desc[slot].q0;
+    const int q_len = desc[slot].q_len, rows = desc[slot].rows;
+    const int L = desc[slot].L, lo = desc[slot].lo, hi = desc[slot].hi;
+    const int kt0 = desc[slot].kt0, t_beg = desc[slot].t_beg;
+    const int n_tiles = desc[slot].n_tiles, pslot = desc[slot].slot;
+    (void)b;
+    if constexpr (KV8) {
+      // Q now lives in the fragment buffer: release the descriptor slot
+      __syncwarp();
+      if (lane == 0) mbar_arrive(uempty(slot));
+    }
+
+    const int ctx = L - q_len;
+    const int pA = ctx + rA / G, pB = ctx + rB / G;
+    const bool okA = rA < rows, okB = rB < rows;
+    float slopeA = 0.f, slopeB = 0.f;
+    if (p.alibi) {
+      if (okA) slopeA = p.alibi[g * G + rA % G];
+      if (okB) slopeB = p.alibi[g * G + rB % G];
+    }
+    const float qk_scale = p.scale * kscale * qshift_f;
+    const float scale_log2 = qk_scale * kLog2e;
+    int full_lo = lo, full_hi = hi;
+    {
+      const int p_lo = ctx, p_hi = ctx + (rows - 1) / G;
+      if (p.wl >= 0) full_lo = max(full_lo, p_hi - p.wl);
+      if (p.causal) full_hi = min(full_hi, p_lo + 1);
+      if (p.wr >= 0) full_hi = min(full_hi, p_lo + p.wr + 1);
+    }
+
+    float o[D / 8][4];
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
+    bool aborted = false;
+
+    for (int jt = 0; jt < n_tiles; ++jt, ++it) {
+      const int s = it % STAGES;
+      const uint32_t par = (it / STAGES) & 1;
+      const int kt = kt0 + (t_beg + jt) * KT;
+      if (!mbar_wait(full_k(s), par, abort_flag, p.err)) {
+        aborted = true;
+        break;
+      }
+      const uint32_t sK = tile_k(s), sV = tile_v(s);
+      constexpr int RCH = KV8 ? D / 16 : D / 8;   // 16-byte chunks per row
+      if (const unsigned bad = bad_boxes[s]) {
+        // pages the table pointed outside the cache: zero keys and values
+        for (int idx = lane; idx < C::KW * RCH; idx += 32) {
+          const int r = kw0 + idx / RCH, ch = idx % RCH;
+          if (!((bad >> (r / p.rb)) & 1u)) continue;
+          asm volatile("st.shared.v4.u32 [%0], {%2, %2, %2, %2};\n"
+                       "st.shared.v4.u32 [%1], {%2, %2, %2, %2};" ::"r"(
+                           sK + kv_off<KT>(r, ch)),
+                       "r"(sV + kv_off<KT>(r, ch)), "r"(0)
+                       : "memory");
+        }
+        fence_proxy_async();
+        __syncwarp();
+      }
+
+      // S = Q K^T for 16 rows x KW keys
+      float sc[C::NKT][4];
+#pragma unroll
+      for (int i = 0; i < C::NKT; ++i)
+        sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
+      if constexpr (KV8) {
+        // one ldmatrix.x4 group holds 4 / NKT k16 steps of all NKT n8
+        // tiles: matrix m covers n8 tile m % NKT of step grp * 4 / NKT +
+        // m / NKT (16 code bytes = one k16 step)
+        constexpr int KPG = 4 / C::NKT;
+#pragma unroll
+        for (int grp = 0; grp < (D / 16) / KPG; ++grp) {
+          uint32_t r4[4];
+          {
+            const int nt = lm_mi % C::NKT, ks = grp * KPG + lm_mi / C::NKT;
+            ldmatrix_x4(sK + kv_off<KT>(kw0 + nt * 8 + lm_r, ks), r4[0],
+                        r4[1], r4[2], r4[3]);
+          }
+#pragma unroll
+          for (int kq = 0; kq < KPG; ++kq) {
+            const int ks = grp * KPG + kq;
+            uint32_t a[4];
+            asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
+                         : "r"(qfrag + (ks * 32 + lane) * 16));
+#pragma unroll
+            for (int nt = 0; nt < C::NKT; ++nt) {
+              uint32_t b0, b1;
+              e4m3x4_to_f16(r4[kq * C::NKT + nt], b0, b1);
+              mma_16816<__half>(sc[nt], a, b0, b1);
+            }
+          }
+        }
+      } else {
+        const uint32_t sQ = qraw(slot);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          uint32_t a[4];
+          {
+            const int r = lm_r + (lm_mi & 1) * 8;
+            const int ch = kk * 2 + (lm_mi >> 1);
+            ldmatrix_x4(sQ + swz<C::ROW_BYTES>(r, ch), a[0], a[1], a[2], a[3]);
+          }
+#pragma unroll
+          for (int np = 0; np < C::NKT / 2; ++np) {
+            uint32_t b0, b1, b2, b3;
+            const int r = kw0 + np * 16 + lm_r + (lm_mi >> 1) * 8;
+            const int ch = kk * 2 + (lm_mi & 1);
+            ldmatrix_x4(sK + kv_off<KT>(r, ch), b0, b1, b2, b3);
+            mma_16816<T>(sc[2 * np], a, b0, b1);
+            mma_16816<T>(sc[2 * np + 1], a, b2, b3);
+          }
+        }
+      }
+
+      // logits (base 2) with masks
+      float mxA = -INFINITY, mxB = -INFINITY;
+      const bool interior = kt >= full_lo && kt + KT <= full_hi;
+      if (plain && interior) {
+#pragma unroll
+        for (int nt = 0; nt < C::NKT; ++nt) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sc[nt][e] *= scale_log2;
+          mxA = fmaxf(mxA, fmaxf(sc[nt][0], sc[nt][1]));
+          mxB = fmaxf(mxB, fmaxf(sc[nt][2], sc[nt][3]));
+        }
+      } else if (capped && interior) {
+        const float pre = qk_scale * inv_cap, post = p.softcap * kLog2e;
+#pragma unroll
+        for (int nt = 0; nt < C::NKT; ++nt) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            sc[nt][e] = post * tanh_fast(sc[nt][e] * pre);
+          mxA = fmaxf(mxA, fmaxf(sc[nt][0], sc[nt][1]));
+          mxB = fmaxf(mxB, fmaxf(sc[nt][2], sc[nt][3]));
+        }
+      } else {
+#pragma unroll
+        for (int nt = 0; nt < C::NKT; ++nt) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int key = kt + kw0 + nt * 8 + 2 * c4 + (e & 1);
+            const bool rowB = e >= 2;
+            const int pos = rowB ? pB : pA;
+            float x = sc[nt][e];
+            if (plain) {
+              x *= scale_log2;
+            } else {
+              x *= qk_scale;
+              if (p.softcap > 0.f) x = p.softcap * tanh_fast(x * inv_cap);
+              if (p.alibi)
+                x -= (rowB ? slopeB : slopeA) * fabsf(float(pos - key));
+              x *= kLog2e;
+            }
+            bool ok = (rowB ? okB : okA) && key >= lo && key < hi;
+            if (p.causal) ok = ok && key <= pos;
+            if (p.wl >= 0) ok = ok && key >= pos - p.wl;
+            if (p.wr >= 0) ok = ok && key <= pos + p.wr;
+            x = ok ? x : -INFINITY;
+            sc[nt][e] = x;
+            if (rowB) mxB = fmaxf(mxB, x); else mxA = fmaxf(mxA, x);
+          }
+        }
+      }
+      mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 1));
+      mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 2));
+      mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 1));
+      mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 2));
+      const float mnA = fmaxf(mA, mxA), mnB = fmaxf(mB, mxB);
+      const float baseA = (mnA == -INFINITY) ? 0.f : mnA;
+      const float baseB = (mnB == -INFINITY) ? 0.f : mnB;
+      const float alA = ex2(mA - baseA), alB = ex2(mB - baseB);
+      mA = mnA;
+      mB = mnB;
+      float sumA = 0.f, sumB = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < C::NKT; ++nt) {
+        sc[nt][0] = ex2(sc[nt][0] - baseA);
+        sc[nt][1] = ex2(sc[nt][1] - baseA);
+        sc[nt][2] = ex2(sc[nt][2] - baseB);
+        sc[nt][3] = ex2(sc[nt][3] - baseB);
+        sumA += sc[nt][0] + sc[nt][1];
+        sumB += sc[nt][2] + sc[nt][3];
+      }
+      lA = lA * alA + sumA;
+      lB = lB * alB + sumB;
+      // once the running maxima settle, alpha is exactly 1: skip the rescale
+      if (__any_sync(0xffffffffu, alA != 1.f || alB != 1.f)) {
+#pragma unroll
+        for (int i = 0; i < D / 8; ++i) {
+          o[i][0] *= alA;
+          o[i][1] *= alA;
+          o[i][2] *= alB;
+          o[i][3] *= alB;
+        }
+      }
+
+      if (!mbar_wait(full_v(s), par, abort_flag, p.err)) {
+        aborted = true;
+        break;
+      }
+      if (kt + kw0 + C::KW > hi) {
+        // rows of this warp at or past the loaded range: zero them, so
+        // that P = 0 never meets NaN padding or a stale row
+        const int r0 = max(hi - kt, kw0);
+        for (int idx = lane; idx < (kw0 + C::KW - r0) * RCH; idx += 32) {
+          const int r = r0 + idx / RCH, ch = idx % RCH;
+          asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(
+                           sV + kv_off<KT>(r, ch)),
+                       "r"(0)
+                       : "memory");
+        }
+        fence_proxy_async();
+        __syncwarp();
+      }
+      // O += P V
+#pragma unroll
+      for (int ks = 0; ks < C::KW / 16; ++ks) {
+        uint32_t a[4];
+        a[0] = pack2<MT>(sc[2 * ks][0], sc[2 * ks][1]);
+        a[1] = pack2<MT>(sc[2 * ks][2], sc[2 * ks][3]);
+        a[2] = pack2<MT>(sc[2 * ks + 1][0], sc[2 * ks + 1][1]);
+        a[3] = pack2<MT>(sc[2 * ks + 1][2], sc[2 * ks + 1][3]);
+        if constexpr (KV8) {
+          // keys 2 c4 + {0, 1, 8, 9} of the 16, head-dimension bytes
+          // 4 g8 .. 4 g8 + 3 of each 32-column chunk; column j of the quad
+          // feeds n8 tile 4 * chunk + j
+          const int kr = kw0 + ks * 16 + 2 * c4;
+#pragma unroll
+          for (int dc = 0; dc < D / 32; ++dc) {
+            const int x = dc * 32 + 4 * g8;            // byte in the row
+            const int ch = x >> 4, wi = x & 15;
+            const uint32_t w0 = lds32(sV + kv_off<KT>(kr, ch) + wi);
+            const uint32_t w1 = lds32(sV + kv_off<KT>(kr + 1, ch) + wi);
+            const uint32_t w2 = lds32(sV + kv_off<KT>(kr + 8, ch) + wi);
+            const uint32_t w3 = lds32(sV + kv_off<KT>(kr + 9, ch) + wi);
+            const uint32_t p01a = prmt(w0, w1, 0x5140);   // cols 0, 1
+            const uint32_t p01b = prmt(w0, w1, 0x7362);   // cols 2, 3
+            const uint32_t p89a = prmt(w2, w3, 0x5140);
+            const uint32_t p89b = prmt(w2, w3, 0x7362);
+            uint32_t lo0, lo1, lo2, lo3, hi0, hi1, hi2, hi3;
+            e4m3x4_to_f16(p01a, lo0, lo1);
+            e4m3x4_to_f16(p01b, lo2, lo3);
+            e4m3x4_to_f16(p89a, hi0, hi1);
+            e4m3x4_to_f16(p89b, hi2, hi3);
+            mma_16816<__half>(o[dc * 4 + 0], a, lo0, hi0);
+            mma_16816<__half>(o[dc * 4 + 1], a, lo1, hi1);
+            mma_16816<__half>(o[dc * 4 + 2], a, lo2, hi2);
+            mma_16816<__half>(o[dc * 4 + 3], a, lo3, hi3);
+          }
+        } else {
+#pragma unroll
+          for (int dp = 0; dp < D / 16; ++dp) {
+            uint32_t b0, b1, b2, b3;
+            const int r = kw0 + ks * 16 + lm_r + (lm_mi & 1) * 8;
+            const int ch = dp * 2 + (lm_mi >> 1);
+            ldmatrix_x4_trans(sV + kv_off<KT>(r, ch), b0, b1, b2, b3);
+            mma_16816<T>(o[2 * dp], a, b0, b1);
+            mma_16816<T>(o[2 * dp + 1], a, b2, b3);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty(s));
+    }
+    if constexpr (!KV8) {
+      // the unit's Q slot and descriptor are no longer read
+      __syncwarp();
+      if (lane == 0 && !aborted) mbar_arrive(uempty(slot));
+    }
+
+    lA += __shfl_xor_sync(0xffffffffu, lA, 1);
+    lA += __shfl_xor_sync(0xffffffffu, lA, 2);
+    lB += __shfl_xor_sync(0xffffffffu, lB, 1);
+    lB += __shfl_xor_sync(0xffffffffu, lB, 2);
+
+    // ---- epilogue: warps 1.. hand their states to warp 0
+    if (bar_or(C::CT, aborted || *abort_flag)) return;
+    if (warp > 0) {
+      float* cw = comb + (warp - 1) * 16 * C::CST;
+      float* mw = ml + (warp - 1) * 32;
+      if (c4 == 0) {
+        mw[rA * 2] = mA;
+        mw[rA * 2 + 1] = lA;
+        mw[rB * 2] = mB;
+        mw[rB * 2 + 1] = lB;
+      }
+      if constexpr (KV8) {
+#pragma unroll
+        for (int dc = 0; dc < D / 32; ++dc) {
+          const int col = dc * 32 + 8 * c4;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            float* dst = cw + (g8 + 8 * h) * C::CST + col;
+            *reinterpret_cast<float4*>(dst) =
+                make_float4(o[dc * 4 + 0][2 * h], o[dc * 4 + 1][2 * h],
+                            o[dc * 4 + 2][2 * h], o[dc * 4 + 3][2 * h]);
+            *reinterpret_cast<float4*>(dst + 4) =
+                make_float4(o[dc * 4 + 0][2 * h + 1], o[dc * 4 + 1][2 * h + 1],
+                            o[dc * 4 + 2][2 * h + 1], o[dc * 4 + 3][2 * h + 1]);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int dn = 0; dn < D / 8; ++dn) {
+          *reinterpret_cast<float2*>(cw + rA * C::CST + dn * 8 + 2 * c4) =
+              make_float2(o[dn][0], o[dn][1]);
+          *reinterpret_cast<float2*>(cw + rB * C::CST + dn * 8 + 2 * c4) =
+              make_float2(o[dn][2], o[dn][3]);
+        }
+      }
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(C::CT) : "memory");
+    if (warp != 0) continue;
+
+    // warp 0: merge, normalise, write the output or the piece's partial
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int r = g8 + 8 * h;
+      if (r >= rows) continue;
+      const float m_own = h ? mB : mA, l_own = h ? lB : lA;
+      float M = m_own;
+#pragma unroll
+      for (int w = 0; w < NCW - 1; ++w) M = fmaxf(M, ml[w * 32 + r * 2]);
+      const float mb = (M == -INFINITY) ? 0.f : M;
+      const float f_own = ex2(m_own - mb);
+      float fw[NCW - 1];
+      float lsum = f_own * l_own;
+#pragma unroll
+      for (int w = 0; w < NCW - 1; ++w) {
+        fw[w] = ex2(ml[w * 32 + r * 2] - mb);
+        lsum += fw[w] * ml[w * 32 + r * 2 + 1];
+      }
+      const int tok = q0 + r / G, hq = g * G + r % G;
+      float inv, lse;   // a sink enters once: here, or in the fold
+      finish_row(M, lsum, pslot < 0 ? p.sinks : nullptr, hq, &inv, &lse);
+      inv *= vscale;
+      T* orow = OUT + static_cast<int64_t>(tok) * p.o_st +
+                static_cast<int64_t>(hq) * p.o_sh;
+      float* prow = pslot >= 0
+                        ? p.part_o + (static_cast<int64_t>(pslot) * 16 + r) * D
+                        : nullptr;
+      if constexpr (KV8) {
+#pragma unroll
+        for (int dc = 0; dc < D / 32; ++dc) {
+          const int col = dc * 32 + 8 * c4;
+          float v[8];
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              v[4 * e + j] = f_own * o[dc * 4 + j][2 * h + e];
+#pragma unroll
+          for (int w = 0; w < NCW - 1; ++w) {
+            const float* src = comb + (w * 16 + r) * C::CST + col;
+            const float4 x0 = *reinterpret_cast<const float4*>(src);
+            const float4 x1 = *reinterpret_cast<const float4*>(src + 4);
+            v[0] += fw[w] * x0.x;
+            v[1] += fw[w] * x0.y;
+            v[2] += fw[w] * x0.z;
+            v[3] += fw[w] * x0.w;
+            v[4] += fw[w] * x1.x;
+            v[5] += fw[w] * x1.y;
+            v[6] += fw[w] * x1.z;
+            v[7] += fw[w] * x1.w;
+          }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[e] *= inv;
+          if (pslot < 0) {
+            uint4 pk;
+            pk.x = pack2<T>(v[0], v[1]);
+            pk.y = pack2<T>(v[2], v[3]);
+            pk.z = pack2<T>(v[4], v[5]);
+            pk.w = pack2<T>(v[6], v[7]);
+            *reinterpret_cast<uint4*>(orow + col) = pk;
+          } else {
+            *reinterpret_cast<float4*>(prow + col) =
+                make_float4(v[0], v[1], v[2], v[3]);
+            *reinterpret_cast<float4*>(prow + col + 4) =
+                make_float4(v[4], v[5], v[6], v[7]);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int dn = 0; dn < D / 8; ++dn) {
+          const int col = dn * 8 + 2 * c4;
+          float v0 = f_own * o[dn][2 * h], v1 = f_own * o[dn][2 * h + 1];
+#pragma unroll
+          for (int w = 0; w < NCW - 1; ++w) {
+            const float2 x = *reinterpret_cast<const float2*>(
+                comb + (w * 16 + r) * C::CST + col);
+            v0 += fw[w] * x.x;
+            v1 += fw[w] * x.y;
+          }
+          v0 *= inv;
+          v1 *= inv;
+          if (pslot < 0)
+            *reinterpret_cast<uint32_t*>(orow + col) = pack2<T>(v0, v1);
+          else
+            *reinterpret_cast<float2*>(prow + col) = make_float2(v0, v1);
+        }
+      }
+      if (c4 == 0) {
+        if (pslot < 0) {
+          if (p.lse) p.lse[static_cast<int64_t>(hq) * p.total_q + tok] = lse;
+        } else {
+          p.part_lse[static_cast<int64_t>(pslot) * 16 + r] = lse;
+        }
+      }
+    }
+  }
+}
+
+// Merge the pieces of the units that CTA range boundaries cut.  Block c
+// (1 <= c < C) looks at the boundary before CTA c: the unit whose first
+// piece CTA c - 1 wrote to slot 2(c-1)+1 continues in slots 2c, 2(c+1), ...
+// for every following CTA that marks it as its head unit.
+template <typename T, int D>
+__global__ void __launch_bounds__(128) fold_kernel(const AttnParams p,
+                                                   int ctas) {
+  const int c = blockIdx.x + 1;
+  const int u = p.sk_marks[c - 1].y;
+  if (u < 0) return;
+  int c_end = c;
+  while (c_end < ctas && p.sk_marks[c_end].x == u) ++c_end;
+  const int npieces = 1 + (c_end - c);
+  const int b = u / p.Hkv, g = u - (u / p.Hkv) * p.Hkv;
+  const int q0 = p.cu_q[b];
+  const int q_len = min(p.cu_q[b + 1] - q0, p.total_q - q0);
+  const int rows = q_len * p.G;
+  T* __restrict__ OUT = static_cast<T*>(p.out);
+  for (int i = threadIdx.x; i < rows * (D / 4); i += blockDim.x) {
+    const int r = i / (D / 4), col = (i - r * (D / 4)) * 4;
+    auto slot_of = [&](int k) { return k == 0 ? 2 * (c - 1) + 1 : 2 * (c + k - 1); };
+    float M = -INFINITY;
+    for (int k = 0; k < npieces; ++k)
+      M = fmaxf(M, p.part_lse[static_cast<int64_t>(slot_of(k)) * 16 + r] *
+                       kLog2e);
+    const float mb = (M == -INFINITY) ? 0.f : M;
+    float wsum = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < npieces; ++k) {
+      const int64_t sr = static_cast<int64_t>(slot_of(k)) * 16 + r;
+      const float w = ex2(p.part_lse[sr] * kLog2e - mb);
+      const float4 v = *reinterpret_cast<const float4*>(p.part_o + sr * D + col);
+      wsum += w;
+      acc.x += w * v.x;
+      acc.y += w * v.y;
+      acc.z += w * v.z;
+      acc.w += w * v.w;
+    }
+    const int tok = q0 + r / p.G, hq = g * p.G + r % p.G;
+    float inv, lse;
+    finish_row(M, wsum, p.sinks, hq, &inv, &lse);
+    T* dst = OUT + static_cast<int64_t>(tok) * p.o_st +
+             static_cast<int64_t>(hq) * p.o_sh + col;
+    uint2 pk;
+    pk.x = pack2<T>(acc.x * inv, acc.y * inv);
+    pk.y = pack2<T>(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2*>(dst) = pk;
+    if (p.lse && col == 0)
+      p.lse[static_cast<int64_t>(hq) * p.total_q + tok] = lse;
+  }
+}
+
+#ifndef PKV_DSK_D64_STAGES
+#define PKV_DSK_D64_STAGES 4
+#endif
+#ifndef PKV_DSK_D128_STAGES
+#define PKV_DSK_D128_STAGES 2
+#endif
+#ifndef PKV_DSK_D256_STAGES
+#define PKV_DSK_D256_STAGES 2
+#endif
+#ifndef PKV_DSK_FP8_STAGES
+#define PKV_DSK_FP8_STAGES 4
+#endif
+
+// Per instantiation: the shared-memory opt-in done on which devices, and
+// the resident CTAs per SM found there.
+template <typename T, int D, int NCW, int KT, int STAGES, bool KV8>
+struct Inst {
+  using C = Cfg<D, NCW, KT, STAGES, KV8>;
+  static std::atomic<int> per_sm[kMaxDevices];
+
+  static cudaError_t prepare(int dev, int* ctas_per_sm) {
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    int n = per_sm[dev].load(std::memory_order_acquire);
+    if (n <= 0) {
+      auto kern = decode_sk_kernel<T, D, NCW, KT, STAGES, KV8>;
+      cudaError_t e = cudaFuncSetAttribute(
+          kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+      if (e != cudaSuccess) return e;
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, C::NT,
+                                                        C::SMEM);
+      if (e != cudaSuccess) return e;
+      if (n <= 0) return cudaErrorInvalidConfiguration;
+      per_sm[dev].store(n, std::memory_order_release);
+    }
+    *ctas_per_sm = n;
+    return cudaSuccess;
+  }
+
+  static cudaError_t launch(const AttnParams& p, const CUtensorMap& mk,
+                            const CUtensorMap& mv, int grid,
+                            cudaStream_t stream) {
+    note_launch();
+    decode_sk_kernel<T, D, NCW, KT, STAGES, KV8>
+        <<<grid, C::NT, C::SMEM, stream>>>(p, mk, mv);
+    return cudaGetLastError();
+  }
+};
+template <typename T, int D, int NCW, int KT, int STAGES, bool KV8>
+std::atomic<int> Inst<T, D, NCW, KT, STAGES, KV8>::per_sm[kMaxDevices];
+
+// The configuration per (head size, cache type); f(Inst) is called with
+// the matching instantiation.
+template <typename T, bool KV8, typename F>
+cudaError_t with_cfg(int D, F&& f) {
+  if constexpr (KV8) {
+    switch (D) {
+      case 128: return f(Inst<T, 128, 4, 64, PKV_DSK_FP8_STAGES, true>{});
+      case 256: return f(Inst<T, 256, 2, 32, PKV_DSK_FP8_STAGES, true>{});
+      default: return cudaErrorInvalidValue;
+    }
+  } else {
+    switch (D) {
+      case 64: return f(Inst<T, 64, 4, 64, PKV_DSK_D64_STAGES, false>{});
+      case 128: return f(Inst<T, 128, 4, 64, PKV_DSK_D128_STAGES, false>{});
+      case 256: return f(Inst<T, 256, 2, 32, PKV_DSK_D256_STAGES, false>{});
+      default: return cudaErrorInvalidValue;
+    }
+  }
+}
+
+template <typename F>
+cudaError_t dispatch(bool bf16, bool kv8, int D, F&& f) {
+  if (bf16)
+    return kv8 ? with_cfg<__nv_bfloat16, true>(D, f)
+               : with_cfg<__nv_bfloat16, false>(D, f);
+  return kv8 ? with_cfg<__half, true>(D, f) : with_cfg<__half, false>(D, f);
+}
+
+}  // namespace dsk
+
+bool decode_sk_supported(int D, bool kv8) {
+  return kv8 ? (D == 128 || D == 256) : (D == 64 || D == 128 || D == 256);
+}
+
+cudaError_t decode_sk_ctas(int D, bool bf16, bool kv8, int sms, int* ctas) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  int per = 0;
+  e = dsk::dispatch(bf16, kv8, D, [&](auto inst) {
+    return decltype(inst)::prepare(dev, &per);
+  });
+  if (e != cudaSuccess) return e;
+  *ctas = per * sms;
+  return cudaSuccess;
+}
+
+size_t decode_sk_workspace_bytes(int D, int ctas) {
+  auto a256 = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  return a256(static_cast<size_t>(2) * ctas * 16 * D * 4) +
+         a256(static_cast<size_t>(2) * ctas * 16 * 4) +
+         a256(static_cast<size_t>(ctas) * 8);
+}
+
+cudaError_t launch_decode_attn_sk(const AttnParams& a, int D, bool bf16,
+                                  int ctas, void* scratch,
+                                  cudaStream_t stream) {
+  AttnParams p = a;
+  const bool kv8 = p.kv_fp8 != 0;
+  auto a256 = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  char* ws = static_cast<char*>(scratch);
+  p.part_o = reinterpret_cast<float*>(ws);
+  p.part_lse = reinterpret_cast<float*>(
+      ws + a256(static_cast<size_t>(2) * ctas * 16 * D * 4));
+  p.sk_marks = reinterpret_cast<int2*>(
+      ws + a256(static_cast<size_t>(2) * ctas * 16 * D * 4) +
+      a256(static_cast<size_t>(2) * ctas * 16 * 4));
+  const int KT = D == 256 ? 32 : 64;
+  int RB = 16;
+  while (RB * 2 <= KT && p.BS % (RB * 2) == 0) RB *= 2;
+  if (p.cu_k) RB = KT;    // non-paged: a box may start on any row
+  p.rb = RB;
+  p.kv_order_hnd = p.c_sh > p.c_sr ? 1 : 0;
+  CUtensorMap mk, mv;
+  if (!make_kv_map_ex(&mk, p.kc, kv8 ? 0 : (bf16 ? 2 : 1), D, p.BS, p.Hkv,
+                      p.num_blocks, p.c_sb, p.c_sr, p.c_sh, RB,
+                      p.kv_order_hnd) ||
+      !make_kv_map_ex(&mv, p.vc, kv8 ? 0 : (bf16 ? 2 : 1), D, p.BS, p.Hkv,
+                      p.num_blocks, p.c_sb, p.c_sr, p.c_sh, RB,
+                      p.kv_order_hnd))
+    return cudaErrorInvalidValue;
+  cudaError_t e = dsk::dispatch(bf16, kv8, D, [&](auto inst) {
+    return decltype(inst)::launch(p, mk, mv, ctas, stream);
+  });
+  if (e != cudaSuccess || ctas < 2) return e;
+  note_launch();
+  switch (D) {
+    case 64:
+      bf16 ? dsk::fold_kernel<__nv_bfloat16, 64><<<ctas - 1, 128, 0, stream>>>(p, ctas)
+           : dsk::fold_kernel<__half, 64><<<ctas - 1, 128, 0, stream>>>(p, ctas);
+      break;
+    case 128:
+      bf16 ? dsk::fold_kernel<__nv_bfloat16, 128><<<ctas - 1, 128, 0, stream>>>(p, ctas)
+           : dsk::fold_kernel<__half, 128><<<ctas - 1, 128, 0, stream>>>(p, ctas);
+      break;
+    default:
+      bf16 ? dsk::fold_kernel<__nv_bfloat16, 256><<<ctas - 1, 128, 0, stream>>>(p, ctas)
+           : dsk::fold_kernel<__half, 256><<<ctas - 1, 128, 0, stream>>>(p, ctas);
+      break;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

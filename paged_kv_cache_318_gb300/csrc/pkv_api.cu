@@ -22,8 +22,8 @@ __device__ unsigned g_device_error = 0;
 static std::atomic<uint64_t> g_launches{0};
 // prefill kernel: PKV_PREFILL_TCGEN05 or PKV_PREFILL_MMA_SYNC
 static std::atomic<int> g_prefill_kernel{PKV_PREFILL_TCGEN05};
-// decode kernel for 16-bit caches: PKV_DECODE_TMA or PKV_DECODE_CP_ASYNC
-static std::atomic<int> g_decode_kernel{PKV_DECODE_TMA};
+// decode kernel: PKV_DECODE_PERSISTENT, PKV_DECODE_TMA or PKV_DECODE_CP_ASYNC
+static std::atomic<int> g_decode_kernel{PKV_DECODE_PERSISTENT};
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 namespace {
@@ -200,10 +200,48 @@ size_t prefill_split_bytes(int splits, int total_q, int Hq, int D) {
   return align256(static_cast<size_t>(splits) * total_q * Hq * D * 4) +
          align256(static_cast<size_t>(splits) * Hq * total_q * 4);
 }
-// The whole workspace: the required part, then (prefill-class calls) the
-// counter and the split partials.
-size_t with_tail(size_t need, bool prefill, size_t split_bytes) {
-  return prefill ? align256(need) + kSchedBytes + split_bytes : need;
+// Calls that leave the split to the library (num_splits = 0, no fixed
+// split size) run their decode-class requests on the persistent decode
+// kernel when the workspace holds its scratch (the pieces of units that its
+// CTA ranges cut); the scratch is sized for the larger of the 16-bit
+// kernels' grids.
+bool sk_candidate(int num_splits, int fixed_split, int D, bool kv8) {
+  return num_splits == 0 && fixed_split <= 0 && decode_sk_supported(D, kv8);
+}
+size_t sk_scratch_bytes(int D, bool kv8, int sms) {
+  int a = 0, b = 0;
+  if (decode_sk_ctas(D, true, kv8, sms, &a) != cudaSuccess ||
+      decode_sk_ctas(D, false, kv8, sms, &b) != cudaSuccess)
+    return 0;
+  return decode_sk_workspace_bytes(D, a > b ? a : b);
+}
+
+// Workspace layout: the required part (decode split partials, fp8 page
+// copies), then the optional tail: the persistent decode kernel's scratch
+// (when the call may use it), and for calls with prefill-class requests
+// the 256-byte item counter and the prefill split partials.
+struct Layout {
+  size_t need = 0;                    // required bytes
+  size_t sk_off = 0, sk_bytes = 0;    // persistent decode scratch
+  size_t sched_off = 0;               // prefill item counter (prefill only)
+  size_t presplit_off = 0, presplit_bytes = 0;
+  size_t total = 0;
+};
+Layout make_layout(size_t need, bool prefill, size_t sk_bytes,
+                   size_t split_bytes) {
+  Layout l;
+  l.need = need;
+  l.sk_off = align256(need);
+  l.sk_bytes = sk_bytes;
+  if (prefill) {
+    l.sched_off = l.sk_off + sk_bytes;
+    l.presplit_off = l.sched_off + kSchedBytes;
+    l.presplit_bytes = split_bytes;
+    l.total = l.presplit_off + split_bytes;
+  } else {
+    l.total = sk_bytes ? l.sk_off + sk_bytes : need;
+  }
+  return l;
 }
 
 // fp8 cache with prefill-class requests: 16-bit copies of up to
@@ -283,7 +321,8 @@ pkv_status pkv_set_prefill_kernel(int which) {
 }
 
 pkv_status pkv_set_decode_kernel(int which) {
-  if (which != PKV_DECODE_TMA && which != PKV_DECODE_CP_ASYNC)
+  if (which != PKV_DECODE_TMA && which != PKV_DECODE_CP_ASYNC &&
+      which != PKV_DECODE_PERSISTENT)
     return fail(PKV_ERR_INVALID_ARG, "unknown decode kernel %d", which);
   g_decode_kernel.store(which);
   return PKV_OK;
@@ -412,13 +451,18 @@ size_t pkv_paged_attention_workspace_size_opts(
                                   num_splits, fixed_split_of(opts))
                  : 1,
       total_q, num_heads, head_size);
-  if (!fp8 || !pl.prefill)
-    return with_tail(pl.workspace, pl.prefill, split_bytes);
-  if (max_blocks_per_seq <= 0) return static_cast<size_t>(-1);
-  return with_tail(align256(pl.workspace) +
-                       fp8_mock_bytes(batch, max_blocks_per_seq, block_size,
-                                      num_kv_heads, head_size),
-                   true, split_bytes);
+  const size_t skb =
+      sk_candidate(num_splits, fixed_split_of(opts), head_size, fp8)
+          ? sk_scratch_bytes(head_size, fp8, sms)
+          : 0;
+  size_t need = pl.workspace;
+  if (fp8 && pl.prefill) {
+    if (max_blocks_per_seq <= 0) return static_cast<size_t>(-1);
+    need = align256(pl.workspace) +
+           fp8_mock_bytes(batch, max_blocks_per_seq, block_size, num_kv_heads,
+                          head_size);
+  }
+  return make_layout(need, pl.prefill, skb, split_bytes).total;
 }
 
 size_t pkv_paged_attention_workspace_size(int batch, int total_q,
@@ -442,7 +486,10 @@ size_t pkv_paged_attention_workspace_size(int batch, int total_q,
                                   num_splits, 0)
                  : 1,
       total_q, num_heads, head_size);
-  return with_tail(pl.workspace, pl.prefill, split_bytes);
+  const size_t skb = sk_candidate(num_splits, 0, head_size, false)
+                         ? sk_scratch_bytes(head_size, false, sms)
+                         : 0;
+  return make_layout(pl.workspace, pl.prefill, skb, split_bytes).total;
 }
 
 pkv_status pkv_paged_attention_varlen(
@@ -556,25 +603,47 @@ pkv_status pkv_paged_attention_varlen_opts(
     if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
       return fail(PKV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   }
-  // optional tail: the prefill item counter, then its split partials
+  // optional tail: the persistent decode scratch, then the prefill item
+  // counter and its split partials
+  const int sp = pl.prefill
+                     ? prefill_splits(batch, total_q, num_heads / num_kv_heads,
+                                      num_kv_heads, max_seqlen_k, head_size,
+                                      sms, num_splits, fixed_split)
+                     : 1;
+  const size_t sb = prefill_split_bytes(sp, total_q, num_heads, head_size);
+  const bool sk_ok =
+      sk_candidate(num_splits, fixed_split, head_size, kv8) &&
+      g_decode_kernel.load() == PKV_DECODE_PERSISTENT;
+  const size_t skb = sk_candidate(num_splits, fixed_split, head_size, kv8)
+                         ? sk_scratch_bytes(head_size, kv8, sms)
+                         : 0;
+  const Layout lay = make_layout(need, pl.prefill, skb, sb);
+  const bool ws_ok = workspace &&
+                     reinterpret_cast<uintptr_t>(workspace) % 256 == 0;
+  int sk_ctas = 0;
+  void* sk_scratch = nullptr;
+  if (sk_ok && pl.decode && skb > 0 && ws_ok &&
+      workspace_bytes >= lay.sk_off + lay.sk_bytes) {
+    if (decode_sk_ctas(head_size, dtype == PKV_BF16, kv8, sms, &sk_ctas) ==
+            cudaSuccess &&
+        decode_sk_workspace_bytes(head_size, sk_ctas) <= lay.sk_bytes)
+      sk_scratch = static_cast<char*>(workspace) + lay.sk_off;
+    else
+      sk_ctas = 0;
+  }
   int* sched = nullptr;
   int pre_splits = 1;
   float* pre_o = nullptr;
   float* pre_lse = nullptr;
-  if (pl.prefill && workspace &&
-      reinterpret_cast<uintptr_t>(workspace) % 256 == 0) {
-    char* tail = static_cast<char*>(workspace) + align256(need);
-    if (workspace_bytes >= with_tail(need, true, 0))
-      sched = reinterpret_cast<int*>(tail);
-    const int sp = prefill_splits(batch, total_q, num_heads / num_kv_heads,
-                                  num_kv_heads, max_seqlen_k, head_size, sms,
-                                  num_splits, fixed_split);
-    const size_t sb = prefill_split_bytes(sp, total_q, num_heads, head_size);
-    if (sp > 1 && workspace_bytes >= with_tail(need, true, sb)) {
+  if (pl.prefill && ws_ok) {
+    char* wsc = static_cast<char*>(workspace);
+    if (workspace_bytes >= lay.sched_off + kSchedBytes)
+      sched = reinterpret_cast<int*>(wsc + lay.sched_off);
+    if (sp > 1 && workspace_bytes >= lay.presplit_off + lay.presplit_bytes) {
       pre_splits = sp;
-      pre_o = reinterpret_cast<float*>(tail + kSchedBytes);
+      pre_o = reinterpret_cast<float*>(wsc + lay.presplit_off);
       pre_lse = reinterpret_cast<float*>(
-          tail + kSchedBytes +
+          wsc + lay.presplit_off +
           align256(static_cast<size_t>(sp) * total_q * num_heads *
                    head_size * 4));
     }
@@ -650,12 +719,18 @@ pkv_status pkv_paged_attention_varlen_opts(
       d.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                             pl.part_o_bytes);
     }
-    cudaError_t e =
-        (!kv8 && g_decode_kernel.load() == PKV_DECODE_TMA)
-            ? launch_decode_attn_tma(d, head_size, bf16, pl.splits, s)
-            : launch_decode_attn(d, head_size, bf16, pl.splits, 1, s);
+    cudaError_t e;
+    const bool persistent = sk_scratch != nullptr;
+    if (persistent) {
+      d.chunk = 0;
+      e = launch_decode_attn_sk(d, head_size, bf16, sk_ctas, sk_scratch, s);
+    } else if (!kv8 && g_decode_kernel.load() != PKV_DECODE_CP_ASYNC) {
+      e = launch_decode_attn_tma(d, head_size, bf16, pl.splits, s);
+    } else {
+      e = launch_decode_attn(d, head_size, bf16, pl.splits, 1, s);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
-    if (pl.chunk > 0) {
+    if (pl.chunk > 0 && !persistent) {
       CombineParams c{};
       c.part_o = d.part_o;
       c.part_lse = d.part_lse;

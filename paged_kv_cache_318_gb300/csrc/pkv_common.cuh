@@ -233,6 +233,9 @@ struct AttnParams {
   // persistent prefill: one int of workspace the kernel hands work items
   // out through (the launcher zeroes it first); null = fixed item order
   int* sched;
+  // persistent decode: per CTA, the unit it starts inside (x) and the unit
+  // it starts that continues past its range (y), -1 for none
+  int2* sk_marks;
   // persistent prefill split-KV: key splits per work item (1 = none); with
   // more, partials go to pre_o [S, total_q, Hq, D] / pre_lse [S, Hq,
   // total_q] and launch_prefill_split_combine folds them
@@ -344,6 +347,17 @@ cudaError_t launch_decode_attn_tma(const AttnParams& p, int D, bool bf16,
 
 cudaError_t launch_split_combine(const CombineParams& p, bool bf16,
                                  cudaStream_t stream);
+// Persistent decode attention (decode_sk.cu): 16-bit caches with D in {64,
+// 128, 256}, E4M3 caches with D in {128, 256}.  decode_sk_ctas gives the
+// launch's CTA count on the current device (resident CTAs per SM x sms);
+// the launch needs decode_sk_workspace_bytes(D, ctas) of scratch (256-byte
+// aligned) for the pieces of units that CTA boundaries cut.
+bool decode_sk_supported(int D, bool kv8);
+cudaError_t decode_sk_ctas(int D, bool bf16, bool kv8, int sms, int* ctas);
+size_t decode_sk_workspace_bytes(int D, int ctas);
+cudaError_t launch_decode_attn_sk(const AttnParams& p, int D, bool bf16,
+                                  int ctas, void* scratch,
+                                  cudaStream_t stream);
 // Required workspace bytes of an attention call (pkv_api.cu): the split-KV
 // partials and fp8 copies it needs, not the optional prefill tail.
 size_t required_workspace_bytes(int batch, int total_q, int max_seqlen_q,

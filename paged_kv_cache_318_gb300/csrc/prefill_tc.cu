@@ -2419,34 +2419,45 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 4-D map over one cache view: (D, Hkv, BS, NB) for NHD strides, (D, BS, Hkv,
-// NB) when the head stride is the larger (HND); box = 64 x 1 x RB x 1.
-bool make_kv_map(CUtensorMap* map, const void* ptr, bool bf16, int D, int BS,
-                 int Hkv, int64_t NB, int64_t s_blk, int64_t s_row,
-                 int64_t s_head, int RB, bool hnd) {
+// NB) when the head stride is the larger (HND); box = BOXC x 1 x RB x 1 with
+// BOXC * element bytes = 128.
+bool make_kv_map_ex(CUtensorMap* map, const void* ptr, int elem, int D,
+                    int BS, int Hkv, int64_t NB, int64_t s_blk, int64_t s_row,
+                    int64_t s_head, int RB, bool hnd) {
   auto fn = encode_fn();
-  if (!fn) return false;
+  if (!fn || elem < 0 || elem > 2) return false;
+  const int eb = elem == 0 ? 1 : 2;
   cuuint64_t dims[4], strides[3];
   cuuint32_t box[4], estr[4] = {1, 1, 1, 1};
   dims[0] = D;
   dims[3] = static_cast<cuuint64_t>(NB);
-  strides[2] = static_cast<cuuint64_t>(s_blk) * 2;
-  box[0] = 64;
+  strides[2] = static_cast<cuuint64_t>(s_blk) * eb;
+  box[0] = 128 / eb;
   box[3] = 1;
   if (hnd) {
-    dims[1] = BS;  strides[0] = static_cast<cuuint64_t>(s_row) * 2;  box[1] = RB;
-    dims[2] = Hkv; strides[1] = static_cast<cuuint64_t>(s_head) * 2; box[2] = 1;
+    dims[1] = BS;  strides[0] = static_cast<cuuint64_t>(s_row) * eb;  box[1] = RB;
+    dims[2] = Hkv; strides[1] = static_cast<cuuint64_t>(s_head) * eb; box[2] = 1;
   } else {
-    dims[1] = Hkv; strides[0] = static_cast<cuuint64_t>(s_head) * 2; box[1] = 1;
-    dims[2] = BS;  strides[1] = static_cast<cuuint64_t>(s_row) * 2;  box[2] = RB;
+    dims[1] = Hkv; strides[0] = static_cast<cuuint64_t>(s_head) * eb; box[1] = 1;
+    dims[2] = BS;  strides[1] = static_cast<cuuint64_t>(s_row) * eb;  box[2] = RB;
   }
-  CUresult r = fn(map,
-                  bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                       : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                  4, const_cast<void*>(ptr), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  const CUtensorMapDataType dt =
+      elem == 0 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                : (elem == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+  CUresult r = fn(map, dt, 4, const_cast<void*>(ptr), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+bool make_kv_map(CUtensorMap* map, const void* ptr, bool bf16, int D, int BS,
+                 int Hkv, int64_t NB, int64_t s_blk, int64_t s_row,
+                 int64_t s_head, int RB, bool hnd) {
+  return make_kv_map_ex(map, ptr, bf16 ? 2 : 1, D, BS, Hkv, NB, s_blk, s_row,
+                        s_head, RB, hnd);
 }
 
 

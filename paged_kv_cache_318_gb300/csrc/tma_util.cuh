@@ -115,5 +115,11 @@ __device__ __forceinline__ void fence_proxy_async() {
 bool make_kv_map(CUtensorMap* map, const void* ptr, bool bf16, int D, int BS,
                  int Hkv, int64_t NB, int64_t s_blk, int64_t s_row,
                  int64_t s_head, int RB, bool hnd);
+// The same map for an element type `elem`: 0 = one-byte codes (E4M3; box
+// 128 x 1 x RB x 1), 1 = f16, 2 = bf16 (box 64 x 1 x RB x 1).  Strides are
+// in elements of that type.
+bool make_kv_map_ex(CUtensorMap* map, const void* ptr, int elem, int D,
+                    int BS, int Hkv, int64_t NB, int64_t s_blk, int64_t s_row,
+                    int64_t s_head, int RB, bool hnd);
 
 }  // namespace pkv

@@ -181,21 +181,25 @@ DECODE_CASES = [
 ]
 
 
-@pytest.mark.parametrize("kernel", ["tma", "cp_async"])
+@pytest.mark.parametrize("kernel", ["persistent", "tma", "cp_async"])
 @pytest.mark.parametrize("idx", range(len(DECODE_CASES)))
 def test_decode_kernels(cuda_device, idx, kernel):
-    """Both decode kernels over page sizes 16-128 (and a non-power-of-two
+    """Every decode kernel over page sizes 16-128 (and a non-power-of-two
     48), window starts off the tile grid, split counts, poisoned page tails
-    and every head size."""
+    and every head size.  The persistent kernel serves calls that leave the
+    split to the library, so its runs use num_splits = 0."""
     q_lens, seq_lens, Hq, Hkv, D, BS, kw = DECODE_CASES[idx]
+    if kernel == "persistent":
+        kw = dict(kw, num_splits=0)
     wl = workloads.build_workload("dec%d" % idx, 950 + idx, q_lens, seq_lens,
                                   Hq, Hkv, D, BS, **kw)
-    which = api.DECODE_TMA if kernel == "tma" else api.DECODE_CP_ASYNC
+    which = {"persistent": api.DECODE_PERSISTENT, "tma": api.DECODE_TMA,
+             "cp_async": api.DECODE_CP_ASYNC}[kernel]
     api.set_decode_kernel(which)
     try:
         _, out, lse = run_batch(wl, cuda_device)
     finally:
-        api.set_decode_kernel(api.DECODE_TMA)
+        api.set_decode_kernel(api.DECODE_PERSISTENT)
     ref_out, ref_lse = full_reference(wl)
     assert_close(wl, out, lse, ref_out, ref_lse, "%s %d" % (kernel, idx))
 

@@ -5,9 +5,11 @@ allocate device memory (runtimes that plan every device byte up front and
 give a call no scratch, loops that must not call cudaMalloc/cudaFree because
 those can block and synchronise the device).  It takes its split-KV scratch
 from a fixed array inside the library.  Here it is called through the C ABI
-twice in a row, on different inputs, and each result must match the regular
-workspace entry point within the parity tolerance of the other tests.  A
-call that needs more scratch than the array holds must be rejected.
+twice in a row, on different inputs.  Each result must equal the regular
+workspace entry point's bit for bit (the two run the same plan and kernels;
+only where the scratch lives differs) and match the float64 oracle within
+the parity tolerance of the other tests.  A call that needs more scratch
+than the array holds must be rejected.
 
 This file sorts last so that a run stopping at the first failure has run
 every other test before it.
@@ -18,6 +20,7 @@ import numpy as np
 import pytest
 import torch
 
+from oracle.harness import request_reference
 from paged_kv_cache_318_gb300 import api, workloads
 from paged_kv_cache_318_gb300.batch import DeviceBatch
 
@@ -58,6 +61,19 @@ def _call_static(fn, b, out, lse, num_splits, max_seqlen_k=None):
               1 if wl.dtype == "bf16" else 0, stream)
 
 
+def _assert_oracle(wl, out, lse):
+    """Every request of wl against the float64 oracle."""
+    o = out.float().cpu().numpy()
+    ls = lse.cpu().numpy()
+    for b in range(wl.batch):
+        t0, t1 = int(wl.cu_seqlens_q[b]), int(wl.cu_seqlens_q[b + 1])
+        ref_o, ref_l = request_reference(wl, b)
+        err = np.abs(o[t0:t1] - ref_o).max()
+        lerr = np.abs(ls[:, t0:t1] - ref_l).max()
+        assert err <= TOL[wl.dtype], (b, err)
+        assert lerr <= LSE_TOL, (b, lerr)
+
+
 @pytest.fixture(scope="module")
 def lib(cuda_device):
     from paged_kv_cache_318_gb300 import _build
@@ -93,11 +109,10 @@ def test_static_scratch_matches_workspace_entry(cuda_device, lib):
         st = _call_static(fn, b, out, lse, splits)
         assert st == 0, lib.pkv_last_error()
         torch.cuda.synchronize()
-        err = (out.float() - ref_out.float()).abs().max().item()
-        lerr = (lse - ref_lse).abs().max().item()
-        assert torch.isfinite(out).all()
-        assert err <= TOL[b.wl.dtype], err
-        assert lerr <= LSE_TOL, lerr
+        api.check_device_errors(cuda_device)
+        assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+        assert torch.equal(lse.view(torch.int32), ref_lse.view(torch.int32))
+        _assert_oracle(b.wl, out, lse)
 
 
 def test_static_scratch_rejects_oversized_plans(cuda_device, lib):
@@ -148,3 +163,5 @@ def test_static_scratch_prefill_uses_the_optional_tail(cuda_device, lib):
         api.check_device_errors(cuda_device)
         assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
         assert torch.equal(lse.view(torch.int32), ref_lse.view(torch.int32))
+        if wl.batch == 1:       # (the oracle runs the small case only)
+            _assert_oracle(wl, out, lse)
