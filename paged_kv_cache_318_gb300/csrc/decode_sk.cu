@@ -78,15 +78,18 @@ struct Cfg {
   static constexpr int RING_BYTES = STAGES * 2 * TILE_BYTES;
   static constexpr int QRAW_BYTES = 16 * ROW_BYTES;
   static constexpr int QFRAG_BYTES = KV8 ? (D / 16) * 32 * 16 : 0;
-  // combine rows: float4 stores (fp8) want a 16-byte row shift, float2
-  // stores (16-bit) a 32-byte one, for conflict-free shared stores
-  static constexpr int CST = D + (KV8 ? 4 : 8);
-  static constexpr int COMB_BYTES = (NCW - 1) * 16 * CST * 4;
+  // The warps' states meet in the ring stage of the unit's last tile (held
+  // until warp 0 has merged them).  Row stride: float4 stores (fp8) want a
+  // 16-byte row shift, float2 stores (16-bit) a 32-byte one, for
+  // conflict-free shared stores, when the stage has room for it.
+  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+  static constexpr int CST_PAD = D + (KV8 ? 4 : 8);
+  static constexpr int CST =
+      (NCW - 1) * 16 * CST_PAD * 4 <= STAGE_BYTES ? CST_PAD : D;
   static constexpr int ML_BYTES = (NCW - 1) * 16 * 2 * 4;
   static constexpr int OFF_QRAW = RING_BYTES;
   static constexpr int OFF_QFRAG = OFF_QRAW + 2 * QRAW_BYTES;
-  static constexpr int OFF_COMB = OFF_QFRAG + QFRAG_BYTES;
-  static constexpr int OFF_ML = OFF_COMB + COMB_BYTES;
+  static constexpr int OFF_ML = OFF_QFRAG + QFRAG_BYTES;
   static constexpr int OFF_DESC = OFF_ML + ML_BYTES;        // 2 x 64 bytes
   static constexpr int OFF_MISC = OFF_DESC + 128;           // 256 bytes
   static constexpr int OFF_BAR = OFF_MISC + 256;
@@ -97,6 +100,9 @@ struct Cfg {
   static_assert(D % BOXC == 0, "whole TMA boxes per row");
   static_assert(CB_BYTES % 1024 == 0, "128-byte swizzle atoms");
   static_assert(NCW >= 2, "warp 0 merges the others' states");
+  static_assert((NCW - 1) * 16 * CST * 4 <= STAGE_BYTES,
+                "the warps' states fit in one ring stage");
+  static constexpr int KTILE = KT;
 };
 
 // One unit piece as the producer hands it to the consumers (64 bytes).
@@ -159,6 +165,12 @@ __device__ __forceinline__ bool bar_or(int nthreads, bool pred) {
       : "r"(static_cast<uint32_t>(pred)), "r"(nthreads)
       : "memory");
   return r != 0;
+}
+
+__device__ __forceinline__ void mbar_arrive_n(uint32_t bar, uint32_t n) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+               "r"(n)
+               : "memory");
 }
 
 __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
@@ -233,7 +245,6 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
   };
   auto qraw = [&](int s) { return base_u + C::OFF_QRAW + s * C::QRAW_BYTES; };
   const uint32_t qfrag = base_u + C::OFF_QFRAG;
-  float* comb = reinterpret_cast<float*>(base + C::OFF_COMB);
   float* ml = reinterpret_cast<float*>(base + C::OFF_ML);
   volatile UnitDesc* desc =
       reinterpret_cast<volatile UnitDesc*>(base + C::OFF_DESC);
@@ -830,7 +841,8 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(empty(s));
+      // the unit's last stage stays held: the epilogue merges in it
+      if (lane == 0 && jt + 1 < n_tiles) mbar_arrive(empty(s));
     }
     if constexpr (!KV8) {
       // the unit's Q slot and descriptor are no longer read
@@ -843,9 +855,14 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
     lB += __shfl_xor_sync(0xffffffffu, lB, 1);
     lB += __shfl_xor_sync(0xffffffffu, lB, 2);
 
-    // ---- epilogue: warps 1.. hand their states to warp 0
+    // ---- epilogue: warps 1.. hand their states to warp 0 through the
+    // held stage of the unit's last tile (a unit without tiles has nothing
+    // to merge: every warp's state is empty)
     if (bar_or(C::CT, aborted || *abort_flag)) return;
-    if (warp > 0) {
+    const int held = (it + STAGES - 1) % STAGES;
+    float* comb = reinterpret_cast<float*>(base + (tile_k(held) - base_u));
+    const int nother = n_tiles > 0 ? NCW - 1 : 0;
+    if (warp > 0 && nother > 0) {
       float* cw = comb + (warp - 1) * 16 * C::CST;
       float* mw = ml + (warp - 1) * 32;
       if (c4 == 0) {
@@ -878,8 +895,9 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
               make_float2(o[dn][2], o[dn][3]);
         }
       }
+      fence_proxy_async();   // the producer's TMA rewrites this stage later
     }
-    asm volatile("bar.sync 1, %0;" ::"n"(C::CT) : "memory");
+    if (nother > 0) asm volatile("bar.sync 1, %0;" ::"n"(C::CT) : "memory");
     if (warp != 0) continue;
 
     // warp 0: merge, normalise, write the output or the piece's partial
@@ -890,15 +908,19 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
       const float m_own = h ? mB : mA, l_own = h ? lB : lA;
       float M = m_own;
 #pragma unroll
-      for (int w = 0; w < NCW - 1; ++w) M = fmaxf(M, ml[w * 32 + r * 2]);
+      for (int w = 0; w < NCW - 1; ++w)
+        if (w < nother) M = fmaxf(M, ml[w * 32 + r * 2]);
       const float mb = (M == -INFINITY) ? 0.f : M;
       const float f_own = ex2(m_own - mb);
       float fw[NCW - 1];
       float lsum = f_own * l_own;
 #pragma unroll
       for (int w = 0; w < NCW - 1; ++w) {
-        fw[w] = ex2(ml[w * 32 + r * 2] - mb);
-        lsum += fw[w] * ml[w * 32 + r * 2 + 1];
+        fw[w] = 0.f;
+        if (w < nother) {
+          fw[w] = ex2(ml[w * 32 + r * 2] - mb);
+          lsum += fw[w] * ml[w * 32 + r * 2 + 1];
+        }
       }
       const int tok = q0 + r / G, hq = g * G + r % G;
       float inv, lse;   // a sink enters once: here, or in the fold
@@ -921,6 +943,7 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
               v[4 * e + j] = f_own * o[dc * 4 + j][2 * h + e];
 #pragma unroll
           for (int w = 0; w < NCW - 1; ++w) {
+            if (w >= nother) break;
             const float* src = comb + (w * 16 + r) * C::CST + col;
             const float4 x0 = *reinterpret_cast<const float4*>(src);
             const float4 x1 = *reinterpret_cast<const float4*>(src + 4);
@@ -956,6 +979,7 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
           float v0 = f_own * o[dn][2 * h], v1 = f_own * o[dn][2 * h + 1];
 #pragma unroll
           for (int w = 0; w < NCW - 1; ++w) {
+            if (w >= nother) break;
             const float2 x = *reinterpret_cast<const float2*>(
                 comb + (w * 16 + r) * C::CST + col);
             v0 += fw[w] * x.x;
@@ -976,6 +1000,12 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
           p.part_lse[static_cast<int64_t>(pslot) * 16 + r] = lse;
         }
       }
+    }
+    if (nother > 0) {
+      // the held stage goes back to the producer (for all NCW warps)
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_n(empty(held), NCW);
     }
   }
 }
@@ -1032,17 +1062,25 @@ __global__ void __launch_bounds__(128) fold_kernel(const AttnParams p,
   }
 }
 
+// Ring depth per configuration: two CTAs per SM, each holding about 96 KB
+// of K/V in flight (D = 256: 64 KB).
 #ifndef PKV_DSK_D64_STAGES
-#define PKV_DSK_D64_STAGES 4
+#define PKV_DSK_D64_STAGES 6
 #endif
 #ifndef PKV_DSK_D128_STAGES
-#define PKV_DSK_D128_STAGES 2
+#define PKV_DSK_D128_STAGES 3
 #endif
 #ifndef PKV_DSK_D256_STAGES
 #define PKV_DSK_D256_STAGES 2
 #endif
-#ifndef PKV_DSK_FP8_STAGES
-#define PKV_DSK_FP8_STAGES 4
+#ifndef PKV_DSK_FP8_D128_KT
+#define PKV_DSK_FP8_D128_KT 128
+#endif
+#ifndef PKV_DSK_FP8_D128_STAGES
+#define PKV_DSK_FP8_D128_STAGES 3
+#endif
+#ifndef PKV_DSK_FP8_D256_STAGES
+#define PKV_DSK_FP8_D256_STAGES 4
 #endif
 
 // Per instantiation: the shared-memory opt-in done on which devices, and
@@ -1088,8 +1126,11 @@ template <typename T, bool KV8, typename F>
 cudaError_t with_cfg(int D, F&& f) {
   if constexpr (KV8) {
     switch (D) {
-      case 128: return f(Inst<T, 128, 4, 64, PKV_DSK_FP8_STAGES, true>{});
-      case 256: return f(Inst<T, 256, 2, 32, PKV_DSK_FP8_STAGES, true>{});
+      case 128:
+        return f(Inst<T, 128, 4, PKV_DSK_FP8_D128_KT, PKV_DSK_FP8_D128_STAGES,
+                      true>{});
+      case 256:
+        return f(Inst<T, 256, 2, 32, PKV_DSK_FP8_D256_STAGES, true>{});
       default: return cudaErrorInvalidValue;
     }
   } else {
@@ -1149,22 +1190,22 @@ cudaError_t launch_decode_attn_sk(const AttnParams& a, int D, bool bf16,
   p.sk_marks = reinterpret_cast<int2*>(
       ws + a256(static_cast<size_t>(2) * ctas * 16 * D * 4) +
       a256(static_cast<size_t>(2) * ctas * 16 * 4));
-  const int KT = D == 256 ? 32 : 64;
-  int RB = 16;
-  while (RB * 2 <= KT && p.BS % (RB * 2) == 0) RB *= 2;
-  if (p.cu_k) RB = KT;    // non-paged: a box may start on any row
-  p.rb = RB;
-  p.kv_order_hnd = p.c_sh > p.c_sr ? 1 : 0;
-  CUtensorMap mk, mv;
-  if (!make_kv_map_ex(&mk, p.kc, kv8 ? 0 : (bf16 ? 2 : 1), D, p.BS, p.Hkv,
-                      p.num_blocks, p.c_sb, p.c_sr, p.c_sh, RB,
-                      p.kv_order_hnd) ||
-      !make_kv_map_ex(&mv, p.vc, kv8 ? 0 : (bf16 ? 2 : 1), D, p.BS, p.Hkv,
-                      p.num_blocks, p.c_sb, p.c_sr, p.c_sh, RB,
-                      p.kv_order_hnd))
-    return cudaErrorInvalidValue;
   cudaError_t e = dsk::dispatch(bf16, kv8, D, [&](auto inst) {
-    return decltype(inst)::launch(p, mk, mv, ctas, stream);
+    using I = decltype(inst);
+    const int KT = I::C::KTILE;
+    int RB = 16;
+    while (RB * 2 <= KT && p.BS % (RB * 2) == 0) RB *= 2;
+    if (p.cu_k) RB = KT;    // non-paged: a box may start on any row
+    p.rb = RB;
+    p.kv_order_hnd = p.c_sh > p.c_sr ? 1 : 0;
+    CUtensorMap mk, mv;
+    const int elem = kv8 ? 0 : (bf16 ? 2 : 1);
+    if (!make_kv_map_ex(&mk, p.kc, elem, D, p.BS, p.Hkv, p.num_blocks,
+                        p.c_sb, p.c_sr, p.c_sh, RB, p.kv_order_hnd) ||
+        !make_kv_map_ex(&mv, p.vc, elem, D, p.BS, p.Hkv, p.num_blocks,
+                        p.c_sb, p.c_sr, p.c_sh, RB, p.kv_order_hnd))
+      return cudaErrorInvalidValue;
+    return I::launch(p, mk, mv, ctas, stream);
   });
   if (e != cudaSuccess || ctas < 2) return e;
   note_launch();
