@@ -53,7 +53,10 @@ typedef enum {
   PKV_ERR_BAD_INDEX = 5,            /* a kernel met an out-of-range block id or
                                        slot and skipped it (see
                                        pkv_check_device_errors)               */
-  PKV_ERR_TIMEOUT = 6               /* reserved: a bounded device wait gave up */
+  PKV_ERR_TIMEOUT = 6               /* a kernel's bounded wait for data ran
+                                       out; its CTA drained its copies and
+                                       stopped without writing (see
+                                       pkv_check_device_errors)               */
 } pkv_status;
 
 typedef enum { PKV_F16 = 0, PKV_BF16 = 1, PKV_F32 = 2 } pkv_dtype;
@@ -407,9 +410,20 @@ PKV_API int pkv_use_cascade_attention(
 
 /*
  * pkv_check_device_errors -- synchronise `stream`, then read and clear the
- * library's device error word.  Returns PKV_OK, or PKV_ERR_BAD_INDEX when a
- * kernel since the last check met an out-of-range block id or slot (the
- * access was skipped, never performed).  Not for use inside graph capture.
+ * library's device error word (one per device; kernels OR bits into it and
+ * never trap).  Returns, by priority:
+ *   PKV_ERR_TIMEOUT    a kernel's bounded wait for its data ran out (about
+ *                      2 s; the CTA drained its copies, freed what it held
+ *                      and returned without writing its outputs);
+ *   PKV_ERR_BAD_INDEX  a kernel met an out-of-range block id or slot (the
+ *                      access was skipped, never performed), a key range
+ *                      past the table row, or a request with more queries
+ *                      than the call's max_seqlen_q (not computed);
+ *   PKV_ERR_CUDA       an internal launch fault was caught (misaligned
+ *                      shared memory);
+ *   PKV_OK             nothing since the last check.
+ * The message (pkv_last_error) lists every cause seen.  Not for use inside
+ * graph capture.
  */
 PKV_API pkv_status pkv_check_device_errors(pkv_stream_t stream);
 
@@ -429,25 +443,29 @@ PKV_API pkv_status pkv_set_prefill_kernel(int which);
 /*
  * Which kernel serves decode-class requests (at most 16 packed query rows
  * per KV head):
- *   PKV_DECODE_PERSISTENT (default)  one wave of CTAs, each streaming an
- *       equal share of the batch's key tiles (a request's keys may be cut
- *       between CTAs; the pieces are merged by LSE).  Used for calls that
- *       leave the split to the library (num_splits = 0, no fixed split
- *       size) when the workspace holds its scratch (see
- *       pkv_paged_attention_workspace_size); 16-bit caches with head_size
- *       64/128/256 and fp8 caches with head_size 128/256.  Other calls fall
- *       back to the kernels below.
+ *   PKV_DECODE_PERSISTENT  one wave of CTAs, each streaming an equal share
+ *       of the batch's key tiles (a request's keys may be cut between CTAs;
+ *       the pieces are merged by LSE).  Taken by calls that leave the split
+ *       to the library (num_splits = 0, no fixed split size) when the
+ *       workspace holds its scratch (see pkv_paged_attention_workspace_size);
+ *       16-bit caches with head_size 64/128/256 and fp8 caches with
+ *       head_size 128/256.  Other calls fall back to the kernels below.
  *   PKV_DECODE_TMA  one CTA per (request, KV head, split), K/V pages moved
  *       by a TMA producer warp (16-bit caches).
  *   PKV_DECODE_CP_ASYNC  one CTA per (request, KV head, split), pages
- *       gathered with 16-byte cp.async (always used for fp8 caches the
- *       persistent kernel does not take).
- * A process-wide diagnostic switch for A/B comparison; all give the same
- * result within rounding.  Returns PKV_ERR_INVALID_ARG for other values.
+ *       gathered with 16-byte cp.async (fp8 caches the persistent kernel
+ *       does not take use it always).
+ *   PKV_DECODE_AUTO (default)  the persistent kernel for fp8 caches and
+ *       for calls with at least two waves of long (request, KV head) units
+ *       (batch * num_kv_heads >= 2 * 3 * SMs, and a key range of at least
+ *       2048 by max_seqlen_k and the window), else PKV_DECODE_TMA.
+ * A process-wide switch for A/B comparison; all give the same result
+ * within rounding.  Returns PKV_ERR_INVALID_ARG for other values.
  */
 #define PKV_DECODE_TMA 0
 #define PKV_DECODE_CP_ASYNC 1
 #define PKV_DECODE_PERSISTENT 2
+#define PKV_DECODE_AUTO 3
 PKV_API pkv_status pkv_set_decode_kernel(int which);
 
 /*

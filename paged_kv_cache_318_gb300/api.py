@@ -32,6 +32,7 @@ PKV_ERR_UNSUPPORTED = 2
 PKV_ERR_WORKSPACE_TOO_SMALL = 3
 PKV_ERR_CUDA = 4
 PKV_ERR_BAD_INDEX = 5
+PKV_ERR_TIMEOUT = 6
 
 _DT = {torch.float16: 0, torch.bfloat16: 1, torch.float32: 2}
 
@@ -169,11 +170,12 @@ def set_prefill_kernel(which: int):
 DECODE_TMA = 0
 DECODE_CP_ASYNC = 1
 DECODE_PERSISTENT = 2
+DECODE_AUTO = 3
 
 
 def set_decode_kernel(which: int):
-    """Choose the decode kernel: DECODE_PERSISTENT (default), DECODE_TMA or
-    DECODE_CP_ASYNC."""
+    """Choose the decode kernel: DECODE_AUTO (default), DECODE_PERSISTENT,
+    DECODE_TMA or DECODE_CP_ASYNC."""
     _check(load_library().pkv_set_decode_kernel(int(which)))
 
 

@@ -10,14 +10,17 @@
 //
 // Work order.  The decode-class requests (q_len * G <= 16 packed query rows
 // per KV head) form a sequence of units u = b * Hkv + g (request b, KV head
-// g), each a run of KT-key tiles over the unit's admissible key range.  The
-// launch is one wave of C CTAs.  CTA c takes tiles [c N / C, (c+1) N / C)
-// of the concatenated sequence (N tiles in all), so every CTA moves the
-// same number of K/V bytes whatever the spread of the request lengths
-// (with one CTA per unit, the longest units of the last wave set the
-// kernel's time).  A unit inside one CTA's range is finished there.  A unit
-// that a range boundary cuts leaves one partial state (O normalised, LSE)
-// per piece in the workspace, and fold_kernel merges the pieces by LSE.
+// g), each a run of KT-key tiles over the unit's admissible key range: N
+// tiles in all.  The launch is one wave of C CTAs, and the sequence is cut
+// into C equal chunks, one per CTA, so every CTA moves the same number of
+// K/V bytes whatever the spread of the request lengths (with one CTA per
+// unit, the longest units of the last wave set the kernel's time).  A unit
+// inside one chunk is finished there.  A unit that a chunk boundary cuts
+// leaves one partial state (O normalised, LSE) per piece in the workspace,
+// and fold_kernel merges the pieces by LSE.  (Measured on GB300: some SM
+// groups stream K/V several percent slower than others, run after run, so
+// equal chunks end a few microseconds apart; chunks dealt at run time from
+// a ticket counter cost more in per-chunk start-up than they recovered.)
 //
 // CTA roles (NCW consumer warps + one producer warp):
 //   producer   walks the CTA's units in order.  For each it publishes a
@@ -29,9 +32,11 @@
 //              between units.
 //   consumers  each own KT / NCW keys of every tile: S = Q K^T, online
 //              softmax (base 2), O += P V on mma.sync m16n8k16.  At the end
-//              of a unit warps 1.. NCW-1 hand their states to warp 0
-//              through shared memory and warp 0 writes the output (or the
-//              piece's partial state).
+//              of a unit the warps' states meet in the ring stage of the
+//              unit's last tile, which stays held until they are merged,
+//              and each warp normalises and writes a slice of the columns
+//              (with D = 256, warp 0 merges all of them); the output, or
+//              the piece's partial state.
 //
 // E4M3 caches.  The ring holds the codes (one byte per element, 128-column
 // boxes).  The consumers convert them to f16 in registers with
@@ -62,6 +67,9 @@ namespace pkv {
 namespace dsk {
 
 constexpr int kMaxDevices = 64;
+// Requests whose tile prefix a CTA keeps in shared memory (it locates its
+// chunk there); larger batches locate it with one scan over the requests.
+constexpr int kMaxPrefixReqs = 512;
 
 template <int D, int NCW, int KT, int STAGES, bool KV8>
 struct Cfg {
@@ -75,22 +83,21 @@ struct Cfg {
   static constexpr int ROW_BYTES = D * 2;       // one 16-bit Q row
   static constexpr int CB_BYTES = KT * 128;     // one column block of a tile
   static constexpr int TILE_BYTES = NCB * CB_BYTES;
-  static constexpr int RING_BYTES = STAGES * 2 * TILE_BYTES;
+  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+  static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
   static constexpr int QRAW_BYTES = 16 * ROW_BYTES;
   static constexpr int QFRAG_BYTES = KV8 ? (D / 16) * 32 * 16 : 0;
-  // The warps' states meet in the ring stage of the unit's last tile (held
-  // until warp 0 has merged them).  Row stride: float4 stores (fp8) want a
-  // 16-byte row shift, float2 stores (16-bit) a 32-byte one, for
-  // conflict-free shared stores, when the stage has room for it.
-  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-  static constexpr int CST_PAD = D + (KV8 ? 4 : 8);
-  static constexpr int CST =
-      (NCW - 1) * 16 * CST_PAD * 4 <= STAGE_BYTES ? CST_PAD : D;
-  static constexpr int ML_BYTES = (NCW - 1) * 16 * 2 * 4;
+  // The warps' states meet in the held stage of the unit's last tile: all
+  // NCW of them when they fit (each warp then merges a column slice), else
+  // those of warps 1.. (warp 0 merges with its own registers).
+  static constexpr bool ALL_MERGE = NCW * 16 * D * 4 <= STAGE_BYTES;
+  static constexpr int ML_BYTES = NCW * 16 * 2 * 4;
+  static constexpr int PRE_BYTES = (kMaxPrefixReqs + 2) * 4;
   static constexpr int OFF_QRAW = RING_BYTES;
   static constexpr int OFF_QFRAG = OFF_QRAW + 2 * QRAW_BYTES;
   static constexpr int OFF_ML = OFF_QFRAG + QFRAG_BYTES;
-  static constexpr int OFF_DESC = OFF_ML + ML_BYTES;        // 2 x 64 bytes
+  static constexpr int OFF_PRE = OFF_ML + ML_BYTES;
+  static constexpr int OFF_DESC = OFF_PRE + PRE_BYTES;      // 2 x 64 bytes
   static constexpr int OFF_MISC = OFF_DESC + 128;           // 256 bytes
   static constexpr int OFF_BAR = OFF_MISC + 256;
   static constexpr int BAR_BYTES = (3 * STAGES + 4) * 8;
@@ -99,11 +106,21 @@ struct Cfg {
   static_assert(NKT == 2 || NKT == 4, "ldmatrix grouping of K");
   static_assert(D % BOXC == 0, "whole TMA boxes per row");
   static_assert(CB_BYTES % 1024 == 0, "128-byte swizzle atoms");
-  static_assert(NCW >= 2, "warp 0 merges the others' states");
-  static_assert((NCW - 1) * 16 * CST * 4 <= STAGE_BYTES,
+  static_assert(NCW >= 2, "several consumer warps");
+  static_assert(ALL_MERGE || (NCW - 1) * 16 * D * 4 <= STAGE_BYTES,
                 "the warps' states fit in one ring stage");
+  static_assert((D / NCW) % 4 == 0, "column slices of whole float4s");
+  static_assert(OFF_PRE % 8 == 0 && OFF_MISC % 8 == 0, "alignment");
   static constexpr int KTILE = KT;
 };
+
+// Index of (row r, column col) of one warp's 16 x D state in the held
+// stage; the column is XOR-swizzled by the row for conflict-free float2
+// (16-bit path) and float4 (fp8 path) stores.
+template <bool KV8, int D>
+__device__ __forceinline__ int cidx(int r, int col) {
+  return r * D + (col ^ ((r & 7) << (KV8 ? 2 : 3)));
+}
 
 // One unit piece as the producer hands it to the consumers (64 bytes).
 struct UnitDesc {
@@ -123,19 +140,25 @@ struct ReqInfo {
 
 template <int KT>
 __device__ __forceinline__ ReqInfo req_info(const AttnParams& p, int b,
-                                            bool flag_table) {
+                                            bool flag) {
   ReqInfo r{};
   r.q0 = p.cu_q[b];
   r.q_len = min(p.cu_q[b + 1] - r.q0, p.total_q - r.q0);
   if (r.q0 < 0 || r.q_len <= 0) return r;
   r.rows = r.q_len * p.G;
   if (r.rows < p.min_rows || r.rows > p.max_rows || r.rows > 16) return r;
+  if (r.rows > p.sk_rows) {
+    // more query rows than the call's max_seqlen_q allows (the partial
+    // slots are sized by it): not computed, and reported
+    if (flag) atomicOr(p.err, kErrQueryLen);
+    return r;
+  }
   r.koff = p.cu_k ? p.cu_k[b] : 0;
   r.L = p.cu_k ? p.cu_k[b + 1] - r.koff : p.seqused_k[b];
   // rows past the table (or, non-paged, past the K/V tensor) are not read
   const int L_tab = p.cu_k ? (r.koff < 0 ? 0 : max(0, min(r.L, p.total_k - r.koff)))
                            : min(r.L, p.max_blocks * p.BS);
-  if (flag_table && L_tab < r.L) atomicOr(p.err, kErrBadTable);
+  if (flag && L_tab < r.L) atomicOr(p.err, kErrBadTable);
   int kmin, kmax;
   key_range(r.L, r.q_len, 0, r.q_len - 1, p.causal, p.wl, p.wr, kmin, kmax);
   r.lo = kmin;
@@ -239,13 +262,14 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
   auto empty = [&](int s) { return bar0 + 8 * (2 * STAGES + s); };
   auto ufull = [&](int s) { return bar0 + 8 * (3 * STAGES + s); };
   auto uempty = [&](int s) { return bar0 + 8 * (3 * STAGES + 2 + s); };
-  auto tile_k = [&](int s) { return ring + s * 2 * C::TILE_BYTES; };
+  auto tile_k = [&](int s) { return ring + s * C::STAGE_BYTES; };
   auto tile_v = [&](int s) {
-    return ring + s * 2 * C::TILE_BYTES + C::TILE_BYTES;
+    return ring + s * C::STAGE_BYTES + C::TILE_BYTES;
   };
   auto qraw = [&](int s) { return base_u + C::OFF_QRAW + s * C::QRAW_BYTES; };
   const uint32_t qfrag = base_u + C::OFF_QFRAG;
   float* ml = reinterpret_cast<float*>(base + C::OFF_ML);
+  int* pre = reinterpret_cast<int*>(base + C::OFF_PRE);
   volatile UnitDesc* desc =
       reinterpret_cast<volatile UnitDesc*>(base + C::OFF_DESC);
   int* misc = reinterpret_cast<int*>(base + C::OFF_MISC);
@@ -270,8 +294,8 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
 
-  // ---- this CTA's share of the tile sequence (every CTA derives the same
-  // prefix over the requests; thread t scans a contiguous run of them)
+  // ---- the tile sequence (every CTA derives the same prefix over the
+  // requests; thread t scans a contiguous run of them)
   const int B = p.batch;
   const int per = (B + C::NT - 1) / C::NT;
   const int b_lo = min(B, tid * per), b_hi = min(B, b_lo + per);
@@ -291,49 +315,52 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
     if (w < warp) excl += scan[w];
     N += scan[w];
   }
-  const int C_all = gridDim.x;
-  const long long C_eff = max(1LL, min(static_cast<long long>(C_all), N / 2));
-  long long T0 = 0, T1 = 0;
-  if (c < C_eff) {
-    T0 = c * N / C_eff;
-    T1 = (c + 1) * N / C_eff;
-  }
-  // the units holding tiles T0 and T1 - 1
-  if (T0 < T1 && mine > 0) {
+  // the per-request prefix in shared memory (small batches): any CTA can
+  // then locate any chunk
+  const bool table = B <= kMaxPrefixReqs && N < (1LL << 30);
+  if (table) {
     long long acc = excl;
     for (int b = b_lo; b < b_hi; ++b) {
-      const int n = req_info<KT>(p, b, false).n;
-      const long long t = static_cast<long long>(n) * Hkv;
-      if (n > 0) {
-        if (T0 >= acc && T0 < acc + t) {
-          const long long rel = T0 - acc;
-          start[0] = b;
-          start[1] = static_cast<int>(rel / n);
-          start[2] = static_cast<int>(rel % n);
+      pre[b] = static_cast<int>(acc);
+      acc += static_cast<long long>(req_info<KT>(p, b, false).n) * Hkv;
+    }
+    if (tid == 0) pre[B] = static_cast<int>(N);
+  }
+
+  // ---- chunks: Cs equal ones, one per CTA, at least two tiles each (every
+  // chunk holds a tile: the fold follows a unit's pieces through
+  // consecutive chunks)
+  const int C_all = gridDim.x;
+  const long long Cs = max(1LL, min(static_cast<long long>(C_all), N / 2));
+  auto bound = [&](long long k) -> long long { return k * N / Cs; };
+  if (c >= Cs && tid == 0) p.sk_marks[c] = make_int2(-1, -1);
+  if (!table && c < Cs) {
+    // the CTA's static chunk located by the thread whose run holds it
+    const long long T0 = bound(c), T1 = bound(c + 1);
+    if (T0 < T1 && mine > 0) {
+      long long acc = excl;
+      for (int b = b_lo; b < b_hi; ++b) {
+        const int n = req_info<KT>(p, b, false).n;
+        const long long t = static_cast<long long>(n) * Hkv;
+        if (n > 0) {
+          if (T0 >= acc && T0 < acc + t) {
+            start[0] = b;
+            start[1] = static_cast<int>((T0 - acc) / n);
+            start[2] = static_cast<int>((T0 - acc) % n);
+            start[7] = n;
+          }
+          if (T1 - 1 >= acc && T1 - 1 < acc + t) {
+            start[3] = b;
+            start[4] = static_cast<int>((T1 - 1 - acc) / n);
+            start[5] = static_cast<int>((T1 - 1 - acc) % n);
+            start[6] = n;
+          }
         }
-        if (T1 - 1 >= acc && T1 - 1 < acc + t) {
-          const long long rel = T1 - 1 - acc;
-          start[3] = b;
-          start[4] = static_cast<int>(rel / n);
-          start[5] = static_cast<int>(rel % n);
-          start[6] = n;
-        }
+        acc += t;
       }
-      acc += t;
     }
   }
   __syncthreads();
-  // pieces this CTA leaves for the fold: the unit it starts inside (head,
-  // slot 2c) and the unit it starts that runs past its range (tail, slot
-  // 2c + 1)
-  int head_u = -1, tail_u = -1;
-  if (T0 < T1) {
-    const int u0 = start[0] * Hkv + start[1];
-    const int u1 = start[3] * Hkv + start[4];
-    if (start[2] > 0) head_u = u0;
-    if (start[5] + 1 < start[6] && !(u1 == u0 && start[2] > 0)) tail_u = u1;
-  }
-  if (tid == 0) p.sk_marks[c] = make_int2(head_u, tail_u);
 
   if (warp == NCW) {
     // ------------------------------------------------------------ producer
@@ -341,141 +368,184 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
     const int RB = p.rb;
     const int nb_max = KT / RB;
     const T* Q = static_cast<const T*>(p.q);
-    int b = start[0], g = start[1], t = start[2];
-    long long pos = T0;
+    // (request, KV head, tile) of tile position P of the sequence
+    auto locate = [&](long long P, int& b, int& g, int& t, int& n) {
+      int lo = 0, hi = B;          // pre[lo] <= P < pre[hi]
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (pre[mid] <= P) lo = mid; else hi = mid;
+      }
+      b = lo;
+      n = (pre[lo + 1] - pre[lo]) / Hkv;
+      const int rel = static_cast<int>(P - pre[lo]);
+      g = rel / n;
+      t = rel - g * n;
+    };
     int k = 0, it = 0;
     bool stop = false;
-    ReqInfo ri{};
-    if (pos < T1) ri = req_info<KT>(p, b, false);
-    for (;;) {
-      const int slot = k & 1;
-      if (k >= 2) {
-        int ok = 1;
-        if (lane == 0)
-          ok = mbar_wait(uempty(slot), ((k >> 1) - 1) & 1, abort_flag, p.err);
-        if (!__shfl_sync(0xffffffffu, ok, 0)) {
-          stop = true;
-          break;
+    const long long chunk = c;
+    if (c < Cs) {
+      const long long T0 = bound(chunk), T1 = bound(chunk + 1);
+      int b, g, t, n0, b1, g1, t1, n1;
+      if (table) {
+        locate(T0, b, g, t, n0);
+        locate(T1 - 1, b1, g1, t1, n1);
+      } else {
+        b = start[0]; g = start[1]; t = start[2]; n0 = start[7];
+        b1 = start[3]; g1 = start[4]; t1 = start[5]; n1 = start[6];
+      }
+      (void)n0;
+      // pieces left for the fold: the unit the chunk starts inside (head,
+      // slot 2 chunk) and the unit it starts that runs past its end (tail,
+      // slot 2 chunk + 1)
+      const int u0 = b * Hkv + g, u1 = b1 * Hkv + g1;
+      const int head_u = t > 0 ? u0 : -1;
+      const int tail_u = (t1 + 1 < n1 && !(u1 == u0 && t > 0)) ? u1 : -1;
+      if (lane == 0) p.sk_marks[chunk] = make_int2(head_u, tail_u);
+
+      long long pos = T0;
+      ReqInfo ri = req_info<KT>(p, b, false);
+      while (pos < T1) {
+        const int slot = k & 1;
+        if (k >= 2) {
+          int ok = 1;
+          if (lane == 0)
+            ok = mbar_wait(uempty(slot), ((k >> 1) - 1) & 1, abort_flag,
+                           p.err);
+          if (!__shfl_sync(0xffffffffu, ok, 0)) {
+            stop = true;
+            break;
+          }
+        }
+        const long long len =
+            min(static_cast<long long>(ri.n - t), T1 - pos);
+        int pslot = -1;
+        if (pos == T0 && head_u >= 0)
+          pslot = 2 * static_cast<int>(chunk);
+        else if (pos + len == T1 && tail_u >= 0)
+          pslot = 2 * static_cast<int>(chunk) + 1;
+        const int j_beg = t;
+        const int j_end = min(t + static_cast<int>(len), ri.n_real);
+        if (lane == 0) {
+          volatile UnitDesc& d = desc[slot];
+          d.b = b;
+          d.g = g;
+          d.q0 = ri.q0;
+          d.q_len = ri.q_len;
+          d.rows = ri.rows;
+          d.L = ri.L;
+          d.lo = ri.lo;
+          d.hi = ri.hi;
+          d.kt0 = ri.kt0;
+          d.t_beg = j_beg;
+          d.n_tiles = max(0, j_end - j_beg);
+          d.slot = pslot;
+          d.end = 0;
+        }
+        // the unit's 16 packed query rows (zeros past `rows`)
+        for (int i = lane; i < 16 * CPR; i += 32) {
+          const int r = i / CPR, ch = i - (i / CPR) * CPR;
+          const bool ok = r < ri.rows;
+          const T* src = Q;
+          if (ok)
+            src = Q + static_cast<int64_t>(ri.q0 + r / G) * p.q_st +
+                  static_cast<int64_t>(g * G + r % G) * p.q_sh + ch * 8;
+          cp_async_16(qraw(slot) + swz<C::ROW_BYTES>(r, ch), src,
+                      ok ? 16 : 0);
+        }
+        if (lane == 0) mbar_arrive(ufull(slot));
+        cp_async_mbar_arrive(ufull(slot));
+
+        // the piece's K and V tiles
+        const int32_t* bt =
+            p.cu_k ? nullptr
+                   : p.block_table + static_cast<int64_t>(b) * p.bt_stride;
+        auto fetch = [&](int j) -> int {          // page id of box `lane`
+          const int k0 = ri.kt0 + j * KT + lane * RB;
+          if (j >= j_end || lane >= nb_max || k0 >= ri.hi || !bt) return 0;
+          const int blk = __ldg(bt + k0 / p.BS);
+          if (blk < 0 || blk >= p.num_blocks) {
+            atomicOr(p.err, kErrBadBlock);
+            return -1;
+          }
+          return blk;
+        };
+        int cur = fetch(j_beg);
+        for (int j = j_beg; j < j_end; ++j) {
+          const int nxt = fetch(j + 1);
+          const int s = it % STAGES;
+          const int kt = ri.kt0 + j * KT;
+          int nbox = (ri.hi - kt + RB - 1) / RB;
+          if (nbox > nb_max) nbox = nb_max;
+          const unsigned bad =
+              __ballot_sync(0xffffffffu, lane < nbox && cur < 0);
+          int halt = 0;
+          if (lane == 0) {
+            if (it >= STAGES &&
+                !mbar_wait(empty(s), ((it / STAGES) - 1) & 1, abort_flag,
+                           p.err)) {
+              halt = 1;
+            } else {
+              bad_boxes[s] = bad;
+              const uint32_t bytes =
+                  (nbox - __popc(bad)) * C::NCB * RB * 128;
+              mbar_expect_tx(full_k(s), bytes);
+              mbar_expect_tx(full_v(s), bytes);
+            }
+          }
+          if (__shfl_sync(0xffffffffu, halt, 0)) {
+            stop = true;
+            break;
+          }
+          if (lane < nbox && cur >= 0) {
+            const int k0 = kt + lane * RB;
+            const int row = p.cu_k ? ri.koff + k0 : k0 % p.BS;
+#pragma unroll
+            for (int cb = 0; cb < C::NCB; ++cb) {
+              const uint32_t dk =
+                  tile_k(s) + cb * C::CB_BYTES + lane * RB * 128;
+              const uint32_t dv =
+                  tile_v(s) + cb * C::CB_BYTES + lane * RB * 128;
+              if (p.kv_order_hnd) {
+                tma_load_4d(dk, &tm_k, cb * C::BOXC, row, g, cur, full_k(s));
+                tma_load_4d(dv, &tm_v, cb * C::BOXC, row, g, cur, full_v(s));
+              } else {
+                tma_load_4d(dk, &tm_k, cb * C::BOXC, g, row, cur, full_k(s));
+                tma_load_4d(dv, &tm_v, cb * C::BOXC, g, row, cur, full_v(s));
+              }
+            }
+          }
+          ++it;
+          cur = nxt;
+        }
+        if (stop) break;
+        pos += len;
+        ++k;
+        if (pos < T1) {
+          t = 0;
+          if (++g == Hkv) {
+            g = 0;
+            do {
+              ++b;
+              ri = req_info<KT>(p, b, false);
+            } while (ri.n == 0 && b + 1 < B);
+            if (ri.n == 0) pos = T1;    // (unreachable: the scan saw tiles)
+          }
         }
       }
-      if (pos >= T1) {
+    }
+    if (!stop) {
+      // no more units: publish the end of the sequence
+      const int slot = k & 1;
+      int ok = 1;
+      if (k >= 2 && lane == 0)
+        ok = mbar_wait(uempty(slot), ((k >> 1) - 1) & 1, abort_flag, p.err);
+      if (__shfl_sync(0xffffffffu, ok, 0)) {
         if (lane == 0) {
           desc[slot].end = 1;
           mbar_arrive(ufull(slot));
         }
         cp_async_mbar_arrive(ufull(slot));
-        break;
-      }
-      const long long len =
-          min(static_cast<long long>(ri.n - t), T1 - pos);
-      int pslot = -1;
-      if (pos == T0 && head_u >= 0)
-        pslot = 2 * c;
-      else if (pos + len == T1 && tail_u >= 0)
-        pslot = 2 * c + 1;
-      const int j_beg = t;
-      const int j_end = min(t + static_cast<int>(len), ri.n_real);
-      if (lane == 0) {
-        volatile UnitDesc& d = desc[slot];
-        d.b = b;
-        d.g = g;
-        d.q0 = ri.q0;
-        d.q_len = ri.q_len;
-        d.rows = ri.rows;
-        d.L = ri.L;
-        d.lo = ri.lo;
-        d.hi = ri.hi;
-        d.kt0 = ri.kt0;
-        d.t_beg = j_beg;
-        d.n_tiles = max(0, j_end - j_beg);
-        d.slot = pslot;
-        d.end = 0;
-      }
-      // the unit's 16 packed query rows (zeros past `rows`)
-      for (int i = lane; i < 16 * CPR; i += 32) {
-        const int r = i / CPR, ch = i - (i / CPR) * CPR;
-        const bool ok = r < ri.rows;
-        const T* src = Q;
-        if (ok)
-          src = Q + static_cast<int64_t>(ri.q0 + r / G) * p.q_st +
-                static_cast<int64_t>(g * G + r % G) * p.q_sh + ch * 8;
-        cp_async_16(qraw(slot) + swz<C::ROW_BYTES>(r, ch), src, ok ? 16 : 0);
-      }
-      if (lane == 0) mbar_arrive(ufull(slot));
-      cp_async_mbar_arrive(ufull(slot));
-
-      // the piece's K and V tiles
-      const int32_t* bt =
-          p.cu_k ? nullptr
-                 : p.block_table + static_cast<int64_t>(b) * p.bt_stride;
-      auto fetch = [&](int j) -> int {            // page id of box `lane`
-        const int k0 = ri.kt0 + j * KT + lane * RB;
-        if (j >= j_end || lane >= nb_max || k0 >= ri.hi || !bt) return 0;
-        const int blk = __ldg(bt + k0 / p.BS);
-        if (blk < 0 || blk >= p.num_blocks) {
-          atomicOr(p.err, kErrBadBlock);
-          return -1;
-        }
-        return blk;
-      };
-      int cur = fetch(j_beg);
-      for (int j = j_beg; j < j_end; ++j) {
-        const int nxt = fetch(j + 1);
-        const int s = it % STAGES;
-        const int kt = ri.kt0 + j * KT;
-        int nbox = (ri.hi - kt + RB - 1) / RB;
-        if (nbox > nb_max) nbox = nb_max;
-        const unsigned bad =
-            __ballot_sync(0xffffffffu, lane < nbox && cur < 0);
-        int halt = 0;
-        if (lane == 0) {
-          if (it >= STAGES &&
-              !mbar_wait(empty(s), ((it / STAGES) - 1) & 1, abort_flag,
-                         p.err)) {
-            halt = 1;
-          } else {
-            bad_boxes[s] = bad;
-            const uint32_t bytes = (nbox - __popc(bad)) * C::NCB * RB * 128;
-            mbar_expect_tx(full_k(s), bytes);
-            mbar_expect_tx(full_v(s), bytes);
-          }
-        }
-        if (__shfl_sync(0xffffffffu, halt, 0)) {
-          stop = true;
-          break;
-        }
-        if (lane < nbox && cur >= 0) {
-          const int k0 = kt + lane * RB;
-          const int row = p.cu_k ? ri.koff + k0 : k0 % p.BS;
-#pragma unroll
-          for (int cb = 0; cb < C::NCB; ++cb) {
-            const uint32_t dk = tile_k(s) + cb * C::CB_BYTES + lane * RB * 128;
-            const uint32_t dv = tile_v(s) + cb * C::CB_BYTES + lane * RB * 128;
-            if (p.kv_order_hnd) {
-              tma_load_4d(dk, &tm_k, cb * C::BOXC, row, g, cur, full_k(s));
-              tma_load_4d(dv, &tm_v, cb * C::BOXC, row, g, cur, full_v(s));
-            } else {
-              tma_load_4d(dk, &tm_k, cb * C::BOXC, g, row, cur, full_k(s));
-              tma_load_4d(dv, &tm_v, cb * C::BOXC, g, row, cur, full_v(s));
-            }
-          }
-        }
-        ++it;
-        cur = nxt;
-      }
-      if (stop) break;
-      pos += len;
-      ++k;
-      if (pos < T1) {
-        t = 0;
-        if (++g == Hkv) {
-          g = 0;
-          do {
-            ++b;
-            ri = req_info<KT>(p, b, false);
-          } while (ri.n == 0 && b + 1 < B);
-          if (ri.n == 0) pos = T1;    // (unreachable: the scan saw tiles)
-        }
       }
     }
     if (lane == 0) {
@@ -486,7 +556,6 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
       }
     }
     cp_async_wait<0>();
-    (void)stop;
     return;
   }
 
@@ -855,33 +924,65 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
     lB += __shfl_xor_sync(0xffffffffu, lB, 1);
     lB += __shfl_xor_sync(0xffffffffu, lB, 2);
 
-    // ---- epilogue: warps 1.. hand their states to warp 0 through the
-    // held stage of the unit's last tile (a unit without tiles has nothing
-    // to merge: every warp's state is empty)
+    // ---- epilogue: the warps' states meet in the held stage of the unit's
+    // last tile (a unit without tiles has nothing to merge: every warp's
+    // state is empty and warp 0 writes the empty row)
     if (bar_or(C::CT, aborted || *abort_flag)) return;
     const int held = (it + STAGES - 1) % STAGES;
     float* comb = reinterpret_cast<float*>(base + (tile_k(held) - base_u));
-    const int nother = n_tiles > 0 ? NCW - 1 : 0;
-    if (warp > 0 && nother > 0) {
-      float* cw = comb + (warp - 1) * 16 * C::CST;
-      float* mw = ml + (warp - 1) * 32;
+    const float* sinks = pslot < 0 ? p.sinks : nullptr;  // once, here or in
+                                                         // the fold
+    auto store_row = [&](int r, int col, float4 v, float inv, float lse) {
+      const int tok = q0 + r / G, hq = g * G + r % G;
+      if (pslot < 0) {
+        T* dst = OUT + static_cast<int64_t>(tok) * p.o_st +
+                 static_cast<int64_t>(hq) * p.o_sh + col;
+        uint2 pk;
+        pk.x = pack2<T>(v.x * inv, v.y * inv);
+        pk.y = pack2<T>(v.z * inv, v.w * inv);
+        *reinterpret_cast<uint2*>(dst) = pk;
+        if (col == 0 && p.lse)
+          p.lse[static_cast<int64_t>(hq) * p.total_q + tok] = lse;
+      } else {
+        const int64_t sr = static_cast<int64_t>(pslot) * p.sk_rows + r;
+        *reinterpret_cast<float4*>(p.part_o + sr * D + col) =
+            make_float4(v.x * inv, v.y * inv, v.z * inv, v.w * inv);
+        if (col == 0) p.part_lse[sr] = lse;
+      }
+    };
+    if (n_tiles == 0) {
+      if (warp == 0) {
+        for (int i = lane; i < rows * (D / 4); i += 32) {
+          const int r = i / (D / 4), col = (i - r * (D / 4)) * 4;
+          float inv, lse;
+          finish_row(-INFINITY, 0.f, sinks, g * G + r % G, &inv, &lse);
+          store_row(r, col, make_float4(0.f, 0.f, 0.f, 0.f), 0.f, lse);
+        }
+      }
+      continue;
+    }
+    // this warp's state into the stage (all warps, or warps 1..)
+    const int wslot = C::ALL_MERGE ? warp : warp - 1;
+    if (wslot >= 0) {
+      float* cw = comb + wslot * 16 * D;
       if (c4 == 0) {
-        mw[rA * 2] = mA;
-        mw[rA * 2 + 1] = lA;
-        mw[rB * 2] = mB;
-        mw[rB * 2 + 1] = lB;
+        ml[wslot * 32 + rA * 2] = mA;
+        ml[wslot * 32 + rA * 2 + 1] = lA;
+        ml[wslot * 32 + rB * 2] = mB;
+        ml[wslot * 32 + rB * 2 + 1] = lB;
       }
       if constexpr (KV8) {
+        // o[4 dc + j][2 h + e] holds column 32 dc + 8 c4 + 4 e + j
 #pragma unroll
         for (int dc = 0; dc < D / 32; ++dc) {
           const int col = dc * 32 + 8 * c4;
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            float* dst = cw + (g8 + 8 * h) * C::CST + col;
-            *reinterpret_cast<float4*>(dst) =
+            const int r = g8 + 8 * h;
+            *reinterpret_cast<float4*>(cw + cidx<KV8, D>(r, col)) =
                 make_float4(o[dc * 4 + 0][2 * h], o[dc * 4 + 1][2 * h],
                             o[dc * 4 + 2][2 * h], o[dc * 4 + 3][2 * h]);
-            *reinterpret_cast<float4*>(dst + 4) =
+            *reinterpret_cast<float4*>(cw + cidx<KV8, D>(r, col + 4)) =
                 make_float4(o[dc * 4 + 0][2 * h + 1], o[dc * 4 + 1][2 * h + 1],
                             o[dc * 4 + 2][2 * h + 1], o[dc * 4 + 3][2 * h + 1]);
           }
@@ -889,119 +990,121 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
       } else {
 #pragma unroll
         for (int dn = 0; dn < D / 8; ++dn) {
-          *reinterpret_cast<float2*>(cw + rA * C::CST + dn * 8 + 2 * c4) =
+          *reinterpret_cast<float2*>(cw + cidx<KV8, D>(rA, dn * 8 + 2 * c4)) =
               make_float2(o[dn][0], o[dn][1]);
-          *reinterpret_cast<float2*>(cw + rB * C::CST + dn * 8 + 2 * c4) =
+          *reinterpret_cast<float2*>(cw + cidx<KV8, D>(rB, dn * 8 + 2 * c4)) =
               make_float2(o[dn][2], o[dn][3]);
         }
       }
       fence_proxy_async();   // the producer's TMA rewrites this stage later
     }
-    if (nother > 0) asm volatile("bar.sync 1, %0;" ::"n"(C::CT) : "memory");
-    if (warp != 0) continue;
+    asm volatile("bar.sync 1, %0;" ::"n"(C::CT) : "memory");
 
-    // warp 0: merge, normalise, write the output or the piece's partial
+    if constexpr (C::ALL_MERGE) {
+      // every warp merges, normalises and writes one column slice
+      constexpr int CW4 = D / NCW / 4;
+      for (int i = lane; i < rows * CW4; i += 32) {
+        const int r = i / CW4;
+        const int col = warp * (D / NCW) + (i - r * CW4) * 4;
+        float M = -INFINITY;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int r = g8 + 8 * h;
-      if (r >= rows) continue;
-      const float m_own = h ? mB : mA, l_own = h ? lB : lA;
-      float M = m_own;
+        for (int w = 0; w < NCW; ++w) M = fmaxf(M, ml[w * 32 + r * 2]);
+        const float mb = (M == -INFINITY) ? 0.f : M;
+        float lsum = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int w = 0; w < NCW - 1; ++w)
-        if (w < nother) M = fmaxf(M, ml[w * 32 + r * 2]);
-      const float mb = (M == -INFINITY) ? 0.f : M;
-      const float f_own = ex2(m_own - mb);
-      float fw[NCW - 1];
-      float lsum = f_own * l_own;
+        for (int w = 0; w < NCW; ++w) {
+          const float f = ex2(ml[w * 32 + r * 2] - mb);
+          lsum += f * ml[w * 32 + r * 2 + 1];
+          const float4 v = *reinterpret_cast<const float4*>(
+              comb + w * 16 * D + cidx<KV8, D>(r, col));
+          acc.x += f * v.x;
+          acc.y += f * v.y;
+          acc.z += f * v.z;
+          acc.w += f * v.w;
+        }
+        float inv, lse;
+        finish_row(M, lsum, sinks, g * G + r % G, &inv, &lse);
+        store_row(r, col, acc, inv * vscale, lse);
+      }
+      // the held stage goes back to the producer (one arrival per warp)
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty(held));
+    } else {
+      if (warp != 0) continue;
+      // warp 0 merges the others' states into its registers' rows
 #pragma unroll
-      for (int w = 0; w < NCW - 1; ++w) {
-        fw[w] = 0.f;
-        if (w < nother) {
+      for (int h = 0; h < 2; ++h) {
+        const int r = g8 + 8 * h;
+        if (r >= rows) continue;
+        const float m_own = h ? mB : mA, l_own = h ? lB : lA;
+        float M = m_own;
+#pragma unroll
+        for (int w = 0; w < NCW - 1; ++w) M = fmaxf(M, ml[w * 32 + r * 2]);
+        const float mb = (M == -INFINITY) ? 0.f : M;
+        const float f_own = ex2(m_own - mb);
+        float fw[NCW - 1];
+        float lsum = f_own * l_own;
+#pragma unroll
+        for (int w = 0; w < NCW - 1; ++w) {
           fw[w] = ex2(ml[w * 32 + r * 2] - mb);
           lsum += fw[w] * ml[w * 32 + r * 2 + 1];
         }
-      }
-      const int tok = q0 + r / G, hq = g * G + r % G;
-      float inv, lse;   // a sink enters once: here, or in the fold
-      finish_row(M, lsum, pslot < 0 ? p.sinks : nullptr, hq, &inv, &lse);
-      inv *= vscale;
-      T* orow = OUT + static_cast<int64_t>(tok) * p.o_st +
-                static_cast<int64_t>(hq) * p.o_sh;
-      float* prow = pslot >= 0
-                        ? p.part_o + (static_cast<int64_t>(pslot) * 16 + r) * D
-                        : nullptr;
-      if constexpr (KV8) {
+        float inv, lse;
+        finish_row(M, lsum, sinks, g * G + r % G, &inv, &lse);
+        inv *= vscale;
+        if constexpr (KV8) {
 #pragma unroll
-        for (int dc = 0; dc < D / 32; ++dc) {
-          const int col = dc * 32 + 8 * c4;
-          float v[8];
+          for (int dc = 0; dc < D / 32; ++dc) {
 #pragma unroll
-          for (int e = 0; e < 2; ++e)
+            for (int e = 0; e < 2; ++e) {
+              const int col = dc * 32 + 8 * c4 + 4 * e;
+              float4 v = make_float4(f_own * o[dc * 4 + 0][2 * h + e],
+                                     f_own * o[dc * 4 + 1][2 * h + e],
+                                     f_own * o[dc * 4 + 2][2 * h + e],
+                                     f_own * o[dc * 4 + 3][2 * h + e]);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              v[4 * e + j] = f_own * o[dc * 4 + j][2 * h + e];
-#pragma unroll
-          for (int w = 0; w < NCW - 1; ++w) {
-            if (w >= nother) break;
-            const float* src = comb + (w * 16 + r) * C::CST + col;
-            const float4 x0 = *reinterpret_cast<const float4*>(src);
-            const float4 x1 = *reinterpret_cast<const float4*>(src + 4);
-            v[0] += fw[w] * x0.x;
-            v[1] += fw[w] * x0.y;
-            v[2] += fw[w] * x0.z;
-            v[3] += fw[w] * x0.w;
-            v[4] += fw[w] * x1.x;
-            v[5] += fw[w] * x1.y;
-            v[6] += fw[w] * x1.z;
-            v[7] += fw[w] * x1.w;
+              for (int w = 0; w < NCW - 1; ++w) {
+                const float4 x = *reinterpret_cast<const float4*>(
+                    comb + w * 16 * D + cidx<KV8, D>(r, col));
+                v.x += fw[w] * x.x;
+                v.y += fw[w] * x.y;
+                v.z += fw[w] * x.z;
+                v.w += fw[w] * x.w;
+              }
+              store_row(r, col, v, inv, lse);
+            }
           }
-#pragma unroll
-          for (int e = 0; e < 8; ++e) v[e] *= inv;
-          if (pslot < 0) {
-            uint4 pk;
-            pk.x = pack2<T>(v[0], v[1]);
-            pk.y = pack2<T>(v[2], v[3]);
-            pk.z = pack2<T>(v[4], v[5]);
-            pk.w = pack2<T>(v[6], v[7]);
-            *reinterpret_cast<uint4*>(orow + col) = pk;
-          } else {
-            *reinterpret_cast<float4*>(prow + col) =
-                make_float4(v[0], v[1], v[2], v[3]);
-            *reinterpret_cast<float4*>(prow + col + 4) =
-                make_float4(v[4], v[5], v[6], v[7]);
-          }
-        }
-      } else {
-#pragma unroll
-        for (int dn = 0; dn < D / 8; ++dn) {
-          const int col = dn * 8 + 2 * c4;
-          float v0 = f_own * o[dn][2 * h], v1 = f_own * o[dn][2 * h + 1];
-#pragma unroll
-          for (int w = 0; w < NCW - 1; ++w) {
-            if (w >= nother) break;
-            const float2 x = *reinterpret_cast<const float2*>(
-                comb + (w * 16 + r) * C::CST + col);
-            v0 += fw[w] * x.x;
-            v1 += fw[w] * x.y;
-          }
-          v0 *= inv;
-          v1 *= inv;
-          if (pslot < 0)
-            *reinterpret_cast<uint32_t*>(orow + col) = pack2<T>(v0, v1);
-          else
-            *reinterpret_cast<float2*>(prow + col) = make_float2(v0, v1);
-        }
-      }
-      if (c4 == 0) {
-        if (pslot < 0) {
-          if (p.lse) p.lse[static_cast<int64_t>(hq) * p.total_q + tok] = lse;
         } else {
-          p.part_lse[static_cast<int64_t>(pslot) * 16 + r] = lse;
+#pragma unroll
+          for (int dn = 0; dn < D / 8; ++dn) {
+            const int col = dn * 8 + 2 * c4;
+            float v0 = f_own * o[dn][2 * h], v1 = f_own * o[dn][2 * h + 1];
+#pragma unroll
+            for (int w = 0; w < NCW - 1; ++w) {
+              const float2 x = *reinterpret_cast<const float2*>(
+                  comb + w * 16 * D + cidx<KV8, D>(r, col));
+              v0 += fw[w] * x.x;
+              v1 += fw[w] * x.y;
+            }
+            const int tok = q0 + r / G, hq = g * G + r % G;
+            if (pslot < 0) {
+              *reinterpret_cast<uint32_t*>(
+                  OUT + static_cast<int64_t>(tok) * p.o_st +
+                  static_cast<int64_t>(hq) * p.o_sh + col) =
+                  pack2<T>(v0 * inv, v1 * inv);
+              if (col == 0 && p.lse)
+                p.lse[static_cast<int64_t>(hq) * p.total_q + tok] = lse;
+            } else {
+              const int64_t sr = static_cast<int64_t>(pslot) * p.sk_rows + r;
+              *reinterpret_cast<float2*>(p.part_o + sr * D + col) =
+                  make_float2(v0 * inv, v1 * inv);
+              if (col == 0) p.part_lse[sr] = lse;
+            }
+          }
         }
       }
-    }
-    if (nother > 0) {
       // the held stage goes back to the producer (for all NCW warps)
       fence_proxy_async();
       __syncwarp();
@@ -1010,36 +1113,38 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
   }
 }
 
-// Merge the pieces of the units that CTA range boundaries cut.  Block c
-// (1 <= c < C) looks at the boundary before CTA c: the unit whose first
-// piece CTA c - 1 wrote to slot 2(c-1)+1 continues in slots 2c, 2(c+1), ...
-// for every following CTA that marks it as its head unit.
+// Merge the pieces of the units that chunk boundaries cut.  Block c
+// (1 <= c < chunks) looks at the boundary before chunk c: the unit whose
+// first piece chunk c - 1 wrote to slot 2(c-1)+1 continues in slots 2c,
+// 2(c+1), ... for every following chunk that marks it as its head unit.
 template <typename T, int D>
 __global__ void __launch_bounds__(128) fold_kernel(const AttnParams p,
-                                                   int ctas) {
+                                                   int chunks) {
   const int c = blockIdx.x + 1;
   const int u = p.sk_marks[c - 1].y;
   if (u < 0) return;
   int c_end = c;
-  while (c_end < ctas && p.sk_marks[c_end].x == u) ++c_end;
+  while (c_end < chunks && p.sk_marks[c_end].x == u) ++c_end;
   const int npieces = 1 + (c_end - c);
   const int b = u / p.Hkv, g = u - (u / p.Hkv) * p.Hkv;
   const int q0 = p.cu_q[b];
   const int q_len = min(p.cu_q[b + 1] - q0, p.total_q - q0);
-  const int rows = q_len * p.G;
+  const int rows = min(q_len * p.G, p.sk_rows);
   T* __restrict__ OUT = static_cast<T*>(p.out);
+  auto slot_of = [&](int k) {
+    return k == 0 ? 2 * (c - 1) + 1 : 2 * (c + k - 1);
+  };
   for (int i = threadIdx.x; i < rows * (D / 4); i += blockDim.x) {
     const int r = i / (D / 4), col = (i - r * (D / 4)) * 4;
-    auto slot_of = [&](int k) { return k == 0 ? 2 * (c - 1) + 1 : 2 * (c + k - 1); };
     float M = -INFINITY;
     for (int k = 0; k < npieces; ++k)
-      M = fmaxf(M, p.part_lse[static_cast<int64_t>(slot_of(k)) * 16 + r] *
+      M = fmaxf(M, p.part_lse[static_cast<int64_t>(slot_of(k)) * p.sk_rows + r] *
                        kLog2e);
     const float mb = (M == -INFINITY) ? 0.f : M;
     float wsum = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int k = 0; k < npieces; ++k) {
-      const int64_t sr = static_cast<int64_t>(slot_of(k)) * 16 + r;
+      const int64_t sr = static_cast<int64_t>(slot_of(k)) * p.sk_rows + r;
       const float w = ex2(p.part_lse[sr] * kLog2e - mb);
       const float4 v = *reinterpret_cast<const float4*>(p.part_o + sr * D + col);
       wsum += w;
@@ -1170,26 +1275,45 @@ cudaError_t decode_sk_ctas(int D, bool bf16, bool kv8, int sms, int* ctas) {
   return cudaSuccess;
 }
 
-size_t decode_sk_workspace_bytes(int D, int ctas) {
-  auto a256 = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
-  return a256(static_cast<size_t>(2) * ctas * 16 * D * 4) +
-         a256(static_cast<size_t>(2) * ctas * 16 * 4) +
-         a256(static_cast<size_t>(ctas) * 8);
+namespace {
+
+// Scratch layout of a launch with `ctas` CTAs (one chunk each) and partial
+// slots of `rows` rows: two partial slots per chunk (O fp32 [rows][D] and
+// LSE [rows]), then the chunk marks.
+struct SkLayout {
+  int chunks;
+  size_t o_off, lse_off, marks_off, total;
+};
+size_t a256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+SkLayout sk_layout(int D, int ctas, int rows) {
+  SkLayout l;
+  l.chunks = ctas;
+  const size_t slots = static_cast<size_t>(2) * l.chunks;
+  l.o_off = 0;
+  l.lse_off = a256(slots * rows * D * 4);
+  l.marks_off = l.lse_off + a256(slots * rows * 4);
+  l.total = l.marks_off + a256(static_cast<size_t>(l.chunks) * 8);
+  return l;
+}
+
+}  // namespace
+
+size_t decode_sk_workspace_bytes(int D, int ctas, int rows) {
+  return sk_layout(D, ctas, rows).total;
 }
 
 cudaError_t launch_decode_attn_sk(const AttnParams& a, int D, bool bf16,
-                                  int ctas, void* scratch,
+                                  int ctas, int rows, void* scratch,
                                   cudaStream_t stream) {
   AttnParams p = a;
   const bool kv8 = p.kv_fp8 != 0;
-  auto a256 = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  const SkLayout l = sk_layout(D, ctas, rows);
   char* ws = static_cast<char*>(scratch);
-  p.part_o = reinterpret_cast<float*>(ws);
-  p.part_lse = reinterpret_cast<float*>(
-      ws + a256(static_cast<size_t>(2) * ctas * 16 * D * 4));
-  p.sk_marks = reinterpret_cast<int2*>(
-      ws + a256(static_cast<size_t>(2) * ctas * 16 * D * 4) +
-      a256(static_cast<size_t>(2) * ctas * 16 * 4));
+  p.part_o = reinterpret_cast<float*>(ws + l.o_off);
+  p.part_lse = reinterpret_cast<float*>(ws + l.lse_off);
+  p.sk_marks = reinterpret_cast<int2*>(ws + l.marks_off);
+  p.sk_chunks = l.chunks;
+  p.sk_rows = rows;
   cudaError_t e = dsk::dispatch(bf16, kv8, D, [&](auto inst) {
     using I = decltype(inst);
     const int KT = I::C::KTILE;
@@ -1207,20 +1331,21 @@ cudaError_t launch_decode_attn_sk(const AttnParams& a, int D, bool bf16,
       return cudaErrorInvalidValue;
     return I::launch(p, mk, mv, ctas, stream);
   });
-  if (e != cudaSuccess || ctas < 2) return e;
+  if (e != cudaSuccess || l.chunks < 2) return e;
   note_launch();
+  const int fb = l.chunks - 1;
   switch (D) {
     case 64:
-      bf16 ? dsk::fold_kernel<__nv_bfloat16, 64><<<ctas - 1, 128, 0, stream>>>(p, ctas)
-           : dsk::fold_kernel<__half, 64><<<ctas - 1, 128, 0, stream>>>(p, ctas);
+      bf16 ? dsk::fold_kernel<__nv_bfloat16, 64><<<fb, 128, 0, stream>>>(p, l.chunks)
+           : dsk::fold_kernel<__half, 64><<<fb, 128, 0, stream>>>(p, l.chunks);
       break;
     case 128:
-      bf16 ? dsk::fold_kernel<__nv_bfloat16, 128><<<ctas - 1, 128, 0, stream>>>(p, ctas)
-           : dsk::fold_kernel<__half, 128><<<ctas - 1, 128, 0, stream>>>(p, ctas);
+      bf16 ? dsk::fold_kernel<__nv_bfloat16, 128><<<fb, 128, 0, stream>>>(p, l.chunks)
+           : dsk::fold_kernel<__half, 128><<<fb, 128, 0, stream>>>(p, l.chunks);
       break;
     default:
-      bf16 ? dsk::fold_kernel<__nv_bfloat16, 256><<<ctas - 1, 128, 0, stream>>>(p, ctas)
-           : dsk::fold_kernel<__half, 256><<<ctas - 1, 128, 0, stream>>>(p, ctas);
+      bf16 ? dsk::fold_kernel<__nv_bfloat16, 256><<<fb, 128, 0, stream>>>(p, l.chunks)
+           : dsk::fold_kernel<__half, 256><<<fb, 128, 0, stream>>>(p, l.chunks);
       break;
   }
   return cudaGetLastError();

@@ -22,8 +22,9 @@ __device__ unsigned g_device_error = 0;
 static std::atomic<uint64_t> g_launches{0};
 // prefill kernel: PKV_PREFILL_TCGEN05 or PKV_PREFILL_MMA_SYNC
 static std::atomic<int> g_prefill_kernel{PKV_PREFILL_TCGEN05};
-// decode kernel: PKV_DECODE_PERSISTENT, PKV_DECODE_TMA or PKV_DECODE_CP_ASYNC
-static std::atomic<int> g_decode_kernel{PKV_DECODE_PERSISTENT};
+// decode kernel: PKV_DECODE_AUTO, PKV_DECODE_PERSISTENT, PKV_DECODE_TMA or
+// PKV_DECODE_CP_ASYNC
+static std::atomic<int> g_decode_kernel{PKV_DECODE_AUTO};
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 namespace {
@@ -79,7 +80,12 @@ bool stride16(int64_t s, int elem) { return (s * elem) % 16 == 0; }
 
 // ----------------------------------------------------------- split plan
 
+// Units of at least this many keys count as long for the decode kernel
+// choice.
+constexpr int64_t kLongUnitKeys = 2048;
+
 struct Plan {
+  int64_t range = 0;      // widest key range of a decode-class unit
   bool decode = false;    // launch the decode (<= 16 packed rows) kernel
   bool prefill = false;   // launch the prefill kernel
   int splits = 1;         // decode grid.x
@@ -112,6 +118,7 @@ Plan make_plan(int batch, int total_q, int max_q, int max_k, int Hq, int Hkv,
                          (wr >= 0 ? wr : (causal ? 0 : max_k));
     if (span < range) range = span;
   }
+  pl.range = range;
   // splits start on 64-key boundaries counted from the first admissible
   // key rounded down; with a left window that adds up to 63 keys of range
   const int64_t pad = wl >= 0 ? 63 : 0;
@@ -208,18 +215,22 @@ size_t prefill_split_bytes(int splits, int total_q, int Hq, int D) {
 bool sk_candidate(int num_splits, int fixed_split, int D, bool kv8) {
   return num_splits == 0 && fixed_split <= 0 && decode_sk_supported(D, kv8);
 }
-size_t sk_scratch_bytes(int D, bool kv8, int sms) {
+int sk_rows(int G, int max_q) {
+  const int64_t r = static_cast<int64_t>(G) * max_q;
+  return r < kDecodeRows ? static_cast<int>(r) : kDecodeRows;
+}
+size_t sk_scratch_bytes(int D, bool kv8, int sms, int rows) {
   int a = 0, b = 0;
   if (decode_sk_ctas(D, true, kv8, sms, &a) != cudaSuccess ||
       decode_sk_ctas(D, false, kv8, sms, &b) != cudaSuccess)
     return 0;
-  return decode_sk_workspace_bytes(D, a > b ? a : b);
+  return decode_sk_workspace_bytes(D, a > b ? a : b, rows);
 }
 
 // Workspace layout: the required part (decode split partials, fp8 page
 // copies), then the optional tail: the persistent decode kernel's scratch
 // (when the call may use it), and for calls with prefill-class requests
-// the 256-byte item counter and the prefill split partials.
+// the 256-byte item counter and the prefill split partials, last.
 struct Layout {
   size_t need = 0;                    // required bytes
   size_t sk_off = 0, sk_bytes = 0;    // persistent decode scratch
@@ -322,7 +333,7 @@ pkv_status pkv_set_prefill_kernel(int which) {
 
 pkv_status pkv_set_decode_kernel(int which) {
   if (which != PKV_DECODE_TMA && which != PKV_DECODE_CP_ASYNC &&
-      which != PKV_DECODE_PERSISTENT)
+      which != PKV_DECODE_PERSISTENT && which != PKV_DECODE_AUTO)
     return fail(PKV_ERR_INVALID_ARG, "unknown decode kernel %d", which);
   g_decode_kernel.store(which);
   return PKV_OK;
@@ -345,15 +356,31 @@ pkv_status pkv_check_device_errors(pkv_stream_t stream) {
   const unsigned zero = 0;
   e = cudaMemcpy(err, &zero, sizeof(unsigned), cudaMemcpyHostToDevice);
   if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
-  if (host) {
-    return fail(PKV_ERR_BAD_INDEX,
-                "kernels skipped out-of-range accesses:%s%s%s",
-                (host & kErrBadBlock) ? " block id outside the cache;" : "",
-                (host & kErrBadSlot) ? " slot outside the cache;" : "",
-                (host & kErrBadTable) ? " key range beyond the table row or the K/V rows;"
-                                      : "");
-  }
-  return PKV_OK;
+  if (!host) return PKV_OK;
+  const char* what[] = {
+      (host & kErrTimeout) ? " a bounded wait for data ran out (the CTA "
+                             "drained its copies and stopped; its outputs "
+                             "are not written);"
+                           : "",
+      (host & kErrBadBlock) ? " block id outside the cache (skipped);" : "",
+      (host & kErrBadSlot) ? " slot outside the cache (skipped);" : "",
+      (host & kErrBadTable)
+          ? " key range beyond the table row or the K/V rows (clipped);"
+          : "",
+      (host & kErrQueryLen) ? " a request with more queries than "
+                              "max_seqlen_q (not computed);"
+                            : "",
+      (host & kErrSmemAlign) ? " shared memory not 1024-byte aligned (the "
+                               "kernel did nothing);"
+                             : ""};
+  const pkv_status code =
+      (host & kErrTimeout)
+          ? PKV_ERR_TIMEOUT
+          : (host & (kErrBadBlock | kErrBadSlot | kErrBadTable | kErrQueryLen))
+                ? PKV_ERR_BAD_INDEX
+                : PKV_ERR_CUDA;
+  return fail(code, "device error word 0x%x:%s%s%s%s%s%s", host, what[0],
+              what[1], what[2], what[3], what[4], what[5]);
 }
 
 pkv_status pkv_reshape_and_cache(
@@ -453,7 +480,8 @@ size_t pkv_paged_attention_workspace_size_opts(
       total_q, num_heads, head_size);
   const size_t skb =
       sk_candidate(num_splits, fixed_split_of(opts), head_size, fp8)
-          ? sk_scratch_bytes(head_size, fp8, sms)
+          ? sk_scratch_bytes(head_size, fp8, sms,
+                             sk_rows(num_heads / num_kv_heads, max_seqlen_q))
           : 0;
   size_t need = pl.workspace;
   if (fp8 && pl.prefill) {
@@ -486,9 +514,11 @@ size_t pkv_paged_attention_workspace_size(int batch, int total_q,
                                   num_splits, 0)
                  : 1,
       total_q, num_heads, head_size);
-  const size_t skb = sk_candidate(num_splits, 0, head_size, false)
-                         ? sk_scratch_bytes(head_size, false, sms)
-                         : 0;
+  const size_t skb =
+      sk_candidate(num_splits, 0, head_size, false)
+          ? sk_scratch_bytes(head_size, false, sms,
+                             sk_rows(num_heads / num_kv_heads, max_seqlen_q))
+          : 0;
   return make_layout(pl.workspace, pl.prefill, skb, split_bytes).total;
 }
 
@@ -611,11 +641,28 @@ pkv_status pkv_paged_attention_varlen_opts(
                                       sms, num_splits, fixed_split)
                      : 1;
   const size_t sb = prefill_split_bytes(sp, total_q, num_heads, head_size);
+  // Persistent or one CTA per (request, KV head, split)?  Measured on
+  // GB300: when the (request, KV head) units fill about one wave of the
+  // per-unit kernel's resident CTAs, the hardware's dealing of CTAs to SMs
+  // balances the SMs better than equal static shares (batched decode,
+  // 512 units: 0.1131 against 0.1157 ms), and so it does for many short
+  // units (cascade suffix, 2048 units of 512 keys: 0.2095 against 0.2181
+  // ms for the whole cascade); from two waves of long units on the
+  // persistent kernel is ahead (124 windowed D = 256 decodes, 992 units of
+  // up to 4096 keys: 0.581 against 0.625 ms).  fp8 caches always take it
+  // (the per-unit fp8 kernel is 1.9 times slower).
+  const int dsel = g_decode_kernel.load();
+  const bool many_units =
+      static_cast<int64_t>(batch) * num_kv_heads >=
+          2 * static_cast<int64_t>(sms) * kDecodeCtasPerSm &&
+      pl.range >= kLongUnitKeys;
   const bool sk_ok =
       sk_candidate(num_splits, fixed_split, head_size, kv8) &&
-      g_decode_kernel.load() == PKV_DECODE_PERSISTENT;
+      (dsel == PKV_DECODE_PERSISTENT ||
+       (dsel == PKV_DECODE_AUTO && (kv8 || many_units)));
+  const int skr = sk_rows(num_heads / num_kv_heads, max_seqlen_q);
   const size_t skb = sk_candidate(num_splits, fixed_split, head_size, kv8)
-                         ? sk_scratch_bytes(head_size, kv8, sms)
+                         ? sk_scratch_bytes(head_size, kv8, sms, skr)
                          : 0;
   const Layout lay = make_layout(need, pl.prefill, skb, sb);
   const bool ws_ok = workspace &&
@@ -626,7 +673,7 @@ pkv_status pkv_paged_attention_varlen_opts(
       workspace_bytes >= lay.sk_off + lay.sk_bytes) {
     if (decode_sk_ctas(head_size, dtype == PKV_BF16, kv8, sms, &sk_ctas) ==
             cudaSuccess &&
-        decode_sk_workspace_bytes(head_size, sk_ctas) <= lay.sk_bytes)
+        decode_sk_workspace_bytes(head_size, sk_ctas, skr) <= lay.sk_bytes)
       sk_scratch = static_cast<char*>(workspace) + lay.sk_off;
     else
       sk_ctas = 0;
@@ -723,8 +770,9 @@ pkv_status pkv_paged_attention_varlen_opts(
     const bool persistent = sk_scratch != nullptr;
     if (persistent) {
       d.chunk = 0;
-      e = launch_decode_attn_sk(d, head_size, bf16, sk_ctas, sk_scratch, s);
-    } else if (!kv8 && g_decode_kernel.load() != PKV_DECODE_CP_ASYNC) {
+      e = launch_decode_attn_sk(d, head_size, bf16, sk_ctas, skr, sk_scratch,
+                                s);
+    } else if (!kv8 && dsel != PKV_DECODE_CP_ASYNC) {
       e = launch_decode_attn_tma(d, head_size, bf16, pl.splits, s);
     } else {
       e = launch_decode_attn(d, head_size, bf16, pl.splits, 1, s);

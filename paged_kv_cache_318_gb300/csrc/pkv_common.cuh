@@ -15,6 +15,9 @@ constexpr unsigned kErrBadBlock = 1u;   // block id outside [0, num_blocks)
 constexpr unsigned kErrBadSlot = 2u;    // slot outside the cache
 constexpr unsigned kErrBadTable = 4u;   // key beyond the block-table row
 constexpr unsigned kErrTimeout = 8u;    // a bounded wait gave up
+constexpr unsigned kErrSmemAlign = 16u; // shared memory not 1024-byte aligned
+constexpr unsigned kErrQueryLen = 32u;  // a request's query count is above
+                                        // the max_seqlen_q the call gave
 
 // ---------------------------------------------------------------- PTX helpers
 
@@ -233,9 +236,13 @@ struct AttnParams {
   // persistent prefill: one int of workspace the kernel hands work items
   // out through (the launcher zeroes it first); null = fixed item order
   int* sched;
-  // persistent decode: per CTA, the unit it starts inside (x) and the unit
-  // it starts that continues past its range (y), -1 for none
+  // persistent decode: the tile sequence is cut into sk_chunks chunks (one
+  // per CTA); per chunk, the unit it starts inside (x) and the unit it
+  // starts that runs past its end (y), -1 for none.  Partial slots hold
+  // sk_rows rows.
   int2* sk_marks;
+  int sk_chunks;
+  int sk_rows;
   // persistent prefill split-KV: key splits per work item (1 = none); with
   // more, partials go to pre_o [S, total_q, Hq, D] / pre_lse [S, Hq,
   // total_q] and launch_prefill_split_combine folds them
@@ -350,13 +357,15 @@ cudaError_t launch_split_combine(const CombineParams& p, bool bf16,
 // Persistent decode attention (decode_sk.cu): 16-bit caches with D in {64,
 // 128, 256}, E4M3 caches with D in {128, 256}.  decode_sk_ctas gives the
 // launch's CTA count on the current device (resident CTAs per SM x sms);
-// the launch needs decode_sk_workspace_bytes(D, ctas) of scratch (256-byte
-// aligned) for the pieces of units that CTA boundaries cut.
+// the launch needs decode_sk_workspace_bytes(D, ctas, rows) of scratch
+// (256-byte aligned) for the pieces of units that chunk boundaries cut,
+// rows = the most packed query rows a decode-class request can have
+// (min(16, G * max_seqlen_q)).
 bool decode_sk_supported(int D, bool kv8);
 cudaError_t decode_sk_ctas(int D, bool bf16, bool kv8, int sms, int* ctas);
-size_t decode_sk_workspace_bytes(int D, int ctas);
+size_t decode_sk_workspace_bytes(int D, int ctas, int rows);
 cudaError_t launch_decode_attn_sk(const AttnParams& p, int D, bool bf16,
-                                  int ctas, void* scratch,
+                                  int ctas, int rows, void* scratch,
                                   cudaStream_t stream);
 // Required workspace bytes of an attention call (pkv_api.cu): the split-KV
 // partials and fp8 copies it needs, not the optional prefill tail.

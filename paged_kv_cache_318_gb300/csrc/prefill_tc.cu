@@ -275,7 +275,7 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
   const uint32_t base_u = smem_u32(smem_raw);
   unsigned char* base = smem_raw;
   if (base_u & 1023u) {            // 128-byte swizzle atoms need 1 KB
-    if (threadIdx.x == 0) atomicOr(p.err, kErrTimeout);
+    if (threadIdx.x == 0) atomicOr(p.err, kErrSmemAlign);
     return;
   }
 
@@ -805,7 +805,7 @@ prefill_pp_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
   const uint32_t base_u = smem_u32(smem_raw);
   unsigned char* base = smem_raw;
   if (base_u & 1023u) {
-    if (threadIdx.x == 0) atomicOr(p.err, kErrTimeout);
+    if (threadIdx.x == 0) atomicOr(p.err, kErrSmemAlign);
     return;
   }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1578,7 +1578,7 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
   const uint32_t base_u = smem_u32(smem_raw);
   unsigned char* base = smem_raw;
   if (base_u & 1023u) {
-    if (threadIdx.x == 0) atomicOr(p.err, kErrTimeout);
+    if (threadIdx.x == 0) atomicOr(p.err, kErrSmemAlign);
     return;
   }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;

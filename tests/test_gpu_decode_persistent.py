@@ -32,6 +32,8 @@ def built(cuda_device):
     _build.build()
     api.load_library()
     api.set_decode_kernel(api.DECODE_PERSISTENT)
+    yield
+    api.set_decode_kernel(api.DECODE_AUTO)
 
 
 def _close(wl, out, lse, ref_out, ref_lse, what):
@@ -131,8 +133,7 @@ def test_persistent_decode_rows_without_keys(cuda_device):
 
 def test_workspace_without_scratch_falls_back(cuda_device):
     """The kernel's scratch is part of the optional workspace tail: without
-    it the call runs one CTA per (request, KV head) and is still right, and
-    with it the two runs agree within rounding."""
+    it the call runs one CTA per (request, KV head) and is still right."""
     wl = workloads.batched_decode(batch=24, lo=100, hi=5000,
                                   pool_blocks=9000)
     ref_out, ref_lse = full_reference(wl)

@@ -199,7 +199,7 @@ def test_decode_kernels(cuda_device, idx, kernel):
     try:
         _, out, lse = run_batch(wl, cuda_device)
     finally:
-        api.set_decode_kernel(api.DECODE_PERSISTENT)
+        api.set_decode_kernel(api.DECODE_AUTO)
     ref_out, ref_lse = full_reference(wl)
     assert_close(wl, out, lse, ref_out, ref_lse, "%s %d" % (kernel, idx))
 
