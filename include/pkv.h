@@ -469,6 +469,20 @@ PKV_API pkv_status pkv_set_prefill_kernel(int which);
 PKV_API pkv_status pkv_set_decode_kernel(int which);
 
 /*
+ * Limit of the bounded waits of the decode kernels (a consumer waiting for
+ * its K/V pages, the producer waiting for a free ring stage), in
+ * nanoseconds; the default is PKV_WAIT_LIMIT_DEFAULT_NS (2 s).  A wait that
+ * runs out records a timeout in the device error word, the CTA drains the
+ * copies it issued (those drains always keep the 2 s limit), frees what it
+ * holds and returns without writing its outputs; pkv_check_device_errors
+ * then reports PKV_ERR_TIMEOUT and the next call runs normally.  A
+ * process-wide diagnostic for testing that path: a small limit makes calls
+ * fail.  No counterpart on the source pages.
+ */
+#define PKV_WAIT_LIMIT_DEFAULT_NS 2000000000ull
+PKV_API pkv_status pkv_set_wait_limit_ns(uint64_t ns);
+
+/*
  * Number of kernels this library has launched in this process (all devices,
  * all threads), for accounting of launches per step.
  */

@@ -111,6 +111,8 @@ def load_library():
         lib.pkv_set_prefill_kernel.argtypes = [i32]
         lib.pkv_set_decode_kernel.restype = i32
         lib.pkv_set_decode_kernel.argtypes = [i32]
+        lib.pkv_set_wait_limit_ns.restype = i32
+        lib.pkv_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
         lib.pkv_launch_count.restype = ctypes.c_uint64
         lib.pkv_launch_count.argtypes = []
         lib.pkv_check_device_errors.restype = i32
@@ -177,6 +179,15 @@ def set_decode_kernel(which: int):
     """Choose the decode kernel: DECODE_AUTO (default), DECODE_PERSISTENT,
     DECODE_TMA or DECODE_CP_ASYNC."""
     _check(load_library().pkv_set_decode_kernel(int(which)))
+
+
+WAIT_LIMIT_DEFAULT_NS = 2_000_000_000
+
+
+def set_wait_limit_ns(ns: int = WAIT_LIMIT_DEFAULT_NS):
+    """Limit of the decode kernels' bounded waits (diagnostic; a small limit
+    makes calls stop with PKV_ERR_TIMEOUT)."""
+    _check(load_library().pkv_set_wait_limit_ns(int(ns)))
 
 
 def launch_count() -> int:

@@ -410,8 +410,8 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
         if (k >= 2) {
           int ok = 1;
           if (lane == 0)
-            ok = mbar_wait(uempty(slot), ((k >> 1) - 1) & 1, abort_flag,
-                           p.err);
+            ok = mbar_wait_lim(uempty(slot), ((k >> 1) - 1) & 1, abort_flag,
+                        p.err, p.wait_ns);
           if (!__shfl_sync(0xffffffffu, ok, 0)) {
             stop = true;
             break;
@@ -482,8 +482,8 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
           int halt = 0;
           if (lane == 0) {
             if (it >= STAGES &&
-                !mbar_wait(empty(s), ((it / STAGES) - 1) & 1, abort_flag,
-                           p.err)) {
+                !mbar_wait_lim(empty(s), ((it / STAGES) - 1) & 1, abort_flag,
+                        p.err, p.wait_ns)) {
               halt = 1;
             } else {
               bad_boxes[s] = bad;
@@ -539,7 +539,8 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
       const int slot = k & 1;
       int ok = 1;
       if (k >= 2 && lane == 0)
-        ok = mbar_wait(uempty(slot), ((k >> 1) - 1) & 1, abort_flag, p.err);
+        ok = mbar_wait_lim(uempty(slot), ((k >> 1) - 1) & 1, abort_flag,
+                        p.err, p.wait_ns);
       if (__shfl_sync(0xffffffffu, ok, 0)) {
         if (lane == 0) {
           desc[slot].end = 1;
@@ -574,7 +575,8 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
 
   for (int k = 0;; ++k) {
     const int slot = k & 1;
-    const bool got = mbar_wait(ufull(slot), (k >> 1) & 1, abort_flag, p.err);
+    const bool got = mbar_wait_lim(ufull(slot), (k >> 1) & 1, abort_flag,
+                        p.err, p.wait_ns);
     float qshift_f = 1.f;    // 2^shift: the query scaling of an fp8 unit
     if constexpr (KV8) {
       // largest |q| of the unit's rows (bf16 queries only)
@@ -686,7 +688,8 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
       const int s = it % STAGES;
       const uint32_t par = (it / STAGES) & 1;
       const int kt = kt0 + (t_beg + jt) * KT;
-      if (!mbar_wait(full_k(s), par, abort_flag, p.err)) {
+      if (!mbar_wait_lim(full_k(s), par, abort_flag,
+                        p.err, p.wait_ns)) {
         aborted = true;
         break;
       }
@@ -844,7 +847,8 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
         }
       }
 
-      if (!mbar_wait(full_v(s), par, abort_flag, p.err)) {
+      if (!mbar_wait_lim(full_v(s), par, abort_flag,
+                        p.err, p.wait_ns)) {
         aborted = true;
         break;
       }

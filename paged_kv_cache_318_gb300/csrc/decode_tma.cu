@@ -177,7 +177,8 @@ decode_tma_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
       int stop = 0;
       if (lane == 0) {
         if (t >= STAGES &&
-            !mbar_wait(empty(s), ((t / STAGES) - 1) & 1, abort_flag, p.err)) {
+            !mbar_wait_lim(empty(s), ((t / STAGES) - 1) & 1, abort_flag,
+                        p.err, p.wait_ns)) {
           stop = 1;
         } else {
           bad_boxes[s] = bad;
@@ -263,7 +264,8 @@ decode_tma_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
     const int s = it % STAGES;
     const uint32_t par = (it / STAGES) & 1;
     const int kt = kt0 + it * KT;
-    if (!mbar_wait(full_k(s), par, abort_flag, p.err)) break;
+    if (!mbar_wait_lim(full_k(s), par, abort_flag,
+                        p.err, p.wait_ns)) break;
     const uint32_t sK = tile_k(s), sV = tile_v(s);
     if (const unsigned bad = bad_boxes[s]) {
       // pages the table pointed outside the cache: zero keys and values
@@ -385,7 +387,8 @@ decode_tma_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
       }
     }
 
-    if (!mbar_wait(full_v(s), par, abort_flag, p.err)) break;
+    if (!mbar_wait_lim(full_v(s), par, abort_flag,
+                        p.err, p.wait_ns)) break;
     if (kt + kw0 + C::KW > hi) {
       // rows of this warp at or past the loaded range: zero them, so that
       // P = 0 never meets NaN padding or a stale row

@@ -25,6 +25,8 @@ static std::atomic<int> g_prefill_kernel{PKV_PREFILL_TCGEN05};
 // decode kernel: PKV_DECODE_AUTO, PKV_DECODE_PERSISTENT, PKV_DECODE_TMA or
 // PKV_DECODE_CP_ASYNC
 static std::atomic<int> g_decode_kernel{PKV_DECODE_AUTO};
+// limit of the decode kernels' bounded waits (pkv_set_wait_limit_ns)
+static std::atomic<uint64_t> g_wait_limit_ns{PKV_WAIT_LIMIT_DEFAULT_NS};
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 namespace {
@@ -336,6 +338,11 @@ pkv_status pkv_set_decode_kernel(int which) {
       which != PKV_DECODE_PERSISTENT && which != PKV_DECODE_AUTO)
     return fail(PKV_ERR_INVALID_ARG, "unknown decode kernel %d", which);
   g_decode_kernel.store(which);
+  return PKV_OK;
+}
+
+pkv_status pkv_set_wait_limit_ns(uint64_t ns) {
+  g_wait_limit_ns.store(ns, std::memory_order_relaxed);
   return PKV_OK;
 }
 
@@ -751,6 +758,7 @@ pkv_status pkv_paged_attention_varlen_opts(
   p.wl = wl;
   p.wr = wr;
   p.err = err;
+  p.wait_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   const bool bf16 = dtype == PKV_BF16;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 

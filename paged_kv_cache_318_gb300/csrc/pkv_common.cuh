@@ -250,6 +250,9 @@ struct AttnParams {
   float* pre_o;
   float* pre_lse;
   unsigned* err;
+  // bounded mbarrier waits of the decode kernels give up after this many
+  // nanoseconds (pkv_set_wait_limit_ns; the drains at exit keep 2 s)
+  uint64_t wait_ns;
 };
 
 struct CombineParams {

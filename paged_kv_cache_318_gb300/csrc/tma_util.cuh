@@ -52,24 +52,32 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
-// Bounded wait: false when the CTA is aborting, or after kWaitLimitNs (then
+// Bounded wait: false when the CTA is aborting, or after limit_ns (then
 // the error word gets kErrTimeout and the CTA-wide abort flag is raised).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          volatile int* abort_flag,
-                                          unsigned* err) {
+__device__ __forceinline__ bool mbar_wait_lim(uint32_t bar, uint32_t parity,
+                                              volatile int* abort_flag,
+                                              unsigned* err,
+                                              uint64_t limit_ns) {
   if (mbar_try(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try(bar, parity)) return true;
-    if ((it & 255u) == 0) {
+    // the time is read after the second poll (a limit of 0 gives up there)
+    // and then every 256 polls
+    if (it == 1 || (it & 255u) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs || it > kSpinLimit) {
+      if (globaltimer_ns() - t0 >= limit_ns || it > kSpinLimit) {
         *abort_flag = 1;
         atomicOr(err, kErrTimeout);
         return false;
       }
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          volatile int* abort_flag,
+                                          unsigned* err) {
+  return mbar_wait_lim(bar, parity, abort_flag, err, kWaitLimitNs);
 }
 
 // Wait used while draining in-flight work: no abort check, still bounded.
