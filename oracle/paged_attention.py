@@ -262,7 +262,10 @@ def merge_attn_states_ref(prefix_output, prefix_lse, suffix_output,
     ``_forward_with_dcp`` (context + new tokens).  With M = max(l1, l2),
     w_i = exp(l_i - M): out = (w1 o1 + w2 o2) / (w1 + w2),
     lse = M + ln(w1 + w2).  A side with lse = -inf holds no keys and drops
-    out; if both are -inf the row is out = 0, lse = -inf.
+    out (its output is not read); if both are -inf the row is out = 0,
+    lse = -inf.  Non-finite LSEs the pages do not define take the limit of
+    the formula: a side with lse = +inf takes all the weight (two such sides
+    weigh the same) and the merged lse is +inf; a NaN lse gives a NaN row.
 
     outputs [T, H, D]; lse [H, T].  Returns (out float64, lse float64).
     """
@@ -270,16 +273,31 @@ def merge_attn_states_ref(prefix_output, prefix_lse, suffix_output,
     o2 = np.asarray(suffix_output, dtype=np.float64)
     l1 = np.asarray(prefix_lse, dtype=np.float64).T      # [T, H]
     l2 = np.asarray(suffix_lse, dtype=np.float64).T
-    m = np.maximum(l1, l2)
-    any_keys = np.isfinite(m)
-    m_safe = np.where(any_keys, m, 0.0)
-    w1 = np.where(np.isfinite(l1), np.exp(l1 - m_safe), 0.0)
-    w2 = np.where(np.isfinite(l2), np.exp(l2 - m_safe), 0.0)
+    nan = np.isnan(l1) | np.isnan(l2)
+    inf1, inf2 = l1 == np.inf, l2 == np.inf
+    pinf = inf1 | inf2
+    with np.errstate(invalid="ignore"):
+        m = np.maximum(l1, l2)
+    finite_m = np.isfinite(m)
+    m_safe = np.where(finite_m, m, 0.0)
+    with np.errstate(invalid="ignore", over="ignore"):
+        w1 = np.where(np.isfinite(l1), np.exp(l1 - m_safe), 0.0)
+        w2 = np.where(np.isfinite(l2), np.exp(l2 - m_safe), 0.0)
+    w1 = np.where(pinf, inf1.astype(np.float64), w1)
+    w2 = np.where(pinf, inf2.astype(np.float64), w2)
+    any_keys = finite_m | pinf
     tot = w1 + w2
-    tot_safe = np.where(any_keys, tot, 1.0)
-    out = (w1[..., None] * o1 + w2[..., None] * o2) / tot_safe[..., None]
+    tot_safe = np.where(any_keys & (tot > 0), tot, 1.0)
+    # a side without weight is not read (its rows may hold anything)
+    with np.errstate(invalid="ignore"):
+        num = np.where((w1 > 0)[..., None], w1[..., None] * o1, 0.0) + \
+            np.where((w2 > 0)[..., None], w2[..., None] * o2, 0.0)
+    out = num / tot_safe[..., None]
     out = np.where(any_keys[..., None], out, 0.0)
-    lse = np.where(any_keys, m_safe + np.log(tot_safe), -np.inf)
+    lse = np.where(finite_m, m_safe + np.log(tot_safe), -np.inf)
+    lse = np.where(pinf, np.inf, lse)
+    out = np.where(nan[..., None], np.nan, out)
+    lse = np.where(nan, np.nan, lse)
     return out, lse.T.copy()
 
 

@@ -158,3 +158,25 @@ def test_cascade_with_sinks_on_prefix_equals_flat_with_sinks():
                        wl.block_table, 8, 0.4, sinks=sinks)
     np.testing.assert_allclose(casc[0], flat[0], atol=1e-13)
     np.testing.assert_allclose(casc[1], flat[1], atol=1e-13)
+
+
+def test_merge_non_finite_lse_edges():
+    """-inf drops a side (its output is not read, even NaN); +inf takes all
+    the weight (two +inf sides weigh the same) with merged lse +inf; NaN
+    propagates.  Limits of the merge formula, evaluated by hand."""
+    inf, nan = np.inf, np.nan
+    o1 = np.array([[[1.0, 2.0]], [[1.0, 2.0]], [[nan, nan]], [[1.0, 2.0]],
+                   [[1.0, 2.0]], [[3.0, 5.0]]])           # [T=6, H=1, D=2]
+    o2 = np.array([[[5.0, 6.0]], [[5.0, 6.0]], [[5.0, 6.0]], [[5.0, 6.0]],
+                   [[nan, 0.0]], [[7.0, 9.0]]])
+    l1 = np.array([[inf, 0.3, -inf, nan, inf, inf]])       # [H=1, T=6]
+    l2 = np.array([[2.0, inf, 1.5, 0.0, -inf, inf]])
+    out, lse = merge_attn_states_ref(o1, l1, o2, l2)
+    np.testing.assert_array_equal(out[0, 0], [1.0, 2.0])   # +inf left
+    np.testing.assert_array_equal(out[1, 0], [5.0, 6.0])   # +inf right
+    np.testing.assert_array_equal(out[2, 0], [5.0, 6.0])   # -inf, NaN rows
+    assert np.isnan(out[3]).all() and np.isnan(lse[0, 3])  # NaN lse
+    np.testing.assert_array_equal(out[4, 0], [1.0, 2.0])   # +inf vs -inf
+    np.testing.assert_array_equal(out[5, 0], [5.0, 7.0])   # both +inf: mean
+    assert lse[0, 0] == inf and lse[0, 1] == inf and lse[0, 4] == inf
+    assert lse[0, 5] == inf and lse[0, 2] == 1.5
