@@ -61,13 +61,21 @@ def decode_bytes(wl) -> dict:
                 step=kv + qo + tables + cache_write)
 
 
-def prefill_flops(wl) -> float:
-    """QK^T + PV flops over admissible (query, key) pairs."""
+def prefill_flops(wl, min_rows=0) -> float:
+    """QK^T + PV flops over admissible (query, key) pairs (causal, with the
+    workload's left window), of requests with at least ``min_rows`` packed
+    query rows."""
+    G = wl.num_heads // wl.num_kv_heads
+    left = wl.window_size[0]
     total = 0
     for b in range(wl.batch):
         q, L = int(wl.q_lens[b]), int(wl.seq_lens[b])
+        if q * G < min_rows:
+            continue
         c = L - q
-        total += sum(c + i + 1 for i in range(q))   # causal pairs
+        for i in range(q):
+            n = c + i + 1                            # causal keys
+            total += n if left < 0 else min(n, left + 1)
     return 4.0 * wl.head_size * wl.num_heads * total
 
 
@@ -431,11 +439,36 @@ def _time_ms(fn, iters=10, warm=3):
 
 
 def _kv_bytes(wl, elem=2):
-    """Admissible K/V bytes of decode-class requests (window aware)."""
+    """Admissible K/V bytes of the requests, each read once (window aware:
+    a request's queries see at most its last window + query-count keys)."""
     L = wl.seq_lens.astype(np.int64)
     if wl.window_size[0] >= 0:
-        L = np.minimum(L, wl.window_size[0] + 1)
+        L = np.minimum(L, wl.window_size[0] + wl.q_lens.astype(np.int64))
     return int(L.sum()) * 2 * wl.num_kv_heads * wl.head_size * elem
+
+
+def cache_write_bytes(wl, elem=2):
+    """Algorithmic bytes of writing the workload's new K/V rows: each row
+    read and written once, plus its 8-byte slot."""
+    T = len(wl.slot_mapping_new)
+    return T * 2 * wl.num_kv_heads * wl.head_size * elem * 2 + 8 * T
+
+
+def _time_flushed_ms(fn, flush, iters=10, warm=3):
+    """Mean device ms of fn, with the L2 flushed (a 256 MB write) before
+    each timed call and events around the call only."""
+    for _ in range(warm):
+        fn()
+    ev = [(torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        flush.zero_()
+        a.record()
+        fn()
+        b.record()
+    torch.cuda.synchronize()
+    return float(np.mean([a.elapsed_time(b) for a, b in ev]))
 
 
 def other_workloads(dev, hbm_peak, tf_peak):
@@ -448,6 +481,47 @@ def other_workloads(dev, hbm_peak, tf_peak):
         out[name] = {"workload": desc, "ms": round(ms, 4),
                      "value": round(rate, 1), "unit": unit,
                      "frac": round(rate / peak, 4)}
+
+    # the varlen prefill workload's cache write (11207 new tokens): its
+    # 92 MB fit in the L2, so the L2 is flushed before each timed call
+    wl = workloads.prefill_with_prefix(seed=SEED_PREFILL, device=dev)
+    b = DeviceBatch(wl, dev, poison=False)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    rec("cache_write", "reshape_and_cache of the varlen prefill workload's "
+        "%d new tokens (8 KV heads, D 128, bf16; L2 flushed before each "
+        "call)" % len(wl.slot_mapping_new),
+        _time_flushed_ms(b.write_new, flush), cache_write_bytes(wl), "GB/s",
+        hbm_peak)
+    del b, flush
+    # the Gemma-like mixed batch as one call, against max(bytes / BW,
+    # flops / F); and its prefill part (four 512-token chunks, D 256) alone
+    wl = workloads.mixed_gemma(device=dev)
+    b = DeviceBatch(wl, dev, poison=False)
+    b.write_context()
+    b.write_new()
+    ms = _time_ms(lambda: b.attend(return_lse=False))
+    nbytes = _kv_bytes(wl)
+    flops = prefill_flops(wl, min_rows=17)
+    t_roof = max(nbytes / (hbm_peak * 1e9), flops / (tf_peak * 1e12))
+    out["mixed_batch"] = {
+        "workload": "one call: 124 decodes (L ~ U[1024, 16384]) + 4 x "
+                    "512-token chunks (context U[0, 8192]), 16/8 heads, "
+                    "D 256, window (4095, 0), soft-cap 50",
+        "ms": round(ms, 4), "bytes": nbytes, "flops": flops,
+        "t_roof_ms": round(t_roof * 1e3, 4),
+        "frac": round(t_roof * 1e3 / ms, 4),
+        "bound": "hbm" if nbytes / (hbm_peak * 1e9) >= flops /
+                 (tf_peak * 1e12) else "tensor"}
+    del b
+    wl = workloads.mixed_gemma(device=dev, n_decode=0)
+    b = DeviceBatch(wl, dev, poison=False)
+    b.write_context()
+    b.write_new()
+    rec("mixed_prefill_part", "the mixed batch's 4 x 512-token prefill "
+        "chunks alone (D 256, window 4095, soft-cap 50)",
+        _time_ms(lambda: b.attend(return_lse=False)),
+        prefill_flops(wl, min_rows=17), "TFLOP/s", tf_peak)
+    del b
 
     wl = workloads.long_decode(device=dev)
     b = DeviceBatch(wl, dev, poison=False)
@@ -512,6 +586,46 @@ def other_workloads(dev, hbm_peak, tf_peak):
 
 
 # -------------------------------------------------------------- CPU legs
+_POOL_WL = None          # the workload the oracle pool's workers read
+
+
+def _oracle_request(b):
+    from oracle.harness import request_reference
+    request_reference(_POOL_WL, b)
+    return b
+
+
+def make_oracle_pool(wl):
+    """A process pool for the oracle on every host core, forked before this
+    process touches the GPU (the workers inherit ``wl`` and never use
+    CUDA)."""
+    import multiprocessing as mp
+    global _POOL_WL
+    _POOL_WL = wl
+    cores = os.cpu_count() or 1
+    return mp.get_context("fork").Pool(cores), cores
+
+
+def _request_bytes(wl, b):
+    e = 2
+    return int(wl.seq_lens[b]) * 2 * wl.num_kv_heads * wl.head_size * e + \
+        2 * wl.num_heads * wl.head_size * e
+
+
+def oracle_pool_sample(pool, cores, wl, budget_s):
+    """Wall time of the oracle over passes of the whole batch, one request
+    per worker at a time, until ``budget_s``.  Returns (bytes, seconds,
+    requests)."""
+    nbytes, done, t_total = 0, 0, 0.0
+    while t_total < budget_s:
+        t0 = time.perf_counter()
+        pool.map(_oracle_request, range(wl.batch), chunksize=1)
+        t_total += time.perf_counter() - t0
+        nbytes += sum(_request_bytes(wl, b) for b in range(wl.batch))
+        done += wl.batch
+    return nbytes, t_total, done
+
+
 def oracle_sample(wl, budget_s, max_requests=None, start=0):
     """Time the oracle on whole requests (from ``start``) until ``budget_s``
     is spent.  Returns (bytes processed, seconds, requests)."""
@@ -532,29 +646,45 @@ def oracle_sample(wl, budget_s, max_requests=None, start=0):
     return nbytes, t_total, done
 
 
-def cpu_baseline(budget_s=12.0):
-    wl = workloads.batched_decode(seed=SEED_DECODE, device="cpu")
-    nbytes, secs, n = oracle_sample(wl, budget_s)
-    return {"value": round(nbytes / secs / 1e9, 4), "unit": UNIT, "cores": 1,
-            "kind": "oracle",
-            "sample": "%d of %d requests of the batched decode workload "
-                      "(float64 numpy oracle, single thread, %.1f s)"
-                      % (n, wl.batch, secs)}
+def cpu_baseline(wl, pool, cores, budget_s=10.0):
+    """The float64 oracle on every host core (a process per core, one
+    request each at a time), and on one core."""
+    nbytes, secs, n = oracle_pool_sample(pool, cores, wl, budget_s)
+    b1, s1, n1 = oracle_sample(wl, budget_s / 3)
+    return {"value": round(nbytes / secs / 1e9, 4), "unit": UNIT,
+            "cores": cores, "kind": "oracle",
+            "sample": "%d requests (%d passes over the 64 of the batched "
+                      "decode workload) in %.1f s of wall time on %d "
+                      "processes (float64 numpy oracle, one thread each)"
+                      % (n, n // wl.batch, secs, cores),
+            "one_core": {"value": round(b1 / s1 / 1e9, 4), "cores": 1,
+                         "sample": "%d requests in %.1f s, one thread"
+                                   % (n1, s1)}}
 
 
 def reference_arm(args):
     wl = workloads.batched_decode(seed=SEED_DECODE, device="cpu")
+    pool, cores = make_oracle_pool(wl)
     per_step = []
-    for i in range(args.warmup + args.steps):
-        nbytes, secs, n = oracle_sample(wl, 0.0, max_requests=1,
-                                        start=i % wl.batch)
-        if i >= args.warmup:
-            per_step.append((nbytes, secs))
+    try:
+        for i in range(args.warmup + args.steps):
+            # one step: `cores` requests of the batch, one per process
+            reqs = [(i * cores + j) % wl.batch for j in range(cores)]
+            t0 = time.perf_counter()
+            pool.map(_oracle_request, reqs, chunksize=1)
+            secs = time.perf_counter() - t0
+            if i >= args.warmup:
+                per_step.append((sum(_request_bytes(wl, b) for b in reqs),
+                                 secs))
+    finally:
+        pool.close()
+        pool.join()
     tot_b = sum(b for b, _ in per_step)
     tot_s = sum(s for _, s in per_step)
     value = tot_b / tot_s / 1e9
-    sample = ("one request of the batched decode workload per step "
-              "(float64 numpy oracle, single thread)")
+    sample = ("%d requests of the batched decode workload per step, one "
+              "per process on %d host cores (float64 numpy oracle, one "
+              "thread each)" % (cores, cores))
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 4),
         "unit": UNIT, "n_gpus": 1, "steps": args.steps,
@@ -564,8 +694,8 @@ def reference_arm(args):
         "dtype": "f64", "data": "synthetic",
         "config": {"workload": "batched_paged_decode_llama3_8b",
                    "requests": wl.batch},
-        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1,
-                         "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT,
+                         "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": UNIT,
                 "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -591,6 +721,11 @@ def main():
             print(json.dumps(reference_arm(args)), flush=True)
         return
 
+    # the oracle's process pool is forked before this process uses CUDA
+    cpu_wl = pool = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu_wl = workloads.batched_decode(seed=SEED_DECODE, device="cpu")
+        pool, cores = make_oracle_pool(cpu_wl)
     local = int(os.environ.get("LOCAL_RANK", "0"))
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
@@ -605,8 +740,12 @@ def main():
     if rank == 0 and world == 1 and not args.no_extras:
         hbm_peak, tf_peak, _ = measured_peaks()
         res["other_workloads"] = other_workloads(dev, hbm_peak, tf_peak)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline()
+    if pool is not None:
+        try:
+            res["cpu_baseline"] = cpu_baseline(cpu_wl, pool, cores)
+        finally:
+            pool.close()
+            pool.join()
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:

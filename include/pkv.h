@@ -304,17 +304,24 @@ PKV_API size_t pkv_paged_attention_workspace_size(
  *
  * - Set-up: the first call on each device looks up the array's device
  *   address (cudaGetSymbolAddress, with that device current) and caches it.
- *   Make that first call before any stream capture.
- * - Limit: a call whose decode split plan (or fp8 page copies) needs more
- *   than PKV_STATIC_SCRATCH_BYTES is rejected with
- *   PKV_ERR_WORKSPACE_TOO_SMALL and a message; nothing is launched.  The
- *   optional prefill tail (see pkv_paged_attention_workspace_size) is used
- *   when it fits in the rest of the array.
+ *   Make that first call before any stream capture.  The cached address
+ *   belongs to the device's current context: a process that resets the
+ *   device (cudaDeviceReset) after that first call must not call this entry
+ *   point again.
+ * - Inputs: the same as pkv_paged_attention_varlen, which has no options,
+ *   so the cache holds fp16/bf16 values (no fp8 cache, sinks or non-paged
+ *   keys through this entry point).
+ * - Limit: a call whose decode split plan needs more than
+ *   PKV_STATIC_SCRATCH_BYTES is rejected with PKV_ERR_WORKSPACE_TOO_SMALL
+ *   and a message; nothing is launched.  The optional tail (see
+ *   pkv_paged_attention_workspace_size) is used when it fits in the rest of
+ *   the array.
  * - Sharing: all calls on a device share the one array and it keeps the
  *   last call's contents.  Nothing in it needs clearing: every scratch value
- *   a call reads was written earlier in the same call.  Calls that overlap on
- *   the GPU (different streams, or several host threads) race on the array
- *   and corrupt each other's results; order them on one stream.
+ *   a call reads was written earlier in the same call (the prefill item
+ *   counter is zeroed by the call).  Calls that overlap on the GPU
+ *   (different streams, or several host threads) race on the array and
+ *   corrupt each other's results; order them on one stream.
  */
 #define PKV_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
 

@@ -93,17 +93,33 @@ def request_rows(wl, b):
     return k, v
 
 
-def request_reference(wl, b, last_rows=None):
+def request_reference(wl, b, last_rows=None, row_range=None):
     """Oracle out [k, Hq, D] and lse [Hq, k] for the last k queries of
-    request b (all q_b queries when ``last_rows`` is None).
+    request b (all q_b queries when ``last_rows`` and ``row_range`` are
+    None), or for its queries i0 .. i1-1 with ``row_range = (i0, i1)``.
 
     The request's rows are laid out in a compact cache (its logical blocks
     in order), which the oracle's block-permutation invariance makes
     equivalent to the workload's own table.  The last k queries of a request
     are themselves a request with q_len = k over the same keys (the queries
-    are the last q_len positions), so sampling needs no other change.
+    are the last q_len positions), so sampling needs no other change.  A
+    causal request's queries i0 .. i1-1 see no key past position c + i1 - 1
+    (c = context length), so they are the last i1 - i0 queries of the same
+    request cut to its first c + i1 keys; row ranges need a causal workload.
     """
     k, v = request_rows(wl, b)
+    if row_range is not None:
+        if not wl.causal:
+            raise ValueError("row_range needs a causal workload")
+        i0, i1 = (int(x) for x in row_range)
+        q_b = int(wl.q_lens[b])
+        assert 0 <= i0 < i1 <= q_b, (i0, i1, q_b)
+        cut = int(wl.seq_lens[b]) - q_b + i1
+        k, v = k[:cut], v[:cut]
+        last_rows = i1 - i0
+        t_end = int(wl.cu_seqlens_q[b]) + i1
+    else:
+        t_end = int(wl.cu_seqlens_q[b + 1])
     BS = wl.block_size
     L = k.shape[0]
     nb = max(-(-L // BS), 1)
@@ -112,7 +128,7 @@ def request_reference(wl, b, last_rows=None):
     vc = np.full((nb, BS, Hkv, D), np.nan)
     kc.reshape(nb * BS, Hkv, D)[:L] = k
     vc.reshape(nb * BS, Hkv, D)[:L] = v
-    t0, t1 = int(wl.cu_seqlens_q[b]), int(wl.cu_seqlens_q[b + 1])
+    t0, t1 = int(wl.cu_seqlens_q[b]), t_end
     if last_rows is not None:
         t0 = max(t0, t1 - int(last_rows))
     q = _f64(wl.q[t0:t1])

@@ -97,7 +97,8 @@ attn_mma_kernel(const AttnParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = blockIdx.z / p.Hkv, g = blockIdx.z - (blockIdx.z / p.Hkv) * p.Hkv;
+  // grid: x = (request, KV head) unit, y = row tile, z = split
+  const int b = blockIdx.x / p.Hkv, g = blockIdx.x - (blockIdx.x / p.Hkv) * p.Hkv;
   const int G = p.G;
   const int q0 = p.cu_q[b];
   // rows past total_q (a cu_seqlens_q beyond the caller's buffers) are
@@ -117,17 +118,17 @@ attn_mma_kernel(const AttnParams p) {
             kmax);
   int lo = kmin, hi = kmax;
   if (p.chunk > 0) {
-    // The grid has gridDim.x splits; if the caller's max_seqlen_k was too
+    // The grid has gridDim.z splits; if the caller's max_seqlen_k was too
     // small for this request, the last split takes the rest of the range.
-    const int nsplit = split_count(kmin, kmax, p.chunk, gridDim.x);
-    if (static_cast<int>(blockIdx.x) >= nsplit) return;
-    split_bounds(kmin, kmax, p.chunk, nsplit, blockIdx.x, lo, hi);
+    const int nsplit = split_count(kmin, kmax, p.chunk, gridDim.z);
+    if (static_cast<int>(blockIdx.z) >= nsplit) return;
+    split_bounds(kmin, kmax, p.chunk, nsplit, blockIdx.z, lo, hi);
   }
   // Keys are only followed through the table while it has entries.
   // rows past the table (or, non-paged, past the K/V tensor) are not read
   const int L_tab = p.cu_k ? (koff < 0 ? 0 : max(0, min(L, p.total_k - koff)))
                            : min(L, p.max_blocks * p.BS);
-  if (L_tab < L && tid == 0 && blockIdx.x == 0 && blockIdx.y == 0)
+  if (L_tab < L && tid == 0 && blockIdx.z == 0 && blockIdx.y == 0)
     atomicOr(p.err, kErrBadTable);
 
   const T* __restrict__ Q = static_cast<const T*>(p.q);
@@ -477,7 +478,7 @@ attn_mma_kernel(const AttnParams p) {
         if (p.lse && c4 == 0) p.lse[static_cast<int64_t>(h) * p.total_q + tok] = lse;
       } else {
         float* dst = p.part_o +
-                     ((static_cast<int64_t>(blockIdx.x) * p.part_rows +
+                     ((static_cast<int64_t>(blockIdx.z) * p.part_rows +
                        part_row(p.part_tpr, b, q0, tok)) *
                           p.Hq + h) * D;
 #pragma unroll
@@ -485,7 +486,7 @@ attn_mma_kernel(const AttnParams p) {
           *reinterpret_cast<float2*>(dst + dn * 8 + 2 * c4) =
               make_float2(o[dn][2 * half] * inv, o[dn][2 * half + 1] * inv);
         if (c4 == 0)
-          p.part_lse[(static_cast<int64_t>(blockIdx.x) * p.Hq + h) *
+          p.part_lse[(static_cast<int64_t>(blockIdx.z) * p.Hq + h) *
                          p.part_rows +
                      part_row(p.part_tpr, b, q0, tok)] = lse;
       }
@@ -545,13 +546,13 @@ attn_mma_kernel(const AttnParams p) {
         if (p.lse && c == 0) p.lse[static_cast<int64_t>(h) * p.total_q + tok] = lse;
       } else {
         float* dst = p.part_o +
-                     ((static_cast<int64_t>(blockIdx.x) * p.part_rows +
+                     ((static_cast<int64_t>(blockIdx.z) * p.part_rows +
                        part_row(p.part_tpr, b, q0, tok)) *
                           p.Hq + h) * D + c;
         *reinterpret_cast<float4*>(dst) =
             make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
         if (c == 0)
-          p.part_lse[(static_cast<int64_t>(blockIdx.x) * p.Hq + h) *
+          p.part_lse[(static_cast<int64_t>(blockIdx.z) * p.Hq + h) *
                          p.part_rows +
                      part_row(p.part_tpr, b, q0, tok)] = lse;
       }
@@ -565,8 +566,8 @@ template <typename T>
 __global__ void __launch_bounds__(128)
 split_combine_kernel(const CombineParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.x * 4 + warp;
-  const int b = blockIdx.y;
+  const int h = blockIdx.y * 4 + warp;
+  const int b = blockIdx.x;
   if (h >= p.Hq) return;
   const int q0 = p.cu_q[b];
   const int q_len = min(p.cu_q[b + 1] - q0, p.total_q - q0);
@@ -639,13 +640,8 @@ static cudaError_t launch_cfg(const AttnParams& p, dim3 grid,
                               cudaStream_t stream) {
   using C = MmaCfg<D, RW, KWp, KT, ST, KV8>;
   auto kern = attn_mma_kernel<T, D, RW, KWp, KT, ST, KV8>;
-  static bool attr_set = false;   // per instantiation; idempotent if racing
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(
-        kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = smem_opt_in(reinterpret_cast<const void*>(kern), C::SMEM);
+  if (e != cudaSuccess) return e;
   note_launch();
   kern<<<grid, C::NT, C::SMEM, stream>>>(p);
   return cudaGetLastError();
@@ -685,21 +681,21 @@ static cudaError_t prefill_dispatch(const AttnParams& p, int D, dim3 grid,
 
 cudaError_t launch_decode_attn(const AttnParams& p, int D, bool bf16,
                                int grid_x, int grid_y, cudaStream_t stream) {
-  dim3 grid(grid_x, grid_y, p.batch * p.Hkv);
+  dim3 grid(static_cast<unsigned>(p.batch) * p.Hkv, grid_y, grid_x);
   return bf16 ? decode_dispatch<__nv_bfloat16>(p, D, grid, stream)
               : decode_dispatch<__half>(p, D, grid, stream);
 }
 
 cudaError_t launch_prefill_attn_mma(const AttnParams& p, int D, bool bf16,
                                     int grid_y, cudaStream_t stream) {
-  dim3 grid(1, grid_y, p.batch * p.Hkv);
+  dim3 grid(static_cast<unsigned>(p.batch) * p.Hkv, grid_y, 1);
   return bf16 ? prefill_dispatch<__nv_bfloat16>(p, D, grid, stream)
               : prefill_dispatch<__half>(p, D, grid, stream);
 }
 
 cudaError_t launch_split_combine(const CombineParams& p, bool bf16,
                                  cudaStream_t stream) {
-  dim3 grid((p.Hq + 3) / 4, p.batch);
+  dim3 grid(static_cast<unsigned>(p.batch), (p.Hq + 3) / 4);
   note_launch();
   if (bf16)
     split_combine_kernel<__nv_bfloat16><<<grid, 128, 0, stream>>>(p);

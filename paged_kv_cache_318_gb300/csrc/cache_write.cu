@@ -131,7 +131,8 @@ cudaError_t launch_cache_write_fp8(const void* key, const void* value,
   const int64_t total = num_tokens * Hkv * (D / 8);
   if (total == 0) return cudaSuccess;
   int64_t blocks = (total + 255) / 256;
-  if (blocks > 152 * 64) blocks = 152 * 64;
+  const int64_t cap = static_cast<int64_t>(current_sm_count()) * 64;
+  if (blocks > cap) blocks = cap;
   note_launch();
   if (bf16)
     cache_write_fp8_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), 256,
@@ -174,7 +175,8 @@ cudaError_t launch_cache_write(const void* key, const void* value,
   if (total == 0) return cudaSuccess;
   const int threads = 256;
   int64_t blocks = (total + threads - 1) / threads;
-  if (blocks > 152 * 64) blocks = 152 * 64;   // grid-stride beyond this
+  const int64_t cap = static_cast<int64_t>(current_sm_count()) * 64;
+  if (blocks > cap) blocks = cap;   // grid-stride beyond
   const int64_t num_slots = num_blocks * BS;
   note_launch();
   if (vec16) {

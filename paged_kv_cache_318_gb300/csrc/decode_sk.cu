@@ -1204,8 +1204,8 @@ struct Inst {
     int n = per_sm[dev].load(std::memory_order_acquire);
     if (n <= 0) {
       auto kern = decode_sk_kernel<T, D, NCW, KT, STAGES, KV8>;
-      cudaError_t e = cudaFuncSetAttribute(
-          kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+      cudaError_t e =
+          smem_opt_in(reinterpret_cast<const void*>(kern), C::SMEM);
       if (e != cudaSuccess) return e;
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, C::NT,
                                                         C::SMEM);

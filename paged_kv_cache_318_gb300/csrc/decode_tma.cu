@@ -81,7 +81,8 @@ decode_tma_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
   unsigned char* base = smem_raw + (base_u - raw_u);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = blockIdx.z / p.Hkv, g = blockIdx.z - (blockIdx.z / p.Hkv) * p.Hkv;
+  // grid: x = (request, KV head) unit, y = split
+  const int b = blockIdx.x / p.Hkv, g = blockIdx.x - (blockIdx.x / p.Hkv) * p.Hkv;
   const int G = p.G;
   const int q0 = p.cu_q[b];
   const int q_len = min(p.cu_q[b + 1] - q0, p.total_q - q0);
@@ -93,16 +94,16 @@ decode_tma_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
   // rows past the table (or, non-paged, past the K/V tensor) are not read
   const int L_tab = p.cu_k ? (koff < 0 ? 0 : max(0, min(L, p.total_k - koff)))
                            : min(L, p.max_blocks * p.BS);
-  if (L_tab < L && tid == 0 && blockIdx.x == 0)
+  if (L_tab < L && tid == 0 && blockIdx.y == 0)
     atomicOr(p.err, kErrBadTable);
 
   int kmin, kmax;
   key_range(L, q_len, 0, q_len - 1, p.causal, p.wl, p.wr, kmin, kmax);
   int lo = kmin, hi = kmax;
   if (p.chunk > 0) {
-    const int nsplit = split_count(kmin, kmax, p.chunk, gridDim.x);
-    if (static_cast<int>(blockIdx.x) >= nsplit) return;
-    split_bounds(kmin, kmax, p.chunk, nsplit, blockIdx.x, lo, hi);
+    const int nsplit = split_count(kmin, kmax, p.chunk, gridDim.y);
+    if (static_cast<int>(blockIdx.y) >= nsplit) return;
+    split_bounds(kmin, kmax, p.chunk, nsplit, blockIdx.y, lo, hi);
   }
   hi = min(hi, L_tab);
   const int kt0 = (lo / KT) * KT;
@@ -486,13 +487,13 @@ decode_tma_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
         p.lse[static_cast<int64_t>(h) * p.total_q + tok] = lse;
     } else {
       float* dst = p.part_o +
-                   ((static_cast<int64_t>(blockIdx.x) * p.part_rows +
+                   ((static_cast<int64_t>(blockIdx.y) * p.part_rows +
                        part_row(p.part_tpr, b, q0, tok)) *
                         p.Hq + h) * D + c;
       *reinterpret_cast<float4*>(dst) =
           make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
       if (c == 0)
-        p.part_lse[(static_cast<int64_t>(blockIdx.x) * p.Hq + h) *
+        p.part_lse[(static_cast<int64_t>(blockIdx.y) * p.Hq + h) *
                        p.part_rows +
                    part_row(p.part_tpr, b, q0, tok)] = lse;
     }
@@ -515,13 +516,8 @@ cudaError_t launch_cfg(const AttnParams& p, const CUtensorMap& mk,
                        cudaStream_t stream) {
   using C = Cfg<D, NCW, KT, STAGES>;
   auto kern = decode_tma_kernel<T, D, NCW, KT, STAGES>;
-  static bool attr_set = false;   // per instantiation; idempotent if racing
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(
-        kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = smem_opt_in(reinterpret_cast<const void*>(kern), C::SMEM);
+  if (e != cudaSuccess) return e;
   note_launch();
   kern<<<grid, C::NT, C::SMEM, stream>>>(p, mk, mv);
   return cudaGetLastError();
@@ -563,7 +559,7 @@ cudaError_t launch_decode_attn_tma(const AttnParams& a, int D, bool bf16,
       !make_kv_map(&mv, p.vc, bf16, D, p.BS, p.Hkv, p.num_blocks, p.c_sb,
                    p.c_sr, p.c_sh, RB, p.kv_order_hnd))
     return cudaErrorInvalidValue;
-  dim3 grid(grid_x, 1, p.batch * p.Hkv);
+  dim3 grid(static_cast<unsigned>(p.batch) * p.Hkv, grid_x, 1);
   return bf16 ? dtma::dispatch<__nv_bfloat16>(p, D, mk, mv, grid, stream)
               : dtma::dispatch<__half>(p, D, mk, mv, grid, stream);
 }

@@ -68,13 +68,24 @@ merge_kernel(void* __restrict__ out, const void* __restrict__ o1,
     const int h = static_cast<int>(row - static_cast<int64_t>(t) * H);
     const float a = l1[static_cast<int64_t>(h) * T + t];
     const float b = l2[static_cast<int64_t>(h) * T + t];
+    // (fmaxf would drop a NaN: a NaN LSE makes a NaN row instead)
+    const bool nan_in = isnan(a) || isnan(b);
+    const bool pa = a == INFINITY, pb = b == INFINITY;
     const float m = fmaxf(a, b);
-    const bool any = m != -INFINITY && !isnan(m);
-    const float base = any ? m : 0.f;
-    const float wa = (a == -INFINITY) ? 0.f : __expf(a - base);
-    const float wb = (b == -INFINITY) ? 0.f : __expf(b - base);
+    const bool finite = m != -INFINITY && m != INFINITY && !nan_in;
+    const float base = finite ? m : 0.f;
+    float wa, wb;
+    if (pa || pb) {
+      // a side with LSE +inf takes all the weight (the formula's limit)
+      wa = pa ? 1.f : 0.f;
+      wb = pb ? 1.f : 0.f;
+    } else {
+      wa = (a == -INFINITY || !finite) ? 0.f : __expf(a - base);
+      wb = (b == -INFINITY || !finite) ? 0.f : __expf(b - base);
+    }
     const float tot = wa + wb;
-    const float inv = tot > 0.f ? 1.f / tot : 0.f;
+    const float inv = nan_in ? __int_as_float(0x7fc00000)
+                             : (tot > 0.f ? 1.f / tot : 0.f);
     const int64_t e = row * D + c * 8;
     float va[8], vb[8], r[8];
     Pack8<TI>::load(o1, e, va);
@@ -89,7 +100,9 @@ merge_kernel(void* __restrict__ out, const void* __restrict__ o1,
     Pack8<TO>::store(out, e, r);
     if (lse_out && c == 0)
       lse_out[static_cast<int64_t>(h) * T + t] =
-          tot > 0.f ? base + __logf(tot) : -INFINITY;
+          nan_in ? __int_as_float(0x7fc00000)
+                 : ((pa || pb) ? INFINITY
+                               : (tot > 0.f ? base + __logf(tot) : -INFINITY));
   }
 }
 
@@ -99,7 +112,8 @@ static void launch_typed(void* out, const void* o1, const float* l1,
                          int H, int D, cudaStream_t stream) {
   const int64_t total = static_cast<int64_t>(T) * H * (D / 8);
   int64_t blocks = (total + 255) / 256;
-  if (blocks > 152 * 32) blocks = 152 * 32;
+  const int64_t cap = static_cast<int64_t>(current_sm_count()) * 32;
+  if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   note_launch();
   merge_kernel<TO, TI><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(

@@ -317,6 +317,36 @@ size_t required_workspace_bytes(int batch, int total_q, int max_seqlen_q,
 
 void set_last_error(const char* msg) { g_last_error = msg; }
 
+cudaError_t smem_opt_in(const void* kern, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static std::mutex mu;
+  constexpr int kSlots = 64;
+  static const void* kerns[kSlots] = {};
+  static uint64_t devs[kSlots] = {};      // bit d: done on device d
+  std::lock_guard<std::mutex> lk(mu);
+  int i = 0;
+  while (i < kSlots && kerns[i] && kerns[i] != kern) ++i;
+  const uint64_t bit = dev < 64 ? (1ull << dev) : 0;
+  if (i < kSlots && kerns[i] == kern && bit && (devs[i] & bit))
+    return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           bytes);
+  if (e != cudaSuccess) return e;
+  if (i < kSlots) {
+    kerns[i] = kern;
+    devs[i] |= bit;
+  }
+  return cudaSuccess;
+}
+
+int current_sm_count() {
+  int sms = 0;
+  if (device_info(nullptr, &sms) != PKV_OK || sms <= 0) return 1;
+  return sms;
+}
+
 }  // namespace pkv
 
 using namespace pkv;

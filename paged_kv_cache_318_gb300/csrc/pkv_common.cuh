@@ -306,6 +306,15 @@ __device__ __forceinline__ void finish_row(float m, float l, const float* sinks,
 // Count one kernel launch (reported by pkv_launch_count).
 void note_launch();
 
+// SM count of the current device (looked up once per device; 1 if the
+// lookup fails).  Grid-stride kernels size their grids from it.
+int current_sm_count();
+
+// Raise the dynamic shared-memory limit of kernel `kern` to `bytes` on the
+// current device, once per (kernel, device): the attribute is per device,
+// so one process driving several GPUs sets it on each.
+cudaError_t smem_opt_in(const void* kern, int bytes);
+
 // Set this thread's pkv_last_error message.
 void set_last_error(const char* msg);
 

@@ -2491,22 +2491,6 @@ static bool make_rows_map(CUtensorMap* map, const void* ptr, bool bf16, int D,
 
 int prefill_tc_block_keys(int) { return 64; }
 
-// Shared-memory opt-in once per kernel (a short list: 10 kernels).
-static cudaError_t smem_opt_in(const void* kern, int smem) {
-  static std::mutex mu;
-  static const void* done[16] = {};
-  std::lock_guard<std::mutex> lk(mu);
-  int i = 0;
-  while (i < 16 && done[i] && done[i] != kern) ++i;
-  if (i == 16 || !done[i]) {
-    cudaError_t e = cudaFuncSetAttribute(
-        kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    if (i < 16) done[i] = kern;
-  }
-  return cudaSuccess;
-}
-
 cudaError_t launch_prefill_split_combine(const CombineParams& p,
                                          int max_seqlen_q, bool bf16,
                                          cudaStream_t stream) {

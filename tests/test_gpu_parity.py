@@ -336,6 +336,34 @@ def test_merge_attn_states(cuda_device, dts):
     assert np.abs(got_l[fin] - rl[fin]).max() <= LSE_TOL
 
 
+def test_merge_non_finite_lse(cuda_device):
+    """LSE +inf takes all the weight, -inf drops a side (even a NaN output),
+    NaN propagates; the kernel against the oracle's reading."""
+    dev = cuda_device
+    inf, nan = math.inf, math.nan
+    T, H, D = 6, 2, 64
+    g = torch.Generator(device="cpu").manual_seed(11)
+    o1 = torch.randn(T, H, D, generator=g)
+    o2 = torch.randn(T, H, D, generator=g)
+    o1[2] = nan                      # a side without keys may hold anything
+    l1 = torch.tensor([[inf, 0.3, -inf, nan, inf, inf]] * H)
+    l2 = torch.tensor([[2.0, inf, 1.5, 0.0, -inf, inf]] * H)
+    out = torch.empty(T, H, D, dtype=torch.float32, device=dev)
+    lse = torch.empty(H, T, dtype=torch.float32, device=dev)
+    api.merge_attn_states(out, o1.to(dev), l1.to(dev), o2.to(dev),
+                          l2.to(dev), output_lse=lse)
+    torch.cuda.synchronize(dev)
+    ro, rl = merge_attn_states_ref(o1.double().numpy(), l1.double().numpy(),
+                                   o2.double().numpy(), l2.double().numpy())
+    got, gl = out.cpu().numpy(), lse.cpu().numpy()
+    assert np.array_equal(np.isnan(got), np.isnan(ro))
+    fin = ~np.isnan(ro)
+    assert np.abs(got[fin] - ro[fin]).max() <= 1e-5
+    assert np.array_equal(np.isnan(gl), np.isnan(rl))
+    assert np.array_equal(gl[~np.isnan(rl)], rl[~np.isnan(rl)]
+                          .astype(np.float32))
+
+
 # -------------------------------------------- full sizes, sampled outputs
 def _sampled(wl, dev, reqs, last_rows=None, cascade=False):
     b, out, lse = run_batch(wl, dev, cascade=cascade)
@@ -361,14 +389,40 @@ def test_full_batched_decode_sampled(cuda_device):
     _sampled(wl, cuda_device, [0, 17, 63])
 
 
+def _row_slices(wl, b, out, lse, tile=128):
+    """The first `tile` rows, a middle run of `tile` rows and the last 96
+    rows of prefill-class request b against the oracle."""
+    q = int(wl.q_lens[b])
+    t0 = int(wl.cu_seqlens_q[b])
+    mid = max(0, q // 2 - tile // 2)
+    for i0, i1 in ((0, min(tile, q)), (mid, min(q, mid + tile)),
+                   (max(0, q - 96), q)):
+        ref_o, ref_l = request_reference(wl, b, row_range=(i0, i1))
+        assert_close(wl, out[t0 + i0:t0 + i1], lse[:, t0 + i0:t0 + i1],
+                     ref_o, ref_l, "%s req %d rows %d-%d" % (wl.name, b, i0,
+                                                             i1))
+
+
 def test_full_prefill_sampled(cuda_device):
+    """Every request of the varlen prefill workload at full size: its first
+    128 packed rows (prefix-only key tiles and the first causal diagonal),
+    a middle tile and its last rows."""
     wl = workloads.prefill_with_prefix(device=cuda_device)
-    _sampled(wl, cuda_device, [0, 5], last_rows=96)
+    _, out, lse = run_batch(wl, cuda_device)
+    for b in range(wl.batch):
+        _row_slices(wl, b, out, lse)
 
 
 def test_full_mixed_sampled(cuda_device):
     wl = workloads.mixed_gemma(device=cuda_device)
-    _sampled(wl, cuda_device, [0, 61, 123, 124, 127], last_rows=64)
+    _, out, lse = run_batch(wl, cuda_device)
+    for b in (0, 61, 123):                       # decode-class
+        t0 = int(wl.cu_seqlens_q[b])
+        ref_o, ref_l = request_reference(wl, b)
+        assert_close(wl, out[t0:t0 + 1], lse[:, t0:t0 + 1], ref_o, ref_l,
+                     "mixed req %d" % b)
+    for b in range(124, wl.batch):               # the prefill chunks
+        _row_slices(wl, b, out, lse)
 
 
 def test_full_long_decode_sampled(cuda_device):

@@ -97,3 +97,23 @@ def test_shared_prefix_rows_are_request_zeros():
         assert np.array_equal(vb[:P], v0[:P])
         # own rows differ from request 0's
         assert not np.array_equal(kb[P:], k0[P:])
+
+
+@pytest.mark.parametrize("name", ["mixed", "prefill", "windowed"])
+def test_request_reference_row_ranges(name):
+    """Queries i0 .. i1-1 of a causal request (first rows, a middle run)
+    against the whole-batch oracle."""
+    wl = CASES[name]()
+    out, lse = full_reference(wl)
+    for b in range(wl.batch):
+        q = int(wl.q_lens[b])
+        t0 = int(wl.cu_seqlens_q[b])
+        for i0, i1 in ((0, min(3, q)), (q // 3, max(q // 3 + 1, 2 * q // 3)),
+                       (0, q)):
+            if i1 <= i0:
+                continue
+            o, l = request_reference(wl, b, row_range=(i0, i1))
+            np.testing.assert_allclose(o, out[t0 + i0:t0 + i1], rtol=0,
+                                       atol=1e-12)
+            np.testing.assert_allclose(l, lse[:, t0 + i0:t0 + i1], rtol=0,
+                                       atol=1e-12)
