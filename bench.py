@@ -455,15 +455,16 @@ def cache_write_bytes(wl, elem=2):
 
 
 def _time_flushed_ms(fn, flush, iters=10, warm=3):
-    """Mean device ms of fn, with the L2 flushed (a 256 MB write) before
-    each timed call and events around the call only."""
+    """Mean device ms of fn, with the L2 flushed before each timed call (a
+    read pass over 256 MB: the L2 then holds clean lines, so no write-back
+    of the flush competes with the call) and events around the call only."""
     for _ in range(warm):
         fn()
     ev = [(torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
     torch.cuda.synchronize()
     for a, b in ev:
-        flush.zero_()
+        flush.max()
         a.record()
         fn()
         b.record()
@@ -486,7 +487,7 @@ def other_workloads(dev, hbm_peak, tf_peak):
     # 92 MB fit in the L2, so the L2 is flushed before each timed call
     wl = workloads.prefill_with_prefix(seed=SEED_PREFILL, device=dev)
     b = DeviceBatch(wl, dev, poison=False)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = torch.zeros(256 << 20, dtype=torch.uint8, device=dev)
     rec("cache_write", "reshape_and_cache of the varlen prefill workload's "
         "%d new tokens (8 KV heads, D 128, bf16; L2 flushed before each "
         "call)" % len(wl.slot_mapping_new),
