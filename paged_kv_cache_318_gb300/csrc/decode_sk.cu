@@ -299,9 +299,15 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
   const int B = p.batch;
   const int per = (B + C::NT - 1) / C::NT;
   const int b_lo = min(B, tid * per), b_hi = min(B, b_lo + per);
+  // (the fold kernel may start: it waits for this grid before reading)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   long long mine = 0;
-  for (int b = b_lo; b < b_hi; ++b)
-    mine += static_cast<long long>(req_info<KT>(p, b, c == 0).n) * Hkv;
+  for (int b = b_lo; b < b_hi; ++b) {
+    const long long n =
+        static_cast<long long>(req_info<KT>(p, b, c == 0).n) * Hkv;
+    mine += n;
+    if (B <= kMaxPrefixReqs) pre[b] = static_cast<int>(n);  // (kept below
+  }                                                          // if N fits)
   long long incl = mine;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -321,8 +327,9 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
   if (table) {
     long long acc = excl;
     for (int b = b_lo; b < b_hi; ++b) {
+      const int n = pre[b];
       pre[b] = static_cast<int>(acc);
-      acc += static_cast<long long>(req_info<KT>(p, b, false).n) * Hkv;
+      acc += n;
     }
     if (tid == 0) pre[B] = static_cast<int>(N);
   }
@@ -1124,6 +1131,9 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
 template <typename T, int D>
 __global__ void __launch_bounds__(128) fold_kernel(const AttnParams p,
                                                    int chunks) {
+  // launched as a programmatic dependent of the decode grid: wait until it
+  // has finished and its writes are visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int c = blockIdx.x + 1;
   const int u = p.sk_marks[c - 1].y;
   if (u < 0) return;
@@ -1336,22 +1346,35 @@ cudaError_t launch_decode_attn_sk(const AttnParams& a, int D, bool bf16,
     return I::launch(p, mk, mv, ctas, stream);
   });
   if (e != cudaSuccess || l.chunks < 2) return e;
+  // the fold as a programmatic dependent launch: its blocks are resident
+  // (waiting) when the decode grid ends, instead of launching after it
   note_launch();
-  const int fb = l.chunks - 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(l.chunks - 1));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const int nch = l.chunks;
   switch (D) {
     case 64:
-      bf16 ? dsk::fold_kernel<__nv_bfloat16, 64><<<fb, 128, 0, stream>>>(p, l.chunks)
-           : dsk::fold_kernel<__half, 64><<<fb, 128, 0, stream>>>(p, l.chunks);
+      e = bf16 ? cudaLaunchKernelEx(&cfg, dsk::fold_kernel<__nv_bfloat16, 64>, p, nch)
+               : cudaLaunchKernelEx(&cfg, dsk::fold_kernel<__half, 64>, p, nch);
       break;
     case 128:
-      bf16 ? dsk::fold_kernel<__nv_bfloat16, 128><<<fb, 128, 0, stream>>>(p, l.chunks)
-           : dsk::fold_kernel<__half, 128><<<fb, 128, 0, stream>>>(p, l.chunks);
+      e = bf16 ? cudaLaunchKernelEx(&cfg, dsk::fold_kernel<__nv_bfloat16, 128>, p, nch)
+               : cudaLaunchKernelEx(&cfg, dsk::fold_kernel<__half, 128>, p, nch);
       break;
     default:
-      bf16 ? dsk::fold_kernel<__nv_bfloat16, 256><<<fb, 128, 0, stream>>>(p, l.chunks)
-           : dsk::fold_kernel<__half, 256><<<fb, 128, 0, stream>>>(p, l.chunks);
+      e = bf16 ? cudaLaunchKernelEx(&cfg, dsk::fold_kernel<__nv_bfloat16, 256>, p, nch)
+               : cudaLaunchKernelEx(&cfg, dsk::fold_kernel<__half, 256>, p, nch);
       break;
   }
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
