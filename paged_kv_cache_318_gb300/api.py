@@ -431,15 +431,31 @@ def merge_attn_states(output, prefix_output, prefix_lse, suffix_output,
     return output
 
 
+_SIDE_STREAMS = {}
+
+
+def _side_stream(device):
+    """One side stream per device for the cascade's prefix."""
+    key = torch.device(device).index
+    if key not in _SIDE_STREAMS:
+        _SIDE_STREAMS[key] = torch.cuda.Stream(device)
+    return _SIDE_STREAMS[key]
+
+
 def cascade_attention(output, query, key_cache, value_cache, cu_query_lens,
                       max_query_len, cu_prefix_query_lens, prefix_kv_lens,
                       suffix_kv_lens, max_kv_len, softmax_scale,
                       alibi_slopes, sliding_window, logits_soft_cap,
                       block_table, common_prefix_len, max_num_splits=0,
-                      workspace=None, s_aux=None):
+                      workspace=None, s_aux=None, overlap=True):
     """Shared-prefix attention: prefix (non-causal, block_table[:1]) +
     suffix (causal, block_table[:, P/BS:]) merged by LSE, as in vLLM v1's
-    ``cascade_attention``."""
+    ``cascade_attention``.
+
+    With ``overlap`` the prefix call (bound by the tensor cores) runs on a
+    side stream next to the suffix call (bound by HBM) on the current
+    stream, and the current stream waits for both before the merge; the
+    prefix kernel leaves some SMs to the suffix's CTAs."""
     if alibi_slopes is not None:
         raise ValueError("Cascade attention does not support ALiBi.")
     if tuple(sliding_window) != (-1, -1):
@@ -451,13 +467,26 @@ def cascade_attention(output, query, key_cache, value_cache, cu_query_lens,
     n_common = common_prefix_len // block_size
     if n_common <= 0:
         raise ValueError("common_prefix_len must be > 0")
-    prefix_out, prefix_lse = flash_attn_varlen_func(
-        query, key_cache, value_cache, num_tokens, cu_prefix_query_lens,
-        common_prefix_len, seqused_k=prefix_kv_lens,
-        softmax_scale=softmax_scale, causal=False,
-        window_size=sliding_window, softcap=logits_soft_cap,
-        block_table=block_table[:1], return_softmax_lse=True,
-        num_splits=max_num_splits, s_aux=s_aux)
+    def prefix():
+        return flash_attn_varlen_func(
+            query, key_cache, value_cache, num_tokens, cu_prefix_query_lens,
+            common_prefix_len, seqused_k=prefix_kv_lens,
+            softmax_scale=softmax_scale, causal=False,
+            window_size=sliding_window, softcap=logits_soft_cap,
+            block_table=block_table[:1], return_softmax_lse=True,
+            num_splits=max_num_splits, s_aux=s_aux)
+
+    main = torch.cuda.current_stream(query.device)
+    if overlap:
+        side = _side_stream(query.device)
+        side.wait_stream(main)
+        with torch.cuda.stream(side):
+            prefix_out, prefix_lse = prefix()
+        # (allocated on the side stream, read on the main one)
+        prefix_out.record_stream(main)
+        prefix_lse.record_stream(main)
+    else:
+        prefix_out, prefix_lse = prefix()
     suffix_out, suffix_lse = flash_attn_varlen_func(
         query, key_cache, value_cache, max_query_len, cu_query_lens,
         max_kv_len - common_prefix_len, seqused_k=suffix_kv_lens,
@@ -465,5 +494,7 @@ def cascade_attention(output, query, key_cache, value_cache, cu_query_lens,
         softcap=logits_soft_cap, block_table=block_table[:, n_common:],
         return_softmax_lse=True, num_splits=max_num_splits,
         workspace=workspace)
+    if overlap:
+        main.wait_stream(side)
     merge_attn_states(output, prefix_out, prefix_lse, suffix_out, suffix_lse)
     return output

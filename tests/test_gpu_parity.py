@@ -95,6 +95,28 @@ def test_cascade_small(cuda_device, dtype):
     assert_close(wl, out, None, ref_out, None, "cascade")
 
 
+def test_cascade_overlap_equals_serial(cuda_device):
+    """The prefix on a side stream (overlapping the suffix) gives the same
+    bits as the two calls back to back."""
+    wl = workloads.cascade_decode(batch=9, prefix=128, unique=70)
+    b = DeviceBatch(wl, cuda_device, cascade=True)
+    b.write_context()
+    b.write_new()
+    outs = []
+    for ov in (True, False):
+        api.cascade_attention(
+            b.out, b.q, b.key_cache, b.value_cache, b.cu_seqlens_q,
+            wl.max_seqlen_q, b.cu_prefix, b.prefix_lens, b.suffix_lens,
+            wl.max_seqlen_k, wl.softmax_scale, None, (-1, -1), 0.0,
+            b.block_table, wl.common_prefix_len, 0, overlap=ov)
+        torch.cuda.synchronize()
+        outs.append(b.out.clone())
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    ref_out, _ = full_reference(wl)
+    assert_close(wl, outs[0].float().cpu().numpy(), None, ref_out, None,
+                 "cascade overlap")
+
+
 # ------------------------------------------------------ feature matrix
 FEATURES = [
     # q_lens, seq_lens, Hq, Hkv, D, BS, kwargs
