@@ -702,6 +702,64 @@ def reference_arm(args):
     }
 
 
+# ------------------------------------------------------ profiling cases
+def profile_case(name, dev):
+    """Set up one workload and run its call a few times (warm-up included),
+    for a profiler to select launches from: batched_decode (the step: cache
+    write, then attention), fp8_decode (the batched decode over an E4M3
+    cache), cache_write (the varlen prefill workload's new rows), prefill
+    (the varlen prefill attention), mixed_prefill (the Gemma-like batch's
+    four D = 256 prefill chunks), cascade (shared-prefix decode)."""
+    if name == "batched_decode":
+        wl = workloads.batched_decode(seed=SEED_DECODE, device=dev)
+        b = DeviceBatch(wl, dev, poison=False)
+        b.write_context()
+        run = b.step
+    elif name == "fp8_decode":
+        wl = workloads.batched_decode(seed=SEED_DECODE, device=dev)
+        b = DeviceBatch(wl, dev, poison=False)
+        b.write_context()
+        b.write_new()
+        c8 = torch.zeros(wl.cache_shape(), dtype=torch.uint8, device=dev)
+        k8, v8 = c8.unbind(0)
+        ks = torch.tensor([0.02], device=dev)
+        vs = torch.tensor([0.02], device=dev)
+        for rk, rv, sl in ((b.k_ctx, b.v_ctx, b.slots_ctx),
+                           (b.k_new, b.v_new, b.slots_new)):
+            api.reshape_and_cache_flash(rk, rv, k8, v8, sl, "fp8", ks, vs)
+
+        def run():
+            api.flash_attn_varlen_func(
+                b.q, k8, v8, 1, b.cu_seqlens_q, wl.max_seqlen_k,
+                seqused_k=b.seqused_k, softmax_scale=wl.softmax_scale,
+                causal=True, block_table=b.block_table, out=b.out,
+                k_descale=ks, v_descale=vs)
+    elif name == "cache_write":
+        wl = workloads.prefill_with_prefix(seed=SEED_PREFILL, device=dev)
+        b = DeviceBatch(wl, dev, poison=False)
+        run = b.write_new
+    elif name in ("prefill", "mixed_prefill", "cascade"):
+        if name == "prefill":
+            wl = workloads.prefill_with_prefix(seed=SEED_PREFILL, device=dev)
+        elif name == "mixed_prefill":
+            wl = workloads.mixed_gemma(device=dev, n_decode=0)
+        else:
+            wl = workloads.cascade_decode(device=dev)
+        b = DeviceBatch(wl, dev, poison=False, cascade=name == "cascade")
+        b.write_context()
+        b.write_new()
+
+        def run():
+            b.attend(return_lse=False)
+    else:
+        raise SystemExit("unknown case %r" % name)
+    for _ in range(6):
+        run()
+    torch.cuda.synchronize()
+    api.check_device_errors(dev)
+    print(json.dumps({"case": name, "calls": 6, "ok": True}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -712,11 +770,23 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the other-workload rates")
+    ap.add_argument("--case", default=None,
+                    help="run one workload's call 6 times and exit (for a "
+                         "profiler): batched_decode, fp8_decode, "
+                         "cache_write, prefill, mixed_prefill, cascade")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
+    if args.case:
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        if not os.path.exists(_build.LIB_PATH):
+            _build.build()
+        api.load_library()
+        profile_case(args.case, dev)
+        return
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(reference_arm(args)), flush=True)

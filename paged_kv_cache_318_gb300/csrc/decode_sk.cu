@@ -1181,13 +1181,15 @@ __global__ void __launch_bounds__(128) fold_kernel(const AttnParams p,
   }
 }
 
-// Ring depth per configuration: two CTAs per SM, each holding about 96 KB
-// of K/V in flight (D = 256: 64 KB).
+// Ring depth per configuration (two CTAs per SM).  D = 128, 16-bit: two
+// stages of 32 KB (measured on GB300 against three: the same on the batched
+// decode, 0.610 against 0.633-0.645 ms on 8 x 131072 keys); E4M3: three
+// stages of 128 keys (32 KB); D = 64: six of 16 KB.
 #ifndef PKV_DSK_D64_STAGES
 #define PKV_DSK_D64_STAGES 6
 #endif
 #ifndef PKV_DSK_D128_STAGES
-#define PKV_DSK_D128_STAGES 3
+#define PKV_DSK_D128_STAGES 2
 #endif
 #ifndef PKV_DSK_D256_STAGES
 #define PKV_DSK_D256_STAGES 2
