@@ -5,12 +5,18 @@ TEST INFRASTRUCTURE ONLY (see oracle/__init__.py).
 Sources: "vllm/v1/attention/backends/flash_attn.py" (kv_cache_dtype "fp8" /
 "fp8_e4m3" views the cache as float8_e4m3fn; the same per-tensor scalars
 layer._k_scale / layer._v_scale go to reshape_and_cache_flash and, as
-k_descale / v_descale, to the attention call) and the FlashInfer backend page
-(_trtllm_prefill_attn_kvfp8_dequant: value = fp8 * k_scale).
+k_descale / v_descale, to the attention call; with an fp8 cache the query
+goes through scaled_fp8_quant(query, layer._q_scale) and the call gets
+q_descale = layer._q_scale) and the FlashInfer backend page
+(_trtllm_prefill_attn_kvfp8_dequant: value = fp8 * k_scale;
+get_xqa_bmm1_scale: the logit scale times q_scale and k_scale).
 
 Readings: the cache write stores code = e4m3(x / scale), the quotient taken
 in float32 and rounded to the nearest E4M3 value (ties to even code),
-saturating at +-448; a cached code reads back as decode(code) * scale.
+saturating at +-448; a cached code reads back as decode(code) * scale.  The
+query quantization is the same map with the query's scale (a static
+per-tensor scale: the pages always pass one), and a query code reads back
+as decode(code) * q_scale.
 
 E4M3 "fn" per its definition: 1 sign bit, 4 exponent bits (bias 7),
 3 mantissa bits; exponent 0 holds subnormals m/8 * 2^-6; the all-ones code
@@ -71,3 +77,17 @@ def reshape_and_cache_fp8_ref(key, value, key_cache, value_cache,
         blk, off = divmod(s, block_size)
         key_cache[blk, off] = quantize_ref(key[t], k_scale)
         value_cache[blk, off] = quantize_ref(value[t], v_scale)
+
+
+def scaled_fp8_quant_ref(x, scale) -> np.ndarray:
+    """Static per-tensor quantization of a [tokens, heads * head_size] (or
+    any-shaped) array: E4M3 codes of x / scale, elementwise as quantize_ref,
+    in x's shape."""
+    x = np.asarray(x, dtype=np.float32)
+    return quantize_ref(x, scale).reshape(x.shape)
+
+
+def dequantize_ref(codes, scale) -> np.ndarray:
+    """float64 values of E4M3 codes read back with a per-tensor scale:
+    decode(code) * scale, the scale as the float32 the device holds."""
+    return e4m3_decode(codes) * np.float64(np.float32(scale))

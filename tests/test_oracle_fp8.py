@@ -3,8 +3,9 @@ import numpy as np
 import pytest
 import torch
 
-from oracle.fp8 import (e4m3_decode, e4m3_encode, quantize_ref,
-                        reshape_and_cache_fp8_ref)
+from oracle.fp8 import (dequantize_ref, e4m3_decode, e4m3_encode,
+                        quantize_ref, reshape_and_cache_fp8_ref,
+                        scaled_fp8_quant_ref)
 
 
 def test_decode_matches_torch_float8_e4m3fn():
@@ -62,3 +63,27 @@ def test_fp8_cache_write_round_trip_within_half_ulp():
     back = e4m3_decode(flat[slots]) * 0.02
     rel = np.abs(back - key) / np.maximum(np.abs(key), 2.0 ** -6 * 0.02)
     assert rel.max() <= 2.0 ** -4 + 1e-9            # 3 mantissa bits
+
+
+def test_scaled_fp8_quant_hand_values():
+    # quotients 0.6, -3.4, 1000, 0 (scale 0.5): 0.6 is nearer 0.625 (0x32)
+    # than 0.5625; 3.4 nearer 3.5 (0x46) than 3.25; 1000 saturates to 448
+    codes = scaled_fp8_quant_ref([[0.3, -1.7], [500.0, 0.0]], 0.5)
+    assert codes.tolist() == [[0x32, 0xC6], [0x7E, 0x00]]
+    assert e4m3_decode([0x32, 0xC6]).tolist() == [0.625, -3.5]
+
+
+def test_scaled_fp8_quant_keeps_shape_and_reads_back():
+    rng = np.random.default_rng(2)
+    q = rng.standard_normal((5, 4, 32)).astype(np.float32)
+    s = 0.01
+    codes = scaled_fp8_quant_ref(q, s)
+    assert codes.shape == q.shape and codes.dtype == np.uint8
+    flat = scaled_fp8_quant_ref(q.reshape(5, 128), s)
+    assert np.array_equal(codes.reshape(5, 128), flat)
+    back = dequantize_ref(codes, s)
+    rel = np.abs(back - q) / np.maximum(np.abs(q), 2.0 ** -6 * s)
+    assert rel.max() <= 2.0 ** -4 + 1e-9            # 3 mantissa bits
+    # the read-back value is the code's value times the float32 scale
+    assert back[0, 0, 0] == e4m3_decode([codes[0, 0, 0]])[0] * \
+        np.float64(np.float32(s))
