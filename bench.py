@@ -574,7 +574,22 @@ def other_workloads(dev, hbm_peak, tf_peak):
             causal=True, block_table=b.block_table, out=b.out,
             k_descale=ks, v_descale=vs)), _kv_bytes(wl, 1), "GB/s",
         hbm_peak)
-    del b, c8
+    # the same with E4M3 queries, as the vLLM FA backend runs an fp8 cache:
+    # scaled_fp8_quant of the query, then the attention call
+    qs = torch.tensor([0.02], device=dev)
+    q8 = torch.empty(b.q.shape, dtype=torch.float8_e4m3fn, device=dev)
+
+    def fp8q_call():
+        api.scaled_fp8_quant(b.q, qs, out=q8)
+        api.flash_attn_varlen_func(
+            q8, k8, v8, 1, b.cu_seqlens_q, wl.max_seqlen_k,
+            seqused_k=b.seqused_k, softmax_scale=wl.softmax_scale,
+            causal=True, block_table=b.block_table, out=b.out,
+            k_descale=ks, v_descale=vs, q_descale=qs)
+    rec("fp8q_decode", "batched decode workload, E4M3 queries and cache "
+        "(query quantization + attention call; fp8 bytes)",
+        _time_ms(fp8q_call), _kv_bytes(wl, 1), "GB/s", hbm_peak)
+    del b, c8, q8
     wl = workloads.build_workload("long_prefill", 324, [2048], [8192], 32, 8,
                                   128, 64, device=dev)
     b = DeviceBatch(wl, dev, poison=False)
@@ -709,11 +724,20 @@ def reference_arm(args):
 def profile_case(name, dev):
     """Set up one workload and run its call a few times (warm-up included),
     for a profiler to select launches from: batched_decode (the step: cache
-    write, then attention), fp8_decode (the batched decode over an E4M3
-    cache), cache_write (the varlen prefill workload's new rows), prefill
+    write, then attention), batched_decode_persistent (the same step on the
+    persistent decode kernel), fp8_decode (the batched decode over an E4M3
+    cache), fp8q_decode (the same with E4M3 queries), cache_write (the varlen prefill workload's new rows), prefill
     (the varlen prefill attention), mixed_prefill (the Gemma-like batch's
     four D = 256 prefill chunks), cascade (shared-prefix decode)."""
     if name == "batched_decode":
+        wl = workloads.batched_decode(seed=SEED_DECODE, device=dev)
+        b = DeviceBatch(wl, dev, poison=False)
+        b.write_context()
+        run = b.step
+    elif name == "batched_decode_persistent":
+        # the persistent decode kernel on the same step, for a side-by-side
+        # capture with the per-unit kernel the library picks here
+        api.set_decode_kernel(api.DECODE_PERSISTENT)
         wl = workloads.batched_decode(seed=SEED_DECODE, device=dev)
         b = DeviceBatch(wl, dev, poison=False)
         b.write_context()
@@ -737,6 +761,28 @@ def profile_case(name, dev):
                 seqused_k=b.seqused_k, softmax_scale=wl.softmax_scale,
                 causal=True, block_table=b.block_table, out=b.out,
                 k_descale=ks, v_descale=vs)
+    elif name == "fp8q_decode":
+        wl = workloads.batched_decode(seed=SEED_DECODE, device=dev)
+        b = DeviceBatch(wl, dev, poison=False)
+        b.write_context()
+        b.write_new()
+        c8 = torch.zeros(wl.cache_shape(), dtype=torch.uint8, device=dev)
+        k8, v8 = c8.unbind(0)
+        ks = torch.tensor([0.02], device=dev)
+        vs = torch.tensor([0.02], device=dev)
+        qs = torch.tensor([0.02], device=dev)
+        for rk, rv, sl in ((b.k_ctx, b.v_ctx, b.slots_ctx),
+                           (b.k_new, b.v_new, b.slots_new)):
+            api.reshape_and_cache_flash(rk, rv, k8, v8, sl, "fp8", ks, vs)
+        q8 = torch.empty(b.q.shape, dtype=torch.float8_e4m3fn, device=dev)
+
+        def run():
+            api.scaled_fp8_quant(b.q, qs, out=q8)
+            api.flash_attn_varlen_func(
+                q8, k8, v8, 1, b.cu_seqlens_q, wl.max_seqlen_k,
+                seqused_k=b.seqused_k, softmax_scale=wl.softmax_scale,
+                causal=True, block_table=b.block_table, out=b.out,
+                k_descale=ks, v_descale=vs, q_descale=qs)
     elif name == "cache_write":
         wl = workloads.prefill_with_prefix(seed=SEED_PREFILL, device=dev)
         b = DeviceBatch(wl, dev, poison=False)
@@ -775,8 +821,10 @@ def main():
                     help="skip the other-workload rates")
     ap.add_argument("--case", default=None,
                     help="run one workload's call 6 times and exit (for a "
-                         "profiler): batched_decode, fp8_decode, "
-                         "cache_write, prefill, mixed_prefill, cascade")
+                         "profiler): batched_decode, "
+                         "batched_decode_persistent, fp8_decode, "
+                         "fp8q_decode, cache_write, prefill, mixed_prefill, "
+                         "cascade")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 

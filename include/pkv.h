@@ -242,11 +242,29 @@ typedef struct {
    * and prefill_fixed_split_size 4096 under batch invariance) and the
    * flash_attn.py page (num_splits = 1 under vllm_is_batch_invariant). */
   int fixed_split_size;
+  /* q_fp8 != 0: q holds E4M3 codes, one byte per element (q strides in
+   * bytes, rows 16-byte aligned), and a query value reads back as
+   * code * (*q_scale) (a device float scalar, the scale given to
+   * pkv_scaled_fp8_quant).  Needs kv_cache_fp8 (PKV_ERR_UNSUPPORTED
+   * otherwise); `dtype` then names the output's type.  The logits are
+   * softmax_scale * q_scale * k_scale * sum_d code_q * code_k.  The
+   * persistent decode kernel multiplies the query and key codes on the E4M3
+   * tensor-core path; the other kernels read an exact 16-bit copy of the
+   * query codes that the call writes to its workspace.  Source:
+   * "vllm/v1/attention/backends/flash_attn.py" (git view and v0.9.0.1 docs),
+   * FlashAttentionImpl.forward (with an fp8 cache the query goes through
+   * scaled_fp8_quant(query, layer._q_scale) and the call gets
+   * q_descale = layer._q_scale); the FlashInfer backend page,
+   * get_xqa_bmm1_scale (bmm1 scale = scale * q_scale * k_scale). */
+  int q_fp8;
+  const float* q_scale;
 } pkv_attention_options;
 
 /* Workspace bytes for pkv_paged_attention_varlen_opts with these options
  * (an fp8 cache with prefill-class requests needs room for 16-bit copies of
- * up to batch * max_blocks_per_seq pages).  (size_t)-1 on bad arguments. */
+ * up to batch * max_blocks_per_seq pages; an fp8 query, for a 16-bit copy
+ * of the query codes: total_q * num_heads * head_size * 2 bytes and one
+ * scalar).  (size_t)-1 on bad arguments. */
 PKV_API size_t pkv_paged_attention_workspace_size_opts(
     int batch, int total_q, int max_seqlen_q, int max_seqlen_k,
     int num_heads, int num_kv_heads, int head_size, int block_size,
@@ -271,6 +289,84 @@ PKV_API pkv_status pkv_paged_attention_varlen_opts(
     void* workspace, size_t workspace_bytes,
     pkv_dtype dtype, pkv_stream_t stream,
     const pkv_attention_options* opts);
+
+/*
+ * pkv_cascade_attention -- shared-prefix ("cascade") attention in one call.
+ *
+ * Source: "vllm/v1/attention/backends/flash_attn.py", cascade_attention:
+ * the prefix call (every query over the common_prefix_len keys of the
+ * shared blocks, block_table[:1], non-causal, cu_prefix_query_lens =
+ * [0, num_tokens], prefix_kv_lens = [common_prefix_len], with s_aux), the
+ * suffix call (block_table[:, common_prefix_len // block_size:],
+ * suffix_kv_lens, causal) and merge_attn_states(output, prefix_output,
+ * prefix_lse, suffix_output, suffix_lse).  Those three steps, with the same
+ * meaning for every argument; window and ALiBi are not taken (the page
+ * rejects both).  The prefix runs unsplit.  With `overlap` the suffix's
+ * decode kernel (16-bit caches) is launched as a programmatic dependent of
+ * the prefix kernel: it starts once the prefix's CTAs are resident and
+ * takes the SMs they leave free, and its last CTA waits for the prefix grid
+ * to end before the merge.  With overlap = 0 the steps run one after the
+ * other; both give the same bits.
+ *
+ * output : [num_tokens, num_heads, head_size] contiguous, `dtype`.
+ * query  : as in pkv_paged_attention_varlen (element strides).
+ * cu_query_lens [batch+1], suffix_kv_lens [batch], cu_prefix_query_lens
+ *          [2], prefix_kv_lens [1]: device int32.  max_kv_len bounds
+ *          common_prefix_len + suffix_kv_lens[b].
+ * block_table : [batch, >= max_blocks_per_seq] int32; the first
+ *          common_prefix_len / block_size entries of row 0 are the shared
+ *          blocks (every row holds them first).
+ * num_splits : split-KV of the suffix call (0 = the library's plan).
+ * opts   : sinks (prefix only), fp8 cache and query; NULL = none.  No
+ *          cu_seqlens_k or fixed split (PKV_ERR_INVALID_ARG).
+ * workspace : pkv_cascade_attention_workspace_size bytes, 256-byte aligned.
+ */
+PKV_API size_t pkv_cascade_attention_workspace_size(
+    int batch, int num_tokens, int max_query_len, int max_kv_len,
+    int common_prefix_len, int num_heads, int num_kv_heads, int head_size,
+    int block_size, int max_blocks_per_seq, int num_splits,
+    const pkv_attention_options* opts);
+
+PKV_API pkv_status pkv_cascade_attention(
+    void* output, const void* query, int64_t q_stride_tok,
+    int64_t q_stride_head, const void* key_cache, const void* value_cache,
+    const int64_t cache_strides[4], const int32_t* cu_query_lens,
+    int max_query_len, const int32_t* cu_prefix_query_lens,
+    const int32_t* prefix_kv_lens, const int32_t* suffix_kv_lens,
+    int max_kv_len, int batch, int num_tokens, float softmax_scale,
+    float logits_soft_cap, const int32_t* block_table,
+    int64_t block_table_stride, int max_blocks_per_seq,
+    int common_prefix_len, int num_heads, int num_kv_heads, int head_size,
+    int block_size, int64_t num_blocks, int num_splits, int overlap,
+    void* workspace, size_t workspace_bytes, pkv_dtype dtype,
+    pkv_stream_t stream, const pkv_attention_options* opts);
+
+/*
+ * pkv_scaled_fp8_quant -- per-tensor E4M3 quantization of a query matrix.
+ *
+ * Source: "vllm/v1/attention/backends/flash_attn.py" (git view and the
+ * v0.9.0.1 docs page), FlashAttentionImpl.forward: with an fp8 KV cache the
+ * query, viewed as [num_tokens, num_heads * head_size], goes through
+ * ops.scaled_fp8_quant(query, layer._q_scale) before the attention call;
+ * the FlashInfer backend page, maybe_quant_query (the same call).  The
+ * scale is static (given); the pages never call the dynamic form.
+ *
+ * out[r, c] = RN_satfinite_e4m3(in[r, c] / *scale) for r < rows, c < cols:
+ * the quotient in IEEE float32, rounded to the nearest E4M3 value (ties to
+ * the even code), saturating at +-448; NaN gives the code 0x7F.
+ *
+ * in     : [rows, cols] fp16/bf16 (`dtype`), row stride in_row_stride
+ *          elements; out: [rows, cols] uint8 codes, row stride
+ *          out_row_stride bytes.  cols % 16 == 0; both base pointers and
+ *          row strides 16-byte aligned (PKV_ERR_UNSUPPORTED otherwise).
+ * scale  : device float32 scalar, > 0.
+ * Enqueued on `stream`; no host synchronisation.
+ */
+PKV_API pkv_status pkv_scaled_fp8_quant(const void* in, int64_t in_row_stride,
+                                        void* out, int64_t out_row_stride,
+                                        int64_t rows, int cols,
+                                        const float* scale, pkv_dtype dtype,
+                                        pkv_stream_t stream);
 
 /*
  * Bytes of workspace pkv_paged_attention_varlen needs for these arguments

@@ -47,7 +47,8 @@ class _Options(ctypes.Structure):
     _fields_ = [("sinks", ctypes.c_void_p), ("kv_cache_fp8", ctypes.c_int),
                 ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
                 ("cu_seqlens_k", ctypes.c_void_p), ("total_k", ctypes.c_int),
-                ("fixed_split_size", ctypes.c_int)]
+                ("fixed_split_size", ctypes.c_int), ("q_fp8", ctypes.c_int),
+                ("q_scale", ctypes.c_void_p)]
 
 
 _FP8_CACHE = (torch.float8_e4m3fn, torch.uint8)
@@ -107,6 +108,16 @@ def load_library():
             vp, vp, vp, vp, i32]
         lib.pkv_use_cascade_attention.restype = i32
         lib.pkv_use_cascade_attention.argtypes = [i32, vp] + [i32] * 8
+        lib.pkv_cascade_attention_workspace_size.restype = sz
+        lib.pkv_cascade_attention_workspace_size.argtypes = [i32] * 11 + [vp]
+        lib.pkv_cascade_attention.restype = i32
+        lib.pkv_cascade_attention.argtypes = (
+            [vp, vp, i64, i64, vp, vp, c_i64p, vp, i32, vp, vp, vp, i32, i32,
+             i32, f32, f32, vp, i64, i32, i32, i32, i32, i32, i32, i64, i32,
+             i32, vp, sz, i32, vp, vp])
+        lib.pkv_scaled_fp8_quant.restype = i32
+        lib.pkv_scaled_fp8_quant.argtypes = [vp, i64, vp, i64, i64, i32, vp,
+                                             i32, vp]
         lib.pkv_set_prefill_kernel.restype = i32
         lib.pkv_set_prefill_kernel.argtypes = [i32]
         lib.pkv_set_decode_kernel.restype = i32
@@ -238,6 +249,37 @@ def reshape_and_cache_flash(key, value, key_cache, value_cache, slot_mapping,
         _stream(key)))
 
 
+def scaled_fp8_quant(input, scale, out=None):
+    """Static per-tensor E4M3 quantization: codes of ``input / scale``.
+
+    input [rows, cols] (or [tokens, heads, head_size], taken as [tokens,
+    heads * head_size]) fp16/bf16 with contiguous rows; scale a float32
+    device tensor of one element.  Returns (codes, scale), codes a
+    float8_e4m3fn tensor of input's shape, as the vLLM FA backend's
+    ``ops.scaled_fp8_quant(query, layer._q_scale)`` does
+    ("vllm/v1/attention/backends/flash_attn.py").
+    """
+    lib = load_library()
+    if scale is None or scale.dtype != torch.float32 or scale.numel() < 1:
+        raise ValueError("scale must be a float32 tensor (static scale)")
+    shape = input.shape
+    x = input.reshape(shape[0], -1) if input.dim() == 3 else input
+    if x.dim() != 2 or x.stride(-1) != 1:
+        raise ValueError("input must be [rows, cols] with contiguous rows")
+    if out is None:
+        out = torch.empty(shape, dtype=torch.float8_e4m3fn,
+                          device=input.device)
+    elif out.dtype not in _FP8_CACHE or out.shape != shape:
+        raise ValueError("out must be float8_e4m3fn/uint8 of input's shape")
+    o = out.reshape(shape[0], -1) if out.dim() == 3 else out
+    if o.stride(-1) != 1:
+        raise ValueError("out rows must be contiguous")
+    _check(lib.pkv_scaled_fp8_quant(
+        _ptr(x), x.stride(0), _ptr(o), o.stride(0), x.shape[0], x.shape[1],
+        _ptr(scale), _dtype(x), _stream(x)))
+    return out, scale
+
+
 # --------------------------------------------------------------- attention
 
 def paged_attention_workspace_size(batch, total_q, max_seqlen_q, max_seqlen_k,
@@ -260,7 +302,7 @@ def flash_attn_varlen_func(q, k, v, max_seqlen_q, cu_seqlens_q, max_seqlen_k,
                            return_softmax_lse=False, out=None, num_splits=0,
                            cu_seqlens_k=None, workspace=None, s_aux=None,
                            k_descale=None, v_descale=None,
-                           fixed_split_size=0):
+                           fixed_split_size=0, q_descale=None):
     """Varlen attention over a paged KV cache, or over plain K/V rows.
 
     q [T, Hq, D].  Paged: k, v are cache views [num_blocks, block_size, Hkv,
@@ -268,6 +310,8 @@ def flash_attn_varlen_func(q, k, v, max_seqlen_q, cu_seqlens_q, max_seqlen_k,
     Non-paged (encoder / cache-free prefill): k, v are [Tk, Hkv, D] and
     cu_seqlens_k int32 [B+1] gives each request's rows.  cu_seqlens_q int32
     [B+1].  fixed_split_size > 0 makes decode split-KV batch-invariant.
+    An fp8 (E4M3) q, from ``scaled_fp8_quant``, needs an fp8 cache, its
+    scale as ``q_descale`` and ``out`` (which names the output type).
     Returns out (and lse [Hq, T] float32 when return_softmax_lse).
     """
     lib = load_library()
@@ -304,6 +348,15 @@ def flash_attn_varlen_func(q, k, v, max_seqlen_q, cu_seqlens_q, max_seqlen_k,
     if Dk != D:
         raise ValueError("q and k head_size differ")
     kv8 = k.dtype in _FP8_CACHE
+    q8 = q.dtype in _FP8_CACHE
+    if q8:
+        if not kv8:
+            raise NotImplementedError("an fp8 query needs an fp8 cache")
+        if q_descale is None or q_descale.dtype != torch.float32 or \
+                q_descale.numel() < 1:
+            raise ValueError("an fp8 query needs a float32 q_descale")
+        if out is None:
+            raise ValueError("an fp8 query needs `out` (the output type)")
     if kv8:
         if nonpaged:
             raise NotImplementedError("fp8 K/V needs the paged cache")
@@ -318,6 +371,8 @@ def flash_attn_varlen_func(q, k, v, max_seqlen_q, cu_seqlens_q, max_seqlen_k,
         softmax_scale = D ** -0.5
     if out is None:
         out = torch.empty_like(q)
+    elif not q8 and out.dtype != q.dtype:
+        raise ValueError("out must have q's dtype")
     lse = None
     if return_softmax_lse:
         lse = torch.empty((Hq, T), dtype=torch.float32, device=q.device)
@@ -333,6 +388,9 @@ def flash_attn_varlen_func(q, k, v, max_seqlen_q, cu_seqlens_q, max_seqlen_k,
         opts.kv_cache_fp8 = 1
         opts.k_scale = k_descale.data_ptr()
         opts.v_scale = v_descale.data_ptr()
+    if q8:
+        opts.q_fp8 = 1
+        opts.q_scale = q_descale.data_ptr()
     if nonpaged:
         opts.cu_seqlens_k = cu_seqlens_k.data_ptr()
         opts.total_k = k.shape[0]
@@ -356,7 +414,7 @@ def flash_attn_varlen_func(q, k, v, max_seqlen_q, cu_seqlens_q, max_seqlen_k,
         bt_stride, max_blocks, Hq, Hkv, D, BS, NB,
         float(softmax_scale), int(bool(causal)), int(window_size[0]),
         int(window_size[1]), float(softcap or 0.0), _ptr(alibi_slopes),
-        int(num_splits), _ptr(lse), _ptr(workspace), ws_bytes, _dtype(q),
+        int(num_splits), _ptr(lse), _ptr(workspace), ws_bytes, _dtype(out),
         _stream(q), ctypes.byref(opts)))
     if return_softmax_lse:
         return out, lse
@@ -434,12 +492,19 @@ def merge_attn_states(output, prefix_output, prefix_lse, suffix_output,
 _SIDE_STREAMS = {}
 
 
-def _side_stream(device):
-    """One side stream per device for the cascade's prefix."""
-    key = torch.device(device).index
-    if key not in _SIDE_STREAMS:
-        _SIDE_STREAMS[key] = torch.cuda.Stream(device)
-    return _SIDE_STREAMS[key]
+def cascade_attention_workspace_size(batch, num_tokens, max_query_len,
+                                     max_kv_len, common_prefix_len,
+                                     num_heads, num_kv_heads, head_size,
+                                     block_size, max_blocks_per_seq,
+                                     num_splits=0) -> int:
+    """Workspace bytes of ``cascade_attention`` (16-bit cache and query)."""
+    n = load_library().pkv_cascade_attention_workspace_size(
+        batch, num_tokens, max_query_len, max_kv_len, common_prefix_len,
+        num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq,
+        num_splits, None)
+    if n == ctypes.c_size_t(-1).value:
+        raise ValueError("invalid cascade shapes")
+    return n
 
 
 def cascade_attention(output, query, key_cache, value_cache, cu_query_lens,
@@ -447,54 +512,76 @@ def cascade_attention(output, query, key_cache, value_cache, cu_query_lens,
                       suffix_kv_lens, max_kv_len, softmax_scale,
                       alibi_slopes, sliding_window, logits_soft_cap,
                       block_table, common_prefix_len, max_num_splits=0,
-                      workspace=None, s_aux=None, overlap=True):
-    """Shared-prefix attention: prefix (non-causal, block_table[:1]) +
-    suffix (causal, block_table[:, P/BS:]) merged by LSE, as in vLLM v1's
-    ``cascade_attention``.
+                      workspace=None, s_aux=None, overlap=True,
+                      k_descale=None, v_descale=None, q_descale=None):
+    """Shared-prefix attention: prefix (non-causal, block_table[:1], with the
+    sinks) + suffix (causal, block_table[:, P/BS:]) merged by LSE, as in
+    vLLM v1's ``cascade_attention``, in one library call.
 
-    With ``overlap`` the prefix call (bound by the tensor cores) runs on a
-    side stream next to the suffix call (bound by HBM) on the current
-    stream, and the current stream waits for both before the merge; the
-    prefix kernel leaves some SMs to the suffix's CTAs."""
+    With ``overlap`` the suffix's decode kernel starts beside the prefix
+    kernel on the SMs it leaves free (same bits as ``overlap=False``).
+    ``max_num_splits`` is the suffix's split-KV; the prefix runs unsplit.
+    ``output`` must be contiguous [num_tokens, num_heads, head_size]."""
+    lib = load_library()
     if alibi_slopes is not None:
         raise ValueError("Cascade attention does not support ALiBi.")
     if tuple(sliding_window) != (-1, -1):
         raise ValueError("Cascade attention does not support sliding window.")
-    num_tokens = query.shape[0]
-    block_size = key_cache.shape[-3]
-    if common_prefix_len % block_size != 0:
+    T, Hq, D = query.shape
+    NB, BS, Hkv, Dk = key_cache.shape
+    if common_prefix_len % BS != 0:
         raise ValueError("common_prefix_len must be a multiple of block_size")
-    n_common = common_prefix_len // block_size
-    if n_common <= 0:
+    if common_prefix_len <= 0:
         raise ValueError("common_prefix_len must be > 0")
-    def prefix():
-        return flash_attn_varlen_func(
-            query, key_cache, value_cache, num_tokens, cu_prefix_query_lens,
-            common_prefix_len, seqused_k=prefix_kv_lens,
-            softmax_scale=softmax_scale, causal=False,
-            window_size=sliding_window, softcap=logits_soft_cap,
-            block_table=block_table[:1], return_softmax_lse=True,
-            num_splits=max_num_splits, s_aux=s_aux)
-
-    main = torch.cuda.current_stream(query.device)
-    if overlap:
-        side = _side_stream(query.device)
-        side.wait_stream(main)
-        with torch.cuda.stream(side):
-            prefix_out, prefix_lse = prefix()
-        # (allocated on the side stream, read on the main one)
-        prefix_out.record_stream(main)
-        prefix_lse.record_stream(main)
-    else:
-        prefix_out, prefix_lse = prefix()
-    suffix_out, suffix_lse = flash_attn_varlen_func(
-        query, key_cache, value_cache, max_query_len, cu_query_lens,
-        max_kv_len - common_prefix_len, seqused_k=suffix_kv_lens,
-        softmax_scale=softmax_scale, causal=True, window_size=sliding_window,
-        softcap=logits_soft_cap, block_table=block_table[:, n_common:],
-        return_softmax_lse=True, num_splits=max_num_splits,
-        workspace=workspace)
-    if overlap:
-        main.wait_stream(side)
-    merge_attn_states(output, prefix_out, prefix_lse, suffix_out, suffix_lse)
+    if not output.is_contiguous() or output.shape != query.shape[:2] + (D,):
+        raise ValueError("output must be contiguous [T, Hq, D]")
+    if query.stride(-1) != 1:
+        raise ValueError("query head_size dim must be contiguous")
+    for t in (cu_query_lens, cu_prefix_query_lens, prefix_kv_lens,
+              suffix_kv_lens, block_table):
+        if t.dtype != torch.int32:
+            raise ValueError("lengths and block_table must be int32")
+    opts = _Options()
+    if s_aux is not None:
+        if s_aux.dtype != torch.float32 or s_aux.shape != (Hq,):
+            raise ValueError("s_aux (sinks) must be float32 [num_heads]")
+        opts.sinks = s_aux.data_ptr()
+    kv8 = key_cache.dtype in _FP8_CACHE
+    q8 = query.dtype in _FP8_CACHE
+    if kv8:
+        if k_descale is None or v_descale is None:
+            raise ValueError("an fp8 cache needs k_descale and v_descale")
+        opts.kv_cache_fp8 = 1
+        opts.k_scale = k_descale.data_ptr()
+        opts.v_scale = v_descale.data_ptr()
+    elif key_cache.dtype != query.dtype:
+        raise NotImplementedError("q and cache dtypes must match")
+    if q8:
+        if q_descale is None:
+            raise ValueError("an fp8 query needs q_descale")
+        opts.q_fp8 = 1
+        opts.q_scale = q_descale.data_ptr()
+    batch = suffix_kv_lens.shape[0]
+    max_blocks = block_table.shape[1]
+    need = lib.pkv_cascade_attention_workspace_size(
+        batch, T, int(max_query_len), int(max_kv_len),
+        int(common_prefix_len), Hq, Hkv, D, BS, max_blocks,
+        int(max_num_splits), ctypes.byref(opts))
+    if need == ctypes.c_size_t(-1).value:
+        raise ValueError("invalid cascade shapes")
+    if workspace is None or workspace.numel() * workspace.element_size() < \
+            need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
+    cs = _cache_strides(key_cache, value_cache)
+    _check(lib.pkv_cascade_attention(
+        _ptr(output), _ptr(query), query.stride(0), query.stride(1),
+        _ptr(key_cache), _ptr(value_cache), cs, _ptr(cu_query_lens),
+        int(max_query_len), _ptr(cu_prefix_query_lens), _ptr(prefix_kv_lens),
+        _ptr(suffix_kv_lens), int(max_kv_len), batch, T,
+        float(softmax_scale), float(logits_soft_cap or 0.0),
+        _ptr(block_table), block_table.stride(0), max_blocks,
+        int(common_prefix_len), Hq, Hkv, D, BS, NB, int(max_num_splits),
+        int(bool(overlap)), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _dtype(output),
+        _stream(query), ctypes.byref(opts)))
     return output

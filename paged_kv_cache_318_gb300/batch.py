@@ -59,10 +59,10 @@ class DeviceBatch:
             self.cu_prefix = dev([0, T], torch.int32)
             self.prefix_lens = dev([P], torch.int32)
             self.suffix_lens = dev(wl.seq_lens - P, torch.int32)
-            n = api.paged_attention_workspace_size(
-                wl.batch, T, wl.max_seqlen_q, wl.max_seqlen_k - P,
+            n = api.cascade_attention_workspace_size(
+                wl.batch, T, wl.max_seqlen_q, wl.max_seqlen_k, P,
                 wl.num_heads, wl.num_kv_heads, wl.head_size, wl.block_size,
-                True, (-1, -1), wl.num_splits)
+                wl.block_table.shape[1], wl.num_splits)
         else:
             n = api.paged_attention_workspace_size(
                 wl.batch, T, wl.max_seqlen_q, wl.max_seqlen_k, wl.num_heads,

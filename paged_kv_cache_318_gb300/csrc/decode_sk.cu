@@ -50,6 +50,13 @@
 // the dot products are unchanged).  k_scale joins the logit scale and
 // v_scale multiplies the output.
 //
+// E4M3 queries (Q8, with an E4M3 cache).  The query rows arrive as codes,
+// which convert exactly to the f16 fragments above (no scaling: every code
+// is an f16 value), and q_scale joins the logit scale.  (The E4M3 form of
+// mma.sync, m16n8k32, which would take the K code words as they are, was
+// measured on GB300 at the same speed with 13 % more instructions issued,
+// so the codes go through f16 like the cache's.)
+//
 // Every mbarrier wait is bounded (kWaitLimitNs).  A wait that runs out
 // records kErrTimeout and raises the CTA's abort flag; the consumers agree
 // on leaving at a barrier that reduces their flags (bar.red.or), and the
@@ -71,7 +78,7 @@ constexpr int kMaxDevices = 64;
 // chunk there); larger batches locate it with one scan over the requests.
 constexpr int kMaxPrefixReqs = 512;
 
-template <int D, int NCW, int KT, int STAGES, bool KV8>
+template <int D, int NCW, int KT, int STAGES, bool KV8, bool Q8 = false>
 struct Cfg {
   static constexpr int NT = (NCW + 1) * 32;     // consumers + producer warp
   static constexpr int CT = NCW * 32;           // consumer threads
@@ -79,8 +86,9 @@ struct Cfg {
   static constexpr int NKT = KW / 8;            // n8 tiles of S per warp
   static constexpr int BOXC = KV8 ? 128 : 64;   // columns per TMA box
   static constexpr int NCB = D / BOXC;          // 128-byte column blocks
-  static constexpr int CPR = D / 8;             // 16-byte chunks per Q row
-  static constexpr int ROW_BYTES = D * 2;       // one 16-bit Q row
+  static constexpr int QEB = Q8 ? 1 : 2;       // bytes per query element
+  static constexpr int CPR = D * QEB / 16;      // 16-byte chunks per Q row
+  static constexpr int ROW_BYTES = D * QEB;     // one Q row
   static constexpr int CB_BYTES = KT * 128;     // one column block of a tile
   static constexpr int TILE_BYTES = NCB * CB_BYTES;
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
@@ -111,6 +119,7 @@ struct Cfg {
                 "the warps' states fit in one ring stage");
   static_assert((D / NCW) % 4 == 0, "column slices of whole float4s");
   static_assert(OFF_PRE % 8 == 0 && OFF_MISC % 8 == 0, "alignment");
+  static_assert(!Q8 || KV8, "E4M3 queries need an E4M3 cache");
   static constexpr int KTILE = KT;
 };
 
@@ -239,11 +248,11 @@ __device__ __forceinline__ float elem_f32<__half>(uint32_t w, int hi) {
       static_cast<unsigned short>(hi ? (w >> 16) : (w & 0xffffu))));
 }
 
-template <typename T, int D, int NCW, int KT, int STAGES, bool KV8>
+template <typename T, int D, int NCW, int KT, int STAGES, bool KV8, bool Q8>
 __global__ void __launch_bounds__((NCW + 1) * 32, 2)
 decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v) {
-  using C = Cfg<D, NCW, KT, STAGES, KV8>;
+  using C = Cfg<D, NCW, KT, STAGES, KV8, Q8>;
   // MMA input type: the cache's type, or f16 for E4M3 codes
   using MT = typename std::conditional<KV8, __half, T>::type;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -374,7 +383,7 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
     constexpr int CPR = C::CPR;
     const int RB = p.rb;
     const int nb_max = KT / RB;
-    const T* Q = static_cast<const T*>(p.q);
+    const char* Q = static_cast<const char*>(p.q);
     // (request, KV head, tile) of tile position P of the sequence
     auto locate = [&](long long P, int& b, int& g, int& t, int& n) {
       int lo = 0, hi = B;          // pre[lo] <= P < pre[hi]
@@ -453,10 +462,12 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
         for (int i = lane; i < 16 * CPR; i += 32) {
           const int r = i / CPR, ch = i - (i / CPR) * CPR;
           const bool ok = r < ri.rows;
-          const T* src = Q;
+          const char* src = Q;
           if (ok)
-            src = Q + static_cast<int64_t>(ri.q0 + r / G) * p.q_st +
-                  static_cast<int64_t>(g * G + r % G) * p.q_sh + ch * 8;
+            src = Q + (static_cast<int64_t>(ri.q0 + r / G) * p.q_st +
+                       static_cast<int64_t>(g * G + r % G) * p.q_sh) *
+                          C::QEB +
+                  ch * 16;
           cp_async_16(qraw(slot) + swz<C::ROW_BYTES>(r, ch), src,
                       ok ? 16 : 0);
         }
@@ -577,6 +588,7 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
   const float inv_cap = p.softcap > 0.f ? 1.f / p.softcap : 0.f;
   const float vscale = p.v_scale ? *p.v_scale : 1.f;
   const float kscale = p.k_scale ? *p.k_scale : 1.f;
+  const float qscale = Q8 ? *p.q_scale : 1.f;
   T* __restrict__ OUT = static_cast<T*>(p.out);
   int it = 0;
 
@@ -585,7 +597,28 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
     const bool got = mbar_wait_lim(ufull(slot), (k >> 1) & 1, abort_flag,
                         p.err, p.wait_ns);
     float qshift_f = 1.f;    // 2^shift: the query scaling of an fp8 unit
-    if constexpr (KV8) {
+    if constexpr (Q8) {
+      if (bar_or(C::CT, !got)) return;
+      // f16 A fragments of the codes for every k16 step, in the order of
+      // the 16-bit query path below (d = 16 ks + 4 c + {0,1} in registers
+      // 0/1, + {2,3} in registers 2/3; rows g and g + 8)
+      for (int i = tid; i < (D / 16) * 32; i += C::CT) {
+        const int ks = i >> 5, ln = i & 31;
+        const int gg = ln >> 2, cc = ln & 3;
+        const int d = 16 * ks + 4 * cc;
+        uint32_t a[4];
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          e4m3x4_to_f16(lds32(qraw(slot) +
+                              swz<C::ROW_BYTES>(gg + 8 * h, d >> 4) + (d & 15)),
+                        a[h], a[2 + h]);
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
+                         qfrag + (ks * 32 + ln) * 16),
+                     "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3])
+                     : "memory");
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(C::CT) : "memory");
+    } else if constexpr (KV8) {
       // largest |q| of the unit's rows (bf16 queries only)
       float mx = 0.f;
       if (got && std::is_same<T, __nv_bfloat16>::value) {
@@ -675,7 +708,7 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
       if (okA) slopeA = p.alibi[g * G + rA % G];
       if (okB) slopeB = p.alibi[g * G + rB % G];
     }
-    const float qk_scale = p.scale * kscale * qshift_f;
+    const float qk_scale = p.scale * kscale * qshift_f * qscale;
     const float scale_log2 = qk_scale * kLog2e;
     int full_lo = lo, full_hi = hi;
     {
@@ -1206,16 +1239,17 @@ __global__ void __launch_bounds__(128) fold_kernel(const AttnParams p,
 
 // Per instantiation: the shared-memory opt-in done on which devices, and
 // the resident CTAs per SM found there.
-template <typename T, int D, int NCW, int KT, int STAGES, bool KV8>
+template <typename T, int D, int NCW, int KT, int STAGES, bool KV8,
+          bool Q8>
 struct Inst {
-  using C = Cfg<D, NCW, KT, STAGES, KV8>;
+  using C = Cfg<D, NCW, KT, STAGES, KV8, Q8>;
   static std::atomic<int> per_sm[kMaxDevices];
 
   static cudaError_t prepare(int dev, int* ctas_per_sm) {
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     int n = per_sm[dev].load(std::memory_order_acquire);
     if (n <= 0) {
-      auto kern = decode_sk_kernel<T, D, NCW, KT, STAGES, KV8>;
+      auto kern = decode_sk_kernel<T, D, NCW, KT, STAGES, KV8, Q8>;
       cudaError_t e =
           smem_opt_in(reinterpret_cast<const void*>(kern), C::SMEM);
       if (e != cudaSuccess) return e;
@@ -1233,43 +1267,52 @@ struct Inst {
                             const CUtensorMap& mv, int grid,
                             cudaStream_t stream) {
     note_launch();
-    decode_sk_kernel<T, D, NCW, KT, STAGES, KV8>
+    decode_sk_kernel<T, D, NCW, KT, STAGES, KV8, Q8>
         <<<grid, C::NT, C::SMEM, stream>>>(p, mk, mv);
     return cudaGetLastError();
   }
 };
-template <typename T, int D, int NCW, int KT, int STAGES, bool KV8>
-std::atomic<int> Inst<T, D, NCW, KT, STAGES, KV8>::per_sm[kMaxDevices];
+template <typename T, int D, int NCW, int KT, int STAGES, bool KV8,
+          bool Q8>
+std::atomic<int> Inst<T, D, NCW, KT, STAGES, KV8, Q8>::per_sm[kMaxDevices];
 
-// The configuration per (head size, cache type); f(Inst) is called with
-// the matching instantiation.
-template <typename T, bool KV8, typename F>
+// The configuration per (head size, cache type, query type); f(Inst) is
+// called with the matching instantiation.
+template <typename T, bool KV8, bool Q8, typename F>
 cudaError_t with_cfg(int D, F&& f) {
   if constexpr (KV8) {
     switch (D) {
       case 128:
         return f(Inst<T, 128, 4, PKV_DSK_FP8_D128_KT, PKV_DSK_FP8_D128_STAGES,
-                      true>{});
+                      true, Q8>{});
       case 256:
-        return f(Inst<T, 256, 2, 32, PKV_DSK_FP8_D256_STAGES, true>{});
+        return f(Inst<T, 256, 2, 32, PKV_DSK_FP8_D256_STAGES, true, Q8>{});
       default: return cudaErrorInvalidValue;
     }
   } else {
     switch (D) {
-      case 64: return f(Inst<T, 64, 4, 64, PKV_DSK_D64_STAGES, false>{});
-      case 128: return f(Inst<T, 128, 4, 64, PKV_DSK_D128_STAGES, false>{});
-      case 256: return f(Inst<T, 256, 2, 32, PKV_DSK_D256_STAGES, false>{});
+      case 64:
+        return f(Inst<T, 64, 4, 64, PKV_DSK_D64_STAGES, false, false>{});
+      case 128:
+        return f(Inst<T, 128, 4, 64, PKV_DSK_D128_STAGES, false, false>{});
+      case 256:
+        return f(Inst<T, 256, 2, 32, PKV_DSK_D256_STAGES, false, false>{});
       default: return cudaErrorInvalidValue;
     }
   }
 }
 
+template <typename T, typename F>
+cudaError_t dispatch_t(bool kv8, bool q8, int D, F&& f) {
+  if (!kv8) return with_cfg<T, false, false>(D, f);
+  return q8 ? with_cfg<T, true, true>(D, f) : with_cfg<T, true, false>(D, f);
+}
+
 template <typename F>
-cudaError_t dispatch(bool bf16, bool kv8, int D, F&& f) {
-  if (bf16)
-    return kv8 ? with_cfg<__nv_bfloat16, true>(D, f)
-               : with_cfg<__nv_bfloat16, false>(D, f);
-  return kv8 ? with_cfg<__half, true>(D, f) : with_cfg<__half, false>(D, f);
+cudaError_t dispatch(bool bf16, bool kv8, bool q8, int D, F&& f) {
+  if (q8 && !kv8) return cudaErrorInvalidValue;
+  return bf16 ? dispatch_t<__nv_bfloat16>(kv8, q8, D, f)
+              : dispatch_t<__half>(kv8, q8, D, f);
 }
 
 }  // namespace dsk
@@ -1278,12 +1321,13 @@ bool decode_sk_supported(int D, bool kv8) {
   return kv8 ? (D == 128 || D == 256) : (D == 64 || D == 128 || D == 256);
 }
 
-cudaError_t decode_sk_ctas(int D, bool bf16, bool kv8, int sms, int* ctas) {
+cudaError_t decode_sk_ctas(int D, bool bf16, bool kv8, bool q8, int sms,
+                           int* ctas) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   int per = 0;
-  e = dsk::dispatch(bf16, kv8, D, [&](auto inst) {
+  e = dsk::dispatch(bf16, kv8, q8, D, [&](auto inst) {
     return decltype(inst)::prepare(dev, &per);
   });
   if (e != cudaSuccess) return e;
@@ -1322,7 +1366,7 @@ cudaError_t launch_decode_attn_sk(const AttnParams& a, int D, bool bf16,
                                   int ctas, int rows, void* scratch,
                                   cudaStream_t stream) {
   AttnParams p = a;
-  const bool kv8 = p.kv_fp8 != 0;
+  const bool kv8 = p.kv_fp8 != 0, q8 = p.q_fp8 != 0;
   const SkLayout l = sk_layout(D, ctas, rows);
   char* ws = static_cast<char*>(scratch);
   p.part_o = reinterpret_cast<float*>(ws + l.o_off);
@@ -1330,7 +1374,7 @@ cudaError_t launch_decode_attn_sk(const AttnParams& a, int D, bool bf16,
   p.sk_marks = reinterpret_cast<int2*>(ws + l.marks_off);
   p.sk_chunks = l.chunks;
   p.sk_rows = rows;
-  cudaError_t e = dsk::dispatch(bf16, kv8, D, [&](auto inst) {
+  cudaError_t e = dsk::dispatch(bf16, kv8, q8, D, [&](auto inst) {
     using I = decltype(inst);
     const int KT = I::C::KTILE;
     int RB = 16;

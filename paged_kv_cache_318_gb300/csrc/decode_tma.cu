@@ -71,9 +71,9 @@ __device__ __forceinline__ uint32_t kv_off(int r, int ch) {
 }
 
 template <typename T, int D, int NCW, int KT, int STAGES>
-__global__ void __launch_bounds__((NCW + 1) * 32)
-decode_tma_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v) {
+__device__ __forceinline__ void decode_tma_body(const AttnParams& p,
+                                                const CUtensorMap& tm_k,
+                                                const CUtensorMap& tm_v) {
   using C = Cfg<D, NCW, KT, STAGES>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t raw_u = smem_u32(smem_raw);
@@ -500,6 +500,26 @@ decode_tma_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
   }
 }
 
+// The kernel.  As a programmatic dependent launch (p.pdl_done set: the
+// launch may start while the grid before it in the stream still runs, once
+// that grid's CTAs have all signalled), every CTA counts itself done in
+// *p.pdl_done and the last one waits for the grid before to complete, so
+// this grid ends after it and work queued after this grid sees both
+// grids' results.  Without a preceding grid the wait returns at once.
+template <typename T, int D, int NCW, int KT, int STAGES>
+__global__ void __launch_bounds__((NCW + 1) * 32)
+decode_tma_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v) {
+  decode_tma_body<T, D, NCW, KT, STAGES>(p, tm_k, tm_v);
+  if (p.pdl_done && threadIdx.x == 0) {
+    const unsigned total = gridDim.x * gridDim.y;
+    if (atomicAdd(reinterpret_cast<unsigned*>(p.pdl_done), 1u) == total - 1) {
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      *p.pdl_done = 0;
+    }
+  }
+}
+
 #ifndef PKV_DTMA_D128_STAGES
 #define PKV_DTMA_D128_STAGES 2
 #endif
@@ -519,7 +539,24 @@ cudaError_t launch_cfg(const AttnParams& p, const CUtensorMap& mk,
   cudaError_t e = smem_opt_in(reinterpret_cast<const void*>(kern), C::SMEM);
   if (e != cudaSuccess) return e;
   note_launch();
-  kern<<<grid, C::NT, C::SMEM, stream>>>(p, mk, mv);
+  if (!p.pdl_done) {
+    kern<<<grid, C::NT, C::SMEM, stream>>>(p, mk, mv);
+    return cudaGetLastError();
+  }
+  // programmatic dependent launch: CTAs may start on the SMs the grid
+  // before leaves free, once all of that grid's CTAs have signalled
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(C::NT);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, p, mk, mv);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -107,8 +107,20 @@ Plan make_plan(int batch, int total_q, int max_q, int max_k, int Hq, int Hkv,
   Plan pl;
   const int G = Hq / Hkv;
   if (batch == 0 || max_q == 0) return pl;
-  pl.decode = true;
+  // Every request has at least total_q - (batch - 1) * max_q queries.  When
+  // that many rows exceed the decode kernel's, no request is decode-class:
+  // the decode kernel is not launched and the prefill launch takes every
+  // request (so one with fewer queries, possible only when max_q
+  // understates a request, is still computed).
+  const int64_t min_q =
+      static_cast<int64_t>(total_q) - static_cast<int64_t>(batch - 1) * max_q;
+  pl.decode = min_q * G <= kDecodeRows;
   pl.prefill = static_cast<int64_t>(max_q) * G > kDecodeRows;
+  if (!pl.decode) {
+    pl.prefill_tiles = static_cast<int>(
+        (static_cast<int64_t>(max_q) * G + 63) / 64);
+    return pl;
+  }
   if (pl.prefill)
     pl.prefill_tiles = static_cast<int>(
         (static_cast<int64_t>(max_q) * G + 63) / 64);
@@ -221,10 +233,10 @@ int sk_rows(int G, int max_q) {
   const int64_t r = static_cast<int64_t>(G) * max_q;
   return r < kDecodeRows ? static_cast<int>(r) : kDecodeRows;
 }
-size_t sk_scratch_bytes(int D, bool kv8, int sms, int rows) {
+size_t sk_scratch_bytes(int D, bool kv8, bool q8, int sms, int rows) {
   int a = 0, b = 0;
-  if (decode_sk_ctas(D, true, kv8, sms, &a) != cudaSuccess ||
-      decode_sk_ctas(D, false, kv8, sms, &b) != cudaSuccess)
+  if (decode_sk_ctas(D, true, kv8, q8, sms, &a) != cudaSuccess ||
+      decode_sk_ctas(D, false, kv8, q8, sms, &b) != cudaSuccess)
     return 0;
   return decode_sk_workspace_bytes(D, a > b ? a : b, rows);
 }
@@ -263,6 +275,12 @@ size_t fp8_mock_bytes(int batch, int max_blocks, int BS, int Hkv, int D) {
   const size_t pages = static_cast<size_t>(batch) * max_blocks;
   return 2 * align256(pages * BS * Hkv * D * 2) + align256(pages * 4);
 }
+// fp8 query: a 16-bit copy of the codes [total_q, Hq, D], then 256 bytes
+// holding k_scale * q_scale.
+size_t q16_bytes(int total_q, int Hq, int D) {
+  return align256(static_cast<size_t>(total_q) * Hq * D * 2) + 256;
+}
+bool q_fp8_of(const pkv_attention_options* o) { return o && o->q_fp8; }
 
 bool non_paged(const pkv_attention_options* o) {
   return o && o->cu_seqlens_k;
@@ -515,9 +533,10 @@ size_t pkv_paged_attention_workspace_size_opts(
                                   num_splits, fixed_split_of(opts))
                  : 1,
       total_q, num_heads, head_size);
+  const bool q8 = fp8 && q_fp8_of(opts);
   const size_t skb =
       sk_candidate(num_splits, fixed_split_of(opts), head_size, fp8)
-          ? sk_scratch_bytes(head_size, fp8, sms,
+          ? sk_scratch_bytes(head_size, fp8, q8, sms,
                              sk_rows(num_heads / num_kv_heads, max_seqlen_q))
           : 0;
   size_t need = pl.workspace;
@@ -527,6 +546,7 @@ size_t pkv_paged_attention_workspace_size_opts(
            fp8_mock_bytes(batch, max_blocks_per_seq, block_size, num_kv_heads,
                           head_size);
   }
+  if (q8) need = align256(need) + q16_bytes(total_q, num_heads, head_size);
   return make_layout(need, pl.prefill, skb, split_bytes).total;
 }
 
@@ -553,7 +573,7 @@ size_t pkv_paged_attention_workspace_size(int batch, int total_q,
       total_q, num_heads, head_size);
   const size_t skb =
       sk_candidate(num_splits, 0, head_size, false)
-          ? sk_scratch_bytes(head_size, false, sms,
+          ? sk_scratch_bytes(head_size, false, false, sms,
                              sk_rows(num_heads / num_kv_heads, max_seqlen_q))
           : 0;
   return make_layout(pl.workspace, pl.prefill, skb, split_bytes).total;
@@ -582,7 +602,14 @@ pkv_status pkv_paged_attention_varlen(
       dtype, stream, nullptr);
 }
 
-pkv_status pkv_paged_attention_varlen_opts(
+}  // extern "C"
+
+namespace {
+
+// The attention call; pdl_done != null launches the TMA decode kernel (when
+// the call takes it) as a programmatic dependent of the grid queued before
+// the call, with that zeroed counter.
+pkv_status attention_impl(
     const void* q, int64_t q_stride_tok, int64_t q_stride_head,
     const void* key_cache, const void* value_cache,
     const int64_t cache_strides[4], void* out, int64_t o_stride_tok,
@@ -594,7 +621,7 @@ pkv_status pkv_paged_attention_varlen_opts(
     int window_left, int window_right, float softcap,
     const float* alibi_slopes, int num_splits, float* softmax_lse,
     void* workspace, size_t workspace_bytes, pkv_dtype dtype,
-    pkv_stream_t stream, const pkv_attention_options* opts) {
+    pkv_stream_t stream, const pkv_attention_options* opts, int* pdl_done) {
   const bool nonpaged = non_paged(opts);
   pkv_status st = check_attn_shape(batch, total_q, max_seqlen_q, max_seqlen_k,
                                    num_heads, num_kv_heads, head_size,
@@ -636,10 +663,15 @@ pkv_status pkv_paged_attention_varlen_opts(
     return fail(PKV_ERR_INVALID_ARG, "fp8 cache needs k_scale and v_scale");
   if (kv8 && head_size % 16 != 0)
     return fail(PKV_ERR_UNSUPPORTED, "fp8 cache needs head_size % 16 == 0");
-  const int eb = 2, cb = kv8 ? 1 : 2;
+  const bool q8 = q_fp8_of(opts);
+  if (q8 && !kv8)
+    return fail(PKV_ERR_UNSUPPORTED, "an fp8 query needs an fp8 cache");
+  if (q8 && !opts->q_scale)
+    return fail(PKV_ERR_INVALID_ARG, "an fp8 query needs q_scale");
+  const int eb = 2, cb = kv8 ? 1 : 2, qb = q8 ? 1 : 2;
   if (!aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache) ||
-      !aligned16(out) || !stride16(q_stride_tok, eb) ||
-      !stride16(q_stride_head, eb) || !stride16(o_stride_tok, eb) ||
+      !aligned16(out) || !stride16(q_stride_tok, qb) ||
+      !stride16(q_stride_head, qb) || !stride16(o_stride_tok, eb) ||
       !stride16(o_stride_head, eb) ||
       !stride16(nonpaged ? 0 : cache_strides[0], cb) ||
       !stride16(cache_strides[1], cb) || !stride16(cache_strides[2], cb))
@@ -656,11 +688,15 @@ pkv_status pkv_paged_attention_varlen_opts(
                             num_heads, num_kv_heads, head_size, causal, wl, wr,
                             num_splits, sms, fixed_split);
   size_t need = pl.workspace;
-  size_t mock_off = 0;
+  size_t mock_off = 0, q16_off = 0;
   if (kv8 && pl.prefill) {
     mock_off = align256(pl.workspace);
     need = mock_off + fp8_mock_bytes(batch, max_blocks_per_seq, block_size,
                                      num_kv_heads, head_size);
+  }
+  if (q8) {
+    q16_off = align256(need);
+    need = q16_off + q16_bytes(total_q, num_heads, head_size);
   }
   if (need > 0) {
     if (workspace_bytes < need || !workspace)
@@ -699,7 +735,7 @@ pkv_status pkv_paged_attention_varlen_opts(
        (dsel == PKV_DECODE_AUTO && (kv8 || many_units)));
   const int skr = sk_rows(num_heads / num_kv_heads, max_seqlen_q);
   const size_t skb = sk_candidate(num_splits, fixed_split, head_size, kv8)
-                         ? sk_scratch_bytes(head_size, kv8, sms, skr)
+                         ? sk_scratch_bytes(head_size, kv8, q8, sms, skr)
                          : 0;
   const Layout lay = make_layout(need, pl.prefill, skb, sb);
   const bool ws_ok = workspace &&
@@ -708,7 +744,8 @@ pkv_status pkv_paged_attention_varlen_opts(
   void* sk_scratch = nullptr;
   if (sk_ok && pl.decode && skb > 0 && ws_ok &&
       workspace_bytes >= lay.sk_off + lay.sk_bytes) {
-    if (decode_sk_ctas(head_size, dtype == PKV_BF16, kv8, sms, &sk_ctas) ==
+    if (decode_sk_ctas(head_size, dtype == PKV_BF16, kv8, q8, sms,
+                       &sk_ctas) ==
             cudaSuccess &&
         decode_sk_workspace_bytes(head_size, sk_ctas, skr) <= lay.sk_bytes)
       sk_scratch = static_cast<char*>(workspace) + lay.sk_off;
@@ -792,8 +829,30 @@ pkv_status pkv_paged_attention_varlen_opts(
   const bool bf16 = dtype == PKV_BF16;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
+  // fp8 query: the persistent decode kernel reads the codes; every other
+  // kernel reads their exact 16-bit copy, with k_scale * q_scale as k_scale
+  AttnParams p16 = p;
+  if (q8 && (pl.prefill || sk_scratch == nullptr)) {
+    char* base_ptr = static_cast<char*>(workspace) + q16_off;
+    float* kq = reinterpret_cast<float*>(
+        base_ptr + align256(static_cast<size_t>(total_q) * num_heads *
+                            head_size * 2));
+    cudaError_t e = launch_widen_q(q, q_stride_tok, q_stride_head, base_ptr,
+                                   total_q, num_heads, head_size,
+                                   opts->k_scale, opts->q_scale, kq, bf16, s);
+    if (e != cudaSuccess) return cuda_fail(e, "fp8 query copy launch");
+    p16.q = base_ptr;
+    p16.q_st = static_cast<int64_t>(num_heads) * head_size;
+    p16.q_sh = head_size;
+    p16.k_scale = kq;
+  }
+  if (q8) {
+    p.q_fp8 = 1;
+    p.q_scale = opts->q_scale;
+  }
+
   if (pl.decode) {
-    AttnParams d = p;
+    AttnParams d = sk_scratch ? p : p16;
     d.min_rows = 1;
     d.max_rows = kDecodeRows;
     d.chunk = pl.chunk;
@@ -811,6 +870,7 @@ pkv_status pkv_paged_attention_varlen_opts(
       e = launch_decode_attn_sk(d, head_size, bf16, sk_ctas, skr, sk_scratch,
                                 s);
     } else if (!kv8 && dsel != PKV_DECODE_CP_ASYNC) {
+      d.pdl_done = pdl_done;
       e = launch_decode_attn_tma(d, head_size, bf16, pl.splits, s);
     } else {
       e = launch_decode_attn(d, head_size, bf16, pl.splits, 1, s);
@@ -847,8 +907,8 @@ pkv_status pkv_paged_attention_varlen_opts(
     }
   }
   if (pl.prefill) {
-    AttnParams f = p;
-    f.min_rows = kDecodeRows + 1;
+    AttnParams f = p16;
+    f.min_rows = pl.decode ? kDecodeRows + 1 : 1;
     f.max_rows = 0x7fffffff;
     f.chunk = 0;
     f.sched = sched;
@@ -907,12 +967,208 @@ pkv_status pkv_paged_attention_varlen_opts(
       c.D = head_size;
       c.splits = used;
       c.sinks = p.sinks;
-      c.min_rows = kDecodeRows + 1;
+      c.min_rows = f.min_rows;
       c.max_rows = 0x7fffffff;
       e = launch_prefill_split_combine(c, max_seqlen_q, bf16, s);
       if (e != cudaSuccess) return cuda_fail(e, "prefill split combine");
     }
   }
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_paged_attention_varlen_opts(
+    const void* q, int64_t q_stride_tok, int64_t q_stride_head,
+    const void* key_cache, const void* value_cache,
+    const int64_t cache_strides[4], void* out, int64_t o_stride_tok,
+    int64_t o_stride_head, const int32_t* cu_seqlens_q,
+    const int32_t* seqused_k, int batch, int total_q, int max_seqlen_q,
+    int max_seqlen_k, const int32_t* block_table, int64_t block_table_stride,
+    int max_blocks_per_seq, int num_heads, int num_kv_heads, int head_size,
+    int block_size, int64_t num_blocks, float softmax_scale, int causal,
+    int window_left, int window_right, float softcap,
+    const float* alibi_slopes, int num_splits, float* softmax_lse,
+    void* workspace, size_t workspace_bytes, pkv_dtype dtype,
+    pkv_stream_t stream, const pkv_attention_options* opts) {
+  return attention_impl(
+      q, q_stride_tok, q_stride_head, key_cache, value_cache, cache_strides,
+      out, o_stride_tok, o_stride_head, cu_seqlens_q, seqused_k, batch,
+      total_q, max_seqlen_q, max_seqlen_k, block_table, block_table_stride,
+      max_blocks_per_seq, num_heads, num_kv_heads, head_size, block_size,
+      num_blocks, softmax_scale, causal, window_left, window_right, softcap,
+      alibi_slopes, num_splits, softmax_lse, workspace, workspace_bytes,
+      dtype, stream, opts, nullptr);
+}
+
+pkv_status pkv_scaled_fp8_quant(const void* in, int64_t in_row_stride,
+                                void* out, int64_t out_row_stride,
+                                int64_t rows, int cols, const float* scale,
+                                pkv_dtype dtype, pkv_stream_t stream) {
+  if (dtype != PKV_F16 && dtype != PKV_BF16)
+    return fail(PKV_ERR_UNSUPPORTED, "dtype must be fp16 or bf16");
+  if (rows < 0 || cols < 0)
+    return fail(PKV_ERR_INVALID_ARG, "negative size argument");
+  if (cols % 16 != 0)
+    return fail(PKV_ERR_UNSUPPORTED, "cols must be a multiple of 16");
+  if (rows == 0 || cols == 0) return PKV_OK;
+  if (!in || !out || !scale)
+    return fail(PKV_ERR_INVALID_ARG, "NULL pointer");
+  if (in_row_stride < cols || out_row_stride < cols)
+    return fail(PKV_ERR_INVALID_ARG, "row strides must be >= cols");
+  if (!aligned16(in) || !aligned16(out) || !stride16(in_row_stride, 2) ||
+      !stride16(out_row_stride, 1))
+    return fail(PKV_ERR_UNSUPPORTED,
+                "rows must start on 16-byte boundaries");
+  cudaError_t e = launch_scaled_fp8_quant(
+      in, in_row_stride, out, out_row_stride, rows, cols, scale,
+      dtype == PKV_BF16, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "scaled_fp8_quant launch");
+  return PKV_OK;
+}
+
+// Cascade: the workspace holds, in order, a 256-byte counter block, the
+// prefix and suffix outputs (16-bit [T, Hq, D]) and LSEs (fp32 [Hq, T]),
+// then the prefix call's workspace and the suffix call's.
+struct CascadeLayout {
+  size_t po = 0, pl = 0, so = 0, sl = 0, pws = 0, sws = 0, total = 0;
+  size_t pws_bytes = 0, sws_bytes = 0;
+};
+
+static bool cascade_layout(int batch, int T, int max_q, int max_kv, int P,
+                           int Hq, int Hkv, int D, int BS, int max_blocks,
+                           int num_splits, const pkv_attention_options* o,
+                           CascadeLayout* l) {
+  const size_t out_b = align256(static_cast<size_t>(T) * Hq * D * 2);
+  const size_t lse_b = align256(static_cast<size_t>(Hq) * T * 4);
+  l->po = 256;
+  l->pl = l->po + out_b;
+  l->so = l->pl + lse_b;
+  l->sl = l->so + out_b;
+  l->pws = l->sl + lse_b;
+  const int nc = BS > 0 ? P / BS : 0;
+  l->pws_bytes = pkv_paged_attention_workspace_size_opts(
+      1, T, T, P, Hq, Hkv, D, BS, 0, -1, -1, 1, nc, o);
+  l->sws_bytes = pkv_paged_attention_workspace_size_opts(
+      batch, T, max_q, max_kv - P, Hq, Hkv, D, BS, 1, -1, -1, num_splits,
+      max_blocks - nc, o);
+  if (l->pws_bytes == static_cast<size_t>(-1) ||
+      l->sws_bytes == static_cast<size_t>(-1))
+    return false;
+  l->sws = l->pws + align256(l->pws_bytes);
+  l->total = l->sws + align256(l->sws_bytes);
+  return true;
+}
+
+size_t pkv_cascade_attention_workspace_size(
+    int batch, int num_tokens, int max_query_len, int max_kv_len,
+    int common_prefix_len, int num_heads, int num_kv_heads, int head_size,
+    int block_size, int max_blocks_per_seq, int num_splits,
+    const pkv_attention_options* opts) {
+  if (block_size <= 0 || common_prefix_len <= 0 ||
+      common_prefix_len % block_size != 0 || max_kv_len < common_prefix_len ||
+      max_blocks_per_seq < common_prefix_len / block_size)
+    return static_cast<size_t>(-1);
+  CascadeLayout l;
+  if (!cascade_layout(batch, num_tokens, max_query_len, max_kv_len,
+                      common_prefix_len, num_heads, num_kv_heads, head_size,
+                      block_size, max_blocks_per_seq, num_splits, opts, &l))
+    return static_cast<size_t>(-1);
+  return l.total;
+}
+
+pkv_status pkv_cascade_attention(
+    void* output, const void* query, int64_t q_stride_tok,
+    int64_t q_stride_head, const void* key_cache, const void* value_cache,
+    const int64_t cache_strides[4], const int32_t* cu_query_lens,
+    int max_query_len, const int32_t* cu_prefix_query_lens,
+    const int32_t* prefix_kv_lens, const int32_t* suffix_kv_lens,
+    int max_kv_len, int batch, int num_tokens, float softmax_scale,
+    float logits_soft_cap, const int32_t* block_table,
+    int64_t block_table_stride, int max_blocks_per_seq,
+    int common_prefix_len, int num_heads, int num_kv_heads, int head_size,
+    int block_size, int64_t num_blocks, int num_splits, int overlap,
+    void* workspace, size_t workspace_bytes, pkv_dtype dtype,
+    pkv_stream_t stream, const pkv_attention_options* opts) {
+  if (opts && (opts->cu_seqlens_k || opts->fixed_split_size))
+    return fail(PKV_ERR_INVALID_ARG,
+                "cascade attention takes no cu_seqlens_k or fixed split");
+  if (dtype != PKV_F16 && dtype != PKV_BF16)
+    return fail(PKV_ERR_UNSUPPORTED, "dtype must be fp16 or bf16");
+  if (block_size <= 0 || common_prefix_len <= 0 ||
+      common_prefix_len % block_size != 0)
+    return fail(PKV_ERR_INVALID_ARG,
+                "common_prefix_len must be a positive multiple of "
+                "block_size");
+  if (max_kv_len < common_prefix_len ||
+      max_blocks_per_seq < common_prefix_len / block_size)
+    return fail(PKV_ERR_INVALID_ARG,
+                "the prefix is longer than max_kv_len or the table");
+  if (batch < 0 || num_tokens < 0 || num_splits < 0)
+    return fail(PKV_ERR_INVALID_ARG, "negative size argument");
+  if (batch == 0 || num_tokens == 0) return PKV_OK;
+  if (!output || !cu_prefix_query_lens || !prefix_kv_lens ||
+      !suffix_kv_lens || !block_table)
+    return fail(PKV_ERR_INVALID_ARG, "NULL tensor pointer");
+  CascadeLayout l;
+  if (!cascade_layout(batch, num_tokens, max_query_len, max_kv_len,
+                      common_prefix_len, num_heads, num_kv_heads, head_size,
+                      block_size, max_blocks_per_seq, num_splits, opts, &l))
+    return fail(PKV_ERR_INVALID_ARG,
+                "invalid shapes for the prefix or suffix attention");
+  if (!workspace || workspace_bytes < l.total)
+    return fail(PKV_ERR_WORKSPACE_TOO_SMALL,
+                "workspace of %zu bytes needed, %zu given", l.total,
+                workspace_bytes);
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+    return fail(PKV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (!aligned16(output))
+    return fail(PKV_ERR_UNSUPPORTED, "output must be 16-byte aligned");
+  char* ws = static_cast<char*>(workspace);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int* done = reinterpret_cast<int*>(ws);
+  if (overlap) {
+    // zeroed before the prefix launch: nothing may come between the prefix
+    // kernel and the suffix decode kernel that depends on it
+    cudaError_t e = cudaMemsetAsync(done, 0, sizeof(int), s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+  }
+  const int T = num_tokens, Hq = num_heads, D = head_size;
+  const int nc = common_prefix_len / block_size;
+  void* po = ws + l.po;
+  float* pl = reinterpret_cast<float*>(ws + l.pl);
+  void* so = ws + l.so;
+  float* sl = reinterpret_cast<float*>(ws + l.sl);
+  // prefix: every query over the shared blocks (row 0 of the table),
+  // non-causal, unsplit (the suffix takes the SMs the prefix leaves), with
+  // the sinks
+  pkv_status st = attention_impl(
+      query, q_stride_tok, q_stride_head, key_cache, value_cache,
+      cache_strides, po, static_cast<int64_t>(Hq) * D, D,
+      cu_prefix_query_lens, prefix_kv_lens, 1, T, T, common_prefix_len,
+      block_table, block_table_stride, nc, Hq, num_kv_heads, D, block_size,
+      num_blocks, softmax_scale, 0, -1, -1, logits_soft_cap, nullptr, 1, pl,
+      ws + l.pws, l.pws_bytes, dtype, stream, opts, nullptr);
+  if (st != PKV_OK) return st;
+  // suffix: each request's own blocks, causal, without the sinks; its
+  // decode kernel may start beside the prefix kernel
+  pkv_attention_options so_opts{};
+  if (opts) so_opts = *opts;
+  so_opts.sinks = nullptr;
+  st = attention_impl(
+      query, q_stride_tok, q_stride_head, key_cache, value_cache,
+      cache_strides, so, static_cast<int64_t>(Hq) * D, D, cu_query_lens,
+      suffix_kv_lens, batch, T, max_query_len, max_kv_len - common_prefix_len,
+      block_table + nc, block_table_stride, max_blocks_per_seq - nc, Hq,
+      num_kv_heads, D, block_size, num_blocks, softmax_scale, 1, -1, -1,
+      logits_soft_cap, nullptr, num_splits, sl, ws + l.sws, l.sws_bytes,
+      dtype, stream, &so_opts, overlap ? done : nullptr);
+  if (st != PKV_OK) return st;
+  cudaError_t e = launch_merge(output, po, pl, so, sl, nullptr, T, Hq, D,
+                               dtype, dtype, s);
+  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
   return PKV_OK;
 }
 

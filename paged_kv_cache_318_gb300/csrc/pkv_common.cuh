@@ -223,6 +223,14 @@ struct AttnParams {
   int kv_fp8;                 // cache holds E4M3 codes (1 byte / element)
   const float* k_scale;       // fp8: device scalar, value = code * scale
   const float* v_scale;
+  // E4M3 query codes (1 byte / element, q_st / q_sh in bytes), value =
+  // code * (*q_scale); only the persistent decode kernel reads them (the
+  // other kernels get a 16-bit copy and k_scale * q_scale as k_scale)
+  int q_fp8;
+  const float* q_scale;
+  // TMA decode kernel launched as a programmatic dependent of the grid
+  // before it: a zeroed counter of finished CTAs (null = ordinary launch)
+  int* pdl_done;
   int causal, wl, wr;
   // which requests this launch owns: rows = q_b * G in [min_rows, max_rows]
   int min_rows, max_rows;
@@ -344,6 +352,16 @@ cudaError_t launch_cache_write_fp8(const void* key, const void* value,
 cudaError_t launch_fp8_dequant_pages(const AttnParams& p, int D, bool bf16,
                                      void* mock_k, void* mock_v,
                                      int32_t* mock_table, cudaStream_t stream);
+// E4M3 queries (q_fp8.cu): the per-tensor quantization, and the exact
+// 16-bit copy of the codes plus kq = k_scale * q_scale.
+cudaError_t launch_scaled_fp8_quant(const void* in, int64_t in_st, void* out,
+                                    int64_t out_st, int64_t rows, int cols,
+                                    const float* scale, bool bf16,
+                                    cudaStream_t stream);
+cudaError_t launch_widen_q(const void* q8, int64_t q_st, int64_t q_sh,
+                           void* q16, int total_q, int Hq, int D,
+                           const float* k_scale, const float* q_scale,
+                           float* kq, bool bf16, cudaStream_t stream);
 
 cudaError_t launch_decode_attn(const AttnParams& p, int D, bool bf16,
                                int grid_x, int grid_y, cudaStream_t stream);
@@ -373,8 +391,10 @@ cudaError_t launch_split_combine(const CombineParams& p, bool bf16,
 // (256-byte aligned) for the pieces of units that chunk boundaries cut,
 // rows = the most packed query rows a decode-class request can have
 // (min(16, G * max_seqlen_q)).
+// q8: E4M3 query codes too (needs kv8).
 bool decode_sk_supported(int D, bool kv8);
-cudaError_t decode_sk_ctas(int D, bool bf16, bool kv8, int sms, int* ctas);
+cudaError_t decode_sk_ctas(int D, bool bf16, bool kv8, bool q8, int sms,
+                           int* ctas);
 size_t decode_sk_workspace_bytes(int D, int ctas, int rows);
 cudaError_t launch_decode_attn_sk(const AttnParams& p, int D, bool bf16,
                                   int ctas, int rows, void* scratch,

@@ -269,6 +269,9 @@ template <typename T, int D>
 __global__ void __launch_bounds__(NUM_THREADS, 2)
 prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v) {
+  // a launch queued after this one as its programmatic dependent (the
+  // cascade's suffix decode) may take the SMs this grid leaves free
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   using C = Cfg<D>;
   constexpr int BN = C::BN;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -799,6 +802,9 @@ template <typename T, int D>
 __global__ void __launch_bounds__(PP_THREADS, 1)
 prefill_pp_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v) {
+  // a launch queued after this one as its programmatic dependent (the
+  // cascade's suffix decode) may take the SMs this grid leaves free
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   using C = PPCfg<D>;
   constexpr int BN = C::BN;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -1572,6 +1578,9 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
 prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_q) {
+  // a launch queued after this one as its programmatic dependent (the
+  // cascade's suffix decode) may take the SMs this grid leaves free
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   using C = PTCfg<D>;
   constexpr int BN = C::BN;
   extern __shared__ __align__(1024) unsigned char smem_raw[];

@@ -112,3 +112,115 @@ def test_fp8_attention(cuda_device, idx):
     assert np.isfinite(o).all()
     assert np.abs(o - ro).max() <= TOL[dtype], np.abs(o - ro).max()
     assert np.abs(lse.cpu().numpy() - rl).max() <= 1e-3
+
+
+# ------------------------------------------------------------ fp8 queries
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_scaled_fp8_quant_bit_exact(cuda_device, dtype):
+    """The query quantization against the oracle's codes: every element of
+    a [tokens, heads * head_size] matrix, with saturating, zero and NaN
+    inputs among them."""
+    from oracle.fp8 import scaled_fp8_quant_ref
+    dev = cuda_device
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
+    g = torch.Generator().manual_seed(11)
+    x = (torch.randn(37, 8, 128, generator=g) *
+         torch.tensor([0.01, 1.0, 30.0, 900.0]).repeat(2)[None, :, None])
+    x = x.to(tdt)
+    x[3, 2, :5] = 0.0
+    x[4, 1, 7] = float("nan")
+    scale = torch.tensor([0.37], dtype=torch.float32, device=dev)
+    codes, s = api.scaled_fp8_quant(x.to(dev), scale)
+    torch.cuda.synchronize()
+    assert s is scale and codes.dtype == torch.float8_e4m3fn
+    got = codes.view(torch.uint8).cpu().numpy()
+    ref = scaled_fp8_quant_ref(f32(x), np.float32(0.37))
+    nan = np.isnan(f32(x))
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert ((got[nan] & 0x7F) == 0x7F).all()
+    # strided rows in, strided rows out
+    xs = torch.zeros(37, 8 * 128 + 64, dtype=tdt, device=dev)
+    xs[:, :1024] = x.reshape(37, 1024).to(dev)
+    out = torch.zeros(37, 1024 + 32, dtype=torch.uint8, device=dev)
+    api.scaled_fp8_quant(xs[:, :1024], scale, out=out[:, :1024])
+    torch.cuda.synchronize()
+    o = out.cpu().numpy()
+    assert np.array_equal(o[:, :1024].reshape(37, 8, 128)[~nan], ref[~nan])
+    assert not o[:, 1024:].any()
+
+
+Q8_CASES = [
+    # q_lens, seq_lens, Hq, Hkv, D, BS, num_splits, dtype, decode kernel
+    ([1, 1, 1, 1], [700, 3000, 9, 1], 32, 8, 128, 16, 0, "bf16", "auto"),
+    ([1, 1, 1], [1200, 77, 4100], 32, 8, 128, 16, 0, "f16", "auto"),
+    ([2, 1], [900, 3000], 16, 8, 256, 32, 0, "bf16", "auto"),
+    ([1, 3, 1], [33, 2049, 4100], 16, 8, 256, 32, 0, "f16", "auto"),
+    ([1, 1], [4000, 64], 16, 2, 128, 64, 4, "bf16", "auto"),
+    ([1, 1, 1], [500, 1500, 40], 32, 8, 128, 16, 0, "bf16", "cp_async"),
+    ([1, 2], [500, 70], 8, 2, 64, 16, 0, "f16", "auto"),
+    ([200, 1, 90], [900, 2000, 90], 32, 8, 128, 16, 0, "bf16", "auto"),
+    ([70, 1], [600, 1200], 16, 8, 256, 32, 0, "bf16", "auto"),
+]
+
+
+@pytest.mark.parametrize("idx", range(len(Q8_CASES)))
+def test_fp8_query_attention(cuda_device, idx):
+    """E4M3 query codes (the library's scaled_fp8_quant, checked against
+    the oracle's codes) over an E4M3 cache: the persistent decode kernel's
+    E4M3 tensor-core path, and the 16-bit copy of the codes that the other
+    kernels read, against the float64 oracle on code * scale values."""
+    from oracle.fp8 import dequantize_ref, scaled_fp8_quant_ref
+    q_lens, seq_lens, Hq, Hkv, D, BS, splits, dtype, kern = Q8_CASES[idx]
+    wl = workloads.build_workload("q8_%d" % idx, 90 + idx, q_lens, seq_lens,
+                                  Hq, Hkv, D, BS, dtype=dtype,
+                                  num_splits=splits)
+    dev = cuda_device
+    ksc, vsc, qsc = 0.011, 0.017, 0.023
+    cache, kc, vc, ks, vs = fp8_batch(wl, dev, ksc, vsc)
+    qs = torch.tensor([qsc], dtype=torch.float32, device=dev)
+    q8, _ = api.scaled_fp8_quant(wl.q.to(dev), qs)
+    qcodes = scaled_fp8_quant_ref(f32(wl.q), np.float32(qsc))
+    assert np.array_equal(q8.view(torch.uint8).cpu().numpy(), qcodes)
+    out = torch.empty(wl.q.shape, dtype=wl.q.dtype, device=dev)
+    api.set_decode_kernel(api.DECODE_CP_ASYNC if kern == "cp_async"
+                          else api.DECODE_AUTO)
+    try:
+        _, lse = api.flash_attn_varlen_func(
+            q8, kc, vc, wl.max_seqlen_q,
+            torch.from_numpy(wl.cu_seqlens_q).to(dev), wl.max_seqlen_k,
+            seqused_k=torch.from_numpy(wl.seq_lens).to(dev),
+            softmax_scale=wl.softmax_scale, causal=True,
+            block_table=torch.from_numpy(wl.block_table).to(dev),
+            return_softmax_lse=True, num_splits=splits, k_descale=ks,
+            v_descale=vs, q_descale=qs, out=out)
+        torch.cuda.synchronize()
+    finally:
+        api.set_decode_kernel(api.DECODE_AUTO)
+    api.check_device_errors(dev)
+    kcodes, vcodes = oracle_codes(wl, ksc, vsc)
+    ro, rl = paged_attention_ref(dequantize_ref(qcodes, qsc),
+                                 dequantize_ref(kcodes, ksc),
+                                 dequantize_ref(vcodes, vsc),
+                                 wl.cu_seqlens_q, wl.seq_lens,
+                                 wl.block_table, wl.softmax_scale)
+    o = out.float().cpu().numpy()
+    assert np.isfinite(o).all()
+    assert np.abs(o - ro).max() <= TOL[dtype], np.abs(o - ro).max()
+    assert np.abs(lse.cpu().numpy() - rl).max() <= 1e-3
+
+
+def test_fp8_query_rejected_without_fp8_cache(cuda_device):
+    wl = workloads.build_workload("q8r", 5, [1], [40], 8, 2, 128, 16)
+    dev = cuda_device
+    qs = torch.tensor([0.02], dtype=torch.float32, device=dev)
+    q8, _ = api.scaled_fp8_quant(wl.q.to(dev), qs)
+    cache = torch.zeros(wl.cache_shape(), dtype=wl.q.dtype, device=dev)
+    kc, vc = cache.unbind(0)
+    with pytest.raises(NotImplementedError):
+        api.flash_attn_varlen_func(
+            q8, kc, vc, 1, torch.from_numpy(wl.cu_seqlens_q).to(dev), 40,
+            seqused_k=torch.from_numpy(wl.seq_lens).to(dev),
+            block_table=torch.from_numpy(wl.block_table).to(dev),
+            q_descale=qs, out=torch.empty(wl.q.shape, dtype=wl.q.dtype,
+                                          device=dev))

@@ -95,10 +95,29 @@ def test_cascade_small(cuda_device, dtype):
     assert_close(wl, out, None, ref_out, None, "cascade")
 
 
-def test_cascade_overlap_equals_serial(cuda_device):
-    """The prefix on a side stream (overlapping the suffix) gives the same
-    bits as the two calls back to back."""
-    wl = workloads.cascade_decode(batch=9, prefix=128, unique=70)
+CASCADE_OVERLAP_CASES = {
+    "decode": lambda: workloads.cascade_decode(batch=9, prefix=128,
+                                               unique=70),
+    # suffix with decode-class and prefill-class requests: the suffix call
+    # launches its decode kernel beside the prefix, then its prefill kernel
+    "mixed_suffix": lambda: workloads.build_workload(
+        "casc_mixed", 71, [1, 37, 1, 90, 2], [200, 177, 129, 260, 300], 16,
+        4, 128, 64, shared_prefix_len=128),
+    "bf16_256": lambda: workloads.build_workload(
+        "casc_d256", 72, [1] * 20, list(range(300, 340, 2)), 16, 8, 256, 32,
+        shared_prefix_len=256),
+    "f16": lambda: workloads.build_workload(
+        "casc_f16", 73, [1] * 40, list(range(700, 740)), 32, 8, 128, 16,
+        shared_prefix_len=512, dtype="f16"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASCADE_OVERLAP_CASES))
+def test_cascade_overlap_equals_serial(cuda_device, name):
+    """The suffix's decode kernel launched beside the prefix kernel (as its
+    programmatic dependent) gives the same bits as the steps one after the
+    other, and both match the oracle."""
+    wl = CASCADE_OVERLAP_CASES[name]()
     b = DeviceBatch(wl, cuda_device, cascade=True)
     b.write_context()
     b.write_new()
@@ -112,9 +131,10 @@ def test_cascade_overlap_equals_serial(cuda_device):
         torch.cuda.synchronize()
         outs.append(b.out.clone())
     assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    api.check_device_errors(cuda_device)
     ref_out, _ = full_reference(wl)
     assert_close(wl, outs[0].float().cpu().numpy(), None, ref_out, None,
-                 "cascade overlap")
+                 "cascade overlap %s" % name)
 
 
 # ------------------------------------------------------ feature matrix
