@@ -384,6 +384,8 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
     const int RB = p.rb;
     const int nb_max = KT / RB;
     const char* Q = static_cast<const char*>(p.q);
+    // K/V pages are read once: their L2 lines go first
+    const uint64_t pol = l2_evict_first_policy();
     // (request, KV head, tile) of tile position P of the sequence
     auto locate = [&](long long P, int& b, int& g, int& t, int& n) {
       int lo = 0, hi = B;          // pre[lo] <= P < pre[hi]
@@ -525,11 +527,15 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
               const uint32_t dv =
                   tile_v(s) + cb * C::CB_BYTES + lane * RB * 128;
               if (p.kv_order_hnd) {
-                tma_load_4d(dk, &tm_k, cb * C::BOXC, row, g, cur, full_k(s));
-                tma_load_4d(dv, &tm_v, cb * C::BOXC, row, g, cur, full_v(s));
+                tma_load_4d_hint(dk, &tm_k, cb * C::BOXC, row, g, cur,
+                                 full_k(s), pol);
+                tma_load_4d_hint(dv, &tm_v, cb * C::BOXC, row, g, cur,
+                                 full_v(s), pol);
               } else {
-                tma_load_4d(dk, &tm_k, cb * C::BOXC, g, row, cur, full_k(s));
-                tma_load_4d(dv, &tm_v, cb * C::BOXC, g, row, cur, full_v(s));
+                tma_load_4d_hint(dk, &tm_k, cb * C::BOXC, g, row, cur,
+                                 full_k(s), pol);
+                tma_load_4d_hint(dv, &tm_v, cb * C::BOXC, g, row, cur,
+                                 full_v(s), pol);
               }
             }
           }

@@ -154,6 +154,14 @@ __device__ __forceinline__ void decode_tma_body(const AttnParams& p,
     // ------------------------------------------------------------ producer
     if (n_tiles == 0) return;
     const int nb_max = KT / RB;
+    // K/V pages are read once: their L2 lines go first (measured on GB300:
+    // batched decode 0.1148 -> 0.1116 ms, long decode 0.654 -> 0.649 ms,
+    // cascade 0.1357 -> 0.1342 ms against plain loads)
+    const uint64_t pol = l2_evict_first_policy();
+    auto kv_load = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1,
+                       int c2, int c3, uint32_t bar) {
+      tma_load_4d_hint(dst, m, c0, c1, c2, c3, bar, pol);
+    };
     const int32_t* bt = p.cu_k ? nullptr
                                : p.block_table + static_cast<int64_t>(b) * p.bt_stride;
     auto fetch = [&](int t) -> int {            // page id of box `lane`
@@ -197,17 +205,17 @@ __device__ __forceinline__ void decode_tma_body(const AttnParams& p,
         for (int cb = 0; cb < C::NCB; ++cb) {
           const uint32_t dst = tile_k(s) + cb * C::CB_BYTES + lane * RB * 128;
           if (p.kv_order_hnd)
-            tma_load_4d(dst, &tm_k, cb * 64, row, g, cur, full_k(s));
+            kv_load(dst, &tm_k, cb * 64, row, g, cur, full_k(s));
           else
-            tma_load_4d(dst, &tm_k, cb * 64, g, row, cur, full_k(s));
+            kv_load(dst, &tm_k, cb * 64, g, row, cur, full_k(s));
         }
 #pragma unroll
         for (int cb = 0; cb < C::NCB; ++cb) {
           const uint32_t dst = tile_v(s) + cb * C::CB_BYTES + lane * RB * 128;
           if (p.kv_order_hnd)
-            tma_load_4d(dst, &tm_v, cb * 64, row, g, cur, full_v(s));
+            kv_load(dst, &tm_v, cb * 64, row, g, cur, full_v(s));
           else
-            tma_load_4d(dst, &tm_v, cb * 64, g, row, cur, full_v(s));
+            kv_load(dst, &tm_v, cb * 64, g, row, cur, full_v(s));
         }
       }
       issued = t + 1;
