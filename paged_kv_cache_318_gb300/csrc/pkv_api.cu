@@ -507,11 +507,19 @@ pkv_status pkv_reshape_and_cache(
   return PKV_OK;
 }
 
-size_t pkv_paged_attention_workspace_size_opts(
-    int batch, int total_q, int max_seqlen_q, int max_seqlen_k, int num_heads,
-    int num_kv_heads, int head_size, int block_size, int causal,
-    int window_left, int window_right, int num_splits,
-    int max_blocks_per_seq, const pkv_attention_options* opts) {
+}  // extern "C"
+
+namespace {
+
+// Workspace of an attention call; pre_splits > 0 fixes the prefill key
+// splits (else the plan's).
+size_t workspace_bytes_impl(int batch, int total_q, int max_seqlen_q,
+                            int max_seqlen_k, int num_heads, int num_kv_heads,
+                            int head_size, int block_size, int causal,
+                            int window_left, int window_right, int num_splits,
+                            int max_blocks_per_seq,
+                            const pkv_attention_options* opts,
+                            int pre_splits) {
   const int bs = non_paged(opts) ? 16 : block_size;
   if (check_attn_shape(batch, total_q, max_seqlen_q, max_seqlen_k, num_heads,
                        num_kv_heads, head_size, bs, num_splits) != PKV_OK)
@@ -528,10 +536,12 @@ size_t pkv_paged_attention_workspace_size_opts(
                 fixed_split_of(opts));
   const bool fp8 = opts && opts->kv_cache_fp8;
   const size_t split_bytes = prefill_split_bytes(
-      pl.prefill ? prefill_splits(batch, total_q, num_heads / num_kv_heads,
-                                  num_kv_heads, max_seqlen_k, head_size, sms,
-                                  num_splits, fixed_split_of(opts))
-                 : 1,
+      !pl.prefill ? 1
+      : pre_splits > 0
+          ? pre_splits
+          : prefill_splits(batch, total_q, num_heads / num_kv_heads,
+                           num_kv_heads, max_seqlen_k, head_size, sms,
+                           num_splits, fixed_split_of(opts)),
       total_q, num_heads, head_size);
   const bool q8 = fp8 && q_fp8_of(opts);
   const size_t skb =
@@ -548,6 +558,21 @@ size_t pkv_paged_attention_workspace_size_opts(
   }
   if (q8) need = align256(need) + q16_bytes(total_q, num_heads, head_size);
   return make_layout(need, pl.prefill, skb, split_bytes).total;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pkv_paged_attention_workspace_size_opts(
+    int batch, int total_q, int max_seqlen_q, int max_seqlen_k, int num_heads,
+    int num_kv_heads, int head_size, int block_size, int causal,
+    int window_left, int window_right, int num_splits,
+    int max_blocks_per_seq, const pkv_attention_options* opts) {
+  return workspace_bytes_impl(batch, total_q, max_seqlen_q, max_seqlen_k,
+                              num_heads, num_kv_heads, head_size, block_size,
+                              causal, window_left, window_right, num_splits,
+                              max_blocks_per_seq, opts, 0);
 }
 
 size_t pkv_paged_attention_workspace_size(int batch, int total_q,
@@ -606,9 +631,21 @@ pkv_status pkv_paged_attention_varlen(
 
 namespace {
 
-// The attention call; pdl_done != null launches the TMA decode kernel (when
-// the call takes it) as a programmatic dependent of the grid queued before
-// the call, with that zeroed counter.
+// Controls of an attention call inside a composed one (the cascade).
+struct Internal {
+  // launch the TMA decode kernel (when the call takes it) as a programmatic
+  // dependent of the grid queued before the call, with this zeroed counter
+  int* pdl_done = nullptr;
+  int pre_splits = 0;       // > 0: prefill key splits (else the plan's)
+  int pre_ctas = 0;         // > 0: cap on the persistent prefill grid
+  // leave the prefill split combine to the caller (filled in below)
+  bool defer_combine = false;
+  bool deferred = false;
+  CombineParams combine{};
+  int combine_max_q = 0;
+  bool combine_bf16 = false;
+};
+
 pkv_status attention_impl(
     const void* q, int64_t q_stride_tok, int64_t q_stride_head,
     const void* key_cache, const void* value_cache,
@@ -621,7 +658,8 @@ pkv_status attention_impl(
     int window_left, int window_right, float softcap,
     const float* alibi_slopes, int num_splits, float* softmax_lse,
     void* workspace, size_t workspace_bytes, pkv_dtype dtype,
-    pkv_stream_t stream, const pkv_attention_options* opts, int* pdl_done) {
+    pkv_stream_t stream, const pkv_attention_options* opts, Internal* in) {
+  int* pdl_done = in ? in->pdl_done : nullptr;
   const bool nonpaged = non_paged(opts);
   pkv_status st = check_attn_shape(batch, total_q, max_seqlen_q, max_seqlen_k,
                                    num_heads, num_kv_heads, head_size,
@@ -708,11 +746,12 @@ pkv_status attention_impl(
   }
   // optional tail: the persistent decode scratch, then the prefill item
   // counter and its split partials
-  const int sp = pl.prefill
-                     ? prefill_splits(batch, total_q, num_heads / num_kv_heads,
+  const int sp = !pl.prefill ? 1
+                 : (in && in->pre_splits > 0)
+                     ? in->pre_splits
+                     : prefill_splits(batch, total_q, num_heads / num_kv_heads,
                                       num_kv_heads, max_seqlen_k, head_size,
-                                      sms, num_splits, fixed_split)
-                     : 1;
+                                      sms, num_splits, fixed_split);
   const size_t sb = prefill_split_bytes(sp, total_q, num_heads, head_size);
   // Persistent or one CTA per (request, KV head, split)?  Measured on
   // GB300: when the (request, KV head) units fill about one wave of the
@@ -915,6 +954,7 @@ pkv_status attention_impl(
     f.pre_splits = pre_splits;
     f.pre_o = pre_o;
     f.pre_lse = pre_lse;
+    f.max_ctas = in ? in->pre_ctas : 0;
     const int64_t prow = static_cast<int64_t>(max_seqlen_q) * p.G;
     cudaError_t e;
     if (kv8) {
@@ -969,8 +1009,15 @@ pkv_status attention_impl(
       c.sinks = p.sinks;
       c.min_rows = f.min_rows;
       c.max_rows = 0x7fffffff;
-      e = launch_prefill_split_combine(c, max_seqlen_q, bf16, s);
-      if (e != cudaSuccess) return cuda_fail(e, "prefill split combine");
+      if (in && in->defer_combine) {
+        in->deferred = true;
+        in->combine = c;
+        in->combine_max_q = max_seqlen_q;
+        in->combine_bf16 = bf16;
+      } else {
+        e = launch_prefill_split_combine(c, max_seqlen_q, bf16, s);
+        if (e != cudaSuccess) return cuda_fail(e, "prefill split combine");
+      }
     }
   }
   return PKV_OK;
@@ -1029,6 +1076,20 @@ pkv_status pkv_scaled_fp8_quant(const void* in, int64_t in_row_stride,
   return PKV_OK;
 }
 
+// Cascade prefix: key splits of the prefill kernel and the SMs its grid
+// leaves to the suffix's decode kernel (0: the grid is not capped).
+// Measured on GB300 (256 decodes over an 8192-key prefix + 512 own keys,
+// 64/8 heads): unsplit and uncapped 0.134 ms (the prefix's 64 items take
+// 64 SMs and the suffix the other 88); 2 splits leaving 24 or 56 SMs 0.170
+// and 0.162 ms; 3 splits leaving 40 or 56 SMs 0.162 and 0.161 ms; 4 splits
+// leaving 24 or 56 SMs 0.178 and 0.166 ms.
+#ifndef PKV_CASCADE_PREFIX_SPLITS
+#define PKV_CASCADE_PREFIX_SPLITS 1
+#endif
+#ifndef PKV_CASCADE_SUFFIX_SMS
+#define PKV_CASCADE_SUFFIX_SMS 0
+#endif
+
 // Cascade: the workspace holds, in order, a 256-byte counter block, the
 // prefix and suffix outputs (16-bit [T, Hq, D]) and LSEs (fp32 [Hq, T]),
 // then the prefix call's workspace and the suffix call's.
@@ -1049,8 +1110,8 @@ static bool cascade_layout(int batch, int T, int max_q, int max_kv, int P,
   l->sl = l->so + out_b;
   l->pws = l->sl + lse_b;
   const int nc = BS > 0 ? P / BS : 0;
-  l->pws_bytes = pkv_paged_attention_workspace_size_opts(
-      1, T, T, P, Hq, Hkv, D, BS, 0, -1, -1, 1, nc, o);
+  l->pws_bytes = workspace_bytes_impl(1, T, T, P, Hq, Hkv, D, BS, 0, -1, -1,
+                                      1, nc, o, PKV_CASCADE_PREFIX_SPLITS);
   l->sws_bytes = pkv_paged_attention_workspace_size_opts(
       batch, T, max_q, max_kv - P, Hq, Hkv, D, BS, 1, -1, -1, num_splits,
       max_blocks - nc, o);
@@ -1142,21 +1203,32 @@ pkv_status pkv_cascade_attention(
   void* so = ws + l.so;
   float* sl = reinterpret_cast<float*>(ws + l.sl);
   // prefix: every query over the shared blocks (row 0 of the table),
-  // non-causal, unsplit (the suffix takes the SMs the prefix leaves), with
-  // the sinks
-  pkv_status st = attention_impl(
+  // non-causal, with the sinks; its grid leaves SMs to the suffix, and its
+  // split combine (if any) waits until the suffix's decode is queued
+  int sms = 0;
+  pkv_status st = device_info(nullptr, &sms);
+  if (st != PKV_OK) return st;
+  Internal pin;
+  pin.pre_splits = PKV_CASCADE_PREFIX_SPLITS;
+  pin.pre_ctas = PKV_CASCADE_SUFFIX_SMS > 0 && sms > PKV_CASCADE_SUFFIX_SMS
+                     ? sms - PKV_CASCADE_SUFFIX_SMS
+                     : 0;
+  pin.defer_combine = true;
+  st = attention_impl(
       query, q_stride_tok, q_stride_head, key_cache, value_cache,
       cache_strides, po, static_cast<int64_t>(Hq) * D, D,
       cu_prefix_query_lens, prefix_kv_lens, 1, T, T, common_prefix_len,
       block_table, block_table_stride, nc, Hq, num_kv_heads, D, block_size,
       num_blocks, softmax_scale, 0, -1, -1, logits_soft_cap, nullptr, 1, pl,
-      ws + l.pws, l.pws_bytes, dtype, stream, opts, nullptr);
+      ws + l.pws, l.pws_bytes, dtype, stream, opts, &pin);
   if (st != PKV_OK) return st;
   // suffix: each request's own blocks, causal, without the sinks; its
   // decode kernel may start beside the prefix kernel
   pkv_attention_options so_opts{};
   if (opts) so_opts = *opts;
   so_opts.sinks = nullptr;
+  Internal sin;
+  sin.pdl_done = overlap ? done : nullptr;
   st = attention_impl(
       query, q_stride_tok, q_stride_head, key_cache, value_cache,
       cache_strides, so, static_cast<int64_t>(Hq) * D, D, cu_query_lens,
@@ -1164,8 +1236,13 @@ pkv_status pkv_cascade_attention(
       block_table + nc, block_table_stride, max_blocks_per_seq - nc, Hq,
       num_kv_heads, D, block_size, num_blocks, softmax_scale, 1, -1, -1,
       logits_soft_cap, nullptr, num_splits, sl, ws + l.sws, l.sws_bytes,
-      dtype, stream, &so_opts, overlap ? done : nullptr);
+      dtype, stream, &so_opts, &sin);
   if (st != PKV_OK) return st;
+  if (pin.deferred) {
+    cudaError_t e = launch_prefill_split_combine(
+        pin.combine, pin.combine_max_q, pin.combine_bf16, s);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill split combine");
+  }
   cudaError_t e = launch_merge(output, po, pl, so, sl, nullptr, T, Hq, D,
                                dtype, dtype, s);
   if (e != cudaSuccess) return cuda_fail(e, "merge launch");

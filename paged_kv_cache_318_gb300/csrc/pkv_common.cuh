@@ -257,6 +257,9 @@ struct AttnParams {
   int pre_splits;
   float* pre_o;
   float* pre_lse;
+  // persistent prefill: at most this many CTAs (0 = one per SM), leaving
+  // the other SMs to a kernel running beside it
+  int max_ctas;
   unsigned* err;
   // bounded mbarrier waits of the decode kernels give up after this many
   // nanoseconds (pkv_set_wait_limit_ns; the drains at exit keep 2 s)

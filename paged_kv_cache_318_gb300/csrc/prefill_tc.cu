@@ -2641,6 +2641,7 @@ cudaError_t launch_prefill_attn_tc(const AttnParams& a, int D, bool bf16,
       if (splits_used) *splits_used = a.pre_splits;
     }
     grid = dim3(static_cast<unsigned>(items));
+    if (a.max_ctas > 0 && a.max_ctas < sms) sms = a.max_ctas;
     if (static_cast<int64_t>(sms) < items) {
       grid = dim3(static_cast<unsigned>(sms));
       // items dealt at run time when the caller's workspace holds a
