@@ -117,6 +117,9 @@ struct TcParams {
   int kv_order_hnd;   // tensor-map dim order: 1 = (D, BS, Hkv, NB)
   int* sched;             // persistent kernel: zeroed item counter, or null
   int q_tma;              // persistent kernel: Q tiles arrive as TMA boxes
+  // persistent kernel: the O of a full 128-row tile leaves through a TMA
+  // store from the ring stage of the item's last K (tile A) or V (tile B)
+  int o_tma;
   // persistent kernel split-KV: every pair tile's key tiles cut into
   // n_split ranges, one work item each; partials to pre_o / pre_lse
   int n_split;
@@ -1577,7 +1580,8 @@ template <typename T, int D>
 __global__ void __launch_bounds__(PT_THREADS, 1)
 prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v,
-                     const __grid_constant__ CUtensorMap tm_q) {
+                     const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_o) {
   // a launch queued after this one as its programmatic dependent (the
   // cascade's suffix decode) may take the SMs this grid leaves free
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -1617,6 +1621,12 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
   auto it_full = [&](int s) { return bar0 + 8 * (19 + s); };
   auto it_empty = [&](int s) { return bar0 + 8 * (19 + PT_ITEM_SLOTS + s); };
   static_assert(8 * (19 + 2 * PT_ITEM_SLOTS) <= C::BAR_BYTES, "barrier area");
+  // per tile x and ring stage s: the tile's 128 threads have staged O in
+  // stage s of K (x = 0) or V (x = 1); the K / V loader then stores it
+  // with TMA and refills the stage
+  auto stg_full = [&](int x, int st) { return bar0 + 8 * (27 + 2 * x + st); };
+  static_assert(8 * 31 <= C::BAR_BYTES, "barrier area");
+  static_assert(19 + 2 * PT_ITEM_SLOTS <= 27, "staging barriers overlap");
   const bool dyn = p.sched != nullptr;
 
   if (tid == 0) {
@@ -1630,6 +1640,8 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
       mbar_init(o_free(s), 128);
     }
     mbar_init(o_ready, 1);
+    for (int xx = 0; xx < 2; ++xx)
+      for (int st = 0; st < 2; ++st) mbar_init(stg_full(xx, st), 128);
     mbar_init(q_full, p.q_tma ? 1 : 32);
     mbar_init(q_empty, 1);
     mbar_init(drain_bar, 1);
@@ -1705,6 +1717,28 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
     const void* tm = mat ? static_cast<const void*>(&tm_v)
                          : static_cast<const void*>(&tm_k);
     int gj = 0;                                // tiles issued so far
+    // O of this loader's tile (A for K, B for V) staged in ring stage st by
+    // an epilogue and not yet stored: its box coordinates
+    bool pend[2] = {false, false};
+    int pend_g[2] = {0, 0}, pend_tok[2] = {0, 0};
+    int flushes[2] = {0, 0};                   // stores done per stage
+    // lane 0: store the O staged in stage st (after the 128 threads of the
+    // tile have written it); false on abort
+    auto flush = [&](int st) -> bool {
+      if (!pend[st]) return true;
+      if (!mbar_wait(stg_full(mat, st), flushes[st] & 1, abort_flag, p.err))
+        return false;
+      ++flushes[st];
+      pend[st] = false;
+      const uint32_t src = (mat ? sV : sK) + st * C::KV_BYTES;
+#pragma unroll
+      for (int cb = 0; cb < C::NCB; ++cb)
+        tma_store_3d(&tm_o, src + cb * (BN * 128), cb * 64, pend_g[st] * G,
+                     pend_tok[st]);
+      bulk_commit();
+      bulk_wait_read_all();
+      return true;
+    };
     bool ok = true;
     for (int n = 0; ok; ++n) {
       PtItem it;
@@ -1743,6 +1777,9 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
           if (gj >= 2 && !mbar_wait(empty, ((gj >> 1) & 1) ^ 1, abort_flag,
                                     p.err))
             stop = 1;
+          // an epilogue staged O in this stage: store it before refilling
+          else if (!flush(s))
+            stop = 1;
           else
             mbar_expect_tx(full, nbox * C::NCB * RB * 128);
         }
@@ -1765,8 +1802,20 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
         }
         cur = nxt;
       }
+      // this item's tile staged by its epilogue in the stage of its last
+      // K / V tile (the softmax warps use the same rule)
+      if (p.o_tma && p.n_split <= 1 && it.nx[mat] > 0 &&
+          it.rx_end[mat] - it.rx0[mat] == BM) {
+        const int st = (gj - 1) & 1;
+        pend[st] = true;
+        pend_g[st] = it.g;
+        pend_tok[st] = it.q0 + it.rx0[mat] / G;
+      }
     }
     if (lane == 0) {
+      // the last items' staged O, then every store complete
+      if (ok && (!flush(0) || !flush(1))) ok = false;
+      bulk_wait_all();
       // no copy may be in flight when the CTA exits
       for (int t = max(0, gj - 2); t < gj; ++t)
         mbar_drain(mat ? v_full(t & 1) : k_full(t & 1), (t >> 1) & 1);
@@ -2045,6 +2094,7 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
     const uint32_t o_addr = s_addr + BN;
     int s_cnt = 0;                            // S_x tiles seen so far
     int n_done = 0;
+    int g_base = 0;                           // K / V tiles of earlier items
     bool ok = true;
     PtItem it;
     int got = take_item(0, it);
@@ -2235,6 +2285,7 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
       // ---- epilogue: every MMA of the item is complete
       if (!mbar_wait(o_ready, n_done & 1, abort_flag, p.err)) break;
       tc_fence_after();
+
       T* dst = OUT + static_cast<int64_t>(tok) * p.o_st +
                static_cast<int64_t>(h) * p.o_sh;
       if (p.n_split > 1) {
@@ -2289,6 +2340,40 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
             p.lse[static_cast<int64_t>(h) * p.total_q + tok] =
                 p.sinks ? p.sinks[h] : -INFINITY;
         }
+      } else if (p.o_tma && my_rx_end - my_rx0 == BM) {
+        // a full tile: O goes through the (consumed) ring stage of the
+        // item's last K (tile A) or V (tile B) tile; that loader stores it
+        // with one TMA store per 64 columns before it refills the stage
+        float inv, lse_v;
+        finish_row(m_ref, l, p.sinks, h, &inv, &lse_v);
+        inv *= vscale;
+        float ov[D];
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c)
+          tmem_ld32(o_addr + c * 32, ov + c * 32);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(o_free(x));              // O_x may be overwritten now
+        const uint32_t stg = (x ? sV : sK) +
+                             ((g_base + it.n_tiles - 1) & 1) * C::KV_BYTES;
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+          const uint32_t w0 = pack2<T>(ov[8 * c] * inv, ov[8 * c + 1] * inv);
+          const uint32_t w1 =
+              pack2<T>(ov[8 * c + 2] * inv, ov[8 * c + 3] * inv);
+          const uint32_t w2 =
+              pack2<T>(ov[8 * c + 4] * inv, ov[8 * c + 5] * inv);
+          const uint32_t w3 =
+              pack2<T>(ov[8 * c + 6] * inv, ov[8 * c + 7] * inv);
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                           stg + (c >> 3) * (BN * 128) + sw128(r, c & 7)),
+                       "r"(w0), "r"(w1), "r"(w2), "r"(w3)
+                       : "memory");
+        }
+        // the K / V loader stores the staged tile and then refills the stage
+        fence_proxy_async();
+        mbar_arrive(stg_full(x, (g_base + it.n_tiles - 1) & 1));
+        if (p.lse) p.lse[static_cast<int64_t>(h) * p.total_q + tok] = lse_v;
       } else {
         float inv, lse_v;
         finish_row(m_ref, l, p.sinks, h, &inv, &lse_v);
@@ -2326,6 +2411,7 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
         }
       }
       ++n_done;
+      g_base += it.n_tiles;
       it = it_next;
       got = got_next;
     }
@@ -2666,13 +2752,22 @@ cudaError_t launch_prefill_attn_tc(const AttnParams& a, int D, bool bf16,
                             a.q_sh, a.G)
                   ? 1
                   : 0;
+    // the output map has the same box (a tile's 128 packed rows, 64
+    // columns); unsplit launches only (split partials are fp32 rows)
+    CUtensorMap mo;
+    memset(&mo, 0, sizeof(mo));
+    p.o_tma = (p.q_tma && p.n_split == 1 &&
+               make_rows_map(&mo, a.out, bf16, D, a.Hq, a.total_q, a.o_st,
+                             a.o_sh, a.G))
+                  ? 1
+                  : 0;
     auto go3 = [&](void (*kern)(TcParams, CUtensorMap, CUtensorMap,
-                                CUtensorMap),
+                                CUtensorMap, CUtensorMap),
                    int smem) -> cudaError_t {
       cudaError_t e = smem_opt_in(reinterpret_cast<const void*>(kern), smem);
       if (e != cudaSuccess) return e;
       note_launch();
-      kern<<<grid, PT_THREADS, smem, stream>>>(p, mk, mv, mq);
+      kern<<<grid, PT_THREADS, smem, stream>>>(p, mk, mv, mq, mo);
       return cudaGetLastError();
     };
     if (bf16)

@@ -135,6 +135,50 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap,
       : "memory");
 }
 
+// Tiled TMA store of a 3-D box from shared memory (bulk-group completion;
+// the box's inner coordinate c0 must be a multiple of 16 bytes).
+__device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src,
+                                             int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group "
+      "[%0, {%1, %2, %3}], [%4];" ::"l"(reinterpret_cast<uint64_t>(tmap)),
+      "r"(c0), "r"(c1), "r"(c2), "r"(src)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Every committed bulk store has finished reading its shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Every committed bulk store is complete.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Bounded wait until *cnt >= target, for a count that only grows: false
+// when the CTA is aborting, or after kWaitLimitNs (then the error word gets
+// kErrTimeout and the CTA-wide abort flag is raised).
+__device__ __forceinline__ bool count_wait(const volatile int* cnt,
+                                           int target,
+                                           volatile int* abort_flag,
+                                           unsigned* err) {
+  if (*cnt >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (*cnt >= target) return true;
+    if (it == 1 || (it & 255u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 >= kWaitLimitNs || it > kSpinLimit) {
+        *abort_flag = 1;
+        atomicOr(err, kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
