@@ -1719,22 +1719,23 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
     int gj = 0;                                // tiles issued so far
     // O of this loader's tile (A for K, B for V) staged in ring stage st by
     // an epilogue and not yet stored: its box coordinates
-    bool pend[2] = {false, false};
-    int pend_g[2] = {0, 0}, pend_tok[2] = {0, 0};
-    int flushes[2] = {0, 0};                   // stores done per stage
+    // (stage 0 and stage 1 kept apart, in registers)
+    bool pend0 = false, pend1 = false;
+    int g0 = 0, g1 = 0, tok0 = 0, tok1 = 0;
+    int fl0 = 0, fl1 = 0;                      // stores done per stage
     // lane 0: store the O staged in stage st (after the 128 threads of the
     // tile have written it); false on abort
     auto flush = [&](int st) -> bool {
-      if (!pend[st]) return true;
-      if (!mbar_wait(stg_full(mat, st), flushes[st] & 1, abort_flag, p.err))
+      if (!(st ? pend1 : pend0)) return true;
+      const int fl = st ? fl1 : fl0;
+      if (!mbar_wait(stg_full(mat, st), fl & 1, abort_flag, p.err))
         return false;
-      ++flushes[st];
-      pend[st] = false;
+      if (st) { ++fl1; pend1 = false; } else { ++fl0; pend0 = false; }
       const uint32_t src = (mat ? sV : sK) + st * C::KV_BYTES;
+      const int gg = st ? g1 : g0, tt = st ? tok1 : tok0;
 #pragma unroll
       for (int cb = 0; cb < C::NCB; ++cb)
-        tma_store_3d(&tm_o, src + cb * (BN * 128), cb * 64, pend_g[st] * G,
-                     pend_tok[st]);
+        tma_store_3d(&tm_o, src + cb * (BN * 128), cb * 64, gg * G, tt);
       bulk_commit();
       bulk_wait_read_all();
       return true;
@@ -1806,10 +1807,9 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
       // K / V tile (the softmax warps use the same rule)
       if (p.o_tma && p.n_split <= 1 && it.nx[mat] > 0 &&
           it.rx_end[mat] - it.rx0[mat] == BM) {
-        const int st = (gj - 1) & 1;
-        pend[st] = true;
-        pend_g[st] = it.g;
-        pend_tok[st] = it.q0 + it.rx0[mat] / G;
+        const int tt = it.q0 + it.rx0[mat] / G;
+        if ((gj - 1) & 1) { pend1 = true; g1 = it.g; tok1 = tt; }
+        else { pend0 = true; g0 = it.g; tok0 = tt; }
       }
     }
     if (lane == 0) {
@@ -2099,28 +2099,55 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
     PtItem it;
     int got = take_item(0, it);
     ok = got >= 0;
-    while (got > 0 && ok) {
-      const int my_rx0 = x ? it.rx0[1] : it.rx0[0];
-      const int my_rx_end = x ? it.rx_end[1] : it.rx_end[0];
-      const bool my_has = x ? it.has[1] : it.has[0];
-      const int my_tlo = x ? it.tlo[1] : it.tlo[0];
-      const int my_nx = x ? it.nx[1] : it.nx[0];
-      const int R = my_rx0 + r;
-      const bool valid = R < my_rx_end;
-      const int pos = it.ctx + (valid ? R / G : 0);
-      const int h = it.g * G + (valid ? R % G : 0);
-      const int tok = it.q0 + (valid ? R / G : 0);
-      const float slope = (p.alibi && valid) ? p.alibi[h] : 0.f;
-      const int kmin = x ? it.kmn[1] : it.kmn[0];
-      const int kmax = x ? it.kmx[1] : it.kmx[0];
-      int full_lo = kmin, full_hi = kmax;
-      if (my_has) {
-        const int p_lo = it.ctx + my_rx0 / G;
-        const int p_hi = it.ctx + (my_rx_end - 1) / G;
-        if (p.wl >= 0) full_lo = max(full_lo, p_hi - p.wl);
-        if (p.causal) full_hi = min(full_hi, p_lo + 1);
-        if (p.wr >= 0) full_hi = min(full_hi, p_lo + p.wr + 1);
+    // this thread's row of tile x in an item: computed for the next item
+    // while this one waits for its last MMAs (the code runs once per item
+    // and would otherwise sit between the epilogue and the next softmax)
+    struct RowGeo {
+      int rx0, rx_end, tlo, nx, pos, h, tok, kmin, kmax, full_lo, full_hi;
+      float slope;
+      bool valid;
+    };
+    auto row_geo = [&](const PtItem& t) {
+      RowGeo e;
+      e.rx0 = x ? t.rx0[1] : t.rx0[0];
+      e.rx_end = x ? t.rx_end[1] : t.rx_end[0];
+      const bool has = x ? t.has[1] : t.has[0];
+      e.tlo = x ? t.tlo[1] : t.tlo[0];
+      e.nx = x ? t.nx[1] : t.nx[0];
+      const int R = e.rx0 + r;
+      e.valid = R < e.rx_end;
+      e.pos = t.ctx + (e.valid ? R / G : 0);
+      e.h = t.g * G + (e.valid ? R % G : 0);
+      e.tok = t.q0 + (e.valid ? R / G : 0);
+      e.slope = (p.alibi && e.valid) ? p.alibi[e.h] : 0.f;
+      e.kmin = x ? t.kmn[1] : t.kmn[0];
+      e.kmax = x ? t.kmx[1] : t.kmx[0];
+      e.full_lo = e.kmin;
+      e.full_hi = e.kmax;
+      if (has) {
+        const int p_lo = t.ctx + e.rx0 / G;
+        const int p_hi = t.ctx + (e.rx_end - 1) / G;
+        if (p.wl >= 0) e.full_lo = max(e.full_lo, p_hi - p.wl);
+        if (p.causal) e.full_hi = min(e.full_hi, p_lo + 1);
+        if (p.wr >= 0) e.full_hi = min(e.full_hi, p_lo + p.wr + 1);
       }
+      return e;
+    };
+    RowGeo cg{};
+    if (got > 0) cg = row_geo(it);
+    while (got > 0 && ok) {
+      const int my_rx0 = cg.rx0;
+      const int my_rx_end = cg.rx_end;
+      const int my_tlo = cg.tlo;
+      const int my_nx = cg.nx;
+      const bool valid = cg.valid;
+      const int pos = cg.pos;
+      const int h = cg.h;
+      const int tok = cg.tok;
+      const float slope = cg.slope;
+      const int kmin = cg.kmin;
+      const int kmax = cg.kmax;
+      const int full_lo = cg.full_lo, full_hi = cg.full_hi;
       float m_ref = -INFINITY, l = 0.f;
       for (int jx = 0; jx < my_nx; ++jx, ++s_cnt) {
         if (!mbar_wait(s_full(x), s_cnt & 1, abort_flag, p.err)) {
@@ -2282,6 +2309,8 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
       PtItem it_next;
       const int got_next = take_item(n_done + 1, it_next);
       if (got_next < 0) break;
+      RowGeo ng{};
+      if (got_next > 0) ng = row_geo(it_next);
       // ---- epilogue: every MMA of the item is complete
       if (!mbar_wait(o_ready, n_done & 1, abort_flag, p.err)) break;
       tc_fence_after();
@@ -2413,6 +2442,7 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
       ++n_done;
       g_base += it.n_tiles;
       it = it_next;
+      cg = ng;
       got = got_next;
     }
   }
