@@ -1609,7 +1609,8 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
   auto s_full = [&](int x) { return bar0 + 8 * (8 + x); };
   auto p_full = [&](int x) { return bar0 + 8 * (10 + x); };
   auto o_free = [&](int x) { return bar0 + 8 * (12 + x); };
-  const uint32_t o_ready = bar0 + 8 * 14;
+  // o_ready(x): every MMA of an item up to its last P_x V is complete
+  auto o_ready = [&](int x) { return bar0 + 8 * (x ? 31 : 14); };
   const uint32_t q_full = bar0 + 8 * 15;
   const uint32_t q_empty = bar0 + 8 * 16;
   const uint32_t drain_bar = bar0 + 8 * 17;    // the MMA warp's final drain
@@ -1625,7 +1626,7 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
   // stage s of K (x = 0) or V (x = 1); the K / V loader then stores it
   // with TMA and refills the stage
   auto stg_full = [&](int x, int st) { return bar0 + 8 * (27 + 2 * x + st); };
-  static_assert(8 * 31 <= C::BAR_BYTES, "barrier area");
+  static_assert(8 * 32 <= C::BAR_BYTES, "barrier area");
   static_assert(19 + 2 * PT_ITEM_SLOTS <= 27, "staging barriers overlap");
   const bool dyn = p.sched != nullptr;
 
@@ -1639,7 +1640,8 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
       mbar_init(p_full(s), 128);
       mbar_init(o_free(s), 128);
     }
-    mbar_init(o_ready, 1);
+    mbar_init(o_ready(0), 1);
+    mbar_init(o_ready(1), 1);
     for (int xx = 0; xx < 2; ++xx)
       for (int st = 0; st < 2; ++st) mbar_init(stg_full(xx, st), 128);
     mbar_init(q_full, p.q_tma ? 1 : 32);
@@ -1822,22 +1824,57 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
     }
   } else if (warp == PT_MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer
+    // Per item, rounds j = 1 .. n - 1 issue P_x(j - 1) V and S_x(j) for both
+    // tiles.  The item's first S MMAs and its last P V MMAs go out at the
+    // boundary with its neighbours: P_A(last) V, o_ready(A), the next
+    // item's S_A(0), P_B(last) V, o_ready(B), S_B(0).  Each tile's epilogue
+    // then starts when its own MMAs are done, while the other tile and the
+    // next item keep the tensor pipe busy.
     constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value;
     constexpr uint32_t ID_S = idesc(128, BN, kBF16, false);
     constexpr uint32_t ID_PV = idesc(128, D, kBF16, true);
     bool ok = true;
-    int gj = 0;                       // K / V tiles consumed so far
+    int gj = 0;                       // K / V tiles of earlier items
     int pv_cnt[2] = {0, 0};           // P_x V MMAs issued so far
     int n_done = 0;                   // items finished
     PtItem it;
     int got = take_item(0, it);
     ok = got >= 0;
-    while (got > 0 && ok) {
-      if (!mbar_wait(q_full, n_done & 1, abort_flag, p.err)) {
-        ok = false;
-        break;
-      }
+    auto issue_s = [&](int x, int gk) {
+      const uint64_t a0 = sdesc(sQ + x * C::Q_BYTES, 16, 1024);
+      const uint64_t b0 = sdesc(sK + (gk & 1) * C::KV_BYTES, 16, 1024);
+#pragma unroll
+      for (int k = 0; k < D / 16; ++k)
+        mma_f16_warp(tmem + x * C::X_COLS,
+                     a0 + (((k >> 2) * (BM * 128) + (k & 3) * 32) >> 4),
+                     b0 + (((k >> 2) * (BN * 128) + (k & 3) * 32) >> 4),
+                     ID_S, k > 0 ? 1 : 0);
+      mma_commit_warp(s_full(x));
+    };
+    // the first round of item t (Q of item m, K / V tiles from gb): its S
+    // MMAs, and q_empty when they are all of the item's; false on abort
+    auto first_round = [&](const PtItem& t, int m, int gb) -> bool {
+      if (!mbar_wait(q_full, m & 1, abort_flag, p.err)) return false;
       tc_fence_after();
+      bool k_here = false;
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        if (t.n_tiles > 0 && t.tlo[x] == 0 && t.nx[x] > 0) {
+          if (!k_here) {
+            if (!mbar_wait(k_full(gb & 1), (gb >> 1) & 1, abort_flag, p.err))
+              return false;
+            tc_fence_after();
+            k_here = true;
+          }
+          issue_s(x, gb);
+        }
+      }
+      if (t.n_tiles > 0) mma_commit_warp(k_empty(gb & 1));
+      if (t.n_tiles <= 1) mma_commit_warp(q_empty);
+      return true;
+    };
+    if (got > 0 && !first_round(it, 0, 0)) ok = false;
+    while (got > 0 && ok) {
       bool o_mine[2] = {n_done == 0, n_done == 0};   // O_x free to write
       auto claim_o = [&](int x) -> bool {
         if (o_mine[x]) return true;
@@ -1893,34 +1930,20 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
                               (ix > 0 || k > 0) ? 1 : 0);
         return true;
       };
-      auto issue_s = [&](int x, int j) {
-        const uint64_t a0 = sdesc(sQ + x * C::Q_BYTES, 16, 1024);
-        const uint64_t b0 =
-            sdesc(sK + ((gj + j) & 1) * C::KV_BYTES, 16, 1024);
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          mma_f16_warp(tmem + x * C::X_COLS,
-                       a0 + (((k >> 2) * (BM * 128) + (k & 3) * 32) >> 4),
-                       b0 + (((k >> 2) * (BN * 128) + (k & 3) * 32) >> 4),
-                       ID_S, k > 0 ? 1 : 0);
-        mma_commit_warp(s_full(x));
-      };
-      for (int j = 0; j <= it.n_tiles && ok; ++j) {
-        const bool pv = j >= 1;              // P(j-1) V_{j-1} this round
-        const bool sj = j < it.n_tiles;      // S(j) this round
+      for (int j = 1; j < it.n_tiles && ok; ++j) {
         const int gk = gj + j;
         bool k_here = false;                 // K_j waited for
-        if (pv && !v_ready(j - 1)) {
+        if (!v_ready(j - 1)) {
           ok = false;
           break;
         }
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
-          if (pv && in_range(x, j - 1) && !issue_pv(x, j - 1)) {
+          if (in_range(x, j - 1) && !issue_pv(x, j - 1)) {
             ok = false;
             break;
           }
-          if (sj && in_range(x, j)) {
+          if (in_range(x, j)) {
             if (!k_here) {
               if (!mbar_wait(k_full(gk & 1), (gk >> 1) & 1, abort_flag,
                              p.err)) {
@@ -1930,26 +1953,73 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
               tc_fence_after();
               k_here = true;
             }
-            issue_s(x, j);
+            issue_s(x, gk);
           }
         }
         if (!ok) break;
-        if (sj) mma_commit_warp(k_empty(gk & 1));
-        if (pv) mma_commit_warp(v_empty((gk - 1) & 1));
-        if (j == it.n_tiles - 1 || it.n_tiles == 0) mma_commit_warp(q_empty);
+        mma_commit_warp(k_empty(gk & 1));
+        mma_commit_warp(v_empty((gk - 1) & 1));
+        if (j == it.n_tiles - 1) mma_commit_warp(q_empty);
       }
       if (!ok) break;
-      // the next item, taken from the ring before o_ready lets the output
-      // stores start (they hold up shared-memory access while they drain)
+      // ---- boundary: this item's last P V MMAs and o_ready per tile, the
+      // next item's first S MMAs between them
       PtItem it_next;
       const int got_next = take_item(n_done + 1, it_next);
       if (got_next < 0) break;
-      // the previous item's O_x must be read before o_ready can move on
-      if (!claim_o(0) || !claim_o(1)) {
-        ok = false;
-        break;
+      const int last = it.n_tiles - 1;
+      const int gn = gj + it.n_tiles;        // the next item's first tile
+      if (last >= 0 && !v_ready(last)) break;
+      bool q_next = false, k_next = false;
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        if (last >= 0 && in_range(x, last) && !issue_pv(x, last)) {
+          ok = false;
+          break;
+        }
+        // an item with no P_x V still waits for the epilogue before it, so
+        // that no o_free phase is skipped
+        if (!claim_o(x)) {
+          ok = false;
+          break;
+        }
+        mma_commit_warp(o_ready(x));
+        if (got_next > 0 && it_next.n_tiles > 0 && it_next.tlo[x] == 0 &&
+            it_next.nx[x] > 0) {
+          if (!q_next) {
+            if (!mbar_wait(q_full, (n_done + 1) & 1, abort_flag, p.err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            q_next = true;
+          }
+          if (!k_next) {
+            if (!mbar_wait(k_full(gn & 1), (gn >> 1) & 1, abort_flag,
+                           p.err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            k_next = true;
+          }
+          issue_s(x, gn);
+        }
       }
-      mma_commit_warp(o_ready);
+      if (!ok) break;
+      if (last >= 0) mma_commit_warp(v_empty((gj + last) & 1));
+      if (got_next > 0) {
+        // the rest of the next item's first round (as in first_round)
+        if (!q_next) {
+          if (!mbar_wait(q_full, (n_done + 1) & 1, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        if (it_next.n_tiles > 0) mma_commit_warp(k_empty(gn & 1));
+        if (it_next.n_tiles <= 1) mma_commit_warp(q_empty);
+      }
       gj += it.n_tiles;
       ++n_done;
       it = it_next;
@@ -2312,7 +2382,7 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
       RowGeo ng{};
       if (got_next > 0) ng = row_geo(it_next);
       // ---- epilogue: every MMA of the item is complete
-      if (!mbar_wait(o_ready, n_done & 1, abort_flag, p.err)) break;
+      if (!mbar_wait(o_ready(x), n_done & 1, abort_flag, p.err)) break;
       tc_fence_after();
 
       T* dst = OUT + static_cast<int64_t>(tok) * p.o_st +
