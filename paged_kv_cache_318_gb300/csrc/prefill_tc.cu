@@ -1943,6 +1943,9 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
             ok = false;
             break;
           }
+          // V_{j-1} is free once both P V MMAs are done: release it before
+          // S_B(j), so that the tile after next starts loading earlier
+          if (x == 1) mma_commit_warp(v_empty((gk - 1) & 1));
           if (in_range(x, j)) {
             if (!k_here) {
               if (!mbar_wait(k_full(gk & 1), (gk >> 1) & 1, abort_flag,
@@ -1958,7 +1961,6 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
         }
         if (!ok) break;
         mma_commit_warp(k_empty(gk & 1));
-        mma_commit_warp(v_empty((gk - 1) & 1));
         if (j == it.n_tiles - 1) mma_commit_warp(q_empty);
       }
       if (!ok) break;
@@ -1984,6 +1986,7 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
           break;
         }
         mma_commit_warp(o_ready(x));
+        if (x == 1 && last >= 0) mma_commit_warp(v_empty((gj + last) & 1));
         if (got_next > 0 && it_next.n_tiles > 0 && it_next.tlo[x] == 0 &&
             it_next.nx[x] > 0) {
           if (!q_next) {
@@ -2007,7 +2010,6 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
         }
       }
       if (!ok) break;
-      if (last >= 0) mma_commit_warp(v_empty((gj + last) & 1));
       if (got_next > 0) {
         // the rest of the next item's first round (as in first_round)
         if (!q_next) {
