@@ -93,6 +93,9 @@ template <typename T, int D, int ROW_WARPS, int KEY_WARPS, int KT, int STAGES,
           bool KV8 = false>
 __global__ void __launch_bounds__(32 * ROW_WARPS * KEY_WARPS)
 attn_mma_kernel(const AttnParams p) {
+  // a prefill launch queued after this one in the same call may start
+  // before this grid ends (it writes other requests' rows)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   using C = MmaCfg<D, ROW_WARPS, KEY_WARPS, KT, STAGES, KV8>;
   extern __shared__ __align__(128) unsigned char smem[];
 
@@ -565,6 +568,9 @@ attn_mma_kernel(const AttnParams p) {
 template <typename T>
 __global__ void __launch_bounds__(128)
 split_combine_kernel(const CombineParams p) {
+  // a prefill launch queued after this one in the same call may start
+  // before this grid ends (it writes other requests' rows)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y * 4 + warp;
   const int b = blockIdx.x;

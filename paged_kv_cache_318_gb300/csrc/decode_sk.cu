@@ -1170,6 +1170,9 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
 template <typename T, int D>
 __global__ void __launch_bounds__(128) fold_kernel(const AttnParams p,
                                                    int chunks) {
+  // a prefill launch queued after this one in the same call may start
+  // before this grid ends (it writes other requests' rows)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // launched as a programmatic dependent of the decode grid: wait until it
   // has finished and its writes are visible
   asm volatile("griddepcontrol.wait;" ::: "memory");

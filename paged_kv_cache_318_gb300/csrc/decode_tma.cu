@@ -518,6 +518,9 @@ template <typename T, int D, int NCW, int KT, int STAGES>
 __global__ void __launch_bounds__((NCW + 1) * 32)
 decode_tma_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v) {
+  // a prefill launch queued after this one in the same call may start
+  // before this grid ends (it writes other requests' rows)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   decode_tma_body<T, D, NCW, KT, STAGES>(p, tm_k, tm_v);
   if (p.pdl_done && threadIdx.x == 0) {
     const unsigned total = gridDim.x * gridDim.y;

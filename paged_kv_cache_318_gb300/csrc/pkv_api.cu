@@ -82,6 +82,15 @@ bool stride16(int64_t s, int elem) { return (s * elem) % 16 == 0; }
 
 // ----------------------------------------------------------- split plan
 
+// Launch the prefill kernel as a programmatic dependent of the call's
+// decode kernels (1) or after them (0).  Measured on GB300, same box: the
+// varlen prefill (8 requests, 11207 tokens, every request prefill-class)
+// 0.249 ms dependent against 0.240 ms after; the Gemma-like mixed batch
+// (124 decodes + 4 prefill chunks) 0.838 against 0.844 ms.
+#ifndef PKV_PREFILL_AFTER_DECODE_PDL
+#define PKV_PREFILL_AFTER_DECODE_PDL 0
+#endif
+
 // Units of at least this many keys count as long for the decode kernel
 // choice.
 constexpr int64_t kLongUnitKeys = 2048;
@@ -890,6 +899,15 @@ pkv_status attention_impl(
     p.q_scale = opts->q_scale;
   }
 
+  // the prefill kernel's item counter is zeroed before any decode kernel, so
+  // that the prefill launch can follow those kernels directly
+  bool sched_zeroed = false;
+  if (pl.prefill && sched) {
+    cudaError_t e = cudaMemsetAsync(sched, 0, sizeof(int), s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    sched_zeroed = true;
+  }
+
   if (pl.decode) {
     AttnParams d = sk_scratch ? p : p16;
     d.min_rows = 1;
@@ -951,6 +969,7 @@ pkv_status attention_impl(
     f.max_rows = 0x7fffffff;
     f.chunk = 0;
     f.sched = sched;
+    f.sched_zeroed = sched_zeroed ? 1 : 0;
     f.pre_splits = pre_splits;
     f.pre_o = pre_o;
     f.pre_lse = pre_lse;
@@ -982,9 +1001,14 @@ pkv_status attention_impl(
     const int which = g_prefill_kernel.load();
     int used = 1;
     if (which == PKV_PREFILL_TCGEN05 || which == PKV_PREFILL_TCGEN05_SMEM_P)
+      // as a programmatic dependent of the decode kernels just launched
+      // (none of their output is read here); not after an fp8 page copy,
+      // which this launch reads
       e = launch_prefill_attn_tc(f, head_size, bf16,
                                  static_cast<int>((prow + 127) / 128),
-                                 which == PKV_PREFILL_TCGEN05, &used, s);
+                                 which == PKV_PREFILL_TCGEN05, &used, s,
+                                 PKV_PREFILL_AFTER_DECODE_PDL && pl.decode &&
+                                     !kv8);
     else
       e = launch_prefill_attn_mma(f, head_size, bf16,
                                   static_cast<int>((prow + 63) / 64), s);

@@ -244,6 +244,7 @@ struct AttnParams {
   // persistent prefill: one int of workspace the kernel hands work items
   // out through (the launcher zeroes it first); null = fixed item order
   int* sched;
+  int sched_zeroed;           // the caller has zeroed *sched already
   // persistent decode: the tile sequence is cut into sk_chunks chunks (one
   // per CTA); per chunk, the unit it starts inside (x) and the unit it
   // starts that runs past its end (y), -1 for none.  Partial slots hold
@@ -372,9 +373,12 @@ cudaError_t launch_prefill_attn_mma(const AttnParams& p, int D, bool bf16,
                                     int grid_y, cudaStream_t stream);
 // *splits_used: the key splits the launch wrote partials for (1 = the
 // outputs themselves were written).
+// pdl: launch as a programmatic dependent of the kernel queued just before
+// (the call's decode kernels, which write other requests' rows).
 cudaError_t launch_prefill_attn_tc(const AttnParams& p, int D, bool bf16,
                                    int grid_y, bool p_in_tmem,
-                                   int* splits_used, cudaStream_t stream);
+                                   int* splits_used, cudaStream_t stream,
+                                   bool pdl = false);
 // Fold the prefill kernel's split-KV partials (p.splits of them, every one
 // written for each row) of the requests with rows >= p.min_rows.
 cudaError_t launch_prefill_split_combine(const CombineParams& p,

@@ -764,6 +764,9 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
         "r"(C::TMEM_COLS)
         : "memory");
   }
+  // launched as a programmatic dependent of the call's decode kernels:
+  // this grid ends after them, so that later work sees both
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ------------------------------------------------ two-tile (ping-pong) kernel
@@ -1324,6 +1327,9 @@ prefill_pp_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
         "r"(C::TMEM_COLS)
         : "memory");
   }
+  // launched as a programmatic dependent of the call's decode kernels:
+  // this grid ends after them, so that later work sees both
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ------------------------------- two-tile kernel with P in tensor memory
@@ -2528,6 +2534,9 @@ prefill_ptmem_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
         "r"(C::TMEM_COLS)
         : "memory");
   }
+  // launched as a programmatic dependent of the call's decode kernels:
+  // this grid ends after them, so that later work sees both
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // Fold the split-KV partials of prefill-class requests.  One warp per
@@ -2716,7 +2725,8 @@ cudaError_t launch_prefill_split_combine(const CombineParams& p,
 
 cudaError_t launch_prefill_attn_tc(const AttnParams& a, int D, bool bf16,
                                    int grid_y, bool p_in_tmem,
-                                   int* splits_used, cudaStream_t stream) {
+                                   int* splits_used, cudaStream_t stream,
+                                   bool pdl) {
   using namespace tc;
   if (splits_used) *splits_used = 1;
   TcParams p{};
@@ -2782,12 +2792,28 @@ cudaError_t launch_prefill_attn_tc(const AttnParams& a, int D, bool bf16,
   dim3 grid(static_cast<unsigned>(gx));
   p.n_items = static_cast<int>(gx);
   p.n_split = 1;
+  // the launch configuration (programmatic dependent when pdl)
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  auto config = [&](int threads, int smem) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = pdl ? attr : nullptr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cfg;
+  };
   auto go = [&](void (*kern)(TcParams, CUtensorMap, CUtensorMap), int smem,
                 int threads) -> cudaError_t {
     cudaError_t e = smem_opt_in(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
     note_launch();
-    kern<<<grid, threads, smem, stream>>>(p, mk, mv);
+    const cudaLaunchConfig_t cfg = config(threads, smem);
+    e = cudaLaunchKernelEx(&cfg, kern, p, mk, mv);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
   };
   if (p_in_tmem) {
@@ -2839,8 +2865,10 @@ cudaError_t launch_prefill_attn_tc(const AttnParams& a, int D, bool bf16,
       // of 1-200 tokens, about 39 items per SM, ran 10 % faster in the
       // fixed order; 9.7 per SM ran 2 % faster dealt at run time)
       if (a.sched && items <= 16 * static_cast<int64_t>(sms)) {
-        cudaError_t e = cudaMemsetAsync(a.sched, 0, sizeof(int), stream);
-        if (e != cudaSuccess) return e;
+        if (!a.sched_zeroed) {
+          cudaError_t e = cudaMemsetAsync(a.sched, 0, sizeof(int), stream);
+          if (e != cudaSuccess) return e;
+        }
         p.sched = a.sched;
       }
     }
@@ -2869,7 +2897,9 @@ cudaError_t launch_prefill_attn_tc(const AttnParams& a, int D, bool bf16,
       cudaError_t e = smem_opt_in(reinterpret_cast<const void*>(kern), smem);
       if (e != cudaSuccess) return e;
       note_launch();
-      kern<<<grid, PT_THREADS, smem, stream>>>(p, mk, mv, mq, mo);
+      const cudaLaunchConfig_t cfg = config(PT_THREADS, smem);
+      e = cudaLaunchKernelEx(&cfg, kern, p, mk, mv, mq, mo);
+      if (e != cudaSuccess) return e;
       return cudaGetLastError();
     };
     if (bf16)
