@@ -571,6 +571,9 @@ split_combine_kernel(const CombineParams p) {
   // a prefill launch queued after this one in the same call may start
   // before this grid ends (it writes other requests' rows)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // launched as a programmatic dependent of the decode grid: its partials
+  // are complete and visible after this
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y * 4 + warp;
   const int b = blockIdx.x;
@@ -700,13 +703,22 @@ cudaError_t launch_prefill_attn_mma(const AttnParams& p, int D, bool bf16,
 }
 
 cudaError_t launch_split_combine(const CombineParams& p, bool bf16,
-                                 cudaStream_t stream) {
+                                 cudaStream_t stream, bool pdl) {
   dim3 grid(static_cast<unsigned>(p.batch), (p.Hq + 3) / 4);
   note_launch();
-  if (bf16)
-    split_combine_kernel<__nv_bfloat16><<<grid, 128, 0, stream>>>(p);
-  else
-    split_combine_kernel<__half><<<grid, 128, 0, stream>>>(p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(128);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  const cudaError_t e =
+      bf16 ? cudaLaunchKernelEx(&cfg, split_combine_kernel<__nv_bfloat16>, p)
+           : cudaLaunchKernelEx(&cfg, split_combine_kernel<__half>, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

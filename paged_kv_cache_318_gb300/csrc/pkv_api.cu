@@ -899,16 +899,32 @@ pkv_status attention_impl(
     p.q_scale = opts->q_scale;
   }
 
-  // the prefill kernel's item counter is zeroed before any decode kernel, so
-  // that the prefill launch can follow those kernels directly
+  const int which = g_prefill_kernel.load();
+  const bool tc_prefill =
+      which == PKV_PREFILL_TCGEN05 || which == PKV_PREFILL_TCGEN05_SMEM_P;
+  // Prefill first: the persistent prefill kernel takes every SM, and the
+  // decode-class requests' kernel (the one-CTA-per-unit TMA decode kernel)
+  // is its programmatic dependent, so that its CTAs run in the prefill's
+  // tail.  The decode grid's last CTA waits for the prefill grid (a counter
+  // beside the item counter), so whatever follows in the stream still sees
+  // both done.  The two write disjoint rows of the output.
+  const bool prefill_first = pl.prefill && pl.decode && sched && tc_prefill &&
+                             sk_scratch == nullptr && !kv8 &&
+                             dsel != PKV_DECODE_CP_ASYNC &&
+                             pdl_done == nullptr;
+  // the prefill kernel's item counter (and the counter above) is zeroed
+  // before any decode kernel, so that the prefill launch can follow those
+  // kernels directly
   bool sched_zeroed = false;
   if (pl.prefill && sched) {
-    cudaError_t e = cudaMemsetAsync(sched, 0, sizeof(int), s);
+    cudaError_t e = cudaMemsetAsync(sched, 0, 2 * sizeof(int), s);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
     sched_zeroed = true;
   }
 
-  if (pl.decode) {
+  // the decode-class requests; done: the counter of the decode grid's CTAs
+  // when it is a programmatic dependent of the launch before it
+  auto run_decode = [&](int* done) -> pkv_status {
     AttnParams d = sk_scratch ? p : p16;
     d.min_rows = 1;
     d.max_rows = kDecodeRows;
@@ -927,7 +943,7 @@ pkv_status attention_impl(
       e = launch_decode_attn_sk(d, head_size, bf16, sk_ctas, skr, sk_scratch,
                                 s);
     } else if (!kv8 && dsel != PKV_DECODE_CP_ASYNC) {
-      d.pdl_done = pdl_done;
+      d.pdl_done = done;
       e = launch_decode_attn_tma(d, head_size, bf16, pl.splits, s);
     } else {
       e = launch_decode_attn(d, head_size, bf16, pl.splits, 1, s);
@@ -959,11 +975,14 @@ pkv_status attention_impl(
       c.sinks = p.sinks;
       c.min_rows = 1;
       c.max_rows = kDecodeRows;
-      e = launch_split_combine(c, bf16, s);
+      // a dependent of the decode grid when that is one itself
+      e = launch_split_combine(c, bf16, s, done != nullptr);
       if (e != cudaSuccess) return cuda_fail(e, "split combine launch");
     }
-  }
-  if (pl.prefill) {
+    return PKV_OK;
+  };
+
+  auto run_prefill = [&]() -> pkv_status {
     AttnParams f = p16;
     f.min_rows = pl.decode ? kDecodeRows + 1 : 1;
     f.max_rows = 0x7fffffff;
@@ -998,9 +1017,8 @@ pkv_status attention_impl(
       f.num_blocks = static_cast<int64_t>(pages);
       f.kv_fp8 = 0;          // 16-bit copies; k_scale / v_scale still apply
     }
-    const int which = g_prefill_kernel.load();
     int used = 1;
-    if (which == PKV_PREFILL_TCGEN05 || which == PKV_PREFILL_TCGEN05_SMEM_P)
+    if (tc_prefill)
       // as a programmatic dependent of the decode kernels just launched
       // (none of their output is read here); not after an fp8 page copy,
       // which this launch reads
@@ -1008,7 +1026,7 @@ pkv_status attention_impl(
                                  static_cast<int>((prow + 127) / 128),
                                  which == PKV_PREFILL_TCGEN05, &used, s,
                                  PKV_PREFILL_AFTER_DECODE_PDL && pl.decode &&
-                                     !kv8);
+                                     !kv8 && !prefill_first);
     else
       e = launch_prefill_attn_mma(f, head_size, bf16,
                                   static_cast<int>((prow + 63) / 64), s);
@@ -1043,8 +1061,18 @@ pkv_status attention_impl(
         if (e != cudaSuccess) return cuda_fail(e, "prefill split combine");
       }
     }
+    return PKV_OK;
+  };
+
+  pkv_status rc = PKV_OK;
+  if (prefill_first) {
+    rc = run_prefill();
+    if (rc == PKV_OK) rc = run_decode(sched + 1);
+  } else {
+    if (pl.decode) rc = run_decode(pdl_done);
+    if (rc == PKV_OK && pl.prefill) rc = run_prefill();
   }
-  return PKV_OK;
+  return rc;
 }
 
 }  // namespace

@@ -389,8 +389,9 @@ int prefill_tc_block_keys(int D);
 cudaError_t launch_decode_attn_tma(const AttnParams& p, int D, bool bf16,
                                    int grid_x, cudaStream_t stream);
 
+// pdl: launch as a programmatic dependent of the decode grid just queued.
 cudaError_t launch_split_combine(const CombineParams& p, bool bf16,
-                                 cudaStream_t stream);
+                                 cudaStream_t stream, bool pdl = false);
 // Persistent decode attention (decode_sk.cu): 16-bit caches with D in {64,
 // 128, 256}, E4M3 caches with D in {128, 256}.  decode_sk_ctas gives the
 // launch's CTA count on the current device (resident CTAs per SM x sms);
