@@ -57,6 +57,9 @@ merge_kernel(void* __restrict__ out, const void* __restrict__ o1,
              const float* __restrict__ l1, const void* __restrict__ o2,
              const float* __restrict__ l2, float* __restrict__ lse_out, int T,
              int H, int D) {
+  // launched as a programmatic dependent of the kernel before it: its
+  // outputs are complete and visible after this (a no-op otherwise)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int chunks = D / 8;
   const int64_t total = static_cast<int64_t>(T) * H * chunks;
   for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) +
@@ -109,25 +112,34 @@ merge_kernel(void* __restrict__ out, const void* __restrict__ o1,
 template <typename TO, typename TI>
 static void launch_typed(void* out, const void* o1, const float* l1,
                          const void* o2, const float* l2, float* lse, int T,
-                         int H, int D, cudaStream_t stream) {
+                         int H, int D, cudaStream_t stream, bool pdl) {
   const int64_t total = static_cast<int64_t>(T) * H * (D / 8);
   int64_t blocks = (total + 255) / 256;
   const int64_t cap = static_cast<int64_t>(current_sm_count()) * 32;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   note_launch();
-  merge_kernel<TO, TI><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-      out, o1, l1, o2, l2, lse, T, H, D);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  (void)cudaLaunchKernelEx(&cfg, merge_kernel<TO, TI>, out, o1, l1, o2, l2,
+                           lse, T, H, D);
 }
 
 cudaError_t launch_merge(void* out, const void* o1, const float* l1,
                          const void* o2, const float* l2, float* lse_out,
                          int T, int H, int D, pkv_dtype out_dt,
-                         pkv_dtype in_dt, cudaStream_t s) {
-#define PKV_MERGE_CASE(OD, ID, TO, TI)                               \
-  if (out_dt == OD && in_dt == ID) {                                 \
-    launch_typed<TO, TI>(out, o1, l1, o2, l2, lse_out, T, H, D, s);  \
-    return cudaGetLastError();                                       \
+                         pkv_dtype in_dt, cudaStream_t s, bool pdl) {
+#define PKV_MERGE_CASE(OD, ID, TO, TI)                                    \
+  if (out_dt == OD && in_dt == ID) {                                      \
+    launch_typed<TO, TI>(out, o1, l1, o2, l2, lse_out, T, H, D, s, pdl);  \
+    return cudaGetLastError();                                            \
   }
   PKV_MERGE_CASE(PKV_BF16, PKV_BF16, __nv_bfloat16, __nv_bfloat16)
   PKV_MERGE_CASE(PKV_F16, PKV_F16, __half, __half)

@@ -653,6 +653,9 @@ struct Internal {
   CombineParams combine{};
   int combine_max_q = 0;
   bool combine_bf16 = false;
+  // set by the call: a workspace int it zeroed before its first kernel and
+  // does not use itself (null if none)
+  int* zeroed_counter = nullptr;
 };
 
 pkv_status attention_impl(
@@ -920,6 +923,8 @@ pkv_status attention_impl(
     cudaError_t e = cudaMemsetAsync(sched, 0, 2 * sizeof(int), s);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
     sched_zeroed = true;
+    // the second counter is free for the caller unless this call uses it
+    if (in && !prefill_first) in->zeroed_counter = sched + 1;
   }
 
   // the decode-class requests; done: the counter of the decode grid's CTAs
@@ -1241,13 +1246,6 @@ pkv_status pkv_cascade_attention(
     return fail(PKV_ERR_UNSUPPORTED, "output must be 16-byte aligned");
   char* ws = static_cast<char*>(workspace);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  int* done = reinterpret_cast<int*>(ws);
-  if (overlap) {
-    // zeroed before the prefix launch: nothing may come between the prefix
-    // kernel and the suffix decode kernel that depends on it
-    cudaError_t e = cudaMemsetAsync(done, 0, sizeof(int), s);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
-  }
   const int T = num_tokens, Hq = num_heads, D = head_size;
   const int nc = common_prefix_len / block_size;
   void* po = ws + l.po;
@@ -1274,6 +1272,19 @@ pkv_status pkv_cascade_attention(
       num_blocks, softmax_scale, 0, -1, -1, logits_soft_cap, nullptr, 1, pl,
       ws + l.pws, l.pws_bytes, dtype, stream, opts, &pin);
   if (st != PKV_OK) return st;
+  // the suffix decode grid's CTA counter: one the prefix call zeroed before
+  // its kernel, so that nothing comes between the prefix kernel and the
+  // suffix decode kernel that depends on it; else one zeroed here (correct,
+  // without the overlap)
+  int* done = nullptr;
+  if (overlap) {
+    done = pin.zeroed_counter;
+    if (!done) {
+      done = reinterpret_cast<int*>(ws);
+      cudaError_t e = cudaMemsetAsync(done, 0, sizeof(int), s);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    }
+  }
   // suffix: each request's own blocks, causal, without the sinks; its
   // decode kernel may start beside the prefix kernel
   pkv_attention_options so_opts{};
@@ -1295,8 +1306,10 @@ pkv_status pkv_cascade_attention(
         pin.combine, pin.combine_max_q, pin.combine_bf16, s);
     if (e != cudaSuccess) return cuda_fail(e, "prefill split combine");
   }
+  // with the overlap, the merge is a programmatic dependent of the last
+  // suffix kernel, whose grid ends after the prefix grid
   cudaError_t e = launch_merge(output, po, pl, so, sl, nullptr, T, Hq, D,
-                               dtype, dtype, s);
+                               dtype, dtype, s, overlap && !pin.deferred);
   if (e != cudaSuccess) return cuda_fail(e, "merge launch");
   return PKV_OK;
 }

@@ -414,9 +414,11 @@ size_t required_workspace_bytes(int batch, int total_q, int max_seqlen_q,
                                 int num_kv_heads, int head_size,
                                 int block_size, int causal, int window_left,
                                 int window_right, int num_splits);
+// pdl: launch as a programmatic dependent of the kernel queued before it.
 cudaError_t launch_merge(void* out, const void* o1, const float* l1,
                          const void* o2, const float* l2, float* lse_out,
                          int T, int H, int D, pkv_dtype out_dt,
-                         pkv_dtype in_dt, cudaStream_t stream);
+                         pkv_dtype in_dt, cudaStream_t stream,
+                         bool pdl = false);
 
 }  // namespace pkv
