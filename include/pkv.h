@@ -248,9 +248,9 @@ typedef struct {
    * pkv_scaled_fp8_quant).  Needs kv_cache_fp8 (PKV_ERR_UNSUPPORTED
    * otherwise); `dtype` then names the output's type.  The logits are
    * softmax_scale * q_scale * k_scale * sum_d code_q * code_k.  The
-   * persistent decode kernel multiplies the query and key codes on the E4M3
-   * tensor-core path; the other kernels read an exact 16-bit copy of the
-   * query codes that the call writes to its workspace.  Source:
+   * persistent decode kernel widens the query codes to f16 in registers (as
+   * it does the key codes: exact); the other kernels read an exact 16-bit
+   * copy of the query codes that the call writes to its workspace.  Source:
    * "vllm/v1/attention/backends/flash_attn.py" (git view and v0.9.0.1 docs),
    * FlashAttentionImpl.forward (with an fp8 cache the query goes through
    * scaled_fp8_quant(query, layer._q_scale) and the call gets
@@ -258,6 +258,16 @@ typedef struct {
    * get_xqa_bmm1_scale (bmm1 scale = scale * q_scale * k_scale). */
   int q_fp8;
   const float* q_scale;
+  /* no_pdl != 0: launch every kernel of the call in plain stream order.  By
+   * default the persistent decode kernel (pkv_set_decode_kernel) is a
+   * programmatic dependent launch of the kernel queued before it: its CTAs
+   * become resident while that kernel ends and wait for it
+   * (griddepcontrol.wait) before they read or write anything.  This is
+   * correct when that kernel completes only after the work queued before
+   * it, which holds for every kernel of this library and for any kernel
+   * that is not itself a programmatic dependent launch.  (Library plumbing
+   * with no counterpart on the pages.) */
+  int no_pdl;
 } pkv_attention_options;
 
 /* Workspace bytes for pkv_paged_attention_varlen_opts with these options

@@ -48,7 +48,7 @@ class _Options(ctypes.Structure):
                 ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
                 ("cu_seqlens_k", ctypes.c_void_p), ("total_k", ctypes.c_int),
                 ("fixed_split_size", ctypes.c_int), ("q_fp8", ctypes.c_int),
-                ("q_scale", ctypes.c_void_p)]
+                ("q_scale", ctypes.c_void_p), ("no_pdl", ctypes.c_int)]
 
 
 _FP8_CACHE = (torch.float8_e4m3fn, torch.uint8)
@@ -302,7 +302,8 @@ def flash_attn_varlen_func(q, k, v, max_seqlen_q, cu_seqlens_q, max_seqlen_k,
                            return_softmax_lse=False, out=None, num_splits=0,
                            cu_seqlens_k=None, workspace=None, s_aux=None,
                            k_descale=None, v_descale=None,
-                           fixed_split_size=0, q_descale=None):
+                           fixed_split_size=0, q_descale=None,
+                           enable_pdl=True):
     """Varlen attention over a paged KV cache, or over plain K/V rows.
 
     q [T, Hq, D].  Paged: k, v are cache views [num_blocks, block_size, Hkv,
@@ -312,6 +313,8 @@ def flash_attn_varlen_func(q, k, v, max_seqlen_q, cu_seqlens_q, max_seqlen_k,
     [B+1].  fixed_split_size > 0 makes decode split-KV batch-invariant.
     An fp8 (E4M3) q, from ``scaled_fp8_quant``, needs an fp8 cache, its
     scale as ``q_descale`` and ``out`` (which names the output type).
+    ``enable_pdl=False`` launches every kernel in plain stream order
+    (``no_pdl`` in pkv_attention_options).
     Returns out (and lse [Hq, T] float32 when return_softmax_lse).
     """
     lib = load_library()
@@ -395,6 +398,7 @@ def flash_attn_varlen_func(q, k, v, max_seqlen_q, cu_seqlens_q, max_seqlen_k,
         opts.cu_seqlens_k = cu_seqlens_k.data_ptr()
         opts.total_k = k.shape[0]
     opts.fixed_split_size = int(fixed_split_size)
+    opts.no_pdl = 0 if enable_pdl else 1
     ws_need = lib.pkv_paged_attention_workspace_size_opts(
         batch, T, max_seqlen_q, max_seqlen_k, Hq, Hkv, D, BS,
         int(bool(causal)), int(window_size[0]), int(window_size[1]),

@@ -78,6 +78,9 @@ cache_write_warp_kernel(const unsigned char* __restrict__ key,
                         const int64_t* __restrict__ slots, int64_t num_tokens,
                         int Hkv, int BS, int bs_shift, int64_t num_slots,
                         int elem_bytes, unsigned* err) {
+  // an attention kernel queued next as a programmatic dependent may become
+  // resident now (it waits for this grid before reading the cache)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   using V = uint4;    // (16 bytes in four 32-bit registers)
   constexpr int LOG_CH = CH == 8 ? 3 : (CH == 16 ? 4 : 5);
   const int lane = threadIdx.x & 31;

@@ -255,6 +255,10 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
   using C = Cfg<D, NCW, KT, STAGES, KV8, Q8>;
   // MMA input type: the cache's type, or f16 for E4M3 codes
   using MT = typename std::conditional<KV8, __half, T>::type;
+  // launched as a programmatic dependent of the kernel before it: the CTAs
+  // are resident while that kernel ends; nothing is read before it is
+  // complete and its writes are visible (a no-op for a plain launch)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t raw_u = smem_u32(smem_raw);
   const uint32_t base_u = (raw_u + 1023u) & ~1023u;
@@ -1273,11 +1277,22 @@ struct Inst {
   }
 
   static cudaError_t launch(const AttnParams& p, const CUtensorMap& mk,
-                            const CUtensorMap& mv, int grid,
+                            const CUtensorMap& mv, int grid, bool pdl,
                             cudaStream_t stream) {
     note_launch();
-    decode_sk_kernel<T, D, NCW, KT, STAGES, KV8, Q8>
-        <<<grid, C::NT, C::SMEM, stream>>>(p, mk, mv);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(C::NT);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = pdl ? attr : nullptr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    const cudaError_t e = cudaLaunchKernelEx(
+        &cfg, decode_sk_kernel<T, D, NCW, KT, STAGES, KV8, Q8>, p, mk, mv);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }
 };
@@ -1373,7 +1388,7 @@ size_t decode_sk_workspace_bytes(int D, int ctas, int rows) {
 
 cudaError_t launch_decode_attn_sk(const AttnParams& a, int D, bool bf16,
                                   int ctas, int rows, void* scratch,
-                                  cudaStream_t stream) {
+                                  bool pdl, cudaStream_t stream) {
   AttnParams p = a;
   const bool kv8 = p.kv_fp8 != 0, q8 = p.q_fp8 != 0;
   const SkLayout l = sk_layout(D, ctas, rows);
@@ -1398,7 +1413,7 @@ cudaError_t launch_decode_attn_sk(const AttnParams& a, int D, bool bf16,
         !make_kv_map_ex(&mv, p.vc, elem, D, p.BS, p.Hkv, p.num_blocks,
                         p.c_sb, p.c_sr, p.c_sh, RB, p.kv_order_hnd))
       return cudaErrorInvalidValue;
-    return I::launch(p, mk, mv, ctas, stream);
+    return I::launch(p, mk, mv, ctas, pdl, stream);
   });
   if (e != cudaSuccess || l.chunks < 2) return e;
   // the fold as a programmatic dependent launch: its blocks are resident

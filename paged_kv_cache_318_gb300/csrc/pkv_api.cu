@@ -946,7 +946,7 @@ pkv_status attention_impl(
     if (persistent) {
       d.chunk = 0;
       e = launch_decode_attn_sk(d, head_size, bf16, sk_ctas, skr, sk_scratch,
-                                s);
+                                !(opts && opts->no_pdl), s);
     } else if (!kv8 && dsel != PKV_DECODE_CP_ASYNC) {
       d.pdl_done = done;
       e = launch_decode_attn_tma(d, head_size, bf16, pl.splits, s);

@@ -404,9 +404,11 @@ bool decode_sk_supported(int D, bool kv8);
 cudaError_t decode_sk_ctas(int D, bool bf16, bool kv8, bool q8, int sms,
                            int* ctas);
 size_t decode_sk_workspace_bytes(int D, int ctas, int rows);
+// pdl: launch as a programmatic dependent of the kernel queued before it
+// (the kernel waits for it at its start).
 cudaError_t launch_decode_attn_sk(const AttnParams& p, int D, bool bf16,
                                   int ctas, int rows, void* scratch,
-                                  cudaStream_t stream);
+                                  bool pdl, cudaStream_t stream);
 // Required workspace bytes of an attention call (pkv_api.cu): the split-KV
 // partials and fp8 copies it needs, not the optional prefill tail.
 size_t required_workspace_bytes(int batch, int total_q, int max_seqlen_q,

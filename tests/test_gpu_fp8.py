@@ -224,3 +224,59 @@ def test_fp8_query_rejected_without_fp8_cache(cuda_device):
             block_table=torch.from_numpy(wl.block_table).to(dev),
             q_descale=qs, out=torch.empty(wl.q.shape, dtype=wl.q.dtype,
                                           device=dev))
+
+
+def test_dependent_launch_after_cache_write(cuda_device):
+    """The persistent decode kernel launches as a programmatic dependent of
+    the kernel before it.  Queued right behind cache writes that change the
+    rows it reads (no synchronisation between), every call must read the
+    written values: bit-equal to the same call in plain stream order after
+    a device sync, and within tolerance of the oracle at the end."""
+    wl = workloads.build_workload("pdl8", 61, [1] * 24,
+                                  [int(x) for x in np.linspace(40, 6000, 24)],
+                                  32, 8, 128, 16)
+    dev = cuda_device
+    ksc, vsc = 0.011, 0.017
+    cache, kc, vc, ks, vs = fp8_batch(wl, dev, ksc, vsc)
+    q = wl.q.to(dev)
+    cu = torch.from_numpy(wl.cu_seqlens_q).to(dev)
+    used = torch.from_numpy(wl.seq_lens).to(dev)
+    bt = torch.from_numpy(wl.block_table).to(dev)
+    slots = torch.from_numpy(wl.slot_mapping_new).to(dev)
+    gen = torch.Generator().manual_seed(62)
+
+    def call(enable_pdl):
+        return api.flash_attn_varlen_func(
+            q, kc, vc, 1, cu, wl.max_seqlen_k, seqused_k=used,
+            softmax_scale=wl.softmax_scale, causal=True, block_table=bt,
+            k_descale=ks, v_descale=vs, enable_pdl=enable_pdl)
+
+    k_rows = v_rows = None
+    for rep in range(4):
+        # every request's last row changes, then the call reads it at once
+        k_rows = (torch.randn(wl.k_new.shape, generator=gen) * 3).to(
+            wl.k_new.dtype)
+        v_rows = (torch.randn(wl.v_new.shape, generator=gen) * 3).to(
+            wl.v_new.dtype)
+        api.reshape_and_cache_flash(k_rows.to(dev), v_rows.to(dev), kc, vc,
+                                    slots, "fp8", ks, vs)
+        got = call(True)
+        torch.cuda.synchronize()
+        want = call(False)
+        torch.cuda.synchronize()
+        assert torch.equal(got, want), rep
+    api.check_device_errors(dev)
+    shape = wl.cache_shape()[1:]
+    kcodes = np.zeros(shape, np.uint8)
+    vcodes = np.zeros(shape, np.uint8)
+    reshape_and_cache_fp8_ref(f32(wl.k_ctx), f32(wl.v_ctx), kcodes, vcodes,
+                              wl.slot_mapping_ctx, ksc, vsc)
+    reshape_and_cache_fp8_ref(f32(k_rows), f32(v_rows), kcodes, vcodes,
+                              wl.slot_mapping_new, ksc, vsc)
+    kref = e4m3_decode(kcodes) * np.float64(np.float32(ksc))
+    vref = e4m3_decode(vcodes) * np.float64(np.float32(vsc))
+    ro, _ = paged_attention_ref(f32(wl.q).astype(np.float64), kref, vref,
+                                wl.cu_seqlens_q, wl.seq_lens, wl.block_table,
+                                wl.softmax_scale)
+    o = got.float().cpu().numpy()
+    assert np.abs(o - ro).max() <= TOL["bf16"], np.abs(o - ro).max()
