@@ -184,6 +184,11 @@ PREFILL_CASES = [
     ([100, 70], [3000, 900], 32, 8, 128, 16, dict(window_size=(200, 0))),
     ([65, 300], [65, 700], 8, 2, 128, 32, dict(causal=False)),
     ([129, 200], [500, 1200], 16, 4, 64, 16, dict(dtype="f16")),
+    # 240 short requests: 480 items dealt at run time, one item per request
+    # and KV head
+    ([9 + (i * 7) % 32 for i in range(240)],
+     [9 + (i * 7) % 32 + (i * 37) % 150 for i in range(240)], 4, 2, 128, 16,
+     dict()),
 ]
 
 
