@@ -408,12 +408,12 @@ PKV_API size_t pkv_paged_attention_workspace_size(
  * memory, which every GPU that loads the library holds until the process
  * exits.  It calls no cudaMalloc, cudaFree or other allocating routine.
  *
- * - Set-up: the first call on each device looks up the array's device
- *   address (cudaGetSymbolAddress, with that device current) and caches it.
- *   Make that first call before any stream capture.  The cached address
- *   belongs to the device's current context: a process that resets the
- *   device (cudaDeviceReset) after that first call must not call this entry
- *   point again.
+ * - Set-up: every call looks up the array's device address on the current
+ *   device (cudaGetSymbolAddress: a host-side lookup once the module is
+ *   loaded, so a device reset cannot leave a stale address).  The first
+ *   call on a device also raises the kernels' shared-memory limits; make it
+ *   before any stream capture.  Later calls can be captured into a CUDA
+ *   graph.
  * - Inputs: the same as pkv_paged_attention_varlen, which has no options,
  *   so the cache holds fp16/bf16 values (no fp8 cache, sinks or non-paged
  *   keys through this entry point).

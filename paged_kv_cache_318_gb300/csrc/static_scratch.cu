@@ -16,7 +16,6 @@
 // current) and caches it.
 #include <stdio.h>
 
-#include <mutex>
 
 #include "pkv_common.cuh"
 
@@ -28,26 +27,12 @@ constexpr size_t kStaticScratchBytes = PKV_STATIC_SCRATCH_BYTES;
 static __device__ __align__(256) unsigned char
     g_static_scratch[kStaticScratchBytes];
 
-constexpr int kMaxScratchDevices = 64;
-std::mutex g_scratch_mu;
-void* g_scratch_ptr[kMaxScratchDevices] = {};
-
-// Device address of g_static_scratch on the current device (looked up once
-// per device).
+// Device address of g_static_scratch on the current device.  Looked up on
+// every call (a host-side lookup once the module is loaded, no allocation),
+// so that a device reset, which reloads the module, cannot leave a stale
+// address behind.
 cudaError_t scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxScratchDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* ptr = nullptr;
-    e = cudaGetSymbolAddress(&ptr, g_static_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = ptr;
-  }
-  *out = g_scratch_ptr[dev];
-  return cudaSuccess;
+  return cudaGetSymbolAddress(out, g_static_scratch);
 }
 
 }  // namespace

@@ -165,3 +165,36 @@ def test_static_scratch_prefill_uses_the_optional_tail(cuda_device, lib):
         assert torch.equal(lse.view(torch.int32), ref_lse.view(torch.int32))
         if wl.batch == 1:       # (the oracle runs the small case only)
             _assert_oracle(wl, out, lse)
+
+
+def test_static_scratch_call_captured_in_cuda_graph(cuda_device, lib):
+    """After a first call (which sets the kernels' shared-memory limits),
+    a call of the allocation-free entry point can be captured into a CUDA
+    graph: a device allocation or a synchronising call inside it would fail
+    the capture.  Replays equal the eager call bit for bit."""
+    fn = _entry(lib)
+    wl = workloads.batched_decode(batch=16, lo=300, hi=3000,
+                                  pool_blocks=4000, device=cuda_device)
+    wl.num_splits = 4
+    b = DeviceBatch(wl, cuda_device)
+    b.write_context()
+    b.write_new()
+    ref_out = torch.empty_like(b.q)
+    ref_lse = torch.empty((wl.num_heads, wl.num_tokens), dtype=torch.float32,
+                          device=cuda_device)
+    assert _call_static(fn, b, ref_out, ref_lse, 4) == 0, lib.pkv_last_error()
+    torch.cuda.synchronize()
+    out = torch.full_like(ref_out, float("nan"))
+    lse = torch.full_like(ref_lse, float("nan"))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        st = _call_static(fn, b, out, lse, 4)
+    assert st == 0, lib.pkv_last_error()
+    for _ in range(2):
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        api.check_device_errors(cuda_device)
+        assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+        assert torch.equal(lse.view(torch.int32), ref_lse.view(torch.int32))
+    _assert_oracle(b.wl, out, lse)
