@@ -705,3 +705,57 @@ def test_prefill_split_kv_with_sinks(cuda_device):
         assert_close(wl, out[t1 - k:t1].float().cpu().numpy(),
                      lse[:, t1 - k:t1].cpu().numpy(), ro, rl,
                      "sinks req %d" % r)
+
+
+GRAPH_CASES = [
+    # decode-class and prefill-class requests in one call (the prefill
+    # kernel launched first, the decode kernel and the split combine as
+    # programmatic dependents, the item counter zeroed by a memset)
+    ("mixed", dict(q_lens=[1, 300, 1, 1, 90], seq_lens=[700, 900, 40, 3000,
+                                                       400])),
+    # the cascade (prefix kernel, suffix decode beside it, merge)
+    ("cascade", None),
+]
+
+
+@pytest.mark.parametrize("idx", range(len(GRAPH_CASES)))
+def test_call_captured_in_cuda_graph(cuda_device, idx):
+    """The attention calls queue only stream-ordered work (kernels, with
+    programmatic dependent launches, and memsets), so a call can be
+    captured into a CUDA graph: replays equal the eager call bit for bit,
+    and the eager call matches the oracle."""
+    name, kw = GRAPH_CASES[idx]
+    if name == "cascade":
+        wl = workloads.build_workload("gcas", 77, [1] * 12, [800] * 12, 16, 4,
+                                      128, 16, shared_prefix_len=512)
+        cascade = True
+    else:
+        wl = workloads.build_workload("gmix", 78, kw["q_lens"],
+                                      kw["seq_lens"], 32, 8, 128, 16)
+        cascade = False
+    b = DeviceBatch(wl, cuda_device, cascade=cascade)
+    b.write_context()
+    b.write_new()
+    res = b.attend(return_lse=not cascade)
+    torch.cuda.synchronize()
+    api.check_device_errors(cuda_device)
+    out_e, lse_e = res if isinstance(res, tuple) else (res, None)
+    ref_out = out_e.clone()
+    ref_lse = None if lse_e is None else lse_e.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        res_g = b.attend(return_lse=not cascade)
+    out_g, lse_g = res_g if isinstance(res_g, tuple) else (res_g, None)
+    for _ in range(2):
+        out_g.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        api.check_device_errors(cuda_device)
+        assert torch.equal(out_g.view(torch.int16), ref_out.view(torch.int16))
+        if ref_lse is not None:
+            assert torch.equal(lse_g.view(torch.int32),
+                               ref_lse.view(torch.int32))
+    o_ref, l_ref = full_reference(wl)
+    assert_close(wl, ref_out.float().cpu().numpy(),
+                 None if ref_lse is None else ref_lse.cpu().numpy(),
+                 o_ref, l_ref, name)
