@@ -82,13 +82,15 @@ bool stride16(int64_t s, int elem) { return (s * elem) % 16 == 0; }
 
 // ----------------------------------------------------------- split plan
 
-// Launch the prefill kernel as a programmatic dependent of the call's
-// decode kernels (1) or after them (0).  Measured on GB300, same box: the
-// varlen prefill (8 requests, 11207 tokens, every request prefill-class)
-// 0.249 ms dependent against 0.240 ms after; the Gemma-like mixed batch
-// (124 decodes + 4 prefill chunks) 0.838 against 0.844 ms.
+// When the decode-class requests run first (on the persistent decode
+// kernel), launch the prefill kernel as a programmatic dependent of the
+// decode kernels (1) or after them (0): its CTAs then take the SMs the
+// decode's static chunks leave early.  Measured on GB300, same box: the
+// Gemma-like mixed batch (124 decodes + 4 prefill chunks) 0.8393 against
+// 0.8424 ms.  (Calls whose decodes take the per-unit kernel launch the
+// prefill kernel first instead.)
 #ifndef PKV_PREFILL_AFTER_DECODE_PDL
-#define PKV_PREFILL_AFTER_DECODE_PDL 0
+#define PKV_PREFILL_AFTER_DECODE_PDL 1
 #endif
 
 // Units of at least this many keys count as long for the decode kernel
