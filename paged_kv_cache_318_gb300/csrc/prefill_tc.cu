@@ -604,6 +604,7 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
     const float scale_log2 = qk_scale * kLog2e;
     const float scale_over_cap = p.softcap > 0.f ? qk_scale / p.softcap : 0.f;
     const float cap_log2e = p.softcap * kLog2e;
+    const float inv_cap = p.softcap > 0.f ? 1.f / p.softcap : 0.f;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
@@ -642,10 +643,25 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
           mx8[e & 7] = fmaxf(mx8[e & 7], v[e]);
         }
       } else {
+        // keys outside this row's admissible interval [a_lo, a_hi)
+        // (causal, window, the CTA's key range) become -inf; one interval
+        // test per key keeps the unrolled code short (a per-key predicate
+        // chain fills the instruction cache)
+        int a_lo = kmin, a_hi = kmax;
+        if (p.causal) a_hi = min(a_hi, pos + 1);
+        if (p.wl >= 0) a_lo = max(a_lo, pos - p.wl);
+        if (p.wr >= 0) a_hi = min(a_hi, pos + p.wr + 1);
+        if (!valid) a_hi = a_lo;
+        const int lo_rel = a_lo - kt;
+        const int n_rel = max(a_hi - a_lo, 0);
 #pragma unroll
         for (int e = 0; e < BN; ++e) {
-          v[e] = masked_logit(v[e], kt + e, pos, valid, kmin, kmax, p, slope,
-                               qk_scale);
+          float xs = v[e] * qk_scale;
+          if (p.softcap > 0.f) xs = p.softcap * tanh_fast(xs * inv_cap);
+          if (p.alibi) xs -= slope * fabsf(float(pos - (kt + e)));
+          const bool in = static_cast<unsigned>(e - lo_rel) <
+                          static_cast<unsigned>(n_rel);
+          v[e] = in ? xs * kLog2e : -INFINITY;
           mx8[e & 7] = fmaxf(mx8[e & 7], v[e]);
         }
       }
