@@ -248,6 +248,50 @@ __device__ __forceinline__ void tmem_wait_st() {
 }
 
 
+// Packed pair arithmetic on the FMA pipe (one instruction for two fp32
+// values): (a0, a1) = (a0, a1) * s + c and (s0, s1) += (a0, a1).
+__device__ __forceinline__ void fma2(float& a0, float& a1, float s, float c) {
+  uint64_t a, sv, cv;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(sv) : "f"(s));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(cv) : "f"(c));
+  asm("fma.rn.f32x2 %0, %0, %1, %2;" : "+l"(a) : "l"(sv), "l"(cv));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(a));
+}
+__device__ __forceinline__ void add2(float& s0, float& s1, float a0,
+                                     float a1) {
+  uint64_t sv, av;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(sv) : "f"(s0), "f"(s1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(av) : "f"(a0), "f"(a1));
+  asm("add.rn.f32x2 %0, %0, %1;" : "+l"(sv) : "l"(av));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(s0), "=f"(s1) : "l"(sv));
+}
+
+// max(a, b, c) in one instruction (three-input max, sm_100 and later).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// min(max(a + b, 0), 1): the saturating add of the FMA pipe.
+__device__ __forceinline__ float add_sat(float a, float b) {
+  float d;
+  asm("add.rn.sat.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+
+// (s0, s1) <- (s0, s1) * m + c, one packed FMA.
+__device__ __forceinline__ void fma2_pair(float& s0, float& s1, float m,
+                                          float c) {
+  uint64_t sv, mv, cv;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(sv) : "f"(s0), "f"(s1));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(mv) : "f"(m));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(cv) : "f"(c));
+  asm("fma.rn.f32x2 %0, %0, %1, %2;" : "+l"(sv) : "l"(mv), "l"(cv));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(s0), "=f"(s1) : "l"(sv));
+}
+
 // ------------------------------------------------------------------ kernel
 
 // Final logit (log2 units) of one score, with soft-cap, ALiBi and the
@@ -632,15 +676,28 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
       float mx8[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
-      if (fast) {
+      // plain scores stay raw in the max (scale > 0: max(scale s) =
+      // scale max(s)); the scale joins the exponent's FMA
+      const bool raw = fast && scale_log2 > 0.f;
+      if (raw) {
+#pragma unroll
+        for (int e = 0; e < BN; e += 2)
+          mx8[(e >> 1) & 7] = max3f(mx8[(e >> 1) & 7], v[e], v[e + 1]);
+      } else if (fast) {
 #pragma unroll
         for (int e = 0; e < BN; ++e)
           mx8[e & 7] = fmaxf(mx8[e & 7], v[e] * scale_log2);
       } else if (fast_cap) {
 #pragma unroll
-        for (int e = 0; e < BN; ++e) {
-          v[e] = cap_log2e * tanh_fast(v[e] * scale_over_cap);
-          mx8[e & 7] = fmaxf(mx8[e & 7], v[e]);
+        for (int e = 0; e < BN; e += 2) {
+          float x0 = v[e], x1 = v[e + 1];
+          fma2(x0, x1, scale_over_cap, 0.f);
+          x0 = tanh_fast(x0);
+          x1 = tanh_fast(x1);
+          fma2(x0, x1, cap_log2e, 0.f);
+          v[e] = x0;
+          v[e + 1] = x1;
+          mx8[(e >> 1) & 7] = max3f(mx8[(e >> 1) & 7], x0, x1);
         }
       } else {
         // keys outside this row's admissible interval [a_lo, a_hi)
@@ -665,8 +722,9 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
           mx8[e & 7] = fmaxf(mx8[e & 7], v[e]);
         }
       }
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      if (raw) mx *= scale_log2;
       const bool grow = mx > m_ref + kRescaleThreshold;
       float alpha = 1.f;
       if (grow) {
@@ -700,18 +758,16 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
       float sum8[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) sum8[e] = 0.f;
-      if (fast) {
+      const float sc = fast ? scale_log2 : 1.f;
 #pragma unroll
-        for (int e = 0; e < BN; ++e) {
-          v[e] = ex2(fmaf(v[e], scale_log2, -base_m));
-          sum8[e & 7] += v[e];
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < BN; ++e) {
-          v[e] = ex2(v[e] - base_m);
-          sum8[e & 7] += v[e];
-        }
+      for (int e = 0; e < BN; e += 2) {
+        float x0 = v[e], x1 = v[e + 1];
+        fma2(x0, x1, sc, -base_m);
+        x0 = ex2(x0);
+        x1 = ex2(x1);
+        v[e] = x0;
+        v[e + 1] = x1;
+        add2(sum8[2 * ((e >> 1) & 3)], sum8[2 * ((e >> 1) & 3) + 1], x0, x1);
       }
       // P buffer j % PBUF was last read by PV_{j-PBUF}
       const int pbj = j % C::PBUF;
@@ -1417,50 +1473,6 @@ __device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t* w) {
       "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]),
       "r"(w[6]), "r"(w[7])
       : "memory");
-}
-
-// Packed pair arithmetic on the FMA pipe (one instruction for two fp32
-// values): (a0, a1) = (a0, a1) * s + c and (s0, s1) += (a0, a1).
-__device__ __forceinline__ void fma2(float& a0, float& a1, float s, float c) {
-  uint64_t a, sv, cv;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(a0), "f"(a1));
-  asm("mov.b64 %0, {%1, %1};" : "=l"(sv) : "f"(s));
-  asm("mov.b64 %0, {%1, %1};" : "=l"(cv) : "f"(c));
-  asm("fma.rn.f32x2 %0, %0, %1, %2;" : "+l"(a) : "l"(sv), "l"(cv));
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(a));
-}
-__device__ __forceinline__ void add2(float& s0, float& s1, float a0,
-                                     float a1) {
-  uint64_t sv, av;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(sv) : "f"(s0), "f"(s1));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(av) : "f"(a0), "f"(a1));
-  asm("add.rn.f32x2 %0, %0, %1;" : "+l"(sv) : "l"(av));
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(s0), "=f"(s1) : "l"(sv));
-}
-
-// max(a, b, c) in one instruction (three-input max, sm_100 and later).
-__device__ __forceinline__ float max3f(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
-
-// min(max(a + b, 0), 1): the saturating add of the FMA pipe.
-__device__ __forceinline__ float add_sat(float a, float b) {
-  float d;
-  asm("add.rn.sat.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
-  return d;
-}
-
-// (s0, s1) <- (s0, s1) * m + c, one packed FMA.
-__device__ __forceinline__ void fma2_pair(float& s0, float& s1, float m,
-                                          float c) {
-  uint64_t sv, mv, cv;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(sv) : "f"(s0), "f"(s1));
-  asm("mov.b64 %0, {%1, %1};" : "=l"(mv) : "f"(m));
-  asm("mov.b64 %0, {%1, %1};" : "=l"(cv) : "f"(c));
-  asm("fma.rn.f32x2 %0, %0, %1, %2;" : "+l"(sv) : "l"(mv), "l"(cv));
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(s0), "=f"(s1) : "l"(sv));
 }
 
 // D += A * B with A (M = 128 rows x K = 16, 16-bit) in tensor memory.
