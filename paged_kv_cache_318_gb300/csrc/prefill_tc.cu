@@ -47,9 +47,10 @@ namespace pkv {
 namespace tc {
 
 constexpr int BM = 128;
-constexpr int NUM_THREADS = 192;
-constexpr int MMA_WARP = 4;
-constexpr int LOAD_WARP = 5;
+// The head-size-256 kernel: softmax warps 0-7, the MMA warp, the loader.
+constexpr int NUM_THREADS = 320;
+constexpr int MMA_WARP = 8;
+constexpr int LOAD_WARP = 9;
 constexpr float kRescaleThreshold = 8.f;   // log2 units
 
 // Tile geometry per head size.  D <= 128: 64-key tiles, one P buffer and
@@ -78,10 +79,14 @@ struct Cfg {
   static constexpr int OFF_P = OFF_V + STAGES * KV_BYTES;
   static constexpr int OFF_BAR = OFF_P + PBUF * P_BYTES;
   static constexpr int BAR_BYTES = 192;
+  // the softmax warps' exchange of row maxima and sums between the two
+  // key halves: [2 sets][2 halves][128 rows] floats
+  static constexpr int OFF_XCH = OFF_BAR + BAR_BYTES;
+  static constexpr int XCH_BYTES = 2 * 2 * 128 * 4;
   // The dynamic shared window starts 1024-byte aligned (checked at run
   // time); a CTA that takes all 512 TMEM columns also takes enough shared
   // memory that no second CTA fits beside it.
-  static constexpr int SMEM_USED = OFF_BAR + BAR_BYTES;
+  static constexpr int SMEM_USED = OFF_XCH + XCH_BYTES;
   // no more CTAs per SM than TMEM can hold (512 columns per SM)
   static constexpr int SMEM_FLOOR = TMEM_COLS == 512 ? 120 * 1024
                                     : (TMEM_COLS == 256 ? 80 * 1024 : 0);
@@ -313,7 +318,7 @@ __device__ __forceinline__ float masked_logit(float s, int key, int pos,
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(NUM_THREADS, 2)
+__global__ void __launch_bounds__(NUM_THREADS, 1)
 prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v) {
   // a launch queued after this one as its programmatic dependent (the
@@ -426,6 +431,10 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
   auto p_full = [&](int s) { return bar0 + 8 * (12 + s); };
   auto pv_done = [&](int s) { return bar0 + 8 * (14 + s); };
   const uint32_t final_bar = bar0 + 8 * 16;
+  // x_bar(q): the two softmax warps of TMEM lane quarter q (one per key
+  // half) have written their exchange value
+  auto x_bar = [&](int q) { return bar0 + 8 * (19 + q); };
+  static_assert(8 * 23 <= C::BAR_BYTES, "barrier area");
   uint32_t* tmem_slot =
       reinterpret_cast<uint32_t*>(base + C::OFF_BAR + 8 * 18);
   volatile int* abort_flag =
@@ -438,11 +447,12 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
       mbar_init(k_empty(s), 1);
       mbar_init(v_empty(s), 1);
       mbar_init(s_full(s), 1);
-      mbar_init(s_free(s), 128);
-      mbar_init(p_full(s), 128);
+      mbar_init(s_free(s), 256);             // every softmax thread
+      mbar_init(p_full(s), 256);
       mbar_init(pv_done(s), 1);
     }
     mbar_init(final_bar, 1);
+    for (int q = 0; q < 4; ++q) mbar_init(x_bar(q), 64);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -635,7 +645,16 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
     mbar_drain(final_bar, 0);
   } else {
     // ---------------------------------------------------- softmax warps
-    const int r = tid;                         // row in tile == TMEM lane
+    // Eight warps: warp w reads TMEM lanes 32 (w % 4) .. + 31 (its rows)
+    // and the key half hf = w / 4 of each 64-key tile (and O columns
+    // hf D / 2 ..), so two warps per SM sub-partition share each row's
+    // softmax.  The halves agree on the row maximum (and, at the end, the
+    // sum) through shared memory.
+    const int hf = warp >> 2;                  // key half of every tile
+    const int q4 = warp & 3;                   // TMEM lane quarter
+    const int r = tid & 127;                   // row in tile == TMEM lane
+    constexpr int BH = BN / 2;                 // keys of a half
+    constexpr int DH = D / 2;                  // O columns of a half
     const int R = row0 + r;
     const bool valid = R < row_end;
     const int pos = ctx + (valid ? R / G : 0);
@@ -649,8 +668,24 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
     const float scale_over_cap = p.softcap > 0.f ? qk_scale / p.softcap : 0.f;
     const float cap_log2e = p.softcap * kLog2e;
     const float inv_cap = p.softcap > 0.f ? 1.f / p.softcap : 0.f;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    float m_ref = -INFINITY, l = 0.f;
+    const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
+    float* xch = reinterpret_cast<float*>(base + C::OFF_XCH);
+    int x_cnt = 0;                             // exchanges so far
+    // this row's value against the other key half's, in slot set `set`;
+    // false on abort.  A tile's maximum goes to set j & 1: that set is
+    // rewritten two tiles later, after an S MMA the MMA warp issues only
+    // once P_j (every thread's p_full arrival, made after its read) is in.
+    // The final sum uses the set the last maximum did not.
+    auto swap_half = [&](int set, float mine, float& other) -> bool {
+      float* slot = xch + set * 256 + r;
+      slot[hf * 128] = mine;
+      mbar_arrive(x_bar(q4));
+      if (!mbar_wait(x_bar(q4), x_cnt & 1, abort_flag, p.err)) return false;
+      ++x_cnt;
+      other = slot[(hf ^ 1) * 128];
+      return true;
+    };
+    float m_ref = -INFINITY, l = 0.f;          // l: this half's sum
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
       const int sb = j & 1;
@@ -660,15 +695,15 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
       }
       tc_fence_after();
       const int kt = kstart + j * BN;
+      const int kth = kt + hf * BH;            // this half's first key
       const bool unmasked = kt >= full_lo && kt + BN <= full_hi;
       const bool fast = plain && unmasked;
       // soft-cap without ALiBi on an unmasked tile: no per-key mask
       const bool fast_cap = !plain && p.alibi == nullptr && unmasked;
-      const uint32_t s_addr = tmem + lane_base + C::S_COL + sb * BN;
-      // the whole S row (BN = 64 fp32) in one load; S is free right after
-      float v[BN];
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_addr + c * 32, v + c * 32);
+      const uint32_t s_addr = tmem + lane_base + C::S_COL + sb * BN + hf * BH;
+      // this half of the S row (32 fp32) in one load; S is free right after
+      float v[BH];
+      tmem_ld32(s_addr, v);
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(s_free(sb));
@@ -681,15 +716,15 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
       const bool raw = fast && scale_log2 > 0.f;
       if (raw) {
 #pragma unroll
-        for (int e = 0; e < BN; e += 2)
+        for (int e = 0; e < BH; e += 2)
           mx8[(e >> 1) & 7] = max3f(mx8[(e >> 1) & 7], v[e], v[e + 1]);
       } else if (fast) {
 #pragma unroll
-        for (int e = 0; e < BN; ++e)
+        for (int e = 0; e < BH; ++e)
           mx8[e & 7] = fmaxf(mx8[e & 7], v[e] * scale_log2);
       } else if (fast_cap) {
 #pragma unroll
-        for (int e = 0; e < BN; e += 2) {
+        for (int e = 0; e < BH; e += 2) {
           float x0 = v[e], x1 = v[e + 1];
           fma2(x0, x1, scale_over_cap, 0.f);
           x0 = tanh_fast(x0);
@@ -709,13 +744,13 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
         if (p.wl >= 0) a_lo = max(a_lo, pos - p.wl);
         if (p.wr >= 0) a_hi = min(a_hi, pos + p.wr + 1);
         if (!valid) a_hi = a_lo;
-        const int lo_rel = a_lo - kt;
+        const int lo_rel = a_lo - kth;
         const int n_rel = max(a_hi - a_lo, 0);
 #pragma unroll
-        for (int e = 0; e < BN; ++e) {
+        for (int e = 0; e < BH; ++e) {
           float xs = v[e] * qk_scale;
           if (p.softcap > 0.f) xs = p.softcap * tanh_fast(xs * inv_cap);
-          if (p.alibi) xs -= slope * fabsf(float(pos - (kt + e)));
+          if (p.alibi) xs -= slope * fabsf(float(pos - (kth + e)));
           const bool in = static_cast<unsigned>(e - lo_rel) <
                           static_cast<unsigned>(n_rel);
           v[e] = in ? xs * kLog2e : -INFINITY;
@@ -725,6 +760,13 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
       float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                        fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       if (raw) mx *= scale_log2;
+      // the row's maximum over both halves
+      float mx_o;
+      if (!swap_half(sb, mx, mx_o)) {
+        ok = false;
+        break;
+      }
+      mx = fmaxf(mx, mx_o);
       const bool grow = mx > m_ref + kRescaleThreshold;
       float alpha = 1.f;
       if (grow) {
@@ -733,7 +775,8 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
         l *= alpha;
       }
       const float base_m = (m_ref == -INFINITY) ? 0.f : m_ref;
-      // O holds PV_0..PV_{j-1}: rescale it once PV_{j-1} is done
+      // O holds PV_0..PV_{j-1}: rescale this half of it once PV_{j-1} is
+      // done (both halves of a row take the same decision)
       if (j >= 1 && __any_sync(0xffffffffu, grow)) {
         const int pb = (j - 1) % C::PBUF;
         if (!mbar_wait(pv_done(pb), ((j - 1) / C::PBUF) & 1, abort_flag,
@@ -743,9 +786,9 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
         }
         tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < DH / 32; ++c) {
           float ov[32];
-          const uint32_t ta = tmem + lane_base + C::O_COL + c * 32;
+          const uint32_t ta = tmem + lane_base + C::O_COL + hf * DH + c * 32;
           tmem_ld32(ta, ov);
           tmem_wait_ld();
 #pragma unroll
@@ -760,7 +803,7 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
       for (int e = 0; e < 8; ++e) sum8[e] = 0.f;
       const float sc = fast ? scale_log2 : 1.f;
 #pragma unroll
-      for (int e = 0; e < BN; e += 2) {
+      for (int e = 0; e < BH; e += 2) {
         float x0 = v[e], x1 = v[e + 1];
         fma2(x0, x1, sc, -base_m);
         x0 = ex2(x0);
@@ -777,11 +820,12 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
         ok = false;
         break;
       }
-      // P row -> shared memory (K-major, 128-byte swizzle)
+      // this half of the P row -> shared memory (K-major, 128-byte swizzle)
       const uint32_t p_row = sP + pbj * C::P_BYTES;
 #pragma unroll
-      for (int q = 0; q < BN / 8; ++q) {
-        const float* e = v + q * 8;
+      for (int qq = 0; qq < BH / 8; ++qq) {
+        const int q = hf * (BH / 8) + qq;        // 16-byte chunk of the row
+        const float* e = v + qq * 8;
         asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
                          p_row + (q >> 3) * (BM * 128) + sw128(r, q & 7)),
                      "r"(pack2<T>(e[0], e[1])), "r"(pack2<T>(e[2], e[3])),
@@ -795,19 +839,21 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
       mbar_arrive(p_full(pbj));
     }
     const int lb = (n_tiles - 1) % C::PBUF;
+    float l_o = 0.f;
     if (ok && mbar_wait(pv_done(lb), ((n_tiles - 1) / C::PBUF) & 1,
-                        abort_flag, p.err)) {
+                        abort_flag, p.err) &&
+        swap_half(n_tiles & 1, l, l_o)) {
       tc_fence_after();
       float inv, lse_v;
-      finish_row(m_ref, l, p.sinks, h, &inv, &lse_v);
+      finish_row(m_ref, l + l_o, p.sinks, h, &inv, &lse_v);
       inv *= vscale;
       const int tok = q0 + (valid ? R / G : 0);
       T* dst = OUT + static_cast<int64_t>(tok) * p.o_st +
-               static_cast<int64_t>(h) * p.o_sh;
+               static_cast<int64_t>(h) * p.o_sh + hf * DH;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < DH / 32; ++c) {
         float ov[32];
-        tmem_ld32(tmem + lane_base + C::O_COL + c * 32, ov);
+        tmem_ld32(tmem + lane_base + C::O_COL + hf * DH + c * 32, ov);
         tmem_wait_ld();
         if (valid) {
 #pragma unroll
@@ -821,7 +867,7 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
           }
         }
       }
-      if (valid && p.lse)
+      if (valid && p.lse && hf == 0)
         p.lse[static_cast<int64_t>(h) * p.total_q + tok] =
             lse_v;
     }
