@@ -184,6 +184,13 @@ PREFILL_CASES = [
     ([100, 70], [3000, 900], 32, 8, 128, 16, dict(window_size=(200, 0))),
     ([65, 300], [65, 700], 8, 2, 128, 32, dict(causal=False)),
     ([129, 200], [500, 1200], 16, 4, 64, 16, dict(dtype="f16")),
+    # head size 256 (two softmax warps per row): window and soft-cap, ALiBi
+    # in fp16, non-causal
+    ([200, 77], [1300, 300], 8, 4, 256, 32, dict(window_size=(150, 0),
+                                                 softcap=30.0)),
+    ([129, 64], [500, 64], 4, 2, 256, 16,
+     dict(alibi_slopes=[0.05, 0.1, 0.2, 0.4], dtype="f16")),
+    ([100, 40], [260, 700], 8, 2, 256, 32, dict(causal=False)),
     # 240 short requests: 480 items dealt at run time, one item per request
     # and KV head
     ([9 + (i * 7) % 32 for i in range(240)],
