@@ -41,7 +41,7 @@
 // E4M3 caches.  The ring holds the codes (one byte per element, 128-column
 // boxes).  The consumers convert them to f16 in registers with
 // cvt.rn.f16x2.e4m3x2 (exact): K straight from an ldmatrix of the code
-// bytes, V from 32-bit loads of four keys' code quads transposed with prmt.
+// bytes, V from an 8-bit transposing ldmatrix of the code bytes.
 // The query rows are converted to f16 once per unit (a bf16 query is first
 // scaled by a power of two that puts its largest magnitude in [2^14, 2^15),
 // which keeps every value exact in f16; the factor joins the logit scale).
@@ -125,10 +125,10 @@ struct Cfg {
 
 // Index of (row r, column col) of one warp's 16 x D state in the held
 // stage; the column is XOR-swizzled by the row for conflict-free float2
-// (16-bit path) and float4 (fp8 path) stores.
-template <bool KV8, int D>
+// stores.
+template <int D>
 __device__ __forceinline__ int cidx(int r, int col) {
-  return r * D + (col ^ ((r & 7) << (KV8 ? 2 : 3)));
+  return r * D + (col ^ ((r & 7) << 3));
 }
 
 // One unit piece as the producer hands it to the consumers (64 bytes).
@@ -222,11 +222,15 @@ __device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t& lo,
       : "r"(w));
 }
 
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b,
-                                         uint32_t sel) {
-  uint32_t d;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-  return d;
+// An 8-bit 16 x 16 block of shared memory (row addresses from lanes 0-15),
+// transposed: lane t receives rows 4 (t % 4) .. + 3 of column t / 4 in d0
+// and of column t / 4 + 8 in d1 (row 4 (t % 4) in the low byte).
+__device__ __forceinline__ void ldmatrix_b8_trans(uint32_t addr, uint32_t& d0,
+                                                  uint32_t& d1) {
+  asm volatile(
+      "ldmatrix.sync.aligned.m16n16.x1.trans.shared.b8 {%0, %1}, [%2];"
+      : "=r"(d0), "=r"(d1)
+      : "r"(addr));
 }
 
 __device__ __forceinline__ uint32_t lds32(uint32_t a) {
@@ -925,31 +929,23 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
         a[2] = pack2<MT>(sc[2 * ks + 1][0], sc[2 * ks + 1][1]);
         a[3] = pack2<MT>(sc[2 * ks + 1][2], sc[2 * ks + 1][3]);
         if constexpr (KV8) {
-          // keys 2 c4 + {0, 1, 8, 9} of the 16, head-dimension bytes
-          // 4 g8 .. 4 g8 + 3 of each 32-column chunk; column j of the quad
-          // feeds n8 tile 4 * chunk + j
-          const int kr = kw0 + ks * 16 + 2 * c4;
+          // V^T fragments straight from the code bytes: the 8-bit
+          // transposing ldmatrix of a 16-key x 16-column block gives each
+          // lane four keys of column g8 (d0) and of column g8 + 8 (d1).
+          // The row addresses take the keys in the order 2c, 2c + 1,
+          // 2c + 8, 2c + 9 (c = 0 .. 3), so a lane's four are the B
+          // fragment's k = 2 c4, 2 c4 + 1, 2 c4 + 8, 2 c4 + 9.
+          const int li = lane & 15;
+          const int kr = kw0 + ks * 16 + 2 * (li >> 2) + (li & 1) +
+                         ((li & 2) ? 8 : 0);
 #pragma unroll
-          for (int dc = 0; dc < D / 32; ++dc) {
-            const int x = dc * 32 + 4 * g8;            // byte in the row
-            const int ch = x >> 4, wi = x & 15;
-            const uint32_t w0 = lds32(sV + kv_off<KT>(kr, ch) + wi);
-            const uint32_t w1 = lds32(sV + kv_off<KT>(kr + 1, ch) + wi);
-            const uint32_t w2 = lds32(sV + kv_off<KT>(kr + 8, ch) + wi);
-            const uint32_t w3 = lds32(sV + kv_off<KT>(kr + 9, ch) + wi);
-            const uint32_t p01a = prmt(w0, w1, 0x5140);   // cols 0, 1
-            const uint32_t p01b = prmt(w0, w1, 0x7362);   // cols 2, 3
-            const uint32_t p89a = prmt(w2, w3, 0x5140);
-            const uint32_t p89b = prmt(w2, w3, 0x7362);
-            uint32_t lo0, lo1, lo2, lo3, hi0, hi1, hi2, hi3;
-            e4m3x4_to_f16(p01a, lo0, lo1);
-            e4m3x4_to_f16(p01b, lo2, lo3);
-            e4m3x4_to_f16(p89a, hi0, hi1);
-            e4m3x4_to_f16(p89b, hi2, hi3);
-            mma_16816<__half>(o[dc * 4 + 0], a, lo0, hi0);
-            mma_16816<__half>(o[dc * 4 + 1], a, lo1, hi1);
-            mma_16816<__half>(o[dc * 4 + 2], a, lo2, hi2);
-            mma_16816<__half>(o[dc * 4 + 3], a, lo3, hi3);
+          for (int q = 0; q < D / 16; ++q) {
+            uint32_t d0, d1, b0, b1, b2, b3;
+            ldmatrix_b8_trans(sV + kv_off<KT>(kr, q), d0, d1);
+            e4m3x4_to_f16(d0, b0, b1);
+            e4m3x4_to_f16(d1, b2, b3);
+            mma_16816<__half>(o[2 * q], a, b0, b1);
+            mma_16816<__half>(o[2 * q + 1], a, b2, b3);
           }
         } else {
 #pragma unroll
@@ -1025,30 +1021,12 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
         ml[wslot * 32 + rB * 2] = mB;
         ml[wslot * 32 + rB * 2 + 1] = lB;
       }
-      if constexpr (KV8) {
-        // o[4 dc + j][2 h + e] holds column 32 dc + 8 c4 + 4 e + j
 #pragma unroll
-        for (int dc = 0; dc < D / 32; ++dc) {
-          const int col = dc * 32 + 8 * c4;
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int r = g8 + 8 * h;
-            *reinterpret_cast<float4*>(cw + cidx<KV8, D>(r, col)) =
-                make_float4(o[dc * 4 + 0][2 * h], o[dc * 4 + 1][2 * h],
-                            o[dc * 4 + 2][2 * h], o[dc * 4 + 3][2 * h]);
-            *reinterpret_cast<float4*>(cw + cidx<KV8, D>(r, col + 4)) =
-                make_float4(o[dc * 4 + 0][2 * h + 1], o[dc * 4 + 1][2 * h + 1],
-                            o[dc * 4 + 2][2 * h + 1], o[dc * 4 + 3][2 * h + 1]);
-          }
-        }
-      } else {
-#pragma unroll
-        for (int dn = 0; dn < D / 8; ++dn) {
-          *reinterpret_cast<float2*>(cw + cidx<KV8, D>(rA, dn * 8 + 2 * c4)) =
-              make_float2(o[dn][0], o[dn][1]);
-          *reinterpret_cast<float2*>(cw + cidx<KV8, D>(rB, dn * 8 + 2 * c4)) =
-              make_float2(o[dn][2], o[dn][3]);
-        }
+      for (int dn = 0; dn < D / 8; ++dn) {
+        *reinterpret_cast<float2*>(cw + cidx<D>(rA, dn * 8 + 2 * c4)) =
+            make_float2(o[dn][0], o[dn][1]);
+        *reinterpret_cast<float2*>(cw + cidx<D>(rB, dn * 8 + 2 * c4)) =
+            make_float2(o[dn][2], o[dn][3]);
       }
       fence_proxy_async();   // the producer's TMA rewrites this stage later
     }
@@ -1071,7 +1049,7 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
           const float f = ex2(ml[w * 32 + r * 2] - mb);
           lsum += f * ml[w * 32 + r * 2 + 1];
           const float4 v = *reinterpret_cast<const float4*>(
-              comb + w * 16 * D + cidx<KV8, D>(r, col));
+              comb + w * 16 * D + cidx<D>(r, col));
           acc.x += f * v.x;
           acc.y += f * v.y;
           acc.z += f * v.z;
@@ -1108,54 +1086,30 @@ decode_sk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
         float inv, lse;
         finish_row(M, lsum, sinks, g * G + r % G, &inv, &lse);
         inv *= vscale;
-        if constexpr (KV8) {
 #pragma unroll
-          for (int dc = 0; dc < D / 32; ++dc) {
+        for (int dn = 0; dn < D / 8; ++dn) {
+          const int col = dn * 8 + 2 * c4;
+          float v0 = f_own * o[dn][2 * h], v1 = f_own * o[dn][2 * h + 1];
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int col = dc * 32 + 8 * c4 + 4 * e;
-              float4 v = make_float4(f_own * o[dc * 4 + 0][2 * h + e],
-                                     f_own * o[dc * 4 + 1][2 * h + e],
-                                     f_own * o[dc * 4 + 2][2 * h + e],
-                                     f_own * o[dc * 4 + 3][2 * h + e]);
-#pragma unroll
-              for (int w = 0; w < NCW - 1; ++w) {
-                const float4 x = *reinterpret_cast<const float4*>(
-                    comb + w * 16 * D + cidx<KV8, D>(r, col));
-                v.x += fw[w] * x.x;
-                v.y += fw[w] * x.y;
-                v.z += fw[w] * x.z;
-                v.w += fw[w] * x.w;
-              }
-              store_row(r, col, v, inv, lse);
-            }
+          for (int w = 0; w < NCW - 1; ++w) {
+            const float2 x = *reinterpret_cast<const float2*>(
+                comb + w * 16 * D + cidx<D>(r, col));
+            v0 += fw[w] * x.x;
+            v1 += fw[w] * x.y;
           }
-        } else {
-#pragma unroll
-          for (int dn = 0; dn < D / 8; ++dn) {
-            const int col = dn * 8 + 2 * c4;
-            float v0 = f_own * o[dn][2 * h], v1 = f_own * o[dn][2 * h + 1];
-#pragma unroll
-            for (int w = 0; w < NCW - 1; ++w) {
-              const float2 x = *reinterpret_cast<const float2*>(
-                  comb + w * 16 * D + cidx<KV8, D>(r, col));
-              v0 += fw[w] * x.x;
-              v1 += fw[w] * x.y;
-            }
-            const int tok = q0 + r / G, hq = g * G + r % G;
-            if (pslot < 0) {
-              *reinterpret_cast<uint32_t*>(
-                  OUT + static_cast<int64_t>(tok) * p.o_st +
-                  static_cast<int64_t>(hq) * p.o_sh + col) =
-                  pack2<T>(v0 * inv, v1 * inv);
-              if (col == 0 && p.lse)
-                p.lse[static_cast<int64_t>(hq) * p.total_q + tok] = lse;
-            } else {
-              const int64_t sr = static_cast<int64_t>(pslot) * p.sk_rows + r;
-              *reinterpret_cast<float2*>(p.part_o + sr * D + col) =
-                  make_float2(v0 * inv, v1 * inv);
-              if (col == 0) p.part_lse[sr] = lse;
-            }
+          const int tok = q0 + r / G, hq = g * G + r % G;
+          if (pslot < 0) {
+            *reinterpret_cast<uint32_t*>(
+                OUT + static_cast<int64_t>(tok) * p.o_st +
+                static_cast<int64_t>(hq) * p.o_sh + col) =
+                pack2<T>(v0 * inv, v1 * inv);
+            if (col == 0 && p.lse)
+              p.lse[static_cast<int64_t>(hq) * p.total_q + tok] = lse;
+          } else {
+            const int64_t sr = static_cast<int64_t>(pslot) * p.sk_rows + r;
+            *reinterpret_cast<float2*>(p.part_o + sr * D + col) =
+                make_float2(v0 * inv, v1 * inv);
+            if (col == 0) p.part_lse[sr] = lse;
           }
         }
       }
