@@ -24,6 +24,9 @@ scaled_fp8_quant_kernel(const T* __restrict__ in, int64_t in_st,
                         uint8_t* __restrict__ out, int64_t out_st,
                         int64_t rows, int cols,
                         const float* __restrict__ scale) {
+  // an attention kernel queued next as a programmatic dependent may become
+  // resident now (it waits for this grid before reading the codes)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int per_row = cols / 16;
   const int64_t total = rows * per_row;
   const float sc = *scale;
@@ -66,6 +69,9 @@ widen_q_kernel(const uint8_t* __restrict__ q8, int64_t q_st, int64_t q_sh,
                T* __restrict__ q16, int total_q, int Hq, int D,
                const float* __restrict__ k_scale,
                const float* __restrict__ q_scale, float* __restrict__ kq) {
+  // a kernel queued next as a programmatic dependent may become resident
+  // now (it waits for this grid before reading the copy)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (blockIdx.x == 0 && threadIdx.x == 0) *kq = *k_scale * *q_scale;
   const int per_head = D / 16;
   const int64_t total = static_cast<int64_t>(total_q) * Hq * per_head;
