@@ -258,15 +258,19 @@ typedef struct {
    * get_xqa_bmm1_scale (bmm1 scale = scale * q_scale * k_scale). */
   int q_fp8;
   const float* q_scale;
-  /* no_pdl != 0: launch every kernel of the call in plain stream order.  By
-   * default the persistent decode kernel (pkv_set_decode_kernel) is a
-   * programmatic dependent launch of the kernel queued before it: its CTAs
-   * become resident while that kernel ends and wait for it
-   * (griddepcontrol.wait) before they read or write anything.  This is
-   * correct when that kernel completes only after the work queued before
-   * it, which holds for every kernel of this library and for any kernel
-   * that is not itself a programmatic dependent launch.  (Library plumbing
-   * with no counterpart on the pages.) */
+  /* no_pdl != 0: launch every kernel of the call in plain stream order.
+   * By default some launches are programmatic dependent launches: the
+   * persistent decode kernel (pkv_set_decode_kernel) depends on the kernel
+   * queued before the call and waits for it (griddepcontrol.wait) before
+   * it reads or writes anything; in a call with both decode-class and
+   * prefill-class requests, the second of the two attention kernels (and
+   * the split combine after it) may start while the first still runs, and
+   * its grid ends only after the first one's.  The first form is correct
+   * when the kernel queued before the call completes only after the work
+   * queued before it, which holds for every kernel of this library and for
+   * any kernel that is not itself a programmatic dependent launch.
+   * (Library plumbing with no counterpart on the pages; the cascade entry
+   * point has its own `overlap` switch.) */
   int no_pdl;
 } pkv_attention_options;
 

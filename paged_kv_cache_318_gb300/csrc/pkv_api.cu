@@ -913,8 +913,10 @@ pkv_status attention_impl(
   // tail.  The decode grid's last CTA waits for the prefill grid (a counter
   // beside the item counter), so whatever follows in the stream still sees
   // both done.  The two write disjoint rows of the output.
-  const bool prefill_first = pl.prefill && pl.decode && sched && tc_prefill &&
-                             sk_scratch == nullptr && !kv8 &&
+  // no_pdl: every kernel of the call in plain stream order
+  const bool pdl_ok = !(opts && opts->no_pdl);
+  const bool prefill_first = pdl_ok && pl.prefill && pl.decode && sched &&
+                             tc_prefill && sk_scratch == nullptr && !kv8 &&
                              dsel != PKV_DECODE_CP_ASYNC &&
                              pdl_done == nullptr;
   // the prefill kernel's item counter (and the counter above) is zeroed
@@ -948,7 +950,7 @@ pkv_status attention_impl(
     if (persistent) {
       d.chunk = 0;
       e = launch_decode_attn_sk(d, head_size, bf16, sk_ctas, skr, sk_scratch,
-                                !(opts && opts->no_pdl), s);
+                                pdl_ok, s);
     } else if (!kv8 && dsel != PKV_DECODE_CP_ASYNC) {
       d.pdl_done = done;
       e = launch_decode_attn_tma(d, head_size, bf16, pl.splits, s);
@@ -1032,7 +1034,8 @@ pkv_status attention_impl(
       e = launch_prefill_attn_tc(f, head_size, bf16,
                                  static_cast<int>((prow + 127) / 128),
                                  which == PKV_PREFILL_TCGEN05, &used, s,
-                                 PKV_PREFILL_AFTER_DECODE_PDL && pl.decode &&
+                                 pdl_ok && PKV_PREFILL_AFTER_DECODE_PDL &&
+                                     pl.decode &&
                                      !kv8 && !prefill_first);
     else
       e = launch_prefill_attn_mma(f, head_size, bf16,

@@ -766,3 +766,33 @@ def test_call_captured_in_cuda_graph(cuda_device, idx):
     assert_close(wl, ref_out.float().cpu().numpy(),
                  None if ref_lse is None else ref_lse.cpu().numpy(),
                  o_ref, l_ref, name)
+
+
+def test_mixed_call_without_dependent_launches(cuda_device):
+    """A call with decode-class and prefill-class requests launches the
+    prefill kernel first and the decode kernel as its programmatic
+    dependent; with the dependent launches off (``enable_pdl=False``) the
+    decode kernel runs first, in plain stream order.  The two orders write
+    the same bits, which match the oracle."""
+    wl = workloads.build_workload("nopdl", 79, [1, 300, 1, 1, 90, 1],
+                                  [700, 900, 40, 3000, 400, 2500], 32, 8,
+                                  128, 16)
+    b = DeviceBatch(wl, cuda_device)
+    b.write_context()
+    b.write_new()
+    outs = []
+    for pdl in (True, False):
+        out, lse = api.flash_attn_varlen_func(
+            b.q, b.key_cache, b.value_cache, wl.max_seqlen_q,
+            b.cu_seqlens_q, wl.max_seqlen_k, seqused_k=b.seqused_k,
+            softmax_scale=wl.softmax_scale, causal=True,
+            block_table=b.block_table, return_softmax_lse=True,
+            enable_pdl=pdl)
+        torch.cuda.synchronize()
+        api.check_device_errors(cuda_device)
+        outs.append((out.clone(), lse.clone()))
+    assert torch.equal(outs[0][0].view(torch.int16), outs[1][0].view(torch.int16))
+    assert torch.equal(outs[0][1].view(torch.int32), outs[1][1].view(torch.int32))
+    o_ref, l_ref = full_reference(wl)
+    assert_close(wl, outs[0][0].float().cpu().numpy(), outs[0][1].cpu().numpy(),
+                 o_ref, l_ref, "no-pdl")
