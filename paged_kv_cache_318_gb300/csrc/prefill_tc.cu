@@ -47,10 +47,11 @@ namespace pkv {
 namespace tc {
 
 constexpr int BM = 128;
-// The head-size-256 kernel: softmax warps 0-7, the MMA warp, the loader.
-constexpr int NUM_THREADS = 320;
+// The head-size-256 kernel: softmax warps 0-7, the MMA warp, the K and V
+// loaders.
+constexpr int NUM_THREADS = 352;
 constexpr int MMA_WARP = 8;
-constexpr int LOAD_WARP = 9;
+constexpr int LOAD_WARP = 9;       // warps 9 (K) and 10 (V)
 constexpr float kRescaleThreshold = 8.f;   // log2 units
 
 // Tile geometry per head size.  D <= 128: 64-key tiles, one P buffer and
@@ -120,6 +121,9 @@ struct TcParams {
   int n_items;            // persistent kernel: work items (an upper bound)
   int out_v8;             // output rows 32-byte aligned: 256-bit stores
   int kv_order_hnd;   // tensor-map dim order: 1 = (D, BS, Hkv, NB)
+  // head-size-256 kernel: the K / V maps are 5-D row-group maps (one box
+  // per page lands as [8-row group][64-column block][8 rows][64 columns])
+  int kv_rg;
   int* sched;             // persistent kernel: zeroed item counter, or null
   int q_tma;              // persistent kernel: Q tiles arrive as TMA boxes
   // persistent kernel: the O of a full 128-row tile leaves through a TMA
@@ -489,12 +493,20 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == LOAD_WARP) {
-    // ---------------------------------------------------------- producer
-    // Lane i fetches the page id of box i of the next tile while lane 0
-    // issues the TMA boxes of the current one, so block-table latency is
-    // off the critical path.
-    constexpr int MAXBOX = BN / 16;
+  // K / V tile layout in shared memory.  4-D boxes (RB rows of one 64-column
+  // block each) give [column block][key][64]; the 5-D row-group boxes give
+  // [8-key group][column block][8 keys][64].  Either way a 128-byte swizzle
+  // atom is 8 keys x 64 columns: cbs is the stride between column blocks,
+  // gs between 8-key groups.
+  const uint32_t cbs = p.kv_rg ? 1024u : static_cast<uint32_t>(BN * 128);
+  const uint32_t gs = p.kv_rg ? static_cast<uint32_t>(C::NCB * 1024) : 1024u;
+  if (warp >= LOAD_WARP) {
+    // --------------------------------------------------------- producers
+    // Warp LOAD_WARP fills the K ring, the next warp the V ring, so a K
+    // tile never waits behind a V stage.  Lane i issues the box of page i
+    // of a tile and meanwhile fetches page i of the next tile, which keeps
+    // block-table latency off the critical path.
+    const int mat = warp - LOAD_WARP;
     const int32_t* bt = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
     auto fetch = [&](int j) -> int {
       const int k0 = kstart + j * BN + lane * RB;
@@ -507,59 +519,58 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
       }
       return blk;
     };
-    int k_iss = 0, v_iss = 0;
+    const void* tm = mat ? static_cast<const void*>(&tm_v)
+                         : static_cast<const void*>(&tm_k);
+    const uint32_t ring = mat ? sV : sK;
+    int iss = 0;
     int cur = fetch(0);
     for (int j = 0; j < n_tiles; ++j) {
       const int nxt = fetch(j + 1);
-      int ids[MAXBOX];
-#pragma unroll
-      for (int i = 0; i < MAXBOX; ++i) ids[i] = __shfl_sync(0xffffffffu, cur, i);
+      const int s = j & 1;
+      const int kt = kstart + j * BN;
+      int nbox = (kmax - kt + RB - 1) / RB;
+      if (nbox > BN / RB) nbox = BN / RB;
+      const uint32_t full = mat ? v_full(s) : k_full(s);
       int stop = 0;
       if (lane == 0) {
-        const int s = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        const int kt = kstart + j * BN;
-        int nbox = (kmax - kt + RB - 1) / RB;
-        if (nbox > BN / RB) nbox = BN / RB;
-        const uint32_t bytes = nbox * C::NCB * RB * 128;
-        for (int mat = 0; mat < 2; ++mat) {
-          const uint32_t empty = mat ? v_empty(s) : k_empty(s);
-          const uint32_t full = mat ? v_full(s) : k_full(s);
-          if (j >= 2 && !mbar_wait(empty, ph ^ 1, abort_flag, p.err)) {
-            stop = 1;
-            break;
-          }
-          mbar_expect_tx(full, bytes);
-          const void* tm = mat ? static_cast<const void*>(&tm_v)
-                               : static_cast<const void*>(&tm_k);
-          const uint32_t dst0 = (mat ? sV : sK) + s * C::KV_BYTES;
-#pragma unroll
-          for (int i = 0; i < MAXBOX; ++i) {
-            if (i >= nbox) break;
-            const int k0 = kt + i * RB;
-            const int row = p.cu_k ? koff + k0 : k0 % p.BS;
-            for (int cb = 0; cb < C::NCB; ++cb) {
-              const uint32_t dst = dst0 + cb * (BN * 128) + i * RB * 128;
-              if (p.kv_order_hnd)
-                tma_load_4d(dst, tm, cb * 64, row, g, ids[i], full);
-              else
-                tma_load_4d(dst, tm, cb * 64, g, row, ids[i], full);
-            }
-          }
-          if (mat) v_iss = j + 1; else k_iss = j + 1;
-        }
-        if (*abort_flag) stop = 1;
+        const uint32_t empty = mat ? v_empty(s) : k_empty(s);
+        if (j >= 2 &&
+            !mbar_wait(empty, ((j >> 1) & 1) ^ 1, abort_flag, p.err))
+          stop = 1;
+        else
+          mbar_expect_tx(full, nbox * C::NCB * RB * 128);
       }
       stop = __shfl_sync(0xffffffffu, stop, 0);
       if (stop) break;
+      if (lane < nbox) {
+        const int k0 = kt + lane * RB;
+        const int row = p.cu_k ? koff + k0 : k0 % p.BS;
+        const uint32_t dst0 = ring + s * C::KV_BYTES;
+        if (p.kv_rg) {
+          // one box: RB / 8 key groups x every column block
+          const uint32_t dst = dst0 + lane * (RB / 8) * gs;
+          if (p.kv_order_hnd)
+            tma_load_5d(dst, tm, 0, 0, 0, row >> 3, cur * p.Hkv + g, full);
+          else
+            tma_load_5d(dst, tm, 0, 0, 0, cur * (p.BS >> 3) + (row >> 3), g,
+                        full);
+        } else {
+          for (int cb = 0; cb < C::NCB; ++cb) {
+            const uint32_t dst = dst0 + cb * cbs + lane * RB * 128;
+            if (p.kv_order_hnd)
+              tma_load_4d(dst, tm, cb * 64, row, g, cur, full);
+            else
+              tma_load_4d(dst, tm, cb * 64, g, row, cur, full);
+          }
+        }
+      }
+      iss = j + 1;
       cur = nxt;
     }
     // drain: the last copies of each stage must land before the CTA exits
     if (lane == 0) {
-      for (int t = max(0, k_iss - 2); t < k_iss; ++t)
-        mbar_drain(k_full(t & 1), (t >> 1) & 1);
-      for (int t = max(0, v_iss - 2); t < v_iss; ++t)
-        mbar_drain(v_full(t & 1), (t >> 1) & 1);
+      for (int t = max(0, iss - 2); t < iss; ++t)
+        mbar_drain(mat ? v_full(t & 1) : k_full(t & 1), (t >> 1) & 1);
     }
   } else if (warp == MMA_WARP) {
     // ---------------------------------------------------------- MMA issuer
@@ -586,7 +597,8 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
           const int rem = idx - cb * ((BN - r0) * 8);
           const int r = r0 + rem / 8, c = rem % 8;
           asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(
-                           v0 + cb * (BN * 128) + r * 128 + (c << 4)),
+                           v0 + (r >> 3) * gs + cb * cbs + (r & 7) * 128 +
+                           (c << 4)),
                        "r"(0)
                        : "memory");
         }
@@ -601,7 +613,7 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
         for (int k = 0; k < BN / 16; ++k) {
           const uint64_t a = sdesc(p0 + (k >> 2) * (BM * 128) + (k & 3) * 32,
                                    16, 1024);
-          const uint64_t bdesc = sdesc(v0 + k * 16 * 128, BN * 128, 1024);
+          const uint64_t bdesc = sdesc(v0 + k * 2 * gs, cbs, gs);
           mma_f16(tmem + C::O_COL, a, bdesc, ID_PV, (i > 0 || k > 0) ? 1 : 0);
         }
         mma_commit(pv_done(pb));
@@ -629,7 +641,7 @@ prefill_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_k,
           const uint64_t a =
               sdesc(sQ + (k >> 2) * (BM * 128) + (k & 3) * 32, 16, 1024);
           const uint64_t bdesc =
-              sdesc(k0 + (k >> 2) * (BN * 128) + (k & 3) * 32, 16, 1024);
+              sdesc(k0 + (k >> 2) * cbs + (k & 3) * 32, 16, gs);
           mma_f16(tmem + C::S_COL + s * BN, a, bdesc, ID_S, k > 0 ? 1 : 0);
         }
         mma_commit(s_full(s));
@@ -2740,6 +2752,53 @@ bool make_kv_map_ex(CUtensorMap* map, const void* ptr, int elem, int D,
   return r == CUDA_SUCCESS;
 }
 
+// 5-D row-group map of a 16-bit cache view: (64 columns, 8 rows, D / 64
+// column blocks, key groups, heads).  The key-group and the page axes merge
+// into one when their strides line up, so one box of RB keys (RB / 8
+// groups) covers every column block of one page and lands in shared memory
+// as [8-key group][column block][8 keys][64 columns]: the NHD view needs
+// s_blk = BS s_row (dims: groups of all pages, then heads), the HND view
+// s_blk = Hkv s_head (dims: groups of a page, then page x head).  False when
+// the view does not fit; the caller keeps the 4-D boxes then.
+bool make_kv_rg_map(CUtensorMap* map, const void* ptr, bool bf16, int D,
+                    int BS, int Hkv, int64_t NB, int64_t s_blk, int64_t s_row,
+                    int64_t s_head, int RB, bool hnd) {
+  auto fn = encode_fn();
+  if (!fn || D % 64 != 0 || BS % 8 != 0 || RB % 8 != 0 || RB > BS ||
+      RB / 8 > 256)
+    return false;
+  const int64_t eb = 2;
+  cuuint64_t dims[5], strides[4];
+  cuuint32_t box[5] = {64, 8, static_cast<cuuint32_t>(D / 64),
+                       static_cast<cuuint32_t>(RB / 8), 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  dims[0] = 64;
+  dims[1] = 8;
+  dims[2] = static_cast<cuuint64_t>(D / 64);
+  strides[0] = static_cast<cuuint64_t>(s_row * eb);
+  strides[1] = 128;
+  strides[2] = static_cast<cuuint64_t>(8 * s_row * eb);
+  strides[3] = static_cast<cuuint64_t>(s_head * eb);
+  if (!hnd) {
+    const int64_t groups = NB * (BS / 8);
+    if (s_blk != BS * s_row || groups > 0x7fffffff) return false;
+    dims[3] = static_cast<cuuint64_t>(groups);
+    dims[4] = static_cast<cuuint64_t>(Hkv);
+  } else {
+    const int64_t ph = NB * Hkv;
+    if (s_blk != Hkv * s_head || ph > 0x7fffffff) return false;
+    dims[3] = static_cast<cuuint64_t>(BS / 8);
+    dims[4] = static_cast<cuuint64_t>(ph);
+  }
+  CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                            : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                  5, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool make_kv_map(CUtensorMap* map, const void* ptr, bool bf16, int D, int BS,
                  int Hkv, int64_t NB, int64_t s_blk, int64_t s_row,
                  int64_t s_head, int RB, bool hnd) {
@@ -2847,10 +2906,20 @@ cudaError_t launch_prefill_attn_tc(const AttnParams& a, int D, bool bf16,
                  ? 1
                  : 0;
   CUtensorMap mk, mv;
-  if (!make_kv_map(&mk, a.kc, bf16, D, a.BS, a.Hkv, a.num_blocks, a.c_sb,
-                   a.c_sr, a.c_sh, RB, p.kv_order_hnd) ||
-      !make_kv_map(&mv, a.vc, bf16, D, a.BS, a.Hkv, a.num_blocks, a.c_sb,
-                   a.c_sr, a.c_sh, RB, p.kv_order_hnd))
+  // head size 256: one row-group box per page (4-D boxes cost one TMA
+  // instruction per 64-column block, and the instruction rate, not the
+  // bytes, bounded the loads)
+  p.kv_rg = 0;
+  if (D == 256 && !a.cu_k &&
+      make_kv_rg_map(&mk, a.kc, bf16, D, a.BS, a.Hkv, a.num_blocks, a.c_sb,
+                     a.c_sr, a.c_sh, RB, p.kv_order_hnd) &&
+      make_kv_rg_map(&mv, a.vc, bf16, D, a.BS, a.Hkv, a.num_blocks, a.c_sb,
+                     a.c_sr, a.c_sh, RB, p.kv_order_hnd))
+    p.kv_rg = 1;
+  else if (!make_kv_map(&mk, a.kc, bf16, D, a.BS, a.Hkv, a.num_blocks, a.c_sb,
+                        a.c_sr, a.c_sh, RB, p.kv_order_hnd) ||
+           !make_kv_map(&mv, a.vc, bf16, D, a.BS, a.Hkv, a.num_blocks, a.c_sb,
+                        a.c_sr, a.c_sh, RB, p.kv_order_hnd))
     return cudaErrorInvalidValue;
   // compact 1-D grid: an upper bound on the row tiles of all requests,
   // sum_b ceil(q_b * G / rows) <= ceil(total_q * G / rows) + batch, with

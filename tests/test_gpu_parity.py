@@ -218,6 +218,38 @@ def test_prefill_kernels(cuda_device, idx, kernel):
     assert_close(wl, out, lse, ref_out, ref_lse, "%s %d" % (kernel, idx))
 
 
+@pytest.mark.parametrize("view", ["hnd", "padded_blocks"])
+def test_head256_prefill_cache_views(cuda_device, view):
+    """Head-size-256 prefill over other cache views: an HND physical cache
+    seen through an NHD view (row-group boxes over the page x head axis) and
+    blocks with 8 padding rows each (block stride != block_size x row
+    stride: the per-column-block boxes)."""
+    wl = workloads.build_workload("v256", 1234, [130, 60], [700, 260], 8, 4,
+                                  256, 32, window_size=(300, 0),
+                                  softcap=30.0)
+    b = DeviceBatch(wl, cuda_device)
+    b.write_context()
+    b.write_new()
+    NB, BS, H, D = b.key_cache.shape
+    dt, dev = b.key_cache.dtype, b.key_cache.device
+    if view == "hnd":
+        phys = torch.full((2, NB, H, BS, D), math.nan, dtype=dt, device=dev)
+        kc, vc = phys.permute(0, 1, 3, 2, 4).unbind(0)
+    else:
+        phys = torch.full((2, NB, BS + 8, H, D), math.nan, dtype=dt,
+                          device=dev)
+        kc, vc = phys[:, :, :BS].unbind(0)
+    kc.copy_(b.key_cache)
+    vc.copy_(b.value_cache)
+    b.key_cache, b.value_cache = kc, vc
+    out, lse = b.attend(return_lse=True)
+    torch.cuda.synchronize(dev)
+    api.check_device_errors(dev)
+    ref_out, ref_lse = full_reference(wl)
+    assert_close(wl, out.float().cpu().numpy(), lse.cpu().numpy(), ref_out,
+                 ref_lse, view)
+
+
 DECODE_CASES = [
     # q_lens, seq_lens, Hq, Hkv, D, BS, kwargs  (all decode-class)
     ([1, 1, 1, 1], [1, 15, 16, 17], 8, 2, 128, 16, dict()),
