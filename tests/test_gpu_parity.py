@@ -218,14 +218,17 @@ def test_prefill_kernels(cuda_device, idx, kernel):
     assert_close(wl, out, lse, ref_out, ref_lse, "%s %d" % (kernel, idx))
 
 
+@pytest.mark.parametrize("D", [128, 256])
 @pytest.mark.parametrize("view", ["hnd", "padded_blocks"])
-def test_head256_prefill_cache_views(cuda_device, view):
-    """Head-size-256 prefill over other cache views: an HND physical cache
-    seen through an NHD view (row-group boxes over the page x head axis) and
-    blocks with 8 padding rows each (block stride != block_size x row
-    stride: the per-column-block boxes)."""
-    wl = workloads.build_workload("v256", 1234, [130, 60], [700, 260], 8, 4,
-                                  256, 32, window_size=(300, 0),
+def test_prefill_cache_views(cuda_device, view, D):
+    """Prefill over other cache views: an HND physical cache seen through an
+    NHD view and blocks with 8 padding rows each (block stride !=
+    block_size x row stride).  At D = 256 the first takes the row-group
+    boxes over the page x head axis and the second the per-column-block
+    boxes; at D = 128 both take the persistent kernel's per-column-block
+    boxes."""
+    wl = workloads.build_workload("v%d" % D, 1234, [130, 60], [700, 260], 8,
+                                  4, D, 32, window_size=(300, 0),
                                   softcap=30.0)
     b = DeviceBatch(wl, cuda_device)
     b.write_context()
