@@ -64,13 +64,19 @@ struct Cfg {
 };
 
 // Byte offset of 16-byte chunk `ch` (0 .. D/8-1) of row r in a K/V tile
-// written by 64-column TMA boxes with the 128-byte swizzle.
-template <int KT>
+// with the 128-byte swizzle: [column block][key][64] from 4-D boxes (RG
+// false), [8-key group][column block][8 keys][64] from row-group boxes.
+template <int KT, int D, bool RG>
 __device__ __forceinline__ uint32_t kv_off(int r, int ch) {
-  return static_cast<uint32_t>((ch >> 3) * (KT * 128)) + sw128(r, ch & 7);
+  if constexpr (RG)
+    return static_cast<uint32_t>((r >> 3) * (D / 64 * 1024) +
+                                 (ch >> 3) * 1024) +
+           sw128(r & 7, ch & 7);
+  else
+    return static_cast<uint32_t>((ch >> 3) * (KT * 128)) + sw128(r, ch & 7);
 }
 
-template <typename T, int D, int NCW, int KT, int STAGES>
+template <typename T, int D, int NCW, int KT, int STAGES, bool RG>
 __device__ __forceinline__ void decode_tma_body(const AttnParams& p,
                                                 const CUtensorMap& tm_k,
                                                 const CUtensorMap& tm_v) {
@@ -198,7 +204,23 @@ __device__ __forceinline__ void decode_tma_body(const AttnParams& p,
       }
       stop = __shfl_sync(0xffffffffu, stop, 0);
       if (stop) break;
-      if (lane < nbox && cur >= 0) {
+      if (RG && lane < nbox && cur >= 0) {
+        // one row-group box per page and matrix
+        const int row = (kt + lane * RB) % p.BS;
+        const uint32_t off = lane * RB * (C::NCB * 128);
+        if (p.kv_order_hnd) {
+          tma_load_5d_hint(tile_k(s) + off, &tm_k, 0, 0, 0, row >> 3,
+                           cur * p.Hkv + g, full_k(s), pol);
+          tma_load_5d_hint(tile_v(s) + off, &tm_v, 0, 0, 0, row >> 3,
+                           cur * p.Hkv + g, full_v(s), pol);
+        } else {
+          const int grp = cur * (p.BS >> 3) + (row >> 3);
+          tma_load_5d_hint(tile_k(s) + off, &tm_k, 0, 0, 0, grp, g,
+                           full_k(s), pol);
+          tma_load_5d_hint(tile_v(s) + off, &tm_v, 0, 0, 0, grp, g,
+                           full_v(s), pol);
+        }
+      } else if (lane < nbox && cur >= 0) {
         const int k0 = kt + lane * RB;
         const int row = p.cu_k ? koff + k0 : k0 % p.BS;
 #pragma unroll
@@ -283,8 +305,8 @@ __device__ __forceinline__ void decode_tma_body(const AttnParams& p,
         if (!((bad >> (r / RB)) & 1u)) continue;
         asm volatile("st.shared.v4.u32 [%0], {%2, %2, %2, %2};\n"
                      "st.shared.v4.u32 [%1], {%2, %2, %2, %2};" ::"r"(
-                         sK + kv_off<KT>(r, ch)),
-                     "r"(sV + kv_off<KT>(r, ch)), "r"(0)
+                         sK + kv_off<KT, D, RG>(r, ch)),
+                     "r"(sV + kv_off<KT, D, RG>(r, ch)), "r"(0)
                      : "memory");
       }
       fence_proxy_async();
@@ -309,7 +331,7 @@ __device__ __forceinline__ void decode_tma_body(const AttnParams& p,
         uint32_t b0, b1, b2, b3;
         const int r = kw0 + np * 16 + lm_r + (lm_mi >> 1) * 8;
         const int ch = kk * 2 + (lm_mi & 1);
-        ldmatrix_x4(sK + kv_off<KT>(r, ch), b0, b1, b2, b3);
+        ldmatrix_x4(sK + kv_off<KT, D, RG>(r, ch), b0, b1, b2, b3);
         mma_16816<T>(sc[2 * np], a, b0, b1);
         mma_16816<T>(sc[2 * np + 1], a, b2, b3);
       }
@@ -405,7 +427,7 @@ __device__ __forceinline__ void decode_tma_body(const AttnParams& p,
       for (int idx = lane; idx < (kw0 + C::KW - r0) * C::CPR; idx += 32) {
         const int r = r0 + idx / C::CPR, ch = idx % C::CPR;
         asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(
-                         sV + kv_off<KT>(r, ch)),
+                         sV + kv_off<KT, D, RG>(r, ch)),
                      "r"(0)
                      : "memory");
       }
@@ -425,7 +447,7 @@ __device__ __forceinline__ void decode_tma_body(const AttnParams& p,
         uint32_t b0, b1, b2, b3;
         const int r = kw0 + ks * 16 + lm_r + (lm_mi & 1) * 8;
         const int ch = dp * 2 + (lm_mi >> 1);
-        ldmatrix_x4_trans(sV + kv_off<KT>(r, ch), b0, b1, b2, b3);
+        ldmatrix_x4_trans(sV + kv_off<KT, D, RG>(r, ch), b0, b1, b2, b3);
         mma_16816<T>(o[2 * dp], a, b0, b1);
         mma_16816<T>(o[2 * dp + 1], a, b2, b3);
       }
@@ -514,14 +536,14 @@ __device__ __forceinline__ void decode_tma_body(const AttnParams& p,
 // *p.pdl_done and the last one waits for the grid before to complete, so
 // this grid ends after it and work queued after this grid sees both
 // grids' results.  Without a preceding grid the wait returns at once.
-template <typename T, int D, int NCW, int KT, int STAGES>
+template <typename T, int D, int NCW, int KT, int STAGES, bool RG>
 __global__ void __launch_bounds__((NCW + 1) * 32)
 decode_tma_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v) {
   // a prefill launch queued after this one in the same call may start
   // before this grid ends (it writes other requests' rows)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  decode_tma_body<T, D, NCW, KT, STAGES>(p, tm_k, tm_v);
+  decode_tma_body<T, D, NCW, KT, STAGES, RG>(p, tm_k, tm_v);
   if (p.pdl_done && threadIdx.x == 0) {
     const unsigned total = gridDim.x * gridDim.y;
     if (atomicAdd(reinterpret_cast<unsigned*>(p.pdl_done), 1u) == total - 1) {
@@ -541,12 +563,12 @@ decode_tma_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
 #define PKV_DTMA_D64_STAGES 4
 #endif
 
-template <typename T, int D, int NCW, int KT, int STAGES>
+template <typename T, int D, int NCW, int KT, int STAGES, bool RG>
 cudaError_t launch_cfg(const AttnParams& p, const CUtensorMap& mk,
                        const CUtensorMap& mv, dim3 grid,
                        cudaStream_t stream) {
   using C = Cfg<D, NCW, KT, STAGES>;
-  auto kern = decode_tma_kernel<T, D, NCW, KT, STAGES>;
+  auto kern = decode_tma_kernel<T, D, NCW, KT, STAGES, RG>;
   cudaError_t e = smem_opt_in(reinterpret_cast<const void*>(kern), C::SMEM);
   if (e != cudaSuccess) return e;
   note_launch();
@@ -572,17 +594,24 @@ cudaError_t launch_cfg(const AttnParams& p, const CUtensorMap& mk,
 }
 
 template <typename T>
-cudaError_t dispatch(const AttnParams& p, int D, const CUtensorMap& mk,
-                     const CUtensorMap& mv, dim3 grid, cudaStream_t s) {
+cudaError_t dispatch(const AttnParams& p, int D, bool rg,
+                     const CUtensorMap& mk, const CUtensorMap& mv, dim3 grid,
+                     cudaStream_t s) {
+  // row-group boxes at D = 128 only: D = 64 has one column block (both
+  // layouts are the same), and at D = 256 their addressing took the
+  // consumers from 200 to 245 registers, one CTA per SM fewer
   switch (D) {
     case 64:
-      return launch_cfg<T, 64, 4, 64, PKV_DTMA_D64_STAGES>(p, mk, mv, grid, s);
+      return launch_cfg<T, 64, 4, 64, PKV_DTMA_D64_STAGES, false>(p, mk, mv,
+                                                                  grid, s);
     case 128:
-      return launch_cfg<T, 128, 4, 64, PKV_DTMA_D128_STAGES>(p, mk, mv, grid,
-                                                             s);
+      return rg ? launch_cfg<T, 128, 4, 64, PKV_DTMA_D128_STAGES, true>(
+                      p, mk, mv, grid, s)
+                : launch_cfg<T, 128, 4, 64, PKV_DTMA_D128_STAGES, false>(
+                      p, mk, mv, grid, s);
     case 256:
-      return launch_cfg<T, 256, 2, 32, PKV_DTMA_D256_STAGES>(p, mk, mv, grid,
-                                                             s);
+      return launch_cfg<T, 256, 2, 32, PKV_DTMA_D256_STAGES, false>(p, mk, mv,
+                                                                    grid, s);
     default:
       return cudaErrorInvalidValue;
   }
@@ -602,14 +631,23 @@ cudaError_t launch_decode_attn_tma(const AttnParams& a, int D, bool bf16,
   p.rb = RB;
   p.kv_order_hnd = p.c_sh > p.c_sr ? 1 : 0;
   CUtensorMap mk, mv;
-  if (!make_kv_map(&mk, p.kc, bf16, D, p.BS, p.Hkv, p.num_blocks, p.c_sb,
-                   p.c_sr, p.c_sh, RB, p.kv_order_hnd) ||
-      !make_kv_map(&mv, p.vc, bf16, D, p.BS, p.Hkv, p.num_blocks, p.c_sb,
-                   p.c_sr, p.c_sh, RB, p.kv_order_hnd))
+  // one row-group box per page and matrix where the view allows it (the
+  // 4-D boxes take one per page and 64-column block)
+  const bool rg =
+      D == 128 && !p.cu_k &&
+      make_kv_rg_map(&mk, p.kc, bf16, D, p.BS, p.Hkv, p.num_blocks, p.c_sb,
+                     p.c_sr, p.c_sh, RB, p.kv_order_hnd) &&
+      make_kv_rg_map(&mv, p.vc, bf16, D, p.BS, p.Hkv, p.num_blocks, p.c_sb,
+                     p.c_sr, p.c_sh, RB, p.kv_order_hnd);
+  if (!rg &&
+      (!make_kv_map(&mk, p.kc, bf16, D, p.BS, p.Hkv, p.num_blocks, p.c_sb,
+                    p.c_sr, p.c_sh, RB, p.kv_order_hnd) ||
+       !make_kv_map(&mv, p.vc, bf16, D, p.BS, p.Hkv, p.num_blocks, p.c_sb,
+                    p.c_sr, p.c_sh, RB, p.kv_order_hnd)))
     return cudaErrorInvalidValue;
   dim3 grid(static_cast<unsigned>(p.batch) * p.Hkv, grid_x, 1);
-  return bf16 ? dtma::dispatch<__nv_bfloat16>(p, D, mk, mv, grid, stream)
-              : dtma::dispatch<__half>(p, D, mk, mv, grid, stream);
+  return bf16 ? dtma::dispatch<__nv_bfloat16>(p, D, rg, mk, mv, grid, stream)
+              : dtma::dispatch<__half>(p, D, rg, mk, mv, grid, stream);
 }
 
 }  // namespace pkv

@@ -135,6 +135,21 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const void* tmap,
       : "memory");
 }
 
+// tma_load_5d with an L2 cache policy (l2_evict_first_policy).
+__device__ __forceinline__ void tma_load_5d_hint(uint32_t dst,
+                                                 const void* tmap, int c0,
+                                                 int c1, int c2, int c3,
+                                                 int c4, uint32_t bar,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::"
+      "complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], "
+      "[%7], %8;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2),
+      "r"(c3), "r"(c4), "r"(bar), "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap,
                                             int c0, int c1, int c2,
                                             uint32_t bar) {
@@ -202,6 +217,16 @@ __device__ __forceinline__ void fence_proxy_async() {
 bool make_kv_map(CUtensorMap* map, const void* ptr, bool bf16, int D, int BS,
                  int Hkv, int64_t NB, int64_t s_blk, int64_t s_row,
                  int64_t s_head, int RB, bool hnd);
+// Row-group map of a 16-bit cache view: one box of RB keys (RB a multiple
+// of 8, at most block_size) holds every 64-column block of one page and
+// lands as [8-key group][column block][8 keys][64 columns]; coordinates
+// (0, 0, 0, page * (BS / 8) + row / 8, head) for NHD views and (0, 0, 0,
+// row / 8, page * Hkv + head) for HND views.  False when the view's
+// strides do not allow it (NHD needs s_blk = BS s_row, HND s_blk = Hkv
+// s_head).
+bool make_kv_rg_map(CUtensorMap* map, const void* ptr, bool bf16, int D,
+                    int BS, int Hkv, int64_t NB, int64_t s_blk, int64_t s_row,
+                    int64_t s_head, int RB, bool hnd);
 // The same map for an element type `elem`: 0 = one-byte codes (E4M3; box
 // 128 x 1 x RB x 1), 1 = f16, 2 = bf16 (box 64 x 1 x RB x 1).  Strides are
 // in elements of that type.

@@ -253,6 +253,42 @@ def test_prefill_cache_views(cuda_device, view, D):
                  ref_lse, view)
 
 
+@pytest.mark.parametrize("BS", [16, 48])
+@pytest.mark.parametrize("view", ["hnd", "padded_blocks"])
+def test_decode_tma_cache_views(cuda_device, view, BS):
+    """The TMA decode kernel over an HND physical cache seen through an NHD
+    view (row-group boxes over the page x head axis) and over blocks with 8
+    padding rows (per-column-block boxes), at block sizes 16 and 48."""
+    wl = workloads.build_workload("dv%d" % BS, 1300 + BS, [1, 1, 2],
+                                  [900, 333, 1500], 16, 4, 128, BS,
+                                  window_size=(700, 0))
+    b = DeviceBatch(wl, cuda_device)
+    b.write_context()
+    b.write_new()
+    NB, BS_, H, D = b.key_cache.shape
+    dt, dev = b.key_cache.dtype, b.key_cache.device
+    if view == "hnd":
+        phys = torch.full((2, NB, H, BS_, D), math.nan, dtype=dt, device=dev)
+        kc, vc = phys.permute(0, 1, 3, 2, 4).unbind(0)
+    else:
+        phys = torch.full((2, NB, BS_ + 8, H, D), math.nan, dtype=dt,
+                          device=dev)
+        kc, vc = phys[:, :, :BS_].unbind(0)
+    kc.copy_(b.key_cache)
+    vc.copy_(b.value_cache)
+    b.key_cache, b.value_cache = kc, vc
+    api.set_decode_kernel(api.DECODE_TMA)
+    try:
+        out, lse = b.attend(return_lse=True)
+        torch.cuda.synchronize(dev)
+    finally:
+        api.set_decode_kernel(api.DECODE_AUTO)
+    api.check_device_errors(dev)
+    ref_out, ref_lse = full_reference(wl)
+    assert_close(wl, out.float().cpu().numpy(), lse.cpu().numpy(), ref_out,
+                 ref_lse, view)
+
+
 DECODE_CASES = [
     # q_lens, seq_lens, Hq, Hkv, D, BS, kwargs  (all decode-class)
     ([1, 1, 1, 1], [1, 15, 16, 17], 8, 2, 128, 16, dict()),
