@@ -211,46 +211,6 @@ __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
                : "memory");
 }
 
-// Four E4M3 codes (low byte first) -> two f16x2 (exact).
-__device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t& lo,
-                                              uint32_t& hi) {
-  asm("{\n.reg .b16 a, b;\n"
-      "mov.b32 {a, b}, %2;\n"
-      "cvt.rn.f16x2.e4m3x2 %0, a;\n"
-      "cvt.rn.f16x2.e4m3x2 %1, b;\n}\n"
-      : "=r"(lo), "=r"(hi)
-      : "r"(w));
-}
-
-// An 8-bit 16 x 16 block of shared memory (row addresses from lanes 0-15),
-// transposed: lane t receives rows 4 (t % 4) .. + 3 of column t / 4 in d0
-// and of column t / 4 + 8 in d1 (row 4 (t % 4) in the low byte).
-__device__ __forceinline__ void ldmatrix_b8_trans(uint32_t addr, uint32_t& d0,
-                                                  uint32_t& d1) {
-  asm volatile(
-      "ldmatrix.sync.aligned.m16n16.x1.trans.shared.b8 {%0, %1}, [%2];"
-      : "=r"(d0), "=r"(d1)
-      : "r"(addr));
-}
-
-__device__ __forceinline__ uint32_t lds32(uint32_t a) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
-  return v;
-}
-
-template <typename T>
-__device__ __forceinline__ float elem_f32(uint32_t w, int hi);
-template <>
-__device__ __forceinline__ float elem_f32<__nv_bfloat16>(uint32_t w,
-                                                         int hi) {
-  return __uint_as_float(hi ? (w & 0xffff0000u) : (w << 16));
-}
-template <>
-__device__ __forceinline__ float elem_f32<__half>(uint32_t w, int hi) {
-  return __half2float(__ushort_as_half(
-      static_cast<unsigned short>(hi ? (w >> 16) : (w & 0xffffu))));
-}
 
 template <typename T, int D, int NCW, int KT, int STAGES, bool KV8, bool Q8>
 __global__ void __launch_bounds__((NCW + 1) * 32, 2)

@@ -33,32 +33,43 @@
 #include <cuda.h>
 #include <math.h>
 
+#include <type_traits>
+
 #include "pkv_common.cuh"
 #include "tma_util.cuh"
 
 namespace pkv {
 namespace dtma {
 
-template <int D, int NCW, int KT, int STAGES>
+template <int D, int NCW, int KT, int STAGES, bool KV8 = false>
 struct Cfg {
   static constexpr int NT = (NCW + 1) * 32;     // consumers + producer warp
   static constexpr int CT = NCW * 32;           // consumer threads
   static constexpr int KW = KT / NCW;           // keys per warp per tile
   static constexpr int NKT = KW / 8;            // n8 tiles of S per warp
-  static constexpr int NCB = D / 64;            // 64-column (128 B) blocks
-  static constexpr int CPR = D / 8;             // 16-byte chunks per row
+  static constexpr int BOXC = KV8 ? 128 : 64;   // columns per TMA box
+  static constexpr int NCB = D / BOXC;          // 128-byte column blocks
+  static constexpr int CPR = D / 8;             // 16-byte chunks per Q row
+  static constexpr int RCH = KV8 ? D / 16 : D / 8;   // ... per K/V row
   static constexpr int ROW_BYTES = D * 2;
   static constexpr int CB_BYTES = KT * 128;     // one column block of a tile
   static constexpr int TILE_BYTES = NCB * CB_BYTES;
   static constexpr int RING_BYTES = STAGES * 2 * TILE_BYTES;
   static constexpr int Q_BYTES = 16 * ROW_BYTES;
+  // E4M3 caches: f16 A fragments of Q per k16 step (32 lanes x 16 bytes),
+  // and the consumer warps' largest |q|
+  static constexpr int QFRAG_BYTES = KV8 ? (D / 16) * 32 * 16 : 0;
+  static constexpr int QMAX_BYTES = KV8 ? 16 * ((NCW * 4 + 15) / 16) : 0;
   static constexpr int OFF_Q = RING_BYTES;
-  static constexpr int OFF_BAR = OFF_Q + Q_BYTES;
+  static constexpr int OFF_QFRAG = OFF_Q + Q_BYTES;
+  static constexpr int OFF_QMAX = OFF_QFRAG + QFRAG_BYTES;
+  static constexpr int OFF_BAR = OFF_QMAX + QMAX_BYTES;
   static constexpr int BAR_BYTES = 3 * STAGES * 8 + 8 + 4 * STAGES;
   static constexpr int SMEM = OFF_BAR + BAR_BYTES + 1024;   // + alignment
   static constexpr int COMBINE_BYTES = NCW * 16 * (D + 2) * 4;
   static_assert(KW % 16 == 0, "each warp needs whole k16 steps of keys");
-  static_assert(D % 64 == 0, "64-column TMA boxes");
+  static_assert(D % BOXC == 0, "whole TMA boxes per row");
+  static_assert(!KV8 || NKT == 2 || NKT == 4, "ldmatrix grouping of codes");
   static_assert(CB_BYTES % 1024 == 0, "128-byte swizzle atoms");
   static_assert(COMBINE_BYTES <= RING_BYTES, "combine buffer");
 };
@@ -76,11 +87,13 @@ __device__ __forceinline__ uint32_t kv_off(int r, int ch) {
     return static_cast<uint32_t>((ch >> 3) * (KT * 128)) + sw128(r, ch & 7);
 }
 
-template <typename T, int D, int NCW, int KT, int STAGES, bool RG>
+template <typename T, int D, int NCW, int KT, int STAGES, bool RG, bool KV8>
 __device__ __forceinline__ void decode_tma_body(const AttnParams& p,
                                                 const CUtensorMap& tm_k,
                                                 const CUtensorMap& tm_v) {
-  using C = Cfg<D, NCW, KT, STAGES>;
+  using C = Cfg<D, NCW, KT, STAGES, KV8>;
+  // E4M3 caches: the MMAs run on f16 (codes convert to f16 exactly)
+  using MT = typename std::conditional<KV8, __half, T>::type;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t raw_u = smem_u32(smem_raw);
   const uint32_t base_u = (raw_u + 1023u) & ~1023u;
@@ -227,17 +240,17 @@ __device__ __forceinline__ void decode_tma_body(const AttnParams& p,
         for (int cb = 0; cb < C::NCB; ++cb) {
           const uint32_t dst = tile_k(s) + cb * C::CB_BYTES + lane * RB * 128;
           if (p.kv_order_hnd)
-            kv_load(dst, &tm_k, cb * 64, row, g, cur, full_k(s));
+            kv_load(dst, &tm_k, cb * C::BOXC, row, g, cur, full_k(s));
           else
-            kv_load(dst, &tm_k, cb * 64, g, row, cur, full_k(s));
+            kv_load(dst, &tm_k, cb * C::BOXC, g, row, cur, full_k(s));
         }
 #pragma unroll
         for (int cb = 0; cb < C::NCB; ++cb) {
           const uint32_t dst = tile_v(s) + cb * C::CB_BYTES + lane * RB * 128;
           if (p.kv_order_hnd)
-            kv_load(dst, &tm_v, cb * 64, row, g, cur, full_v(s));
+            kv_load(dst, &tm_v, cb * C::BOXC, row, g, cur, full_v(s));
           else
-            kv_load(dst, &tm_v, cb * 64, g, row, cur, full_v(s));
+            kv_load(dst, &tm_v, cb * C::BOXC, g, row, cur, full_v(s));
         }
       }
       issued = t + 1;
@@ -257,6 +270,74 @@ __device__ __forceinline__ void decode_tma_body(const AttnParams& p,
   // -------------------------------------------------------------- consumers
   cp_async_wait<0>();
   asm volatile("bar.sync 1, %0;" ::"n"(C::CT) : "memory");
+  // E4M3 cache: Q as f16 A fragments in the head-dimension order the K
+  // code fragments arrive in (d = 16 ks + 4 c4 + {0,1} in registers 0/1,
+  // + {2,3} in registers 2/3).  A bf16 query is scaled by the power of two
+  // that puts its largest magnitude in [2^14, 2^15), so every value is
+  // exact in f16; the factor joins the logit scale.
+  const uint32_t qfrag = base_u + C::OFF_QFRAG;
+  float qshift_f = 1.f;
+  if constexpr (KV8) {
+    float* qmax = reinterpret_cast<float*>(base + C::OFF_QMAX);
+    int shift = 0;
+    if (std::is_same<T, __nv_bfloat16>::value) {
+      float mx = 0.f;
+      for (int i = tid; i < 16 * C::CPR; i += C::CT) {
+        const int r = i / C::CPR, ch = i - (i / C::CPR) * C::CPR;
+        uint32_t w[4];
+        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                     : "r"(sQ + swz<C::ROW_BYTES>(r, ch)));
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          mx = fmaxf(mx, fabsf(elem_f32<T>(w[e], 0)));
+          mx = fmaxf(mx, fabsf(elem_f32<T>(w[e], 1)));
+        }
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1)
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      if (lane == 0) qmax[warp] = mx;
+      asm volatile("bar.sync 1, %0;" ::"n"(C::CT) : "memory");
+      float m = 0.f;
+#pragma unroll
+      for (int w = 0; w < NCW; ++w) m = fmaxf(m, qmax[w]);
+      if (m > 0.f) {
+        const int e = static_cast<int>((__float_as_uint(m) >> 23) & 0xff) - 127;
+        shift = max(-100, min(100, e - 14));
+      }
+    }
+    qshift_f = exp2f(static_cast<float>(shift));
+    const float qmul = exp2f(static_cast<float>(-shift));
+    for (int i = tid; i < (D / 16) * 32; i += C::CT) {
+      const int ks = i >> 5, ln = i & 31;
+      const int gg = ln >> 2, cc = ln & 3;
+      const int d = 16 * ks + 4 * cc;
+      const uint32_t off = (d & 7) * 2;
+      uint32_t a[4];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t w0, w1;
+        asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];"
+                     : "=r"(w0), "=r"(w1)
+                     : "r"(sQ + swz<C::ROW_BYTES>(gg + 8 * h, d >> 3) + off));
+        if (std::is_same<T, __half>::value) {
+          a[h] = w0;
+          a[2 + h] = w1;
+        } else {
+          a[h] = pack2<__half>(elem_f32<T>(w0, 0) * qmul,
+                               elem_f32<T>(w0, 1) * qmul);
+          a[2 + h] = pack2<__half>(elem_f32<T>(w1, 0) * qmul,
+                                   elem_f32<T>(w1, 1) * qmul);
+        }
+      }
+      asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
+                       qfrag + (ks * 32 + ln) * 16),
+                   "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3])
+                   : "memory");
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(C::CT) : "memory");
+  }
 
   const int g8 = lane >> 2, c4 = lane & 3;
   const int rA = g8, rB = g8 + 8;
@@ -272,7 +353,7 @@ __device__ __forceinline__ void decode_tma_body(const AttnParams& p,
   // soft-cap without ALiBi: interior tiles need only the capped logit
   const bool capped = (p.softcap > 0.f) && (p.alibi == nullptr);
   const float inv_cap = p.softcap > 0.f ? 1.f / p.softcap : 0.f;
-  const float qk_scale = p.scale * (p.k_scale ? *p.k_scale : 1.f);
+  const float qk_scale = p.scale * (p.k_scale ? *p.k_scale : 1.f) * qshift_f;
   const float vscale = p.v_scale ? *p.v_scale : 1.f;
   const float scale_log2 = qk_scale * kLog2e;
   // keys every row admits: tiles inside [full_lo, full_hi) skip the mask
@@ -300,8 +381,8 @@ __device__ __forceinline__ void decode_tma_body(const AttnParams& p,
     const uint32_t sK = tile_k(s), sV = tile_v(s);
     if (const unsigned bad = bad_boxes[s]) {
       // pages the table pointed outside the cache: zero keys and values
-      for (int idx = lane; idx < C::KW * C::CPR; idx += 32) {
-        const int r = kw0 + idx / C::CPR, ch = idx % C::CPR;
+      for (int idx = lane; idx < C::KW * C::RCH; idx += 32) {
+        const int r = kw0 + idx / C::RCH, ch = idx % C::RCH;
         if (!((bad >> (r / RB)) & 1u)) continue;
         asm volatile("st.shared.v4.u32 [%0], {%2, %2, %2, %2};\n"
                      "st.shared.v4.u32 [%1], {%2, %2, %2, %2};" ::"r"(
@@ -318,22 +399,52 @@ __device__ __forceinline__ void decode_tma_body(const AttnParams& p,
 #pragma unroll
     for (int i = 0; i < C::NKT; ++i)
       sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
+    if constexpr (KV8) {
+      // one ldmatrix.x4 of code bytes holds 4 / NKT k16 steps of all NKT
+      // n8 tiles: matrix m covers n8 tile m % NKT of step grp * 4 / NKT +
+      // m / NKT (16 code bytes = one k16 step)
+      constexpr int KPG = 4 / C::NKT;
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      uint32_t a[4];
-      {
-        const int r = lm_r + (lm_mi & 1) * 8;
-        const int ch = kk * 2 + (lm_mi >> 1);
-        ldmatrix_x4(sQ + swz<C::ROW_BYTES>(r, ch), a[0], a[1], a[2], a[3]);
+      for (int grp = 0; grp < (D / 16) / KPG; ++grp) {
+        uint32_t r4[4];
+        {
+          const int nt = lm_mi % C::NKT, ks = grp * KPG + lm_mi / C::NKT;
+          ldmatrix_x4(sK + kv_off<KT, D, RG>(kw0 + nt * 8 + lm_r, ks), r4[0],
+                      r4[1], r4[2], r4[3]);
+        }
+#pragma unroll
+        for (int kq = 0; kq < KPG; ++kq) {
+          const int ks = grp * KPG + kq;
+          uint32_t a[4];
+          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
+                       : "r"(qfrag + (ks * 32 + lane) * 16));
+#pragma unroll
+          for (int nt = 0; nt < C::NKT; ++nt) {
+            uint32_t b0, b1;
+            e4m3x4_to_f16(r4[kq * C::NKT + nt], b0, b1);
+            mma_16816<__half>(sc[nt], a, b0, b1);
+          }
+        }
       }
+    } else {
 #pragma unroll
-      for (int np = 0; np < C::NKT / 2; ++np) {
-        uint32_t b0, b1, b2, b3;
-        const int r = kw0 + np * 16 + lm_r + (lm_mi >> 1) * 8;
-        const int ch = kk * 2 + (lm_mi & 1);
-        ldmatrix_x4(sK + kv_off<KT, D, RG>(r, ch), b0, b1, b2, b3);
-        mma_16816<T>(sc[2 * np], a, b0, b1);
-        mma_16816<T>(sc[2 * np + 1], a, b2, b3);
+      for (int kk = 0; kk < D / 16; ++kk) {
+        uint32_t a[4];
+        {
+          const int r = lm_r + (lm_mi & 1) * 8;
+          const int ch = kk * 2 + (lm_mi >> 1);
+          ldmatrix_x4(sQ + swz<C::ROW_BYTES>(r, ch), a[0], a[1], a[2], a[3]);
+        }
+#pragma unroll
+        for (int np = 0; np < C::NKT / 2; ++np) {
+          uint32_t b0, b1, b2, b3;
+          const int r = kw0 + np * 16 + lm_r + (lm_mi >> 1) * 8;
+          const int ch = kk * 2 + (lm_mi & 1);
+          ldmatrix_x4(sK + kv_off<KT, D, RG>(r, ch), b0, b1, b2, b3);
+          mma_16816<T>(sc[2 * np], a, b0, b1);
+          mma_16816<T>(sc[2 * np + 1], a, b2, b3);
+        }
       }
     }
 
@@ -424,8 +535,8 @@ __device__ __forceinline__ void decode_tma_body(const AttnParams& p,
       // rows of this warp at or past the loaded range: zero them, so that
       // P = 0 never meets NaN padding or a stale row
       const int r0 = max(hi - kt, kw0);
-      for (int idx = lane; idx < (kw0 + C::KW - r0) * C::CPR; idx += 32) {
-        const int r = r0 + idx / C::CPR, ch = idx % C::CPR;
+      for (int idx = lane; idx < (kw0 + C::KW - r0) * C::RCH; idx += 32) {
+        const int r = r0 + idx / C::RCH, ch = idx % C::RCH;
         asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(
                          sV + kv_off<KT, D, RG>(r, ch)),
                      "r"(0)
@@ -438,18 +549,39 @@ __device__ __forceinline__ void decode_tma_body(const AttnParams& p,
 #pragma unroll
     for (int ks = 0; ks < C::KW / 16; ++ks) {
       uint32_t a[4];
-      a[0] = pack2<T>(sc[2 * ks][0], sc[2 * ks][1]);
-      a[1] = pack2<T>(sc[2 * ks][2], sc[2 * ks][3]);
-      a[2] = pack2<T>(sc[2 * ks + 1][0], sc[2 * ks + 1][1]);
-      a[3] = pack2<T>(sc[2 * ks + 1][2], sc[2 * ks + 1][3]);
+      a[0] = pack2<MT>(sc[2 * ks][0], sc[2 * ks][1]);
+      a[1] = pack2<MT>(sc[2 * ks][2], sc[2 * ks][3]);
+      a[2] = pack2<MT>(sc[2 * ks + 1][0], sc[2 * ks + 1][1]);
+      a[3] = pack2<MT>(sc[2 * ks + 1][2], sc[2 * ks + 1][3]);
+      if constexpr (KV8) {
+        // V^T fragments straight from the code bytes: the 8-bit transposing
+        // ldmatrix of a 16-key x 16-column block gives each lane four keys
+        // of column g8 (d0) and of column g8 + 8 (d1); the row addresses
+        // take the keys in the order 2c, 2c + 1, 2c + 8, 2c + 9 (c = 0 ..
+        // 3), so a lane's four are the B fragment's k = 2 c4, 2 c4 + 1,
+        // 2 c4 + 8, 2 c4 + 9.
+        const int li = lane & 15;
+        const int kr = kw0 + ks * 16 + 2 * (li >> 2) + (li & 1) +
+                       ((li & 2) ? 8 : 0);
 #pragma unroll
-      for (int dp = 0; dp < D / 16; ++dp) {
-        uint32_t b0, b1, b2, b3;
-        const int r = kw0 + ks * 16 + lm_r + (lm_mi & 1) * 8;
-        const int ch = dp * 2 + (lm_mi >> 1);
-        ldmatrix_x4_trans(sV + kv_off<KT, D, RG>(r, ch), b0, b1, b2, b3);
-        mma_16816<T>(o[2 * dp], a, b0, b1);
-        mma_16816<T>(o[2 * dp + 1], a, b2, b3);
+        for (int q = 0; q < D / 16; ++q) {
+          uint32_t d0, d1, b0, b1, b2, b3;
+          ldmatrix_b8_trans(sV + kv_off<KT, D, RG>(kr, q), d0, d1);
+          e4m3x4_to_f16(d0, b0, b1);
+          e4m3x4_to_f16(d1, b2, b3);
+          mma_16816<__half>(o[2 * q], a, b0, b1);
+          mma_16816<__half>(o[2 * q + 1], a, b2, b3);
+        }
+      } else {
+#pragma unroll
+        for (int dp = 0; dp < D / 16; ++dp) {
+          uint32_t b0, b1, b2, b3;
+          const int r = kw0 + ks * 16 + lm_r + (lm_mi & 1) * 8;
+          const int ch = dp * 2 + (lm_mi >> 1);
+          ldmatrix_x4_trans(sV + kv_off<KT, D, RG>(r, ch), b0, b1, b2, b3);
+          mma_16816<T>(o[2 * dp], a, b0, b1);
+          mma_16816<T>(o[2 * dp + 1], a, b2, b3);
+        }
       }
     }
     __syncwarp();
@@ -536,14 +668,14 @@ __device__ __forceinline__ void decode_tma_body(const AttnParams& p,
 // *p.pdl_done and the last one waits for the grid before to complete, so
 // this grid ends after it and work queued after this grid sees both
 // grids' results.  Without a preceding grid the wait returns at once.
-template <typename T, int D, int NCW, int KT, int STAGES, bool RG>
+template <typename T, int D, int NCW, int KT, int STAGES, bool RG, bool KV8>
 __global__ void __launch_bounds__((NCW + 1) * 32)
 decode_tma_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v) {
   // a prefill launch queued after this one in the same call may start
   // before this grid ends (it writes other requests' rows)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  decode_tma_body<T, D, NCW, KT, STAGES, RG>(p, tm_k, tm_v);
+  decode_tma_body<T, D, NCW, KT, STAGES, RG, KV8>(p, tm_k, tm_v);
   if (p.pdl_done && threadIdx.x == 0) {
     const unsigned total = gridDim.x * gridDim.y;
     if (atomicAdd(reinterpret_cast<unsigned*>(p.pdl_done), 1u) == total - 1) {
@@ -559,16 +691,20 @@ decode_tma_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
 #ifndef PKV_DTMA_D256_STAGES
 #define PKV_DTMA_D256_STAGES 2
 #endif
+#ifndef PKV_DTMA_FP8_STAGES
+#define PKV_DTMA_FP8_STAGES 4
+#endif
 #ifndef PKV_DTMA_D64_STAGES
 #define PKV_DTMA_D64_STAGES 4
 #endif
 
-template <typename T, int D, int NCW, int KT, int STAGES, bool RG>
+template <typename T, int D, int NCW, int KT, int STAGES, bool RG,
+          bool KV8 = false>
 cudaError_t launch_cfg(const AttnParams& p, const CUtensorMap& mk,
                        const CUtensorMap& mv, dim3 grid,
                        cudaStream_t stream) {
-  using C = Cfg<D, NCW, KT, STAGES>;
-  auto kern = decode_tma_kernel<T, D, NCW, KT, STAGES, RG>;
+  using C = Cfg<D, NCW, KT, STAGES, KV8>;
+  auto kern = decode_tma_kernel<T, D, NCW, KT, STAGES, RG, KV8>;
   cudaError_t e = smem_opt_in(reinterpret_cast<const void*>(kern), C::SMEM);
   if (e != cudaSuccess) return e;
   note_launch();
@@ -597,6 +733,12 @@ template <typename T>
 cudaError_t dispatch(const AttnParams& p, int D, bool rg,
                      const CUtensorMap& mk, const CUtensorMap& mv, dim3 grid,
                      cudaStream_t s) {
+  // E4M3 cache (D = 128): one-byte codes in 128-column boxes, 4 stages of
+  // 64 keys (the bytes in flight of the 16-bit kernel's 2 stages)
+  if (p.kv_fp8)
+    return D == 128 ? launch_cfg<T, 128, 4, 64, PKV_DTMA_FP8_STAGES, false,
+                                 true>(p, mk, mv, grid, s)
+                    : cudaErrorInvalidValue;
   // row-group boxes at D = 128 only: D = 64 has one column block (both
   // layouts are the same), and at D = 256 their addressing took the
   // consumers from 200 to 245 registers, one CTA per SM fewer
@@ -631,6 +773,19 @@ cudaError_t launch_decode_attn_tma(const AttnParams& a, int D, bool bf16,
   p.rb = RB;
   p.kv_order_hnd = p.c_sh > p.c_sr ? 1 : 0;
   CUtensorMap mk, mv;
+  if (p.kv_fp8) {
+    // E4M3 codes: a row of D = 128 is one 128-byte box column
+    if (D != 128 || p.cu_k ||
+        !make_kv_map_ex(&mk, p.kc, 0, D, p.BS, p.Hkv, p.num_blocks, p.c_sb,
+                        p.c_sr, p.c_sh, RB, p.kv_order_hnd) ||
+        !make_kv_map_ex(&mv, p.vc, 0, D, p.BS, p.Hkv, p.num_blocks, p.c_sb,
+                        p.c_sr, p.c_sh, RB, p.kv_order_hnd))
+      return cudaErrorInvalidValue;
+    dim3 grid(static_cast<unsigned>(p.batch) * p.Hkv, grid_x, 1);
+    return bf16 ? dtma::dispatch<__nv_bfloat16>(p, D, false, mk, mv, grid,
+                                                stream)
+                : dtma::dispatch<__half>(p, D, false, mk, mv, grid, stream);
+  }
   // one row-group box per page and matrix where the view allows it (the
   // 4-D boxes take one per page and 64-column block)
   const bool rg =

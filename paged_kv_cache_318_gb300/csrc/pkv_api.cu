@@ -951,7 +951,7 @@ pkv_status attention_impl(
       d.chunk = 0;
       e = launch_decode_attn_sk(d, head_size, bf16, sk_ctas, skr, sk_scratch,
                                 pdl_ok, s);
-    } else if (!kv8 && dsel != PKV_DECODE_CP_ASYNC) {
+    } else if ((!kv8 || head_size == 128) && dsel != PKV_DECODE_CP_ASYNC) {
       d.pdl_done = done;
       e = launch_decode_attn_tma(d, head_size, bf16, pl.splits, s);
     } else {

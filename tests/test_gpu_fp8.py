@@ -77,9 +77,15 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("dkern", ["auto", "tma"])
 @pytest.mark.parametrize("idx", range(len(CASES)))
-def test_fp8_attention(cuda_device, idx):
+def test_fp8_attention(cuda_device, idx, dkern):
+    """E4M3 cache against the float64 oracle on code * scale values; the
+    decode-class requests through the automatic choice and, at D = 128,
+    through the one-CTA-per-unit TMA kernel (codes in 128-byte boxes)."""
     q_lens, seq_lens, Hq, Hkv, D, BS, splits, dtype, kern = CASES[idx]
+    if dkern == "tma" and D != 128:
+        pytest.skip("the TMA decode kernel reads E4M3 codes at D = 128")
     wl = workloads.build_workload("a8_%d" % idx, 40 + idx, q_lens, seq_lens,
                                   Hq, Hkv, D, BS, dtype=dtype,
                                   num_splits=splits)
@@ -89,6 +95,8 @@ def test_fp8_attention(cuda_device, idx):
     q = wl.q.to(dev)
     api.set_prefill_kernel(api.PREFILL_TCGEN05 if kern == "tcgen05"
                            else api.PREFILL_MMA_SYNC)
+    api.set_decode_kernel(api.DECODE_TMA if dkern == "tma"
+                          else api.DECODE_AUTO)
     try:
         out, lse = api.flash_attn_varlen_func(
             q, kc, vc, wl.max_seqlen_q,
@@ -101,6 +109,7 @@ def test_fp8_attention(cuda_device, idx):
         torch.cuda.synchronize()
     finally:
         api.set_prefill_kernel(api.PREFILL_TCGEN05)
+        api.set_decode_kernel(api.DECODE_AUTO)
     api.check_device_errors(dev)
     kcodes, vcodes = oracle_codes(wl, ksc, vsc)
     kref = e4m3_decode(kcodes) * np.float64(np.float32(ksc))
@@ -158,6 +167,9 @@ Q8_CASES = [
     ([1, 3, 1], [33, 2049, 4100], 16, 8, 256, 32, 0, "f16", "auto"),
     ([1, 1], [4000, 64], 16, 2, 128, 64, 4, "bf16", "auto"),
     ([1, 1, 1], [500, 1500, 40], 32, 8, 128, 16, 0, "bf16", "cp_async"),
+    ([1, 1, 1, 1], [700, 3000, 9, 1], 32, 8, 128, 16, 0, "bf16", "tma"),
+    ([1, 1, 1], [1200, 77, 4100], 32, 8, 128, 16, 0, "f16", "tma"),
+    ([1, 1], [4000, 64], 16, 2, 128, 64, 4, "bf16", "tma"),
     ([1, 2], [500, 70], 8, 2, 64, 16, 0, "f16", "auto"),
     ([200, 1, 90], [900, 2000, 90], 32, 8, 128, 16, 0, "bf16", "auto"),
     ([70, 1], [600, 1200], 16, 8, 256, 32, 0, "bf16", "auto"),
@@ -183,8 +195,8 @@ def test_fp8_query_attention(cuda_device, idx):
     qcodes = scaled_fp8_quant_ref(f32(wl.q), np.float32(qsc))
     assert np.array_equal(q8.view(torch.uint8).cpu().numpy(), qcodes)
     out = torch.empty(wl.q.shape, dtype=wl.q.dtype, device=dev)
-    api.set_decode_kernel(api.DECODE_CP_ASYNC if kern == "cp_async"
-                          else api.DECODE_AUTO)
+    api.set_decode_kernel({"cp_async": api.DECODE_CP_ASYNC,
+                           "tma": api.DECODE_TMA}.get(kern, api.DECODE_AUTO))
     try:
         _, lse = api.flash_attn_varlen_func(
             q8, kc, vc, wl.max_seqlen_q,
