@@ -15,13 +15,22 @@
 //
 //   warp NCW (producer)  lane i fetches the page id of box i of the next
 //                        tile from the block table, then issues the tile's
-//                        K and V boxes (cp.async.bulk.tensor.4d, RB rows x
-//                        64 columns, 128-byte swizzle) into a STAGES-deep
-//                        ring; K and V complete on separate mbarriers
+//                        K and V boxes (128-byte swizzle) into a
+//                        STAGES-deep ring; K and V complete on separate
+//                        mbarriers.  A box is RB rows x 64 columns
+//                        (cp.async.bulk.tensor.4d), or at D = 128 over
+//                        views that allow it one row-group box holding
+//                        both column blocks of the page's RB rows (5-D),
+//                        or for an E4M3 cache RB rows x 128 one-byte codes
 //   warps 0..NCW-1       each owns KW = KT / NCW keys of every tile:
 //                        S = Q K^T, online softmax (base 2), O += P V, then
 //                        releases the stage; at the end the warps' partial
 //                        states are merged through shared memory
+//
+// E4M3 caches (D = 128): the MMAs run on f16; Q becomes f16 A fragments
+// once per CTA (a bf16 query scaled by a power of two, exact in f16), and
+// the K and V code fragments convert in registers after their ldmatrix
+// (k_scale joins the logit scale, v_scale the output).
 //
 // Tiles start on KT-key boundaries, so every box starts on a page boundary
 // multiple of RB (RB divides both block_size and KT).  Keys outside the
